@@ -1,0 +1,662 @@
+/*
+ * kvc_oracle.c -- plain fp64 CPU oracle for the budgeted-KV decode step and
+ * the LaProx prefill scorer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
+ * call this file; it exists so that tests, the smoke check and the CPU
+ * baseline leg of the benchmark can compare the CUDA library against a
+ * slow, obviously correct restatement of the method.  It shares no code,
+ * header, table or constant with the CUDA sources.
+ *
+ * Inputs are bf16 bit patterns (uint16) exactly as the GPU received them;
+ * every value is widened to double before any arithmetic.  All arithmetic
+ * is double precision, in the order the method states it, with no blocking
+ * or fusion.
+ *
+ * Sources (web pages; section / equation / algorithm named per function):
+ *   [MomentKV]  "MOMENTKV: Closing the Directional Gap in KV Cache Eviction
+ *               for Long-Context Inference" (arXiv 2606.01563)
+ *   [InertiaKV] "Key factors of KV cache eviction in aggressive decoding:
+ *               temporal aggregation and rank preservation" (InertiaKV,
+ *               arXiv 2609.03515)
+ *   [KeepKV]    "KeepKV: lossless KV cache compression with electoral votes
+ *               and zero-perturbation merging" (reading notes on arXiv
+ *               2504.09936)
+ *   [LaProx]    "Reformulating KV Cache Eviction Problem for Long-Context
+ *               LLM Inference" (NeurIPS 2026 notes, arXiv 2605.07234)
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------ */
+/* helpers                                                             */
+/* ------------------------------------------------------------------ */
+
+/* bf16 -> double: the bf16 bit pattern is the top half of an IEEE float. */
+static double bfd(uint16_t b)
+{
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* ------------------------------------------------------------------ */
+/* decode-step session                                                 */
+/* ------------------------------------------------------------------ */
+
+/*
+ * One session holds U independent units (sequence, layer, KV head).  Each
+ * unit keeps its cache as a list of slots ordered by token position, and the
+ * eviction-set moment statistics as the four raw running sums the MomentKV
+ * page defines (count n_e, key sum s_k, value sum s_v, outer-product sum
+ * S = sum v k^T) [MomentKV sec 4.1 "efficient statistics update"; App. A.1].
+ */
+typedef struct {
+    int U, G, d, cap;
+    int *n;           /* slots present per unit                           */
+    int32_t *pos;     /* [U][cap] token position of each slot              */
+    int32_t *vote;    /* [U][cap] integer vote p_i (KeepKV eq 6)           */
+    double *util;     /* [U][cap] aggregated utility m(i)                  */
+    uint8_t *scored;  /* [U][cap] 0 = never scored (protected)             */
+    uint16_t *k, *v;  /* [U][cap][d] bf16 bits                             */
+    double *ne;       /* [U]      eviction count n_e (vote-weighted)       */
+    double *sk, *sv;  /* [U][d]   s_k, s_v                                 */
+    double *S;        /* [U][d][d] S[a][b] = sum v_a k_b                   */
+} ocl_session;
+
+void *ocl_create(int U, int G, int d, int cap)
+{
+    ocl_session *s = (ocl_session *)calloc(1, sizeof *s);
+    if (!s) return NULL;
+    s->U = U; s->G = G; s->d = d; s->cap = cap;
+    size_t uc = (size_t)U * cap;
+    s->n = (int *)calloc((size_t)U, sizeof(int));
+    s->pos = (int32_t *)calloc(uc, sizeof(int32_t));
+    s->vote = (int32_t *)calloc(uc, sizeof(int32_t));
+    s->util = (double *)calloc(uc, sizeof(double));
+    s->scored = (uint8_t *)calloc(uc, 1);
+    s->k = (uint16_t *)calloc(uc * d, sizeof(uint16_t));
+    s->v = (uint16_t *)calloc(uc * d, sizeof(uint16_t));
+    s->ne = (double *)calloc((size_t)U, sizeof(double));
+    s->sk = (double *)calloc((size_t)U * d, sizeof(double));
+    s->sv = (double *)calloc((size_t)U * d, sizeof(double));
+    s->S = (double *)calloc((size_t)U * d * d, sizeof(double));
+    if (!s->n || !s->pos || !s->vote || !s->util || !s->scored || !s->k ||
+        !s->v || !s->ne || !s->sk || !s->sv || !s->S) {
+        free(s->n); free(s->pos); free(s->vote); free(s->util);
+        free(s->scored); free(s->k); free(s->v); free(s->ne); free(s->sk);
+        free(s->sv); free(s->S); free(s);
+        return NULL;
+    }
+    return s;
+}
+
+void ocl_destroy(void *h)
+{
+    ocl_session *s = (ocl_session *)h;
+    if (!s) return;
+    free(s->n); free(s->pos); free(s->vote); free(s->util); free(s->scored);
+    free(s->k); free(s->v); free(s->ne); free(s->sk); free(s->sv); free(s->S);
+    free(s);
+}
+
+/*
+ * Load the prefill cache of unit u: n slots, positions pos[0..n), optional
+ * votes (NULL = all 1).  All slots start unscored; the moment statistics
+ * start at zero at the start of each generation [MomentKV sec A4 setup].
+ * Returns 0, or -1 if n exceeds the capacity.
+ */
+int ocl_load(void *h, int u, int n, const uint16_t *k, const uint16_t *v,
+             const int32_t *vote, const int32_t *pos)
+{
+    ocl_session *s = (ocl_session *)h;
+    int d = s->d;
+    if (u < 0 || u >= s->U || n < 0 || n > s->cap) return -1;
+    size_t base = (size_t)u * s->cap;
+    for (int i = 0; i < n; i++) {
+        s->pos[base + i] = pos[i];
+        s->vote[base + i] = vote ? vote[i] : 1;
+        s->util[base + i] = 0.0;
+        s->scored[base + i] = 0;
+        memcpy(&s->k[(base + i) * d], &k[(size_t)i * d], d * sizeof(uint16_t));
+        memcpy(&s->v[(base + i) * d], &v[(size_t)i * d], d * sizeof(uint16_t));
+    }
+    s->n[u] = n;
+    s->ne[u] = 0.0;
+    memset(&s->sk[(size_t)u * d], 0, d * sizeof(double));
+    memset(&s->sv[(size_t)u * d], 0, d * sizeof(double));
+    memset(&s->S[(size_t)u * d * d], 0, (size_t)d * d * sizeof(double));
+    return 0;
+}
+
+/*
+ * Append the new token of this decode step to every unit: its key and value,
+ * vote 1, position new_pos, not yet scored.  [MomentKV Algorithm 1, steps
+ * 1-2 "R <- R u {(k_new, v_new)}"; KeepKV Algorithm 1, decode steps 6a-6b
+ * "add (k_t, v_t, p_t = 1)"].  Returns -1 if a unit is full.
+ */
+int ocl_append(void *h, const uint16_t *knew, const uint16_t *vnew,
+               int32_t new_pos)
+{
+    ocl_session *s = (ocl_session *)h;
+    int d = s->d;
+    for (int u = 0; u < s->U; u++)
+        if (s->n[u] >= s->cap) return -1;
+    for (int u = 0; u < s->U; u++) {
+        size_t i = (size_t)u * s->cap + s->n[u];
+        s->pos[i] = new_pos;
+        s->vote[i] = 1;
+        s->util[i] = 0.0;
+        s->scored[i] = 0;
+        memcpy(&s->k[i * d], &knew[(size_t)u * d], d * sizeof(uint16_t));
+        memcpy(&s->v[i * d], &vnew[(size_t)u * d], d * sizeof(uint16_t));
+        s->n[u] += 1;
+    }
+    return 0;
+}
+
+/*
+ * Vote-weighted single-query attention over all slots present, for each of
+ * the G query heads that share the unit's KV head.
+ *
+ *   logit  x_hi = q_h . k_i / sqrt(d) + ln p_i
+ *          [MomentKV sec 2 notation s_i = q^T k_i / sqrt(d); KeepKV eq 6 /
+ *           eq 23 vote weighting, written as the logit bias ln p_i of the
+ *           KeepKV "integration" item 2]
+ *   lse_h  = log sum_i exp(x_hi)                  (max-shifted)
+ *   a_hi   = exp(x_hi - lse_h)                    (attention probability)
+ *   f_h    = sum_i a_hi v_i                       [MomentKV sec 2; KeepKV eq 1]
+ *   probs_i = (1/G) sum_h a_hi   head-mean score  [InertiaKV sec 3.1 eq 1,
+ *                                 mean taken over the query heads of the
+ *                                 KV group]
+ *
+ * Outputs: lse [U][G], f [U][G][d], probs [U][cap] (slot order; entries past
+ * n[u] untouched).  Any output pointer may be NULL.
+ */
+void ocl_attend(void *h, const uint16_t *q, double *lse, double *f,
+                double *probs)
+{
+    ocl_session *s = (ocl_session *)h;
+    int G = s->G, d = s->d, cap = s->cap;
+    double rsd = 1.0 / sqrt((double)d);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int u = 0; u < s->U; u++) {
+        int n = s->n[u];
+        size_t base = (size_t)u * cap;
+        double *x = (double *)malloc((size_t)(n > 0 ? n : 1) * sizeof(double));
+        double *ps = (double *)calloc((size_t)(n > 0 ? n : 1), sizeof(double));
+        for (int hh = 0; hh < G; hh++) {
+            const uint16_t *qh = &q[((size_t)u * G + hh) * d];
+            double mx = -INFINITY;
+            for (int i = 0; i < n; i++) {
+                const uint16_t *ki = &s->k[(base + i) * d];
+                double dot = 0.0;
+                for (int a = 0; a < d; a++) dot += bfd(qh[a]) * bfd(ki[a]);
+                x[i] = dot * rsd + log((double)s->vote[base + i]);
+                if (x[i] > mx) mx = x[i];
+            }
+            double z = 0.0;
+            for (int i = 0; i < n; i++) z += exp(x[i] - mx);
+            double l = mx + log(z);
+            if (lse) lse[(size_t)u * G + hh] = l;
+            if (f) {
+                double *fh = &f[((size_t)u * G + hh) * d];
+                for (int a = 0; a < d; a++) fh[a] = 0.0;
+                for (int i = 0; i < n; i++) {
+                    double ai = exp(x[i] - l);
+                    const uint16_t *vi = &s->v[(base + i) * d];
+                    for (int a = 0; a < d; a++) fh[a] += ai * bfd(vi[a]);
+                }
+            }
+            for (int i = 0; i < n; i++) ps[i] += exp(x[i] - l);
+        }
+        if (probs)
+            for (int i = 0; i < n; i++) probs[base + i] = ps[i] / (double)G;
+        free(x);
+        free(ps);
+    }
+}
+
+/*
+ * Temporal utility aggregation on a refresh step [InertiaKV sec 3.1 eqs 2-4]:
+ *   single      m = s
+ *   cumulative  m = m_prev + s
+ *   EMA         m = alpha * m_prev + (1 - alpha) * s
+ * A slot seen for the first time takes m = s under every rule (reading of a
+ * step the surviving InertiaKV text leaves open; it equals the KeepKV
+ * bias-corrected EMA at its first observation, eq 14).
+ * probs is [U][cap] in slot order.
+ */
+void ocl_update_util(void *h, const double *probs, int rule, double alpha)
+{
+    ocl_session *s = (ocl_session *)h;
+    for (int u = 0; u < s->U; u++) {
+        size_t base = (size_t)u * s->cap;
+        for (int i = 0; i < s->n[u]; i++) {
+            double sc = probs[base + i];
+            double *m = &s->util[base + i];
+            if (!s->scored[base + i]) {
+                *m = sc;
+                s->scored[base + i] = 1;
+            } else if (rule == 0) {
+                *m = sc;
+            } else if (rule == 1) {
+                *m = *m + sc;
+            } else {
+                *m = alpha * (*m) + (1.0 - alpha) * sc;
+            }
+        }
+    }
+}
+
+/* Export the slot table (positions, votes, utilities, scored flags). */
+void ocl_get_slots(void *h, int32_t *n, int32_t *pos, int32_t *vote,
+                   double *util, uint8_t *scored)
+{
+    ocl_session *s = (ocl_session *)h;
+    size_t uc = (size_t)s->U * s->cap;
+    for (int u = 0; u < s->U; u++) n[u] = s->n[u];
+    if (pos) memcpy(pos, s->pos, uc * sizeof(int32_t));
+    if (vote) memcpy(vote, s->vote, uc * sizeof(int32_t));
+    if (util) memcpy(util, s->util, uc * sizeof(double));
+    if (scored) memcpy(scored, s->scored, uc);
+}
+
+typedef struct { double m; int32_t pos; } ocl_key;
+
+static int key_cmp(const void *a, const void *b)
+{
+    const ocl_key *x = (const ocl_key *)a, *y = (const ocl_key *)b;
+    if (x->m < y->m) return -1;
+    if (x->m > y->m) return 1;
+    return (x->pos < y->pos) ? -1 : (x->pos > y->pos);
+}
+
+/*
+ * Proposed victims of one eviction round: while a unit holds more than L
+ * slots, the lowest-utility slots go [InertiaKV sec 3.1 "evict the token
+ * with the lowest m_t(i)"; MomentKV Algorithm 1 phase 1 argmin loop].
+ * k = n - L victims are the first k scored slots in (m ascending, position
+ * ascending) order; unscored slots are never candidates.  Writes victim
+ * positions in that order to victims [U][kmax], their count to nvict [U],
+ * and the k-th (largest evicted) utility to thr [U] (0 when k = 0).
+ * Returns 0, or -1 if some unit has fewer than k scored slots or k > kmax.
+ */
+int ocl_select(void *h, int L, int kmax, int32_t *victims, int32_t *nvict,
+               double *thr)
+{
+    ocl_session *s = (ocl_session *)h;
+    int rc = 0;
+    for (int u = 0; u < s->U; u++) {
+        size_t base = (size_t)u * s->cap;
+        int n = s->n[u];
+        int k = n > L ? n - L : 0;
+        nvict[u] = 0;
+        if (thr) thr[u] = 0.0;
+        if (k == 0) continue;
+        ocl_key *keys = (ocl_key *)malloc((size_t)n * sizeof(ocl_key));
+        int ns = 0;
+        for (int i = 0; i < n; i++)
+            if (s->scored[base + i]) {
+                keys[ns].m = s->util[base + i];
+                keys[ns].pos = s->pos[base + i];
+                ns++;
+            }
+        if (ns < k || k > kmax) { free(keys); rc = -1; continue; }
+        qsort(keys, (size_t)ns, sizeof(ocl_key), key_cmp);
+        for (int j = 0; j < k; j++) victims[(size_t)u * kmax + j] = keys[j].pos;
+        nvict[u] = k;
+        if (thr) thr[u] = keys[k - 1].m;
+        free(keys);
+    }
+    return rc;
+}
+
+/*
+ * Evict the given positions.  Each evicted token is folded into the raw
+ * eviction-set sums with its vote as weight (a slot with vote p stands for
+ * p identical tokens, KeepKV eq 6 "equivalent to p duplicated pairs"):
+ *   n_e += p,  s_k += p k,  s_v += p v,  S += p v k^T
+ * [MomentKV Algorithm 1 steps 11-13; App. A.1 "updated by plain addition"],
+ * then the slot is removed, keeping the rest in position order [Algorithm 1
+ * step 14].  Returns 0, or -1 if a position is not present.
+ */
+int ocl_evict(void *h, const int32_t *victims, const int32_t *nvict, int kmax)
+{
+    ocl_session *s = (ocl_session *)h;
+    int d = s->d, rc = 0;
+    for (int u = 0; u < s->U; u++) {
+        size_t base = (size_t)u * s->cap;
+        int n = s->n[u];
+        uint8_t *gone = (uint8_t *)calloc((size_t)(n > 0 ? n : 1), 1);
+        for (int j = 0; j < nvict[u]; j++) {
+            int32_t p = victims[(size_t)u * kmax + j];
+            int i = 0;
+            while (i < n && (s->pos[base + i] != p || gone[i])) i++;
+            if (i == n) { rc = -1; continue; }
+            gone[i] = 1;
+            double w = (double)s->vote[base + i];
+            const uint16_t *ki = &s->k[(base + i) * d];
+            const uint16_t *vi = &s->v[(base + i) * d];
+            double *sk = &s->sk[(size_t)u * d], *sv = &s->sv[(size_t)u * d];
+            double *S = &s->S[(size_t)u * d * d];
+            s->ne[u] += w;
+            for (int a = 0; a < d; a++) {
+                sk[a] += w * bfd(ki[a]);
+                sv[a] += w * bfd(vi[a]);
+            }
+            for (int a = 0; a < d; a++)
+                for (int b = 0; b < d; b++)
+                    S[(size_t)a * d + b] += w * bfd(vi[a]) * bfd(ki[b]);
+        }
+        int w = 0;
+        for (int i = 0; i < n; i++) {
+            if (gone[i]) continue;
+            if (w != i) {
+                s->pos[base + w] = s->pos[base + i];
+                s->vote[base + w] = s->vote[base + i];
+                s->util[base + w] = s->util[base + i];
+                s->scored[base + w] = s->scored[base + i];
+                memmove(&s->k[(base + w) * d], &s->k[(base + i) * d], d * sizeof(uint16_t));
+                memmove(&s->v[(base + w) * d], &s->v[(base + i) * d], d * sizeof(uint16_t));
+            }
+            w++;
+        }
+        s->n[u] = w;
+        free(gone);
+    }
+    return rc;
+}
+
+/*
+ * Moments in mean / covariance form, recovered from the raw sums
+ * [MomentKV sec 4.1 and App. A.1: k_bar = s_k / n_e, v_bar = s_v / n_e,
+ *  S_tilde = S - s_v s_k^T / n_e]; C = S_tilde / n_e (the population
+ * value-key covariance, C[a][b] = cov(v_a, k_b)).  All zero when n_e = 0.
+ */
+void ocl_moments(void *h, double *n, double *mu_k, double *mu_v, double *C)
+{
+    ocl_session *s = (ocl_session *)h;
+    int d = s->d;
+    for (int u = 0; u < s->U; u++) {
+        double ne = s->ne[u];
+        const double *sk = &s->sk[(size_t)u * d], *sv = &s->sv[(size_t)u * d];
+        const double *S = &s->S[(size_t)u * d * d];
+        if (n) n[u] = ne;
+        for (int a = 0; a < d; a++) {
+            if (mu_k) mu_k[(size_t)u * d + a] = ne > 0 ? sk[a] / ne : 0.0;
+            if (mu_v) mu_v[(size_t)u * d + a] = ne > 0 ? sv[a] / ne : 0.0;
+        }
+        if (C)
+            for (int a = 0; a < d; a++)
+                for (int b = 0; b < d; b++)
+                    C[(size_t)u * d * d + (size_t)a * d + b] =
+                        ne > 0 ? (S[(size_t)a * d + b] - sv[a] * sk[b] / ne) / ne : 0.0;
+    }
+}
+
+/*
+ * Output of the decode step after eviction [MomentKV Algorithm 1 phase 2]:
+ *   f_R, Z_R  = attention over the retained slots, computed directly
+ *               (step 16; logZ_R = log Z_R with vote weights)
+ *   n_e = 0 or correction off:  o = f_R                         (step 17)
+ *   otherwise, from the raw sums:
+ *     k_bar = s_k/n_e, v_bar = s_v/n_e, S_tilde = S - s_v s_k^T / n_e
+ *     log Zhat_E = ln n_e + q . k_bar / sqrt(d)    Jensen lower bound
+ *                                                 (step 18; sec 4.2 eq 10)
+ *     fhat_E = v_bar + S_tilde q / (n_e sqrt(d))   first order   (step 19;
+ *                                                 sec 4.1 eq 9)
+ *            = v_bar                               zero order (sec A4,
+ *                                                 Table 4 zero-order variant)
+ *     w_R = Z_R / (Z_R + Zhat_E) evaluated as 1 / (1 + exp(log Zhat_E -
+ *           log Z_R)), the log-domain form of App. C.2          (step 20)
+ *     o = w_R f_R + (1 - w_R) fhat_E                            (step 21)
+ * correction: 0 off, 1 zero order, 2 first order.
+ * Outputs: o, f_R [U][G][d]; logZ_R [U][G]  (f_R / logZ_R may be NULL).
+ */
+void ocl_output(void *h, const uint16_t *q, int correction, double *o,
+                double *fR, double *logZR)
+{
+    ocl_session *s = (ocl_session *)h;
+    int G = s->G, d = s->d;
+    double rsd = 1.0 / sqrt((double)d);
+    double *lse = (double *)malloc((size_t)s->U * G * sizeof(double));
+    double *f = (double *)malloc((size_t)s->U * G * d * sizeof(double));
+    ocl_attend(h, q, lse, f, NULL);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int u = 0; u < s->U; u++) {
+        double ne = s->ne[u];
+        const double *sk = &s->sk[(size_t)u * d], *sv = &s->sv[(size_t)u * d];
+        const double *S = &s->S[(size_t)u * d * d];
+        for (int hh = 0; hh < G; hh++) {
+            size_t uh = (size_t)u * G + hh;
+            const uint16_t *qh = &q[uh * d];
+            const double *fr = &f[uh * d];
+            double *oh = &o[uh * d];
+            if (fR) memcpy(&fR[uh * d], fr, d * sizeof(double));
+            if (logZR) logZR[uh] = lse[uh];
+            if (ne <= 0.0 || correction == 0) {
+                for (int a = 0; a < d; a++) oh[a] = fr[a];
+                continue;
+            }
+            double qk = 0.0;
+            for (int b = 0; b < d; b++) qk += bfd(qh[b]) * (sk[b] / ne);
+            double logZE = log(ne) + qk * rsd;
+            double wR = 1.0 / (1.0 + exp(logZE - lse[uh]));
+            for (int a = 0; a < d; a++) {
+                double fe = sv[a] / ne;
+                if (correction == 2) {
+                    double st = 0.0;
+                    for (int b = 0; b < d; b++)
+                        st += (S[(size_t)a * d + b] - sv[a] * sk[b] / ne) * bfd(qh[b]);
+                    fe += st / (ne * sqrt((double)d));
+                }
+                oh[a] = wR * fr[a] + (1.0 - wR) * fe;
+            }
+        }
+    }
+    free(lse);
+    free(f);
+}
+
+/* ------------------------------------------------------------------ */
+/* LaProx prefill scorer                                               */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Per-group Gram matrix of the output projection.  The MHA output splits as
+ * sum_h A^h (V^h W_O^h) [LaProx key design 1]; with the GQA group mean of
+ * the attention standing in for every A^h of the group [LaProx
+ * "training-free" paragraph], the group's product is A_bar (V_g W_g) with
+ * W_g = sum over the group's query heads h of W_O^h, W_O^h being rows
+ * [h d, (h+1) d) of W_O (a reading: the page is silent on GQA slicing).
+ * Gram[l][g] = W_g W_g^T (d x d), so that ||v W_g||^2 = v^T Gram v.
+ * Query head h belongs to KV group h / (Hq / Hkv).
+ * W_O: [NL][Hq*d][D] bf16; Gram: [NL][Hkv][d][d] double.
+ */
+void ocl_prefill_gram(int NL, int Hq, int Hkv, int d, int D,
+                      const uint16_t *W_O, double *Gram)
+{
+    int G = Hq / Hkv;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int l = 0; l < NL; l++)
+        for (int g = 0; g < Hkv; g++) {
+            double *W = (double *)calloc((size_t)d * D, sizeof(double));
+            for (int hh = g * G; hh < (g + 1) * G; hh++)
+                for (int a = 0; a < d; a++) {
+                    const uint16_t *row = &W_O[((size_t)l * Hq * d + (size_t)hh * d + a) * D];
+                    for (int c = 0; c < D; c++) W[(size_t)a * D + c] += bfd(row[c]);
+                }
+            double *Gm = &Gram[((size_t)l * Hkv + g) * d * d];
+            for (int a = 0; a < d; a++)
+                for (int b = 0; b < d; b++) {
+                    double acc = 0.0;
+                    for (int c = 0; c < D; c++)
+                        acc += W[(size_t)a * D + c] * W[(size_t)b * D + c];
+                    Gm[(size_t)a * d + b] = acc;
+                }
+            free(W);
+        }
+}
+
+/*
+ * Column norm of the group-mean window attention [LaProx key design 1 and
+ * the GQA group-mean paragraph; SnapKV-style observation window of w
+ * queries, MomentKV sec A4]:
+ *   window query j (0..w-1) sits at position N - w + j and sees keys
+ *   0..N-w+j (causal);  A^h[j,i] = softmax_i(q_hj . k_i / sqrt(d));
+ *   A_bar[j,i] = (1/G) sum_{h in group} A^h[j,i];   c_i = ||A_bar[:,i]||_2.
+ * q_win: [NL][Hq][w][d]; K: [NL][Hkv][N][d]; c: [NL][Hkv][N].
+ */
+void ocl_prefill_colnorm(int NL, int Hq, int Hkv, int d, int N, int w,
+                         const uint16_t *q_win, const uint16_t *K, double *c)
+{
+    int G = Hq / Hkv;
+    double rsd = 1.0 / sqrt((double)d);
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int l = 0; l < NL; l++)
+        for (int g = 0; g < Hkv; g++) {
+            const uint16_t *Kg = &K[((size_t)l * Hkv + g) * N * d];
+            double *Abar = (double *)calloc((size_t)w * N, sizeof(double));
+            double *x = (double *)malloc((size_t)N * sizeof(double));
+            for (int hh = g * G; hh < (g + 1) * G; hh++)
+                for (int j = 0; j < w; j++) {
+                    const uint16_t *qj = &q_win[(((size_t)l * Hq + hh) * w + j) * d];
+                    int last = N - w + j;           /* last visible key */
+                    double mx = -INFINITY;
+                    for (int i = 0; i <= last; i++) {
+                        double dot = 0.0;
+                        for (int a = 0; a < d; a++)
+                            dot += bfd(qj[a]) * bfd(Kg[(size_t)i * d + a]);
+                        x[i] = dot * rsd;
+                        if (x[i] > mx) mx = x[i];
+                    }
+                    double z = 0.0;
+                    for (int i = 0; i <= last; i++) z += exp(x[i] - mx);
+                    for (int i = 0; i <= last; i++)
+                        Abar[(size_t)j * N + i] += exp(x[i] - mx) / z / (double)G;
+                }
+            double *cg = &c[((size_t)l * Hkv + g) * N];
+            for (int i = 0; i < N; i++) {
+                double ss = 0.0;
+                for (int j = 0; j < w; j++)
+                    ss += Abar[(size_t)j * N + i] * Abar[(size_t)j * N + i];
+                cg[i] = sqrt(ss);
+            }
+            free(Abar);
+            free(x);
+        }
+}
+
+/*
+ * Row norm of the projected values through the Gram matrix:
+ *   r_i = ||v_i W_g||_2 = sqrt(max(0, v_i^T Gram v_i))  [LaProx key design 1,
+ *   ||(V W_O)[i,:]||_2].  V: [NL][Hkv][N][d]; Gram: [NL][Hkv][d][d].
+ */
+void ocl_prefill_rownorm(int NL, int Hkv, int d, int N, const uint16_t *V,
+                         const double *Gram, double *r)
+{
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int l = 0; l < NL; l++)
+        for (int g = 0; g < Hkv; g++) {
+            const double *Gm = &Gram[((size_t)l * Hkv + g) * d * d];
+            const uint16_t *Vg = &V[((size_t)l * Hkv + g) * N * d];
+            double *vd = (double *)malloc((size_t)d * sizeof(double));
+            for (int i = 0; i < N; i++) {
+                for (int a = 0; a < d; a++) vd[a] = bfd(Vg[(size_t)i * d + a]);
+                double acc = 0.0;
+                for (int a = 0; a < d; a++) {
+                    double t = 0.0;
+                    for (int b = 0; b < d; b++) t += Gm[(size_t)a * d + b] * vd[b];
+                    acc += vd[a] * t;
+                }
+                r[((size_t)l * Hkv + g) * N + i] = sqrt(acc > 0.0 ? acc : 0.0);
+            }
+            free(vd);
+        }
+}
+
+/*
+ * Direct form ||v_i W_g||_2 for a list of token indices of one (l, g), as a
+ * cross-check of the Gram route.  tokens: nt indices; out: nt values.
+ */
+void ocl_prefill_rownorm_direct(int Hq, int Hkv, int d, int D, int N, int l,
+                                int g, const uint16_t *V, const uint16_t *W_O,
+                                int nt, const int32_t *tokens, double *out)
+{
+    int G = Hq / Hkv;
+    const uint16_t *Vg = &V[((size_t)l * Hkv + g) * N * d];
+    for (int t = 0; t < nt; t++) {
+        int i = tokens[t];
+        double ss = 0.0;
+        for (int c = 0; c < D; c++) {
+            double acc = 0.0;
+            for (int hh = g * G; hh < (g + 1) * G; hh++)
+                for (int a = 0; a < d; a++)
+                    acc += bfd(Vg[(size_t)i * d + a]) *
+                           bfd(W_O[((size_t)l * Hq * d + (size_t)hh * d + a) * D + c]);
+            ss += acc * acc;
+        }
+        out[t] = sqrt(ss);
+    }
+}
+
+typedef struct { double s; int64_t flat; } ocl_skey;
+
+static int skey_cmp(const void *a, const void *b)
+{
+    const ocl_skey *x = (const ocl_skey *)a, *y = (const ocl_skey *)b;
+    if (x->s > y->s) return -1;
+    if (x->s < y->s) return 1;
+    return (x->flat < y->flat) ? -1 : (x->flat > y->flat);
+}
+
+/*
+ * Indicator, per-layer normalization and one model-wide top-K
+ * [LaProx key designs 1-3]:
+ *   p_{l,g,i} = c_{l,g,i} * r_{l,g,i}
+ *   s_{l,g,i} = p_{l,g,i} / sum_{g',i'} p_{l,g',i'}   (normalize != 0;
+ *               the layer's heads and tokens flattened together)
+ *   keep the B_total largest s over all (l, g, i); equal scores are kept in
+ *   ascending flat index (l*Hkv + g)*N + i (a reading; the page does not
+ *   order ties).
+ * Outputs: s [NL][Hkv][N]; keep [NL][Hkv][N] (0/1); counts [NL][Hkv];
+ * idx [B_total] kept flat indices in ascending order; thr = the B_total-th
+ * largest score.  Returns 0, or -1 if B_total is out of range.
+ */
+int ocl_prefill_select(int NL, int Hkv, int N, const double *c,
+                       const double *r, int normalize, int64_t B_total,
+                       double *s, uint8_t *keep, int32_t *counts, int64_t *idx,
+                       double *thr)
+{
+    int64_t M = (int64_t)NL * Hkv * N;
+    if (B_total < 0 || B_total > M) return -1;
+    for (int l = 0; l < NL; l++) {
+        double sum = 0.0;
+        size_t lo = (size_t)l * Hkv * N, hi = lo + (size_t)Hkv * N;
+        for (size_t j = lo; j < hi; j++) sum += c[j] * r[j];
+        for (size_t j = lo; j < hi; j++)
+            s[j] = normalize ? (sum > 0.0 ? c[j] * r[j] / sum : 0.0) : c[j] * r[j];
+    }
+    ocl_skey *keys = (ocl_skey *)malloc((size_t)M * sizeof(ocl_skey));
+    for (int64_t j = 0; j < M; j++) { keys[j].s = s[j]; keys[j].flat = j; }
+    qsort(keys, (size_t)M, sizeof(ocl_skey), skey_cmp);
+    memset(keep, 0, (size_t)M);
+    for (int64_t j = 0; j < B_total; j++) keep[keys[j].flat] = 1;
+    if (thr) *thr = B_total > 0 ? keys[B_total - 1].s : 0.0;
+    free(keys);
+    int64_t w = 0;
+    for (int l = 0; l < NL; l++)
+        for (int g = 0; g < Hkv; g++) {
+            int32_t cnt = 0;
+            for (int i = 0; i < N; i++) {
+                int64_t j = ((int64_t)l * Hkv + g) * N + i;
+                if (keep[j]) { cnt++; if (idx) idx[w++] = j; }
+            }
+            counts[l * Hkv + g] = cnt;
+        }
+    return 0;
+}

@@ -1,0 +1,455 @@
+"""Pins of the fp64 oracle's decode step against facts fixed outside it:
+closed forms, identities the pages state, brute force and numpy routines.
+
+Sources: MomentKV (arXiv 2606.01563) sec 2, 4.1-4.2, Algorithm 1, App. A-C;
+InertiaKV (arXiv 2609.03515) sec 3.1 eqs 1-4; KeepKV reading notes (arXiv
+2504.09936) eqs 1-3, 6, 23.
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+
+from oracle import oracle as O
+
+
+def bf(x):
+    return O.bf16_round(x)
+
+
+def make_session(k, v, vote=None, G=None, cap=None):
+    """One-unit session from float arrays (bf16-exact)."""
+    k = np.asarray(k, float)
+    n, d = k.shape
+    s = O.DecodeSession(1, 1 if G is None else G, d, cap or n + 4)
+    s.load(0, k, v, vote)
+    return s
+
+
+# ---------------------------------------------------------------- attention
+
+def test_two_slot_logistic():
+    """Two slots whose logits are 0 and 1 give the logistic weights
+    1/(1+e), e/(1+e); a vote p on slot 2 scales its weight to pe/(1+pe)
+    (KeepKV eq 6)."""
+    d = 4
+    q = np.array([[[1.0, 0, 0, 0]]])            # [U=1][G=1][d]
+    k = np.array([[0.0, 0, 0, 0], [2.0, 0, 0, 0]])  # q.k/sqrt(4) = 0, 1
+    v = np.array([[1.0, 2, 3, 4], [-1.0, 0.5, 0, 8]])
+    for p in (1, 3):
+        s = make_session(k, v, vote=[1, p])
+        lse, f, probs = s.attend(q)
+        w2 = p * math.e / (1 + p * math.e)
+        assert lse[0, 0] == pytest.approx(math.log(1 + p * math.e), abs=1e-14)
+        np.testing.assert_allclose(f[0, 0], (1 - w2) * v[0] + w2 * v[1], atol=1e-14)
+        np.testing.assert_allclose(probs[0, :2], [1 - w2, w2], atol=1e-15)
+        s.close()
+
+
+def test_scale_is_inverse_sqrt_d():
+    """d = 16: q = 4 e_0, k = e_0 gives logit 4/sqrt(16) = 1 against a zero key."""
+    d = 16
+    q = np.zeros((1, 1, d)); q[0, 0, 0] = 4.0
+    k = np.zeros((2, d)); k[1, 0] = 1.0
+    v = np.zeros((2, d)); v[1, 0] = 1.0
+    s = make_session(k, v)
+    lse, f, _ = s.attend(q)
+    assert f[0, 0, 0] == pytest.approx(math.e / (1 + math.e), abs=1e-15)
+    s.close()
+
+
+def test_uniform_logits_give_vote_weighted_mean():
+    """q = 0: every logit is ln p_i, so weights are p_i / sum p and lse = ln sum p."""
+    rng = np.random.default_rng(1)
+    n, d, G = 9, 8, 3
+    k, v = bf(rng.normal(size=(n, d))), bf(rng.normal(size=(n, d)))
+    p = rng.integers(1, 6, size=n)
+    s = make_session(k, v, vote=p, G=G)
+    lse, f, probs = s.attend(np.zeros((1, G, d)))
+    for h in range(G):
+        assert lse[0, h] == pytest.approx(math.log(p.sum()), abs=1e-14)
+        np.testing.assert_allclose(f[0, h], (p[:, None] * v).sum(0) / p.sum(), atol=1e-14)
+    np.testing.assert_allclose(probs[0, :n], p / p.sum(), atol=1e-15)
+    s.close()
+
+
+def test_vote_equals_duplication():
+    """A slot with vote p gives the same output as p identical slots
+    (KeepKV eq 6 and eq 23); its probability equals the duplicates' sum."""
+    rng = np.random.default_rng(2)
+    n, d, G = 7, 16, 4
+    k, v = bf(rng.normal(size=(n, d))), bf(rng.normal(size=(n, d)))
+    q = bf(rng.normal(size=(1, G, d)))
+    p = rng.integers(1, 5, size=n)
+    a = make_session(k, v, vote=p, G=G)
+    rep = np.repeat(np.arange(n), p)
+    b = make_session(k[rep], v[rep], G=G)
+    la, fa, pa = a.attend(q)
+    lb, fb, pb = b.attend(q)
+    np.testing.assert_allclose(la, lb, atol=1e-13)
+    np.testing.assert_allclose(fa, fb, atol=1e-13)
+    dup = np.zeros(n)
+    np.add.at(dup, rep, pb[0, : rep.size])
+    np.testing.assert_allclose(pa[0, :n], dup, atol=1e-14)
+    a.close(); b.close()
+
+
+def test_probs_match_softmax_and_sum_to_one():
+    """Head-mean probabilities (InertiaKV eq 1) against scipy's softmax of
+    q K^T / sqrt(d) + ln p, averaged over the group; they sum to 1."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(3)
+    n, d, G = 33, 32, 4
+    k, v = bf(rng.normal(size=(n, d))), bf(rng.normal(size=(n, d)))
+    q = bf(rng.normal(size=(1, G, d)))
+    p = rng.integers(1, 9, size=n)
+    s = make_session(k, v, vote=p, G=G)
+    lse, f, probs = s.attend(q)
+    A = softmax(q[0] @ k.T / math.sqrt(d) + np.log(p)[None, :], axis=1)
+    np.testing.assert_allclose(probs[0, :n], A.mean(0), rtol=1e-12)
+    np.testing.assert_allclose(f[0], A @ v, atol=1e-12)
+    assert probs[0, :n].sum() == pytest.approx(1.0, abs=1e-13)
+    s.close()
+
+
+def test_split_decomposition():
+    """Z = Z_R + Z_E and f = w_R f_R + w_E f_E with w_R = Z_R / Z
+    (MomentKV sec 2, exact decomposition of the full output)."""
+    rng = np.random.default_rng(4)
+    n, d, G = 40, 16, 2
+    k, v = bf(rng.normal(size=(n, d))), bf(rng.normal(size=(n, d)))
+    q = bf(rng.normal(size=(1, G, d)))
+    p = rng.integers(1, 4, size=n)
+    E = rng.permutation(n)[:13]
+    R = np.setdiff1d(np.arange(n), E)
+    full = make_session(k, v, vote=p, G=G)
+    sR = make_session(k[R], v[R], vote=p[R], G=G)
+    sE = make_session(k[E], v[E], vote=p[E], G=G)
+    l, f, _ = full.attend(q)
+    lR, fR, _ = sR.attend(q)
+    lE, fE, _ = sE.attend(q)
+    np.testing.assert_allclose(np.exp(l), np.exp(lR) + np.exp(lE), rtol=1e-13)
+    wR = np.exp(lR - l)[..., None]
+    np.testing.assert_allclose(f, wR * fR + (1 - wR) * fE, atol=1e-13)
+    for s in (full, sR, sE):
+        s.close()
+
+
+def test_eviction_error_identity():
+    """o' = (o - A_e v_e) / (1 - A_e) (KeepKV eq 3): evicting one slot and
+    recomputing equals removing its share from the full output (G = 1, so the
+    emitted probability is A_e)."""
+    rng = np.random.default_rng(5)
+    n, d = 21, 32
+    k, v = bf(rng.normal(size=(n, d))), bf(rng.normal(size=(n, d)))
+    q = bf(rng.normal(size=(1, 1, d)))
+    p = rng.integers(1, 4, size=n)
+    for e in (0, 7, n - 1):
+        full = make_session(k, v, vote=p)
+        l, o, probs = full.attend(q)
+        keep = np.setdiff1d(np.arange(n), [e])
+        red = make_session(k[keep], v[keep], vote=p[keep])
+        _, o2, _ = red.attend(q)
+        Ae = probs[0, e]
+        np.testing.assert_allclose(o2[0, 0], (o[0, 0] - Ae * v[e]) / (1 - Ae), atol=1e-13)
+        full.close(); red.close()
+
+
+# ---------------------------------------------------------------- utilities
+
+def test_utility_rules_closed_forms():
+    """InertiaKV eqs 2-4 with first observation m = s: constant s gives m = s
+    under single and EMA; EMA after k refreshes of s' from m0 is
+    alpha^k m0 + (1 - alpha^k) s'; cumulative is the running sum."""
+    n, d = 5, 4
+    k = np.zeros((n, d)); v = np.zeros((n, d))
+    alpha = 0.9
+    s0 = np.array([0.1, 0.2, 0.3, 0.25, 0.15])
+    s1 = np.array([0.05, 0.4, 0.1, 0.3, 0.15])
+    for rule in (O.RULE_SINGLE, O.RULE_CUMULATIVE, O.RULE_EMA):
+        s = make_session(k, v, cap=n)
+        probs = np.zeros((1, n))
+        probs[0] = s0
+        s.update_util(probs, rule, alpha)
+        np.testing.assert_array_equal(s.slots()[3][0], s0)      # first observation
+        for it in range(1, 6):
+            probs[0] = s1
+            s.update_util(probs, rule, alpha)
+            m = s.slots()[3][0]
+            if rule == O.RULE_SINGLE:
+                np.testing.assert_array_equal(m, s1)
+            elif rule == O.RULE_CUMULATIVE:
+                np.testing.assert_allclose(m, s0 + it * s1, rtol=1e-15)
+            else:
+                np.testing.assert_allclose(m, alpha ** it * s0 + (1 - alpha ** it) * s1,
+                                           rtol=1e-14)
+        s.close()
+
+
+def brute_force_victims(m, pos, scored, k):
+    """Independent formulation: among all k-subsets of scored slots, those
+    with the least total utility; among those, the one whose sorted positions
+    are lexicographically smallest (evict the older token on equal utility)."""
+    cand = [i for i in range(len(m)) if scored[i]]
+    best = None
+    for E in itertools.combinations(cand, k):
+        key = (sum(m[i] for i in E), sorted(pos[i] for i in E))
+        if best is None or key < best[0]:
+            best = (key, E)
+    return sorted(pos[i] for i in best[1])
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_selection_matches_brute_force(seed):
+    """Lowest-utility eviction (InertiaKV sec 3.1; MomentKV Alg. 1 argmin
+    loop) against subset enumeration, with ties from small integer utilities
+    and some unscored (protected) slots."""
+    rng = np.random.default_rng(100 + seed)
+    n = int(rng.integers(4, 12))
+    L = int(rng.integers(1, n))
+    d = 4
+    s = O.DecodeSession(1, 1, d, n + 2)
+    n_old = n - int(rng.integers(0, min(3, L) + 1))
+    pos = rng.permutation(1000)[:n_old].astype(np.int32)
+    s.load(0, np.zeros((n_old, d)), np.zeros((n_old, d)), pos=pos)
+    util = rng.integers(0, 4, size=n_old) / 8.0      # exact ties
+    probs = np.zeros((1, n + 2)); probs[0, :n_old] = util
+    s.update_util(probs, O.RULE_SINGLE, 0.0)
+    for j in range(n - n_old):                          # unscored newcomers
+        s.append(np.zeros((1, d)), np.zeros((1, d)), 2000 + j)
+    nn, P, _, M, SC = s.slots()
+    k = n - L
+    vic, nv, thr = s.select(L, k)
+    assert nv[0] == k
+    expect = brute_force_victims(M[0, :n], P[0, :n], SC[0, :n], k)
+    assert sorted(vic[0, :k].tolist()) == expect
+    s.close()
+
+
+# ---------------------------------------------------------------- moments
+
+def test_moments_match_two_pass_numpy():
+    """Raw running sums (MomentKV App. A.1) reproduce the two-pass weighted
+    mean and value-key covariance of the evicted set (numpy, centred first)."""
+    rng = np.random.default_rng(6)
+    n, d = 30, 8
+    k = bf(rng.normal(1.0, 2.0, size=(n, d)))
+    v = bf(rng.normal(-0.5, 1.0, size=(n, d)))
+    p = rng.integers(1, 5, size=n)
+    s = O.DecodeSession(1, 1, d, n)
+    s.load(0, k, v, vote=p)
+    E = rng.permutation(n)[:17]
+    s.evict(E[None, :].astype(np.int32), np.array([E.size], np.int32))
+    ne, mk, mv, C = s.moments()
+    w = p[E].astype(float)
+    muk = (w[:, None] * k[E]).sum(0) / w.sum()
+    muv = (w[:, None] * v[E]).sum(0) / w.sum()
+    Cn = ((w[:, None] * (v[E] - muv)).T @ (k[E] - muk)) / w.sum()
+    assert ne[0] == w.sum()
+    np.testing.assert_allclose(mk[0], muk, atol=1e-13)
+    np.testing.assert_allclose(mv[0], muv, atol=1e-13)
+    np.testing.assert_allclose(C[0], Cn, atol=1e-12)
+    assert s.slots()[0][0] == n - E.size
+    s.close()
+
+
+def test_vote_fold_equals_duplicate_fold():
+    rng = np.random.default_rng(7)
+    n, d = 10, 8
+    k, v = bf(rng.normal(size=(n, d))), bf(rng.normal(size=(n, d)))
+    p = rng.integers(1, 4, size=n)
+    a = O.DecodeSession(1, 1, d, n)
+    a.load(0, k, v, vote=p)
+    rep = np.repeat(np.arange(n), p)
+    b = O.DecodeSession(1, 1, d, rep.size)
+    b.load(0, k[rep], v[rep])
+    a.evict(np.arange(n, dtype=np.int32)[None], np.array([n], np.int32))
+    b.evict(np.arange(rep.size, dtype=np.int32)[None], np.array([rep.size], np.int32))
+    for x, y in zip(a.moments(), b.moments()):
+        np.testing.assert_allclose(x, y, atol=1e-12)
+    a.close(); b.close()
+
+
+# ---------------------------------------------------------------- correction
+
+def _corrected_vs_full(k, v, p, q, E, correction):
+    n, d = k.shape
+    G = q.shape[1]
+    full = make_session(k, v, vote=p, G=G)
+    _, f_full, _ = full.attend(q)
+    full.close()
+    s = make_session(k, v, vote=p, G=G)
+    s.evict(np.asarray(E, np.int32)[None], np.array([len(E)], np.int32))
+    o, fR, lz = s.output(q, correction)
+    s.close()
+    return o, fR, f_full
+
+
+def test_correction_off_and_empty_moments_give_renormalized_output():
+    """Correction off, or n_e = 0, returns f_R (MomentKV Alg. 1 step 17)."""
+    rng = np.random.default_rng(8)
+    n, d, G = 20, 16, 2
+    k, v = bf(rng.normal(size=(n, d))), bf(rng.normal(size=(n, d)))
+    q = bf(rng.normal(size=(1, G, d)))
+    p = np.ones(n, int)
+    o, fR, _ = _corrected_vs_full(k, v, p, q, [3, 4, 5], O.CORR_OFF)
+    np.testing.assert_array_equal(o, fR)
+    o, fR, f_full = _corrected_vs_full(k, v, p, q, [], O.CORR_FIRST_ORDER)
+    np.testing.assert_array_equal(o, fR)
+    np.testing.assert_allclose(o, f_full, atol=1e-14)
+
+
+@pytest.mark.parametrize("correction", [O.CORR_ZERO_ORDER, O.CORR_FIRST_ORDER])
+def test_identical_evicted_keys_recover_full_output(correction):
+    """If every evicted key is the same vector, all centred logits vanish:
+    the Jensen bound is an equality (App. B.1) and fhat_E = v_bar = f_E, so
+    the corrected output equals the full-cache output exactly."""
+    rng = np.random.default_rng(9)
+    n, d, G = 24, 16, 4
+    k, v = bf(rng.normal(size=(n, d))), bf(rng.normal(size=(n, d)))
+    E = [2, 5, 11, 17, 20]
+    k[E] = k[E[0]]
+    p = rng.integers(1, 4, size=n)
+    q = bf(rng.normal(size=(1, G, d)))
+    o, fR, f_full = _corrected_vs_full(k, v, p, q, E, correction)
+    np.testing.assert_allclose(o, f_full, atol=1e-13)
+    assert np.abs(fR - f_full).max() > 1e-3       # plain renormalization is off
+
+
+def test_zero_query_recovers_full_output():
+    rng = np.random.default_rng(10)
+    n, d, G = 24, 16, 2
+    k, v = bf(rng.normal(size=(n, d))), bf(rng.normal(size=(n, d)))
+    p = rng.integers(1, 4, size=n)
+    o, fR, f_full = _corrected_vs_full(k, v, p, np.zeros((1, G, d)), [0, 1, 2, 9],
+                                       O.CORR_FIRST_ORDER)
+    np.testing.assert_allclose(o, f_full, atol=1e-14)
+
+
+def _error_at_spread(sigma, correction, seed=11):
+    rng = np.random.default_rng(seed)
+    d, G, nR, nE = 16, 1, 12, 40
+    A = rng.normal(size=(d, d)) / 4
+    kR = rng.normal(size=(nR, d))
+    xi = rng.normal(size=(nE, d))
+    kE = sigma * xi
+    k = np.vstack([kR, kE])
+    v = np.vstack([rng.normal(size=(nR, d)), 0.5 + xi @ A.T + 0.02 * rng.normal(size=(nE, d))])
+    k, v = bf(k), bf(v)
+    q = bf(2.0 * rng.normal(size=(1, G, d)))
+    E = list(range(nR, nR + nE))
+    o, fR, f_full = _corrected_vs_full(k, v, np.ones(nR + nE, int), q, E, correction)
+    return np.abs(o - f_full).max()
+
+
+def test_first_order_error_is_second_order_in_spread():
+    """The corrected output's error scales as sigma^2 (MomentKV sec 4.1 and
+    App. A.2): halving the key spread quarters it.  The zero-order variant
+    (v_bar only) is first order: halving sigma only halves it.  A sign error
+    in the covariance term would also show up as first-order scaling."""
+    e1 = [_error_at_spread(s, O.CORR_FIRST_ORDER) for s in (0.05, 0.025, 0.0125)]
+    e0 = [_error_at_spread(s, O.CORR_ZERO_ORDER) for s in (0.05, 0.025, 0.0125)]
+    for a, b in zip(e1, e1[1:]):
+        assert 3.0 < a / b < 5.0, e1
+    for a, b in zip(e0, e0[1:]):
+        assert 1.6 < a / b < 2.6, e0
+    assert e1[-1] < e0[-1] / 10
+
+
+def test_jensen_lower_bound_tightness_and_self_regulation():
+    """Zhat_E = n_e exp(q.k_bar/sqrt d) <= Z_E (MomentKV sec 4.2 eq 10,
+    App. B.1).  Zhat_E is read back from the zero-order output
+    o = w f_R + (1 - w) v_bar as Zhat_E = Z_R (1 - w) / w and compared with
+    the exact Z_E of the evicted set:
+      * w >= w_R and Zhat_E <= Z_E at every spread;
+      * tightness: Z_E / Zhat_E - 1 ~ Var(delta) / 2 for a small spread, with
+        delta_i = q.(k_i - k_bar)/sqrt(d) computed here in numpy (App. B.1);
+      * self-regulation: Zhat_E / Z_E falls as the spread grows (App. B.2)."""
+    rng = np.random.default_rng(12)
+    d, nR, nE = 16, 10, 30
+    kR = bf(rng.normal(size=(nR, d)))
+    vR = bf(rng.normal(size=(nR, d)))
+    vE = bf(rng.normal(size=(nE, d)) + 3.0)
+    xi = rng.normal(size=(nE, d))
+    q = bf(rng.normal(size=(1, 1, d)))
+    ratios = []
+    for sigma in (0.02, 0.04, 0.5, 2.0, 8.0):
+        kE = bf(sigma * xi)
+        k = np.vstack([kR, kE]); v = np.vstack([vR, vE])
+        E = list(range(nR, nR + nE))
+        s = make_session(k, v)
+        s.evict(np.asarray(E, np.int32)[None], np.array([nE], np.int32))
+        o, fR, lzR = s.output(q, O.CORR_ZERO_ORDER)
+        s.close()
+        vbar = vE.mean(0)
+        dvec = fR[0, 0] - vbar
+        w = float((o[0, 0] - vbar) @ dvec / (dvec @ dvec))
+        sE = make_session(kE, vE)
+        lE, _, _ = sE.attend(q)
+        sE.close()
+        wR = 1.0 / (1.0 + math.exp(lE[0, 0] - lzR[0, 0]))
+        assert w >= wR - 1e-12
+        log_zhat = lzR[0, 0] + math.log((1 - w) / w)
+        assert log_zhat <= lE[0, 0] + 1e-12
+        ratios.append(math.exp(log_zhat - lE[0, 0]))
+        if sigma <= 0.04:
+            delta = (kE - kE.mean(0)) @ q[0, 0] / math.sqrt(d)
+            half_var = 0.5 * np.mean(delta ** 2)
+            assert (1.0 / ratios[-1] - 1.0) == pytest.approx(half_var, rel=0.05)
+    assert all(a > b for a, b in zip(ratios, ratios[1:])), ratios
+    assert ratios[-1] < 1e-3
+
+
+# ---------------------------------------------------------------- pipeline
+
+def test_no_eviction_when_budget_covers_everything():
+    """With L >= N + steps nothing is evicted: the output is plain attention
+    over every token and the moments stay zero."""
+    rng = np.random.default_rng(13)
+    U, N, d, G, S = 2, 12, 8, 2, 4
+    kp, vp = bf(rng.normal(size=(U, N, d))), bf(rng.normal(size=(U, N, d)))
+    qs = bf(rng.normal(size=(S, U, G, d)))
+    ks, vs = bf(rng.normal(size=(S, U, d))), bf(rng.normal(size=(S, U, d)))
+    res = O.decode_generation(kp, vp, qs, ks, vs, L=N + S, rule=O.RULE_EMA,
+                              alpha=0.9, T=1, correction=O.CORR_FIRST_ORDER)
+    for r in res:
+        assert (r["applied_nvict"] == 0).all()
+        np.testing.assert_allclose(r["o"], r["f_all"], atol=1e-14)
+        assert (r["moments"][0] == 0).all()
+
+
+def test_generation_invariants_and_lazy_refresh():
+    """Whole decode loop: after every step each unit holds min(L, ...) slots;
+    step 1 evicts N + 1 - L, later steps one each; under a refresh period T
+    the utilities only change on refresh steps (InertiaKV-Lazy), so with T
+    longer than the run every surviving prefill slot keeps its step-1 score
+    (Score-Free)."""
+    rng = np.random.default_rng(14)
+    U, N, d, G, S, L = 2, 20, 8, 2, 6, 8
+    kp, vp = bf(rng.normal(size=(U, N, d))), bf(rng.normal(size=(U, N, d)))
+    qs = bf(rng.normal(size=(S, U, G, d)))
+    ks, vs = bf(rng.normal(size=(S, U, d))), bf(rng.normal(size=(S, U, d)))
+    sess = O.DecodeSession(U, G, d, N + S)
+    for u in range(U):
+        sess.load(u, kp[u], vp[u])
+    step1 = None
+    for s in range(S):
+        t = s + 1
+        r = O.decode_step(sess, t, N + t - 1, qs[s], ks[s], vs[s], L=L,
+                          rule=O.RULE_EMA, alpha=0.9, T=S + 5,
+                          correction=O.CORR_FIRST_ORDER)
+        n, pos, _, util, scored = sess.slots()
+        assert (n == L).all()
+        assert (r["applied_nvict"] == (N + 1 - L if t == 1 else 1)).all()
+        assert r["refresh"] == (t == 1)
+        if t == 1:
+            # before the step-1 eviction slot i held position i
+            step1 = {(u, i): r["probs"][u, i] for u in range(U) for i in range(N + 1)}
+        for u in range(U):
+            for i in range(L):
+                if scored[u, i]:
+                    assert util[u, i] == step1[(u, int(pos[u, i]))]
+                else:
+                    assert pos[u, i] >= N + 1     # appended after the refresh
+    sess.close()

@@ -1,0 +1,128 @@
+"""Pins of the fp64 oracle's LaProx prefill scorer ("Reformulating KV Cache
+Eviction Problem for Long-Context LLM Inference", arXiv 2605.07234, key
+designs 1-3) against closed forms, numpy and brute force."""
+import itertools
+import math
+
+import numpy as np
+import pytest
+
+from oracle import oracle as O
+
+
+def bf(x):
+    return O.bf16_round(x)
+
+
+def test_gram_route_matches_direct_projection():
+    """r_i = sqrt(v^T W_g W_g^T v) equals ||v W_g|| computed by numpy's matmul
+    and by the oracle's direct route, W_g the sum of the group's W_O slices."""
+    rng = np.random.default_rng(0)
+    NL, Hq, Hkv, d, N = 2, 4, 2, 8, 20
+    D = Hq * d
+    W = bf(rng.normal(0, 0.2, size=(NL, Hq * d, D)))
+    V = bf(rng.normal(size=(NL, Hkv, N, d)))
+    Gram = O.prefill_gram(W, NL, Hq, Hkv, d)
+    r = O.prefill_rownorm(V, Gram, NL, Hkv, d, N)
+    G = Hq // Hkv
+    for l in range(NL):
+        for g in range(Hkv):
+            Wg = sum(W[l, h * d:(h + 1) * d, :] for h in range(g * G, (g + 1) * G))
+            np.testing.assert_allclose(r[l, g], np.linalg.norm(V[l, g] @ Wg, axis=1), rtol=1e-12)
+            tok = np.array([0, 7, N - 1], np.int32)
+            direct = O.prefill_rownorm_direct(V, W, Hq, Hkv, d, N, l, g, tok)
+            np.testing.assert_allclose(direct, r[l, g, tok], rtol=1e-12)
+
+
+def test_orthonormal_projection_scales_norm():
+    """If W_g = c [I | 0] (orthonormal rows times c) then r_i = c ||v_i||."""
+    rng = np.random.default_rng(1)
+    NL, Hq, Hkv, d, N = 1, 4, 1, 8, 6
+    D = Hq * d
+    W = np.zeros((NL, Hq * d, D))
+    for h in range(Hq):
+        W[0, h * d:(h + 1) * d, :d] = 0.5 * np.eye(d)      # sum over 4 heads: 2 I
+    V = bf(rng.normal(size=(NL, Hkv, N, d)))
+    r = O.prefill_rownorm(V, O.prefill_gram(W, NL, Hq, Hkv, d), NL, Hkv, d, N)
+    np.testing.assert_allclose(r[0, 0], 2.0 * np.linalg.norm(V[0, 0], axis=1), rtol=1e-14)
+
+
+def test_uniform_window_attention_closed_form():
+    """q = 0: window row j (position N-w+j) spreads weight 1/(N-w+j+1) over
+    the keys it sees, so c_i = sqrt(sum over rows that see key i of
+    1/(N-w+j+1)^2); this pins the causal mask and the group mean."""
+    NL, Hq, Hkv, d, N, w = 1, 4, 2, 8, 12, 5
+    rng = np.random.default_rng(2)
+    K = bf(rng.normal(size=(NL, Hkv, N, d)))
+    q = np.zeros((NL, Hq, w, d))
+    c = O.prefill_colnorm(q, K, NL, Hq, Hkv, d, N, w)
+    for i in range(N):
+        expect = math.sqrt(sum(1.0 / (N - w + j + 1) ** 2 for j in range(w) if i <= N - w + j))
+        np.testing.assert_allclose(c[0, :, i], expect, rtol=1e-13)
+
+
+def test_dominant_key_gives_sqrt_window():
+    """Every window row of every head putting all its weight on key i* gives
+    A_bar[:, i*] = 1, so c_{i*} = sqrt(w) and the other columns vanish."""
+    NL, Hq, Hkv, d, N, w = 1, 4, 1, 16, 40, 8
+    K = np.zeros((NL, Hkv, N, d))
+    istar = 13
+    K[0, 0, istar, 0] = 64.0
+    q = np.zeros((NL, Hq, w, d)); q[..., 0] = 8.0            # logit 128 vs 0
+    c = O.prefill_colnorm(q, K, NL, Hq, Hkv, d, N, w)
+    assert c[0, 0, istar] == pytest.approx(math.sqrt(w), rel=1e-12)
+    assert np.delete(c[0, 0], istar).max() < 1e-40
+
+
+def test_colnorm_matches_scipy_softmax():
+    from scipy.special import softmax
+    rng = np.random.default_rng(3)
+    NL, Hq, Hkv, d, N, w = 1, 6, 2, 8, 15, 4
+    K = bf(rng.normal(size=(NL, Hkv, N, d)))
+    q = bf(rng.normal(size=(NL, Hq, w, d)))
+    c = O.prefill_colnorm(q, K, NL, Hq, Hkv, d, N, w)
+    G = Hq // Hkv
+    for g in range(Hkv):
+        Abar = np.zeros((w, N))
+        for h in range(g * G, (g + 1) * G):
+            x = q[0, h] @ K[0, g].T / math.sqrt(d)
+            mask = np.arange(N)[None, :] > (N - w + np.arange(w))[:, None]
+            x[mask] = -np.inf
+            Abar += softmax(x, axis=1) / G
+        np.testing.assert_allclose(c[0, g], np.linalg.norm(Abar, axis=0), rtol=1e-12)
+
+
+def test_layer_normalization_sums_to_one():
+    rng = np.random.default_rng(4)
+    NL, Hkv, N = 3, 2, 10
+    c = rng.random((NL, Hkv, N)); r = rng.random((NL, Hkv, N)) * 10 ** np.arange(NL)[:, None, None]
+    res = O.prefill_select(c, r, 7, normalize=True)
+    np.testing.assert_allclose(res["s"].sum(axis=(1, 2)), 1.0, rtol=1e-14)
+    raw = O.prefill_select(c, r, 7, normalize=False)
+    np.testing.assert_allclose(raw["s"], c * r, rtol=0)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_global_topk_matches_brute_force(seed):
+    """Model-wide top-K (LaProx key design 3) against subset enumeration:
+    the K-subset of largest total score, ties broken towards the
+    lexicographically smallest flat indices."""
+    rng = np.random.default_rng(50 + seed)
+    NL, Hkv, N = 2, 2, int(rng.integers(2, 4))
+    M = NL * Hkv * N
+    Kb = int(rng.integers(1, M))
+    c = rng.integers(1, 4, size=(NL, Hkv, N)).astype(float)
+    r = np.ones((NL, Hkv, N))
+    res = O.prefill_select(c, r, Kb, normalize=True)
+    from fractions import Fraction
+    p = (c * r).astype(int)
+    s = [Fraction(int(p.ravel()[j]), int(p[j // (Hkv * N)].sum())) for j in range(M)]
+    best = None
+    for S in itertools.combinations(range(M), Kb):
+        key = (-sum(s[j] for j in S), list(S))     # exact rational sums
+        if best is None or key < best[0]:
+            best = (key, S)
+    assert sorted(res["idx"].tolist()) == list(best[1])
+    assert res["keep"].ravel().nonzero()[0].tolist() == list(best[1])
+    assert res["counts"].sum() == Kb
+    np.testing.assert_array_equal(res["counts"], res["keep"].sum(axis=2))
