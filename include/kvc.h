@@ -1,0 +1,354 @@
+/*
+ * kvc.h -- C ABI of libkvc, the GB300 (sm_103a) budgeted-KV decode step and
+ * LaProx prefill scorer.
+ *
+ * Method sources (web pages), cited per entry point:
+ *   MomentKV  "MOMENTKV: Closing the Directional Gap in KV Cache Eviction for
+ *             Long-Context Inference" (arXiv 2606.01563)
+ *   InertiaKV "Key factors of KV cache eviction in aggressive decoding:
+ *             temporal aggregation and rank preservation" (arXiv 2609.03515)
+ *   KeepKV    "KeepKV: lossless KV cache compression with electoral votes and
+ *             zero-perturbation merging" (reading notes, arXiv 2504.09936)
+ *   LaProx    "Reformulating KV Cache Eviction Problem for Long-Context LLM
+ *             Inference" (arXiv 2605.07234)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - A unit is one (sequence, layer, KV head); units are independent.  The
+ *   unit index of sequence b, layer l, KV head g is u = (b*NL + l)*Hkv + g.
+ *   G = query heads per KV head (GQA group); query head h of the unit is the
+ *   group's h-th head.
+ * - bf16 values are passed as uint16_t bit patterns.  Every pointer is a
+ *   DEVICE pointer owned by the caller unless stated otherwise; the library
+ *   allocates no device memory.  Scratch lives in a caller-allocated
+ *   workspace whose size the *_workspace_size functions return.
+ * - Every call is asynchronous on the CUDA stream passed as `stream`
+ *   (a cudaStream_t; NULL = legacy default stream).  Only
+ *   kvc_get_device_status blocks.
+ * - Arguments are validated on the host before any launch; a failed check
+ *   returns an error code, launches nothing and sets kvc_last_error().
+ *   Conditions that only the device can see (a unit whose length does not
+ *   fit the caller's bounds) set a status word in the workspace and leave
+ *   that unit untouched; kvc_get_device_status reads and clears it.
+ * - Errors never trap or abort on the device.
+ * - Layouts (row-major, innermost last):
+ *     q        [U][G][d]   bf16     query of the current step
+ *     k_new    [U][d]      bf16     key of the token appended this step
+ *     v_new    [U][d]      bf16
+ *     K, V     [U][cap][d] bf16     slot i of unit u at (u*cap + i)*d
+ *     votes    [U][cap]    int32    integer vote p_i >= 1, or NULL = all 1
+ *     pos      [U][cap]    int32    token position of each slot
+ *     util     [U][cap]    fp64     aggregated utility m(i); +inf = never
+ *                                   scored (protected from eviction).  fp64
+ *                                   keeps the order of utilities far below
+ *                                   fp32's range (sharp attention)
+ *     len      [U]         int32    slots in use (slots [0, len) are live)
+ *     moments  n [U], mu_k [U][d], mu_v [U][d], C [U][d][d]   fp32
+ *              C[a][b] = cov(v_a, k_b) over the evicted set (population)
+ * - Supported shapes: d = 128, G in {1, 2, 4, 8}.
+ */
+#ifndef KVC_H
+#define KVC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVC_VERSION 10000  /* major*10000 + minor*100 + patch */
+
+/* Exported symbols (the library is built with hidden default visibility). */
+#if defined(__GNUC__)
+#define KVC_API __attribute__((visibility("default")))
+#else
+#define KVC_API
+#endif
+
+typedef enum {
+    KVC_OK = 0,
+    KVC_ERR_INVALID_ARG = 1,  /* a null pointer or a value out of range      */
+    KVC_ERR_SHAPE = 2,        /* sizes inconsistent (e.g. len + 1 > cap)     */
+    KVC_ERR_CUDA = 3,         /* a CUDA runtime call failed                  */
+    KVC_ERR_TIMEOUT = 4,      /* a bounded device wait ran out               */
+    KVC_ERR_UNSUPPORTED = 5,  /* shape outside the supported set             */
+    KVC_ERR_WORKSPACE = 6     /* workspace missing, misaligned or too small  */
+} kvc_status;
+
+enum { KVC_RULE_SINGLE = 0, KVC_RULE_CUMULATIVE = 1, KVC_RULE_EMA = 2 };
+enum { KVC_CORR_OFF = 0, KVC_CORR_ZERO_ORDER = 1, KVC_CORR_FIRST_ORDER = 2 };
+
+/* Method parameters of a decode stream. */
+typedef struct {
+    int32_t U;               /* units                                        */
+    int32_t G;               /* query heads per KV head (1, 2, 4, 8)         */
+    int32_t d;               /* head dimension (128)                         */
+    int32_t cap;             /* slot capacity per unit (row stride of K, V)  */
+    int32_t L;               /* budget: slots kept per unit after a step     */
+    int32_t rule;            /* KVC_RULE_*  (InertiaKV sec 3.1 eqs 2-4)      */
+    float alpha;             /* EMA coefficient, 0 <= alpha < 1              */
+    int32_t refresh_period;  /* T >= 1, T <= L: utilities refresh on step
+                                t = 1 and whenever (t - 1) mod T == 0
+                                (InertiaKV-Lazy; T = 1 is full refresh)      */
+    int32_t correction;      /* KVC_CORR_* (MomentKV sec 4.2 eq 12; the zero-
+                                order variant of MomentKV Table 4)           */
+} kvc_params;
+
+/* The budgeted cache of every unit (device pointers, caller-owned). */
+typedef struct {
+    uint16_t *K;
+    uint16_t *V;
+    int32_t *votes;   /* NULL = every vote is 1 (no vote weighting)        */
+    int32_t *pos;
+    double *util;
+    int32_t *len;
+} kvc_cache;
+
+/* Eviction-set moment statistics (device pointers, caller-owned; zero at the
+ * start of each generation, MomentKV sec A4 setup). */
+typedef struct {
+    float *n;      /* [U]       vote-weighted count n_e                    */
+    float *mu_k;   /* [U][d]    key mean k_bar                             */
+    float *mu_v;   /* [U][d]    value mean v_bar                           */
+    float *C;      /* [U][d][d] S_tilde / n_e, C[a][b] = cov(v_a, k_b)     */
+} kvc_moments;
+
+/* ------------------------------------------------------------------ */
+/* library                                                             */
+/* ------------------------------------------------------------------ */
+
+/* KVC_VERSION of the loaded library. */
+KVC_API int32_t kvc_version(void);
+
+/* Message of the last failed call on this host thread ("" if none).  The
+ * string is owned by the library and valid until the next call on the same
+ * thread. */
+KVC_API const char *kvc_last_error(void);
+
+/* Static name of a status code. */
+KVC_API const char *kvc_status_string(int32_t status);
+
+/* ------------------------------------------------------------------ */
+/* decode step                                                          */
+/* ------------------------------------------------------------------ */
+
+/* Bytes of workspace the decode entry points need for these parameters
+ * (covers every decode call, including a step-1 pass over cap slots).  The
+ * same workspace (device memory, 256-byte aligned) must be passed to every
+ * call of one decode stream and left untouched between calls: it carries
+ * per-step scratch and per-stream state. */
+KVC_API size_t kvc_decode_workspace_size(const kvc_params *p);
+
+/* Zero the workspace's persistent state and status word (enqueued on
+ * `stream`).  Call once before the first step of a decode stream. */
+KVC_API kvc_status kvc_decode_workspace_init(const kvc_params *p, void *ws,
+                                     size_t ws_bytes, void *stream);
+
+/* Read and clear the device status word of a workspace (blocks on `stream`).
+ * *device_status receives KVC_OK or the first error a kernel recorded. */
+KVC_API kvc_status kvc_get_device_status(void *ws, size_t ws_bytes, void *stream,
+                                 int32_t *device_status);
+
+/*
+ * kvc_decode_attend -- append the step's token, then vote-weighted
+ * single-query GQA attention over every slot of every unit.
+ *
+ * Defined by: MomentKV sec 2 (s_i = q^T k_i / sqrt(d), Z, alpha_i, f) and
+ * Algorithm 1 (append before eviction); KeepKV eq 6 / eq 23 (votes, applied as the
+ * logit bias ln p_i, KeepKV "integration" item 2); InertiaKV sec 3.1 eq 1
+ * (head-mean probability s_t(i), averaged over the G query heads sharing the
+ * KV head).
+ *
+ * For each unit u (n = len[u] on entry):
+ *   slot n receives k_new[u], v_new[u], vote 1, position new_pos, utility
+ *   +inf (unscored); len[u] becomes n + 1;
+ *   x_hi = q_h . k_i / sqrt(d) + ln p_i, i in [0, n];
+ *   lse[u][h]  = log sum_i exp(x_hi);
+ *   f_all[u][h][:] = sum_i exp(x_hi - lse) v_i;
+ *   probs[u][i] = (1/G) sum_h exp(x_hi - lse_h)   (only if probs != NULL).
+ * t is the 1-based decode step (only recorded; it does not change the
+ * arithmetic).  max_len >= n + 1 for every unit bounds the launch; a unit
+ * with n + 1 > max_len or n + 1 > cap is skipped and sets the device status
+ * KVC_ERR_SHAPE.
+ * Outputs lse [U][G], f_all [U][G][d] fp32 (required), probs [U][cap] fp64
+ * (optional; entries past len untouched).  Logits are fp32; the
+ * probabilities are formed in fp64 so that values below fp32's range keep
+ * their order.
+ */
+KVC_API kvc_status kvc_decode_attend(const kvc_params *p, int32_t t, int32_t new_pos,
+                             int32_t max_len, const uint16_t *q,
+                             const uint16_t *k_new, const uint16_t *v_new,
+                             const kvc_cache *cache, float *lse, float *f_all,
+                             double *probs, void *ws, size_t ws_bytes,
+                             void *stream);
+
+/*
+ * kvc_aggregate_evict -- temporal utility update and lowest-utility victim
+ * selection.
+ *
+ * Defined by: InertiaKV sec 3.1 eqs 2-4 (single m = s, cumulative
+ * m = m + s, EMA m = alpha m + (1 - alpha) s) and "evict the lowest m_t(i)
+ * while the cache exceeds the budget"; InertiaKV-Lazy periodic refresh;
+ * MomentKV Algorithm 1 phase 1 (argmin loop).
+ *
+ * On a refresh step (t = 1 or (t - 1) mod T == 0) every live slot's utility
+ * is updated from probs (required then): an unscored slot takes m = s, a
+ * scored one the rule.  On other steps utilities are left as they are.
+ * Then k = len[u] - L victims (0 if len <= L) are chosen among scored slots:
+ * the k smallest (m, pos) pairs, utility ascending, ties to the smaller
+ * token position.  evict_idx[u][0..k) receives their slot indices in
+ * ascending slot order, evict_pos (optional) their positions in the same
+ * order, n_evict[u] = k.  A unit needing more than kmax victims, or with
+ * fewer than k scored slots, gets n_evict = 0 and sets the device status
+ * (KVC_ERR_SHAPE / KVC_ERR_INVALID_ARG).  Nothing is removed here.
+ */
+KVC_API kvc_status kvc_aggregate_evict(const kvc_params *p, int32_t t,
+                               const double *probs, const kvc_cache *cache,
+                               int32_t kmax, int32_t *evict_idx,
+                               int32_t *evict_pos, int32_t *n_evict, void *ws,
+                               size_t ws_bytes, void *stream);
+
+/*
+ * kvc_moment_update -- fold the evicted tokens into the eviction-set
+ * moments, each weighted by its vote.
+ *
+ * Defined by: MomentKV sec 4.1 "efficient statistics update", Algorithm 1
+ * eviction phase and App. A.1 (n_e, s_k, s_v, S updated by addition;
+ * S_tilde = S - s_v s_k^T / n_e).  The library keeps the equivalent mean /
+ * covariance form (n, mu_k, mu_v, C = S_tilde / n) and updates it with the
+ * weighted pairwise merge of Chan, Golub and LeVeque (1979), the one-token
+ * case being West's (1979) weighted incremental update.  A vote p counts as
+ * p identical tokens (KeepKV eq 6).
+ * Reads K, V, votes at evict_idx[u][0..n_evict[u]) (before compaction).
+ */
+KVC_API kvc_status kvc_moment_update(const kvc_params *p, const kvc_cache *cache,
+                             int32_t kmax, const int32_t *evict_idx,
+                             const int32_t *n_evict, const kvc_moments *mom,
+                             void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * kvc_correct -- retained-only attention and the moment-based normalization
+ * correction.
+ *
+ * Defined by: MomentKV Algorithm 1 inference phase, sec 4.1 eq 9
+ * (fhat_E = v_bar + S_tilde q / (n_e sqrt d)), sec 4.2 eqs 10-12 (Jensen
+ * bound Zhat_E = n_e exp(q . k_bar / sqrt d), w_R = Z_R / (Z_R + Zhat_E)),
+ * App. C.2 (log-domain weight); KeepKV eq 3 (o' = (o - A_e v_e)/(1 - A_e)),
+ * used to obtain the retained-only output from the full pass.
+ *
+ * Call after kvc_moment_update and before kvc_compact, with lse / f_all from
+ * kvc_decode_attend of the same step.  Per unit and head:
+ *   f_R, log Z_R over the live slots not in evict_idx: by the eviction-error
+ *     identity when at most 16 slots go and their attention mass is <= 0.5,
+ *     otherwise by a direct pass over the retained slots;
+ *   n = 0 or correction off: o = f_R;
+ *   else log Zhat_E = ln n + q . mu_k / sqrt(d),
+ *        fhat_E = mu_v + C q / sqrt(d)   (first order) or mu_v (zero order),
+ *        w_R = 1 / (1 + exp(log Zhat_E - log Z_R)),
+ *        o = w_R f_R + (1 - w_R) fhat_E.
+ * Outputs o [U][G][d] fp32 (required), f_R [U][G][d] and logZ_R [U][G]
+ * (optional).
+ */
+KVC_API kvc_status kvc_correct(const kvc_params *p, const uint16_t *q,
+                       const kvc_cache *cache, int32_t kmax,
+                       const int32_t *evict_idx, const int32_t *n_evict,
+                       const float *lse, const float *f_all,
+                       const kvc_moments *mom, float *o, float *f_R,
+                       float *logZ_R, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * kvc_compact -- remove the evicted slots (MomentKV Algorithm 1, end of the
+ * eviction phase).
+ * Live slots keep their contents; the slot order is not significant (slots
+ * are identified by position).  With n = len - k, every evicted slot below
+ * n is filled by a live slot at or above n (both taken in ascending order);
+ * K, V, votes, pos and util move together; len[u] = n.
+ */
+KVC_API kvc_status kvc_compact(const kvc_params *p, const kvc_cache *cache,
+                       int32_t kmax, const int32_t *evict_idx,
+                       const int32_t *n_evict, void *ws, size_t ws_bytes,
+                       void *stream);
+
+/*
+ * kvc_decode_step -- the whole decode step, fused: the same results as
+ * kvc_decode_attend, kvc_aggregate_evict, kvc_moment_update, kvc_correct and
+ * kvc_compact called in that order (same sets; outputs within fp32
+ * rounding).
+ *
+ * In the steady state (max_len == L + 1: every unit enters with len = L and
+ * evicts exactly one slot) one cluster kernel per step does everything: the
+ * new token is written straight into the victim's slot.  Otherwise (e.g.
+ * step 1 over the prefill cache) the five-call sequence runs.
+ * probs (optional [U][cap] fp64) receives the head-mean probabilities on refresh
+ * steps in the slot order of the step's input (the new token at index
+ * len); evict_pos / evict_idx (optional [U][kmax]) the evicted positions /
+ * slot indices; n_evict [U] (required) the victim counts; o [U][G][d] the
+ * corrected output.
+ */
+KVC_API kvc_status kvc_decode_step(const kvc_params *p, int32_t t, int32_t new_pos,
+                           int32_t max_len, const uint16_t *q,
+                           const uint16_t *k_new, const uint16_t *v_new,
+                           const kvc_cache *cache, const kvc_moments *mom,
+                           float *o, double *probs, int32_t kmax,
+                           int32_t *evict_idx, int32_t *evict_pos,
+                           int32_t *n_evict, void *ws, size_t ws_bytes,
+                           void *stream);
+
+/* ------------------------------------------------------------------ */
+/* prefill scorer                                                       */
+/* ------------------------------------------------------------------ */
+
+/*
+ * kvc_prefill_prepare -- per-group Gram matrices of the output projection,
+ * once per weight set.
+ *
+ * Defined by: LaProx key design 1 (Output = sum_h A^h (V^h W_O^h)) and its
+ * GQA group-mean paragraph.  Reading: the group's attention is the mean over
+ * its query heads, so the group's product is A_bar V_g W_g with
+ * W_g = sum of W_O^h over the group's heads (W_O^h = rows [h d, (h+1) d)).
+ * Gram[l][g] = W_g W_g^T, accumulated in fp64 and stored fp32, so that
+ * ||(V W_g)[i,:]||^2 = v_i^T Gram v_i.
+ * W_O [NL][Hq*d][D] bf16; Gram [NL][Hkv][d][d] fp32.
+ */
+KVC_API kvc_status kvc_prefill_prepare(int32_t NL, int32_t Hq, int32_t Hkv, int32_t d,
+                               int32_t D, const uint16_t *W_O, float *Gram,
+                               void *stream);
+
+/* Bytes of workspace kvc_prefill_score needs. */
+KVC_API size_t kvc_prefill_workspace_size(int32_t NL, int32_t Hkv, int32_t N,
+                                  int64_t B_total);
+
+/*
+ * kvc_prefill_score -- LaProx indicator, per-layer normalization and one
+ * model-wide top-K.
+ *
+ * Defined by: LaProx key design 1 (p_i = ||A[:,i]||_2 ||(V W_O)[i,:]||_2),
+ * key design 2 (s_{l,j} = p_{l,j} / sum_k p_{l,k}), key design 3 (global
+ * top-K under B_total), the GQA group-mean attention paragraph; the
+ * observation window of the last w prompt queries (SnapKV protocol, MomentKV
+ * sec A4).
+ *   window query j (0..w-1) sits at position N - w + j and sees keys
+ *   0..N-w+j; A^h = row softmax of q K^T / sqrt(d); A_bar = mean over the
+ *   group's G heads; c_i = ||A_bar[:, i]||_2; r_i = sqrt(v_i^T Gram v_i);
+ *   p = c r; s = p / (sum of p over the layer's heads and tokens) when
+ *   normalize != 0, else s = p; keep the B_total largest s over all
+ *   (l, g, i), equal scores kept in ascending flat index (l*Hkv + g)*N + i.
+ * q_win [NL][Hq][w][d], K, V [NL][Hkv][N][d] bf16; Gram from
+ * kvc_prefill_prepare.  Outputs: scores [NL][Hkv][N] fp32, keep
+ * [NL][Hkv][N] uint8 (0/1), counts [NL][Hkv] int32, idx [B_total] int64 kept
+ * flat indices ascending.  Any output except keep may be NULL.
+ */
+KVC_API kvc_status kvc_prefill_score(int32_t NL, int32_t Hq, int32_t Hkv, int32_t d,
+                             int32_t N, int32_t w, int64_t B_total,
+                             int32_t normalize, const uint16_t *q_win,
+                             const uint16_t *K, const uint16_t *V,
+                             const float *Gram, float *scores, uint8_t *keep,
+                             int32_t *counts, int64_t *idx, void *ws,
+                             size_t ws_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVC_H */

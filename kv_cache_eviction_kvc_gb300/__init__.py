@@ -1,0 +1,7 @@
+"""Budgeted-KV decode step and LaProx prefill scorer on GB300 (sm_103a).
+
+The compute lives in libkvc (``csrc/``, C ABI in ``include/kvc.h``); ``kvc``
+is its thin ctypes binding, ``state`` allocates device memory for a decode
+stream and ``workloads`` draws the seeded synthetic inputs.
+"""
+__all__ = ["kvc", "state", "workloads"]

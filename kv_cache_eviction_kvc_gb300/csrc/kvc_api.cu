@@ -1,0 +1,319 @@
+// kvc_api.cu -- the extern "C" entry points of libkvc: host-side argument
+// validation, workspace carve-up, error reporting and kernel dispatch.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <cuda_runtime.h>
+
+#include "kvc_common.cuh"
+#include "kvc_internal.h"
+
+namespace kvc {
+
+static thread_local char g_err[512] = "";
+
+void set_error(const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+}
+
+DecodeWs decode_ws_layout(const kvc_params &p, void *base)
+{
+    DecodeWs w{};
+    char *b = static_cast<char *>(base);
+    size_t off = 0;
+    const size_t U = (size_t)p.U, G = (size_t)p.G, cap = (size_t)p.cap;
+    const size_t S = (cap + kAttendChunk - 1) / kAttendChunk;
+    w.status = reinterpret_cast<int32_t *>(b ? b + off : nullptr);
+    off += align_up(sizeof(WsHeader));
+    w.xbuf = reinterpret_cast<float *>(b ? b + off : nullptr);
+    off += align_up(U * G * cap * sizeof(float));
+    w.part = reinterpret_cast<float *>(b ? b + off : nullptr);
+    off += align_up(U * S * G * (kD + 2) * sizeof(float));
+    w.nlen = reinterpret_cast<int32_t *>(b ? b + off : nullptr);
+    off += align_up(U * sizeof(int32_t));
+    w.pend = reinterpret_cast<int32_t *>(b ? b + off : nullptr);
+    off += align_up(U * kPendStride * sizeof(int32_t));
+    w.lse = reinterpret_cast<float *>(b ? b + off : nullptr);
+    off += align_up(U * G * sizeof(float));
+    w.fall = reinterpret_cast<float *>(b ? b + off : nullptr);
+    off += align_up(U * G * kD * sizeof(float));
+    w.probs = reinterpret_cast<double *>(b ? b + off : nullptr);
+    off += align_up(U * cap * sizeof(double));
+    w.bytes = off;
+    return w;
+}
+
+}  // namespace kvc
+
+using namespace kvc;
+
+#define KVC_CHECK_ARG(cond, code, ...)       \
+    do {                                     \
+        if (!(cond)) {                       \
+            set_error(__VA_ARGS__);          \
+            return (code);                   \
+        }                                    \
+    } while (0)
+
+static kvc_status cuda_status(cudaError_t e, const char *what)
+{
+    if (e == cudaSuccess) return KVC_OK;
+    set_error("%s: %s", what, cudaGetErrorString(e));
+    return KVC_ERR_CUDA;
+}
+
+static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+static kvc_status check_params(const kvc_params *p)
+{
+    KVC_CHECK_ARG(p != nullptr, KVC_ERR_INVALID_ARG, "params is NULL");
+    KVC_CHECK_ARG(p->d == kD, KVC_ERR_UNSUPPORTED, "d = %d unsupported (only 128)", p->d);
+    KVC_CHECK_ARG(p->G == 1 || p->G == 2 || p->G == 4 || p->G == 8, KVC_ERR_UNSUPPORTED,
+                  "G = %d unsupported (1, 2, 4, 8)", p->G);
+    KVC_CHECK_ARG(p->U >= 1, KVC_ERR_INVALID_ARG, "U = %d must be >= 1", p->U);
+    KVC_CHECK_ARG(p->cap >= 1 && p->cap <= kMaxCap, KVC_ERR_UNSUPPORTED,
+                  "cap = %d outside [1, %d]", p->cap, kMaxCap);
+    KVC_CHECK_ARG(p->L >= 1 && p->L < p->cap, KVC_ERR_INVALID_ARG,
+                  "L = %d must satisfy 1 <= L < cap = %d", p->L, p->cap);
+    KVC_CHECK_ARG(p->rule >= KVC_RULE_SINGLE && p->rule <= KVC_RULE_EMA, KVC_ERR_INVALID_ARG,
+                  "rule = %d unknown", p->rule);
+    KVC_CHECK_ARG(p->rule != KVC_RULE_EMA || (p->alpha >= 0.f && p->alpha < 1.f),
+                  KVC_ERR_INVALID_ARG, "alpha = %g outside [0, 1)", (double)p->alpha);
+    KVC_CHECK_ARG(p->refresh_period >= 1 && p->refresh_period <= p->L, KVC_ERR_INVALID_ARG,
+                  "refresh period T = %d must satisfy 1 <= T <= L = %d", p->refresh_period, p->L);
+    KVC_CHECK_ARG(p->correction >= KVC_CORR_OFF && p->correction <= KVC_CORR_FIRST_ORDER,
+                  KVC_ERR_INVALID_ARG, "correction = %d unknown", p->correction);
+    return KVC_OK;
+}
+
+static kvc_status check_cache(const kvc_cache *c)
+{
+    KVC_CHECK_ARG(c != nullptr, KVC_ERR_INVALID_ARG, "cache is NULL");
+    KVC_CHECK_ARG(c->K && c->V && c->pos && c->util && c->len, KVC_ERR_INVALID_ARG,
+                  "cache K, V, pos, util and len must be non-NULL");
+    KVC_CHECK_ARG(aligned16(c->K) && aligned16(c->V), KVC_ERR_INVALID_ARG,
+                  "cache K and V must be 16-byte aligned");
+    KVC_CHECK_ARG(((uintptr_t)c->util & 7u) == 0, KVC_ERR_INVALID_ARG,
+                  "cache util must be 8-byte aligned");
+    return KVC_OK;
+}
+
+static kvc_status check_ws(const kvc_params *p, void *ws, size_t bytes, DecodeWs *out)
+{
+    DecodeWs w = decode_ws_layout(*p, nullptr);
+    KVC_CHECK_ARG(ws != nullptr, KVC_ERR_WORKSPACE, "workspace is NULL");
+    KVC_CHECK_ARG(((uintptr_t)ws & (kAlign - 1)) == 0, KVC_ERR_WORKSPACE,
+                  "workspace must be 256-byte aligned");
+    KVC_CHECK_ARG(bytes >= w.bytes, KVC_ERR_WORKSPACE,
+                  "workspace has %zu bytes, needs %zu", bytes, w.bytes);
+    *out = decode_ws_layout(*p, ws);
+    return KVC_OK;
+}
+
+static kvc_status check_moments(const kvc_moments *m)
+{
+    KVC_CHECK_ARG(m != nullptr && m->n && m->mu_k && m->mu_v && m->C, KVC_ERR_INVALID_ARG,
+                  "moments and all their arrays must be non-NULL");
+    KVC_CHECK_ARG(aligned16(m->C), KVC_ERR_INVALID_ARG, "moments C must be 16-byte aligned");
+    return KVC_OK;
+}
+
+#define KVC_TRY(expr)                     \
+    do {                                  \
+        kvc_status _s = (expr);           \
+        if (_s != KVC_OK) return _s;      \
+    } while (0)
+
+extern "C" {
+
+int32_t kvc_version(void) { return KVC_VERSION; }
+
+const char *kvc_last_error(void) { return g_err; }
+
+const char *kvc_status_string(int32_t s)
+{
+    switch (s) {
+    case KVC_OK: return "KVC_OK";
+    case KVC_ERR_INVALID_ARG: return "KVC_ERR_INVALID_ARG";
+    case KVC_ERR_SHAPE: return "KVC_ERR_SHAPE";
+    case KVC_ERR_CUDA: return "KVC_ERR_CUDA";
+    case KVC_ERR_TIMEOUT: return "KVC_ERR_TIMEOUT";
+    case KVC_ERR_UNSUPPORTED: return "KVC_ERR_UNSUPPORTED";
+    case KVC_ERR_WORKSPACE: return "KVC_ERR_WORKSPACE";
+    default: return "KVC_ERR_UNKNOWN";
+    }
+}
+
+size_t kvc_decode_workspace_size(const kvc_params *p)
+{
+    if (check_params(p) != KVC_OK) return 0;
+    return decode_ws_layout(*p, nullptr).bytes;
+}
+
+kvc_status kvc_decode_workspace_init(const kvc_params *p, void *ws, size_t ws_bytes,
+                                     void *stream)
+{
+    KVC_TRY(check_params(p));
+    DecodeWs w;
+    KVC_TRY(check_ws(p, ws, ws_bytes, &w));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    KVC_TRY(cuda_status(cudaMemsetAsync(w.status, 0, sizeof(WsHeader), st), "workspace init"));
+    KVC_TRY(cuda_status(cudaMemsetAsync(w.pend, 0, (size_t)p->U * kPendStride * sizeof(int32_t), st),
+                        "workspace init"));
+    return KVC_OK;
+}
+
+kvc_status kvc_get_device_status(void *ws, size_t ws_bytes, void *stream, int32_t *device_status)
+{
+    KVC_CHECK_ARG(ws != nullptr && ws_bytes >= sizeof(WsHeader), KVC_ERR_WORKSPACE,
+                  "workspace missing or too small");
+    KVC_CHECK_ARG(device_status != nullptr, KVC_ERR_INVALID_ARG, "device_status is NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    KVC_TRY(cuda_status(cudaMemcpyAsync(&v, ws, sizeof v, cudaMemcpyDeviceToHost, st), "status read"));
+    KVC_TRY(cuda_status(cudaStreamSynchronize(st), "status read"));
+    KVC_TRY(cuda_status(cudaMemsetAsync(ws, 0, sizeof(int32_t), st), "status clear"));
+    *device_status = v;
+    return KVC_OK;
+}
+
+kvc_status kvc_decode_attend(const kvc_params *p, int32_t t, int32_t new_pos, int32_t max_len,
+                             const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
+                             const kvc_cache *cache, float *lse, float *f_all, double *probs,
+                             void *ws, size_t ws_bytes, void *stream)
+{
+    KVC_TRY(check_params(p));
+    KVC_TRY(check_cache(cache));
+    DecodeWs w;
+    KVC_TRY(check_ws(p, ws, ws_bytes, &w));
+    KVC_CHECK_ARG(t >= 1, KVC_ERR_INVALID_ARG, "step t = %d must be >= 1", t);
+    KVC_CHECK_ARG(max_len >= 1 && max_len <= p->cap, KVC_ERR_SHAPE,
+                  "max_len = %d must satisfy 1 <= max_len <= cap = %d", max_len, p->cap);
+    KVC_CHECK_ARG(q && k_new && v_new && lse && f_all, KVC_ERR_INVALID_ARG,
+                  "q, k_new, v_new, lse and f_all must be non-NULL");
+    KVC_CHECK_ARG(aligned16(q) && aligned16(k_new) && aligned16(v_new), KVC_ERR_INVALID_ARG,
+                  "q, k_new and v_new must be 16-byte aligned");
+    return cuda_status(launch_attend(*p, t, new_pos, max_len, q, k_new, v_new, *cache, lse, f_all,
+                                     probs, w, static_cast<cudaStream_t>(stream)),
+                       "kvc_decode_attend launch");
+}
+
+kvc_status kvc_aggregate_evict(const kvc_params *p, int32_t t, const double *probs,
+                               const kvc_cache *cache, int32_t kmax, int32_t *evict_idx,
+                               int32_t *evict_pos, int32_t *n_evict, void *ws, size_t ws_bytes,
+                               void *stream)
+{
+    KVC_TRY(check_params(p));
+    KVC_TRY(check_cache(cache));
+    DecodeWs w;
+    KVC_TRY(check_ws(p, ws, ws_bytes, &w));
+    KVC_CHECK_ARG(t >= 1, KVC_ERR_INVALID_ARG, "step t = %d must be >= 1", t);
+    KVC_CHECK_ARG(kmax >= 1, KVC_ERR_INVALID_ARG, "kmax = %d must be >= 1", kmax);
+    KVC_CHECK_ARG(evict_idx && n_evict, KVC_ERR_INVALID_ARG, "evict_idx and n_evict must be non-NULL");
+    KVC_CHECK_ARG(probs || !is_refresh(t, p->refresh_period), KVC_ERR_INVALID_ARG,
+                  "probs is required on refresh step t = %d", t);
+    return cuda_status(launch_aggregate(*p, t, probs, *cache, kmax, evict_idx, evict_pos, n_evict,
+                                        w, static_cast<cudaStream_t>(stream)),
+                       "kvc_aggregate_evict launch");
+}
+
+kvc_status kvc_moment_update(const kvc_params *p, const kvc_cache *cache, int32_t kmax,
+                             const int32_t *evict_idx, const int32_t *n_evict,
+                             const kvc_moments *mom, void *ws, size_t ws_bytes, void *stream)
+{
+    KVC_TRY(check_params(p));
+    KVC_TRY(check_cache(cache));
+    KVC_TRY(check_moments(mom));
+    DecodeWs w;
+    KVC_TRY(check_ws(p, ws, ws_bytes, &w));
+    KVC_CHECK_ARG(kmax >= 1 && evict_idx && n_evict, KVC_ERR_INVALID_ARG,
+                  "kmax >= 1, evict_idx and n_evict required");
+    return cuda_status(launch_moment(*p, *cache, kmax, evict_idx, n_evict, *mom, w,
+                                     static_cast<cudaStream_t>(stream)),
+                       "kvc_moment_update launch");
+}
+
+kvc_status kvc_correct(const kvc_params *p, const uint16_t *q, const kvc_cache *cache,
+                       int32_t kmax, const int32_t *evict_idx, const int32_t *n_evict,
+                       const float *lse, const float *f_all, const kvc_moments *mom, float *o,
+                       float *f_R, float *logZ_R, void *ws, size_t ws_bytes, void *stream)
+{
+    KVC_TRY(check_params(p));
+    KVC_TRY(check_cache(cache));
+    KVC_TRY(check_moments(mom));
+    DecodeWs w;
+    KVC_TRY(check_ws(p, ws, ws_bytes, &w));
+    KVC_CHECK_ARG(q && lse && f_all && o, KVC_ERR_INVALID_ARG, "q, lse, f_all and o must be non-NULL");
+    KVC_CHECK_ARG(kmax >= 1 && evict_idx && n_evict, KVC_ERR_INVALID_ARG,
+                  "kmax >= 1, evict_idx and n_evict required");
+    return cuda_status(launch_correct(*p, q, *cache, kmax, evict_idx, n_evict, lse, f_all, *mom, o,
+                                      f_R, logZ_R, w, static_cast<cudaStream_t>(stream)),
+                       "kvc_correct launch");
+}
+
+kvc_status kvc_compact(const kvc_params *p, const kvc_cache *cache, int32_t kmax,
+                       const int32_t *evict_idx, const int32_t *n_evict, void *ws,
+                       size_t ws_bytes, void *stream)
+{
+    KVC_TRY(check_params(p));
+    KVC_TRY(check_cache(cache));
+    DecodeWs w;
+    KVC_TRY(check_ws(p, ws, ws_bytes, &w));
+    KVC_CHECK_ARG(kmax >= 1 && evict_idx && n_evict, KVC_ERR_INVALID_ARG,
+                  "kmax >= 1, evict_idx and n_evict required");
+    return cuda_status(launch_compact(*p, *cache, kmax, evict_idx, n_evict, w,
+                                      static_cast<cudaStream_t>(stream)),
+                       "kvc_compact launch");
+}
+
+kvc_status kvc_decode_step(const kvc_params *p, int32_t t, int32_t new_pos, int32_t max_len,
+                           const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
+                           const kvc_cache *cache, const kvc_moments *mom, float *o,
+                           double *probs, int32_t kmax, int32_t *evict_idx, int32_t *evict_pos,
+                           int32_t *n_evict, void *ws, size_t ws_bytes, void *stream)
+{
+    KVC_TRY(check_params(p));
+    KVC_TRY(check_cache(cache));
+    KVC_TRY(check_moments(mom));
+    DecodeWs w;
+    KVC_TRY(check_ws(p, ws, ws_bytes, &w));
+    KVC_CHECK_ARG(t >= 1, KVC_ERR_INVALID_ARG, "step t = %d must be >= 1", t);
+    KVC_CHECK_ARG(max_len >= 1 && max_len <= p->cap, KVC_ERR_SHAPE,
+                  "max_len = %d must satisfy 1 <= max_len <= cap = %d", max_len, p->cap);
+    KVC_CHECK_ARG(q && k_new && v_new && o && n_evict, KVC_ERR_INVALID_ARG,
+                  "q, k_new, v_new, o and n_evict must be non-NULL");
+    KVC_CHECK_ARG(aligned16(q) && aligned16(k_new) && aligned16(v_new), KVC_ERR_INVALID_ARG,
+                  "q, k_new and v_new must be 16-byte aligned");
+    KVC_CHECK_ARG(kmax >= 1 && kmax >= max_len - p->L, KVC_ERR_SHAPE,
+                  "kmax = %d must be >= max(1, max_len - L = %d)", kmax, max_len - p->L);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (max_len == p->L + 1) {
+        cudaError_t e = launch_fused_step(*p, t, new_pos, q, k_new, v_new, *cache, *mom, o, probs,
+                                          kmax, evict_idx, evict_pos, n_evict, w, st);
+        if (e != cudaErrorNotSupported) return cuda_status(e, "kvc_decode_step fused launch");
+    }
+    // general case: the five-call sequence with workspace scratch
+    KVC_CHECK_ARG(evict_idx != nullptr, KVC_ERR_INVALID_ARG,
+                  "evict_idx is required when the step is not in the steady state");
+    const bool refresh = is_refresh(t, p->refresh_period);
+    double *pr = probs ? probs : w.probs;
+    KVC_TRY(cuda_status(launch_attend(*p, t, new_pos, max_len, q, k_new, v_new, *cache, w.lse,
+                                      w.fall, refresh ? pr : nullptr, w, st),
+                        "kvc_decode_step attend"));
+    KVC_TRY(cuda_status(launch_aggregate(*p, t, pr, *cache, kmax, evict_idx, evict_pos, n_evict, w, st),
+                        "kvc_decode_step aggregate"));
+    KVC_TRY(cuda_status(launch_moment(*p, *cache, kmax, evict_idx, n_evict, *mom, w, st),
+                        "kvc_decode_step moments"));
+    KVC_TRY(cuda_status(launch_correct(*p, q, *cache, kmax, evict_idx, n_evict, w.lse, w.fall, *mom,
+                                       o, nullptr, nullptr, w, st),
+                        "kvc_decode_step correct"));
+    return cuda_status(launch_compact(*p, *cache, kmax, evict_idx, n_evict, w, st),
+                       "kvc_decode_step compact");
+}
+
+}  // extern "C"

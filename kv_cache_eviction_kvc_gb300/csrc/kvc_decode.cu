@@ -1,0 +1,1057 @@
+// kvc_decode.cu -- the decode step as five separate kernels (any number of
+// victims per step; step 1 over the whole prefill cache runs here).
+//
+//   attend_chunk  : append + vote-biased logits + per-chunk softmax partials
+//   attend_final  : split merge -> lse, f_all; head-mean probabilities
+//   aggregate     : utility update (refresh steps) + lowest-(m, pos) select
+//   moment_fold   : weighted Chan/West merge of the victims into (n, mu, C)
+//   correct       : retained-only output (identity or direct) + correction
+//   compact       : fill holes below the new length from slots above it
+//
+// Method: MomentKV Algorithm 1 (phase order), sec 4.1-4.2, App. A.1, C.2;
+// InertiaKV sec 3.1 eqs 1-4; KeepKV eqs 3, 6, 23.
+#include <math.h>
+
+#include "kvc_common.cuh"
+#include "kvc_internal.h"
+
+namespace kvc {
+
+// ===================================================================== attend
+//
+// One CTA = one unit x one chunk of kAttendChunk slots, 8 warps.  A warp
+// works on 4 slots at a time: 8 lanes per slot, lane c holding dims
+// [8c, 8c+8) and [64+8c, 64+8c+8) (two coalesced 16-byte loads per row).
+// Pass 1 computes the logits of the chunk into shared memory (and the
+// workspace when probabilities are wanted) and the chunk max per head;
+// pass 2 streams V with p = exp(x - max): no online rescaling is needed.
+
+struct AttendArgs {
+    const uint16_t *q, *k_new, *v_new;
+    uint16_t *K, *V;
+    int32_t *votes, *pos;
+    double *util;
+    const int32_t *len;
+    float *xbuf, *part;
+    int32_t *nlen, *status;
+    int U, cap, max_len, new_pos, S;
+    int want_x;
+};
+
+template <int G>
+__global__ void __launch_bounds__(256) attend_chunk_kernel(AttendArgs a)
+{
+    constexpr int CH = kAttendChunk;
+    constexpr int kBuf = (G * CH > 8 * G * kD) ? G * CH : 8 * G * kD;
+    __shared__ __align__(16) float sbuf[kBuf];
+    __shared__ float red[8][G];
+    float (*xs)[CH] = reinterpret_cast<float (*)[CH]>(sbuf);          // pass 1-2
+    float (*accs)[G][kD] = reinterpret_cast<float (*)[G][kD]>(sbuf);  // after
+
+    const int u = blockIdx.x, s = blockIdx.y;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int grp = lane >> 3, c = lane & 7;
+
+    const int n_old = a.len[u];
+    const int n = n_old + 1;
+    if (n_old < 0 || n > a.max_len || n > a.cap) {
+        if (s == 0 && tid == 0) {
+            record_status(a.status, KVC_ERR_SHAPE);
+            a.nlen[u] = -1;
+        }
+        return;
+    }
+    const int s0 = s * CH;
+    if (s0 >= n) return;
+    const int s1 = min(n, s0 + CH);
+    if (s == 0 && tid == 0) a.nlen[u] = n;
+
+    const size_t ubase = (size_t)u * a.cap;
+    const uint16_t *knew = a.k_new + (size_t)u * kD;
+    const uint16_t *vnew = a.v_new + (size_t)u * kD;
+
+    // the chunk holding the new slot appends it
+    if (n_old >= s0 && n_old < s1) {
+        if (tid < 32) {
+            uint16_t *kd = a.K + (ubase + n_old) * kD;
+            uint16_t *vd = a.V + (ubase + n_old) * kD;
+            reinterpret_cast<uint2 *>(kd)[tid] = reinterpret_cast<const uint2 *>(knew)[tid];
+            reinterpret_cast<uint2 *>(vd)[tid] = reinterpret_cast<const uint2 *>(vnew)[tid];
+        } else if (tid == 32) {
+            if (a.votes) a.votes[ubase + n_old] = 1;
+            a.pos[ubase + n_old] = a.new_pos;
+            a.util[ubase + n_old] = __longlong_as_double(0x7ff0000000000000ll);
+        }
+    }
+
+    // q of the group, scaled by 1/sqrt(d), dims of this lane
+    const float rs = rsqrtf((float)kD);
+    float qf[G][16];
+#pragma unroll
+    for (int h = 0; h < G; h++) {
+        const uint16_t *qh = a.q + ((size_t)u * G + h) * kD;
+        uint4 r0 = *reinterpret_cast<const uint4 *>(qh + 8 * c);
+        uint4 r1 = *reinterpret_cast<const uint4 *>(qh + 64 + 8 * c);
+        unpack8(r0, qf[h]);
+        unpack8(r1, qf[h] + 8);
+#pragma unroll
+        for (int j = 0; j < 16; j++) qf[h][j] *= rs;
+    }
+
+    // ---- pass 1: logits
+    float mx[G];
+#pragma unroll
+    for (int h = 0; h < G; h++) mx[h] = -INFINITY;
+    for (int base = s0 + w * 4; base < s1; base += 32) {
+        const int i = base + grp;
+        const bool ok = i < s1;
+        float kf[16];
+        if (ok) {
+            const uint16_t *kr = (i == n_old) ? knew : a.K + (ubase + i) * kD;
+            uint4 r0 = (i == n_old) ? *reinterpret_cast<const uint4 *>(kr + 8 * c)
+                                    : ldg_nc_v4(kr + 8 * c);
+            uint4 r1 = (i == n_old) ? *reinterpret_cast<const uint4 *>(kr + 64 + 8 * c)
+                                    : ldg_nc_v4(kr + 64 + 8 * c);
+            unpack8(r0, kf);
+            unpack8(r1, kf + 8);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; j++) kf[j] = 0.f;
+        }
+        float part[G];
+#pragma unroll
+        for (int h = 0; h < G; h++) {
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; j++) acc = fmaf(qf[h][j], kf[j], acc);
+            part[h] = acc;
+        }
+#pragma unroll
+        for (int m = 1; m < 8; m <<= 1)
+#pragma unroll
+            for (int h = 0; h < G; h++) part[h] += __shfl_xor_sync(kFull, part[h], m);
+        if (ok) {
+            float lnp = 0.f;
+            if (a.votes && i != n_old) lnp = logf((float)a.votes[ubase + i]);
+#pragma unroll
+            for (int h = 0; h < G; h++) {
+                const float x = part[h] + lnp;
+                mx[h] = fmaxf(mx[h], x);
+                if (c == h) {
+                    xs[h][i - s0] = x;
+                    if (a.want_x) a.xbuf[((size_t)u * G + h) * a.cap + i] = x;
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < G; h++) {
+        float v = warp_max(mx[h]);
+        if (lane == 0) red[w][h] = v;
+    }
+    __syncthreads();
+    float M[G];
+#pragma unroll
+    for (int h = 0; h < G; h++) {
+        float v = red[0][h];
+#pragma unroll
+        for (int j = 1; j < 8; j++) v = fmaxf(v, red[j][h]);
+        M[h] = v;
+    }
+    __syncthreads();
+
+    // ---- pass 2: p = exp(x - M), accumulate p v and sum p
+    float acc[G][16];
+    float lsum[G];
+#pragma unroll
+    for (int h = 0; h < G; h++) {
+        lsum[h] = 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; j++) acc[h][j] = 0.f;
+    }
+    for (int base = s0 + w * 4; base < s1; base += 32) {
+        const int i = base + grp;
+        if (i < s1) {
+            const uint16_t *vr = (i == n_old) ? vnew : a.V + (ubase + i) * kD;
+            uint4 r0 = (i == n_old) ? *reinterpret_cast<const uint4 *>(vr + 8 * c)
+                                    : ldg_nc_v4(vr + 8 * c);
+            uint4 r1 = (i == n_old) ? *reinterpret_cast<const uint4 *>(vr + 64 + 8 * c)
+                                    : ldg_nc_v4(vr + 64 + 8 * c);
+            float vf[16];
+            unpack8(r0, vf);
+            unpack8(r1, vf + 8);
+#pragma unroll
+            for (int h = 0; h < G; h++) {
+                const float p = expf(xs[h][i - s0] - M[h]);
+                if (c == 0) lsum[h] += p;
+#pragma unroll
+                for (int j = 0; j < 16; j++) acc[h][j] = fmaf(p, vf[j], acc[h][j]);
+            }
+        }
+    }
+    // reduce over the 4 slot groups of the warp
+#pragma unroll
+    for (int h = 0; h < G; h++) {
+#pragma unroll
+        for (int j = 0; j < 16; j++) {
+            acc[h][j] += __shfl_xor_sync(kFull, acc[h][j], 8);
+            acc[h][j] += __shfl_xor_sync(kFull, acc[h][j], 16);
+        }
+        lsum[h] = warp_sum(lsum[h]);
+    }
+    __syncthreads();   // every warp is done with xs before accs overwrites it
+    if (grp == 0) {
+#pragma unroll
+        for (int h = 0; h < G; h++)
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                accs[w][h][8 * c + j] = acc[h][j];
+                accs[w][h][64 + 8 * c + j] = acc[h][8 + j];
+            }
+    }
+    if (lane == 0)
+#pragma unroll
+        for (int h = 0; h < G; h++) red[w][h] = lsum[h];
+    __syncthreads();
+    float *pp = a.part + ((size_t)u * a.S + s) * G * (kD + 2);
+    for (int e = tid; e < G * kD; e += blockDim.x) {
+        const int h = e / kD, dd = e % kD;
+        float v = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; j++) v += accs[j][h][dd];
+        pp[h * (kD + 2) + 2 + dd] = v;
+    }
+    if (tid < G) {
+        float l = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; j++) l += red[j][tid];
+        pp[tid * (kD + 2) + 0] = M[tid];
+        pp[tid * (kD + 2) + 1] = l;
+    }
+}
+
+// Merge the split partials of a unit: global max and sum per head; CTA
+// (u, 0) writes lse, f_all and the new length; every CTA writes the
+// probabilities of its slot chunk.
+struct FinalArgs {
+    const float *part, *xbuf;
+    const int32_t *nlen;
+    int32_t *len;
+    float *lse, *f_all;
+    double *probs;
+    int U, cap, S;
+};
+
+template <int G>
+__global__ void __launch_bounds__(256) attend_final_kernel(FinalArgs a)
+{
+    __shared__ float Ms[G], Ls[G];
+    __shared__ double Rl[G];
+    const int u = blockIdx.x, s2 = blockIdx.y, tid = threadIdx.x;
+    const int n = a.nlen[u];
+    if (n <= 0) return;
+    const int Su = (n + kAttendChunk - 1) / kAttendChunk;
+    const float *pu = a.part + (size_t)u * a.S * G * (kD + 2);
+    const int lane = tid & 31, w = tid >> 5;
+    if (w < G) {
+        const int h = w;
+        float m = -INFINITY;
+        for (int s = lane; s < Su; s += 32) m = fmaxf(m, pu[(size_t)s * G * (kD + 2) + h * (kD + 2)]);
+        m = warp_max(m);
+        float l = 0.f;
+        for (int s = lane; s < Su; s += 32) {
+            const float *ph = pu + (size_t)s * G * (kD + 2) + h * (kD + 2);
+            l += ph[1] * expf(ph[0] - m);
+        }
+        l = warp_sum(l);
+        if (lane == 0) { Ms[h] = m; Ls[h] = l; Rl[h] = 1.0 / (double)l; }
+    }
+    __syncthreads();
+    if (s2 == 0) {
+        if (tid == 0) a.len[u] = n;
+        if (tid < G) a.lse[(size_t)u * G + tid] = Ms[tid] + logf(Ls[tid]);
+        for (int e = tid; e < G * kD; e += blockDim.x) {
+            const int h = e / kD, dd = e % kD;
+            float v = 0.f;
+            for (int s = 0; s < Su; s++) {
+                const float *ph = pu + (size_t)s * G * (kD + 2) + h * (kD + 2);
+                v += ph[2 + dd] * expf(ph[0] - Ms[h]);
+            }
+            a.f_all[((size_t)u * G + h) * kD + dd] = v / Ls[h];
+        }
+    }
+    if (a.probs) {
+        // s_i = (1/G) sum_h exp(x_hi - M_h) / l_h, formed in fp64
+        const int i0 = s2 * kProbsChunk, i1 = min(n, i0 + kProbsChunk);
+        for (int i = i0 + tid; i < i1; i += blockDim.x) {
+            double sacc = 0.0;
+#pragma unroll
+            for (int h = 0; h < G; h++)
+                sacc += exp_wide(a.xbuf[((size_t)u * G + h) * a.cap + i] - Ms[h]) * Rl[h];
+            a.probs[(size_t)u * a.cap + i] = sacc / G;
+        }
+    }
+}
+
+template <int G>
+static cudaError_t launch_attend_g(const kvc_params &p, int new_pos, int max_len,
+                                   const uint16_t *q, const uint16_t *k_new,
+                                   const uint16_t *v_new, const kvc_cache &c,
+                                   float *lse, float *f_all, double *probs,
+                                   const DecodeWs &ws, cudaStream_t st)
+{
+    const int S = (p.cap + kAttendChunk - 1) / kAttendChunk;
+    const int Sl = (max_len + kAttendChunk - 1) / kAttendChunk;
+    AttendArgs a{q, k_new, v_new, c.K, c.V, c.votes, c.pos, c.util, c.len,
+                 ws.xbuf, ws.part, ws.nlen, ws.status, p.U, p.cap, max_len,
+                 new_pos, S, probs != nullptr};
+    dim3 g1(p.U, Sl);
+    attend_chunk_kernel<G><<<g1, 256, 0, st>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    FinalArgs f{ws.part, ws.xbuf, ws.nlen, c.len, lse, f_all, probs, p.U, p.cap, S};
+    const int S2 = probs ? (max_len + kProbsChunk - 1) / kProbsChunk : 1;
+    attend_final_kernel<G><<<dim3(p.U, S2), 256, 0, st>>>(f);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attend(const kvc_params &p, int t, int new_pos, int max_len,
+                          const uint16_t *q, const uint16_t *k_new,
+                          const uint16_t *v_new, const kvc_cache &c,
+                          float *lse, float *f_all, double *probs,
+                          const DecodeWs &ws, cudaStream_t st)
+{
+    (void)t;
+    switch (p.G) {
+    case 1: return launch_attend_g<1>(p, new_pos, max_len, q, k_new, v_new, c, lse, f_all, probs, ws, st);
+    case 2: return launch_attend_g<2>(p, new_pos, max_len, q, k_new, v_new, c, lse, f_all, probs, ws, st);
+    case 4: return launch_attend_g<4>(p, new_pos, max_len, q, k_new, v_new, c, lse, f_all, probs, ws, st);
+    case 8: return launch_attend_g<8>(p, new_pos, max_len, q, k_new, v_new, c, lse, f_all, probs, ws, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+// ================================================================== aggregate
+//
+// One CTA per unit.  Refresh steps update the utilities in place; then the
+// k = len - L victims are the k smallest (utility, position) keys among the
+// scored slots: a 4-pass 8-bit radix select on the utility's order key finds
+// the k-th smallest utility, a second select on positions settles the group
+// of equal utilities at the threshold.
+
+struct AggArgs {
+    const double *probs;
+    double *util;
+    const int32_t *pos, *len;
+    int32_t *evict_idx, *evict_pos, *n_evict, *status;
+    int cap, L, rule, refresh, kmax;
+    float alpha;
+};
+
+// k-th smallest (0-based rank) key among the slots where valid(i); returns
+// the key and, through *below, how many valid keys are strictly smaller.
+template <typename Key, typename KeyF, typename ValidF>
+__device__ Key block_select(int n, int rank, KeyF key, ValidF valid,
+                            int *hist, int *bcast, int *below)
+{
+    Key prefix = 0, mask = 0;
+    const int rank0 = rank;
+    for (int shift = (int)sizeof(Key) * 8 - 8; shift >= 0; shift -= 8) {
+        for (int b = threadIdx.x; b < 256; b += blockDim.x) hist[b] = 0;
+        __syncthreads();
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+            if (!valid(i)) continue;
+            const Key k = key(i);
+            if ((k & mask) == prefix) atomicAdd(&hist[(int)((k >> shift) & 255)], 1);
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int cum = 0, b = 0;
+            for (; b < 255; b++) {
+                if (cum + hist[b] > rank) break;
+                cum += hist[b];
+            }
+            bcast[0] = b;
+            bcast[1] = rank - cum;
+        }
+        __syncthreads();
+        prefix |= ((Key)bcast[0]) << shift;
+        mask |= ((Key)255) << shift;
+        rank = bcast[1];
+        __syncthreads();
+    }
+    *below = rank0 - rank;
+    return prefix;
+}
+
+__global__ void __launch_bounds__(512) aggregate_kernel(AggArgs a)
+{
+    __shared__ int hist[256];
+    __shared__ int bcast[4];
+    __shared__ int scan[40];
+    const int u = blockIdx.x, tid = threadIdx.x;
+    const int n = a.len[u];
+    double *util = a.util + (size_t)u * a.cap;
+    const int32_t *pos = a.pos + (size_t)u * a.cap;
+    if (n < 0 || n > a.cap) {
+        if (tid == 0) { a.n_evict[u] = 0; record_status(a.status, KVC_ERR_SHAPE); }
+        return;
+    }
+    if (a.refresh) {
+        const double *pr = a.probs + (size_t)u * a.cap;
+        const double al = (double)a.alpha;
+        for (int i = tid; i < n; i += blockDim.x) {
+            const double s = pr[i], m = util[i];
+            double r;
+            if (isinf(m)) r = s;                           // first observation
+            else if (a.rule == KVC_RULE_SINGLE) r = s;
+            else if (a.rule == KVC_RULE_CUMULATIVE) r = m + s;
+            else r = al * m + (1.0 - al) * s;
+            util[i] = r;
+        }
+        __syncthreads();
+    }
+    const int k = n - a.L;
+    if (k <= 0) {
+        if (tid == 0) a.n_evict[u] = 0;
+        return;
+    }
+    if (k > a.kmax) {
+        if (tid == 0) { a.n_evict[u] = 0; record_status(a.status, KVC_ERR_SHAPE); }
+        return;
+    }
+    int cnt = 0;
+    for (int i = tid; i < n; i += blockDim.x) cnt += !isinf(util[i]);
+    int total;
+    block_exscan(cnt, scan, &total);
+    if (total < k) {
+        if (tid == 0) { a.n_evict[u] = 0; record_status(a.status, KVC_ERR_INVALID_ARG); }
+        return;
+    }
+    auto scored = [&](int i) { return !isinf(util[i]); };
+    auto ukey = [&](int i) { return double_key(util[i]); };
+    int below;
+    const uint64_t kth = block_select<uint64_t>(n, k - 1, ukey, scored, hist, bcast, &below);
+    const int need = k - below;       // slots to take from the tie group
+    auto tie = [&](int i) { return !isinf(util[i]) && double_key(util[i]) == kth; };
+    auto pkey = [&](int i) { return (uint32_t)pos[i] ^ 0x80000000u; };
+    int below2;
+    const uint32_t pth = block_select<uint32_t>(n, need - 1, pkey, tie, hist, bcast, &below2);
+    // write the victims in ascending slot order
+    int written = 0;
+    for (int b0 = 0; b0 < n; b0 += blockDim.x) {
+        const int i = b0 + tid;
+        int sel = 0;
+        if (i < n && !isinf(util[i])) {
+            const uint64_t kk = double_key(util[i]);
+            sel = kk < kth || (kk == kth && pkey(i) <= pth);
+        }
+        int tot;
+        const int ex = block_exscan(sel, scan, &tot);
+        if (sel && written + ex < a.kmax) {
+            a.evict_idx[(size_t)u * a.kmax + written + ex] = i;
+            if (a.evict_pos) a.evict_pos[(size_t)u * a.kmax + written + ex] = pos[i];
+        }
+        written += tot;
+    }
+    if (tid == 0) {
+        a.n_evict[u] = written == k ? k : 0;     // duplicate positions: refuse
+        if (written != k) record_status(a.status, KVC_ERR_INVALID_ARG);
+    }
+}
+
+cudaError_t launch_aggregate(const kvc_params &p, int t, const double *probs,
+                             const kvc_cache &c, int kmax, int32_t *evict_idx,
+                             int32_t *evict_pos, int32_t *n_evict,
+                             const DecodeWs &ws, cudaStream_t st)
+{
+    AggArgs a{probs, c.util, c.pos, c.len, evict_idx, evict_pos, n_evict,
+              ws.status, p.cap, p.L, p.rule, is_refresh(t, p.refresh_period),
+              kmax, p.alpha};
+    aggregate_kernel<<<p.U, 512, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+// Victim lists come from the caller: every kernel that reads one checks that
+// the count fits kmax and every slot lies in [0, len) before touching memory.
+__device__ bool victims_ok(const int32_t *ev, int k, int n, int cap, int *flag)
+{
+    if (threadIdx.x == 0) *flag = (n >= 0 && n <= cap) ? 1 : 0;
+    __syncthreads();
+    for (int e = threadIdx.x; e < k; e += blockDim.x) {
+        const int s = ev[e];
+        if (s < 0 || s >= n) *flag = 0;
+    }
+    __syncthreads();
+    const bool ok = *flag != 0;
+    __syncthreads();
+    return ok;
+}
+
+// ================================================================ moment fold
+//
+// One CTA per unit, 256 threads; thread t owns the 8 x 8 block of the
+// co-moment M = n C at rows 8*(t/16), columns 8*(t%16).  The victims are
+// taken in tiles of 32: a tile's weighted mean and centred co-moment are
+// merged into the running (n, mu_k, mu_v, M) by the pairwise update of Chan,
+// Golub and LeVeque (1979); a one-token tile is West's (1979) weighted
+// incremental update.
+
+struct MomArgs {
+    const uint16_t *K, *V;
+    const int32_t *votes, *len;
+    const int32_t *evict_idx, *n_evict;
+    float *n, *mu_k, *mu_v, *C;
+    int32_t *status;
+    int cap, kmax;
+};
+
+constexpr int kFoldTile = 32;
+
+__global__ void __launch_bounds__(256) moment_fold_kernel(MomArgs a)
+{
+    __shared__ __align__(16) float kt[kFoldTile][kD];
+    __shared__ __align__(16) float vt[kFoldTile][kD];
+    __shared__ float wt[kFoldTile];
+    __shared__ float muk[kD], muv[kD], tk[kD], tv[kD];
+    __shared__ float nb[2];
+    __shared__ int okf;
+    const int u = blockIdx.x, tid = threadIdx.x;
+    const int k = a.n_evict[u];
+    if (k <= 0) return;
+    if (k > a.kmax || !victims_ok(a.evict_idx + (size_t)u * a.kmax, k, a.len[u], a.cap, &okf)) {
+        if (tid == 0) record_status(a.status, KVC_ERR_INVALID_ARG);
+        return;
+    }
+    const int r0 = 8 * (tid >> 4), c0 = 8 * (tid & 15);
+    float *Cu = a.C + (size_t)u * kD * kD;
+    float nacc = a.n[u];
+    if (tid < kD) {
+        muk[tid] = a.mu_k[(size_t)u * kD + tid];
+        muv[tid] = a.mu_v[(size_t)u * kD + tid];
+    }
+    float M[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        const float4 x0 = *reinterpret_cast<const float4 *>(Cu + (r0 + i) * kD + c0);
+        const float4 x1 = *reinterpret_cast<const float4 *>(Cu + (r0 + i) * kD + c0 + 4);
+        M[i][0] = x0.x * nacc; M[i][1] = x0.y * nacc; M[i][2] = x0.z * nacc; M[i][3] = x0.w * nacc;
+        M[i][4] = x1.x * nacc; M[i][5] = x1.y * nacc; M[i][6] = x1.z * nacc; M[i][7] = x1.w * nacc;
+    }
+    const int32_t *ev = a.evict_idx + (size_t)u * a.kmax;
+    const size_t ubase = (size_t)u * a.cap;
+    for (int j0 = 0; j0 < k; j0 += kFoldTile) {
+        const int nt = min(kFoldTile, k - j0);
+        __syncthreads();
+        {   // load the tile: thread -> (token, 16-dim chunk)
+            const int tok = tid >> 3, ch = tid & 7;
+            if (tok < nt) {
+                const int slot = ev[j0 + tok];
+                const uint16_t *kr = a.K + (ubase + slot) * kD + 16 * ch;
+                const uint16_t *vr = a.V + (ubase + slot) * kD + 16 * ch;
+                float f[16];
+                unpack8(*reinterpret_cast<const uint4 *>(kr), f);
+                unpack8(*reinterpret_cast<const uint4 *>(kr + 8), f + 8);
+#pragma unroll
+                for (int j = 0; j < 16; j++) kt[tok][16 * ch + j] = f[j];
+                unpack8(*reinterpret_cast<const uint4 *>(vr), f);
+                unpack8(*reinterpret_cast<const uint4 *>(vr + 8), f + 8);
+#pragma unroll
+                for (int j = 0; j < 16; j++) vt[tok][16 * ch + j] = f[j];
+                if (ch == 0) wt[tok] = a.votes ? (float)a.votes[ubase + slot] : 1.f;
+            } else if (tok < kFoldTile && ch == 0) {
+                wt[tok] = 0.f;
+            }
+        }
+        __syncthreads();
+        if (tid == 0) {
+            float s = 0.f;
+            for (int j = 0; j < nt; j++) s += wt[j];
+            nb[0] = s;
+        }
+        __syncthreads();
+        const float nt_w = nb[0];
+        // tile means
+        if (tid < kD) {
+            float s = 0.f;
+            for (int j = 0; j < nt; j++) s = fmaf(wt[j], kt[j][tid], s);
+            tk[tid] = s / nt_w;
+        } else {
+            const int dd = tid - kD;
+            float s = 0.f;
+            for (int j = 0; j < nt; j++) s = fmaf(wt[j], vt[j][dd], s);
+            tv[dd] = s / nt_w;
+        }
+        __syncthreads();
+        // centre the tile (values also carry the weight)
+        for (int e = tid; e < nt * kD; e += blockDim.x) {
+            const int j = e / kD, dd = e % kD;
+            kt[j][dd] -= tk[dd];
+            vt[j][dd] = wt[j] * (vt[j][dd] - tv[dd]);
+        }
+        __syncthreads();
+        const float nn = nacc + nt_w;
+        const float cross = nacc * nt_w / nn;
+        float dv[8], dk[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            dv[i] = tv[r0 + i] - muv[r0 + i];
+            dk[i] = tk[c0 + i] - muk[c0 + i];
+        }
+        for (int j = 0; j < nt; j++) {
+            const float4 va = *reinterpret_cast<const float4 *>(&vt[j][r0]);
+            const float4 vb = *reinterpret_cast<const float4 *>(&vt[j][r0 + 4]);
+            const float4 ka = *reinterpret_cast<const float4 *>(&kt[j][c0]);
+            const float4 kb = *reinterpret_cast<const float4 *>(&kt[j][c0 + 4]);
+            const float vv[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+            const float kk[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+#pragma unroll
+            for (int i = 0; i < 8; i++)
+#pragma unroll
+                for (int jj = 0; jj < 8; jj++) M[i][jj] = fmaf(vv[i], kk[jj], M[i][jj]);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; i++)
+#pragma unroll
+            for (int jj = 0; jj < 8; jj++) M[i][jj] = fmaf(cross * dv[i], dk[jj], M[i][jj]);
+        __syncthreads();
+        if (tid < kD) muk[tid] += (tk[tid] - muk[tid]) * (nt_w / nn);
+        else muv[tid - kD] += (tv[tid - kD] - muv[tid - kD]) * (nt_w / nn);
+        nacc = nn;
+    }
+    __syncthreads();
+    const float rn = 1.f / nacc;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        float4 x0 = make_float4(M[i][0] * rn, M[i][1] * rn, M[i][2] * rn, M[i][3] * rn);
+        float4 x1 = make_float4(M[i][4] * rn, M[i][5] * rn, M[i][6] * rn, M[i][7] * rn);
+        *reinterpret_cast<float4 *>(Cu + (r0 + i) * kD + c0) = x0;
+        *reinterpret_cast<float4 *>(Cu + (r0 + i) * kD + c0 + 4) = x1;
+    }
+    if (tid < kD) {
+        a.mu_k[(size_t)u * kD + tid] = muk[tid];
+        a.mu_v[(size_t)u * kD + tid] = muv[tid];
+    }
+    if (tid == 0) a.n[u] = nacc;
+}
+
+cudaError_t launch_moment(const kvc_params &p, const kvc_cache &c, int kmax,
+                          const int32_t *evict_idx, const int32_t *n_evict,
+                          const kvc_moments &m, const DecodeWs &ws,
+                          cudaStream_t st)
+{
+    MomArgs a{c.K, c.V, c.votes, c.len, evict_idx, n_evict, m.n, m.mu_k, m.mu_v, m.C,
+              ws.status, p.cap, kmax};
+    moment_fold_kernel<<<p.U, 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+// ==================================================================== correct
+//
+// One CTA per unit, 8 warps.  f_R / log Z_R by the eviction-error identity
+// (KeepKV eq 3) when at most 16 slots went and their mass is <= 1/2 in every
+// head; otherwise by a direct online-softmax pass over the live slots that
+// are not evicted.  Then the inference phase of MomentKV Algorithm 1.
+
+struct CorrArgs {
+    const uint16_t *q, *K, *V;
+    const int32_t *votes, *len;
+    const int32_t *evict_idx, *n_evict;
+    const float *lse, *f_all;
+    const float *mn, *mu_k, *mu_v, *C;
+    float *o, *f_R, *logZ_R;
+    int32_t *status;
+    int cap, kmax, correction;
+};
+
+constexpr int kIdentityMax = 16;
+
+template <int G>
+__global__ void __launch_bounds__(256) correct_kernel(CorrArgs a)
+{
+    extern __shared__ uint32_t evbits[];   // ceil(cap/32) words
+    __shared__ __align__(16) float qs[G][kD];
+    __shared__ float fR[G][kD];
+    __shared__ float lz[G];
+    __shared__ float Ae[kIdentityMax][G];
+    __shared__ float mass[G];
+    __shared__ int direct_s;
+    __shared__ int okf;
+    __shared__ float wst[8][4][G][2];      // per warp/group (m, l)
+
+    const int u = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int k = max(0, a.n_evict[u]);
+    const int n = a.len[u];
+    if (k > a.kmax || !victims_ok(a.evict_idx + (size_t)u * a.kmax, k, n, a.cap, &okf)) {
+        if (tid == 0) record_status(a.status, KVC_ERR_INVALID_ARG);
+        return;
+    }
+    const size_t ubase = (size_t)u * a.cap;
+    const float rs = rsqrtf((float)kD);
+    for (int e = tid; e < G * kD; e += blockDim.x)
+        qs[e / kD][e % kD] = bf2f(a.q[(size_t)u * G * kD + e]);
+    if (tid == 0) direct_s = 0;
+    __syncthreads();
+
+    const int32_t *ev = a.evict_idx + (size_t)u * a.kmax;
+    if (k <= 0) {
+        for (int e = tid; e < G * kD; e += blockDim.x)
+            fR[e / kD][e % kD] = a.f_all[(size_t)u * G * kD + e];
+        if (tid < G) lz[tid] = a.lse[(size_t)u * G + tid];
+    } else if (k <= kIdentityMax) {
+        // A_e^h = exp(q_h . k_e / sqrt(d) + ln p_e - lse_h)
+        for (int e = w; e < k; e += 8) {
+            const int slot = ev[e];
+            const uint16_t *kr = a.K + (ubase + slot) * kD;
+            float kv[4];
+            for (int j = 0; j < 4; j++) kv[j] = bf2f(kr[lane * 4 + j]);
+            const float lnp = a.votes ? logf((float)a.votes[ubase + slot]) : 0.f;
+#pragma unroll
+            for (int h = 0; h < G; h++) {
+                float s = 0.f;
+                for (int j = 0; j < 4; j++) s = fmaf(qs[h][lane * 4 + j] * rs, kv[j], s);
+                s = warp_sum(s);
+                if (lane == 0) Ae[e][h] = expf(s + lnp - a.lse[(size_t)u * G + h]);
+            }
+        }
+        __syncthreads();
+        if (tid < G) {
+            float m = 0.f;
+            for (int e = 0; e < k; e++) m += Ae[e][tid];
+            mass[tid] = m;
+            if (m > 0.5f) atomicExch(&direct_s, 1);
+        }
+        __syncthreads();
+        if (!direct_s) {
+            for (int e = tid; e < G * kD; e += blockDim.x) {
+                const int h = e / kD, dd = e % kD;
+                float num = a.f_all[(size_t)u * G * kD + e];
+                for (int j = 0; j < k; j++)
+                    num = fmaf(-Ae[j][h], bf2f(a.V[(ubase + ev[j]) * kD + dd]), num);
+                fR[h][dd] = num / (1.f - mass[h]);
+            }
+            if (tid < G) lz[tid] = a.lse[(size_t)u * G + tid] + log1pf(-mass[tid]);
+        }
+    } else {
+        if (tid == 0) direct_s = 1;
+    }
+    __syncthreads();
+
+    if (direct_s) {
+        const int words = (a.cap + 31) >> 5;
+        for (int i = tid; i < words; i += blockDim.x) evbits[i] = 0;
+        for (int e = tid; e < G * kD; e += blockDim.x) fR[e / kD][e % kD] = 0.f;
+        __syncthreads();
+        for (int e = tid; e < k; e += blockDim.x) {
+            const int slot = ev[e];
+            atomicOr(&evbits[slot >> 5], 1u << (slot & 31));
+        }
+        __syncthreads();
+        const int grp = lane >> 3, c = lane & 7;
+        float qf[G][16];
+#pragma unroll
+        for (int h = 0; h < G; h++)
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                qf[h][j] = qs[h][8 * c + j] * rs;
+                qf[h][8 + j] = qs[h][64 + 8 * c + j] * rs;
+            }
+        float m[G], l[G], acc[G][16];
+#pragma unroll
+        for (int h = 0; h < G; h++) {
+            m[h] = -INFINITY; l[h] = 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; j++) acc[h][j] = 0.f;
+        }
+        for (int base = w * 4; base < n; base += 32) {
+            const int i = base + grp;
+            const bool live = i < n && !((evbits[i >> 5] >> (i & 31)) & 1u);
+            float kf[16], vf[16];
+            if (live) {
+                const uint16_t *kr = a.K + (ubase + i) * kD;
+                const uint16_t *vr = a.V + (ubase + i) * kD;
+                unpack8(ldg_nc_v4(kr + 8 * c), kf);
+                unpack8(ldg_nc_v4(kr + 64 + 8 * c), kf + 8);
+                unpack8(ldg_nc_v4(vr + 8 * c), vf);
+                unpack8(ldg_nc_v4(vr + 64 + 8 * c), vf + 8);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; j++) { kf[j] = 0.f; vf[j] = 0.f; }
+            }
+            float part[G];
+#pragma unroll
+            for (int h = 0; h < G; h++) {
+                float s = 0.f;
+#pragma unroll
+                for (int j = 0; j < 16; j++) s = fmaf(qf[h][j], kf[j], s);
+                part[h] = s;
+            }
+#pragma unroll
+            for (int mm = 1; mm < 8; mm <<= 1)
+#pragma unroll
+                for (int h = 0; h < G; h++) part[h] += __shfl_xor_sync(kFull, part[h], mm);
+            if (live) {
+                const float lnp = a.votes ? logf((float)a.votes[ubase + i]) : 0.f;
+#pragma unroll
+                for (int h = 0; h < G; h++) {
+                    const float x = part[h] + lnp;
+                    if (x > m[h]) {
+                        const float corr = expf(m[h] - x);
+                        l[h] *= corr;
+#pragma unroll
+                        for (int j = 0; j < 16; j++) acc[h][j] *= corr;
+                        m[h] = x;
+                    }
+                    const float pp = expf(x - m[h]);
+                    l[h] += pp;
+#pragma unroll
+                    for (int j = 0; j < 16; j++) acc[h][j] = fmaf(pp, vf[j], acc[h][j]);
+                }
+            }
+        }
+        // merge the 4 slot groups of each warp, then the 8 warps
+        if (c == 0)
+#pragma unroll
+            for (int h = 0; h < G; h++) { wst[w][grp][h][0] = m[h]; wst[w][grp][h][1] = l[h]; }
+        __syncthreads();
+        if (tid < G) {
+            const int h = tid;
+            float mm = -INFINITY;
+            for (int j = 0; j < 32; j++) mm = fmaxf(mm, wst[j >> 2][j & 3][h][0]);
+            float ll = 0.f;
+            for (int j = 0; j < 32; j++) {
+                const float mj = wst[j >> 2][j & 3][h][0];
+                if (mj != -INFINITY) ll += wst[j >> 2][j & 3][h][1] * expf(mj - mm);
+            }
+            mass[h] = mm;                       // reuse: global max
+            lz[h] = ll > 0.f ? mm + logf(ll) : -INFINITY;
+            Ae[0][h] = ll;                      // reuse: global sum
+        }
+        __syncthreads();
+        float sc[G];
+#pragma unroll
+        for (int h = 0; h < G; h++) sc[h] = (m[h] == -INFINITY) ? 0.f : expf(m[h] - mass[h]);
+        for (int h = 0; h < G; h++)
+            for (int j = 0; j < 16; j++) {
+                float v = acc[h][j] * sc[h];
+                v += __shfl_xor_sync(kFull, v, 8);
+                v += __shfl_xor_sync(kFull, v, 16);
+                acc[h][j] = v;
+            }
+        if (grp == 0)
+            for (int h = 0; h < G; h++)
+                for (int j = 0; j < 8; j++) {
+                    atomicAdd(&fR[h][8 * c + j], acc[h][j]);
+                    atomicAdd(&fR[h][64 + 8 * c + j], acc[h][8 + j]);
+                }
+        __syncthreads();
+        for (int e = tid; e < G * kD; e += blockDim.x) {
+            const int h = e / kD, dd = e % kD;
+            const float ll = Ae[0][h];
+            fR[h][dd] = ll > 0.f ? fR[h][dd] / ll : 0.f;
+        }
+        __syncthreads();
+    }
+
+    // ---- MomentKV Algorithm 1, normalization-corrected inference phase
+    const float ne = a.mn[u];
+    float *ou = a.o + (size_t)u * G * kD;
+    if (a.f_R)
+        for (int e = tid; e < G * kD; e += blockDim.x) a.f_R[(size_t)u * G * kD + e] = fR[e / kD][e % kD];
+    if (a.logZ_R && tid < G) a.logZ_R[(size_t)u * G + tid] = lz[tid];
+    if (ne <= 0.f || a.correction == KVC_CORR_OFF) {
+        for (int e = tid; e < G * kD; e += blockDim.x) ou[e] = fR[e / kD][e % kD];
+        return;
+    }
+    __shared__ float wR[G];
+    __shared__ float cq[G][kD];
+    const float *mk = a.mu_k + (size_t)u * kD, *mv = a.mu_v + (size_t)u * kD;
+    if (w < G) {
+        float s = 0.f;
+        for (int j = lane; j < kD; j += 32) s = fmaf(qs[w][j], mk[j], s);
+        s = warp_sum(s);
+        if (lane == 0) {
+            const float logZE = logf(ne) + s * rs;
+            wR[w] = 1.f / (1.f + expf(logZE - lz[w]));
+        }
+    }
+    if (a.correction == KVC_CORR_FIRST_ORDER) {
+        const float *Cu = a.C + (size_t)u * kD * kD;
+        const int row = tid >> 1, half = tid & 1;
+        float acc[G];
+#pragma unroll
+        for (int h = 0; h < G; h++) acc[h] = 0.f;
+        const float *cr = Cu + (size_t)row * kD + half * 64;
+        for (int j = 0; j < 64; j += 4) {
+            const float4 cv = *reinterpret_cast<const float4 *>(cr + j);
+#pragma unroll
+            for (int h = 0; h < G; h++) {
+                const float *qq = &qs[h][half * 64 + j];
+                acc[h] = fmaf(cv.x, qq[0], acc[h]);
+                acc[h] = fmaf(cv.y, qq[1], acc[h]);
+                acc[h] = fmaf(cv.z, qq[2], acc[h]);
+                acc[h] = fmaf(cv.w, qq[3], acc[h]);
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < G; h++) {
+            acc[h] += __shfl_xor_sync(kFull, acc[h], 1);
+            if (half == 0) cq[h][row] = acc[h] * rs;
+        }
+    } else {
+        for (int e = tid; e < G * kD; e += blockDim.x) cq[e / kD][e % kD] = 0.f;
+    }
+    __syncthreads();
+    for (int e = tid; e < G * kD; e += blockDim.x) {
+        const int h = e / kD, dd = e % kD;
+        const float fe = mv[dd] + cq[h][dd];
+        ou[e] = wR[h] * fR[h][dd] + (1.f - wR[h]) * fe;
+    }
+}
+
+template <int G>
+static cudaError_t launch_correct_g(const CorrArgs &a, int U, int cap, cudaStream_t st)
+{
+    const size_t smem = (size_t)((cap + 31) / 32) * 4;
+    if (smem > 16384) {
+        cudaError_t e = cudaFuncSetAttribute(correct_kernel<G>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    correct_kernel<G><<<U, 256, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_correct(const kvc_params &p, const uint16_t *q,
+                           const kvc_cache &c, int kmax,
+                           const int32_t *evict_idx, const int32_t *n_evict,
+                           const float *lse, const float *f_all,
+                           const kvc_moments &m, float *o, float *f_R,
+                           float *logZ_R, const DecodeWs &ws, cudaStream_t st)
+{
+    CorrArgs a{q, c.K, c.V, c.votes, c.len, evict_idx, n_evict, lse, f_all,
+               m.n, m.mu_k, m.mu_v, m.C, o, f_R, logZ_R, ws.status, p.cap, kmax, p.correction};
+    switch (p.G) {
+    case 1: return launch_correct_g<1>(a, p.U, p.cap, st);
+    case 2: return launch_correct_g<2>(a, p.U, p.cap, st);
+    case 4: return launch_correct_g<4>(a, p.U, p.cap, st);
+    case 8: return launch_correct_g<8>(a, p.U, p.cap, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+// ==================================================================== compact
+//
+// One CTA per unit.  With n2 = len - k, the r-th evicted slot below n2 (in
+// ascending order) receives the r-th live slot at or above n2.  Ranks come
+// from per-word prefix counts of an eviction bitmap; pairs are formed in
+// windows of kCompactWin ranks.
+
+struct CompactArgs {
+    uint16_t *K, *V;
+    int32_t *votes, *pos;
+    double *util;
+    int32_t *len;
+    const int32_t *evict_idx, *n_evict;
+    int32_t *status;
+    int cap, kmax;
+};
+
+constexpr int kCompactWin = 2048;
+
+__global__ void __launch_bounds__(512) compact_kernel(CompactArgs a)
+{
+    extern __shared__ uint32_t sm[];
+    __shared__ int src[kCompactWin], dst[kCompactWin];
+    __shared__ int scan[40];
+    __shared__ int okf;
+    const int u = blockIdx.x, tid = threadIdx.x;
+    const int k = a.n_evict[u];
+    if (k <= 0) return;
+    const int n = a.len[u];
+    if (k > a.kmax || k > n || !victims_ok(a.evict_idx + (size_t)u * a.kmax, k, n, a.cap, &okf)) {
+        if (tid == 0) record_status(a.status, KVC_ERR_INVALID_ARG);
+        return;
+    }
+    const int n2 = n - k;
+    const int words = (n + 31) >> 5;
+    uint32_t *bits = sm;
+    int *wpre = reinterpret_cast<int *>(sm + ((a.cap + 31) >> 5));
+    for (int i = tid; i < words; i += blockDim.x) bits[i] = 0;
+    __syncthreads();
+    const int32_t *ev = a.evict_idx + (size_t)u * a.kmax;
+    for (int e = tid; e < k; e += blockDim.x) {
+        const int s = ev[e];
+        atomicOr(&bits[s >> 5], 1u << (s & 31));
+    }
+    __syncthreads();
+    // exclusive prefix of popcounts over words
+    int carry = 0;
+    for (int b0 = 0; b0 < words; b0 += blockDim.x) {
+        const int i = b0 + tid;
+        const int v = i < words ? __popc(bits[i]) : 0;
+        int tot;
+        const int ex = block_exscan(v, scan, &tot);
+        if (i < words) wpre[i] = carry + ex;
+        carry += tot;
+    }
+    __syncthreads();
+    auto ev_below = [&](int i) {   // evicted slots in [0, i)
+        return wpre[i >> 5] + __popc(bits[i >> 5] & ((1u << (i & 31)) - 1u));
+    };
+    const int holes = (n2 > 0) ? ev_below(n2) : 0;
+    const int ev_n2 = holes;
+    const size_t ubase = (size_t)u * a.cap;
+    for (int r0 = 0; r0 < holes; r0 += kCompactWin) {
+        const int r1 = min(holes, r0 + kCompactWin);
+        for (int i = tid; i < n2; i += blockDim.x) {
+            if ((bits[i >> 5] >> (i & 31)) & 1u) {
+                const int r = ev_below(i);
+                if (r >= r0 && r < r1) dst[r - r0] = i;
+            }
+        }
+        for (int i = n2 + tid; i < n; i += blockDim.x) {
+            if (!((bits[i >> 5] >> (i & 31)) & 1u)) {
+                const int r = (i - n2) - (ev_below(i) - ev_n2);
+                if (r >= r0 && r < r1) src[r - r0] = i;
+            }
+        }
+        __syncthreads();
+        const int np = r1 - r0;
+        for (int e = tid; e < np * 32; e += blockDim.x) {
+            const int pr = e >> 5, ch = e & 31;
+            const size_t from = ubase + src[pr], to = ubase + dst[pr];
+            if (ch < 16)
+                reinterpret_cast<uint4 *>(a.K + to * kD)[ch] =
+                    reinterpret_cast<const uint4 *>(a.K + from * kD)[ch];
+            else
+                reinterpret_cast<uint4 *>(a.V + to * kD)[ch - 16] =
+                    reinterpret_cast<const uint4 *>(a.V + from * kD)[ch - 16];
+            if (ch == 0) {
+                a.pos[to] = a.pos[from];
+                a.util[to] = a.util[from];
+                if (a.votes) a.votes[to] = a.votes[from];
+            }
+        }
+        __syncthreads();
+    }
+    if (tid == 0) a.len[u] = n2;
+}
+
+cudaError_t launch_compact(const kvc_params &p, const kvc_cache &c, int kmax,
+                           const int32_t *evict_idx, const int32_t *n_evict,
+                           const DecodeWs &ws, cudaStream_t st)
+{
+    const size_t smem = (size_t)((p.cap + 31) / 32) * 8;
+    if (smem > 16384) {
+        cudaError_t e = cudaFuncSetAttribute(compact_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    CompactArgs a{c.K, c.V, c.votes, c.pos, c.util, c.len, evict_idx, n_evict,
+                  ws.status, p.cap, kmax};
+    compact_kernel<<<p.U, 512, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace kvc

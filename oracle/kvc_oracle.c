@@ -134,9 +134,10 @@ int ocl_load(void *h, int u, int n, const uint16_t *k, const uint16_t *v,
 
 /*
  * Append the new token of this decode step to every unit: its key and value,
- * vote 1, position new_pos, not yet scored.  [MomentKV Algorithm 1, steps
- * 1-2 "R <- R u {(k_new, v_new)}"; KeepKV Algorithm 1, decode steps 6a-6b
- * "add (k_t, v_t, p_t = 1)"].  Returns -1 if a unit is full.
+ * vote 1, position new_pos, not yet scored.  [MomentKV Algorithm 1: the
+ * new pair joins the retained set before eviction; KeepKV Algorithm 1,
+ * decoding stage: a new pair enters with vote 1].  Returns -1 if a unit is
+ * full.
  */
 int ocl_append(void *h, const uint16_t *knew, const uint16_t *vnew,
                int32_t new_pos)
@@ -320,9 +321,9 @@ int ocl_select(void *h, int L, int kmax, int32_t *victims, int32_t *nvict,
  * eviction-set sums with its vote as weight (a slot with vote p stands for
  * p identical tokens, KeepKV eq 6 "equivalent to p duplicated pairs"):
  *   n_e += p,  s_k += p k,  s_v += p v,  S += p v k^T
- * [MomentKV Algorithm 1 steps 11-13; App. A.1 "updated by plain addition"],
- * then the slot is removed, keeping the rest in position order [Algorithm 1
- * step 14].  Returns 0, or -1 if a position is not present.
+ * [MomentKV Algorithm 1, eviction phase; App. A.1 update by plain
+ * addition], then the slot is removed, keeping the rest in position order.
+ * Returns 0, or -1 if a position is not present.
  */
 int ocl_evict(void *h, const int32_t *victims, const int32_t *nvict, int kmax)
 {
@@ -399,21 +400,21 @@ void ocl_moments(void *h, double *n, double *mu_k, double *mu_v, double *C)
 }
 
 /*
- * Output of the decode step after eviction [MomentKV Algorithm 1 phase 2]:
+ * Output of the decode step after eviction [MomentKV Algorithm 1,
+ * normalization-corrected inference phase]:
  *   f_R, Z_R  = attention over the retained slots, computed directly
- *               (step 16; logZ_R = log Z_R with vote weights)
- *   n_e = 0 or correction off:  o = f_R                         (step 17)
+ *               (logZ_R = log Z_R with vote weights)
+ *   n_e = 0 or correction off:  o = f_R
  *   otherwise, from the raw sums:
  *     k_bar = s_k/n_e, v_bar = s_v/n_e, S_tilde = S - s_v s_k^T / n_e
  *     log Zhat_E = ln n_e + q . k_bar / sqrt(d)    Jensen lower bound
- *                                                 (step 18; sec 4.2 eq 10)
- *     fhat_E = v_bar + S_tilde q / (n_e sqrt(d))   first order   (step 19;
- *                                                 sec 4.1 eq 9)
+ *                                                 (sec 4.2 eq 10)
+ *     fhat_E = v_bar + S_tilde q / (n_e sqrt(d))   first order (sec 4.1 eq 9)
  *            = v_bar                               zero order (sec A4,
  *                                                 Table 4 zero-order variant)
  *     w_R = Z_R / (Z_R + Zhat_E) evaluated as 1 / (1 + exp(log Zhat_E -
- *           log Z_R)), the log-domain form of App. C.2          (step 20)
- *     o = w_R f_R + (1 - w_R) fhat_E                            (step 21)
+ *           log Z_R)), the log-domain form of App. C.2
+ *     o = w_R f_R + (1 - w_R) fhat_E                (sec 4.2 eq 12)
  * correction: 0 off, 1 zero order, 2 first order.
  * Outputs: o, f_R [U][G][d]; logZ_R [U][G]  (f_R / logZ_R may be NULL).
  */

@@ -232,12 +232,12 @@ def decode_step(sess: DecodeSession, t: int, new_pos: int, q, knew, vnew, *,
     """One decode step on every unit of ``sess``, in the order of MomentKV
     Algorithm 1 with the InertiaKV utility in place of its scoring:
 
-    1. append (k_new, v_new) with vote 1                       (Alg. 1 steps 1-2)
+    1. append (k_new, v_new) with vote 1
     2. vote-weighted attention over all slots -> lse, f_all, head-mean probs
     3. refresh step: utility update                 (InertiaKV sec 3.1 eqs 2-4)
     4. victims: the k = n - L lowest (utility, position) scored slots
-    5. fold victims into the moments and remove them            (steps 11-14)
-    6. retained attention + moment correction                   (steps 16-21)
+    5. fold victims into the moments and remove them  (eviction phase)
+    6. retained attention + moment correction         (inference phase)
 
     ``choose(t, proposal)``, if given, receives the oracle's proposal dict and
     returns the victim positions to apply ([U][kmax], [U]); tests use it to

@@ -1,0 +1,175 @@
+"""GPU-vs-oracle parity driver for the decode step (test helper).
+
+The CUDA path (through the C ABI) and the fp64 oracle run the same seeded
+inputs step by step.  Each step compares:
+
+* eviction sets, by token position: they must be equal, except that a token
+  in the symmetric difference is accepted when the oracle's utility for it is
+  within 1e-6 relative of the oracle's k-th (threshold) utility (a near-tie:
+  both choices are valid orders of equal-up-to-rounding utilities).  Accepted
+  near-tie choices are counted; the oracle then applies the GPU's set, which
+  is one of the valid sets, so one tie does not change every later step.
+  Any other difference is a mismatch (the test fails).
+* the corrected output o: max over units and heads of
+  ||o_gpu - o_ref||_inf / ||o_ref||_inf <= 2e-3;
+* the moments: ||d mu|| / ||mu|| and ||d C||_F / ||C||_F <= 1e-4 per unit
+  (absolute 1e-6 when the norm is below 1e-3), n exact;
+* the head-mean probabilities on refresh steps (by position), and with the
+  five-call path lse and f_all.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+import torch
+
+from kv_cache_eviction_kvc_gb300 import workloads as W
+from kv_cache_eviction_kvc_gb300.state import DecodeState
+from oracle import oracle as O
+
+TIE_REL = 1e-6
+O_TOL = 2e-3
+MOM_TOL = 1e-4
+PROB_TOL = 2e-3   # head-mean probabilities are attention outputs
+
+
+@dataclasses.dataclass
+class ParityReport:
+    steps: int = 0
+    band_hits: int = 0
+    mismatches: int = 0
+    max_o_err: float = 0.0
+    max_mu_err: float = 0.0
+    max_C_err: float = 0.0
+    max_prob_err: float = 0.0
+    max_lse_err: float = 0.0
+    max_fall_err: float = 0.0
+    n_err: int = 0
+    first_mismatch: str = ""
+
+    def ok(self):
+        return (self.mismatches == 0 and self.max_o_err <= O_TOL and self.max_mu_err <= MOM_TOL
+                and self.max_C_err <= MOM_TOL and self.max_prob_err <= PROB_TOL
+                and self.n_err == 0 and self.max_lse_err <= O_TOL and self.max_fall_err <= O_TOL)
+
+
+def _rel(a, b, floor=1e-3, absfloor=1e-6):
+    nb = np.linalg.norm(b)
+    d = np.linalg.norm(a - b)
+    return d / nb if nb >= floor else (0.0 if d <= absfloor else d / max(nb, 1e-30))
+
+
+def run_decode_parity(cfg: W.DecodeConfig, *, steps: int | None = None, units=None,
+                      fused: bool = True, seed: int = 0, device="cuda",
+                      cap: int | None = None) -> ParityReport:
+    S = cfg.steps if steps is None else steps
+    U, G, d, N, L = cfg.U, cfg.G, cfg.d, cfg.N, cfg.L
+    units = list(range(U)) if units is None else list(units)
+    uidx = torch.tensor(units, device=device, dtype=torch.long)
+    cap = max(N + 1, L + 1) if cap is None else cap
+    P = W.unit_params(cfg, device, seed)
+    pre = W.gen_prefill(cfg, device, seed, cap=cap, P=P)
+    st = DecodeState(U, G, cap, L, rule=cfg.rule, alpha=cfg.alpha, refresh_period=cfg.T,
+                     correction=cfg.correction, votes=bool(cfg.votes_max),
+                     kmax=max(1, N + 1 - L), device=device)
+    st.load_prefill(pre["K"], pre["V"], pre["votes"], pre["pos"], pre["len"])
+    sess = O.DecodeSession(len(units), G, d, cap + 1)
+    Kh = pre["K"][uidx, :N].cpu()
+    Vh = pre["V"][uidx, :N].cpu()
+    vh = None if pre["votes"] is None else pre["votes"][uidx, :N].cpu().numpy()
+    for j in range(len(units)):
+        sess.load(j, Kh[j], Vh[j], None if vh is None else vh[j], np.arange(N, dtype=np.int32))
+    del Kh, Vh, pre
+    rep = ParityReport()
+    try:
+        n_len = N
+        for t in range(1, S + 1):
+            inp = W.gen_step(cfg, device, t, seed, P)
+            new_pos = N + t - 1
+            max_len = n_len + 1
+            refresh = O.is_refresh(t, cfg.T)
+            pos_before = st.pos[uidx, :max_len].cpu().numpy().copy()
+            len_before = st.len[uidx].cpu().numpy().copy()
+            if fused:
+                st.step(t, new_pos, inp["q"], inp["k_new"], inp["v_new"], max_len)
+            else:
+                st.step_calls(t, new_pos, inp["q"], inp["k_new"], inp["v_new"], max_len)
+            torch.cuda.synchronize()
+            ds = st.device_status()
+            assert ds == 0, f"device status {ds} at step {t}"
+            nev = st.n_evict[uidx].cpu().numpy()
+            evp = st.evict_pos[uidx].cpu().numpy()
+            o_gpu = st.o[uidx].cpu().numpy().astype(np.float64)
+            probs_gpu = st.probs[uidx, :max_len].cpu().numpy() if refresh else None
+            if not fused:
+                lse_gpu = st.lse[uidx].cpu().numpy()
+                fall_gpu = st.f_all[uidx].cpu().numpy()
+
+            qh = inp["q"][uidx].cpu()
+            kh = inp["k_new"][uidx].cpu()
+            vh2 = inp["v_new"][uidx].cpu()
+
+            def choose(tt, prop):
+                nonlocal rep
+                n_o, pos_o, _, util_o, _ = sess.slots()
+                vic, nv, thr = prop["victims"], prop["nvict"], prop["thr"]
+                kmax = max(1, int(nev.max()), vic.shape[1])
+                out = np.full((len(units), kmax), -1, np.int32)
+                for j in range(len(units)):
+                    g = set(evp[j, : nev[j]].tolist())
+                    o_set = set(vic[j, : nv[j]].tolist())
+                    if g != o_set:
+                        umap = dict(zip(pos_o[j, : n_o[j]].tolist(), util_o[j, : n_o[j]].tolist()))
+                        bad = [p for p in g ^ o_set
+                               if p not in umap or abs(umap[p] - thr[j]) > TIE_REL * abs(thr[j])]
+                        if bad or len(g) != len(o_set):
+                            rep.mismatches += 1
+                            if not rep.first_mismatch:
+                                rep.first_mismatch = (f"step {tt} unit {units[j]}: gpu-only "
+                                                      f"{sorted(g - o_set)[:5]} oracle-only "
+                                                      f"{sorted(o_set - g)[:5]} thr {thr[j]!r}")
+                        else:
+                            rep.band_hits += 1
+                    gl = sorted(g)
+                    out[j, : len(gl)] = gl
+                return out, nev.astype(np.int32)
+
+            prop = O.decode_step(sess, t, new_pos, qh, kh, vh2, L=L, rule=cfg.rule,
+                                 alpha=cfg.alpha, T=cfg.T, correction=cfg.correction,
+                                 choose=choose)
+            # output
+            o_ref = prop["o"]
+            num = np.abs(o_gpu - o_ref).max(axis=2)
+            den = np.abs(o_ref).max(axis=2)
+            rep.max_o_err = max(rep.max_o_err, float((num / np.maximum(den, 1e-30)).max()))
+            if not fused:
+                rep.max_lse_err = max(rep.max_lse_err, float(np.abs(lse_gpu - prop["lse"]).max()))
+                fn = np.abs(fall_gpu - prop["f_all"]).max(axis=2)
+                fd = np.abs(prop["f_all"]).max(axis=2)
+                rep.max_fall_err = max(rep.max_fall_err, float((fn / np.maximum(fd, 1e-30)).max()))
+            if refresh:
+                pr = prop["probs"]
+                for j in range(len(units)):
+                    nb = int(len_before[j])
+                    gp = probs_gpu[j, : nb + 1]
+                    gpos = np.append(pos_before[j, :nb], new_pos)
+                    order = np.argsort(gpos)
+                    ref = pr[j, : nb + 1]          # oracle slots are in position order
+                    err = np.abs(gp[order] - ref) / np.maximum(ref, 1e-300)
+                    rep.max_prob_err = max(rep.max_prob_err, float(err.max()))
+            # moments
+            n_g = st.n[uidx].cpu().numpy()
+            mk_g = st.mu_k[uidx].cpu().numpy()
+            mv_g = st.mu_v[uidx].cpu().numpy()
+            C_g = st.C[uidx].cpu().numpy()
+            n_r, mk_r, mv_r, C_r = sess.moments()
+            rep.n_err += int((n_g != n_r).sum())
+            for j in range(len(units)):
+                rep.max_mu_err = max(rep.max_mu_err, _rel(mk_g[j], mk_r[j]), _rel(mv_g[j], mv_r[j]))
+                rep.max_C_err = max(rep.max_C_err, _rel(C_g[j], C_r[j]))
+            n_len = int(st.len.max().item())
+            rep.steps += 1
+    finally:
+        sess.close()
+    return rep

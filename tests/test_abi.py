@@ -1,0 +1,81 @@
+"""The C-ABI library builds for sm_103a, loads, exports every entry point the
+header declares, and rejects bad arguments on the host before touching a
+device (these calls need no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from kv_cache_eviction_kvc_gb300 import kvc as K
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "kvc.h")).read()
+    return re.findall(r"^KVC_API\s+[\w\s\*]+?\b(kvc_\w+)\s*\(", src, flags=re.M)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = K.load()
+    names = header_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(K.EXPORTED)
+
+
+def test_version_matches_header():
+    src = open(os.path.join(ROOT, "include", "kvc.h")).read()
+    v = int(re.search(r"#define KVC_VERSION (\d+)", src).group(1))
+    assert K.kvc_version() == v
+    assert K.kvc_status_string(0) == "KVC_OK"
+    assert K.kvc_status_string(6) == "KVC_ERR_WORKSPACE"
+
+
+def test_workspace_size_host_only():
+    p = K.make_params(U=4, G=4, cap=100, L=10)
+    n = K.kvc_decode_workspace_size(p)
+    # status + logits + split partials + lengths + queues + scratch
+    assert n >= 4 * 4 * 100 * 4 + 4 * 1 * 4 * 130 * 4
+    assert K.kvc_decode_workspace_size(K.make_params(U=4, G=3, cap=100, L=10)) == 0
+
+
+def _lib_call_attend(p, **kw):
+    lib = K.load()
+    cache = K.kvc_cache(*(kw.get(k, 16 * (i + 1)) for i, k in enumerate(["K", "V", "votes", "pos", "util", "len"])))
+    ws = kw.get("ws", 256)
+    return lib.kvc_decode_attend(ctypes.byref(p), kw.get("t", 1), 0, kw.get("max_len", 5),
+                                 16, 16, 16, ctypes.byref(cache), 16, 16, None,
+                                 ws, kw.get("ws_bytes", 1 << 40), None)
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("d", 64, 5), ("G", 3, 5), ("U", 0, 1), ("L", 0, 1), ("L", 100, 1),
+    ("refresh_period", 0, 1), ("refresh_period", 11, 1), ("rule", 7, 1),
+    ("alpha", 1.0, 1), ("correction", 3, 1), ("cap", 0, 5)])
+def test_bad_params_rejected_on_host(field, value, code):
+    p = K.make_params(U=2, G=4, cap=100, L=10)
+    setattr(p, field, value)
+    assert _lib_call_attend(p) == code
+    assert K.kvc_last_error() != ""
+
+
+def test_bad_buffers_rejected_on_host():
+    p = K.make_params(U=2, G=4, cap=100, L=10)
+    assert _lib_call_attend(p, K=None) == 1                 # null cache pointer
+    assert _lib_call_attend(p, K=18) == 1                   # misaligned K
+    assert _lib_call_attend(p, ws=None) == 6                # no workspace
+    assert _lib_call_attend(p, ws=128) == 6                 # misaligned workspace
+    assert _lib_call_attend(p, ws_bytes=16) == 6            # too small
+    assert _lib_call_attend(p, max_len=101) == 2            # beyond capacity
+    assert _lib_call_attend(p, t=0) == 1                    # steps are 1-based
+    assert "workspace" in K.kvc_last_error() or "t =" in K.kvc_last_error()
+
+
+def test_binding_refuses_host_tensors():
+    import torch
+    p = K.make_params(U=1, G=4, cap=8, L=4)
+    with pytest.raises(ValueError):
+        K.kvc_decode_workspace_init(p, torch.zeros(16, dtype=torch.uint8))

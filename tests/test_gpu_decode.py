@@ -1,0 +1,76 @@
+"""GPU parity of the decode step (through the C ABI) against the fp64 oracle
+on the seeded workloads: the small configurations in full, the large ones on
+64 sampled units at full size and every step, plus edge cases."""
+import numpy as np
+import pytest
+import torch
+
+from kv_cache_eviction_kvc_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from parity import run_decode_parity  # noqa: E402
+
+
+def sample_units(U, n=64, seed=0):
+    rng = np.random.default_rng(seed)
+    rest = rng.choice(np.arange(1, U - 1), size=n - 2, replace=False)
+    return sorted({0, U - 1, *rest.tolist()})
+
+
+def check(rep):
+    print(rep)
+    assert rep.ok(), rep
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_c0_full(fused):
+    check(run_decode_parity(W.C0, fused=fused))
+
+
+def test_c1_full():
+    check(run_decode_parity(W.C1))
+
+
+def test_c2_sampled_full_size():
+    check(run_decode_parity(W.C2, units=sample_units(W.C2.U)))
+
+
+def test_c4_sampled_full_size():
+    check(run_decode_parity(W.C4, units=sample_units(W.C4.U)))
+
+
+SMALL = W.C0.with_(name="small", N=700, L=50, steps=24)
+
+
+@pytest.mark.parametrize("cfg", [
+    SMALL,                                                           # ragged chunk tail
+    SMALL.with_(votes_max=8, rule=W.RULE_CUMULATIVE),
+    SMALL.with_(rule=W.RULE_SINGLE, T=4),
+    SMALL.with_(T=50, correction=W.CORR_ZERO_ORDER),                 # T = L
+    SMALL.with_(correction=W.CORR_OFF, k_dist="mixture", centres=8),
+    SMALL.with_(Hq=2, Hkv=2, N=300, L=20),                           # G = 1
+    SMALL.with_(Hq=4, Hkv=2, N=129, L=128, steps=6),                 # k = 2 at step 1
+    SMALL.with_(Hq=16, Hkv=2, B=2, N=513, L=17, votes_max=3),        # G = 8
+    SMALL.with_(N=40, L=64, steps=30),                               # no eviction at first
+], ids=["ragged", "votes-cumulative", "single-lazy", "T=L-zero-order", "corr-off",
+        "G1", "k2", "G8-votes", "under-budget"])
+@pytest.mark.parametrize("fused", [True, False])
+def test_edge_cases(cfg, fused):
+    check(run_decode_parity(cfg, fused=fused))
+
+
+def test_device_status_reports_overlong_unit():
+    from kv_cache_eviction_kvc_gb300.state import DecodeState
+    cfg = SMALL
+    st = DecodeState(2, 4, 80, 50, kmax=4)
+    st.len.fill_(60)
+    inp = W.gen_step(cfg, "cuda", 1)
+    st.step(1, 60, inp["q"], inp["k_new"], inp["v_new"], max_len=55)   # 61 > 55
+    torch.cuda.synchronize()
+    assert st.device_status() == 2          # KVC_ERR_SHAPE recorded, nothing done
+    assert st.len.tolist() == [60, 60]
+    assert st.device_status() == 0          # reading clears it

@@ -287,7 +287,8 @@ def _corrected_vs_full(k, v, p, q, E, correction):
 
 
 def test_correction_off_and_empty_moments_give_renormalized_output():
-    """Correction off, or n_e = 0, returns f_R (MomentKV Alg. 1 step 17)."""
+    """Correction off, or n_e = 0, returns f_R (MomentKV Algorithm 1: no
+    evicted token yet means plain retained attention)."""
     rng = np.random.default_rng(8)
     n, d, G = 20, 16, 2
     k, v = bf(rng.normal(size=(n, d))), bf(rng.normal(size=(n, d)))
