@@ -1,0 +1,367 @@
+"""Benchmark of the budgeted-KV decode step on GB300.
+
+Workload (default): the Qwen3-4B attention shape -- batch 16, 36 layers, 32
+query / 8 KV heads (4608 units), d = 128, prefill N = 32768, budget L = 3277
+slots per KV head, EMA utility (alpha 0.9) refreshed every 8 steps, moment
+correction on, fp32 moments.  Step 1 (the one-off pass over N + 1 slots that
+evicts down to L) runs untimed-for-the-metric and is reported separately; a
+timed step is one steady-state decode step over every unit (append, attention,
+head-mean scores, utility refresh on refresh steps, eviction, moment fold,
+correction, compaction), i.e. one call of kvc_decode_step.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle
+instead (a bounded sample of the same workload on the host cores).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode steps/sec and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+UNIT = "steps/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="C2")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------ byte model
+def step_bytes(cfg, refresh: bool, emit_probs: bool) -> int:
+    """Algorithmic HBM bytes of one steady-state step over every unit.
+
+    Per unit: K and V rows of the L slots (the victim's row is read once for
+    the moment fold, the new token's row is written), q, k_new, v_new, o, the
+    moments (C read + written, means, count), votes when present; on refresh
+    steps the utilities (read + written, fp64), positions and the emitted
+    fp64 probabilities.
+    """
+    d, G, L = cfg.d, cfg.G, cfg.L
+    b = 2 * L * d * 2                 # K, V rows read
+    b += 2 * d * 2                    # k_new, v_new read
+    b += 2 * d * 2                    # new token written into the victim slot
+    b += G * d * 2                    # q
+    b += G * d * 4                    # o
+    b += 2 * (d * d * 4) + 4 * d * 4 + 8   # C r/w, mu_k / mu_v r/w, n
+    b += 16                           # pos / votes / util of the new slot, counts
+    if cfg.votes_max:
+        b += L * 4
+    if refresh:
+        b += (L + 1) * 8 * 2 + L * 4  # util r/w, positions
+        if emit_probs:
+            b += (L + 1) * 8
+    return b * cfg.U
+
+
+# ------------------------------------------------------------ clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="kvc_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------ CPU oracle
+def oracle_sample(cfg, seconds: float, max_steps: int | None = None):
+    """Time the fp64 oracle on a bounded sample of the steady-state workload:
+    Us units whose cache holds L slots, stepping through refresh and lazy
+    steps.  Returns (steps/s extrapolated to all units, cores, sample text,
+    per-step times)."""
+    import numpy as np
+    import torch
+    from kv_cache_eviction_kvc_gb300 import workloads as W
+    from oracle import oracle as O
+    cores = len(os.sched_getaffinity(0))
+    Us = max(cores, 16)
+    small = cfg.with_(B=1, NL=1, Hkv=Us, Hq=Us * cfg.G, N=cfg.L)
+    P = W.unit_params(small, "cpu", 0)
+    pre = W.gen_prefill(small, "cpu", 0, cap=cfg.L + 1, P=P)
+    sess = O.DecodeSession(Us, cfg.G, cfg.d, cfg.L + 64)
+    for u in range(Us):
+        sess.load(u, pre["K"][u, : cfg.L], pre["V"][u, : cfg.L],
+                  None if pre["votes"] is None else pre["votes"][u, : cfg.L].numpy())
+    times = []
+    t = 0
+    t_start = time.perf_counter()
+    while True:
+        t += 1
+        inp = W.gen_step(small, "cpu", t, 0, P)
+        t0 = time.perf_counter()
+        O.decode_step(sess, t, cfg.L + t - 1, inp["q"], inp["k_new"], inp["v_new"], L=cfg.L,
+                      rule=cfg.rule, alpha=cfg.alpha, T=cfg.T, correction=cfg.correction)
+        times.append(time.perf_counter() - t0)
+        if max_steps is not None and t >= max_steps:
+            break
+        if max_steps is None and (time.perf_counter() - t_start > seconds or t >= 40):
+            break
+    sess.close()
+    per_unit_step = sum(times) / (len(times) * Us)
+    rate = 1.0 / (per_unit_step * cfg.U)
+    sample = (f"{Us} units x {len(times)} steady-state steps of this workload (L={cfg.L}, "
+              f"T={cfg.T}) on the fp64 oracle, OpenMP over units; steps/s scaled by "
+              f"{Us}/{cfg.U} units")
+    return rate, cores, sample, times
+
+
+# ------------------------------------------------------------ GPU arm
+def run_ours(args, cfg, rank, world):
+    import torch
+    from kv_cache_eviction_kvc_gb300 import kvc, workloads as W
+    from kv_cache_eviction_kvc_gb300.state import DecodeState
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    kvc.load()
+    seed = rank
+    U, G, N, L = cfg.U, cfg.G, cfg.N, cfg.L
+    P = W.unit_params(cfg, dev, seed)
+    st = DecodeState(U, G, N + 1, L, rule=cfg.rule, alpha=cfg.alpha, refresh_period=cfg.T,
+                     correction=cfg.correction, votes=bool(cfg.votes_max), kmax=N + 1 - L,
+                     device=dev)
+    pre = W.gen_prefill(cfg, dev, seed, cap=N + 1, P=P)
+    st.load_prefill(pre["K"], pre["V"], pre["votes"], pre["pos"], pre["len"])
+    del pre
+    torch.cuda.empty_cache()
+    stream = torch.cuda.current_stream(dev)
+
+    # step 1: the one-off pass over N + 1 slots (general five-kernel path)
+    inp = W.gen_step(cfg, dev, 1, seed, P)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    st.step(1, N, inp["q"], inp["k_new"], inp["v_new"], max_len=N + 1)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    step1_ms = e0.elapsed_time(e1)
+    assert st.device_status() == 0
+    st.set_kmax(1)
+
+    total = args.warmup + args.steps
+    inputs = [W.gen_step(cfg, dev, 2 + i, seed, P) for i in range(total)]
+    torch.cuda.synchronize()
+    launches = 0
+
+    def do_step(i, events=None):
+        nonlocal launches
+        t = 2 + i
+        x = inputs[i]
+        if events is not None:
+            events[0].record(stream)
+        st.step(t, N + t - 1, x["q"], x["k_new"], x["v_new"], max_len=L + 1)
+        if events is not None:
+            events[1].record(stream)
+        launches += 1
+
+    for i in range(args.warmup):
+        do_step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    launches = 0
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for k in range(args.steps):
+        do_step(args.warmup + k, ev[k])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    per_launch = [a.elapsed_time(b) for a, b in ev]
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    assert st.device_status() == 0
+
+    # algorithmic bytes of the timed launches (refresh pattern of steps 2 + i)
+    def is_refresh(t, T):      # utilities refresh on t = 1 and every T-th step after
+        return T <= 1 or (t - 1) % T == 0
+    steps_t = [2 + args.warmup + k for k in range(args.steps)]
+    bytes_list = [step_bytes(cfg, is_refresh(t, cfg.T), True) for t in steps_t]
+    avg_bytes = sum(bytes_list) / len(bytes_list)
+    avg_launch_ms = sum(per_launch) / len(per_launch)
+    achieved = avg_bytes / (avg_launch_ms * 1e-3) / 1e9
+
+    # end to end through host buffers: H2D of the step inputs, D2H of o
+    e2e = None
+    if not args.no_e2e:
+        nE = min(args.steps, 100)
+        host_in = [{k: v.cpu().pin_memory() for k, v in inputs[args.warmup + k].items()}
+                   for k in range(nE)]
+        dq = torch.empty_like(inputs[0]["q"])
+        dk = torch.empty_like(inputs[0]["k_new"])
+        dv = torch.empty_like(inputs[0]["v_new"])
+        o_host = torch.empty(st.o.shape, dtype=st.o.dtype).pin_memory()
+        base_t = 2 + total
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for k in range(nE):
+            h = host_in[k]
+            dq.copy_(h["q"], non_blocking=True)
+            dk.copy_(h["k_new"], non_blocking=True)
+            dv.copy_(h["v_new"], non_blocking=True)
+            t = base_t + k
+            st.step(t, N + t - 1, dq, dk, dv, max_len=L + 1)
+            o_host.copy_(st.o, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(b) / nE
+        bi = sum(v.numel() * v.element_size() for v in host_in[0].values())
+        bo = o_host.numel() * o_host.element_size()
+        e2e = {"value": world * 1000.0 / e2e_ms, "unit": UNIT, "h2d_bytes_per_step": bi,
+               "d2h_bytes_per_step": bo, "steps": nE}
+        assert st.device_status() == 0
+
+    peak, peak_kind = peaks()
+    ms_per_step = total_ms / args.steps
+    value = world * args.steps / (total_ms * 1e-3)
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 K/V/q, fp32 accumulate and moments, fp64 utilities",
+        "data": "synthetic (seeded K/V 64-centre mixtures; no model weights)",
+        "config": {"workload": cfg.name, "description": cfg.description, "units": cfg.U,
+                   "budget_L": L, "prefill_N": N, "refresh_period": cfg.T,
+                   "alpha": cfg.alpha, "parallelism": f"replicas x{world} (independent units)",
+                   "l2": "inputs larger than L2: %.2f GB of HBM traffic per step" % (avg_bytes / 1e9)},
+        "achieved_gbs": achieved,
+        "hbm_frac": achieved / peak,
+        "step1_ms": step1_ms,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_kind": peak_kind,
+                     "kernel": "fused_step_kernel (kvc_decode_step, steady state)",
+                     "bytes_per_launch": avg_bytes, "avg_launch_ms": avg_launch_ms},
+        "clocks": clocks,
+        "gpu_launches": launches,
+        "e2e": e2e,
+    }
+    return res
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    from kv_cache_eviction_kvc_gb300 import workloads as W
+    cfg = W.DECODE_CONFIGS[args.config]
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        rate_steps = []
+        cores = len(os.sched_getaffinity(0))
+        budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
+        rate, cores, sample, times = oracle_sample(cfg, budget, max_steps=args.warmup + args.steps + 1)
+        times = times[1 + args.warmup:] or times
+        Us = max(cores, 16)
+        per = sum(times) / len(times)
+        value = 1.0 / (per / Us * cfg.U)
+        res = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+               "steps": len(times), "warmup": args.warmup, "ms_per_step": 1e3 / value,
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+               "dtype": "f64", "data": "synthetic",
+               "config": {"workload": cfg.name, "description": cfg.description},
+               "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": sample},
+               "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                       "d2h_bytes_per_step": 0}}
+        print(json.dumps(res))
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    res = run_ours(args, cfg, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            rate, cores, sample, _ = oracle_sample(cfg, args.cpu_seconds)
+            res["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                   "sample": sample}
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

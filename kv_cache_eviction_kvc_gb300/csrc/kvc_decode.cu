@@ -343,7 +343,7 @@ struct AggArgs {
     const double *probs;
     double *util;
     const int32_t *pos, *len;
-    int32_t *evict_idx, *evict_pos, *n_evict, *status;
+    int32_t *evict_idx, *evict_pos, *n_evict, *status, *pend;
     int cap, L, rule, refresh, kmax;
     float alpha;
 };
@@ -398,6 +398,7 @@ __global__ void __launch_bounds__(512) aggregate_kernel(AggArgs a)
         return;
     }
     if (a.refresh) {
+        if (tid == 0) a.pend[(size_t)u * kPendStride] = 0;   // fused-step queue now stale
         const double *pr = a.probs + (size_t)u * a.cap;
         const double al = (double)a.alpha;
         for (int i = tid; i < n; i += blockDim.x) {
@@ -466,7 +467,7 @@ cudaError_t launch_aggregate(const kvc_params &p, int t, const double *probs,
                              const DecodeWs &ws, cudaStream_t st)
 {
     AggArgs a{probs, c.util, c.pos, c.len, evict_idx, evict_pos, n_evict,
-              ws.status, p.cap, p.L, p.rule, is_refresh(t, p.refresh_period),
+              ws.status, ws.pend, p.cap, p.L, p.rule, is_refresh(t, p.refresh_period),
               kmax, p.alpha};
     aggregate_kernel<<<p.U, 512, 0, st>>>(a);
     return cudaGetLastError();

@@ -14,7 +14,7 @@ constexpr int kProbsChunk = 4096;     // slots per CTA of the probability pass
 constexpr int kMaxCap = 1 << 19;      // largest supported slot capacity
 constexpr size_t kAlign = 256;
 
-inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+__host__ __device__ inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 // Carve-up of a decode workspace (all offsets 256-byte aligned).
 struct DecodeWs {
