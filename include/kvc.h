@@ -295,6 +295,37 @@ KVC_API kvc_status kvc_decode_step(const kvc_params *p, int32_t t, int32_t new_p
                            int32_t *n_evict, void *ws, size_t ws_bytes,
                            void *stream);
 
+/*
+ * kvc_decode_attend_noalloc -- kvc_decode_attend for callers that cannot
+ * allocate device memory.  The pages have no counterpart to this entry
+ * point; it exists for hosts that own every device allocation (a serving
+ * runtime that reserves its memory pool at start-up and allows no cudaMalloc
+ * afterwards, a plugin interface that passes tensors but no workspace).
+ *
+ * Same arguments, arithmetic and outputs as kvc_decode_attend, without the
+ * workspace: the scratch (status word, logits, split partials, lengths) lives
+ * in a static device array of 32 MiB inside the library, which every GPU that
+ * loads the library holds until the process exits.  The call allocates
+ * nothing (no cudaMalloc, cudaFree or allocating library routine).
+ * - Sizes whose scratch exceeds 32 MiB (about U*G*cap*4 + U*ceil(cap/512)*
+ *   G*520 bytes) are rejected with KVC_ERR_WORKSPACE and a message.
+ * - The first call on a device resolves the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ * - Every call on a device shares the one array and it keeps the previous
+ *   call's contents: calls whose kernels overlap on the GPU race and must be
+ *   ordered by the caller.
+ * - device_status (optional device pointer to one int32) receives the device
+ *   status of this call (KVC_OK or the KVC_ERR_* a kernel recorded).
+ */
+KVC_API kvc_status kvc_decode_attend_noalloc(const kvc_params *p, int32_t t,
+                                             int32_t new_pos, int32_t max_len,
+                                             const uint16_t *q, const uint16_t *k_new,
+                                             const uint16_t *v_new,
+                                             const kvc_cache *cache, float *lse,
+                                             float *f_all, double *probs,
+                                             int32_t *device_status, void *stream);
+
 /* ------------------------------------------------------------------ */
 /* prefill scorer                                                       */
 /* ------------------------------------------------------------------ */

@@ -27,7 +27,7 @@ EXPORTED = (
     "kvc_version", "kvc_last_error", "kvc_status_string",
     "kvc_decode_workspace_size", "kvc_decode_workspace_init", "kvc_get_device_status",
     "kvc_decode_attend", "kvc_aggregate_evict", "kvc_moment_update", "kvc_correct",
-    "kvc_compact", "kvc_decode_step", "kvc_prefill_prepare",
+    "kvc_compact", "kvc_decode_step", "kvc_decode_attend_noalloc", "kvc_prefill_prepare",
     "kvc_prefill_workspace_size", "kvc_prefill_score",
 )
 
@@ -88,6 +88,7 @@ def load(build: bool = True):
         "kvc_correct": (I32, [PP, P, PC, I32, P, P, P, P, PM, P, P, P, P, SZ, P]),
         "kvc_compact": (I32, [PP, PC, I32, P, P, P, SZ, P]),
         "kvc_decode_step": (I32, [PP, I32, I32, I32, P, P, P, PC, PM, P, P, I32, P, P, P, P, SZ, P]),
+        "kvc_decode_attend_noalloc": (I32, [PP, I32, I32, I32, P, P, P, PC, P, P, P, P, P]),
         "kvc_prefill_prepare": (I32, [I32, I32, I32, I32, I32, P, P, P]),
         "kvc_prefill_workspace_size": (SZ, [I32, I32, I32, I64]),
         "kvc_prefill_score": (I32, [I32, I32, I32, I32, I32, I32, I64, I32, P, P, P, P, P, P,
@@ -239,6 +240,19 @@ def kvc_decode_step(p, t, new_pos, max_len, q, k_new, v_new, cache: kvc_cache,
         _ptr(evict_idx, i32, "evict_idx", optional=True),
         _ptr(evict_pos, i32, "evict_pos", optional=True), _ptr(n_evict, i32, "n_evict"),
         _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
+
+
+def kvc_decode_attend_noalloc(p, t, new_pos, max_len, q, k_new, v_new, cache: kvc_cache, lse,
+                              f_all, probs, device_status=None, stream=None):
+    """kvc_decode_attend without a workspace, for callers that cannot allocate
+    device memory: the scratch is a 32 MiB static array inside the library."""
+    bf = torch.bfloat16
+    _check(load().kvc_decode_attend_noalloc(
+        ctypes.byref(p), int(t), int(new_pos), int(max_len), _ptr(q, bf, "q"),
+        _ptr(k_new, bf, "k_new"), _ptr(v_new, bf, "v_new"), ctypes.byref(cache),
+        _ptr(lse, torch.float32, "lse"), _ptr(f_all, torch.float32, "f_all"),
+        _ptr(probs, torch.float64, "probs", optional=True),
+        _ptr(device_status, torch.int32, "device_status", optional=True), _stream(stream)))
 
 
 # ------------------------------------------------------------------ prefill
