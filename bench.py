@@ -41,6 +41,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the sequence count (smaller case for profiling)")
+    ap.add_argument("--prefill", type=int, default=None,
+                    help="override the prefill length N (smaller case for profiling)")
     return ap.parse_args()
 
 
@@ -325,6 +329,10 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", 1))
     from kv_cache_eviction_kvc_gb300 import workloads as W
     cfg = W.DECODE_CONFIGS[args.config]
+    if args.batch is not None:
+        cfg = cfg.with_(B=args.batch, name=cfg.name + f"-b{args.batch}")
+    if args.prefill is not None:
+        cfg = cfg.with_(N=args.prefill, name=cfg.name + f"-n{args.prefill}")
     if args.impl == "reference":
         if rank != 0:
             return

@@ -25,7 +25,12 @@
 // update of the mean / covariance form), and the normalization correction of
 // MomentKV sec 4.2 eq 12 (with eq 9 and App. C.2) gives the output.
 #include <cooperative_groups.h>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <math.h>
+#include <mutex>
+
+#include <cuda_bf16.h>
 
 #include "kvc_common.cuh"
 #include "kvc_internal.h"
@@ -37,6 +42,141 @@ namespace kvc {
 constexpr int kFusedMaxChunk = 4096;   // slots per CTA
 constexpr int kFusedMaxCS = 8;         // CTAs per cluster
 constexpr int kMaxQueue = kPendStride - 2;
+constexpr int kNC = 4;                 // consumer warps
+constexpr int kWarps = kNC + 1;        // + one producer warp
+constexpr int kThreads = kWarps * 32;
+constexpr int kTile = 64;              // slots per ring stage: 16 per consumer warp
+constexpr int kBoxBytes = kTile * 128; // one box: 64 rows x 64 bf16, 128B-swizzled
+constexpr int kTileBytes = 2 * kBoxBytes;
+constexpr int kStages = 4;
+constexpr long long kWaitCycles = 4000000000ll;   // ~2 s: a wait that long means a fault
+
+// ---------------------------------------------------------------- TMA ring
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *b)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *b, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of the given parity to complete; false after ~2 s
+// (the caller then records KVC_ERR_TIMEOUT instead of waiting forever).
+__device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity)
+{
+    if (mbar_try_wait(b, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(b, parity))
+        if (clock64() - t0 > kWaitCycles) return false;
+    return true;
+}
+
+// One bulk copy global -> this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void consumer_sync()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(kNC * 32) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds_v4(const void *p)
+{
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(smem_u32(p)));
+    return r;
+}
+
+// 2D tile copy (box of 64 columns x 64 rows) described by a tensor map.
+__device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                      uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Byte offset of 16-byte chunk j (0..15) of row r (0..63) in a stage: the
+// row's two 128-byte halves live in two boxes; inside a box the chunk index
+// is XOR-ed with the row index mod 8 (the TMA 128-byte swizzle), which makes
+// the 8-row ldmatrix reads below conflict-free.
+__device__ __forceinline__ uint32_t sw_off(int r, int j)
+{
+    return (uint32_t)(((j >> 3) * kBoxBytes) + (r << 7) + ((((j & 7) ^ (r & 7))) << 4));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                          uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+// D += A (16x16 bf16, row) * B (16x8 bf16, col), fp32 accumulate
+__device__ __forceinline__ void mma16816(float *d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// round-to-nearest bf16 of x and of the remainder x - hi (so hi + lo keeps
+// about 16 significant bits)
+__device__ __forceinline__ void split_bf16(float x, uint16_t &hi, uint16_t &lo)
+{
+    const __nv_bfloat16 h = __float2bfloat16_rn(x);
+    const __nv_bfloat16 l = __float2bfloat16_rn(x - __bfloat162float(h));
+    hi = __bfloat16_as_ushort(h);
+    lo = __bfloat16_as_ushort(l);
+}
 
 struct FusedArgs {
     const uint16_t *q, *k_new, *v_new;
@@ -75,8 +215,10 @@ __device__ __forceinline__ Cand shfl_cand(const Cand &c, int m)
 
 template <int G>
 struct FusedSmem {
+    uint64_t full[kStages];     // ring: stage filled (producer -> consumers)
+    uint64_t empty[kStages];    // ring: stage drained (consumers -> producer)
     float qs[G][kD];            // q / sqrt(d), fp32
-    float red[8][G];
+    float red[kWarps][G];
     float pM[G], pl[G];         // this CTA's partial max / sum
     float po[G][kD];            // this CTA's partial unnormalized output
     float gM[G], gl[G];         // merged
@@ -99,14 +241,67 @@ struct FusedSmem {
     double vm;                  // utility of the new token (refresh, last CTA)
     Cand cand[kMaxQueue];
     int ncand;
-    Cand bc[8];
+    Cand bc[kWarps];
     int victim;                 // slot index of the victim (L = the new token)
     int qvalid;
     int direct;
+    int bad;                    // a ring wait timed out
 };
 
+// Stream the rows of this CTA's slots (8 lanes per row, lane c holding the
+// 16-byte chunks c and 8 + c), keeping kPrefetch iterations of loads in
+// flight per warp so that enough bytes are outstanding to cover HBM latency.
+// body(li, i, isnew, ok, r0, r1) consumes one row; the new token (virtual
+// slot L, or the victim's slot on a lazy step) is read from `newrow`.
+constexpr int kPrefetch = 3;
+
+template <typename Body>
+__device__ __forceinline__ void stream_rows(const uint16_t *rows, const uint16_t *newrow, int s0,
+                                            int nloc, int L, int victim, int w, int nw, int grp,
+                                            int c, Body body)
+{
+    const int first = w * 4, stride = nw * 4;
+    const int niter = nloc > first ? (nloc - first + stride - 1) / stride : 0;   // uniform per warp
+    uint4 rb[kPrefetch][2];
+    auto issue = [&](int it, uint4 *dst) {
+        const int li = first + it * stride + grp;
+        const int i = s0 + li;
+        if (it < niter && li < nloc) {
+            const bool isnew = (i == L || i == victim);
+            if (isnew) {
+                dst[0] = *reinterpret_cast<const uint4 *>(newrow + 8 * c);
+                dst[1] = *reinterpret_cast<const uint4 *>(newrow + 64 + 8 * c);
+            } else {
+                const uint16_t *r = rows + (size_t)i * kD;
+                dst[0] = ldg_nc_v4(r + 8 * c);
+                dst[1] = ldg_nc_v4(r + 64 + 8 * c);
+            }
+        } else {
+            dst[0] = make_uint4(0, 0, 0, 0);
+            dst[1] = make_uint4(0, 0, 0, 0);
+        }
+    };
+#pragma unroll
+    for (int p = 0; p < kPrefetch; p++) issue(p, rb[p]);
+    for (int it = 0; it < niter; it += kPrefetch) {
+#pragma unroll
+        for (int p = 0; p < kPrefetch; p++) {
+            if (it + p < niter) {
+                const uint4 c0 = rb[p][0], c1 = rb[p][1];
+                issue(it + p + kPrefetch, rb[p]);
+                const int li = first + (it + p) * stride + grp;
+                const int i = s0 + li;
+                const bool ok = li < nloc;
+                body(li, i, ok && (i == L || i == victim), ok, c0, c1);
+            }
+        }
+    }
+}
+
 template <int G>
-__global__ void __launch_bounds__(256, 2) fused_step_kernel(FusedArgs a)
+__global__ void __launch_bounds__(kThreads, 2)
+fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV)
 {
     cg::cluster_group cluster = cg::this_cluster();
     const int CS = (int)cluster.num_blocks();
@@ -116,13 +311,16 @@ __global__ void __launch_bounds__(256, 2) fused_step_kernel(FusedArgs a)
     const int grp = lane >> 3, c = lane & 7;
 
     __shared__ FusedSmem<G> S;
-    extern __shared__ __align__(16) unsigned char dyn[];
+    extern __shared__ __align__(128) unsigned char dyn[];
     const int ch = a.chunk;
-    float *xsb = reinterpret_cast<float *>(dyn);                       // [G][ch + 1]
-    double *msm = reinterpret_cast<double *>(dyn + align_up((size_t)G * (ch + 1) * 4));
-    int32_t *possm = reinterpret_cast<int32_t *>(reinterpret_cast<unsigned char *>(msm) +
-                                                  align_up((size_t)(ch + 1) * 8));
-    unsigned char *chosen = reinterpret_cast<unsigned char *>(possm) + align_up((size_t)(ch + 1) * 4);
+    // [ring: kStages x 8 KB][logits G x (ch + 1)]; the refresh-step selection
+    // arrays reuse the ring once both passes have drained it
+    unsigned char *ring = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(dyn) + 1023) & ~uintptr_t(1023));       // swizzle atoms
+    float *xsb = reinterpret_cast<float *>(ring + (size_t)kStages * kTileBytes);   // [G][ch + 1]
+    double *msm = reinterpret_cast<double *>(ring);
+    int32_t *possm = reinterpret_cast<int32_t *>(ring + align_up((size_t)(ch + 1) * 8));
+    unsigned char *chosen = ring + align_up((size_t)(ch + 1) * 8) + align_up((size_t)(ch + 1) * 4);
     auto XS = [&](int h, int li) -> float & { return xsb[h * (ch + 1) + li]; };
 
     const int L = a.L;
@@ -151,7 +349,14 @@ __global__ void __launch_bounds__(256, 2) fused_step_kernel(FusedArgs a)
         S.mk0[e] = a.mu_k[(size_t)u * kD + e];
         S.mv0[e] = a.mu_v[(size_t)u * kD + e];
     }
-    if (tid == 0) { S.qvalid = 0; S.direct = 0; S.ncand = 0; S.n0 = a.mn[u]; }
+    if (tid == 0) {
+        S.qvalid = 0; S.direct = 0; S.ncand = 0; S.bad = 0; S.n0 = a.mn[u];
+        for (int j = 0; j < kStages; j++) {
+            mbar_init(&S.full[j], 1);
+            mbar_init(&S.empty[j], kNC);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
     __syncthreads();
 
     // ------------------------------------------------ victim (non-refresh)
@@ -182,7 +387,7 @@ __global__ void __launch_bounds__(256, 2) fused_step_kernel(FusedArgs a)
             __syncthreads();
             if (tid == 0) {
                 Cand b = S.bc[0];
-                for (int j = 1; j < 8; j++)
+                for (int j = 1; j < kWarps; j++)
                     if (cand_less(S.bc[j], b)) b = S.bc[j];
                 S.cand[0] = b;
                 S.ncand = b.slot >= 0 ? 1 : 0;
@@ -218,119 +423,282 @@ __global__ void __launch_bounds__(256, 2) fused_step_kernel(FusedArgs a)
         }
     }
 
-    // ------------------------------------------------ pass 1: logits
-    float qf[G][16];
+    // ------------------------------------------------ passes 1 and 2 over the ring
+    // The producer warp streams the K rows of [s0, s1), then the V rows, in
+    // 64-slot tiles (two 128B-swizzled TMA boxes each) through the ring.  A
+    // consumer warp owns 16 slots of a tile.  Pass 1: S = q K^T on tensor
+    // cores (m16n8k16, the G query heads in rows 0..G-1 of A, exact bf16
+    // products, fp32 accumulate); logits go to shared memory and the CTA max
+    // is fixed.  Pass 2: O += P V with P = exp(x - max) split into bf16
+    // hi + lo halves (two MMAs), so no online rescaling is needed.
+    const uint16_t *Vu = a.V + ubase * kD;
+    const int nrows = s1 - s0;
+    const int ntile = (nrows + kTile - 1) / kTile;
+    const int gq = lane >> 2, tq = lane & 3;        // mma fragment coordinates
+    const uint32_t ring_s = smem_u32(ring);
+    float O[16][4];
+    float lsq = 0.f;                                 // sum of p for head gq (this lane's slots)
 #pragma unroll
-    for (int h = 0; h < G; h++)
-#pragma unroll
-        for (int j = 0; j < 8; j++) {
-            qf[h][j] = S.qs[h][8 * c + j];
-            qf[h][8 + j] = S.qs[h][64 + 8 * c + j];
-        }
-    float mx[G];
-#pragma unroll
-    for (int h = 0; h < G; h++) mx[h] = -INFINITY;
-    for (int base = w * 4; base < nloc; base += 32) {
-        const int li = base + grp;
-        const bool ok = li < nloc;
-        const int i = s0 + li;                              // == L for the virtual slot
-        const bool isnew = ok && (i == L || i == victim);
-        float kf[16];
-        if (ok) {
-            const uint16_t *kr = isnew ? knew : a.K + (ubase + i) * kD;
-            uint4 r0 = isnew ? *reinterpret_cast<const uint4 *>(kr + 8 * c) : ldg_nc_v4(kr + 8 * c);
-            uint4 r1 = isnew ? *reinterpret_cast<const uint4 *>(kr + 64 + 8 * c)
-                             : ldg_nc_v4(kr + 64 + 8 * c);
-            unpack8(r0, kf);
-            unpack8(r1, kf + 8);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 16; j++) kf[j] = 0.f;
-        }
-        float part[G];
-#pragma unroll
-        for (int h = 0; h < G; h++) {
-            float acc = 0.f;
-#pragma unroll
-            for (int j = 0; j < 16; j++) acc = fmaf(qf[h][j], kf[j], acc);
-            part[h] = acc;
-        }
-#pragma unroll
-        for (int m = 1; m < 8; m <<= 1)
-#pragma unroll
-            for (int h = 0; h < G; h++) part[h] += __shfl_xor_sync(kFull, part[h], m);
-        if (ok) {
-            const float lnp = (!isnew && a.votes) ? logf((float)a.votes[ubase + i]) : 0.f;
-#pragma unroll
-            for (int h = 0; h < G; h++) {
-                const float x = part[h] + lnp;
-                mx[h] = fmaxf(mx[h], x);
-                if (c == h) XS(h, li) = x;
+    for (int n = 0; n < 16; n++) O[n][0] = O[n][1] = O[n][2] = O[n][3] = 0.f;
+    if (w == kNC) {
+        // ---------------- producer
+        if (lane == 0) {
+            int g = 0;
+            bool ok = true;
+            const int row0 = (int)((size_t)u * a.cap + s0);
+            for (int pass = 0; pass < 2 && ok; pass++) {
+                const CUtensorMap *map = pass == 0 ? &tmK : &tmV;
+                for (int t = 0; t < ntile; t++, g++) {
+                    const int stage = g % kStages;
+                    const uint32_t ph = (uint32_t)(g / kStages) & 1u;
+                    if (!mbar_wait(&S.empty[stage], ph ^ 1u)) { ok = false; break; }
+                    mbar_expect_tx(&S.full[stage], (uint32_t)kTileBytes);
+                    unsigned char *dst = ring + (size_t)stage * kTileBytes;
+                    tma_2d(dst, map, 0, row0 + t * kTile, &S.full[stage]);
+                    tma_2d(dst + kBoxBytes, map, 64, row0 + t * kTile, &S.full[stage]);
+                }
+            }
+            if (!ok) {
+                atomicExch(&S.bad, 1);
+                for (int j = max(0, g - kStages); j < g; j++)   // let issued copies land
+                    mbar_wait(&S.full[j % kStages], (uint32_t)(j / kStages) & 1u);
             }
         }
-    }
+        __syncwarp();
+    } else {
+        // ---------------- consumers
+        // A fragments of q: rows = heads (gq < G), k = 16 dims per step
+        uint32_t qa[8][2];
+        {
+            const uint32_t *q32 = reinterpret_cast<const uint32_t *>(a.q + (size_t)u * G * kD);
 #pragma unroll
-    for (int h = 0; h < G; h++) {
-        const float v = warp_max(mx[h]);
-        if (lane == 0) S.red[w][h] = v;
+            for (int ks = 0; ks < 8; ks++) {
+                qa[ks][0] = gq < G ? q32[(gq * kD + 16 * ks + 2 * tq) >> 1] : 0u;
+                qa[ks][1] = gq < G ? q32[(gq * kD + 16 * ks + 8 + 2 * tq) >> 1] : 0u;
+            }
+        }
+        const int rb = w * 16;                   // this warp's rows in a tile
+        bool good = true;
+        float mxq = -INFINITY;                   // max logit of head gq over this lane's slots
+        // Rows of this warp that must not be used as loaded: slots past the
+        // CTA's range (zeroed) and, on a lazy step, the victim's slot (the new
+        // token's row is written there).  Generic writes into the ring are
+        // fenced against the next TMA write of the stage.
+        auto patch = [&](uint32_t stage_off, int t, const uint16_t *newrow) -> bool {
+            bool any = false;
+            const int base_li = t * kTile + rb;
+            if (base_li + 16 > nrows) {
+                for (int e = lane; e < 16 * 16; e += 32) {
+                    const int r = e >> 4, j = e & 15;
+                    if (base_li + r >= nrows) {
+                        *reinterpret_cast<uint4 *>(ring + stage_off + sw_off(rb + r, j)) = make_uint4(0, 0, 0, 0);
+                        any = true;
+                    }
+                }
+            }
+            const int vr = victim - s0 - t * kTile - rb;
+            if (victim >= 0 && vr >= 0 && vr < 16) {
+                if (lane < 16)
+                    *reinterpret_cast<uint4 *>(ring + stage_off + sw_off(rb + vr, lane)) =
+                        *reinterpret_cast<const uint4 *>(newrow + 8 * lane);
+                any = true;
+            }
+            any = __any_sync(kFull, any);
+            if (any) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+            }
+            return any;
+        };
+        int g = 0;
+        // pass 1: logits
+        for (int t = 0; t < ntile; t++, g++) {
+            const int stage = g % kStages;
+            const uint32_t ph = (uint32_t)(g / kStages) & 1u;
+            if (good && !mbar_wait(&S.full[stage], ph)) good = false;
+            if (good) {
+                const uint32_t so = (uint32_t)stage * kTileBytes;
+                patch(so, t, knew);
+                float s0a[4] = {0.f, 0.f, 0.f, 0.f}, s1a[4] = {0.f, 0.f, 0.f, 0.f};
+                const int mi = lane >> 3;
+                const int lrow = rb + ((mi >> 1) << 3) + (lane & 7);
+#pragma unroll
+                for (int ks = 0; ks < 8; ks++) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(ring_s + so + sw_off(lrow, 2 * ks + (mi & 1)), b0, b1, b2, b3);
+                    mma16816(s0a, qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
+                    mma16816(s1a, qa[ks][0], 0u, qa[ks][1], 0u, b2, b3);
+                }
+                if (gq < G) {
+                    const float xv[4] = {s0a[0], s0a[1], s1a[0], s1a[1]};
+                    const int sl[4] = {2 * tq, 2 * tq + 1, 8 + 2 * tq, 9 + 2 * tq};
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        const int li = t * kTile + rb + sl[e];
+                        if (li < nrows) {
+                            const bool isnew = (s0 + li == victim);
+                            const float lnp = (!isnew && a.votes) ? logf((float)a.votes[ubase + s0 + li]) : 0.f;
+                            const float x = xv[e] * rs + lnp;
+                            XS(gq, li) = x;
+                            mxq = fmaxf(mxq, x);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0 && good) mbar_arrive(&S.empty[stage]);
+        }
+        // the virtual slot L (refresh steps): scalar dot products on warp 0
+        float xv_new[G];
+        if (has_new && w == 0) {
+#pragma unroll
+            for (int h = 0; h < G; h++) {
+                float sacc = 0.f;
+                for (int j = lane; j < kD; j += 32) sacc = fmaf(S.qs[h][j], bf2f(knew[j]), sacc);
+                xv_new[h] = warp_sum(sacc);          // S.qs already carries 1/sqrt(d)
+                if (lane == 0) XS(h, nrows) = xv_new[h];
+            }
+#pragma unroll
+            for (int h = 0; h < G; h++)
+                if (gq == h) mxq = fmaxf(mxq, xv_new[h]);
+        }
+        mxq = fmaxf(mxq, __shfl_xor_sync(kFull, mxq, 1));
+        mxq = fmaxf(mxq, __shfl_xor_sync(kFull, mxq, 2));
+        if (tq == 0 && gq < G) S.red[w][gq] = mxq;
+        consumer_sync();
+        float Mg = -INFINITY;                     // CTA max of head gq
+        if (gq < G)
+            for (int j = 0; j < kNC; j++) Mg = fmaxf(Mg, S.red[j][gq]);
+        if (tid < G) {
+            float v = S.red[0][tid];
+            for (int j = 1; j < kNC; j++) v = fmaxf(v, S.red[j][tid]);
+            S.pM[tid] = v;
+        }
+        consumer_sync();                          // S.red is reused below
+        // pass 2: O += P V
+        for (int t = 0; t < ntile; t++, g++) {
+            const int stage = g % kStages;
+            const uint32_t ph = (uint32_t)(g / kStages) & 1u;
+            if (good && !mbar_wait(&S.full[stage], ph)) good = false;
+            if (good) {
+                const uint32_t so = (uint32_t)stage * kTileBytes;
+                patch(so, t, vnew);
+                float pv[4];
+                const int sl[4] = {2 * tq, 2 * tq + 1, 8 + 2 * tq, 9 + 2 * tq};
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    const int li = t * kTile + rb + sl[e];
+                    pv[e] = (gq < G && li < nrows) ? expf(XS(gq, li) - Mg) : 0.f;
+                    lsq += pv[e];
+                }
+                uint16_t h0, l0, h1, l1, h2, l2, h3, l3;
+                split_bf16(pv[0], h0, l0);
+                split_bf16(pv[1], h1, l1);
+                split_bf16(pv[2], h2, l2);
+                split_bf16(pv[3], h3, l3);
+                const uint32_t ah0 = (uint32_t)h0 | ((uint32_t)h1 << 16), ah2 = (uint32_t)h2 | ((uint32_t)h3 << 16);
+                const uint32_t al0 = (uint32_t)l0 | ((uint32_t)l1 << 16), al2 = (uint32_t)l2 | ((uint32_t)l3 << 16);
+                const int mi = lane >> 3;
+                const int lrow = rb + ((mi & 1) << 3) + (lane & 7);
+#pragma unroll
+                for (int pp = 0; pp < 8; pp++) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(ring_s + so + sw_off(lrow, 2 * pp + (mi >> 1)), b0, b1, b2, b3);
+                    mma16816(O[2 * pp], ah0, 0u, ah2, 0u, b0, b1);
+                    mma16816(O[2 * pp], al0, 0u, al2, 0u, b0, b1);
+                    mma16816(O[2 * pp + 1], ah0, 0u, ah2, 0u, b2, b3);
+                    mma16816(O[2 * pp + 1], al0, 0u, al2, 0u, b2, b3);
+                }
+            }
+            __syncwarp();
+            if (lane == 0 && good) mbar_arrive(&S.empty[stage]);
+        }
+        if (has_new && w == 0 && gq < G) {
+            float pnew = 0.f;
+#pragma unroll
+            for (int h = 0; h < G; h++)
+                if (gq == h) pnew = expf(xv_new[h] - Mg);
+            if (tq == 0) lsq += pnew;
+#pragma unroll
+            for (int n = 0; n < 16; n++) {
+                O[n][0] = fmaf(pnew, bf2f(vnew[8 * n + 2 * tq]), O[n][0]);
+                O[n][1] = fmaf(pnew, bf2f(vnew[8 * n + 2 * tq + 1]), O[n][1]);
+            }
+        }
+        if (!good) atomicExch(&S.bad, 1);
+    }
+    // reduce the p v partials of the consumer warps (fragment layout: lane
+    // (gq, tq) holds head gq, dims 8n + 2tq and + 1)
+    for (int e = tid; e < G * kD; e += blockDim.x) S.po[e / kD][e % kD] = 0.f;
+    lsq += __shfl_xor_sync(kFull, lsq, 1);
+    lsq += __shfl_xor_sync(kFull, lsq, 2);
+    __syncthreads();
+    if (w < kNC && gq < G) {
+#pragma unroll
+        for (int n = 0; n < 16; n++) {
+            atomicAdd(&S.po[gq][8 * n + 2 * tq], O[n][0]);
+            atomicAdd(&S.po[gq][8 * n + 2 * tq + 1], O[n][1]);
+        }
+        if (tq == 0) S.red[w][gq] = lsq;
     }
     __syncthreads();
     if (tid < G) {
-        float v = S.red[0][tid];
-        for (int j = 1; j < 8; j++) v = fmaxf(v, S.red[j][tid]);
-        S.pM[tid] = v;
+        float l = 0.f;
+        for (int j = 0; j < kNC; j++) l += S.red[j][tid];
+        S.pl[tid] = l;
     }
     __syncthreads();
 
-    // ------------------------------------------------ pass 2: p v
+    // The rare direct recomputation of a refresh step (victim mass > 1/2)
+    // re-reads V from global memory with CUDA cores: 8 lanes per slot, the
+    // consumer warps only.
     auto pv_pass = [&](int skip, const float *Mref) {
-        float acc[G][16], lsum[G], Mr[G];
+        float accv[G][16], lsum[G];
 #pragma unroll
         for (int h = 0; h < G; h++) {
-            Mr[h] = Mref[h];
             lsum[h] = 0.f;
 #pragma unroll
-            for (int j = 0; j < 16; j++) acc[h][j] = 0.f;
+            for (int j = 0; j < 16; j++) accv[h][j] = 0.f;
         }
-        for (int base = w * 4; base < nloc; base += 32) {
-            const int li = base + grp;
-            const int i = s0 + li;
-            if (li < nloc && i != skip) {
-                const bool isnew = (i == L || i == victim);
-                const uint16_t *vr = isnew ? vnew : a.V + (ubase + i) * kD;
-                uint4 r0 = isnew ? *reinterpret_cast<const uint4 *>(vr + 8 * c) : ldg_nc_v4(vr + 8 * c);
-                uint4 r1 = isnew ? *reinterpret_cast<const uint4 *>(vr + 64 + 8 * c)
-                                 : ldg_nc_v4(vr + 64 + 8 * c);
-                float vf[16];
-                unpack8(r0, vf);
-                unpack8(r1, vf + 8);
+        if (w < kNC) {
+            float Mr[G];
 #pragma unroll
-                for (int h = 0; h < G; h++) {
-                    const float p = expf(XS(h, li) - Mr[h]);
-                    if (c == 0) lsum[h] += p;
+            for (int h = 0; h < G; h++) Mr[h] = Mref[h];
+            stream_rows(Vu, vnew, s0, nloc, L, victim, w, kNC, grp, c,
+                        [&](int li, int i, bool isnew, bool ok, const uint4 &r0, const uint4 &r1) {
+                (void)isnew;
+                if (ok && i != skip) {
+                    float vf[16];
+                    unpack8(r0, vf);
+                    unpack8(r1, vf + 8);
 #pragma unroll
-                    for (int j = 0; j < 16; j++) acc[h][j] = fmaf(p, vf[j], acc[h][j]);
+                    for (int h = 0; h < G; h++) {
+                        const float p = expf(XS(h, li) - Mr[h]);
+                        if (c == 0) lsum[h] += p;
+#pragma unroll
+                        for (int j = 0; j < 16; j++) accv[h][j] = fmaf(p, vf[j], accv[h][j]);
+                    }
                 }
-            }
+            });
         }
 #pragma unroll
         for (int h = 0; h < G; h++) {
 #pragma unroll
             for (int j = 0; j < 16; j++) {
-                acc[h][j] += __shfl_xor_sync(kFull, acc[h][j], 8);
-                acc[h][j] += __shfl_xor_sync(kFull, acc[h][j], 16);
+                accv[h][j] += __shfl_xor_sync(kFull, accv[h][j], 8);
+                accv[h][j] += __shfl_xor_sync(kFull, accv[h][j], 16);
             }
             lsum[h] = warp_sum(lsum[h]);
         }
         for (int e = tid; e < G * kD; e += blockDim.x) S.po[e / kD][e % kD] = 0.f;
         __syncthreads();
-        if (grp == 0)
+        if (grp == 0 && w < kNC)
 #pragma unroll
             for (int h = 0; h < G; h++)
 #pragma unroll
                 for (int j = 0; j < 8; j++) {
-                    atomicAdd(&S.po[h][8 * c + j], acc[h][j]);
-                    atomicAdd(&S.po[h][64 + 8 * c + j], acc[h][8 + j]);
+                    atomicAdd(&S.po[h][8 * c + j], accv[h][j]);
+                    atomicAdd(&S.po[h][64 + 8 * c + j], accv[h][8 + j]);
                 }
         if (lane == 0)
 #pragma unroll
@@ -338,12 +706,11 @@ __global__ void __launch_bounds__(256, 2) fused_step_kernel(FusedArgs a)
         __syncthreads();
         if (tid < G) {
             float l = 0.f;
-            for (int j = 0; j < 8; j++) l += S.red[j][tid];
+            for (int j = 0; j < kNC; j++) l += S.red[j][tid];
             S.pl[tid] = l;
         }
         __syncthreads();
     };
-    pv_pass(-1, S.pM);
 
     // ------------------------------------------------ cluster merge
     cluster.sync();                                                    // partials visible
@@ -417,7 +784,7 @@ __global__ void __launch_bounds__(256, 2) fused_step_kernel(FusedArgs a)
             __syncthreads();
             if (tid == 0) {
                 Cand b = S.bc[0];
-                for (int j = 1; j < 8; j++)
+                for (int j = 1; j < kWarps; j++)
                     if (cand_less(S.bc[j], b)) b = S.bc[j];
                 S.cand[rnd] = b;
                 chosen[b.slot - s0] = 1;
@@ -574,13 +941,13 @@ __global__ void __launch_bounds__(256, 2) fused_step_kernel(FusedArgs a)
         }
     }
     // correction weights (every CTA, full dot with the new key mean)
-    if (w < G) {
+    for (int h = w; h < G; h += kWarps) {
         float s = 0.f;
-        for (int j = lane; j < kD; j += 32) s = fmaf(S.qs[w][j], S.muk[j], s);
+        for (int j = lane; j < kD; j += 32) s = fmaf(S.qs[h][j], S.muk[j], s);
         s = warp_sum(s);
         if (lane == 0) {
             const float logZE = logf(n1) + s;
-            S.wR[w] = 1.f / (1.f + expf(logZE - S.lzR[w]));
+            S.wR[h] = 1.f / (1.f + expf(logZE - S.lzR[h]));
         }
     }
     __syncthreads();
@@ -618,15 +985,54 @@ __global__ void __launch_bounds__(256, 2) fused_step_kernel(FusedArgs a)
                                              : __longlong_as_double(0x7ff0000000000000ll);
         }
     }
+    if (tid == 0 && S.bad) record_status(a.status, KVC_ERR_TIMEOUT);
     cluster.sync();             // no CTA leaves while another may read its shared memory
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// [rows][128] bf16 rows of 256 bytes, loaded as boxes of 64 columns x kTile
+// rows with the 128-byte swizzle.  Rows past the end read as zero.
+static bool make_row_map(CUtensorMap *m, const void *base, uint64_t rows)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)kTile};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int G>
 static cudaError_t launch_fused_g(const FusedArgs &a0, int U, int CS, cudaStream_t st)
 {
     FusedArgs a = a0;
-    const size_t dyn = align_up((size_t)G * (a.chunk + 1) * 4) + align_up((size_t)(a.chunk + 1) * 8) +
-                       align_up((size_t)(a.chunk + 1) * 4) + align_up((size_t)(a.chunk + 1));
+    const size_t sel = align_up((size_t)(a.chunk + 1) * 8) + align_up((size_t)(a.chunk + 1) * 4) +
+                       align_up((size_t)(a.chunk + 1));
+    if (sel > (size_t)kStages * kTileBytes) return cudaErrorNotSupported;
+    CUtensorMap tmK, tmV;
+    const uint64_t rows = (uint64_t)U * (uint64_t)a.cap;
+    if (rows >= (1ull << 31) || !make_row_map(&tmK, a.K, rows) || !make_row_map(&tmV, a.V, rows))
+        return cudaErrorNotSupported;
+    const size_t dyn = 1024 + (size_t)kStages * kTileBytes + align_up((size_t)G * (a.chunk + 1) * 4);
     cudaError_t e = cudaFuncSetAttribute(fused_step_kernel<G>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
     if (e != cudaSuccess) return e;
@@ -634,7 +1040,7 @@ static cudaError_t launch_fused_g(const FusedArgs &a0, int U, int CS, cudaStream
     (void)e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(U * CS);
-    cfg.blockDim = dim3(256);
+    cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = dyn;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -644,12 +1050,12 @@ static cudaError_t launch_fused_g(const FusedArgs &a0, int U, int CS, cudaStream
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fused_step_kernel<G>, a);
+    return cudaLaunchKernelEx(&cfg, fused_step_kernel<G>, a, tmK, tmV);
 }
 
 int fused_cluster_size(int U, int L)
 {
-    int cs = (L + kFusedMaxChunk - 1) / kFusedMaxChunk;
+    int cs = (L + 2047) / 2048;                        // about 1-2 K slots per CTA
     const int want = (4 * 152 + U - 1) / U;            // fill the SMs for small U
     cs = max(cs, min(want, (L + 31) / 32));
     cs = max(1, min(kFusedMaxCS, cs));
