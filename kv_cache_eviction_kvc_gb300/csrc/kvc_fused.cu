@@ -43,7 +43,7 @@ constexpr int kFusedMaxChunk = 4096;   // slots per CTA
 constexpr int kFusedMaxCS = 8;         // CTAs per cluster
 constexpr int kMaxQueue = kPendStride - 2;
 constexpr int kNC = 4;                 // consumer warps
-constexpr int kWarps = kNC + 1;        // + one producer warp
+constexpr int kWarps = kNC + 2;        // + one producer warp + one moment-fold warp
 constexpr int kThreads = kWarps * 32;
 constexpr int kTile = 64;              // slots per ring stage: 16 per consumer warp
 constexpr int kBoxBytes = kTile * 128; // one box: 64 rows x 64 bf16, 128B-swizzled
@@ -237,6 +237,7 @@ struct FusedSmem {
     float n0;
     float muk[kD], muv[kD];
     float cq[G][kD];
+    float zq[G];                // q_h . mu_k' / sqrt(d) after the fold
     float wR[G];
     double vm;                  // utility of the new token (refresh, last CTA)
     Cand cand[kMaxQueue];
@@ -408,20 +409,8 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
                 return;
             }
         }
-        // the owner publishes the victim's key / value / vote / position
-        if (victim >= s0 && victim < s1) {
-            const uint16_t *kr = a.K + (ubase + victim) * kD;
-            const uint16_t *vr = a.V + (ubase + victim) * kD;
-            for (int e = tid; e < kD; e += blockDim.x) {
-                S.pk[e] = bf2f(kr[e]);
-                S.pv[e] = bf2f(vr[e]);
-            }
-            if (tid == 0) {
-                S.pvp = a.votes ? (float)a.votes[ubase + victim] : 1.f;
-                S.pvpos = a.pos[ubase + victim];
-            }
-        }
     }
+
 
     // ------------------------------------------------ passes 1 and 2 over the ring
     // The producer warp streams the K rows of [s0, s1), then the V rows, in
@@ -440,7 +429,100 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
     float lsq = 0.f;                                 // sum of p for head gq (this lane's slots)
 #pragma unroll
     for (int n = 0; n < 16; n++) O[n][0] = O[n][1] = O[n][2] = O[n][3] = 0.f;
-    if (w == kNC) {
+
+    // Moment fold of the victim (West's weighted incremental update of the
+    // mean / covariance form): mu' = mu + (x - mu) p / n', C' = (n/n') C +
+    // (p n / n'^2) dv dk^T with dk, dv taken against the old means; this
+    // CTA updates its rows of C and forms C' q / sqrt(d) for them, and
+    // q . mu_k' / sqrt(d) for the Jensen bound.  Run by the fold warp during
+    // the passes on lazy steps (the victim is known up front), by the whole
+    // CTA after the selection on refresh steps.
+    const int rows = (kD + CS - 1) / CS;
+    const int r0 = min(kD, r * rows), r1 = min(kD, r0 + rows);
+    float *Cu = a.C + (size_t)u * kD * kD;
+    auto fold = [&](int p, int np, bool block_sync) {
+        auto psync = [&]() {
+            if (block_sync) __syncthreads();
+            else __syncwarp();
+        };
+        const float n0 = S.n0, pe = S.vp, n1 = n0 + pe, fw = pe / n1;
+        for (int e = p; e < kD; e += np) {
+            const float mk = S.mk0[e], mv = S.mv0[e];
+            S.muk[e] = mk + (S.vk[e] - mk) * fw;
+            S.muv[e] = mv + (S.vv[e] - mv) * fw;
+            S.vk[e] -= mk;                  // delta k (old mean)
+            S.vv[e] -= mv;                  // delta v
+        }
+        psync();
+        const float sc_old = n0 / n1, sc_rank = pe * n0 / (n1 * n1);
+        // participant -> (row, quarter of columns); the loop bound is uniform
+        // so that every lane reaches the shuffles
+        for (int rb = r0; rb < r1; rb += np >> 2) {
+            const int rr = rb + (p >> 2);
+            const bool valid = rr < r1;
+            const int q4 = p & 3;
+            float acc[G];
+#pragma unroll
+            for (int h = 0; h < G; h++) acc[h] = 0.f;
+            if (valid) {
+                float *crow = Cu + (size_t)rr * kD + q4 * 32;
+                const float dv = S.vv[rr] * sc_rank;
+                float4 cv[8];
+#pragma unroll
+                for (int j = 0; j < 8; j++) cv[j] = *reinterpret_cast<float4 *>(crow + 4 * j);
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    const float *dk = &S.vk[q4 * 32 + 4 * j];
+                    cv[j].x = fmaf(cv[j].x, sc_old, dv * dk[0]);
+                    cv[j].y = fmaf(cv[j].y, sc_old, dv * dk[1]);
+                    cv[j].z = fmaf(cv[j].z, sc_old, dv * dk[2]);
+                    cv[j].w = fmaf(cv[j].w, sc_old, dv * dk[3]);
+                    *reinterpret_cast<float4 *>(crow + 4 * j) = cv[j];
+#pragma unroll
+                    for (int h = 0; h < G; h++) {
+                        const float *qq = &S.qs[h][q4 * 32 + 4 * j];
+                        acc[h] = fmaf(cv[j].x, qq[0], acc[h]);
+                        acc[h] = fmaf(cv[j].y, qq[1], acc[h]);
+                        acc[h] = fmaf(cv[j].z, qq[2], acc[h]);
+                        acc[h] = fmaf(cv[j].w, qq[3], acc[h]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < G; h++) {
+                acc[h] += __shfl_xor_sync(kFull, acc[h], 1);
+                acc[h] += __shfl_xor_sync(kFull, acc[h], 2);
+                if (valid && q4 == 0) S.cq[h][rr] = acc[h];    // q already carries 1/sqrt(d)
+            }
+        }
+        psync();
+        const int pw = p >> 5, npw = np >> 5, pl = p & 31;
+        for (int h = pw; h < G; h += npw) {
+            float sacc = 0.f;
+            for (int j = pl; j < kD; j += 32) sacc = fmaf(S.qs[h][j], S.muk[j], sacc);
+            sacc = warp_sum(sacc);
+            if (pl == 0) S.zq[h] = sacc;
+        }
+        psync();
+    };
+
+    if (w == kNC + 1) {
+        // ---------------- moment fold (lazy steps), concurrent with the passes
+        if (!refresh) {
+            const uint16_t *kr = a.K + (ubase + victim) * kD;
+            const uint16_t *vr = a.V + (ubase + victim) * kD;
+            for (int e = lane; e < kD; e += 32) {
+                S.vk[e] = bf2f(kr[e]);
+                S.vv[e] = bf2f(vr[e]);
+            }
+            if (lane == 0) {
+                S.vp = a.votes ? (float)a.votes[ubase + victim] : 1.f;
+                S.vpos = a.pos[ubase + victim];
+            }
+            __syncwarp();
+            fold(lane, 32, false);
+        }
+    } else if (w == kNC) {
         // ---------------- producer
         if (lane == 0) {
             int g = 0;
@@ -876,79 +958,14 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
         vic_owner = victim / ch;
         for (int e = tid; e < G * kD; e += blockDim.x) S.fR[e / kD][e % kD] /= S.gl[e / kD];
         if (tid < G) S.lzR[tid] = S.gM[tid] + logf(S.gl[tid]);
-        cluster.sync();                                                // victim visible
-        FusedSmem<G> *O = cluster.map_shared_rank(&S, vic_owner);
-        for (int e = tid; e < kD; e += blockDim.x) {
-            S.vk[e] = O->pk[e];
-            S.vv[e] = O->pv[e];
-        }
-        if (tid == 0) { S.vp = O->pvp; S.vpos = O->pvpos; }
         __syncthreads();
     }
 
-    // ------------------------------------------------ moment fold (West)
-    const float n0 = S.n0;
-    const float pe = S.vp;
-    const float n1 = n0 + pe;
-    const float fw = pe / n1;
-    for (int e = tid; e < kD; e += blockDim.x) {
-        const float mk = S.mk0[e], mv = S.mv0[e];
-        S.muk[e] = mk + (S.vk[e] - mk) * fw;
-        S.muv[e] = mv + (S.vv[e] - mv) * fw;
-        S.vk[e] -= mk;                  // delta k (old mean)
-        S.vv[e] -= mv;                  // delta v
-    }
-    __syncthreads();
-    const int rows = (kD + CS - 1) / CS;
-    const int r0 = min(kD, r * rows), r1 = min(kD, r0 + rows);
-    const float sc_old = n0 / n1, sc_rank = pe * n0 / (n1 * n1);
-    float *Cu = a.C + (size_t)u * kD * kD;
-    // thread -> (row, quarter of columns); 4 threads per row.  The loop bound
-    // is uniform so that every lane reaches the shuffles.
-    for (int rb = r0; rb < r1; rb += (int)blockDim.x >> 2) {
-        const int rr = rb + (tid >> 2);
-        const bool valid = rr < r1;
-        const int q4 = tid & 3;
-        float acc[G];
-#pragma unroll
-        for (int h = 0; h < G; h++) acc[h] = 0.f;
-        if (valid) {
-            float *crow = Cu + (size_t)rr * kD + q4 * 32;
-            const float dv = S.vv[rr] * sc_rank;
-#pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-                float4 cv = *reinterpret_cast<float4 *>(crow + j);
-                cv.x = fmaf(cv.x, sc_old, dv * S.vk[q4 * 32 + j]);
-                cv.y = fmaf(cv.y, sc_old, dv * S.vk[q4 * 32 + j + 1]);
-                cv.z = fmaf(cv.z, sc_old, dv * S.vk[q4 * 32 + j + 2]);
-                cv.w = fmaf(cv.w, sc_old, dv * S.vk[q4 * 32 + j + 3]);
-                *reinterpret_cast<float4 *>(crow + j) = cv;
-#pragma unroll
-                for (int h = 0; h < G; h++) {
-                    const float *qq = &S.qs[h][q4 * 32 + j];
-                    acc[h] = fmaf(cv.x, qq[0], acc[h]);
-                    acc[h] = fmaf(cv.y, qq[1], acc[h]);
-                    acc[h] = fmaf(cv.z, qq[2], acc[h]);
-                    acc[h] = fmaf(cv.w, qq[3], acc[h]);
-                }
-            }
-        }
-#pragma unroll
-        for (int h = 0; h < G; h++) {
-            acc[h] += __shfl_xor_sync(kFull, acc[h], 1);
-            acc[h] += __shfl_xor_sync(kFull, acc[h], 2);
-            if (valid && q4 == 0) S.cq[h][rr] = acc[h];    // q already carries 1/sqrt(d)
-        }
-    }
-    // correction weights (every CTA, full dot with the new key mean)
-    for (int h = w; h < G; h += kWarps) {
-        float s = 0.f;
-        for (int j = lane; j < kD; j += 32) s = fmaf(S.qs[h][j], S.muk[j], s);
-        s = warp_sum(s);
-        if (lane == 0) {
-            const float logZE = logf(n1) + s;
-            S.wR[h] = 1.f / (1.f + expf(logZE - S.lzR[h]));
-        }
+    if (refresh) fold(tid, blockDim.x, true);         // lazy steps folded during the passes
+    const float n1 = S.n0 + S.vp;
+    for (int h = tid; h < G; h += blockDim.x) {
+        const float logZE = logf(n1) + S.zq[h];
+        S.wR[h] = 1.f / (1.f + expf(logZE - S.lzR[h]));
     }
     __syncthreads();
     float *ou = a.o + (size_t)u * G * kD;
