@@ -45,6 +45,11 @@ def parse():
                     help="override the sequence count (smaller case for profiling)")
     ap.add_argument("--prefill", type=int, default=None,
                     help="override the prefill length N (smaller case for profiling)")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="time only the LaProx prefill scorer (prefill-scoring workload)")
+    ap.add_argument("--prefill-layers", type=int, default=None,
+                    help="override the layer count of the prefill-scoring workload")
+    ap.add_argument("--no-prefill", action="store_true")
     return ap.parse_args()
 
 
@@ -82,6 +87,75 @@ def step_bytes(cfg, refresh: bool, emit_probs: bool) -> int:
         if emit_probs:
             b += (L + 1) * 8
     return b * cfg.U
+
+
+def prefill_bytes(pc) -> int:
+    """Algorithmic HBM bytes of one prefill scoring call: K and V once, the
+    window queries, the Gram matrices, the indicator written, then read and
+    written by the normalization, read by the four radix passes, the count
+    and the write pass, and the keep mask / counts / indices written."""
+    M = pc.NL * pc.Hkv * pc.N
+    b = 2 * M * pc.d * 2
+    b += pc.NL * pc.Hq * pc.w * pc.d * 2
+    b += pc.NL * pc.Hkv * pc.d * pc.d * 4
+    b += M * 4 * (1 + 2 + 4 + 1 + 1)
+    b += M + pc.NL * pc.Hkv * 4 + pc.B_total * 8
+    return b
+
+
+def prefill_flops(pc) -> int:
+    """Algorithmic tensor-core FLOPs: q K^T of the G*w window rows once and
+    v Gram once (the second q K^T pass and the three-term Gram split are
+    implementation choices on top)."""
+    M = pc.NL * pc.Hkv * pc.N
+    return 2 * M * pc.G * pc.w * pc.d + 2 * M * pc.d * pc.d
+
+
+def run_prefill(pc, dev, reps=5):
+    import torch
+    from kv_cache_eviction_kvc_gb300 import kvc, workloads as W
+    inp = W.gen_prefill_scorer(pc, dev, 0)
+    NL, Hq, Hkv, d, N, w, B = pc.NL, pc.Hq, pc.Hkv, pc.d, pc.N, pc.w, pc.B_total
+    gram = torch.empty(NL, Hkv, d, d, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    kvc.kvc_prefill_prepare(NL, Hq, Hkv, d, pc.D, inp["W_O"], gram)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    prep_ms = e0.elapsed_time(e1)
+    ws = torch.empty(kvc.kvc_prefill_workspace_size(NL, Hkv, N, B), dtype=torch.uint8, device=dev)
+    scores = torch.empty(NL, Hkv, N, dtype=torch.float32, device=dev)
+    keep = torch.empty(NL, Hkv, N, dtype=torch.uint8, device=dev)
+    counts = torch.empty(NL, Hkv, dtype=torch.int32, device=dev)
+    idx = torch.empty(max(B, 1), dtype=torch.int64, device=dev)
+
+    def call():
+        kvc.kvc_prefill_score(NL, Hq, Hkv, d, N, w, B, 1, inp["q_win"], inp["K"], inp["V"], gram,
+                              scores, keep, counts, idx, ws)
+    for _ in range(2):
+        call()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    ms = sorted(times)[len(times) // 2]
+    peak, kind = peaks()
+    by = prefill_bytes(pc)
+    ach = by / (ms * 1e-3) / 1e9
+    fl = prefill_flops(pc)
+    return {"workload": pc.name, "description": pc.description, "ms_per_call": ms,
+            "calls_per_s": 1000.0 / ms, "prepare_ms": prep_ms,
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
+                         "frac": ach / peak, "peak_kind": kind, "bytes_per_call": by,
+                         "algorithmic_tflops": fl / (ms * 1e-3) / 1e12,
+                         "kernels": "prefill_score_kernel + normalize + radix top-K"},
+            "kept": int(counts.sum().item())}
 
 
 # ------------------------------------------------------------ clocks
@@ -329,6 +403,13 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", 1))
     from kv_cache_eviction_kvc_gb300 import workloads as W
     cfg = W.DECODE_CONFIGS[args.config]
+    if args.prefill_only:
+        import torch
+        pc = W.C3 if args.prefill_layers is None else W.C3.with_(NL=args.prefill_layers)
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        print(json.dumps({"metric": "prefill scoring calls/sec", **run_prefill(pc, dev)}))
+        return
     if args.batch is not None:
         cfg = cfg.with_(B=args.batch, name=cfg.name + f"-b{args.batch}")
     if args.prefill is not None:
@@ -360,6 +441,10 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     res = run_ours(args, cfg, rank, world)
+    if rank == 0 and not args.no_prefill and args.batch is None and args.prefill is None:
+        import torch
+        torch.cuda.empty_cache()
+        res["prefill"] = run_prefill(W.C3, torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0))))
     if rank == 0:
         if not args.no_cpu_baseline:
             rate, cores, sample, _ = oracle_sample(cfg, args.cpu_seconds)

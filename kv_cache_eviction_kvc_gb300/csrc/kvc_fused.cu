@@ -28,12 +28,12 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
-#include <mutex>
 
 #include <cuda_bf16.h>
 
 #include "kvc_common.cuh"
 #include "kvc_internal.h"
+#include "kvc_tma.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -49,134 +49,9 @@ constexpr int kTile = 64;              // slots per ring stage: 16 per consumer 
 constexpr int kBoxBytes = kTile * 128; // one box: 64 rows x 64 bf16, 128B-swizzled
 constexpr int kTileBytes = 2 * kBoxBytes;
 constexpr int kStages = 4;
-constexpr long long kWaitCycles = 4000000000ll;   // ~2 s: a wait that long means a fault
 
-// ---------------------------------------------------------------- TMA ring
-__device__ __forceinline__ uint32_t smem_u32(const void *p)
-{
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *b)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *b, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(smem_u32(b)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Wait for the phase of the given parity to complete; false after ~2 s
-// (the caller then records KVC_ERR_TIMEOUT instead of waiting forever).
-__device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity)
-{
-    if (mbar_try_wait(b, parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_try_wait(b, parity))
-        if (clock64() - t0 > kWaitCycles) return false;
-    return true;
-}
-
-// One bulk copy global -> this CTA's shared memory, completing on `bar`.
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void consumer_sync()
-{
-    asm volatile("bar.sync 1, %0;" ::"n"(kNC * 32) : "memory");
-}
-
-__device__ __forceinline__ uint4 lds_v4(const void *p)
-{
-    uint4 r;
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "r"(smem_u32(p)));
-    return r;
-}
-
-// 2D tile copy (box of 64 columns x 64 rows) described by a tensor map.
-__device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *map, int x, int y,
-                                      uint64_t *bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
-
-// Byte offset of 16-byte chunk j (0..15) of row r (0..63) in a stage: the
-// row's two 128-byte halves live in two boxes; inside a box the chunk index
-// is XOR-ed with the row index mod 8 (the TMA 128-byte swizzle), which makes
-// the 8-row ldmatrix reads below conflict-free.
-__device__ __forceinline__ uint32_t sw_off(int r, int j)
-{
-    return (uint32_t)(((j >> 3) * kBoxBytes) + (r << 7) + ((((j & 7) ^ (r & 7))) << 4));
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                        uint32_t &r3)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                          uint32_t &r3)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-
-// D += A (16x16 bf16, row) * B (16x8 bf16, col), fp32 accumulate
-__device__ __forceinline__ void mma16816(float *d, uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// round-to-nearest bf16 of x and of the remainder x - hi (so hi + lo keeps
-// about 16 significant bits)
-__device__ __forceinline__ void split_bf16(float x, uint16_t &hi, uint16_t &lo)
-{
-    const __nv_bfloat16 h = __float2bfloat16_rn(x);
-    const __nv_bfloat16 l = __float2bfloat16_rn(x - __bfloat162float(h));
-    hi = __bfloat16_as_ushort(h);
-    lo = __bfloat16_as_ushort(l);
-}
+__device__ __forceinline__ uint32_t sw_off(int r, int j) { return sw_off_t<kTile>(r, j); }
+__device__ __forceinline__ void consumer_sync() { named_sync<kNC * 32>(); }
 
 struct FusedArgs {
     const uint16_t *q, *k_new, *v_new;
@@ -1006,38 +881,6 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
     cluster.sync();             // no CTA leaves while another may read its shared memory
 }
 
-// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
-// against the driver library).
-static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
-{
-    static std::once_flag once;
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
-// [rows][128] bf16 rows of 256 bytes, loaded as boxes of 64 columns x kTile
-// rows with the 128-byte swizzle.  Rows past the end read as zero.
-static bool make_row_map(CUtensorMap *m, const void *base, uint64_t rows)
-{
-    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-    if (!enc) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
-    const cuuint32_t box[2] = {64u, (cuuint32_t)kTile};
-    const cuuint32_t estr[2] = {1u, 1u};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int G>
 static cudaError_t launch_fused_g(const FusedArgs &a0, int U, int CS, cudaStream_t st)
 {
@@ -1047,7 +890,7 @@ static cudaError_t launch_fused_g(const FusedArgs &a0, int U, int CS, cudaStream
     if (sel > (size_t)kStages * kTileBytes) return cudaErrorNotSupported;
     CUtensorMap tmK, tmV;
     const uint64_t rows = (uint64_t)U * (uint64_t)a.cap;
-    if (rows >= (1ull << 31) || !make_row_map(&tmK, a.K, rows) || !make_row_map(&tmV, a.V, rows))
+    if (rows >= (1ull << 31) || !make_row_map(&tmK, a.K, rows, kTile) || !make_row_map(&tmV, a.V, rows, kTile))
         return cudaErrorNotSupported;
     const size_t dyn = 1024 + (size_t)kStages * kTileBytes + align_up((size_t)G * (a.chunk + 1) * 4);
     cudaError_t e = cudaFuncSetAttribute(fused_step_kernel<G>,

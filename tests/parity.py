@@ -173,3 +173,67 @@ def run_decode_parity(cfg: W.DecodeConfig, *, steps: int | None = None, units=No
     finally:
         sess.close()
     return rep
+
+
+# ---------------------------------------------------------------------------
+# prefill scorer
+# ---------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class PrefillReport:
+    band_hits: int = 0
+    mismatches: int = 0
+    max_gram_err: float = 0.0
+    max_s_err: float = 0.0
+    counts_ok: bool = True
+    idx_ok: bool = True
+    kept: int = 0
+    first_mismatch: str = ""
+
+    def ok(self):
+        return (self.mismatches == 0 and self.max_gram_err <= MOM_TOL
+                and self.max_s_err <= O_TOL and self.counts_ok and self.idx_ok)
+
+
+def run_prefill_parity(cfg: W.PrefillConfig, *, seed: int = 0, device="cuda",
+                       normalize: bool = True) -> PrefillReport:
+    from kv_cache_eviction_kvc_gb300 import kvc as K
+    NL, Hq, Hkv, d, N, w, B = cfg.NL, cfg.Hq, cfg.Hkv, cfg.d, cfg.N, cfg.w, cfg.B_total
+    inp = W.gen_prefill_scorer(cfg, device, seed)
+    gram = torch.empty(NL, Hkv, d, d, dtype=torch.float32, device=device)
+    K.kvc_prefill_prepare(NL, Hq, Hkv, d, cfg.D, inp["W_O"], gram)
+    M = NL * Hkv * N
+    ws = torch.empty(max(256, K.kvc_prefill_workspace_size(NL, Hkv, N, B)), dtype=torch.uint8,
+                     device=device)
+    scores = torch.empty(NL, Hkv, N, dtype=torch.float32, device=device)
+    keep = torch.empty(NL, Hkv, N, dtype=torch.uint8, device=device)
+    counts = torch.empty(NL, Hkv, dtype=torch.int32, device=device)
+    idx = torch.empty(max(B, 1), dtype=torch.int64, device=device)
+    K.kvc_prefill_score(NL, Hq, Hkv, d, N, w, B, int(normalize), inp["q_win"], inp["K"],
+                        inp["V"], gram, scores, keep, counts, idx, ws)
+    torch.cuda.synchronize()
+    ref = O.prefill_score(inp["q_win"], inp["K"], inp["V"], inp["W_O"], NL=NL, Hq=Hq, Hkv=Hkv,
+                          d=d, N=N, w=w, B_total=B, normalize=normalize)
+    rep = PrefillReport()
+    g = gram.cpu().numpy().astype(np.float64)
+    rep.max_gram_err = float(np.abs(g - ref["Gram"]).max() / np.abs(ref["Gram"]).max())
+    s_gpu = scores.cpu().numpy().astype(np.float64)
+    s_ref = ref["s"]
+    rep.max_s_err = float((np.abs(s_gpu - s_ref) / np.maximum(np.abs(s_ref), 1e-30)).max())
+    kg = keep.cpu().numpy().astype(bool).ravel()
+    kr = ref["keep"].astype(bool).ravel()
+    diff = np.nonzero(kg ^ kr)[0]
+    thr = ref["thr"]
+    flat_s = s_ref.ravel()
+    for j in diff:
+        if abs(flat_s[j] - thr) <= TIE_REL * abs(thr):
+            rep.band_hits += 1
+        else:
+            rep.mismatches += 1
+            if not rep.first_mismatch:
+                rep.first_mismatch = f"flat {j}: s_ref {flat_s[j]!r} thr {thr!r} gpu keep {kg[j]}"
+    rep.kept = int(kg.sum())
+    rep.counts_ok = bool(rep.kept == B and np.array_equal(
+        counts.cpu().numpy(), kg.reshape(NL, Hkv, N).sum(axis=2)))
+    rep.idx_ok = bool(np.array_equal(idx[:B].cpu().numpy(), np.nonzero(kg)[0]))
+    return rep

@@ -1,0 +1,36 @@
+"""GPU parity of the LaProx prefill scorer (through the C ABI) against the
+fp64 oracle: the full prefill-scoring workload and edge cases."""
+import pytest
+import torch
+
+from kv_cache_eviction_kvc_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from parity import run_prefill_parity  # noqa: E402
+
+
+def check(rep):
+    print(rep)
+    assert rep.ok(), rep
+
+
+def test_c3_full():
+    check(run_prefill_parity(W.C3))
+
+
+SMALL = W.C3.with_(NL=2, N=1024, B_total=512)
+
+
+@pytest.mark.parametrize("cfg,normalize", [
+    (SMALL, True),
+    (SMALL.with_(N=1000, B_total=777), True),            # ragged key tiles per CTA
+    (SMALL.with_(N=200, w=8, B_total=1), True),          # short window, one kept
+    (SMALL.with_(NL=1, Hq=8, Hkv=2, N=513, B_total=1026), True),   # keep everything
+    (SMALL, False),                                       # no per-layer normalization
+], ids=["small", "ragged", "w8-k1", "keep-all", "unnormalized"])
+def test_prefill_edge_cases(cfg, normalize):
+    check(run_prefill_parity(cfg, normalize=normalize))
