@@ -300,10 +300,10 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
     const int ntile = (nrows + kTile - 1) / kTile;
     const int gq = lane >> 2, tq = lane & 3;        // mma fragment coordinates
     const uint32_t ring_s = smem_u32(ring);
-    float O[16][4];
+    float O[8][4];                                   // O^T fragments: dims 16 m + gq (+8), heads 2 tq (+1)
     float lsq = 0.f;                                 // sum of p for head gq (this lane's slots)
 #pragma unroll
-    for (int n = 0; n < 16; n++) O[n][0] = O[n][1] = O[n][2] = O[n][3] = 0.f;
+    for (int n = 0; n < 8; n++) O[n][0] = O[n][1] = O[n][2] = O[n][3] = 0.f;
 
     // Moment fold of the victim (West's weighted incremental update of the
     // mean / covariance form): mu' = mu + (x - mu) p / n', C' = (n/n') C +
@@ -424,19 +424,24 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
         __syncwarp();
     } else {
         // ---------------- consumers
-        // A fragments of q: rows = heads (gq < G), k = 16 dims per step
-        uint32_t qa[8][2];
+        // q K^T as D[slot][head]: A = 16 K rows (ldmatrix from the swizzled
+        // tile), B = q^T (16 dims x 8 heads, heads >= G zero).  P V as
+        // O^T[dim][head]: A = V^T (ldmatrix.trans), B = P^T (16 slots x 8
+        // heads, p split into bf16 hi + lo).  A lane (gq, tq) holds logits of
+        // slots gq, gq + 8 for heads 2 tq, 2 tq + 1, and p of head gq.
+        uint32_t qb[8][2];
         {
             const uint32_t *q32 = reinterpret_cast<const uint32_t *>(a.q + (size_t)u * G * kD);
 #pragma unroll
             for (int ks = 0; ks < 8; ks++) {
-                qa[ks][0] = gq < G ? q32[(gq * kD + 16 * ks + 2 * tq) >> 1] : 0u;
-                qa[ks][1] = gq < G ? q32[(gq * kD + 16 * ks + 8 + 2 * tq) >> 1] : 0u;
+                qb[ks][0] = gq < G ? q32[(gq * kD + 16 * ks + 2 * tq) >> 1] : 0u;
+                qb[ks][1] = gq < G ? q32[(gq * kD + 16 * ks + 8 + 2 * tq) >> 1] : 0u;
             }
         }
         const int rb = w * 16;                   // this warp's rows in a tile
+        const int h0 = 2 * tq, h1 = 2 * tq + 1;  // heads of this lane's logits
         bool good = true;
-        float mxq = -INFINITY;                   // max logit of head gq over this lane's slots
+        float mx0 = -INFINITY, mx1 = -INFINITY;  // max logit of heads h0, h1 over this lane's slots
         // Rows of this warp that must not be used as loaded: slots past the
         // CTA's range (zeroed) and, on a lazy step, the victim's slot (the new
         // token's row is written there).  Generic writes into the ring are
@@ -476,28 +481,30 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             if (good) {
                 const uint32_t so = (uint32_t)stage * kTileBytes;
                 patch(so, t, knew);
-                float s0a[4] = {0.f, 0.f, 0.f, 0.f}, s1a[4] = {0.f, 0.f, 0.f, 0.f};
+                float sacc[4] = {0.f, 0.f, 0.f, 0.f};
                 const int mi = lane >> 3;
-                const int lrow = rb + ((mi >> 1) << 3) + (lane & 7);
+                const int lrow = rb + ((mi & 1) << 3) + (lane & 7);
 #pragma unroll
                 for (int ks = 0; ks < 8; ks++) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(ring_s + so + sw_off(lrow, 2 * ks + (mi & 1)), b0, b1, b2, b3);
-                    mma16816(s0a, qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
-                    mma16816(s1a, qa[ks][0], 0u, qa[ks][1], 0u, b2, b3);
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(ring_s + so + sw_off(lrow, 2 * ks + (mi >> 1)), a0, a1, a2, a3);
+                    mma16816(sacc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
                 }
-                if (gq < G) {
-                    const float xv[4] = {s0a[0], s0a[1], s1a[0], s1a[1]};
-                    const int sl[4] = {2 * tq, 2 * tq + 1, 8 + 2 * tq, 9 + 2 * tq};
 #pragma unroll
-                    for (int e = 0; e < 4; e++) {
-                        const int li = t * kTile + rb + sl[e];
-                        if (li < nrows) {
-                            const bool isnew = (s0 + li == victim);
-                            const float lnp = (!isnew && a.votes) ? logf((float)a.votes[ubase + s0 + li]) : 0.f;
-                            const float x = xv[e] * rs + lnp;
-                            XS(gq, li) = x;
-                            mxq = fmaxf(mxq, x);
+                for (int hf = 0; hf < 2; hf++) {           // slot gq, then gq + 8
+                    const int li = t * kTile + rb + gq + 8 * hf;
+                    if (li < nrows) {
+                        const bool isnew = (s0 + li == victim);
+                        const float lnp = (!isnew && a.votes) ? logf((float)a.votes[ubase + s0 + li]) : 0.f;
+                        if (h0 < G) {
+                            const float x = sacc[2 * hf] * rs + lnp;
+                            XS(h0, li) = x;
+                            mx0 = fmaxf(mx0, x);
+                        }
+                        if (h1 < G) {
+                            const float x = sacc[2 * hf + 1] * rs + lnp;
+                            XS(h1, li) = x;
+                            mx1 = fmaxf(mx1, x);
                         }
                     }
                 }
@@ -516,14 +523,22 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
                 if (lane == 0) XS(h, nrows) = xv_new[h];
             }
 #pragma unroll
-            for (int h = 0; h < G; h++)
-                if (gq == h) mxq = fmaxf(mxq, xv_new[h]);
+            for (int h = 0; h < G; h++) {
+                if (h == h0) mx0 = fmaxf(mx0, xv_new[h]);
+                if (h == h1) mx1 = fmaxf(mx1, xv_new[h]);
+            }
         }
-        mxq = fmaxf(mxq, __shfl_xor_sync(kFull, mxq, 1));
-        mxq = fmaxf(mxq, __shfl_xor_sync(kFull, mxq, 2));
-        if (tq == 0 && gq < G) S.red[w][gq] = mxq;
+#pragma unroll
+        for (int m = 4; m <= 16; m <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, m));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, m));
+        }
+        if (gq == 0) {
+            if (h0 < G) S.red[w][h0] = mx0;
+            if (h1 < G) S.red[w][h1] = mx1;
+        }
         consumer_sync();
-        float Mg = -INFINITY;                     // CTA max of head gq
+        float Mg = -INFINITY;                     // CTA max of head gq (the head of this lane's p)
         if (gq < G)
             for (int j = 0; j < kNC; j++) Mg = fmaxf(Mg, S.red[j][gq]);
         if (tid < G) {
@@ -532,7 +547,7 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             S.pM[tid] = v;
         }
         consumer_sync();                          // S.red is reused below
-        // pass 2: O += P V
+        // pass 2: O^T += V^T P^T
         for (int t = 0; t < ntile; t++, g++) {
             const int stage = g % kStages;
             const uint32_t ph = (uint32_t)(g / kStages) & 1u;
@@ -548,55 +563,69 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
                     pv[e] = (gq < G && li < nrows) ? expf(XS(gq, li) - Mg) : 0.f;
                     lsq += pv[e];
                 }
-                uint16_t h0, l0, h1, l1, h2, l2, h3, l3;
-                split_bf16(pv[0], h0, l0);
-                split_bf16(pv[1], h1, l1);
-                split_bf16(pv[2], h2, l2);
-                split_bf16(pv[3], h3, l3);
-                const uint32_t ah0 = (uint32_t)h0 | ((uint32_t)h1 << 16), ah2 = (uint32_t)h2 | ((uint32_t)h3 << 16);
-                const uint32_t al0 = (uint32_t)l0 | ((uint32_t)l1 << 16), al2 = (uint32_t)l2 | ((uint32_t)l3 << 16);
+                uint16_t hi0, lo0, hi1, lo1, hi2, lo2, hi3, lo3;
+                split_bf16(pv[0], hi0, lo0);
+                split_bf16(pv[1], hi1, lo1);
+                split_bf16(pv[2], hi2, lo2);
+                split_bf16(pv[3], hi3, lo3);
+                const uint32_t bh0 = (uint32_t)hi0 | ((uint32_t)hi1 << 16), bh1 = (uint32_t)hi2 | ((uint32_t)hi3 << 16);
+                const uint32_t bl0 = (uint32_t)lo0 | ((uint32_t)lo1 << 16), bl1 = (uint32_t)lo2 | ((uint32_t)lo3 << 16);
                 const int mi = lane >> 3;
-                const int lrow = rb + ((mi & 1) << 3) + (lane & 7);
+                const int lrow = rb + ((mi >> 1) << 3) + (lane & 7);
 #pragma unroll
-                for (int pp = 0; pp < 8; pp++) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(ring_s + so + sw_off(lrow, 2 * pp + (mi >> 1)), b0, b1, b2, b3);
-                    mma16816(O[2 * pp], ah0, 0u, ah2, 0u, b0, b1);
-                    mma16816(O[2 * pp], al0, 0u, al2, 0u, b0, b1);
-                    mma16816(O[2 * pp + 1], ah0, 0u, ah2, 0u, b2, b3);
-                    mma16816(O[2 * pp + 1], al0, 0u, al2, 0u, b2, b3);
+                for (int mt = 0; mt < 8; mt++) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4_t(ring_s + so + sw_off(lrow, 2 * mt + (mi & 1)), a0, a1, a2, a3);
+                    mma16816(O[mt], a0, a1, a2, a3, bh0, bh1);
+                    mma16816(O[mt], a0, a1, a2, a3, bl0, bl1);
                 }
             }
             __syncwarp();
             if (lane == 0 && good) mbar_arrive(&S.empty[stage]);
         }
-        if (has_new && w == 0 && gq < G) {
-            float pnew = 0.f;
+        if (has_new && w == 0) {
+            float pn0 = 0.f, pn1 = 0.f, pnq = 0.f;
+            const float M0 = h0 < G ? S.pM[h0] : 0.f, M1 = h1 < G ? S.pM[h1] : 0.f;
 #pragma unroll
-            for (int h = 0; h < G; h++)
-                if (gq == h) pnew = expf(xv_new[h] - Mg);
-            if (tq == 0) lsq += pnew;
+            for (int h = 0; h < G; h++) {
+                const float pe = expf(xv_new[h] - S.pM[h]);
+                if (h == h0) pn0 = pe;
+                if (h == h1) pn1 = pe;
+                if (h == gq) pnq = pe;
+            }
+            (void)M0; (void)M1;
+            if (tq == 0 && gq < G) lsq += pnq;
 #pragma unroll
-            for (int n = 0; n < 16; n++) {
-                O[n][0] = fmaf(pnew, bf2f(vnew[8 * n + 2 * tq]), O[n][0]);
-                O[n][1] = fmaf(pnew, bf2f(vnew[8 * n + 2 * tq + 1]), O[n][1]);
+            for (int mt = 0; mt < 8; mt++) {
+                const float va = bf2f(vnew[16 * mt + gq]), vb = bf2f(vnew[16 * mt + gq + 8]);
+                O[mt][0] = fmaf(pn0, va, O[mt][0]);
+                O[mt][1] = fmaf(pn1, va, O[mt][1]);
+                O[mt][2] = fmaf(pn0, vb, O[mt][2]);
+                O[mt][3] = fmaf(pn1, vb, O[mt][3]);
             }
         }
         if (!good) atomicExch(&S.bad, 1);
     }
-    // reduce the p v partials of the consumer warps (fragment layout: lane
-    // (gq, tq) holds head gq, dims 8n + 2tq and + 1)
+    // reduce the p v partials of the consumer warps (O^T fragment layout:
+    // lane (gq, tq) holds dims 16 m + gq and + 8 for heads 2 tq and 2 tq + 1)
     for (int e = tid; e < G * kD; e += blockDim.x) S.po[e / kD][e % kD] = 0.f;
     lsq += __shfl_xor_sync(kFull, lsq, 1);
     lsq += __shfl_xor_sync(kFull, lsq, 2);
     __syncthreads();
-    if (w < kNC && gq < G) {
+    if (w < kNC) {
+        const int h0 = 2 * tq, h1 = 2 * tq + 1;
 #pragma unroll
-        for (int n = 0; n < 16; n++) {
-            atomicAdd(&S.po[gq][8 * n + 2 * tq], O[n][0]);
-            atomicAdd(&S.po[gq][8 * n + 2 * tq + 1], O[n][1]);
+        for (int mt = 0; mt < 8; mt++) {
+            if (h0 < G) {
+                atomicAdd(&S.po[h0][16 * mt + gq], O[mt][0]);
+                atomicAdd(&S.po[h0][16 * mt + gq + 8], O[mt][2]);
+            }
+            if (h1 < G) {
+                atomicAdd(&S.po[h1][16 * mt + gq], O[mt][1]);
+                atomicAdd(&S.po[h1][16 * mt + gq + 8], O[mt][3]);
+            }
         }
-        if (tq == 0) S.red[w][gq] = lsq;
+        if (tq == 0 && gq < G) S.red[w][gq] = lsq;
     }
     __syncthreads();
     if (tid < G) {
