@@ -158,6 +158,34 @@ def run_prefill(pc, dev, reps=5):
             "kept": int(counts.sum().item())}
 
 
+KERNEL_SOURCES = ["kv_cache_eviction_kvc_gb300/csrc/kvc_fused.cu",
+                  "kv_cache_eviction_kvc_gb300/csrc/kvc_tma.cuh",
+                  "kv_cache_eviction_kvc_gb300/csrc/kvc_common.cuh",
+                  "kv_cache_eviction_kvc_gb300/csrc/kvc_internal.h"]
+
+
+def profiled_traffic():
+    """DRAM bytes per lazy-step launch of the fused kernel on this workload
+    from the committed ncu summary, or None when the kernel sources changed
+    since the counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "fused_step_kernel_qwen3-4b.md")
+    if not os.path.exists(path):
+        return None
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    want, traffic = None, None
+    with open(path) as fh:
+        for line in fh:
+            if line.startswith("source_sha256_16:"):
+                want = line.split(":", 1)[1].strip()
+            elif line.startswith("traffic_bytes_per_launch_full:"):
+                traffic = int(line.split(":", 1)[1].strip())
+    return traffic if want == h.hexdigest()[:16] else None
+
+
 # ------------------------------------------------------------ clocks
 class ClockSampler:
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -386,7 +414,11 @@ def run_ours(args, cfg, rank, world):
         "hbm_frac": achieved / peak,
         "step1_ms": step1_ms,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak,
+                     "traffic": (profiled_traffic() if (args.batch is None and args.prefill is None
+                                                        and args.config == "C2") else None),
+                     "traffic_note": "ncu dram read+write per lazy-step launch, 864-unit capture "
+                                     "scaled by units (profiles/fused_step_kernel_qwen3-4b.md)",
                      "peak_kind": peak_kind,
                      "kernel": "fused_step_kernel (kvc_decode_step, steady state)",
                      "bytes_per_launch": avg_bytes, "avg_launch_ms": avg_launch_ms},
