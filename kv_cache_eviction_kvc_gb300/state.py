@@ -77,12 +77,14 @@ class DecodeState:
 
     # --------------------------------------------------------------- steps
     def step(self, t: int, new_pos: int, q, k_new, v_new, max_len: int, emit_probs=True,
-             stream=None):
+             stream=None, o=None):
         """Fused kvc_decode_step (falls back to the five-call sequence inside
-        the library when the step is not in the steady state)."""
+        the library when the step is not in the steady state).  `o` may name
+        another [U][G][d] fp32 output buffer."""
         self.set_kmax(max_len - self.L)
         K_.kvc_decode_step(self.params, t, new_pos, max_len, q, k_new, v_new, self.cache,
-                           self.moments, self.o, self.probs if emit_probs else None,
+                           self.moments, self.o if o is None else o,
+                           self.probs if emit_probs else None,
                            self.kmax, self.evict_idx, self.evict_pos, self.n_evict, self.ws,
                            stream)
 
