@@ -2,15 +2,19 @@
 //
 //   gram_kernel        W_g = sum of the group's W_O slices; Gram = W_g W_g^T
 //                      (fp64 accumulation, once per weight set)
-//   prefill_score      one cluster of kCS CTAs per (layer, KV head):
-//                        phase 0  row max / sum of the window logits
-//                                 (q K^T on tensor cores), merged over the
-//                                 cluster through distributed shared memory
-//                        phase 1  group-mean attention column norms
-//                                 c_i = ||A_bar[:, i]||_2
-//                        phase 2  r_i = sqrt(v_i^T Gram v_i) on tensor cores
-//                                 (Gram split into three bf16 terms)
-//                        p_i = c_i r_i; per-layer sums (fp64)
+//   pack_kernel        per (layer, KV head): the window queries and the Gram
+//                      matrix split into three bf16 terms, laid out as the
+//                      scorer's shared-memory tensor-core operands
+//   prefill_score      one cluster of kCS CTAs per (layer, KV head), 128-key
+//                      tiles, every contraction on tcgen05 with the
+//                      accumulators in tensor memory:
+//                        stat   S = Q K^T (rows x keys): row max / sum of the
+//                               window logits, merged over the cluster
+//                        norm   S^T = K Q^T (keys x rows): group-mean
+//                               attention column norms c_i = ||A_bar[:, i]||_2
+//                        val    T = V Gram (keys x dims, three bf16 terms):
+//                               r_i^2 = sum_b T[i][b] v_i[b]
+//                      p_i = c_i r_i; per-layer sums (fp64)
 //   normalize / top-K  s = p / layer sum; global radix select of the B_total
 //                      largest (ties to the smaller flat index); keep mask,
 //                      per-(layer, KV head) counts, ascending kept indices
@@ -24,6 +28,7 @@
 #include "kvc_common.cuh"
 #include "kvc_internal.h"
 #include "kvc_tma.cuh"
+#include "kvc_umma.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -32,32 +37,73 @@ namespace {
 
 constexpr int kPG = 4;               // query heads per KV head (the supported GQA group)
 constexpr int kRows = 128;           // window rows: row r = 4 j + h (j = window query, h = head)
-constexpr int kPCW = 8;              // consumer warps: 16 rows each
-constexpr int kPThreads = (kPCW + 1) * 32;
 constexpr int kCS = 8;               // CTAs per (layer, KV head)
-constexpr int kTk = 64;              // keys per ring stage
-constexpr int kPBox = kTk * 128;     // bytes of one box (64 keys x 64 dims)
-constexpr int kPStage = 2 * kPBox;   // 16 KB: 64 keys x 128 dims
-constexpr int kPStages = 4;
-constexpr int kMaxKeysCTA = 4096;
+constexpr int kTk = 128;             // keys per tile
+constexpr int kOp = 2 * kUmmaBox;    // 32 KB: one 128 x 128 bf16 operand
+constexpr int kStages = 3;           // K / V tile ring
+constexpr int kAcc = 4;              // tensor-memory accumulators of 128 fp32 columns
+constexpr int kEpiWarps = 8;         // two sets of four warps, one per tensor-memory lane quarter
+constexpr int kPThreads = (2 + kEpiWarps) * 32;
+constexpr int kPackBytes = 4 * kOp;  // [Q][Gram hi][Gram mid][Gram lo]
+// shared memory: [Q | Gram x 3 | ring], 1024-byte aligned for the swizzle
+constexpr size_t kPDyn = 1024 + (size_t)kPackBytes + (size_t)kStages * kOp;
+constexpr uint32_t kIdesc = umma_idesc_bf16(128, 128);
 
-__device__ __forceinline__ uint32_t psw(int r, int j) { return sw_off_t<kTk>(r, j); }
+enum JobKind : int { kStat = 0, kNorm = 1, kVal = 2 };
+
+// Byte offset of 16-byte chunk c (0..15) of row r (0..127) in an operand tile.
+__host__ __device__ __forceinline__ uint32_t opnd_off(int r, int c)
+{
+    return (uint32_t)((c >> 3) * kUmmaBox + (r << 7) + (((c & 7) ^ (r & 7)) << 4));
+}
+
+// The value norms of tiles t with bit 1 clear run in stage A (with the
+// statistics), the others in stage B just before the tile's column norms: both
+// stages then mix tensor-bound and exponential-bound jobs.
+__host__ __device__ __forceinline__ bool val_in_a(int t) { return ((t >> 1) & 1) == 0; }
+
+// Job order, identical for the TMA producer, the MMA issuer and the epilogue:
+// stage A walks the tiles forward, stage B backward (the K tiles read last in
+// stage A are read again first, while still in L2).
+template <class F>
+__device__ __forceinline__ int jobs_stage_a(int nt, F &&f)
+{
+    int gi = 0;
+    for (int t = 0; t < nt; t++) {
+        f(gi++, kStat, t);
+        if (val_in_a(t)) f(gi++, kVal, t);
+    }
+    return gi;
+}
+
+template <class F>
+__device__ __forceinline__ void jobs_stage_b(int nt, int gi, F &&f)
+{
+    for (int t = nt - 1; t >= 0; t--) {
+        if (!val_in_a(t)) f(gi++, kVal, t);
+        f(gi++, kNorm, t);
+    }
+}
 
 struct ScoreArgs {
-    const uint16_t *q;     // [NL][Hq][w][d]
-    const float *gram;     // [NL][Hkv][d][d]
-    float *p;              // [NL][Hkv][N]  indicator p = c r
-    double *layer_sum;     // [NL]
-    int NL, Hq, Hkv, N, w, per_cta;
+    const unsigned char *pack;   // [NL][Hkv][kPackBytes] from pack_kernel
+    float *p;                    // [NL][Hkv][N]: r^2 (after val), then p = c r
+    float2 *stats;               // [NL][Hkv][kCS][2][kRows] partial (max, sum) per row
+    double *layer_sum;           // [NL]
+    int NL, Hkv, N, w, per_cta;
+    float cs;                    // log2(e) / sqrt(d): logits in base-2 units
 };
 
 struct PfSmem {
-    uint64_t full[kPStages];
-    uint64_t empty[kPStages];
-    float pm[kRows], pl[kRows];      // this CTA's row max / sum (read by the cluster)
-    float c2[kMaxKeysCTA];           // sum_j A_bar[j, i]^2
-    float r2[kMaxKeysCTA];           // v_i^T Gram v_i
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t accf[kAcc];         // accumulator ready (MMA commit)
+    uint64_t acce[kAcc];         // accumulator drained (4 epilogue warps)
+    uint64_t opnd;               // Q and Gram operands landed
+    uint64_t fin;                // every MMA of the CTA completed
+    float2 rs[kRows];            // per row: cluster max (base 2) and 1 / sum
     double red[kPThreads / 32];
+    uint32_t tmem;
     int bad;
 };
 
@@ -68,324 +114,296 @@ prefill_score_kernel(ScoreArgs a, const __grid_constant__ CUtensorMap tmK,
     cg::cluster_group cluster = cg::this_cluster();
     const int cr = (int)cluster.block_rank();
     const int lg = blockIdx.x / kCS;
-    const int l = lg / a.Hkv, g = lg % a.Hkv;
+    const int l = lg / a.Hkv;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    const int gq = lane >> 2, tq = lane & 3;
 
-    __shared__ PfSmem S;
-    extern __shared__ __align__(128) unsigned char dyn[];
-    unsigned char *ring = reinterpret_cast<unsigned char *>(
+    __shared__ __align__(16) PfSmem S;
+    extern __shared__ __align__(1024) unsigned char dyn[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(dyn) + 1023) & ~uintptr_t(1023));
-    const uint32_t ring_s = smem_u32(ring);
+    unsigned char *ring = sm + kPackBytes;
+    const uint32_t sm_s = smem_u32(sm), ring_s = smem_u32(ring);
 
     const int N = a.N, W = a.w;
     const int k0 = min(N, cr * a.per_cta), k1 = min(N, k0 + a.per_cta);
-    const int nk = k1 - k0;
-    const int ntile = (nk + kTk - 1) / kTk;
-    const float rs = rsqrtf((float)kD);
+    const int nt = (k1 - k0 + kTk - 1) / kTk;
+    float *pout = a.p + (size_t)lg * N + k0;
 
-    for (int i = tid; i < kMaxKeysCTA; i += blockDim.x) {
-        S.c2[i] = 0.f;
-        S.r2[i] = 0.f;
-    }
     if (tid == 0) {
         S.bad = 0;
-        for (int j = 0; j < kPStages; j++) {
+        for (int j = 0; j < kStages; j++) {
             mbar_init(&S.full[j], 1);
-            mbar_init(&S.empty[j], kPCW);
+            mbar_init(&S.empty[j], 1);
         }
+        for (int j = 0; j < kAcc; j++) {
+            mbar_init(&S.accf[j], 1);
+            mbar_init(&S.acce[j], 4);
+        }
+        mbar_init(&S.opnd, 1);
+        mbar_init(&S.fin, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if (w == 1) tmem_alloc(&S.tmem, 512);
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = S.tmem;
+    double lsum = 0.0;
 
-    if (w == kPCW) {
-        // ------------------------------------------------ producer warp
-        // K tiles (phase 0), K tiles again (phase 1, mostly from L2), V tiles
-        const int row0 = (int)((size_t)lg * N + k0);
-        bool ok = true;
-        int gi = 0;
-        auto issue = [&](const CUtensorMap *map) {
-            for (int t = 0; t < ntile && ok; t++, gi++) {
-                const int stage = gi % kPStages;
-                const uint32_t ph = (uint32_t)(gi / kPStages) & 1u;
-                if (!mbar_wait(&S.empty[stage], ph ^ 1u)) { ok = false; break; }
-                mbar_expect_tx(&S.full[stage], (uint32_t)kPStage);
-                unsigned char *dst = ring + (size_t)stage * kPStage;
-                tma_2d(dst, map, 0, row0 + t * kTk, &S.full[stage]);
-                tma_2d(dst + kPBox, map, 64, row0 + t * kTk, &S.full[stage]);
-            }
-        };
-        if (lane == 0) issue(&tmK);
-        __syncwarp();
-        cluster_arrive();                 // phase-0 barrier: arrive now, wait after issuing
+    if (w == 0) {
+        // ------------------------------------------------ TMA producer
+        cluster_arrive();                 // contributes nothing to the row statistics
         if (lane == 0) {
-            issue(&tmK);
-            issue(&tmV);
+            bool ok = true;
+            int issued = 0;
+            mbar_expect_tx(&S.opnd, (uint32_t)kPackBytes);
+            const unsigned char *src = a.pack + (size_t)lg * kPackBytes;
+            for (int j = 0; j < 4; j++) bulk_g2s(sm + j * kOp, src + j * kOp, kOp, &S.opnd);
+            const int row0 = lg * N + k0;
+            auto issue = [&](int gi, int kind, int t) {
+                if (!ok) return;
+                const int s = gi % kStages;
+                const uint32_t ph = (uint32_t)(gi / kStages) & 1u;
+                if (!mbar_wait(&S.empty[s], ph ^ 1u)) { ok = false; return; }
+                mbar_expect_tx(&S.full[s], (uint32_t)kOp);
+                const CUtensorMap *map = kind == kVal ? &tmV : &tmK;
+                unsigned char *dst = ring + (size_t)s * kOp;
+                tma_2d(dst, map, 0, row0 + t * kTk, &S.full[s]);
+                tma_2d(dst + kUmmaBox, map, 64, row0 + t * kTk, &S.full[s]);
+                issued = gi + 1;
+            };
+            const int ga = jobs_stage_a(nt, issue);
+            jobs_stage_b(nt, ga, issue);
             if (!ok) {
+                // let the copies in flight land before the CTA may exit
                 atomicExch(&S.bad, 1);
-                for (int j = max(0, gi - kPStages); j < gi; j++)
-                    mbar_wait(&S.full[j % kPStages], (uint32_t)(j / kPStages) & 1u);
+                mbar_wait(&S.opnd, 0);
+                for (int j = max(0, issued - kStages); j < issued; j++)
+                    mbar_wait(&S.full[j % kStages], (uint32_t)(j / kStages) & 1u);
             }
+        }
+        __syncwarp();
+        cluster_wait();
+    } else if (w == 1) {
+        // ------------------------------------------------ MMA issuer
+        cluster_arrive();
+        if (lane == 0) {
+            bool ok = mbar_wait(&S.opnd, 0);
+            auto mma = [&](int gi, int kind, int t) {
+                (void)t;
+                if (!ok) return;
+                const int s = gi % kStages, b = gi % kAcc;
+                if (!mbar_wait(&S.full[s], (uint32_t)(gi / kStages) & 1u) ||
+                    !mbar_wait(&S.acce[b], ((uint32_t)(gi / kAcc) & 1u) ^ 1u)) {
+                    ok = false;
+                    return;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(b * 128);
+                const uint32_t tile = ring_s + (uint32_t)(s * kOp);
+                if (kind == kVal) {
+#pragma unroll 1
+                    for (int sp = 0; sp < 3; sp++) {
+                        const uint32_t g = sm_s + (uint32_t)((1 + sp) * kOp);
+#pragma unroll
+                        for (int ks = 0; ks < 8; ks++)
+                            umma_bf16(d, umma_sdesc(tile + umma_kstep(ks)),
+                                      umma_sdesc(g + umma_kstep(ks)), kIdesc, sp > 0 || ks > 0);
+                    }
+                } else {
+                    // stat: A = Q (rows), B = K tile (keys); norm: the transpose
+                    const uint32_t A = kind == kStat ? sm_s : tile;
+                    const uint32_t B = kind == kStat ? tile : sm_s;
+#pragma unroll
+                    for (int ks = 0; ks < 8; ks++)
+                        umma_bf16(d, umma_sdesc(A + umma_kstep(ks)), umma_sdesc(B + umma_kstep(ks)),
+                                  kIdesc, ks > 0);
+                }
+                umma_commit(&S.accf[b]);
+                // a K tile is free once its MMAs completed; a V tile is also
+                // read by the epilogue, which frees it
+                if (kind != kVal) umma_commit(&S.empty[s]);
+            };
+            const int ga = jobs_stage_a(nt, mma);
+            jobs_stage_b(nt, ga, mma);
+            umma_commit(&S.fin);
+            if (!mbar_wait(&S.fin, 0)) ok = false;
+            if (!ok) atomicExch(&S.bad, 1);
         }
         __syncwarp();
         cluster_wait();
     } else {
-        // ------------------------------------------------ consumers
-        // rows of this lane: r1 = 16 w + gq and r2 = r1 + 8 (same head, window + 2)
-        const int r1 = 16 * w + gq;
-        const int j1 = r1 >> 2, j2 = j1 + 2, hh = r1 & 3;
-        const int lim1 = N - W + j1, lim2 = N - W + j2;     // last visible key of each row
-        const bool v1 = j1 < W, v2 = j2 < W;
-        uint32_t qa[8][4];
-        {
-            const uint32_t *q32 = reinterpret_cast<const uint32_t *>(a.q);
-            const size_t hq = (size_t)l * a.Hq + (size_t)g * kPG + hh;
-            const size_t b1 = ((hq * W + j1) * kD) >> 1, b2 = ((hq * W + j2) * kD) >> 1;
-#pragma unroll
-            for (int ks = 0; ks < 8; ks++) {
-                qa[ks][0] = v1 ? q32[b1 + 8 * ks + tq] : 0u;
-                qa[ks][1] = v2 ? q32[b2 + 8 * ks + tq] : 0u;
-                qa[ks][2] = v1 ? q32[b1 + 8 * ks + 4 + tq] : 0u;
-                qa[ks][3] = v2 ? q32[b2 + 8 * ks + 4 + tq] : 0u;
-            }
-        }
+        // ------------------------------------------------ epilogue warps
+        const int set = (w - 2) >> 2;              // tiles t with t % 2 == set
+        const int qd = w & 3;                      // tensor-memory lane quarter
+        const int ln = 32 * qd + lane;             // row (stat) or tile key (norm, val)
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * qd) << 16);
+        const float cs = a.cs;
         bool good = true;
-        int gi = 0;
-        // S (16 rows x 64 keys) of one tile on tensor cores
-        auto qk_tile = [&](uint32_t so, float (&Sf)[8][4]) {
-#pragma unroll
-            for (int n = 0; n < 8; n++) Sf[n][0] = Sf[n][1] = Sf[n][2] = Sf[n][3] = 0.f;
-            const int mi = lane >> 3;
-#pragma unroll
-            for (int ks = 0; ks < 8; ks++) {
-#pragma unroll
-                for (int np = 0; np < 4; np++) {
-                    const int lrow = 16 * np + ((mi >> 1) << 3) + (lane & 7);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(ring_s + so + psw(lrow, 2 * ks + (mi & 1)), b0, b1, b2, b3);
-                    mma16816(Sf[2 * np], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-                    mma16816(Sf[2 * np + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
-                }
-            }
+
+        // wait for accumulator gi (uniform over the warp)
+        auto acquire = [&](int gi) {
+            bool ok = good && mbar_wait(&S.accf[gi % kAcc], (uint32_t)(gi / kAcc) & 1u);
+            good = __all_sync(kFull, ok);
+            if (good) tc_fence_after();
+            return good;
         };
-        auto acquire = [&](int &stage, uint32_t &so) {
-            stage = gi % kPStages;
-            const uint32_t ph = (uint32_t)(gi / kPStages) & 1u;
-            if (good && !mbar_wait(&S.full[stage], ph)) good = false;
-            so = (uint32_t)stage * kPStage;
-        };
-        auto release = [&](int stage) {
+        auto release = [&](int gi) {
+            tc_fence_before();
             __syncwarp();
-            if (lane == 0 && good) mbar_arrive(&S.empty[stage]);
-            gi++;
+            if (lane == 0 && good) mbar_arrive(&S.acce[gi % kAcc]);
         };
 
-        // ---------------- phase 0: row max and sum
-        float m1 = -INFINITY, s1 = 0.f, m2 = -INFINITY, s2 = 0.f;
-        for (int t = 0; t < ntile; t++) {
-            int stage;
-            uint32_t so;
-            acquire(stage, so);
-            if (good) {
-                float Sf[8][4];
-                qk_tile(so, Sf);
-                float x[8][4];
-                float tm1 = -INFINITY, tm2 = -INFINITY;
-#pragma unroll
-                for (int n = 0; n < 8; n++)
-#pragma unroll
-                    for (int e = 0; e < 2; e++) {
-                        const int key = k0 + t * kTk + 8 * n + 2 * tq + e;
-                        const bool ok = key < k1;
-                        x[n][e] = (ok && v1 && key <= lim1) ? Sf[n][e] * rs : -INFINITY;
-                        x[n][2 + e] = (ok && v2 && key <= lim2) ? Sf[n][2 + e] * rs : -INFINITY;
-                        tm1 = fmaxf(tm1, x[n][e]);
-                        tm2 = fmaxf(tm2, x[n][2 + e]);
-                    }
-                const float n1m = fmaxf(m1, tm1), n2m = fmaxf(m2, tm2);
-                if (n1m != -INFINITY) {
-                    float acc = (m1 == -INFINITY) ? 0.f : s1 * expf(m1 - n1m);
-#pragma unroll
-                    for (int n = 0; n < 8; n++)
-#pragma unroll
-                        for (int e = 0; e < 2; e++) acc += expf(x[n][e] - n1m);
-                    s1 = acc;
-                    m1 = n1m;
-                }
-                if (n2m != -INFINITY) {
-                    float acc = (m2 == -INFINITY) ? 0.f : s2 * expf(m2 - n2m);
-#pragma unroll
-                    for (int n = 0; n < 8; n++)
-#pragma unroll
-                        for (int e = 0; e < 2; e++) acc += expf(x[n][2 + e] - n2m);
-                    s2 = acc;
-                    m2 = n2m;
-                }
+        // r^2 of this lane's key: T (keys x 128 dims) against the V tile in smem
+        auto val_job = [&](int gi, int t) {
+            const int s = gi % kStages;
+            if (acquire(gi)) {
+                // the V tile is read directly: observe its TMA completion
+                bool ok = mbar_wait(&S.full[s], (uint32_t)(gi / kStages) & 1u);
+                good = __all_sync(kFull, ok);
             }
-            release(stage);
-        }
-        // merge over the 4 lanes sharing the rows
-#pragma unroll
-        for (int msk = 1; msk <= 2; msk <<= 1) {
-            const float om1 = __shfl_xor_sync(kFull, m1, msk), os1 = __shfl_xor_sync(kFull, s1, msk);
-            const float om2 = __shfl_xor_sync(kFull, m2, msk), os2 = __shfl_xor_sync(kFull, s2, msk);
-            const float nm1 = fmaxf(m1, om1), nm2 = fmaxf(m2, om2);
-            s1 = (nm1 == -INFINITY) ? 0.f
-                                    : ((m1 == -INFINITY ? 0.f : s1 * expf(m1 - nm1)) +
-                                       (om1 == -INFINITY ? 0.f : os1 * expf(om1 - nm1)));
-            s2 = (nm2 == -INFINITY) ? 0.f
-                                    : ((m2 == -INFINITY ? 0.f : s2 * expf(m2 - nm2)) +
-                                       (om2 == -INFINITY ? 0.f : os2 * expf(om2 - nm2)));
-            m1 = nm1;
-            m2 = nm2;
-        }
-        if (tq == 0) {
-            S.pm[r1] = m1; S.pl[r1] = s1;
-            S.pm[r1 + 8] = m2; S.pl[r1 + 8] = s2;
-        }
-        cluster_arrive();
-        cluster_wait();
-        // cluster-wide row statistics of this lane's two rows
-        float M1 = -INFINITY, M2 = -INFINITY;
-        for (int q = 0; q < kCS; q++) {
-            PfSmem *R = cluster.map_shared_rank(&S, q);
-            M1 = fmaxf(M1, R->pm[r1]);
-            M2 = fmaxf(M2, R->pm[r1 + 8]);
-        }
-        float Z1 = 0.f, Z2 = 0.f;
-        for (int q = 0; q < kCS; q++) {
-            PfSmem *R = cluster.map_shared_rank(&S, q);
-            if (R->pm[r1] != -INFINITY) Z1 += R->pl[r1] * expf(R->pm[r1] - M1);
-            if (R->pm[r1 + 8] != -INFINITY) Z2 += R->pl[r1 + 8] * expf(R->pm[r1 + 8] - M2);
-        }
-        const float iz1 = Z1 > 0.f ? 1.f / Z1 : 0.f, iz2 = Z2 > 0.f ? 1.f / Z2 : 0.f;
-
-        // ---------------- phase 1: group-mean column norms
-        for (int t = 0; t < ntile; t++) {
-            int stage;
-            uint32_t so;
-            acquire(stage, so);
             if (good) {
-                float Sf[8][4];
-                qk_tile(so, Sf);
+                const unsigned char *vt = ring + (size_t)s * kOp;
+                const uint32_t tb = lane_base + (uint32_t)((gi % kAcc) * 128);
+                float r2a = 0.f, r2b = 0.f;
 #pragma unroll
-                for (int n = 0; n < 8; n++)
+                for (int cb = 0; cb < 4; cb++) {
+                    float x[32];
+                    tmem_ld32(tb + 32 * cb, x);
 #pragma unroll
-                    for (int e = 0; e < 2; e++) {
-                        const int key = k0 + t * kTk + 8 * n + 2 * tq + e;
-                        const bool ok = key < k1;
-                        float pa = (ok && v1 && key <= lim1) ? expf(Sf[n][e] * rs - M1) * iz1 : 0.f;
-                        float pb = (ok && v2 && key <= lim2) ? expf(Sf[n][2 + e] * rs - M2) * iz2 : 0.f;
-                        // sum over the 4 heads of the window row (lane bits 2-3)
-                        pa += __shfl_xor_sync(kFull, pa, 4);
-                        pa += __shfl_xor_sync(kFull, pa, 8);
-                        pb += __shfl_xor_sync(kFull, pb, 4);
-                        pb += __shfl_xor_sync(kFull, pb, 8);
-                        pa *= 1.f / kPG;
-                        pb *= 1.f / kPG;
-                        float sq = pa * pa + pb * pb;
-                        sq += __shfl_xor_sync(kFull, sq, 16);   // the warp's 4 window rows
-                        if (gq == 0 && ok) atomicAdd(&S.c2[key - k0], sq);
-                    }
-            }
-            release(stage);
-        }
-
-        // ---------------- phase 2: r_i^2 = v_i^T Gram v_i
-        // warp w owns Gram rows b = 16 w .. 16 w + 15; A = Gram (b x a, three
-        // bf16 terms), B = V^T (a x keys): T^T[b][key] = sum_a Gram[b][a] v[key][a]
-        uint32_t ga[3][8][4];
-        {
-            const float *G0 = a.gram + (size_t)lg * kD * kD;
-            const int b1 = 16 * w + gq, b2 = b1 + 8;
+                    for (int c = 0; c < 4; c++) {
+                        const uint4 v = lds_v4(vt + opnd_off(ln, 4 * cb + c));
+                        float f[8];
+                        unpack8(v, f);
 #pragma unroll
-            for (int ks = 0; ks < 8; ks++) {
-                const int c0 = 16 * ks + 2 * tq;
-                const float vals[4][2] = {{G0[b1 * kD + c0], G0[b1 * kD + c0 + 1]},
-                                          {G0[b2 * kD + c0], G0[b2 * kD + c0 + 1]},
-                                          {G0[b1 * kD + c0 + 8], G0[b1 * kD + c0 + 9]},
-                                          {G0[b2 * kD + c0 + 8], G0[b2 * kD + c0 + 9]}};
-#pragma unroll
-                for (int rg = 0; rg < 4; rg++) {
-                    uint16_t t0[3], t1[3];
-                    float x0 = vals[rg][0], x1 = vals[rg][1];
-#pragma unroll
-                    for (int sp = 0; sp < 3; sp++) {
-                        const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
-                        t0[sp] = __bfloat16_as_ushort(h0);
-                        t1[sp] = __bfloat16_as_ushort(h1);
-                        x0 -= __bfloat162float(h0);
-                        x1 -= __bfloat162float(h1);
-                    }
-#pragma unroll
-                    for (int sp = 0; sp < 3; sp++)
-                        ga[sp][ks][rg] = (uint32_t)t0[sp] | ((uint32_t)t1[sp] << 16);
-                }
-            }
-        }
-        const int b1 = 16 * w + gq;
-        for (int t = 0; t < ntile; t++) {
-            int stage;
-            uint32_t so;
-            acquire(stage, so);
-            if (good) {
-                float T[8][4];
-#pragma unroll
-                for (int n = 0; n < 8; n++) T[n][0] = T[n][1] = T[n][2] = T[n][3] = 0.f;
-                const int mi = lane >> 3;
-#pragma unroll
-                for (int ks = 0; ks < 8; ks++) {
-#pragma unroll
-                    for (int np = 0; np < 4; np++) {
-                        const int lrow = 16 * np + ((mi >> 1) << 3) + (lane & 7);
-                        uint32_t b0, bb1, b2, b3;
-                        ldsm_x4(ring_s + so + psw(lrow, 2 * ks + (mi & 1)), b0, bb1, b2, b3);
-#pragma unroll
-                        for (int sp = 0; sp < 3; sp++) {
-                            mma16816(T[2 * np], ga[sp][ks][0], ga[sp][ks][1], ga[sp][ks][2],
-                                     ga[sp][ks][3], b0, bb1);
-                            mma16816(T[2 * np + 1], ga[sp][ks][0], ga[sp][ks][1], ga[sp][ks][2],
-                                     ga[sp][ks][3], b2, b3);
+                        for (int e = 0; e < 8; e += 2) {
+                            r2a = fmaf(x[8 * c + e], f[e], r2a);
+                            r2b = fmaf(x[8 * c + e + 1], f[e + 1], r2b);
                         }
                     }
                 }
-                // r^2 partial = sum over this lane's b rows of T^T[b][key] v[key][b]
-                const unsigned char *tile = ring + so;
-#pragma unroll
-                for (int n = 0; n < 8; n++)
-#pragma unroll
-                    for (int e = 0; e < 2; e++) {
-                        const int krow = 8 * n + 2 * tq + e;
-                        const uint16_t va = *reinterpret_cast<const uint16_t *>(
-                            tile + psw(krow, b1 >> 3) + (b1 & 7) * 2);
-                        const uint16_t vb = *reinterpret_cast<const uint16_t *>(
-                            tile + psw(krow, (b1 + 8) >> 3) + ((b1 + 8) & 7) * 2);
-                        float part = T[n][e] * bf2f(va) + T[n][2 + e] * bf2f(vb);
-                        part += __shfl_xor_sync(kFull, part, 4);
-                        part += __shfl_xor_sync(kFull, part, 8);
-                        part += __shfl_xor_sync(kFull, part, 16);
-                        const int key = k0 + t * kTk + krow;
-                        if (gq == 0 && key < k1) atomicAdd(&S.r2[krow + t * kTk], part);
-                    }
+                const int kl = t * kTk + ln;
+                if (k0 + kl < k1) pout[kl] = r2a + r2b;
             }
-            release(stage);
+            release(gi);
+            // every warp of the set has read the V tile: free its ring stage
+            asm volatile("bar.sync %0, 128;" ::"r"(2 + set) : "memory");
+            if ((w & 3) == 2 && lane == 0 && good) mbar_arrive(&S.empty[s]);
+        };
+
+        // ---------------- stage A: row statistics of row ln (base-2 logits)
+        const int jr = ln >> 2;
+        const int lim = N - W + jr;                // last key window row jr sees
+        float m = -INFINITY, sum = 0.f;
+        auto stat_job = [&](int gi, int t) {
+            if (acquire(gi)) {
+                const uint32_t tb = lane_base + (uint32_t)((gi % kAcc) * 128);
+                const int kbase = k0 + t * kTk;
+                const bool interior = kbase + kTk <= k1 && kbase + kTk - 1 <= N - W;
+#pragma unroll
+                for (int cb = 0; cb < 4; cb++) {
+                    float x[32];
+                    tmem_ld32(tb + 32 * cb, x);
+                    if (!interior) {
+#pragma unroll
+                        for (int i = 0; i < 32; i++) {
+                            const int key = kbase + 32 * cb + i;
+                            if (key >= k1 || key > lim) x[i] = -INFINITY;
+                        }
+                    }
+                    float mx = x[0];
+#pragma unroll
+                    for (int i = 1; i < 32; i++) mx = fmaxf(mx, x[i]);
+                    if (mx != -INFINITY) {
+                        const float mn = fmaxf(m, mx * cs);
+                        float e0 = 0.f, e1 = 0.f, e2 = 0.f, e3 = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4) {
+                            e0 += ex2_approx(fmaf(x[i], cs, -mn));
+                            e1 += ex2_approx(fmaf(x[i + 1], cs, -mn));
+                            e2 += ex2_approx(fmaf(x[i + 2], cs, -mn));
+                            e3 += ex2_approx(fmaf(x[i + 3], cs, -mn));
+                        }
+                        sum = sum * ex2_approx(m - mn) + ((e0 + e1) + (e2 + e3));
+                        m = mn;
+                    }
+                }
+            }
+            release(gi);
+        };
+        const int ga = jobs_stage_a(nt, [&](int gi, int kind, int t) {
+            if ((t & 1) != set) return;
+            if (kind == kStat) stat_job(gi, t);
+            else val_job(gi, t);
+        });
+        // this set's partial statistics of row ln -> global, then the cluster
+        // barrier publishes them to the other CTAs of the (layer, KV head)
+        a.stats[(((size_t)lg * kCS + cr) * 2 + set) * kRows + ln] = make_float2(m, sum);
+        cluster_arrive();
+        cluster_wait();
+        if (set == 0) {
+            const float2 *st = a.stats + (size_t)lg * kCS * 2 * kRows + ln;
+            float M = -INFINITY;
+            for (int c = 0; c < 2 * kCS; c++) M = fmaxf(M, __ldcg(st + (size_t)c * kRows).x);
+            float Z = 0.f;
+            for (int c = 0; c < 2 * kCS; c++) {
+                const float2 v = __ldcg(st + (size_t)c * kRows);
+                if (v.x != -INFINITY) Z += v.y * ex2_approx(v.x - M);
+            }
+            // rows past the window (zero queries) and empty rows contribute 0
+            const bool live = jr < W && M != -INFINITY && Z > 0.f;
+            S.rs[ln] = live ? make_float2(M, 1.f / Z) : make_float2(0.f, 0.f);
         }
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+
+        // ---------------- stage B: column norms, p = c r
+        const float4 *rs4 = reinterpret_cast<const float4 *>(S.rs);
+        auto norm_job = [&](int gi, int t) {
+            if (acquire(gi)) {
+                const uint32_t tb = lane_base + (uint32_t)((gi % kAcc) * 128);
+                const int kl = t * kTk + ln;
+                const int jmin = k0 + kl - (N - W);     // window rows j < jmin do not see the key
+                float c2a = 0.f, c2b = 0.f;
+#pragma unroll
+                for (int cb = 0; cb < 4; cb++) {
+                    float x[32];
+                    tmem_ld32(tb + 32 * cb, x);
+#pragma unroll
+                    for (int jj = 0; jj < 8; jj++) {
+                        const float4 A = rs4[16 * cb + 2 * jj], B = rs4[16 * cb + 2 * jj + 1];
+                        float sh = ex2_approx(fmaf(x[4 * jj], cs, -A.x)) * A.y;
+                        sh = fmaf(ex2_approx(fmaf(x[4 * jj + 1], cs, -A.z)), A.w, sh);
+                        sh = fmaf(ex2_approx(fmaf(x[4 * jj + 2], cs, -B.x)), B.y, sh);
+                        sh = fmaf(ex2_approx(fmaf(x[4 * jj + 3], cs, -B.z)), B.w, sh);
+                        sh = (8 * cb + jj >= jmin) ? sh : 0.f;
+                        if (jj & 1) c2b = fmaf(sh, sh, c2b);
+                        else c2a = fmaf(sh, sh, c2a);
+                    }
+                }
+                if (k0 + kl < k1) {
+                    const float r2 = pout[kl];
+                    const float pv = sqrtf((c2a + c2b) * (1.f / (kPG * kPG))) * sqrtf(fmaxf(r2, 0.f));
+                    pout[kl] = pv;
+                    lsum += (double)pv;
+                }
+            }
+            release(gi);
+        };
+        jobs_stage_b(nt, ga, [&](int gi, int kind, int t) {
+            if ((t & 1) != set) return;
+            if (kind == kNorm) norm_job(gi, t);
+            else val_job(gi, t);
+        });
         if (!good) atomicExch(&S.bad, 1);
     }
     __syncthreads();
-    // ---------------- p = c r and the layer's partial sum
-    double part = 0.0;
-    float *pout = a.p + (size_t)lg * N + k0;
-    for (int i = tid; i < nk; i += blockDim.x) {
-        const float c = sqrtf(S.c2[i]);
-        const float r = sqrtf(fmaxf(S.r2[i], 0.f));
-        const float pv = c * r;
-        pout[i] = pv;
-        part += (double)pv;
+    if (w == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
     }
+    // the layer's partial sum of p
 #pragma unroll
-    for (int m = 16; m > 0; m >>= 1) part += __shfl_xor_sync(kFull, part, m);
-    if (lane == 0) S.red[w] = part;
+    for (int msk = 16; msk > 0; msk >>= 1) lsum += __shfl_xor_sync(kFull, lsum, msk);
+    if (lane == 0) S.red[w] = lsum;
     __syncthreads();
     if (tid == 0) {
         double s = 0.0;
@@ -393,8 +411,54 @@ prefill_score_kernel(ScoreArgs a, const __grid_constant__ CUtensorMap tmK,
         atomicAdd(&a.layer_sum[l], s);
         if (S.bad) a.layer_sum[l] = __longlong_as_double(0x7ff8000000000000ll);   // NaN: timed out
     }
-    cluster_arrive();              // no CTA leaves while another may read its partials
-    cluster_wait();
+}
+
+// --------------------------------------------------------------- operands
+// Per (layer, KV head): the 128 window rows (row 4 j + h = query head h of
+// the group at window position j; zero past the window) and the three bf16
+// terms of the Gram matrix (hi + mid + lo carries its fp32 value), each a
+// 128 x 128 K-major tile in the layout of a 128-byte-swizzled TMA load.
+__global__ void __launch_bounds__(256) pack_kernel(const uint16_t *q, const float *gram,
+                                                   unsigned char *pack, int Hq, int Hkv, int W)
+{
+    const int lg = blockIdx.x, l = lg / Hkv, g = lg % Hkv;
+    unsigned char *dst = pack + (size_t)lg * kPackBytes;
+    for (int e = threadIdx.x; e < kRows * 16; e += blockDim.x) {
+        const int r = e >> 4, c = e & 15, j = r >> 2, h = r & 3;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (j < W) {
+            const uint32_t *src = reinterpret_cast<const uint32_t *>(
+                q + (((size_t)l * Hq + (size_t)g * kPG + h) * W + j) * kD + 8 * c);
+            v = make_uint4(src[0], src[1], src[2], src[3]);
+        }
+        *reinterpret_cast<uint4 *>(dst + opnd_off(r, c)) = v;
+    }
+    const float *G0 = gram + (size_t)lg * kD * kD;
+    for (int e = threadIdx.x; e < kD * 16; e += blockDim.x) {
+        const int b = e >> 4, c = e & 15;
+        float x[8];
+        const float4 lo = *reinterpret_cast<const float4 *>(G0 + (size_t)b * kD + 8 * c);
+        const float4 hi = *reinterpret_cast<const float4 *>(G0 + (size_t)b * kD + 8 * c + 4);
+        x[0] = lo.x; x[1] = lo.y; x[2] = lo.z; x[3] = lo.w;
+        x[4] = hi.x; x[5] = hi.y; x[6] = hi.z; x[7] = hi.w;
+        uint32_t t[3][4];
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+            float x0 = x[i], x1 = x[i + 1];
+#pragma unroll
+            for (int sp = 0; sp < 3; sp++) {
+                const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
+                t[sp][i >> 1] = (uint32_t)__bfloat16_as_ushort(h0) |
+                                ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+                x0 -= __bfloat162float(h0);
+                x1 -= __bfloat162float(h1);
+            }
+        }
+#pragma unroll
+        for (int sp = 0; sp < 3; sp++)
+            *reinterpret_cast<uint4 *>(dst + (size_t)(1 + sp) * kOp + opnd_off(b, c)) =
+                make_uint4(t[sp][0], t[sp][1], t[sp][2], t[sp][3]);
+    }
 }
 
 // --------------------------------------------------------------- Gram
@@ -605,6 +669,8 @@ __global__ void __launch_bounds__(kTkBlock) topk_write_kernel(const float *s, in
 struct PfWs {
     float *p;
     double *layer_sum;
+    unsigned char *pack;
+    float2 *stats;
     TopkState *st;
     unsigned *hist;
     int *lt, *eq;
@@ -626,6 +692,8 @@ PfWs pf_layout(int NL, int Hkv, int N, void *base)
     };
     w.p = reinterpret_cast<float *>(take((size_t)M * 4));
     w.layer_sum = reinterpret_cast<double *>(take((size_t)NL * 8));
+    w.pack = reinterpret_cast<unsigned char *>(take((size_t)NL * Hkv * kPackBytes));
+    w.stats = reinterpret_cast<float2 *>(take((size_t)NL * Hkv * kCS * 2 * kRows * sizeof(float2)));
     w.st = reinterpret_cast<TopkState *>(take(sizeof(TopkState)));
     w.hist = reinterpret_cast<unsigned *>(take(256 * 4));
     w.lt = reinterpret_cast<int *>(take((size_t)nblk * 4));
@@ -694,12 +762,11 @@ kvc_status kvc_prefill_score(int32_t NL, int32_t Hq, int32_t Hkv, int32_t d, int
     PF_CHECK(B_total >= 0 && B_total <= M, KVC_ERR_INVALID_ARG,
              "kvc_prefill_score: B_total = %lld outside [0, %lld]", (long long)B_total, (long long)M);
     const int per_cta = ((N + kCS - 1) / kCS + kTk - 1) / kTk * kTk;
-    PF_CHECK(per_cta <= kMaxKeysCTA, KVC_ERR_UNSUPPORTED,
-             "kvc_prefill_score: N = %d too long (at most %d)", N, kCS * kMaxKeysCTA);
     PF_CHECK(q_win && K && V && Gram && keep, KVC_ERR_INVALID_ARG,
              "kvc_prefill_score: q_win, K, V, Gram and keep are required");
-    PF_CHECK(((uintptr_t)K & 15u) == 0 && ((uintptr_t)V & 15u) == 0 && ((uintptr_t)q_win & 3u) == 0,
-             KVC_ERR_INVALID_ARG, "kvc_prefill_score: K, V must be 16-byte aligned");
+    PF_CHECK(((uintptr_t)K & 15u) == 0 && ((uintptr_t)V & 15u) == 0 && ((uintptr_t)Gram & 15u) == 0 &&
+                 ((uintptr_t)q_win & 3u) == 0,
+             KVC_ERR_INVALID_ARG, "kvc_prefill_score: K, V, Gram must be 16-byte aligned, q_win 4-byte");
     PfWs pw = pf_layout(NL, Hkv, N, nullptr);
     PF_CHECK(ws != nullptr && ws_bytes >= pw.bytes && ((uintptr_t)ws & 255u) == 0, KVC_ERR_WORKSPACE,
              "kvc_prefill_score: workspace of %zu bytes (256-byte aligned) required", pw.bytes);
@@ -709,7 +776,7 @@ kvc_status kvc_prefill_score(int32_t NL, int32_t Hq, int32_t Hkv, int32_t d, int
 
     CUtensorMap tmK, tmV;
     const uint64_t rows = (uint64_t)NL * Hkv * N;
-    PF_CHECK(rows < (1ull << 31), KVC_ERR_UNSUPPORTED, "kvc_prefill_score: too many rows");
+    PF_CHECK(rows + kTk < (1ull << 31), KVC_ERR_UNSUPPORTED, "kvc_prefill_score: too many rows");
     PF_CHECK(make_row_map(&tmK, K, rows, kTk) && make_row_map(&tmV, V, rows, kTk), KVC_ERR_CUDA,
              "kvc_prefill_score: tensor map encoding failed");
     kvc_status s = pf_cuda(cudaMemsetAsync(pw.layer_sum, 0, (size_t)NL * 8, st), "memset");
@@ -723,15 +790,18 @@ kvc_status kvc_prefill_score(int32_t NL, int32_t Hq, int32_t Hkv, int32_t d, int
         if (s != KVC_OK) return s;
     }
 
-    ScoreArgs a{q_win, Gram, pbuf, pw.layer_sum, NL, Hq, Hkv, N, w, per_cta};
-    const size_t dyn = 1024 + (size_t)kPStages * kPStage;
-    cudaError_t e = cudaFuncSetAttribute(prefill_score_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+    pack_kernel<<<NL * Hkv, 256, 0, st>>>(q_win, Gram, pw.pack, Hq, Hkv, w);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return pf_cuda(e, "kvc_prefill_score pack launch");
+    ScoreArgs a{pw.pack, pbuf, pw.stats, pw.layer_sum, NL, Hkv, N, w, per_cta,
+                (float)(1.4426950408889634 / sqrt((double)kD))};
+    e = cudaFuncSetAttribute(prefill_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kPDyn);
     if (e != cudaSuccess) return pf_cuda(e, "kvc_prefill_score attribute");
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(NL * Hkv * kCS);
     cfg.blockDim = dim3(kPThreads);
-    cfg.dynamicSmemBytes = dyn;
+    cfg.dynamicSmemBytes = kPDyn;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
