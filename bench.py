@@ -91,7 +91,7 @@ def step_bytes(cfg, refresh: bool, emit_probs: bool) -> int:
 
 def prefill_bytes(pc) -> int:
     """Algorithmic HBM bytes of one prefill scoring call: K and V once, the
-    window queries, the Gram matrices, the indicator written, then read and
+    window queries, the value-norm factors, the indicator written, then read and
     written by the normalization, read by the four radix passes, the count
     and the write pass, and the keep mask / counts / indices written."""
     M = pc.NL * pc.Hkv * pc.N
@@ -105,8 +105,9 @@ def prefill_bytes(pc) -> int:
 
 def prefill_flops(pc) -> int:
     """Algorithmic tensor-core FLOPs: q K^T of the G*w window rows once and
-    v Gram once (the second q K^T pass and the three-term Gram split are
-    implementation choices on top)."""
+    the d x d value-norm factor applied to every v once (the second q K^T pass
+    and the three-term split of the factor are implementation choices on
+    top)."""
     M = pc.NL * pc.Hkv * pc.N
     return 2 * M * pc.G * pc.w * pc.d + 2 * M * pc.d * pc.d
 
@@ -116,11 +117,11 @@ def run_prefill(pc, dev, reps=5):
     from kv_cache_eviction_kvc_gb300 import kvc, workloads as W
     inp = W.gen_prefill_scorer(pc, dev, 0)
     NL, Hq, Hkv, d, N, w, B = pc.NL, pc.Hq, pc.Hkv, pc.d, pc.N, pc.w, pc.B_total
-    gram = torch.empty(NL, Hkv, d, d, dtype=torch.float32, device=dev)
+    R = torch.empty(NL, Hkv, d, d, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    kvc.kvc_prefill_prepare(NL, Hq, Hkv, d, pc.D, inp["W_O"], gram)
+    kvc.kvc_prefill_prepare(NL, Hq, Hkv, d, pc.D, inp["W_O"], R)
     e1.record(stream)
     torch.cuda.synchronize()
     prep_ms = e0.elapsed_time(e1)
@@ -131,7 +132,7 @@ def run_prefill(pc, dev, reps=5):
     idx = torch.empty(max(B, 1), dtype=torch.int64, device=dev)
 
     def call():
-        kvc.kvc_prefill_score(NL, Hq, Hkv, d, N, w, B, 1, inp["q_win"], inp["K"], inp["V"], gram,
+        kvc.kvc_prefill_score(NL, Hq, Hkv, d, N, w, B, 1, inp["q_win"], inp["K"], inp["V"], R,
                               scores, keep, counts, idx, ws)
     for _ in range(2):
         call()

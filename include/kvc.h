@@ -331,19 +331,20 @@ KVC_API kvc_status kvc_decode_attend_noalloc(const kvc_params *p, int32_t t,
 /* ------------------------------------------------------------------ */
 
 /*
- * kvc_prefill_prepare -- per-group Gram matrices of the output projection,
- * once per weight set.
+ * kvc_prefill_prepare -- per-group value-norm factors of the output
+ * projection, once per weight set.
  *
  * Defined by: LaProx key design 1 (Output = sum_h A^h (V^h W_O^h)) and its
  * GQA group-mean paragraph.  Reading: the group's attention is the mean over
  * its query heads, so the group's product is A_bar V_g W_g with
  * W_g = sum of W_O^h over the group's heads (W_O^h = rows [h d, (h+1) d)).
- * Gram[l][g] = W_g W_g^T, accumulated in fp64 and stored fp32, so that
- * ||(V W_g)[i,:]||^2 = v_i^T Gram v_i.
- * W_O [NL][Hq*d][D] bf16; Gram [NL][Hkv][d][d] fp32.
+ * Gram = W_g W_g^T is accumulated in fp64 and factored in fp64 by pivoted
+ * Cholesky; R[l][g] (d x d, fp32) satisfies R^T R = Gram, so that
+ * ||(V W_g)[i,:]||_2 = ||R v_i||_2 (a sum of squares, free of cancellation).
+ * W_O [NL][Hq*d][D] bf16; R [NL][Hkv][d][d] fp32, 16-byte aligned.
  */
 KVC_API kvc_status kvc_prefill_prepare(int32_t NL, int32_t Hq, int32_t Hkv, int32_t d,
-                               int32_t D, const uint16_t *W_O, float *Gram,
+                               int32_t D, const uint16_t *W_O, float *R,
                                void *stream);
 
 /* Bytes of workspace kvc_prefill_score needs. */
@@ -361,20 +362,24 @@ KVC_API size_t kvc_prefill_workspace_size(int32_t NL, int32_t Hkv, int32_t N,
  * sec A4).
  *   window query j (0..w-1) sits at position N - w + j and sees keys
  *   0..N-w+j; A^h = row softmax of q K^T / sqrt(d); A_bar = mean over the
- *   group's G heads; c_i = ||A_bar[:, i]||_2; r_i = sqrt(v_i^T Gram v_i);
+ *   group's G heads; c_i = ||A_bar[:, i]||_2; r_i = ||R v_i||_2;
  *   p = c r; s = p / (sum of p over the layer's heads and tokens) when
  *   normalize != 0, else s = p; keep the B_total largest s over all
  *   (l, g, i), equal scores kept in ascending flat index (l*Hkv + g)*N + i.
- * q_win [NL][Hq][w][d], K, V [NL][Hkv][N][d] bf16; Gram from
- * kvc_prefill_prepare.  Outputs: scores [NL][Hkv][N] fp32, keep
- * [NL][Hkv][N] uint8 (0/1), counts [NL][Hkv] int32, idx [B_total] int64 kept
- * flat indices ascending.  Any output except keep may be NULL.
+ * q_win [NL][Hq][w][d] bf16 (4-byte aligned), K, V [NL][Hkv][N][d] bf16
+ * (16-byte aligned); R from kvc_prefill_prepare.  Outputs: scores
+ * [NL][Hkv][N] fp32, keep [NL][Hkv][N] uint8 (0/1), counts [NL][Hkv] int32,
+ * idx [B_total] int64 kept flat indices ascending.  Any output except keep
+ * may be NULL.  Supported: d = 128, Hq = 4 Hkv, 1 <= w <= min(32, N),
+ * NL * Hkv * N + 128 < 2^31 (else KVC_ERR_UNSUPPORTED).  ws: device memory of
+ * kvc_prefill_workspace_size bytes, 256-byte aligned (KVC_ERR_WORKSPACE).
+ * A kernel wait that ran out (a fault) leaves NaN scores.
  */
 KVC_API kvc_status kvc_prefill_score(int32_t NL, int32_t Hq, int32_t Hkv, int32_t d,
                              int32_t N, int32_t w, int64_t B_total,
                              int32_t normalize, const uint16_t *q_win,
                              const uint16_t *K, const uint16_t *V,
-                             const float *Gram, float *scores, uint8_t *keep,
+                             const float *R, float *scores, uint8_t *keep,
                              int32_t *counts, int64_t *idx, void *ws,
                              size_t ws_bytes, void *stream);
 

@@ -1,20 +1,25 @@
 // kvc_prefill.cu -- LaProx prefill scorer (sm_103a).
 //
-//   gram_kernel        W_g = sum of the group's W_O slices; Gram = W_g W_g^T
-//                      (fp64 accumulation, once per weight set)
-//   pack_kernel        per (layer, KV head): the window queries and the Gram
-//                      matrix split into three bf16 terms, laid out as the
-//                      scorer's shared-memory tensor-core operands
-//   prefill_score      one cluster of kCS CTAs per (layer, KV head), 128-key
-//                      tiles, every contraction on tcgen05 with the
-//                      accumulators in tensor memory:
+//   factor_kernel      W_g = sum of the group's W_O slices; Gram = W_g W_g^T
+//                      in fp64 and its pivoted Cholesky factor R (R^T R =
+//                      Gram), once per weight set
+//   pack_kernel        per (layer, KV head): the window queries and R split
+//                      into three bf16 terms, laid out as the scorer's
+//                      shared-memory tensor-core operands
+//   prefill_val        r_i^2 = ||(V W_g)[i, :]||^2 = sum_b T[i][b]^2 with
+//                      T = V R^T (keys x dims, R as three bf16 terms), 32
+//                      key tiles of 128 per CTA
+//   prefill_attn       one cluster of kCS CTAs per (layer, KV head), 128-key
+//                      tiles:
 //                        stat   S = Q K^T (rows x keys): row max / sum of the
 //                               window logits, merged over the cluster
 //                        norm   S^T = K Q^T (keys x rows): group-mean
 //                               attention column norms c_i = ||A_bar[:, i]||_2
-//                        val    T = V Gram (keys x dims, three bf16 terms):
-//                               r_i^2 = sum_b T[i][b] v_i[b]
 //                      p_i = c_i r_i; per-layer sums (fp64)
+//                      Both kernels: every contraction on tcgen05 (128 x 128
+//                      x 128 bf16, fp32 accumulators in tensor memory), a TMA
+//                      producer warp, one MMA-issuing thread, epilogue warps
+//                      reading the accumulators by lane quarter.
 //   normalize / top-K  s = p / layer sum; global radix select of the B_total
 //                      largest (ties to the smaller flat index); keep mask,
 //                      per-(layer, KV head) counts, ascending kept indices
@@ -24,6 +29,10 @@
 // MomentKV's experimental setup).
 #include <cooperative_groups.h>
 #include <math.h>
+
+#include <algorithm>
+#include <cstddef>
+#include <mutex>
 
 #include "kvc_common.cuh"
 #include "kvc_internal.h"
@@ -37,19 +46,22 @@ namespace {
 
 constexpr int kPG = 4;               // query heads per KV head (the supported GQA group)
 constexpr int kRows = 128;           // window rows: row r = 4 j + h (j = window query, h = head)
-constexpr int kCS = 8;               // CTAs per (layer, KV head)
+constexpr int kCS = 8;               // CTAs per (layer, KV head) in the attention kernel
 constexpr int kTk = 128;             // keys per tile
 constexpr int kOp = 2 * kUmmaBox;    // 32 KB: one 128 x 128 bf16 operand
-constexpr int kStages = 3;           // K / V tile ring
 constexpr int kAcc = 4;              // tensor-memory accumulators of 128 fp32 columns
-constexpr int kEpiWarps = 8;         // two sets of four warps, one per tensor-memory lane quarter
-constexpr int kPThreads = (2 + kEpiWarps) * 32;
-constexpr int kPackBytes = 4 * kOp;  // [Q][Gram hi][Gram mid][Gram lo]
-// shared memory: [Q | Gram x 3 | ring], 1024-byte aligned for the swizzle
-constexpr size_t kPDyn = 1024 + (size_t)kPackBytes + (size_t)kStages * kOp;
+constexpr int kPackBytes = 4 * kOp;  // [Q][R hi][R mid][R lo]
 constexpr uint32_t kIdesc = umma_idesc_bf16(128, 128);
 
-enum JobKind : int { kStat = 0, kNorm = 1, kVal = 2 };
+// attention kernel: [Q (two buffers) | ring of K tiles]
+constexpr int kAStages = 5;
+constexpr int kAEpiWarps = 8;        // two sets of four warps, one per tensor-memory lane quarter
+constexpr int kAThreads = (2 + kAEpiWarps) * 32;
+constexpr size_t kADyn = 1024 + (size_t)2 * kOp + (size_t)kAStages * kOp;
+// value-norm kernel: [R x 3 | ring of V tiles]
+constexpr int kVStages = 4;
+constexpr int kVThreads = (2 + 4 + 1) * 32;   // producer, MMA, 4 epilogue, scheduler
+constexpr size_t kVDyn = 1024 + (size_t)3 * kOp + (size_t)kVStages * kOp;
 
 // Byte offset of 16-byte chunk c (0..15) of row r (0..127) in an operand tile.
 __host__ __device__ __forceinline__ uint32_t opnd_off(int r, int c)
@@ -57,81 +69,73 @@ __host__ __device__ __forceinline__ uint32_t opnd_off(int r, int c)
     return (uint32_t)((c >> 3) * kUmmaBox + (r << 7) + (((c & 7) ^ (r & 7)) << 4));
 }
 
-// The value norms of tiles t with bit 1 clear run in stage A (with the
-// statistics), the others in stage B just before the tile's column norms: both
-// stages then mix tensor-bound and exponential-bound jobs.
-__host__ __device__ __forceinline__ bool val_in_a(int t) { return ((t >> 1) & 1) == 0; }
-
-// Job order, identical for the TMA producer, the MMA issuer and the epilogue:
-// stage A walks the tiles forward, stage B backward (the K tiles read last in
-// stage A are read again first, while still in L2).
-template <class F>
-__device__ __forceinline__ int jobs_stage_a(int nt, F &&f)
-{
-    int gi = 0;
-    for (int t = 0; t < nt; t++) {
-        f(gi++, kStat, t);
-        if (val_in_a(t)) f(gi++, kVal, t);
+struct Ring {
+    // shared by the producer, the MMA issuer and the epilogue: job gi uses
+    // ring stage gi % stages and accumulator gi % kAcc
+    static __device__ __forceinline__ uint32_t stage_parity(int gi, int stages)
+    {
+        return (uint32_t)(gi / stages) & 1u;
     }
-    return gi;
-}
+    static __device__ __forceinline__ uint32_t acc_parity(int gi) { return (uint32_t)(gi / kAcc) & 1u; }
+};
 
-template <class F>
-__device__ __forceinline__ void jobs_stage_b(int nt, int gi, F &&f)
-{
-    for (int t = nt - 1; t >= 0; t--) {
-        if (!val_in_a(t)) f(gi++, kVal, t);
-        f(gi++, kNorm, t);
-    }
-}
-
-struct ScoreArgs {
+// =============================================================== attention
+// Persistent: gridDim.x / kCS clusters of kCS CTAs; cluster c takes the
+// (layer, KV head) items c, c + nclu, ...; within an item CTA cr owns keys
+// [cr per_cta, (cr + 1) per_cta).  Jobs of an item: stat(t) for t = 0..nt-1
+// (S = Q K_t^T, rows x keys: row max / sum), then norm(t) for t = nt-1..0
+// (S^T = K_t Q^T, keys x rows: column norms; the K tiles read last in the
+// first pass are read again first, from L2).  The producer and the MMA issuer
+// run on across items; only the epilogue waits for the cluster's statistics.
+// Output: c_i^2 = ||A_bar[:, i]||^2.
+struct AttnArgs {
     const unsigned char *pack;   // [NL][Hkv][kPackBytes] from pack_kernel
-    float *p;                    // [NL][Hkv][N]: r^2 (after val), then p = c r
+    float *c2;                   // [NL][Hkv][N]: squared group-mean column norms
     float2 *stats;               // [NL][Hkv][kCS][2][kRows] partial (max, sum) per row
-    double *layer_sum;           // [NL]
-    int NL, Hkv, N, w, per_cta;
+    double *layer_sum;           // [NL]: NaN on a timed-out wait
+    int Hkv, N, w, per_cta, nitem;
     float cs;                    // log2(e) / sqrt(d): logits in base-2 units
 };
 
-struct PfSmem {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
+struct AttnSmem {
+    uint64_t full[kAStages];
+    uint64_t empty[kAStages];
     uint64_t accf[kAcc];         // accumulator ready (MMA commit)
     uint64_t acce[kAcc];         // accumulator drained (4 epilogue warps)
-    uint64_t opnd;               // Q and Gram operands landed
+    uint64_t qfull[2];           // Q buffer loaded
+    uint64_t qfree[2];           // every MMA reading the Q buffer completed
+    uint64_t ready[2];           // the cluster's partial statistics of an item are published
     uint64_t fin;                // every MMA of the CTA completed
-    float2 rs[kRows];            // per row: cluster max (base 2) and 1 / sum
-    double red[kPThreads / 32];
+    __align__(16) float2 rs[kRows];   // per row: cluster max (base 2) and 1 / sum; read as float4
     uint32_t tmem;
     int bad;
 };
+static_assert(offsetof(AttnSmem, rs) % 16 == 0, "rs is read as float4");
 
-__global__ void __launch_bounds__(kPThreads, 1)
-prefill_score_kernel(ScoreArgs a, const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV)
+__global__ void __launch_bounds__(kAThreads, 1)
+prefill_attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap tmK)
 {
     cg::cluster_group cluster = cg::this_cluster();
     const int cr = (int)cluster.block_rank();
-    const int lg = blockIdx.x / kCS;
-    const int l = lg / a.Hkv;
+    const int cid = blockIdx.x / kCS, nclu = gridDim.x / kCS;
+    const int nmine = cid < a.nitem ? (a.nitem - cid + nclu - 1) / nclu : 0;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
 
-    __shared__ __align__(16) PfSmem S;
+    __shared__ __align__(16) AttnSmem S;
     extern __shared__ __align__(1024) unsigned char dyn[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(dyn) + 1023) & ~uintptr_t(1023));
-    unsigned char *ring = sm + kPackBytes;
-    const uint32_t sm_s = smem_u32(sm), ring_s = smem_u32(ring);
+    unsigned char *ring = sm + 2 * kOp;        // [Q0 | Q1 | ring]
+    const uint32_t q_s = smem_u32(sm), ring_s = smem_u32(ring);
 
     const int N = a.N, W = a.w;
     const int k0 = min(N, cr * a.per_cta), k1 = min(N, k0 + a.per_cta);
     const int nt = (k1 - k0 + kTk - 1) / kTk;
-    float *pout = a.p + (size_t)lg * N + k0;
+    const int njob = 2 * nt;                   // per item
 
     if (tid == 0) {
         S.bad = 0;
-        for (int j = 0; j < kStages; j++) {
+        for (int j = 0; j < kAStages; j++) {
             mbar_init(&S.full[j], 1);
             mbar_init(&S.empty[j], 1);
         }
@@ -139,110 +143,118 @@ prefill_score_kernel(ScoreArgs a, const __grid_constant__ CUtensorMap tmK,
             mbar_init(&S.accf[j], 1);
             mbar_init(&S.acce[j], 4);
         }
-        mbar_init(&S.opnd, 1);
+        for (int j = 0; j < 2; j++) {
+            mbar_init(&S.qfull[j], 1);
+            mbar_init(&S.qfree[j], 1);
+            mbar_init(&S.ready[j], kCS);
+        }
         mbar_init(&S.fin, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (w == 1) tmem_alloc(&S.tmem, 512);
     __syncthreads();
+    // peers arrive on this CTA's barriers: all of them are initialized first
+    cluster_arrive();
+    cluster_wait();
     tc_fence_after();
     const uint32_t tmem = S.tmem;
-    double lsum = 0.0;
 
     if (w == 0) {
         // ------------------------------------------------ TMA producer
-        cluster_arrive();                 // contributes nothing to the row statistics
         if (lane == 0) {
             bool ok = true;
-            int issued = 0;
-            mbar_expect_tx(&S.opnd, (uint32_t)kPackBytes);
-            const unsigned char *src = a.pack + (size_t)lg * kPackBytes;
-            for (int j = 0; j < 4; j++) bulk_g2s(sm + j * kOp, src + j * kOp, kOp, &S.opnd);
-            const int row0 = lg * N + k0;
-            auto issue = [&](int gi, int kind, int t) {
-                if (!ok) return;
-                const int s = gi % kStages;
-                const uint32_t ph = (uint32_t)(gi / kStages) & 1u;
-                if (!mbar_wait(&S.empty[s], ph ^ 1u)) { ok = false; return; }
-                mbar_expect_tx(&S.full[s], (uint32_t)kOp);
-                const CUtensorMap *map = kind == kVal ? &tmV : &tmK;
-                unsigned char *dst = ring + (size_t)s * kOp;
-                tma_2d(dst, map, 0, row0 + t * kTk, &S.full[s]);
-                tma_2d(dst + kUmmaBox, map, 64, row0 + t * kTk, &S.full[s]);
-                issued = gi + 1;
-            };
-            const int ga = jobs_stage_a(nt, issue);
-            jobs_stage_b(nt, ga, issue);
+            int issued = 0, qloads = 0;
+            // each K tile is read twice: kept in L2 until its second read
+            const uint64_t keep = l2_policy_evict_last(), once = l2_policy_evict_first();
+            for (int ii = 0; ii < nmine && ok; ii++) {
+                const int lg = cid + ii * nclu, qb = ii & 1;
+                if (ii >= 2 && !mbar_wait(&S.qfree[qb], (uint32_t)((ii - 2) >> 1) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                mbar_expect_tx(&S.qfull[qb], (uint32_t)kOp);
+                bulk_g2s(sm + qb * kOp, a.pack + (size_t)lg * kPackBytes, kOp, &S.qfull[qb]);
+                qloads = ii + 1;
+                const int row0 = lg * N + k0;
+                for (int j = 0; j < njob; j++) {
+                    const int gi = ii * njob + j, s = gi % kAStages;
+                    const int t = j < nt ? j : njob - 1 - j;
+                    if (!mbar_wait(&S.empty[s], Ring::stage_parity(gi, kAStages) ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(&S.full[s], (uint32_t)kOp);
+                    unsigned char *dst = ring + (size_t)s * kOp;
+                    const uint64_t pol = j < nt ? keep : once;
+                    tma_2d_hint(dst, &tmK, 0, row0 + t * kTk, &S.full[s], pol);
+                    tma_2d_hint(dst + kUmmaBox, &tmK, 64, row0 + t * kTk, &S.full[s], pol);
+                    issued = gi + 1;
+                }
+            }
             if (!ok) {
                 // let the copies in flight land before the CTA may exit
                 atomicExch(&S.bad, 1);
-                mbar_wait(&S.opnd, 0);
-                for (int j = max(0, issued - kStages); j < issued; j++)
-                    mbar_wait(&S.full[j % kStages], (uint32_t)(j / kStages) & 1u);
+                for (int j = max(0, qloads - 2); j < qloads; j++)
+                    mbar_wait(&S.qfull[j & 1], (uint32_t)(j >> 1) & 1u);
+                for (int j = max(0, issued - kAStages); j < issued; j++)
+                    mbar_wait(&S.full[j % kAStages], Ring::stage_parity(j, kAStages));
             }
         }
         __syncwarp();
-        cluster_wait();
     } else if (w == 1) {
         // ------------------------------------------------ MMA issuer
-        cluster_arrive();
         if (lane == 0) {
-            bool ok = mbar_wait(&S.opnd, 0);
-            auto mma = [&](int gi, int kind, int t) {
-                (void)t;
-                if (!ok) return;
-                const int s = gi % kStages, b = gi % kAcc;
-                if (!mbar_wait(&S.full[s], (uint32_t)(gi / kStages) & 1u) ||
-                    !mbar_wait(&S.acce[b], ((uint32_t)(gi / kAcc) & 1u) ^ 1u)) {
+            bool ok = true;
+            for (int ii = 0; ii < nmine && ok; ii++) {
+                const int qb = ii & 1;
+                if (!mbar_wait(&S.qfull[qb], (uint32_t)(ii >> 1) & 1u)) {
                     ok = false;
-                    return;
+                    break;
                 }
-                tc_fence_after();
-                const uint32_t d = tmem + (uint32_t)(b * 128);
-                const uint32_t tile = ring_s + (uint32_t)(s * kOp);
-                if (kind == kVal) {
-#pragma unroll 1
-                    for (int sp = 0; sp < 3; sp++) {
-                        const uint32_t g = sm_s + (uint32_t)((1 + sp) * kOp);
-#pragma unroll
-                        for (int ks = 0; ks < 8; ks++)
-                            umma_bf16(d, umma_sdesc(tile + umma_kstep(ks)),
-                                      umma_sdesc(g + umma_kstep(ks)), kIdesc, sp > 0 || ks > 0);
+                const uint32_t qa = q_s + (uint32_t)(qb * kOp);
+                for (int j = 0; j < njob; j++) {
+                    const int gi = ii * njob + j, s = gi % kAStages, b = gi % kAcc;
+                    if (!mbar_wait(&S.full[s], Ring::stage_parity(gi, kAStages)) ||
+                        !mbar_wait(&S.acce[b], Ring::acc_parity(gi) ^ 1u)) {
+                        ok = false;
+                        break;
                     }
-                } else {
+                    tc_fence_after();
+                    const uint32_t d = tmem + (uint32_t)(b * 128);
+                    const uint32_t tile = ring_s + (uint32_t)(s * kOp);
                     // stat: A = Q (rows), B = K tile (keys); norm: the transpose
-                    const uint32_t A = kind == kStat ? sm_s : tile;
-                    const uint32_t B = kind == kStat ? tile : sm_s;
+                    const uint32_t A = j < nt ? qa : tile;
+                    const uint32_t B = j < nt ? tile : qa;
 #pragma unroll
                     for (int ks = 0; ks < 8; ks++)
                         umma_bf16(d, umma_sdesc(A + umma_kstep(ks)), umma_sdesc(B + umma_kstep(ks)),
                                   kIdesc, ks > 0);
+                    umma_commit(&S.accf[b]);
+                    umma_commit(&S.empty[s]);     // the tile is free once its MMAs completed
                 }
-                umma_commit(&S.accf[b]);
-                // a K tile is free once its MMAs completed; a V tile is also
-                // read by the epilogue, which frees it
-                if (kind != kVal) umma_commit(&S.empty[s]);
-            };
-            const int ga = jobs_stage_a(nt, mma);
-            jobs_stage_b(nt, ga, mma);
+                umma_commit(&S.qfree[qb]);        // ... and the Q buffer after the item
+            }
             umma_commit(&S.fin);
             if (!mbar_wait(&S.fin, 0)) ok = false;
             if (!ok) atomicExch(&S.bad, 1);
         }
         __syncwarp();
-        cluster_wait();
     } else {
         // ------------------------------------------------ epilogue warps
         const int set = (w - 2) >> 2;              // tiles t with t % 2 == set
         const int qd = w & 3;                      // tensor-memory lane quarter
-        const int ln = 32 * qd + lane;             // row (stat) or tile key (norm, val)
+        const int ln = 32 * qd + lane;             // row (stat) or tile key (norm)
         const uint32_t lane_base = tmem + ((uint32_t)(32 * qd) << 16);
         const float cs = a.cs;
+        const float4 *rs4 = reinterpret_cast<const float4 *>(S.rs);
+        const int jr = ln >> 2;
+        const int lim = N - W + jr;                // last key window row jr sees
+        const int tlast = nt - 1 - ((nt - 1 - set) & 1);   // this set's first tile of the norm pass
         bool good = true;
 
         // wait for accumulator gi (uniform over the warp)
         auto acquire = [&](int gi) {
-            bool ok = good && mbar_wait(&S.accf[gi % kAcc], (uint32_t)(gi / kAcc) & 1u);
+            bool ok = good && mbar_wait(&S.accf[gi % kAcc], Ring::acc_parity(gi));
             good = __all_sync(kFull, ok);
             if (good) tc_fence_after();
             return good;
@@ -253,146 +265,101 @@ prefill_score_kernel(ScoreArgs a, const __grid_constant__ CUtensorMap tmK,
             if (lane == 0 && good) mbar_arrive(&S.acce[gi % kAcc]);
         };
 
-        // r^2 of this lane's key: T (keys x 128 dims) against the V tile in smem
-        auto val_job = [&](int gi, int t) {
-            const int s = gi % kStages;
-            if (acquire(gi)) {
-                // the V tile is read directly: observe its TMA completion
-                bool ok = mbar_wait(&S.full[s], (uint32_t)(gi / kStages) & 1u);
-                good = __all_sync(kFull, ok);
-            }
-            if (good) {
-                const unsigned char *vt = ring + (size_t)s * kOp;
-                const uint32_t tb = lane_base + (uint32_t)((gi % kAcc) * 128);
-                float r2a = 0.f, r2b = 0.f;
-#pragma unroll
-                for (int cb = 0; cb < 4; cb++) {
-                    float x[32];
-                    tmem_ld32(tb + 32 * cb, x);
-#pragma unroll
-                    for (int c = 0; c < 4; c++) {
-                        const uint4 v = lds_v4(vt + opnd_off(ln, 4 * cb + c));
-                        float f[8];
-                        unpack8(v, f);
-#pragma unroll
-                        for (int e = 0; e < 8; e += 2) {
-                            r2a = fmaf(x[8 * c + e], f[e], r2a);
-                            r2b = fmaf(x[8 * c + e + 1], f[e + 1], r2b);
-                        }
-                    }
-                }
-                const int kl = t * kTk + ln;
-                if (k0 + kl < k1) pout[kl] = r2a + r2b;
-            }
-            release(gi);
-            // every warp of the set has read the V tile: free its ring stage
-            asm volatile("bar.sync %0, 128;" ::"r"(2 + set) : "memory");
-            if ((w & 3) == 2 && lane == 0 && good) mbar_arrive(&S.empty[s]);
-        };
+        for (int ii = 0; ii < nmine; ii++) {
+            const int lg = cid + ii * nclu;
+            const int gi0 = ii * njob;
+            float *cout = a.c2 + (size_t)lg * N + k0;
 
-        // ---------------- stage A: row statistics of row ln (base-2 logits)
-        const int jr = ln >> 2;
-        const int lim = N - W + jr;                // last key window row jr sees
-        float m = -INFINITY, sum = 0.f;
-        auto stat_job = [&](int gi, int t) {
-            if (acquire(gi)) {
-                const uint32_t tb = lane_base + (uint32_t)((gi % kAcc) * 128);
-                const int kbase = k0 + t * kTk;
-                const bool interior = kbase + kTk <= k1 && kbase + kTk - 1 <= N - W;
+            // ---------------- statistics of row ln (base-2 logits)
+            float m = -INFINITY, sum = 0.f;
+            for (int t = set; t < nt; t += 2) {
+                const int gi = gi0 + t;
+                if (acquire(gi)) {
+                    const uint32_t tb = lane_base + (uint32_t)((gi % kAcc) * 128);
+                    const int kbase = k0 + t * kTk;
+                    float x[128];
+                    tmem_ld128(tb, x);
+                    if (!(kbase + kTk <= k1 && kbase + kTk - 1 <= N - W)) {
 #pragma unroll
-                for (int cb = 0; cb < 4; cb++) {
-                    float x[32];
-                    tmem_ld32(tb + 32 * cb, x);
-                    if (!interior) {
-#pragma unroll
-                        for (int i = 0; i < 32; i++) {
-                            const int key = kbase + 32 * cb + i;
+                        for (int i = 0; i < 128; i++) {
+                            const int key = kbase + i;
                             if (key >= k1 || key > lim) x[i] = -INFINITY;
                         }
                     }
-                    float mx = x[0];
+                    float mx[8];
 #pragma unroll
-                    for (int i = 1; i < 32; i++) mx = fmaxf(mx, x[i]);
-                    if (mx != -INFINITY) {
-                        const float mn = fmaxf(m, mx * cs);
-                        float e0 = 0.f, e1 = 0.f, e2 = 0.f, e3 = 0.f;
+                    for (int k = 0; k < 8; k++) mx[k] = x[k];
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4) {
-                            e0 += ex2_approx(fmaf(x[i], cs, -mn));
-                            e1 += ex2_approx(fmaf(x[i + 1], cs, -mn));
-                            e2 += ex2_approx(fmaf(x[i + 2], cs, -mn));
-                            e3 += ex2_approx(fmaf(x[i + 3], cs, -mn));
-                        }
-                        sum = sum * ex2_approx(m - mn) + ((e0 + e1) + (e2 + e3));
+                    for (int i = 8; i < 128; i++) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+                    const float tm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                           fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                    if (tm != -INFINITY) {
+                        const float mn = fmaxf(m, tm * cs);
+                        float e[8];
+#pragma unroll
+                        for (int k = 0; k < 8; k++) e[k] = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 128; i++) e[i & 7] += ex2_approx(fmaf(x[i], cs, -mn));
+                        sum = sum * ex2_approx(m - mn) +
+                              (((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7])));
                         m = mn;
                     }
                 }
+                release(gi);
             }
-            release(gi);
-        };
-        const int ga = jobs_stage_a(nt, [&](int gi, int kind, int t) {
-            if ((t & 1) != set) return;
-            if (kind == kStat) stat_job(gi, t);
-            else val_job(gi, t);
-        });
-        // this set's partial statistics of row ln -> global, then the cluster
-        // barrier publishes them to the other CTAs of the (layer, KV head)
-        a.stats[(((size_t)lg * kCS + cr) * 2 + set) * kRows + ln] = make_float2(m, sum);
-        cluster_arrive();
-        cluster_wait();
-        if (set == 0) {
-            const float2 *st = a.stats + (size_t)lg * kCS * 2 * kRows + ln;
-            float M = -INFINITY;
-            for (int c = 0; c < 2 * kCS; c++) M = fmaxf(M, __ldcg(st + (size_t)c * kRows).x);
-            float Z = 0.f;
-            for (int c = 0; c < 2 * kCS; c++) {
-                const float2 v = __ldcg(st + (size_t)c * kRows);
-                if (v.x != -INFINITY) Z += v.y * ex2_approx(v.x - M);
+            // publish this set's partial statistics of row ln; one thread then
+            // tells every CTA of the cluster (release at cluster scope)
+            a.stats[(((size_t)lg * kCS + cr) * 2 + set) * kRows + ln] = make_float2(m, sum);
+            __threadfence();
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            if (tid == 64)
+                for (int q = 0; q < kCS; q++) mbar_arrive_remote(&S.ready[ii & 1], (uint32_t)q);
+            if (set == 0) {
+                bool ok = good && mbar_wait_cluster(&S.ready[ii & 1], (uint32_t)(ii >> 1) & 1u);
+                good = __all_sync(kFull, ok);
+                const float2 *st = a.stats + (size_t)lg * kCS * 2 * kRows + ln;
+                float2 v[2 * kCS];
+#pragma unroll
+                for (int c = 0; c < 2 * kCS; c++) v[c] = __ldcg(st + (size_t)c * kRows);
+                float M = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 2 * kCS; c++) M = fmaxf(M, v[c].x);
+                float Z = 0.f;
+#pragma unroll
+                for (int c = 0; c < 2 * kCS; c++)
+                    if (v[c].x != -INFINITY) Z += v[c].y * ex2_approx(v[c].x - M);
+                // rows past the window (zero queries) and empty rows contribute 0
+                const bool live = jr < W && M != -INFINITY && Z > 0.f;
+                S.rs[ln] = live ? make_float2(M, 1.f / Z) : make_float2(0.f, 0.f);
             }
-            // rows past the window (zero queries) and empty rows contribute 0
-            const bool live = jr < W && M != -INFINITY && Z > 0.f;
-            S.rs[ln] = live ? make_float2(M, 1.f / Z) : make_float2(0.f, 0.f);
-        }
-        asm volatile("bar.sync 1, 256;" ::: "memory");
+            asm volatile("bar.sync 1, 256;" ::: "memory");
 
-        // ---------------- stage B: column norms, p = c r
-        const float4 *rs4 = reinterpret_cast<const float4 *>(S.rs);
-        auto norm_job = [&](int gi, int t) {
-            if (acquire(gi)) {
-                const uint32_t tb = lane_base + (uint32_t)((gi % kAcc) * 128);
+            // ---------------- column norms c^2
+            for (int t = tlast; t >= 0; t -= 2) {
+                const int gi = gi0 + njob - 1 - t;
                 const int kl = t * kTk + ln;
-                const int jmin = k0 + kl - (N - W);     // window rows j < jmin do not see the key
-                float c2a = 0.f, c2b = 0.f;
+                if (acquire(gi)) {
+                    const uint32_t tb = lane_base + (uint32_t)((gi % kAcc) * 128);
+                    const int jmin = k0 + kl - (N - W);     // window rows j < jmin do not see the key
+                    float x[128];
+                    tmem_ld128(tb, x);
+                    float c2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int cb = 0; cb < 4; cb++) {
-                    float x[32];
-                    tmem_ld32(tb + 32 * cb, x);
-#pragma unroll
-                    for (int jj = 0; jj < 8; jj++) {
-                        const float4 A = rs4[16 * cb + 2 * jj], B = rs4[16 * cb + 2 * jj + 1];
-                        float sh = ex2_approx(fmaf(x[4 * jj], cs, -A.x)) * A.y;
-                        sh = fmaf(ex2_approx(fmaf(x[4 * jj + 1], cs, -A.z)), A.w, sh);
-                        sh = fmaf(ex2_approx(fmaf(x[4 * jj + 2], cs, -B.x)), B.y, sh);
-                        sh = fmaf(ex2_approx(fmaf(x[4 * jj + 3], cs, -B.z)), B.w, sh);
-                        sh = (8 * cb + jj >= jmin) ? sh : 0.f;
-                        if (jj & 1) c2b = fmaf(sh, sh, c2b);
-                        else c2a = fmaf(sh, sh, c2a);
+                    for (int j = 0; j < 32; j++) {
+                        const float4 A = rs4[2 * j], B = rs4[2 * j + 1];
+                        float sh = ex2_approx(fmaf(x[4 * j], cs, -A.x)) * A.y;
+                        sh = fmaf(ex2_approx(fmaf(x[4 * j + 1], cs, -A.z)), A.w, sh);
+                        sh = fmaf(ex2_approx(fmaf(x[4 * j + 2], cs, -B.x)), B.y, sh);
+                        sh = fmaf(ex2_approx(fmaf(x[4 * j + 3], cs, -B.z)), B.w, sh);
+                        sh = (j >= jmin) ? sh : 0.f;
+                        c2[j & 3] = fmaf(sh, sh, c2[j & 3]);
                     }
+                    if (k0 + kl < k1)
+                        cout[kl] = ((c2[0] + c2[1]) + (c2[2] + c2[3])) * (1.f / (kPG * kPG));
                 }
-                if (k0 + kl < k1) {
-                    const float r2 = pout[kl];
-                    const float pv = sqrtf((c2a + c2b) * (1.f / (kPG * kPG))) * sqrtf(fmaxf(r2, 0.f));
-                    pout[kl] = pv;
-                    lsum += (double)pv;
-                }
+                release(gi);
             }
-            release(gi);
-        };
-        jobs_stage_b(nt, ga, [&](int gi, int kind, int t) {
-            if ((t & 1) != set) return;
-            if (kind == kNorm) norm_job(gi, t);
-            else val_job(gi, t);
-        });
+        }
         if (!good) atomicExch(&S.bad, 1);
     }
     __syncthreads();
@@ -400,25 +367,331 @@ prefill_score_kernel(ScoreArgs a, const __grid_constant__ CUtensorMap tmK,
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
-    // the layer's partial sum of p
-#pragma unroll
-    for (int msk = 16; msk > 0; msk >>= 1) lsum += __shfl_xor_sync(kFull, lsum, msk);
-    if (lane == 0) S.red[w] = lsum;
-    __syncthreads();
+    if (tid == 0 && S.bad)
+        for (int ii = 0; ii < nmine; ii++)    // NaN: a wait timed out
+            a.layer_sum[(cid + ii * nclu) / a.Hkv] = __longlong_as_double(0x7ff8000000000000ll);
+    // no CTA leaves while a peer may still arrive on its barriers
+    cluster_arrive();
+    cluster_wait();
+}
+
+// =============================================================== value norms
+// Persistent, dynamically scheduled: the producer of each CTA opens a
+// (layer, KV head) item from a global counter and takes chunks of kVChunk of
+// its key tiles from the item's own counter until the item runs dry, then
+// opens the next; once every item is open it helps with whatever tiles are
+// left.  Chunks reach the MMA issuer and the epilogue through a small
+// shared-memory queue; R is reloaded only where the item changes.  Per tile: T = V_t R^T (keys x dims; R as three
+// bf16 terms accumulated into one fp32 accumulator), r^2 = sum_b T[i][b]^2.
+// Run beside the attention kernel, it takes whatever SMs that leaves free.
+constexpr int kVChunk = 4;           // tiles per chunk
+constexpr int kVQueue = 3;           // chunks posted ahead of the epilogue
+
+struct ValArgs {
+    const unsigned char *pack;   // [NL][Hkv][kPackBytes]
+    float *r2;                   // [NL][Hkv][N]
+    double *layer_sum;           // [NL]: NaN on a timed-out wait
+    int *item_next;              // next unopened item (zero before the launch)
+    int *tile_next;              // [NL Hkv] next free tile of each item (zero before the launch)
+    int NL, N, ntl;              // ntl = tiles per (layer, KV head)
+    int nitem;                   // NL Hkv
+};
+
+struct ValSmem {
+    uint64_t full[kVStages];
+    uint64_t empty[kVStages];
+    uint64_t accf[kAcc];
+    uint64_t acce[kAcc];
+    uint64_t qfull[kVQueue];     // chunk posted by the producer
+    uint64_t qfree[kVQueue];     // chunk finished by the epilogue (4 warps)
+    uint64_t rfull, rfree;       // R loaded / every MMA reading it completed
+    uint64_t fin;
+    long long chunk[kVQueue];    // first tile of the chunk, -1: no more work
+    uint32_t tmem;
+    int bad;
+};
+
+__global__ void __launch_bounds__(kVThreads, 1)
+prefill_val_kernel(ValArgs a, const __grid_constant__ CUtensorMap tmV)
+{
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int N = a.N, ntl = a.ntl;
+
+    __shared__ __align__(16) ValSmem S;
+    extern __shared__ __align__(1024) unsigned char dyn[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(dyn) + 1023) & ~uintptr_t(1023));
+    unsigned char *ring = sm + 3 * kOp;
+    const uint32_t r_s = smem_u32(sm), ring_s = smem_u32(ring);
+
     if (tid == 0) {
-        double s = 0.0;
-        for (int j = 0; j < kPThreads / 32; j++) s += S.red[j];
-        atomicAdd(&a.layer_sum[l], s);
-        if (S.bad) a.layer_sum[l] = __longlong_as_double(0x7ff8000000000000ll);   // NaN: timed out
+        S.bad = 0;
+        for (int j = 0; j < kVStages; j++) {
+            mbar_init(&S.full[j], 1);
+            mbar_init(&S.empty[j], 1);
+        }
+        for (int j = 0; j < kAcc; j++) {
+            mbar_init(&S.accf[j], 1);
+            mbar_init(&S.acce[j], 4);
+        }
+        for (int j = 0; j < kVQueue; j++) {
+            mbar_init(&S.qfull[j], 1);
+            mbar_init(&S.qfree[j], 4);
+        }
+        mbar_init(&S.rfull, 1);
+        mbar_init(&S.rfree, 1);
+        mbar_init(&S.fin, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (w == 1) tmem_alloc(&S.tmem, 512);
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = S.tmem;
+
+    // chunk k of this CTA: wait until posted, return its first tile (-1: done)
+    auto take = [&](int k, bool &ok) -> long long {
+        const int slot = k % kVQueue;
+        if (!ok || !mbar_wait(&S.qfull[slot], (uint32_t)(k / kVQueue) & 1u)) {
+            ok = false;
+            return -1;
+        }
+        return S.chunk[slot];
+    };
+
+    if (w == 6) {
+        // ------------------------------------------------ scheduler (whole warp)
+        int item = -1;
+        for (int k = 0;; k++) {
+            // next chunk: global index of its first tile, -1 when no tile is left
+            long long c0 = -2;
+            if (lane == 0) {
+                for (;;) {
+                    if (item >= 0) {
+                        const int c = atomicAdd(&a.tile_next[item], kVChunk);
+                        if (c < ntl) {
+                            c0 = (long long)item * ntl + c;
+                            break;
+                        }
+                    }
+                    const int nx = atomicAdd(a.item_next, 1);
+                    if (nx >= a.nitem) break;       // every item is open: help below
+                    item = nx;
+                }
+            }
+            c0 = __shfl_sync(kFull, c0, 0);
+            item = __shfl_sync(kFull, item, 0);
+            if (c0 == -2) {
+                // take tiles left in any item: 32 counters per round, in parallel
+                c0 = -1;
+                const int from = max(item, 0);
+                for (int base = 0; base < a.nitem && c0 < 0; base += 32) {
+                    const int cand = (from + 1 + base + lane) % a.nitem;
+                    const bool has = base + lane < a.nitem &&
+                                     *(volatile int *)&a.tile_next[cand] < ntl;
+                    unsigned m = __ballot_sync(kFull, has);
+                    while (m != 0u && c0 < 0) {
+                        const int src = __ffs(m) - 1;
+                        m &= m - 1u;
+                        const int cc = __shfl_sync(kFull, cand, src);
+                        long long got = -1;
+                        if (lane == 0) {
+                            const int c = atomicAdd(&a.tile_next[cc], kVChunk);
+                            if (c < ntl) got = (long long)cc * ntl + c;
+                        }
+                        got = __shfl_sync(kFull, got, 0);
+                        if (got >= 0) {
+                            c0 = got;
+                            item = cc;
+                        }
+                    }
+                }
+            }
+            int ok = 1;
+            if (lane == 0) {
+                const int slot = k % kVQueue;
+                if (mbar_wait(&S.qfree[slot], ((uint32_t)(k / kVQueue) & 1u) ^ 1u)) {
+                    S.chunk[slot] = c0;
+                    mbar_arrive(&S.qfull[slot]);
+                } else {
+                    // nobody reads the queue any more: the others time out
+                    atomicExch(&S.bad, 1);
+                    ok = 0;
+                }
+            }
+            ok = __shfl_sync(kFull, ok, 0);
+            if (!ok || c0 < 0) break;
+        }
+    } else if (w == 0) {
+        // ------------------------------------------------ producer
+        if (lane == 0) {
+            bool ok = true;
+            int issued = 0, rloads = 0, cur_lg = -1;
+            const uint64_t once = l2_policy_evict_first();
+            int j = 0;
+            for (int k = 0; ok; k++) {
+                const long long c0 = take(k, ok);
+                if (c0 < 0) break;
+                const int lg = (int)c0 / ntl, t0 = (int)c0 - lg * ntl, t1 = min(ntl, t0 + kVChunk);
+                for (int t = t0; t < t1 && ok; t++, j++) {
+                    if (lg != cur_lg) {
+                        // R of (layer, KV head) lg, once the MMAs reading the previous R are done
+                        if (rloads > 0 && !mbar_wait(&S.rfree, (uint32_t)(rloads - 1) & 1u)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_expect_tx(&S.rfull, (uint32_t)(3 * kOp));
+                        const unsigned char *src = a.pack + (size_t)lg * kPackBytes + kOp;
+                        for (int q = 0; q < 3; q++) bulk_g2s(sm + q * kOp, src + q * kOp, kOp, &S.rfull);
+                        rloads++;
+                        cur_lg = lg;
+                    }
+                    const int s = j % kVStages;
+                    if (!mbar_wait(&S.empty[s], Ring::stage_parity(j, kVStages) ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(&S.full[s], (uint32_t)kOp);
+                    unsigned char *dst = ring + (size_t)s * kOp;
+                    const int row = lg * N + t * kTk;
+                    tma_2d_hint(dst, &tmV, 0, row, &S.full[s], once);
+                    tma_2d_hint(dst + kUmmaBox, &tmV, 64, row, &S.full[s], once);
+                    issued = j + 1;
+                }
+            }
+            if (!ok) {
+                atomicExch(&S.bad, 1);
+                if (rloads > 0) mbar_wait(&S.rfull, (uint32_t)(rloads - 1) & 1u);
+                for (int q = max(0, issued - kVStages); q < issued; q++)
+                    mbar_wait(&S.full[q % kVStages], Ring::stage_parity(q, kVStages));
+            }
+        }
+    } else if (w == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            bool ok = true;
+            int j = 0, rloads = 0, cur_lg = -1;
+            for (int k = 0; ok; k++) {
+                const long long c0 = take(k, ok);
+                if (c0 < 0) break;
+                const int lg = (int)c0 / ntl, t0 = (int)c0 - lg * ntl, t1 = min(ntl, t0 + kVChunk);
+                for (int t = t0; t < t1; t++, j++) {
+                    if (lg != cur_lg) {
+                        if (rloads > 0) umma_commit(&S.rfree);   // the previous R is free once these complete
+                        if (!mbar_wait(&S.rfull, (uint32_t)rloads & 1u)) {
+                            ok = false;
+                            break;
+                        }
+                        rloads++;
+                        cur_lg = lg;
+                    }
+                    const int s = j % kVStages, b = j % kAcc;
+                    if (!mbar_wait(&S.full[s], Ring::stage_parity(j, kVStages)) ||
+                        !mbar_wait(&S.acce[b], Ring::acc_parity(j) ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d = tmem + (uint32_t)(b * 128);
+                    const uint32_t tile = ring_s + (uint32_t)(s * kOp);
+#pragma unroll 1
+                    for (int sp = 0; sp < 3; sp++) {
+                        const uint32_t rb = r_s + (uint32_t)(sp * kOp);
+#pragma unroll
+                        for (int ks = 0; ks < 8; ks++)
+                            umma_bf16(d, umma_sdesc(tile + umma_kstep(ks)),
+                                      umma_sdesc(rb + umma_kstep(ks)), kIdesc, sp > 0 || ks > 0);
+                    }
+                    umma_commit(&S.accf[b]);
+                    umma_commit(&S.empty[s]);
+                }
+            }
+            umma_commit(&S.fin);
+            if (!mbar_wait(&S.fin, 0)) ok = false;
+            if (!ok) atomicExch(&S.bad, 1);
+        }
+    } else {
+        // ------------------------------------------------ epilogue (warps 2-5)
+        const int qd = w & 3;
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * qd) << 16);
+        bool good = true;
+        int j = 0;
+        for (int k = 0; good; k++) {
+            bool ok = good;
+            const long long c0 = take(k, ok);
+            good = __all_sync(kFull, ok);
+            if (!good || c0 < 0) break;
+            const int lg = (int)c0 / ntl, t0 = (int)c0 - lg * ntl, t1 = min(ntl, t0 + kVChunk);
+            for (int t = t0; t < t1; t++, j++) {
+                const int b = j % kAcc;
+                ok = good && mbar_wait(&S.accf[b], Ring::acc_parity(j));
+                good = __all_sync(kFull, ok);
+                if (good) {
+                    tc_fence_after();
+                    float x[128];
+                    tmem_ld128(lane_base + (uint32_t)(b * 128), x);
+                    float r2[8];
+#pragma unroll
+                    for (int q = 0; q < 8; q++) r2[q] = x[q] * x[q];
+#pragma unroll
+                    for (int e = 8; e < 128; e++) r2[e & 7] = fmaf(x[e], x[e], r2[e & 7]);
+                    const int key = t * kTk + 32 * qd + lane;
+                    if (key < N)
+                        a.r2[(size_t)lg * N + key] =
+                            ((r2[0] + r2[1]) + (r2[2] + r2[3])) + ((r2[4] + r2[5]) + (r2[6] + r2[7]));
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0 && good) mbar_arrive(&S.acce[b]);
+            }
+            __syncwarp();
+            if (lane == 0 && good) mbar_arrive(&S.qfree[k % kVQueue]);
+        }
+        if (!good) atomicExch(&S.bad, 1);
+    }
+    __syncthreads();
+    if (w == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+    if (tid == 0 && S.bad)
+        for (int l = 0; l < a.NL; l++)     // NaN: a wait timed out
+            a.layer_sum[l] = __longlong_as_double(0x7ff8000000000000ll);
+}
+
+// p = c r per key and the per-layer sums of p (fp64); block b covers
+// elements [c kCombSpan, (c + 1) kCombSpan) of layer b / cpl, c = b % cpl.
+constexpr int kCombSpan = 4096;
+
+__global__ void __launch_bounds__(256) combine_kernel(float *p, const float *c2, const float *r2,
+                                                      double *layer_sum, int64_t per_layer, int cpl)
+{
+    __shared__ double red[8];
+    const int l = blockIdx.x / cpl, c = blockIdx.x % cpl;
+    const int64_t e0 = (int64_t)c * kCombSpan, e1 = min(per_layer, e0 + kCombSpan);
+    const int64_t off = (int64_t)l * per_layer;
+    double s = 0.0;
+    for (int64_t i = e0 + threadIdx.x; i < e1; i += blockDim.x) {
+        const float v = sqrtf(c2[off + i]) * sqrtf(r2[off + i]);
+        p[off + i] = v;
+        s += (double)v;
+    }
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) s += __shfl_xor_sync(kFull, s, m);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double t = 0.0;
+        for (int j = 0; j < 8; j++) t += red[j];
+        atomicAdd(&layer_sum[l], t);
     }
 }
 
 // --------------------------------------------------------------- operands
 // Per (layer, KV head): the 128 window rows (row 4 j + h = query head h of
 // the group at window position j; zero past the window) and the three bf16
-// terms of the Gram matrix (hi + mid + lo carries its fp32 value), each a
+// terms of the factor R (hi + mid + lo carries its fp32 value), each a
 // 128 x 128 K-major tile in the layout of a 128-byte-swizzled TMA load.
-__global__ void __launch_bounds__(256) pack_kernel(const uint16_t *q, const float *gram,
+__global__ void __launch_bounds__(256) pack_kernel(const uint16_t *q, const float *R,
                                                    unsigned char *pack, int Hq, int Hkv, int W)
 {
     const int lg = blockIdx.x, l = lg / Hkv, g = lg % Hkv;
@@ -433,7 +706,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint16_t *q, const floa
         }
         *reinterpret_cast<uint4 *>(dst + opnd_off(r, c)) = v;
     }
-    const float *G0 = gram + (size_t)lg * kD * kD;
+    const float *G0 = R + (size_t)lg * kD * kD;
     for (int e = threadIdx.x; e < kD * 16; e += blockDim.x) {
         const int b = e >> 4, c = e & 15;
         float x[8];
@@ -461,14 +734,27 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint16_t *q, const floa
     }
 }
 
-// --------------------------------------------------------------- Gram
-// One CTA per (layer, KV head); thread (ta, tb) owns the 8 x 8 block of the
-// Gram matrix at rows 8 ta, columns 8 tb.  Columns of W_g are taken 32 at a
-// time; W_g entries are fp32 sums of the group's bf16 W_O entries.
-__global__ void __launch_bounds__(256) gram_kernel(const uint16_t *W, float *Gram, int Hq, int Hkv,
-                                                   int D)
+// --------------------------------------------------------------- factor
+// One CTA per (layer, KV head).  Phase 1: Gram = W_g W_g^T in fp64, thread
+// (ta, tb) owning the 8 x 8 block at rows 8 ta, columns 8 tb, the columns of
+// W_g (fp32 sums of the group's bf16 W_O entries) taken 32 at a time.
+// Phase 2: pivoted Cholesky of Gram in fp64 (outer-product form, the largest
+// remaining diagonal as pivot; stops when that falls to d * eps * the largest
+// diagonal, the rest of the factor being zero).  Step k gives the column l_k
+// of F with F F^T = Gram, written as row k of R = F^T, so that
+// ||v W_g||^2 = v Gram v^T = ||R v^T||^2.
+constexpr size_t kFacSmem = (size_t)kD * kD * 8 + (size_t)kD * 8;
+
+__global__ void __launch_bounds__(256) factor_kernel(const uint16_t *W, float *R, int Hq, int Hkv,
+                                                     int D)
 {
+    extern __shared__ __align__(16) unsigned char fsm[];
+    double *A = reinterpret_cast<double *>(fsm);     // Gram, then its Schur complements
+    double *lk = A + kD * kD;                         // current factor column
     __shared__ float Wc[kD][33];
+    __shared__ int done[kD];
+    __shared__ int piv;
+    __shared__ double pd, tol;
     const int lg = blockIdx.x, l = lg / Hkv, g = lg % Hkv;
     const int G = Hq / Hkv;
     const int tid = threadIdx.x, ta = tid >> 4, tb = tid & 15;
@@ -502,11 +788,52 @@ __global__ void __launch_bounds__(256) gram_kernel(const uint16_t *W, float *Gra
                 for (int j = 0; j < 8; j++) acc[i][j] = fma(wa[i], wb[j], acc[i][j]);
         }
     }
-    float *Gm = Gram + (size_t)lg * kD * kD;
 #pragma unroll
     for (int i = 0; i < 8; i++)
 #pragma unroll
-        for (int j = 0; j < 8; j++) Gm[(8 * ta + i) * kD + 8 * tb + j] = (float)acc[i][j];
+        for (int j = 0; j < 8; j++) A[(8 * ta + i) * kD + 8 * tb + j] = acc[i][j];
+    if (tid < kD) done[tid] = 0;
+    __syncthreads();
+
+    float *Rg = R + (size_t)lg * kD * kD;
+    bool live = true;
+    for (int k = 0; k < kD; k++) {
+        if (tid < 32) {
+            // largest remaining diagonal (ties to the smaller index)
+            double best = -1.0;
+            int bi = kD;
+            for (int i = tid; i < kD; i += 32)
+                if (!done[i] && A[i * kD + i] > best) { best = A[i * kD + i]; bi = i; }
+#pragma unroll
+            for (int m = 16; m > 0; m >>= 1) {
+                const double ob = __shfl_xor_sync(kFull, best, m);
+                const int oi = __shfl_xor_sync(kFull, bi, m);
+                if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
+            }
+            if (tid == 0) {
+                piv = bi;
+                pd = best;
+                if (k == 0) tol = (double)kD * 2.220446049250313e-16 * fmax(best, 0.0);
+            }
+        }
+        __syncthreads();
+        const int p = piv;
+        live = live && pd > tol && p < kD;
+        const double inv = live ? 1.0 / sqrt(pd) : 0.0;
+        if (tid < kD) {
+            const double v = (live && !done[tid]) ? A[tid * kD + p] * inv : 0.0;
+            lk[tid] = v;
+            Rg[(size_t)k * kD + tid] = (float)v;
+        }
+        __syncthreads();
+        if (tid == 0 && p < kD) done[p] = 1;
+        if (live)
+            for (int e = tid; e < kD * kD; e += blockDim.x) {
+                const double li = lk[e >> 7];
+                if (li != 0.0) A[e] = fma(-li, lk[e & (kD - 1)], A[e]);
+            }
+        __syncthreads();
+    }
 }
 
 // --------------------------------------------------------------- top-K
@@ -525,13 +852,20 @@ constexpr int kTkSpan = kTkBlock * kTkPer;
 // order key: ascending key = descending score
 __device__ __forceinline__ uint32_t desc_key(float s) { return ~float_key(s); }
 
-__global__ void normalize_kernel(float *s, const double *layer_sum, int64_t per_layer, int64_t M,
-                                 int normalize)
+// inv[l] = 1 / (sum of p over layer l), 0 for an all-zero layer
+__global__ void layer_inv_kernel(const double *layer_sum, float *inv, int NL)
 {
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= M || !normalize) return;
-    const double z = layer_sum[i / per_layer];
-    s[i] = z > 0.0 ? (float)((double)s[i] / z) : 0.f;
+    for (int l = threadIdx.x; l < NL; l += blockDim.x) {
+        const double z = layer_sum[l];
+        inv[l] = z > 0.0 ? (float)(1.0 / z) : (z == 0.0 ? 0.f : __int_as_float(0x7fc00000));
+    }
+}
+
+__global__ void normalize_kernel(float *s, const float *inv, int64_t per_layer, int64_t M)
+{
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < M;
+         i += (int64_t)gridDim.x * blockDim.x)
+        s[i] *= inv[i / per_layer];
 }
 
 __global__ void topk_hist_kernel(const float *s, int64_t M, const TopkState *st, int shift,
@@ -669,6 +1003,9 @@ __global__ void __launch_bounds__(kTkBlock) topk_write_kernel(const float *s, in
 struct PfWs {
     float *p;
     double *layer_sum;
+    float *inv;
+    float *r2;
+    int *counter;                // [0]: next unopened item, [1 + i]: next tile of item i
     unsigned char *pack;
     float2 *stats;
     TopkState *st;
@@ -692,6 +1029,9 @@ PfWs pf_layout(int NL, int Hkv, int N, void *base)
     };
     w.p = reinterpret_cast<float *>(take((size_t)M * 4));
     w.layer_sum = reinterpret_cast<double *>(take((size_t)NL * 8));
+    w.inv = reinterpret_cast<float *>(take((size_t)NL * 4));
+    w.r2 = reinterpret_cast<float *>(take((size_t)M * 4));
+    w.counter = reinterpret_cast<int *>(take((size_t)(NL * Hkv + 1) * 4));
     w.pack = reinterpret_cast<unsigned char *>(take((size_t)NL * Hkv * kPackBytes));
     w.stats = reinterpret_cast<float2 *>(take((size_t)NL * Hkv * kCS * 2 * kRows * sizeof(float2)));
     w.st = reinterpret_cast<TopkState *>(take(sizeof(TopkState)));
@@ -702,6 +1042,39 @@ PfWs pf_layout(int NL, int Hkv, int N, void *base)
     w.keep_off = reinterpret_cast<int64_t *>(take((size_t)nblk * 8));
     w.bytes = off;
     return w;
+}
+
+// A second stream per device (and the events that fork to it and join back)
+// for the kernels of a call that run side by side; one call at a time
+// enqueues on it (mu).
+struct SideStream {
+    std::mutex mu;
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+SideStream *side_stream(int dev)
+{
+    constexpr int kMaxDev = 64;
+    static SideStream table[kMaxDev];
+    static std::mutex init_mu;
+    if (dev < 0 || dev >= kMaxDev) {
+        set_error("kvc_prefill_score: device %d out of range", dev);
+        return nullptr;
+    }
+    SideStream &t = table[dev];
+    std::lock_guard<std::mutex> lock(init_mu);
+    if (t.s == nullptr) {
+        cudaError_t e = cudaStreamCreateWithFlags(&t.s, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&t.fork, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&t.join, cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            set_error("kvc_prefill_score: side stream: %s", cudaGetErrorString(e));
+            t.s = nullptr;
+            return nullptr;
+        }
+    }
+    return &t;
 }
 
 }  // namespace
@@ -727,14 +1100,17 @@ static kvc_status pf_cuda(cudaError_t e, const char *what)
 extern "C" {
 
 kvc_status kvc_prefill_prepare(int32_t NL, int32_t Hq, int32_t Hkv, int32_t d, int32_t D,
-                               const uint16_t *W_O, float *Gram, void *stream)
+                               const uint16_t *W_O, float *R, void *stream)
 {
     PF_CHECK(NL >= 1 && Hq >= 1 && Hkv >= 1 && D >= 1, KVC_ERR_INVALID_ARG,
              "kvc_prefill_prepare: NL, Hq, Hkv, D must be >= 1");
     PF_CHECK(d == kD, KVC_ERR_UNSUPPORTED, "kvc_prefill_prepare: d = %d unsupported", d);
     PF_CHECK(Hq % Hkv == 0, KVC_ERR_INVALID_ARG, "kvc_prefill_prepare: Hq %% Hkv != 0");
-    PF_CHECK(W_O && Gram, KVC_ERR_INVALID_ARG, "kvc_prefill_prepare: NULL pointer");
-    gram_kernel<<<NL * Hkv, 256, 0, static_cast<cudaStream_t>(stream)>>>(W_O, Gram, Hq, Hkv, D);
+    PF_CHECK(W_O && R, KVC_ERR_INVALID_ARG, "kvc_prefill_prepare: NULL pointer");
+    cudaError_t e = cudaFuncSetAttribute(factor_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kFacSmem);
+    if (e != cudaSuccess) return pf_cuda(e, "kvc_prefill_prepare attribute");
+    factor_kernel<<<NL * Hkv, 256, kFacSmem, static_cast<cudaStream_t>(stream)>>>(W_O, R, Hq, Hkv, D);
     return pf_cuda(cudaGetLastError(), "kvc_prefill_prepare launch");
 }
 
@@ -747,7 +1123,7 @@ size_t kvc_prefill_workspace_size(int32_t NL, int32_t Hkv, int32_t N, int64_t B_
 
 kvc_status kvc_prefill_score(int32_t NL, int32_t Hq, int32_t Hkv, int32_t d, int32_t N,
                              int32_t w, int64_t B_total, int32_t normalize, const uint16_t *q_win,
-                             const uint16_t *K, const uint16_t *V, const float *Gram,
+                             const uint16_t *K, const uint16_t *V, const float *R,
                              float *scores, uint8_t *keep, int32_t *counts, int64_t *idx,
                              void *ws, size_t ws_bytes, void *stream)
 {
@@ -762,11 +1138,11 @@ kvc_status kvc_prefill_score(int32_t NL, int32_t Hq, int32_t Hkv, int32_t d, int
     PF_CHECK(B_total >= 0 && B_total <= M, KVC_ERR_INVALID_ARG,
              "kvc_prefill_score: B_total = %lld outside [0, %lld]", (long long)B_total, (long long)M);
     const int per_cta = ((N + kCS - 1) / kCS + kTk - 1) / kTk * kTk;
-    PF_CHECK(q_win && K && V && Gram && keep, KVC_ERR_INVALID_ARG,
-             "kvc_prefill_score: q_win, K, V, Gram and keep are required");
-    PF_CHECK(((uintptr_t)K & 15u) == 0 && ((uintptr_t)V & 15u) == 0 && ((uintptr_t)Gram & 15u) == 0 &&
+    PF_CHECK(q_win && K && V && R && keep, KVC_ERR_INVALID_ARG,
+             "kvc_prefill_score: q_win, K, V, R and keep are required");
+    PF_CHECK(((uintptr_t)K & 15u) == 0 && ((uintptr_t)V & 15u) == 0 && ((uintptr_t)R & 15u) == 0 &&
                  ((uintptr_t)q_win & 3u) == 0,
-             KVC_ERR_INVALID_ARG, "kvc_prefill_score: K, V, Gram must be 16-byte aligned, q_win 4-byte");
+             KVC_ERR_INVALID_ARG, "kvc_prefill_score: K, V, R must be 16-byte aligned, q_win 4-byte");
     PfWs pw = pf_layout(NL, Hkv, N, nullptr);
     PF_CHECK(ws != nullptr && ws_bytes >= pw.bytes && ((uintptr_t)ws & 255u) == 0, KVC_ERR_WORKSPACE,
              "kvc_prefill_score: workspace of %zu bytes (256-byte aligned) required", pw.bytes);
@@ -785,23 +1161,41 @@ kvc_status kvc_prefill_score(int32_t NL, int32_t Hq, int32_t Hkv, int32_t d, int
     if (s != KVC_OK) return s;
     s = pf_cuda(cudaMemsetAsync(pw.hist, 0, 256 * 4, st), "memset");
     if (s != KVC_OK) return s;
+    s = pf_cuda(cudaMemsetAsync(pw.counter, 0, (size_t)(NL * Hkv + 1) * 4, st), "memset");
+    if (s != KVC_OK) return s;
     if (counts) {
         s = pf_cuda(cudaMemsetAsync(counts, 0, (size_t)NL * Hkv * 4, st), "memset");
         if (s != KVC_OK) return s;
     }
 
-    pack_kernel<<<NL * Hkv, 256, 0, st>>>(q_win, Gram, pw.pack, Hq, Hkv, w);
+    pack_kernel<<<NL * Hkv, 256, 0, st>>>(q_win, R, pw.pack, Hq, Hkv, w);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return pf_cuda(e, "kvc_prefill_score pack launch");
-    ScoreArgs a{pw.pack, pbuf, pw.stats, pw.layer_sum, NL, Hkv, N, w, per_cta,
+    // The attention kernel (c^2 into the score buffer) and the value-norm
+    // kernel (r^2) are independent: the value kernel runs on a second stream
+    // and takes the SMs the attention clusters leave free; p = c r after both.
+    const int ntl = (N + kTk - 1) / kTk;
+    const long long total = (long long)NL * Hkv * ntl;
+    int dev = 0, nsm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return pf_cuda(e, "kvc_prefill_score device query");
+    SideStream *side = side_stream(dev);
+    if (side == nullptr) return KVC_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(side->mu);
+
+    const int nitem = NL * Hkv;
+    AttnArgs aa{pw.pack, pbuf, pw.stats, pw.layer_sum, Hkv, N, w, per_cta, nitem,
                 (float)(1.4426950408889634 / sqrt((double)kD))};
-    e = cudaFuncSetAttribute(prefill_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kPDyn);
+    e = cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kADyn);
+    if (e != cudaSuccess) return pf_cuda(e, "kvc_prefill_score attribute");
+    e = cudaFuncSetAttribute(prefill_val_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kVDyn);
     if (e != cudaSuccess) return pf_cuda(e, "kvc_prefill_score attribute");
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(NL * Hkv * kCS);
-    cfg.blockDim = dim3(kPThreads);
-    cfg.dynamicSmemBytes = kPDyn;
+    cfg.blockDim = dim3(kAThreads);
+    cfg.dynamicSmemBytes = kADyn;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -810,12 +1204,36 @@ kvc_status kvc_prefill_score(int32_t NL, int32_t Hq, int32_t Hkv, int32_t d, int
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, prefill_score_kernel, a, tmK, tmV);
-    if (e != cudaSuccess) return pf_cuda(e, "kvc_prefill_score launch");
+    // persistent: as many clusters as the GPU holds at once (each loops over items)
+    cfg.gridDim = dim3(kCS * std::min(nitem, std::max(1, nsm / kCS)));
+    int nclu = 0;
+    if (cudaOccupancyMaxActiveClusters(&nclu, prefill_attn_kernel, &cfg) != cudaSuccess || nclu < 1)
+        nclu = std::max(1, nsm / (2 * kCS));
+    (void)cudaGetLastError();
+    cfg.gridDim = dim3(kCS * std::min(nitem, nclu));
 
-    normalize_kernel<<<(unsigned)((M + 255) / 256), 256, 0, st>>>(pbuf, pw.layer_sum, (int64_t)Hkv * N,
-                                                                  M, normalize);
-    if ((e = cudaGetLastError()) != cudaSuccess) return pf_cuda(e, "normalize launch");
+    if ((e = cudaEventRecord(side->fork, st)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(side->s, side->fork, 0)) != cudaSuccess)
+        return pf_cuda(e, "kvc_prefill_score stream fork");
+    e = cudaLaunchKernelEx(&cfg, prefill_attn_kernel, aa, tmK);
+    if (e != cudaSuccess) return pf_cuda(e, "kvc_prefill_score attention launch");
+    ValArgs va{pw.pack, pw.r2, pw.layer_sum, pw.counter, pw.counter + 1, NL, N, ntl, nitem};
+    prefill_val_kernel<<<(unsigned)std::min<long long>((total + kVChunk - 1) / kVChunk, nsm), kVThreads,
+                         kVDyn, side->s>>>(va, tmV);
+    if ((e = cudaGetLastError()) != cudaSuccess) return pf_cuda(e, "kvc_prefill_score value launch");
+    if ((e = cudaEventRecord(side->join, side->s)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(st, side->join, 0)) != cudaSuccess)
+        return pf_cuda(e, "kvc_prefill_score stream join");
+    const int64_t per_layer = (int64_t)Hkv * N;
+    const int cpl = (int)((per_layer + kCombSpan - 1) / kCombSpan);
+    combine_kernel<<<NL * cpl, 256, 0, st>>>(pbuf, pbuf, pw.r2, pw.layer_sum, per_layer, cpl);
+    if ((e = cudaGetLastError()) != cudaSuccess) return pf_cuda(e, "kvc_prefill_score combine launch");
+
+    if (normalize) {
+        layer_inv_kernel<<<1, 256, 0, st>>>(pw.layer_sum, pw.inv, NL);
+        normalize_kernel<<<4 * 152, 256, 0, st>>>(pbuf, pw.inv, (int64_t)Hkv * N, M);
+        if ((e = cudaGetLastError()) != cudaSuccess) return pf_cuda(e, "normalize launch");
+    }
     const int nblk = (int)((M + kTkSpan - 1) / kTkSpan);
     if (B_total == 0) {
         s = pf_cuda(cudaMemsetAsync(keep, 0, (size_t)M, st), "memset");

@@ -112,6 +112,63 @@ __device__ __forceinline__ void tmem_ld32(uint32_t addr, float (&v)[32])
     for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
 }
 
+#define KVC_R32(r)                                                                              \
+    "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),          \
+        "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),  \
+        "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),            \
+        "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),            \
+        "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+
+// Asynchronous form: issue the load now, wait with tmem_wait_ld(), then pass
+// every destination through tmem_bind() so that no use of the registers can
+// be scheduled before the wait.
+__device__ __forceinline__ void tmem_ld32_async(uint32_t addr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+        "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(addr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld()
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_bind(uint32_t (&r)[32])
+{
+    asm volatile("" : KVC_R32(r)::"memory");
+}
+
+// 128 consecutive fp32 columns of this warp's 32 lanes: four loads in flight,
+// one wait.
+__device__ __forceinline__ void tmem_ld128(uint32_t addr, float (&v)[128])
+{
+    uint32_t r0[32], r1[32], r2[32], r3[32];
+    tmem_ld32_async(addr, r0);
+    tmem_ld32_async(addr + 32, r1);
+    tmem_ld32_async(addr + 64, r2);
+    tmem_ld32_async(addr + 96, r3);
+    tmem_wait_ld();
+    tmem_bind(r0);
+    tmem_bind(r1);
+    tmem_bind(r2);
+    tmem_bind(r3);
+#pragma unroll
+    for (int i = 0; i < 32; i++) {
+        v[i] = __uint_as_float(r0[i]);
+        v[32 + i] = __uint_as_float(r1[i]);
+        v[64 + i] = __uint_as_float(r2[i]);
+        v[96 + i] = __uint_as_float(r3[i]);
+    }
+}
+
 // 2^x on the special-function unit (relative error a few units in the last
 // place; -inf gives +0).
 __device__ __forceinline__ float ex2_approx(float x)

@@ -257,23 +257,23 @@ def kvc_decode_attend_noalloc(p, t, new_pos, max_len, q, k_new, v_new, cache: kv
 
 # ------------------------------------------------------------------ prefill
 
-def kvc_prefill_prepare(NL, Hq, Hkv, d, D, W_O, Gram, stream=None):
+def kvc_prefill_prepare(NL, Hq, Hkv, d, D, W_O, R, stream=None):
     _check(load().kvc_prefill_prepare(int(NL), int(Hq), int(Hkv), int(d), int(D),
                                       _ptr(W_O, torch.bfloat16, "W_O"),
-                                      _ptr(Gram, torch.float32, "Gram"), _stream(stream)))
+                                      _ptr(R, torch.float32, "R"), _stream(stream)))
 
 
 def kvc_prefill_workspace_size(NL, Hkv, N, B_total) -> int:
     return int(load().kvc_prefill_workspace_size(int(NL), int(Hkv), int(N), int(B_total)))
 
 
-def kvc_prefill_score(NL, Hq, Hkv, d, N, w, B_total, normalize, q_win, K, V, Gram, scores, keep,
+def kvc_prefill_score(NL, Hq, Hkv, d, N, w, B_total, normalize, q_win, K, V, R, scores, keep,
                       counts, idx, ws, stream=None):
     bf = torch.bfloat16
     _check(load().kvc_prefill_score(
         int(NL), int(Hq), int(Hkv), int(d), int(N), int(w), int(B_total), int(normalize),
         _ptr(q_win, bf, "q_win"), _ptr(K, bf, "K"), _ptr(V, bf, "V"),
-        _ptr(Gram, torch.float32, "Gram"), _ptr(scores, torch.float32, "scores", optional=True),
+        _ptr(R, torch.float32, "R"), _ptr(scores, torch.float32, "scores", optional=True),
         _ptr(keep, torch.uint8, "keep"), _ptr(counts, torch.int32, "counts", optional=True),
         _ptr(idx, torch.int64, "idx", optional=True), _ptr(ws, torch.uint8, "ws", optional=True),
         0 if ws is None else ws.numel(), _stream(stream)))

@@ -92,6 +92,7 @@ class PrefillConfig:
     B_total: int
     wo_std: float = 1.0 / 64.0
     description: str = ""
+    D_out: int = 0            # output width of W_O; 0 = Hq * d (the model width)
 
     @property
     def G(self) -> int:
@@ -99,7 +100,7 @@ class PrefillConfig:
 
     @property
     def D(self) -> int:
-        return self.Hq * self.d
+        return self.D_out or self.Hq * self.d
 
     def with_(self, **kw) -> "PrefillConfig":
         return replace(self, **kw)

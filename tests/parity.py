@@ -183,7 +183,7 @@ def run_decode_parity(cfg: W.DecodeConfig, *, steps: int | None = None, units=No
 class PrefillReport:
     band_hits: int = 0
     mismatches: int = 0
-    max_gram_err: float = 0.0
+    max_gram_err: float = 0.0      # of R^T R against the oracle's Gram
     max_s_err: float = 0.0
     counts_ok: bool = True
     idx_ok: bool = True
@@ -200,8 +200,8 @@ def run_prefill_parity(cfg: W.PrefillConfig, *, seed: int = 0, device="cuda",
     from kv_cache_eviction_kvc_gb300 import kvc as K
     NL, Hq, Hkv, d, N, w, B = cfg.NL, cfg.Hq, cfg.Hkv, cfg.d, cfg.N, cfg.w, cfg.B_total
     inp = W.gen_prefill_scorer(cfg, device, seed)
-    gram = torch.empty(NL, Hkv, d, d, dtype=torch.float32, device=device)
-    K.kvc_prefill_prepare(NL, Hq, Hkv, d, cfg.D, inp["W_O"], gram)
+    R = torch.empty(NL, Hkv, d, d, dtype=torch.float32, device=device)
+    K.kvc_prefill_prepare(NL, Hq, Hkv, d, cfg.D, inp["W_O"], R)
     M = NL * Hkv * N
     ws = torch.empty(max(256, K.kvc_prefill_workspace_size(NL, Hkv, N, B)), dtype=torch.uint8,
                      device=device)
@@ -210,12 +210,14 @@ def run_prefill_parity(cfg: W.PrefillConfig, *, seed: int = 0, device="cuda",
     counts = torch.empty(NL, Hkv, dtype=torch.int32, device=device)
     idx = torch.empty(max(B, 1), dtype=torch.int64, device=device)
     K.kvc_prefill_score(NL, Hq, Hkv, d, N, w, B, int(normalize), inp["q_win"], inp["K"],
-                        inp["V"], gram, scores, keep, counts, idx, ws)
+                        inp["V"], R, scores, keep, counts, idx, ws)
     torch.cuda.synchronize()
     ref = O.prefill_score(inp["q_win"], inp["K"], inp["V"], inp["W_O"], NL=NL, Hq=Hq, Hkv=Hkv,
                           d=d, N=N, w=w, B_total=B, normalize=normalize)
     rep = PrefillReport()
-    g = gram.cpu().numpy().astype(np.float64)
+    # the factor is not unique; R^T R is the Gram matrix
+    Rn = R.cpu().numpy().astype(np.float64)
+    g = np.einsum("lgka,lgkb->lgab", Rn, Rn)
     rep.max_gram_err = float(np.abs(g - ref["Gram"]).max() / np.abs(ref["Gram"]).max())
     s_gpu = scores.cpu().numpy().astype(np.float64)
     s_ref = ref["s"]

@@ -34,7 +34,8 @@ SMALL = W.C3.with_(NL=2, N=1024, B_total=512)
     (SMALL.with_(N=100, B_total=50), True),               # one CTA holds every key, 7 are empty
     (SMALL.with_(N=32, B_total=20), True),                # every key inside the window
     (SMALL.with_(NL=1, Hq=8, Hkv=2, N=40000, B_total=9000), True),   # 5000 keys per CTA
+    (SMALL.with_(D_out=96), True),                        # rank-deficient Gram (rank 96 < d)
 ], ids=["small", "ragged", "w8-k1", "keep-all", "unnormalized", "empty-ctas", "all-window",
-        "long"])
+        "long", "rank-deficient"])
 def test_prefill_edge_cases(cfg, normalize):
     check(run_prefill_parity(cfg, normalize=normalize))
