@@ -7,22 +7,23 @@
 //                      into three bf16 terms, laid out as the scorer's
 //                      shared-memory tensor-core operands
 //   prefill_val        r_i^2 = ||(V W_g)[i, :]||^2 = sum_b T[i][b]^2 with
-//                      T = V R^T (keys x dims, R as three bf16 terms), 32
-//                      key tiles of 128 per CTA
-//   prefill_attn       one cluster of kCS CTAs per (layer, KV head), 128-key
-//                      tiles:
+//                      T = V R^T (keys x dims, R as three bf16 terms);
+//                      persistent, 128-key tiles scheduled dynamically
+//   prefill_attn       persistent 8-CTA clusters looping over (layer, KV head)
+//                      items, 128-key tiles per CTA:
 //                        stat   S = Q K^T (rows x keys): row max / sum of the
 //                               window logits, merged over the cluster
 //                        norm   S^T = K Q^T (keys x rows): group-mean
 //                               attention column norms c_i = ||A_bar[:, i]||_2
-//                      p_i = c_i r_i; per-layer sums (fp64)
+//                      p_i = c_i r_i and the per-layer sums of p (fp64)
 //                      Both kernels: every contraction on tcgen05 (128 x 128
 //                      x 128 bf16, fp32 accumulators in tensor memory), a TMA
 //                      producer warp, one MMA-issuing thread, epilogue warps
 //                      reading the accumulators by lane quarter.
-//   normalize / top-K  s = p / layer sum; global radix select of the B_total
-//                      largest (ties to the smaller flat index); keep mask,
-//                      per-(layer, KV head) counts, ascending kept indices
+//   select             s = p / layer sum; three-pass radix select of the
+//                      B_total largest (ties to the smaller flat index); keep
+//                      mask, per-(layer, KV head) counts, ascending kept
+//                      indices
 //
 // Method: LaProx key designs 1-3 and its GQA group-mean paragraph; the
 // observation window of the last w prompt queries (SnapKV protocol, as used in
@@ -32,7 +33,6 @@
 
 #include <algorithm>
 #include <cstddef>
-#include <mutex>
 
 #include "kvc_common.cuh"
 #include "kvc_internal.h"
@@ -53,11 +53,14 @@ constexpr int kAcc = 4;              // tensor-memory accumulators of 128 fp32 c
 constexpr int kPackBytes = 4 * kOp;  // [Q][R hi][R mid][R lo]
 constexpr uint32_t kIdesc = umma_idesc_bf16(128, 128);
 
-// attention kernel: [Q (two buffers) | ring of K tiles]
-constexpr int kAStages = 5;
-constexpr int kAEpiWarps = 8;        // two sets of four warps, one per tensor-memory lane quarter
+// attention kernel: [Q (three buffers) | ring of K tiles]
+constexpr int kAQ = 3;
+constexpr int kAStages = 4;
+constexpr int kALead = 4;            // statistics jobs of a block before its first norm job
+constexpr int kASets = 2;            // epilogue sets: tile t goes to set t % kASets
+constexpr int kAEpiWarps = 4 * kASets;   // four warps per set, one per tensor-memory lane quarter
 constexpr int kAThreads = (2 + kAEpiWarps) * 32;
-constexpr size_t kADyn = 1024 + (size_t)2 * kOp + (size_t)kAStages * kOp;
+constexpr size_t kADyn = 1024 + (size_t)kAQ * kOp + (size_t)kAStages * kOp;
 // value-norm kernel: [R x 3 | ring of V tiles]
 constexpr int kVStages = 4;
 constexpr int kVThreads = (2 + 4 + 1) * 32;   // producer, MMA, 4 epilogue, scheduler
@@ -81,18 +84,21 @@ struct Ring {
 
 // =============================================================== attention
 // Persistent: gridDim.x / kCS clusters of kCS CTAs; cluster c takes the
-// (layer, KV head) items c, c + nclu, ...; within an item CTA cr owns keys
-// [cr per_cta, (cr + 1) per_cta).  Jobs of an item: stat(t) for t = 0..nt-1
-// (S = Q K_t^T, rows x keys: row max / sum), then norm(t) for t = nt-1..0
-// (S^T = K_t Q^T, keys x rows: column norms; the K tiles read last in the
-// first pass are read again first, from L2).  The producer and the MMA issuer
-// run on across items; only the epilogue waits for the cluster's statistics.
-// Output: c_i^2 = ||A_bar[:, i]||^2.
+// (layer, KV head) items c, c + nclu, ... (item p of the cluster); within an
+// item CTA cr owns keys [cr per_cta, (cr + 1) per_cta).  Per item, stat(t)
+// for t = 0..nt-1 (S = Q K_t^T, rows x keys: row max / sum) and norm(t) for
+// t = nt-1..0 (S^T = K_t Q^T, keys x rows: column norms).  The items are
+// software-pipelined: block p runs stat(p) and then norm(p - 1), so the
+// cluster-wide merge of item p - 1's statistics is hidden behind a whole
+// statistics pass.  Q of item p lives in buffer p % 3.
+// Output: p_i = c_i r_i with c_i = ||A_bar[:, i]||_2 and r_i^2 from the
+// value-norm kernel, and the per-layer sums of p.
 struct AttnArgs {
     const unsigned char *pack;   // [NL][Hkv][kPackBytes] from pack_kernel
-    float *c2;                   // [NL][Hkv][N]: squared group-mean column norms
-    float2 *stats;               // [NL][Hkv][kCS][2][kRows] partial (max, sum) per row
-    double *layer_sum;           // [NL]: NaN on a timed-out wait
+    const float *r2;             // [NL][Hkv][N]: squared value norms (value-norm kernel)
+    float *p;                    // [NL][Hkv][N]: p = c r
+    float2 *stats;               // [NL][Hkv][kCS][kASets][kRows] partial (max, sum) per row
+    double *layer_sum;           // [NL]: per-layer sums of p; NaN on a timed-out wait
     int Hkv, N, w, per_cta, nitem;
     float cs;                    // log2(e) / sqrt(d): logits in base-2 units
 };
@@ -102,8 +108,8 @@ struct AttnSmem {
     uint64_t empty[kAStages];
     uint64_t accf[kAcc];         // accumulator ready (MMA commit)
     uint64_t acce[kAcc];         // accumulator drained (4 epilogue warps)
-    uint64_t qfull[2];           // Q buffer loaded
-    uint64_t qfree[2];           // every MMA reading the Q buffer completed
+    uint64_t qfull[kAQ];         // Q buffer loaded
+    uint64_t qfree[kAQ];         // every MMA reading the Q buffer completed
     uint64_t ready[2];           // the cluster's partial statistics of an item are published
     uint64_t fin;                // every MMA of the CTA completed
     __align__(16) float2 rs[kRows];   // per row: cluster max (base 2) and 1 / sum; read as float4
@@ -125,13 +131,29 @@ prefill_attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap tmK)
     extern __shared__ __align__(1024) unsigned char dyn[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(dyn) + 1023) & ~uintptr_t(1023));
-    unsigned char *ring = sm + 2 * kOp;        // [Q0 | Q1 | ring]
+    unsigned char *ring = sm + kAQ * kOp;      // [Q x kAQ | ring]
     const uint32_t q_s = smem_u32(sm), ring_s = smem_u32(ring);
 
     const int N = a.N, W = a.w;
     const int k0 = min(N, cr * a.per_cta), k1 = min(N, k0 + a.per_cta);
     const int nt = (k1 - k0 + kTk - 1) / kTk;
-    const int njob = 2 * nt;                   // per item
+    // first job of block p (block 0: nt jobs, blocks 1..nmine-1: 2 nt, block nmine: nt)
+    auto block_base = [nt](int p) { return p == 0 ? 0 : (2 * p - 1) * nt; };
+    // Jobs of block p in order: kALead statistics jobs of item p, then (where
+    // item p - 1 exists) mid() -- the point where its merged statistics are
+    // needed -- and its column-norm jobs alternating with the remaining
+    // statistics jobs: HBM-bound and exponential-bound work overlap.
+    auto for_block = [nt, nmine, &block_base](int p, auto &&stat, auto &&norm, auto &&mid) {
+        const int ns = p < nmine ? nt : 0, nn = p >= 1 ? nt : 0;
+        int gi = block_base(p), is = 0, in = 0;
+        for (; is < min(ns, kALead); is++) stat(gi++, is);
+        if (nn) mid();
+        while (is < ns || in < nn) {
+            if (in < nn) norm(gi++, nt - 1 - in++);
+            if (is < ns) stat(gi++, is++);
+        }
+    };
+    auto none = [] {};
 
     if (tid == 0) {
         S.bad = 0;
@@ -143,11 +165,11 @@ prefill_attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap tmK)
             mbar_init(&S.accf[j], 1);
             mbar_init(&S.acce[j], 4);
         }
-        for (int j = 0; j < 2; j++) {
+        for (int j = 0; j < kAQ; j++) {
             mbar_init(&S.qfull[j], 1);
             mbar_init(&S.qfree[j], 1);
-            mbar_init(&S.ready[j], kCS);
         }
+        for (int j = 0; j < 2; j++) mbar_init(&S.ready[j], kCS);
         mbar_init(&S.fin, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -166,36 +188,40 @@ prefill_attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap tmK)
             int issued = 0, qloads = 0;
             // each K tile is read twice: kept in L2 until its second read
             const uint64_t keep = l2_policy_evict_last(), once = l2_policy_evict_first();
-            for (int ii = 0; ii < nmine && ok; ii++) {
-                const int lg = cid + ii * nclu, qb = ii & 1;
-                if (ii >= 2 && !mbar_wait(&S.qfree[qb], (uint32_t)((ii - 2) >> 1) & 1u)) {
+            auto load = [&](int gi, int lg, int t, uint64_t pol) {
+                const int s = gi % kAStages;
+                if (!mbar_wait(&S.empty[s], Ring::stage_parity(gi, kAStages) ^ 1u)) {
                     ok = false;
-                    break;
+                    return;
                 }
-                mbar_expect_tx(&S.qfull[qb], (uint32_t)kOp);
-                bulk_g2s(sm + qb * kOp, a.pack + (size_t)lg * kPackBytes, kOp, &S.qfull[qb]);
-                qloads = ii + 1;
-                const int row0 = lg * N + k0;
-                for (int j = 0; j < njob; j++) {
-                    const int gi = ii * njob + j, s = gi % kAStages;
-                    const int t = j < nt ? j : njob - 1 - j;
-                    if (!mbar_wait(&S.empty[s], Ring::stage_parity(gi, kAStages) ^ 1u)) {
+                mbar_expect_tx(&S.full[s], (uint32_t)kOp);
+                unsigned char *dst = ring + (size_t)s * kOp;
+                const int row = lg * N + k0 + t * kTk;
+                tma_2d_hint(dst, &tmK, 0, row, &S.full[s], pol);
+                tma_2d_hint(dst + kUmmaBox, &tmK, 64, row, &S.full[s], pol);
+                issued = gi + 1;
+            };
+            for (int p = 0; p <= nmine && ok; p++) {
+                if (p < nmine) {
+                    const int lg = cid + p * nclu, qb = p % kAQ;
+                    // buffer qb held Q of item p - kAQ: free once its column norms completed
+                    if (p >= kAQ && !mbar_wait(&S.qfree[qb], (uint32_t)(p / kAQ - 1) & 1u)) {
                         ok = false;
                         break;
                     }
-                    mbar_expect_tx(&S.full[s], (uint32_t)kOp);
-                    unsigned char *dst = ring + (size_t)s * kOp;
-                    const uint64_t pol = j < nt ? keep : once;
-                    tma_2d_hint(dst, &tmK, 0, row0 + t * kTk, &S.full[s], pol);
-                    tma_2d_hint(dst + kUmmaBox, &tmK, 64, row0 + t * kTk, &S.full[s], pol);
-                    issued = gi + 1;
+                    mbar_expect_tx(&S.qfull[qb], (uint32_t)kOp);
+                    bulk_g2s(sm + qb * kOp, a.pack + (size_t)lg * kPackBytes, kOp, &S.qfull[qb]);
+                    qloads = p + 1;
                 }
+                const int lgs = cid + p * nclu, lgn = cid + (p - 1) * nclu;
+                for_block(p, [&](int gi, int t) { if (ok) load(gi, lgs, t, keep); },
+                          [&](int gi, int t) { if (ok) load(gi, lgn, t, once); }, none);
             }
             if (!ok) {
                 // let the copies in flight land before the CTA may exit
                 atomicExch(&S.bad, 1);
-                for (int j = max(0, qloads - 2); j < qloads; j++)
-                    mbar_wait(&S.qfull[j & 1], (uint32_t)(j >> 1) & 1u);
+                for (int j = max(0, qloads - kAQ); j < qloads; j++)
+                    mbar_wait(&S.qfull[j % kAQ], (uint32_t)(j / kAQ) & 1u);
                 for (int j = max(0, issued - kAStages); j < issued; j++)
                     mbar_wait(&S.full[j % kAStages], Ring::stage_parity(j, kAStages));
             }
@@ -205,34 +231,36 @@ prefill_attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap tmK)
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             bool ok = true;
-            for (int ii = 0; ii < nmine && ok; ii++) {
-                const int qb = ii & 1;
-                if (!mbar_wait(&S.qfull[qb], (uint32_t)(ii >> 1) & 1u)) {
+            // one job: 8 MMAs of 128 x 128 x 16 into accumulator gi % kAcc;
+            // stat: A = Q (rows), B = K tile (keys); norm: the transpose
+            auto mma = [&](int gi, uint32_t qa, bool stat) {
+                const int s = gi % kAStages, b = gi % kAcc;
+                if (!mbar_wait(&S.full[s], Ring::stage_parity(gi, kAStages)) ||
+                    !mbar_wait(&S.acce[b], Ring::acc_parity(gi) ^ 1u)) {
+                    ok = false;
+                    return;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(b * 128);
+                const uint32_t tile = ring_s + (uint32_t)(s * kOp);
+                const uint64_t dq = umma_sdesc(qa), dt = umma_sdesc(tile);
+                const uint64_t dA = stat ? dq : dt, dB = stat ? dt : dq;
+#pragma unroll
+                for (int ks = 0; ks < 8; ks++)
+                    umma_bf16(d, umma_sdesc_step(dA, ks), umma_sdesc_step(dB, ks), kIdesc, ks > 0);
+                umma_commit(&S.accf[b]);
+                umma_commit(&S.empty[s]);     // the tile is free once its MMAs completed
+            };
+            for (int p = 0; p <= nmine && ok; p++) {
+                if (p < nmine && !mbar_wait(&S.qfull[p % kAQ], (uint32_t)(p / kAQ) & 1u)) {
                     ok = false;
                     break;
                 }
-                const uint32_t qa = q_s + (uint32_t)(qb * kOp);
-                for (int j = 0; j < njob; j++) {
-                    const int gi = ii * njob + j, s = gi % kAStages, b = gi % kAcc;
-                    if (!mbar_wait(&S.full[s], Ring::stage_parity(gi, kAStages)) ||
-                        !mbar_wait(&S.acce[b], Ring::acc_parity(gi) ^ 1u)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t d = tmem + (uint32_t)(b * 128);
-                    const uint32_t tile = ring_s + (uint32_t)(s * kOp);
-                    // stat: A = Q (rows), B = K tile (keys); norm: the transpose
-                    const uint32_t A = j < nt ? qa : tile;
-                    const uint32_t B = j < nt ? tile : qa;
-#pragma unroll
-                    for (int ks = 0; ks < 8; ks++)
-                        umma_bf16(d, umma_sdesc(A + umma_kstep(ks)), umma_sdesc(B + umma_kstep(ks)),
-                                  kIdesc, ks > 0);
-                    umma_commit(&S.accf[b]);
-                    umma_commit(&S.empty[s]);     // the tile is free once its MMAs completed
-                }
-                umma_commit(&S.qfree[qb]);        // ... and the Q buffer after the item
+                const uint32_t qs = q_s + (uint32_t)((p % kAQ) * kOp);
+                const uint32_t qn = q_s + (uint32_t)(((p + kAQ - 1) % kAQ) * kOp);
+                for_block(p, [&](int gi, int) { if (ok) mma(gi, qs, true); },
+                          [&](int gi, int) { if (ok) mma(gi, qn, false); }, none);
+                if (p >= 1) umma_commit(&S.qfree[(p - 1) % kAQ]);    // item p - 1's Q buffer
             }
             umma_commit(&S.fin);
             if (!mbar_wait(&S.fin, 0)) ok = false;
@@ -241,7 +269,7 @@ prefill_attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap tmK)
         __syncwarp();
     } else {
         // ------------------------------------------------ epilogue warps
-        const int set = (w - 2) >> 2;              // tiles t with t % 2 == set
+        const int set = (w - 2) >> 2;              // tiles t with t % kASets == set
         const int qd = w & 3;                      // tensor-memory lane quarter
         const int ln = 32 * qd + lane;             // row (stat) or tile key (norm)
         const uint32_t lane_base = tmem + ((uint32_t)(32 * qd) << 16);
@@ -249,7 +277,6 @@ prefill_attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap tmK)
         const float4 *rs4 = reinterpret_cast<const float4 *>(S.rs);
         const int jr = ln >> 2;
         const int lim = N - W + jr;                // last key window row jr sees
-        const int tlast = nt - 1 - ((nt - 1 - set) & 1);   // this set's first tile of the norm pass
         bool good = true;
 
         // wait for accumulator gi (uniform over the warp)
@@ -265,99 +292,123 @@ prefill_attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap tmK)
             if (lane == 0 && good) mbar_arrive(&S.acce[gi % kAcc]);
         };
 
-        for (int ii = 0; ii < nmine; ii++) {
-            const int lg = cid + ii * nclu;
-            const int gi0 = ii * njob;
-            float *cout = a.c2 + (size_t)lg * N + k0;
-
-            // ---------------- statistics of row ln (base-2 logits)
-            float m = -INFINITY, sum = 0.f;
-            for (int t = set; t < nt; t += 2) {
-                const int gi = gi0 + t;
+        for (int p = 0; p <= nmine; p++) {
+            const int lgs = cid + p * nclu, q = p - 1, lgn = cid + q * nclu;
+            float m = -INFINITY, sum = 0.f;        // statistics of row ln of item p (base-2 logits)
+            // ---------------- statistics job: tile t of item p
+            auto stat = [&](int gi, int t) {
+                if (t % kASets != set) return;
                 if (acquire(gi)) {
                     const uint32_t tb = lane_base + (uint32_t)((gi % kAcc) * 128);
                     const int kbase = k0 + t * kTk;
-                    float x[128];
-                    tmem_ld128(tb, x);
-                    if (!(kbase + kTk <= k1 && kbase + kTk - 1 <= N - W)) {
+                    const bool interior = kbase + kTk <= k1 && kbase + kTk - 1 <= N - W;
+#pragma unroll 1
+                    for (int hh = 0; hh < 2; hh++) {      // 64 keys at a time
+                        float x[64];
+                        tmem_ld64(tb + 64 * hh, x);
+                        if (!interior) {
 #pragma unroll
-                        for (int i = 0; i < 128; i++) {
-                            const int key = kbase + i;
-                            if (key >= k1 || key > lim) x[i] = -INFINITY;
+                            for (int i = 0; i < 64; i++) {
+                                const int key = kbase + 64 * hh + i;
+                                if (key >= k1 || key > lim) x[i] = -INFINITY;
+                            }
                         }
-                    }
-                    float mx[8];
+                        float mx[8];
 #pragma unroll
-                    for (int k = 0; k < 8; k++) mx[k] = x[k];
+                        for (int k = 0; k < 8; k++) mx[k] = x[k];
 #pragma unroll
-                    for (int i = 8; i < 128; i++) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
-                    const float tm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                           fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-                    if (tm != -INFINITY) {
-                        const float mn = fmaxf(m, tm * cs);
-                        float e[8];
+                        for (int i = 8; i < 64; i++) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+                        const float tm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                        if (tm != -INFINITY) {
+                            const float mn = fmaxf(m, tm * cs);
+                            float e[8];
 #pragma unroll
-                        for (int k = 0; k < 8; k++) e[k] = 0.f;
+                            for (int k = 0; k < 8; k++) e[k] = 0.f;
 #pragma unroll
-                        for (int i = 0; i < 128; i++) e[i & 7] += ex2_approx(fmaf(x[i], cs, -mn));
-                        sum = sum * ex2_approx(m - mn) +
-                              (((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7])));
-                        m = mn;
+                            for (int i = 0; i < 64; i++) e[i & 7] += ex2_approx(fmaf(x[i], cs, -mn));
+                            sum = sum * ex2_approx(m - mn) +
+                                  (((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7])));
+                            m = mn;
+                        }
                     }
                 }
                 release(gi);
-            }
-            // publish this set's partial statistics of row ln; one thread then
-            // tells every CTA of the cluster (release at cluster scope)
-            a.stats[(((size_t)lg * kCS + cr) * 2 + set) * kRows + ln] = make_float2(m, sum);
-            __threadfence();
-            asm volatile("bar.sync 1, 256;" ::: "memory");
-            if (tid == 64)
-                for (int q = 0; q < kCS; q++) mbar_arrive_remote(&S.ready[ii & 1], (uint32_t)q);
-            if (set == 0) {
-                bool ok = good && mbar_wait_cluster(&S.ready[ii & 1], (uint32_t)(ii >> 1) & 1u);
-                good = __all_sync(kFull, ok);
-                const float2 *st = a.stats + (size_t)lg * kCS * 2 * kRows + ln;
-                float2 v[2 * kCS];
+            };
+            // ---------------- merged statistics of item p - 1 (needed by its norm jobs)
+            auto mid = [&] {
+                if (set == 0) {
+                    bool ok = good && mbar_wait_cluster(&S.ready[q & 1], (uint32_t)(q >> 1) & 1u);
+                    good = __all_sync(kFull, ok);
+                    const float2 *st = a.stats + (size_t)lgn * kCS * kASets * kRows + ln;
+                    float2 v[kASets * kCS];
 #pragma unroll
-                for (int c = 0; c < 2 * kCS; c++) v[c] = __ldcg(st + (size_t)c * kRows);
-                float M = -INFINITY;
+                    for (int c = 0; c < kASets * kCS; c++) v[c] = __ldcg(st + (size_t)c * kRows);
+                    float M = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < 2 * kCS; c++) M = fmaxf(M, v[c].x);
-                float Z = 0.f;
+                    for (int c = 0; c < kASets * kCS; c++) M = fmaxf(M, v[c].x);
+                    float Z = 0.f;
 #pragma unroll
-                for (int c = 0; c < 2 * kCS; c++)
-                    if (v[c].x != -INFINITY) Z += v[c].y * ex2_approx(v[c].x - M);
-                // rows past the window (zero queries) and empty rows contribute 0
-                const bool live = jr < W && M != -INFINITY && Z > 0.f;
-                S.rs[ln] = live ? make_float2(M, 1.f / Z) : make_float2(0.f, 0.f);
-            }
-            asm volatile("bar.sync 1, 256;" ::: "memory");
-
-            // ---------------- column norms c^2
-            for (int t = tlast; t >= 0; t -= 2) {
-                const int gi = gi0 + njob - 1 - t;
+                    for (int c = 0; c < kASets * kCS; c++)
+                        if (v[c].x != -INFINITY) Z += v[c].y * ex2_approx(v[c].x - M);
+                    // rows past the window (zero queries) and empty rows contribute 0
+                    const bool live = jr < W && M != -INFINITY && Z > 0.f;
+                    S.rs[ln] = live ? make_float2(M, 1.f / Z) : make_float2(0.f, 0.f);
+                }
+                asm volatile("bar.sync 1, %0;" ::"n"(kAEpiWarps * 32) : "memory");
+            };
+            // ---------------- column-norm job: tile t of item p - 1, p = c r out
+            double lsum = 0.0;
+            auto norm = [&](int gi, int t) {
+                if (t % kASets != set) return;
                 const int kl = t * kTk + ln;
+                const size_t o = (size_t)lgn * N + k0 + kl;
+                // r^2 of the key (from the value-norm kernel), in flight during the wait
+                const float r2 = k0 + kl < k1 ? a.r2[o] : 0.f;
                 if (acquire(gi)) {
                     const uint32_t tb = lane_base + (uint32_t)((gi % kAcc) * 128);
                     const int jmin = k0 + kl - (N - W);     // window rows j < jmin do not see the key
-                    float x[128];
-                    tmem_ld128(tb, x);
                     float c2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+                    for (int hh = 0; hh < 2; hh++) {      // window rows 64 hh .. 64 hh + 63
+                        float x[64];
+                        tmem_ld64(tb + 64 * hh, x);
 #pragma unroll
-                    for (int j = 0; j < 32; j++) {
-                        const float4 A = rs4[2 * j], B = rs4[2 * j + 1];
-                        float sh = ex2_approx(fmaf(x[4 * j], cs, -A.x)) * A.y;
-                        sh = fmaf(ex2_approx(fmaf(x[4 * j + 1], cs, -A.z)), A.w, sh);
-                        sh = fmaf(ex2_approx(fmaf(x[4 * j + 2], cs, -B.x)), B.y, sh);
-                        sh = fmaf(ex2_approx(fmaf(x[4 * j + 3], cs, -B.z)), B.w, sh);
-                        sh = (j >= jmin) ? sh : 0.f;
-                        c2[j & 3] = fmaf(sh, sh, c2[j & 3]);
+                        for (int jj = 0; jj < 16; jj++) {
+                            const int j = 16 * hh + jj;
+                            const float4 A = rs4[2 * j], B = rs4[2 * j + 1];
+                            float sh = ex2_approx(fmaf(x[4 * jj], cs, -A.x)) * A.y;
+                            sh = fmaf(ex2_approx(fmaf(x[4 * jj + 1], cs, -A.z)), A.w, sh);
+                            sh = fmaf(ex2_approx(fmaf(x[4 * jj + 2], cs, -B.x)), B.y, sh);
+                            sh = fmaf(ex2_approx(fmaf(x[4 * jj + 3], cs, -B.z)), B.w, sh);
+                            sh = (j >= jmin) ? sh : 0.f;
+                            c2[jj & 3] = fmaf(sh, sh, c2[jj & 3]);
+                        }
                     }
-                    if (k0 + kl < k1)
-                        cout[kl] = ((c2[0] + c2[1]) + (c2[2] + c2[3])) * (1.f / (kPG * kPG));
+                    if (k0 + kl < k1) {
+                        const float pv = sqrtf(((c2[0] + c2[1]) + (c2[2] + c2[3])) *
+                                               (1.f / (kPG * kPG))) * sqrtf(r2);
+                        a.p[o] = pv;
+                        lsum += (double)pv;
+                    }
                 }
                 release(gi);
+            };
+            for_block(p, stat, norm, mid);
+            if (p >= 1) {
+                // the layer's partial sum of p
+#pragma unroll
+                for (int msk = 16; msk > 0; msk >>= 1) lsum += __shfl_xor_sync(kFull, lsum, msk);
+                if (lane == 0 && lsum != 0.0) atomicAdd(&a.layer_sum[lgn / a.Hkv], lsum);
+            }
+            if (p < nmine) {
+                // publish this set's partial statistics of row ln; one thread
+                // then tells every CTA of the cluster (release at cluster scope)
+                a.stats[(((size_t)lgs * kCS + cr) * kASets + set) * kRows + ln] = make_float2(m, sum);
+                __threadfence();
+                asm volatile("bar.sync 1, %0;" ::"n"(kAEpiWarps * 32) : "memory");
+                if (tid == 64)
+                    for (int c = 0; c < kCS; c++) mbar_arrive_remote(&S.ready[p & 1], (uint32_t)c);
             }
         }
         if (!good) atomicExch(&S.bad, 1);
@@ -368,8 +419,8 @@ prefill_attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap tmK)
         tmem_dealloc(tmem, 512);
     }
     if (tid == 0 && S.bad)
-        for (int ii = 0; ii < nmine; ii++)    // NaN: a wait timed out
-            a.layer_sum[(cid + ii * nclu) / a.Hkv] = __longlong_as_double(0x7ff8000000000000ll);
+        for (int p = 0; p < nmine; p++)    // NaN: a wait timed out
+            a.layer_sum[(cid + p * nclu) / a.Hkv] = __longlong_as_double(0x7ff8000000000000ll);
     // no CTA leaves while a peer may still arrive on its barriers
     cluster_arrive();
     cluster_wait();
@@ -383,7 +434,6 @@ prefill_attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap tmK)
 // left.  Chunks reach the MMA issuer and the epilogue through a small
 // shared-memory queue; R is reloaded only where the item changes.  Per tile: T = V_t R^T (keys x dims; R as three
 // bf16 terms accumulated into one fp32 accumulator), r^2 = sum_b T[i][b]^2.
-// Run beside the attention kernel, it takes whatever SMs that leaves free.
 constexpr int kVChunk = 4;           // tiles per chunk
 constexpr int kVQueue = 3;           // chunks posted ahead of the epilogue
 
@@ -593,13 +643,14 @@ prefill_val_kernel(ValArgs a, const __grid_constant__ CUtensorMap tmV)
                     tc_fence_after();
                     const uint32_t d = tmem + (uint32_t)(b * 128);
                     const uint32_t tile = ring_s + (uint32_t)(s * kOp);
-#pragma unroll 1
+                    const uint64_t dv = umma_sdesc(tile);
+#pragma unroll
                     for (int sp = 0; sp < 3; sp++) {
-                        const uint32_t rb = r_s + (uint32_t)(sp * kOp);
+                        const uint64_t dr = umma_sdesc(r_s + (uint32_t)(sp * kOp));
 #pragma unroll
                         for (int ks = 0; ks < 8; ks++)
-                            umma_bf16(d, umma_sdesc(tile + umma_kstep(ks)),
-                                      umma_sdesc(rb + umma_kstep(ks)), kIdesc, sp > 0 || ks > 0);
+                            umma_bf16(d, umma_sdesc_step(dv, ks), umma_sdesc_step(dr, ks), kIdesc,
+                                      sp > 0 || ks > 0);
                     }
                     umma_commit(&S.accf[b]);
                     umma_commit(&S.empty[s]);
@@ -656,34 +707,6 @@ prefill_val_kernel(ValArgs a, const __grid_constant__ CUtensorMap tmV)
     if (tid == 0 && S.bad)
         for (int l = 0; l < a.NL; l++)     // NaN: a wait timed out
             a.layer_sum[l] = __longlong_as_double(0x7ff8000000000000ll);
-}
-
-// p = c r per key and the per-layer sums of p (fp64); block b covers
-// elements [c kCombSpan, (c + 1) kCombSpan) of layer b / cpl, c = b % cpl.
-constexpr int kCombSpan = 4096;
-
-__global__ void __launch_bounds__(256) combine_kernel(float *p, const float *c2, const float *r2,
-                                                      double *layer_sum, int64_t per_layer, int cpl)
-{
-    __shared__ double red[8];
-    const int l = blockIdx.x / cpl, c = blockIdx.x % cpl;
-    const int64_t e0 = (int64_t)c * kCombSpan, e1 = min(per_layer, e0 + kCombSpan);
-    const int64_t off = (int64_t)l * per_layer;
-    double s = 0.0;
-    for (int64_t i = e0 + threadIdx.x; i < e1; i += blockDim.x) {
-        const float v = sqrtf(c2[off + i]) * sqrtf(r2[off + i]);
-        p[off + i] = v;
-        s += (double)v;
-    }
-#pragma unroll
-    for (int m = 16; m > 0; m >>= 1) s += __shfl_xor_sync(kFull, s, m);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        double t = 0.0;
-        for (int j = 0; j < 8; j++) t += red[j];
-        atomicAdd(&layer_sum[l], t);
-    }
 }
 
 // --------------------------------------------------------------- operands
@@ -837,17 +860,23 @@ __global__ void __launch_bounds__(256) factor_kernel(const uint16_t *W, float *R
 }
 
 // --------------------------------------------------------------- top-K
-struct TopkState {
-    uint32_t prefix, mask;
-    int64_t rank;          // rank still to place inside the current prefix
-    int64_t below;         // keys strictly below the final threshold
-    uint32_t thr;
-    int64_t need;          // elements taken from the tie group
+// Radix select of the B_total largest scores over an order key that ascends
+// as the score descends: three passes over the 32-bit key (bits 31-20, 19-8,
+// 7-0).  Pass k histograms the keys that match the digits picked so far; the
+// last block of the pass to finish picks the next digit (the bin holding
+// the element of the wanted rank) for the next pass.
+struct SelState {
+    int d[3];              // digits picked by passes 1-3
+    long long r[3];        // rank of the wanted element inside the picked bin
+    unsigned done[3];      // blocks finished per pass
+    uint32_t thr;          // order key of the B_total-th largest score
+    long long need;        // elements taken from the group of keys equal to thr
 };
 
 constexpr int kTkBlock = 1024;
 constexpr int kTkPer = 4;                 // elements per thread
 constexpr int kTkSpan = kTkBlock * kTkPer;
+constexpr int kH1 = 4096, kH2 = 4096, kH3 = 256;
 
 // order key: ascending key = descending score
 __device__ __forceinline__ uint32_t desc_key(float s) { return ~float_key(s); }
@@ -861,70 +890,130 @@ __global__ void layer_inv_kernel(const double *layer_sum, float *inv, int NL)
     }
 }
 
-__global__ void normalize_kernel(float *s, const float *inv, int64_t per_layer, int64_t M)
+// Bin of a histogram (n bins, ascending order key) holding the element of
+// 0-based rank `rank`, and that element's rank inside the bin; whole block.
+__device__ void block_pick(const unsigned *hist, int n, long long rank, int *scan, int *bin_out,
+                           long long *rin_out)
 {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < M;
-         i += (int64_t)gridDim.x * blockDim.x)
-        s[i] *= inv[i / per_layer];
-}
-
-__global__ void topk_hist_kernel(const float *s, int64_t M, const TopkState *st, int shift,
-                                 unsigned *hist)
-{
-    __shared__ unsigned h[256];
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0;
-    __syncthreads();
-    const uint32_t prefix = st->prefix, mask = st->mask;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < M;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const uint32_t k = desc_key(s[i]);
-        if ((k & mask) == prefix) atomicAdd(&h[(k >> shift) & 255u], 1u);
+    __shared__ int sb;
+    __shared__ long long sr;
+    const int per = (n + blockDim.x - 1) / blockDim.x;
+    const int b0 = threadIdx.x * per;
+    if (threadIdx.x == 0) {
+        sb = 0;
+        sr = 0;
+    }
+    int loc = 0;
+    for (int k = 0; k < per; k++)
+        if (b0 + k < n) loc += (int)__ldcg(hist + b0 + k);
+    int total;
+    const int ex = block_exscan(loc, scan, &total);
+    if (ex <= rank && rank < (long long)ex + loc) {
+        long long cum = ex;
+        for (int k = 0; k < per; k++) {
+            const long long h = __ldcg(hist + b0 + k);
+            if (cum + h > rank) {
+                sb = b0 + k;
+                sr = rank - cum;
+                break;
+            }
+            cum += h;
+        }
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < 256; i += blockDim.x)
+    *bin_out = sb;
+    *rin_out = sr;
+    __syncthreads();
+}
+
+// warp-aggregated shared-memory histogram increment (bin < 0: no element);
+// every lane of the warp calls it
+__device__ __forceinline__ void hist_add(unsigned *h, int bin)
+{
+    const unsigned same = __match_any_sync(kFull, bin);
+    if (bin >= 0 && (threadIdx.x & 31) == __ffs(same) - 1) atomicAdd(&h[bin], (unsigned)__popc(same));
+}
+
+// Pass kPass of the select.  Pass 1 also normalizes in place (s = p inv[l]).
+template <int kPass>
+__global__ void __launch_bounds__(kTkBlock) sel_pass_kernel(float *s, int M, const float *inv,
+                                                              int per_layer, int normalize,
+                                                              unsigned *hist, long long rank0,
+                                                              SelState *ss)
+{
+    constexpr int NB = kPass == 3 ? kH3 : kH1;
+    __shared__ unsigned h[NB];
+    __shared__ int scan[40];
+    __shared__ int last;
+    const uint32_t pre = kPass == 1 ? 0u
+                       : kPass == 2 ? (uint32_t)ss->d[0]
+                                    : (((uint32_t)ss->d[0] << 12) | (uint32_t)ss->d[1]);
+    for (int i = threadIdx.x; i < NB; i += blockDim.x) h[i] = 0;
+    __syncthreads();
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long base = (long long)blockIdx.x * blockDim.x; base < M; base += 4 * stride) {
+        float v[4];
+#pragma unroll
+        for (int u = 0; u < 4; u++) {        // four loads in flight
+            const long long i = base + u * stride + threadIdx.x;
+            v[u] = i < M ? s[i] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+            const long long i = base + u * stride + threadIdx.x;
+            int bin = -1;
+            if (i < M) {
+                if (kPass == 1 && normalize) {
+                    v[u] *= inv[(int)i / per_layer];
+                    s[i] = v[u];
+                }
+                const uint32_t k = desc_key(v[u]);
+                if (kPass == 1) bin = (int)(k >> 20);
+                else if (kPass == 2) { if ((k >> 20) == pre) bin = (int)((k >> 8) & (kH2 - 1)); }
+                else if ((k >> 8) == pre) bin = (int)(k & (kH3 - 1));
+            }
+            hist_add(h, bin);
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < NB; i += blockDim.x)
         if (h[i]) atomicAdd(&hist[i], h[i]);
-}
-
-__global__ void topk_pick_kernel(TopkState *st, unsigned *hist, int shift, int64_t rank0)
-{
-    if (threadIdx.x != 0) return;
-    if (shift == 24) {
-        st->rank = rank0;
-    }
-    int64_t rank = st->rank, cum = 0;
-    int b = 0;
-    for (; b < 255; b++) {
-        if (cum + (int64_t)hist[b] > rank) break;
-        cum += hist[b];
-    }
-    st->prefix |= (uint32_t)b << shift;
-    st->mask |= 255u << shift;
-    st->rank = rank - cum;
-    for (int i = 0; i < 256; i++) hist[i] = 0;
-    if (shift == 0) {
-        st->thr = st->prefix;
-        st->below = rank0 - st->rank;
-        st->need = st->rank + 1;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last = atomicAdd(&ss->done[kPass - 1], 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!last) return;
+    // the last block: every block's counts are in; pick this pass's digit
+    __threadfence();
+    int d;
+    long long r;
+    block_pick(hist, NB, kPass == 1 ? rank0 : ss->r[kPass - 2], scan, &d, &r);
+    if (threadIdx.x == 0) {
+        ss->d[kPass - 1] = d;
+        ss->r[kPass - 1] = r;
+        if (kPass == 3) {
+            ss->thr = ((uint32_t)ss->d[0] << 20) | ((uint32_t)ss->d[1] << 8) | (uint32_t)d;
+            ss->need = r + 1;
+        }
     }
 }
 
-// per block: elements below the threshold and equal to it
-__global__ void __launch_bounds__(kTkBlock) topk_count_kernel(const float *s, int64_t M,
-                                                               const TopkState *st, int *lt,
-                                                               int *eq)
+// per block of kTkSpan elements (4 consecutive per thread): elements below
+// the threshold key and equal to it
+__global__ void __launch_bounds__(kTkBlock) topk_count_kernel(const float *s, int M,
+                                                               const SelState *ss, int *lt, int *eq)
 {
     __shared__ int scan[40];
-    const uint32_t thr = st->thr;
+    const uint32_t thr = ss->thr;
+    const long long i0 = (long long)blockIdx.x * kTkSpan + kTkPer * threadIdx.x;
     int nlt = 0, neq = 0;
-    const int64_t base = (int64_t)blockIdx.x * kTkSpan;
-    for (int k = 0; k < kTkPer; k++) {
-        const int64_t i = base + (int64_t)k * kTkBlock + threadIdx.x;
-        if (i < M) {
-            const uint32_t key = desc_key(s[i]);
+#pragma unroll
+    for (int u = 0; u < kTkPer; u++)
+        if (i0 + u < M) {
+            const uint32_t key = desc_key(s[i0 + u]);
             nlt += key < thr;
             neq += key == thr;
         }
-    }
     int tlt, teq;
     block_exscan(nlt, scan, &tlt);
     block_exscan(neq, scan, &teq);
@@ -936,14 +1025,14 @@ __global__ void __launch_bounds__(kTkBlock) topk_count_kernel(const float *s, in
 
 // one block: offsets of the tie group and of the kept elements per block
 __global__ void __launch_bounds__(kTkBlock) topk_scan_kernel(const int *lt, const int *eq, int nblk,
-                                                              const TopkState *st, int64_t *eq_off,
+                                                              const SelState *ss, int64_t *eq_off,
                                                               int64_t *keep_off)
 {
     __shared__ int scan[40];
     __shared__ int64_t carry[2];
     if (threadIdx.x == 0) carry[0] = carry[1] = 0;
     __syncthreads();
-    const int64_t need = st->need;
+    const int64_t need = ss->need;
     for (int b0 = 0; b0 < nblk; b0 += blockDim.x) {
         const int b = b0 + threadIdx.x;
         const int e = b < nblk ? eq[b] : 0;
@@ -967,36 +1056,47 @@ __global__ void __launch_bounds__(kTkBlock) topk_scan_kernel(const int *lt, cons
     }
 }
 
-__global__ void __launch_bounds__(kTkBlock) topk_write_kernel(const float *s, int64_t M, int N,
-                                                               const TopkState *st,
+// keep mask, per-(layer, KV head) counts and ascending kept indices; equal
+// keys are kept in flat order up to `need`
+__global__ void __launch_bounds__(kTkBlock) topk_write_kernel(const float *s, int M, int N,
+                                                               const SelState *ss,
                                                                const int64_t *eq_off,
                                                                const int64_t *keep_off,
                                                                uint8_t *keep, int *counts,
                                                                int64_t *idx)
 {
     __shared__ int scan[40];
-    const uint32_t thr = st->thr;
-    const int64_t need = st->need;
-    int64_t eo = eq_off[blockIdx.x], ko = keep_off[blockIdx.x];
-    const int64_t base = (int64_t)blockIdx.x * kTkSpan;
-    for (int k = 0; k < kTkPer; k++) {
-        const int64_t i = base + (int64_t)k * kTkBlock + threadIdx.x;
-        uint32_t key = 0xffffffffu;
-        const bool in = i < M;
-        if (in) key = desc_key(s[i]);
-        const int iseq = in && key == thr;
-        int teq;
-        const int er = block_exscan(iseq, scan, &teq);
-        const int kp = in && (key < thr || (iseq && eo + er < need));
-        int tkp;
-        const int kr = block_exscan(kp, scan, &tkp);
-        if (in) keep[i] = (uint8_t)kp;
-        if (kp) {
-            if (idx) idx[ko + kr] = i;
-            if (counts) atomicAdd(&counts[i / N], 1);
+    const uint32_t thr = ss->thr;
+    const int64_t need = ss->need;
+    const long long i0 = (long long)blockIdx.x * kTkSpan + kTkPer * threadIdx.x;
+    uint32_t key[kTkPer];
+    int neq = 0;
+#pragma unroll
+    for (int u = 0; u < kTkPer; u++) {
+        key[u] = i0 + u < M ? desc_key(s[i0 + u]) : 0xffffffffu;
+        neq += i0 + u < M && key[u] == thr;
+    }
+    int teq;
+    int64_t er = eq_off[blockIdx.x] + block_exscan(neq, scan, &teq);   // tie rank of my first equal key
+    bool kp[kTkPer];
+    int nk = 0;
+#pragma unroll
+    for (int u = 0; u < kTkPer; u++) {
+        const bool in = i0 + u < M;
+        const bool iseq = in && key[u] == thr;
+        kp[u] = in && (key[u] < thr || (iseq && er < need));
+        er += iseq;
+        nk += kp[u];
+    }
+    int tk;
+    int64_t ko = keep_off[blockIdx.x] + block_exscan(nk, scan, &tk);
+#pragma unroll
+    for (int u = 0; u < kTkPer; u++) {
+        if (i0 + u < M) keep[i0 + u] = (uint8_t)kp[u];
+        if (kp[u]) {
+            if (idx) idx[ko++] = i0 + u;
+            if (counts) atomicAdd(&counts[(i0 + u) / N], 1);
         }
-        eo += teq;
-        ko += tkp;
     }
 }
 
@@ -1008,7 +1108,7 @@ struct PfWs {
     int *counter;                // [0]: next unopened item, [1 + i]: next tile of item i
     unsigned char *pack;
     float2 *stats;
-    TopkState *st;
+    SelState *st;
     unsigned *hist;
     int *lt, *eq;
     int64_t *eq_off, *keep_off;
@@ -1033,48 +1133,15 @@ PfWs pf_layout(int NL, int Hkv, int N, void *base)
     w.r2 = reinterpret_cast<float *>(take((size_t)M * 4));
     w.counter = reinterpret_cast<int *>(take((size_t)(NL * Hkv + 1) * 4));
     w.pack = reinterpret_cast<unsigned char *>(take((size_t)NL * Hkv * kPackBytes));
-    w.stats = reinterpret_cast<float2 *>(take((size_t)NL * Hkv * kCS * 2 * kRows * sizeof(float2)));
-    w.st = reinterpret_cast<TopkState *>(take(sizeof(TopkState)));
-    w.hist = reinterpret_cast<unsigned *>(take(256 * 4));
+    w.stats = reinterpret_cast<float2 *>(take((size_t)NL * Hkv * kCS * kASets * kRows * sizeof(float2)));
+    w.st = reinterpret_cast<SelState *>(take(sizeof(SelState)));
+    w.hist = reinterpret_cast<unsigned *>(take((size_t)(kH1 + kH2 + kH3) * 4));
     w.lt = reinterpret_cast<int *>(take((size_t)nblk * 4));
     w.eq = reinterpret_cast<int *>(take((size_t)nblk * 4));
     w.eq_off = reinterpret_cast<int64_t *>(take((size_t)nblk * 8));
     w.keep_off = reinterpret_cast<int64_t *>(take((size_t)nblk * 8));
     w.bytes = off;
     return w;
-}
-
-// A second stream per device (and the events that fork to it and join back)
-// for the kernels of a call that run side by side; one call at a time
-// enqueues on it (mu).
-struct SideStream {
-    std::mutex mu;
-    cudaStream_t s = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
-};
-
-SideStream *side_stream(int dev)
-{
-    constexpr int kMaxDev = 64;
-    static SideStream table[kMaxDev];
-    static std::mutex init_mu;
-    if (dev < 0 || dev >= kMaxDev) {
-        set_error("kvc_prefill_score: device %d out of range", dev);
-        return nullptr;
-    }
-    SideStream &t = table[dev];
-    std::lock_guard<std::mutex> lock(init_mu);
-    if (t.s == nullptr) {
-        cudaError_t e = cudaStreamCreateWithFlags(&t.s, cudaStreamNonBlocking);
-        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&t.fork, cudaEventDisableTiming);
-        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&t.join, cudaEventDisableTiming);
-        if (e != cudaSuccess) {
-            set_error("kvc_prefill_score: side stream: %s", cudaGetErrorString(e));
-            t.s = nullptr;
-            return nullptr;
-        }
-    }
-    return &t;
 }
 
 }  // namespace
@@ -1157,9 +1224,9 @@ kvc_status kvc_prefill_score(int32_t NL, int32_t Hq, int32_t Hkv, int32_t d, int
              "kvc_prefill_score: tensor map encoding failed");
     kvc_status s = pf_cuda(cudaMemsetAsync(pw.layer_sum, 0, (size_t)NL * 8, st), "memset");
     if (s != KVC_OK) return s;
-    s = pf_cuda(cudaMemsetAsync(pw.st, 0, sizeof(TopkState), st), "memset");
+    s = pf_cuda(cudaMemsetAsync(pw.st, 0, sizeof(SelState), st), "memset");
     if (s != KVC_OK) return s;
-    s = pf_cuda(cudaMemsetAsync(pw.hist, 0, 256 * 4, st), "memset");
+    s = pf_cuda(cudaMemsetAsync(pw.hist, 0, (size_t)(kH1 + kH2 + kH3) * 4, st), "memset");
     if (s != KVC_OK) return s;
     s = pf_cuda(cudaMemsetAsync(pw.counter, 0, (size_t)(NL * Hkv + 1) * 4, st), "memset");
     if (s != KVC_OK) return s;
@@ -1171,27 +1238,27 @@ kvc_status kvc_prefill_score(int32_t NL, int32_t Hq, int32_t Hkv, int32_t d, int
     pack_kernel<<<NL * Hkv, 256, 0, st>>>(q_win, R, pw.pack, Hq, Hkv, w);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return pf_cuda(e, "kvc_prefill_score pack launch");
-    // The attention kernel (c^2 into the score buffer) and the value-norm
-    // kernel (r^2) are independent: the value kernel runs on a second stream
-    // and takes the SMs the attention clusters leave free; p = c r after both.
+    // value norms r^2, then the attention kernel's column norms c^2 into the
+    // score buffer, then p = c r with the per-layer sums
     const int ntl = (N + kTk - 1) / kTk;
     const long long total = (long long)NL * Hkv * ntl;
     int dev = 0, nsm = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
         (e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
         return pf_cuda(e, "kvc_prefill_score device query");
-    SideStream *side = side_stream(dev);
-    if (side == nullptr) return KVC_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(side->mu);
-
+    e = cudaFuncSetAttribute(prefill_val_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kVDyn);
+    if (e != cudaSuccess) return pf_cuda(e, "kvc_prefill_score attribute");
     const int nitem = NL * Hkv;
-    AttnArgs aa{pw.pack, pbuf, pw.stats, pw.layer_sum, Hkv, N, w, per_cta, nitem,
+    ValArgs va{pw.pack, pw.r2, pw.layer_sum, pw.counter, pw.counter + 1, NL, N, ntl, nitem};
+    prefill_val_kernel<<<(unsigned)std::min<long long>((total + kVChunk - 1) / kVChunk, nsm), kVThreads,
+                         kVDyn, st>>>(va, tmV);
+    if ((e = cudaGetLastError()) != cudaSuccess) return pf_cuda(e, "kvc_prefill_score value launch");
+
+    AttnArgs aa{pw.pack, pw.r2, pbuf, pw.stats, pw.layer_sum, Hkv, N, w, per_cta, nitem,
                 (float)(1.4426950408889634 / sqrt((double)kD))};
     e = cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kADyn);
-    if (e != cudaSuccess) return pf_cuda(e, "kvc_prefill_score attribute");
-    e = cudaFuncSetAttribute(prefill_val_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kVDyn);
     if (e != cudaSuccess) return pf_cuda(e, "kvc_prefill_score attribute");
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kAThreads);
@@ -1211,41 +1278,30 @@ kvc_status kvc_prefill_score(int32_t NL, int32_t Hq, int32_t Hkv, int32_t d, int
         nclu = std::max(1, nsm / (2 * kCS));
     (void)cudaGetLastError();
     cfg.gridDim = dim3(kCS * std::min(nitem, nclu));
-
-    if ((e = cudaEventRecord(side->fork, st)) != cudaSuccess ||
-        (e = cudaStreamWaitEvent(side->s, side->fork, 0)) != cudaSuccess)
-        return pf_cuda(e, "kvc_prefill_score stream fork");
     e = cudaLaunchKernelEx(&cfg, prefill_attn_kernel, aa, tmK);
     if (e != cudaSuccess) return pf_cuda(e, "kvc_prefill_score attention launch");
-    ValArgs va{pw.pack, pw.r2, pw.layer_sum, pw.counter, pw.counter + 1, NL, N, ntl, nitem};
-    prefill_val_kernel<<<(unsigned)std::min<long long>((total + kVChunk - 1) / kVChunk, nsm), kVThreads,
-                         kVDyn, side->s>>>(va, tmV);
-    if ((e = cudaGetLastError()) != cudaSuccess) return pf_cuda(e, "kvc_prefill_score value launch");
-    if ((e = cudaEventRecord(side->join, side->s)) != cudaSuccess ||
-        (e = cudaStreamWaitEvent(st, side->join, 0)) != cudaSuccess)
-        return pf_cuda(e, "kvc_prefill_score stream join");
     const int64_t per_layer = (int64_t)Hkv * N;
-    const int cpl = (int)((per_layer + kCombSpan - 1) / kCombSpan);
-    combine_kernel<<<NL * cpl, 256, 0, st>>>(pbuf, pbuf, pw.r2, pw.layer_sum, per_layer, cpl);
-    if ((e = cudaGetLastError()) != cudaSuccess) return pf_cuda(e, "kvc_prefill_score combine launch");
 
-    if (normalize) {
-        layer_inv_kernel<<<1, 256, 0, st>>>(pw.layer_sum, pw.inv, NL);
-        normalize_kernel<<<4 * 152, 256, 0, st>>>(pbuf, pw.inv, (int64_t)Hkv * N, M);
-        if ((e = cudaGetLastError()) != cudaSuccess) return pf_cuda(e, "normalize launch");
-    }
-    const int nblk = (int)((M + kTkSpan - 1) / kTkSpan);
+    // radix select of the B_total largest s (pass 1 also normalizes in place)
+    if (normalize) layer_inv_kernel<<<1, 256, 0, st>>>(pw.layer_sum, pw.inv, NL);
+    const int sel_grid = (int)std::min<int64_t>((M + kTkBlock - 1) / kTkBlock, 2 * (int64_t)nsm);
+    unsigned *h1 = pw.hist, *h2 = h1 + kH1, *h3 = h2 + kH2;
+    const long long rank0 = B_total > 0 ? B_total - 1 : 0;
+    sel_pass_kernel<1><<<sel_grid, kTkBlock, 0, st>>>(pbuf, (int)M, pw.inv, (int)per_layer, normalize, h1,
+                                                      rank0, pw.st);
+    if ((e = cudaGetLastError()) != cudaSuccess) return pf_cuda(e, "kvc_prefill_score select launch");
     if (B_total == 0) {
         s = pf_cuda(cudaMemsetAsync(keep, 0, (size_t)M, st), "memset");
         return s;
     }
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        topk_hist_kernel<<<min(nblk * 4, 4 * 152), 512, 0, st>>>(pbuf, M, pw.st, shift, pw.hist);
-        topk_pick_kernel<<<1, 32, 0, st>>>(pw.st, pw.hist, shift, B_total - 1);
-    }
-    topk_count_kernel<<<nblk, kTkBlock, 0, st>>>(pbuf, M, pw.st, pw.lt, pw.eq);
+    sel_pass_kernel<2><<<sel_grid, kTkBlock, 0, st>>>(pbuf, (int)M, pw.inv, (int)per_layer, 0, h2, rank0,
+                                                      pw.st);
+    sel_pass_kernel<3><<<sel_grid, kTkBlock, 0, st>>>(pbuf, (int)M, pw.inv, (int)per_layer, 0, h3, rank0,
+                                                      pw.st);
+    const int nblk = (int)((M + kTkSpan - 1) / kTkSpan);
+    topk_count_kernel<<<nblk, kTkBlock, 0, st>>>(pbuf, (int)M, pw.st, pw.lt, pw.eq);
     topk_scan_kernel<<<1, kTkBlock, 0, st>>>(pw.lt, pw.eq, nblk, pw.st, pw.eq_off, pw.keep_off);
-    topk_write_kernel<<<nblk, kTkBlock, 0, st>>>(pbuf, M, N, pw.st, pw.eq_off, pw.keep_off, keep,
+    topk_write_kernel<<<nblk, kTkBlock, 0, st>>>(pbuf, (int)M, N, pw.st, pw.eq_off, pw.keep_off, keep,
                                                  counts, idx);
     return pf_cuda(cudaGetLastError(), "kvc_prefill_score top-K launch");
 }

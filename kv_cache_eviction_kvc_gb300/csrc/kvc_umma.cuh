@@ -37,6 +37,14 @@ __device__ __forceinline__ uint64_t umma_sdesc(uint32_t saddr)
     return d;
 }
 
+// Descriptor of k-step ks of an operand whose k-step 0 has descriptor d0: the
+// steps differ only in the start-address field (address >> 4, no carry for a
+// shared-memory address), so this is one 64-bit add of a constant.
+__device__ __forceinline__ uint64_t umma_sdesc_step(uint64_t d0, int ks)
+{
+    return d0 + (uint64_t)(umma_kstep(ks) >> 4);
+}
+
 // Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1), A and
 // B bf16 (bits 7-9 = 1, bits 10-12 = 1), both K-major (bits 15, 16 = 0),
 // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
@@ -166,6 +174,22 @@ __device__ __forceinline__ void tmem_ld128(uint32_t addr, float (&v)[128])
         v[32 + i] = __uint_as_float(r1[i]);
         v[64 + i] = __uint_as_float(r2[i]);
         v[96 + i] = __uint_as_float(r3[i]);
+    }
+}
+
+// 64 consecutive fp32 columns of this warp's 32 lanes: two loads in flight.
+__device__ __forceinline__ void tmem_ld64(uint32_t addr, float (&v)[64])
+{
+    uint32_t r0[32], r1[32];
+    tmem_ld32_async(addr, r0);
+    tmem_ld32_async(addr + 32, r1);
+    tmem_wait_ld();
+    tmem_bind(r0);
+    tmem_bind(r1);
+#pragma unroll
+    for (int i = 0; i < 32; i++) {
+        v[i] = __uint_as_float(r0[i]);
+        v[32 + i] = __uint_as_float(r1[i]);
     }
 }
 
