@@ -155,7 +155,7 @@ def run_prefill(pc, dev, reps=5):
             "roofline": {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
                          "frac": ach / peak, "peak_kind": kind, "bytes_per_call": by,
                          "algorithmic_tflops": fl / (ms * 1e-3) / 1e12,
-                         "kernels": "prefill_score_kernel + normalize + radix top-K"},
+                         "kernels": "pack + prefill_val + prefill_attn + radix select"},
             "kept": int(counts.sum().item())}
 
 
