@@ -101,6 +101,7 @@ struct FusedSmem {
     float lzR[G];
     float mass[G];
     float ae[G];                // exp(x_e - M) of the victim (refresh)
+    double igl[G];              // 1 / merged sum (refresh)
     float pk[kD], pv[kD];       // victim key / value as published by its owner
     float pvp;                  // (never modified after publication)
     int32_t pvpos;
@@ -202,15 +203,40 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
     const int L = a.L;
     const bool refresh = is_refresh(a.t, a.T);
     const size_t ubase = (size_t)u * a.cap;
+    const int s0 = min(L, r * ch), s1 = min(L, s0 + ch);
+    const int ntile = (s1 - s0 + kTile - 1) / kTile;
+
+    // The ring starts before anything else: the first kStages K tiles of this
+    // CTA's range depend on nothing but the geometry, so they are in flight
+    // while the step's scalars, q and the moments are read.
+    if (tid == 0) {
+        for (int j = 0; j < kStages; j++) {
+            mbar_init(&S.full[j], 1);
+            mbar_init(&S.empty[j], kNC);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const int pre = min(kStages, ntile);    // K tiles issued up front (stages 0..pre-1)
+    if (w == kNC && lane == 0) {
+        const int row0 = (int)(ubase + s0);
+        for (int g = 0; g < pre; g++) {
+            mbar_expect_tx(&S.full[g], (uint32_t)kTileBytes);
+            unsigned char *dst = ring + (size_t)g * kTileBytes;
+            tma_2d(dst, &tmK, 0, row0 + g * kTile, &S.full[g]);
+            tma_2d(dst + kBoxBytes, &tmK, 64, row0 + g * kTile, &S.full[g]);
+        }
+    }
     const int n_old = a.len[u];
     if (n_old != L) {                      // uniform over the cluster
         if (r == 0 && tid == 0) {
             record_status(a.status, KVC_ERR_SHAPE);
             a.n_evict[u] = 0;
         }
+        if (w == kNC && lane == 0)         // the copies land before the CTA leaves
+            for (int g = 0; g < pre; g++) mbar_wait(&S.full[g], 0);
         return;
     }
-    const int s0 = min(L, r * ch), s1 = min(L, s0 + ch);
     const bool has_new = refresh && (r == CS - 1);
     const int nloc = (s1 - s0) + (has_new ? 1 : 0);
     const float rs = rsqrtf((float)kD);
@@ -227,11 +253,6 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
     }
     if (tid == 0) {
         S.qvalid = 0; S.direct = 0; S.ncand = 0; S.bad = 0; S.n0 = a.mn[u];
-        for (int j = 0; j < kStages; j++) {
-            mbar_init(&S.full[j], 1);
-            mbar_init(&S.empty[j], kNC);
-        }
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
 
@@ -281,6 +302,8 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
                     record_status(a.status, KVC_ERR_INVALID_ARG);
                     a.n_evict[u] = 0;
                 }
+                if (w == kNC && lane == 0)          // the copies land before the CTA leaves
+                    for (int g = 0; g < pre; g++) mbar_wait(&S.full[g], 0);
                 return;
             }
         }
@@ -297,7 +320,6 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
     // hi + lo halves (two MMAs), so no online rescaling is needed.
     const uint16_t *Vu = a.V + ubase * kD;
     const int nrows = s1 - s0;
-    const int ntile = (nrows + kTile - 1) / kTile;
     const int gq = lane >> 2, tq = lane & 3;        // mma fragment coordinates
     const uint32_t ring_s = smem_u32(ring);
     float O[8][4];                                   // O^T fragments: dims 16 m + gq (+8), heads 2 tq (+1)
@@ -400,12 +422,12 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
     } else if (w == kNC) {
         // ---------------- producer
         if (lane == 0) {
-            int g = 0;
+            int g = pre;                    // the first pre K tiles are in flight already
             bool ok = true;
             const int row0 = (int)((size_t)u * a.cap + s0);
             for (int pass = 0; pass < 2 && ok; pass++) {
                 const CUtensorMap *map = pass == 0 ? &tmK : &tmV;
-                for (int t = 0; t < ntile; t++, g++) {
+                for (int t = pass == 0 ? pre : 0; t < ntile; t++, g++) {
                     const int stage = g % kStages;
                     const uint32_t ph = (uint32_t)(g / kStages) & 1u;
                     if (!mbar_wait(&S.empty[stage], ph ^ 1u)) { ok = false; break; }
@@ -731,21 +753,30 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
     if (refresh) {
         // -------------------------------------------- probabilities + utilities
         const double al = (double)a.alpha;
+        if (tid < G) S.igl[tid] = 1.0 / (double)S.gl[tid];      // one fp64 division per head
+        // the old utilities and the positions first: independent loads, all
+        // in flight at once, staged in shared memory
+        for (int li = tid; li < nloc; li += blockDim.x) {
+            const int i = s0 + li;
+            const bool isv = (i == L);
+            msm[li] = isv ? __longlong_as_double(0x7ff0000000000000ll) : a.util[ubase + i];
+            possm[li] = isv ? a.new_pos : a.pos[ubase + i];
+        }
+        __syncthreads();
         for (int li = tid; li < nloc; li += blockDim.x) {
             const int i = s0 + li;
             double s = 0.0;
 #pragma unroll
-            for (int h = 0; h < G; h++) s += exp_wide(XS(h, li) - S.gM[h]) / (double)S.gl[h];
-            s /= G;
+            for (int h = 0; h < G; h++) s = fma(exp_wide(XS(h, li) - S.gM[h]), S.igl[h], s);
+            s *= 1.0 / G;                  // G is a power of two: exact
             const bool isv = (i == L);
-            const double m = isv ? __longlong_as_double(0x7ff0000000000000ll) : a.util[ubase + i];
+            const double m = msm[li];
             double mn;
             if (isinf(m)) mn = s;
             else if (a.rule == KVC_RULE_SINGLE) mn = s;
             else if (a.rule == KVC_RULE_CUMULATIVE) mn = m + s;
             else mn = al * m + (1.0 - al) * s;
             msm[li] = mn;
-            possm[li] = isv ? a.new_pos : a.pos[ubase + i];
             chosen[li] = 0;
             if (!isv) a.util[ubase + i] = mn;
             else S.vm = mn;
@@ -753,33 +784,69 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
         }
         __syncthreads();
         // -------------------------------------------- local T lowest
+        // Each warp finds the `want` lowest (utility, position) pairs among
+        // its own slots (li = 32 w + lane + 32 kWarps j), with no block
+        // barrier: every lane keeps the minimum of its own slots, a round is
+        // a warp argmin over those, and only the lane that owned the winner
+        // rescans its slots.  Thread 0 then merges the sorted per-warp lists.
         const int want = min(a.T, nloc);
-        for (int rnd = 0; rnd < want; rnd++) {
+        Cand *wl = reinterpret_cast<Cand *>(chosen + align_up((size_t)(ch + 1)));   // [kWarps][kMaxQueue]
+        auto lane_min = [&]() {
             Cand best{~0ull, 0x7fffffff, -1};
-            for (int li = tid; li < nloc; li += blockDim.x) {
+            for (int li = w * 32 + lane; li < nloc; li += kWarps * 32) {
                 if (chosen[li]) continue;
                 Cand cd{double_key(msm[li]), possm[li], s0 + li};
                 if (cand_less(cd, best)) best = cd;
             }
+            return best;
+        };
+        Cand mine = lane_min();
+        for (int rnd = 0; rnd < want; rnd++) {
+            Cand best = mine;
 #pragma unroll
             for (int m = 16; m > 0; m >>= 1) {
                 Cand o = shfl_cand(best, m);
                 if (cand_less(o, best)) best = o;
             }
-            if (lane == 0) S.bc[w] = best;
-            __syncthreads();
-            if (tid == 0) {
-                Cand b = S.bc[0];
-                for (int j = 1; j < kWarps; j++)
-                    if (cand_less(S.bc[j], b)) b = S.bc[j];
-                S.cand[rnd] = b;
-                chosen[b.slot - s0] = 1;
+            if (lane == 0) wl[w * kMaxQueue + rnd] = best;
+            if (best.slot >= 0 && ((best.slot - s0) & 31) == lane) {
+                chosen[best.slot - s0] = 1;
+                mine = lane_min();
             }
-            __syncthreads();
+            __syncwarp();
         }
-        if (tid == 0) S.ncand = want;
+        __syncthreads();
+        if (tid == 0) {
+            int ptr[kWarps];
+            for (int q = 0; q < kWarps; q++) ptr[q] = 0;
+            int nc = 0;
+            for (; nc < want; nc++) {
+                int bq = -1;
+                Cand b{~0ull, 0x7fffffff, -1};
+                for (int q = 0; q < kWarps; q++) {
+                    if (ptr[q] >= want) continue;
+                    const Cand cq = wl[q * kMaxQueue + ptr[q]];
+                    if (cq.slot >= 0 && cand_less(cq, b)) {
+                        b = cq;
+                        bq = q;
+                    }
+                }
+                if (bq < 0) break;
+                ptr[bq]++;
+                S.cand[nc] = b;
+            }
+            S.ncand = nc;
+        }
         cluster.sync();                                                // candidates visible
-        // every CTA merges the candidate lists the same way
+        // every CTA merges the candidate lists the same way: one parallel
+        // gather over distributed shared memory, then a local merge
+        Cand *gc = wl + kWarps * kMaxQueue;                  // [CS][kMaxQueue]
+        for (int e = tid; e < CS * a.T; e += blockDim.x) {
+            const int q = e / a.T, jj = e % a.T;
+            FusedSmem<G> *R = cluster.map_shared_rank(&S, q);
+            gc[q * kMaxQueue + jj] = jj < R->ncand ? R->cand[jj] : Cand{~0ull, 0x7fffffff, -1};
+        }
+        __syncthreads();
         if (tid == 0) {
             int ptr[kFusedMaxCS];
             for (int q = 0; q < CS; q++) ptr[q] = 0;
@@ -789,9 +856,10 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
                 int bq = -1;
                 Cand b{~0ull, 0x7fffffff, -1};
                 for (int q = 0; q < CS; q++) {
-                    FusedSmem<G> *R = cluster.map_shared_rank(&S, q);
-                    if (ptr[q] < R->ncand && cand_less(R->cand[ptr[q]], b)) {
-                        b = R->cand[ptr[q]];
+                    if (ptr[q] >= a.T) continue;
+                    const Cand cq = gc[q * kMaxQueue + ptr[q]];
+                    if (cq.slot >= 0 && cand_less(cq, b)) {
+                        b = cq;
                         bq = q;
                     }
                 }
@@ -915,7 +983,7 @@ static cudaError_t launch_fused_g(const FusedArgs &a0, int U, int CS, cudaStream
 {
     FusedArgs a = a0;
     const size_t sel = align_up((size_t)(a.chunk + 1) * 8) + align_up((size_t)(a.chunk + 1) * 4) +
-                       align_up((size_t)(a.chunk + 1));
+                       align_up((size_t)(a.chunk + 1)) + (size_t)(kWarps + kFusedMaxCS) * kMaxQueue * sizeof(Cand);
     if (sel > (size_t)kStages * kTileBytes) return cudaErrorNotSupported;
     CUtensorMap tmK, tmV;
     const uint64_t rows = (uint64_t)U * (uint64_t)a.cap;
