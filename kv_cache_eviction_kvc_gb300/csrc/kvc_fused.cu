@@ -101,7 +101,8 @@ struct FusedSmem {
     float lzR[G];
     float mass[G];
     float ae[G];                // exp(x_e - M) of the victim (refresh)
-    double igl[G];              // 1 / merged sum (refresh)
+    double igl[G];              // (1/G) / merged sum (refresh)
+    float igl32[G];
     float pk[kD], pv[kD];       // victim key / value as published by its owner
     float pvp;                  // (never modified after publication)
     int32_t pvpos;
@@ -753,7 +754,12 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
     if (refresh) {
         // -------------------------------------------- probabilities + utilities
         const double al = (double)a.alpha;
-        if (tid < G) S.igl[tid] = 1.0 / (double)S.gl[tid];      // one fp64 division per head
+        if (tid < G) {
+            // (1/G) / merged sum per head: one fp64 division per head; G is a
+            // power of two, so the 1/G factor is exact
+            S.igl[tid] = (1.0 / G) / (double)S.gl[tid];
+            S.igl32[tid] = (float)S.igl[tid];
+        }
         // the old utilities and the positions first: independent loads, all
         // in flight at once, staged in shared memory
         for (int li = tid; li < nloc; li += blockDim.x) {
@@ -765,10 +771,27 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
         __syncthreads();
         for (int li = tid; li < nloc; li += blockDim.x) {
             const int i = s0 + li;
-            double s = 0.0;
+            // head-mean probability.  While the largest head term is above
+            // e^-60 the sum is far inside fp32's range (a term fp32 would
+            // flush is below 1e-8 of it) and fp32 carries it to a few units
+            // in the last place; below that the fp64 form keeps the range.
+            float y[G], ymax = -INFINITY;
 #pragma unroll
-            for (int h = 0; h < G; h++) s = fma(exp_wide(XS(h, li) - S.gM[h]), S.igl[h], s);
-            s *= 1.0 / G;                  // G is a power of two: exact
+            for (int h = 0; h < G; h++) {
+                y[h] = XS(h, li) - S.gM[h];
+                ymax = fmaxf(ymax, y[h]);
+            }
+            double s;
+            if (ymax > -60.f) {
+                float s32 = 0.f;
+#pragma unroll
+                for (int h = 0; h < G; h++) s32 = fmaf(expf(y[h]), S.igl32[h], s32);
+                s = (double)s32;
+            } else {
+                s = 0.0;
+#pragma unroll
+                for (int h = 0; h < G; h++) s = fma(exp_wide(y[h]), S.igl[h], s);
+            }
             const bool isv = (i == L);
             const double m = msm[li];
             double mn;
@@ -786,34 +809,60 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
         // -------------------------------------------- local T lowest
         // Each warp finds the `want` lowest (utility, position) pairs among
         // its own slots (li = 32 w + lane + 32 kWarps j), with no block
-        // barrier: every lane keeps the minimum of its own slots, a round is
-        // a warp argmin over those, and only the lane that owned the winner
-        // rescans its slots.  Thread 0 then merges the sorted per-warp lists.
+        // barrier.  Every lane caches the two lowest of its own slots; a
+        // round is a warp minimum by hardware reductions (key high word, key
+        // low word, then position among equal keys), the winning lane
+        // promotes its second entry and rescans only when it wins again.
+        // Thread 0 then merges the sorted per-warp lists.
         const int want = min(a.T, nloc);
         Cand *wl = reinterpret_cast<Cand *>(chosen + align_up((size_t)(ch + 1)));   // [kWarps][kMaxQueue]
-        auto lane_min = [&]() {
-            Cand best{~0ull, 0x7fffffff, -1};
+        const Cand none{~0ull, 0x7fffffff, -1};
+        Cand c1 = none, c2 = none;         // this lane's two lowest not yet taken
+        auto lane_scan = [&]() {
+            c1 = none;
+            c2 = none;
             for (int li = w * 32 + lane; li < nloc; li += kWarps * 32) {
                 if (chosen[li]) continue;
-                Cand cd{double_key(msm[li]), possm[li], s0 + li};
-                if (cand_less(cd, best)) best = cd;
+                const Cand cd{double_key(msm[li]), possm[li], s0 + li};
+                if (cand_less(cd, c1)) {
+                    c2 = c1;
+                    c1 = cd;
+                } else if (cand_less(cd, c2)) {
+                    c2 = cd;
+                }
             }
-            return best;
         };
-        Cand mine = lane_min();
+        lane_scan();
+        bool c2_valid = true;              // c2 is the true second of the remaining slots
         for (int rnd = 0; rnd < want; rnd++) {
-            Cand best = mine;
-#pragma unroll
-            for (int m = 16; m > 0; m >>= 1) {
-                Cand o = shfl_cand(best, m);
-                if (cand_less(o, best)) best = o;
+            const uint32_t hi = (uint32_t)(c1.key >> 32), lo = (uint32_t)c1.key;
+            const uint32_t mhi = __reduce_min_sync(kFull, hi);
+            const uint32_t mlo = __reduce_min_sync(kFull, hi == mhi ? lo : 0xffffffffu);
+            const bool tie = hi == mhi && lo == mlo;
+            const uint32_t mpos = __reduce_min_sync(kFull, tie ? (uint32_t)c1.pos ^ 0x80000000u : 0xffffffffu);
+            const bool win = tie && ((uint32_t)c1.pos ^ 0x80000000u) == mpos;
+            const uint32_t wm = __ballot_sync(kFull, win && c1.slot >= 0);
+            if (wm == 0u) {                 // nothing left in this warp
+                if (lane == 0) wl[w * kMaxQueue + rnd] = none;
+                continue;
             }
+            const int src = __ffs(wm) - 1;
+            Cand best;
+            best.key = __shfl_sync(kFull, (unsigned long long)c1.key, src);
+            best.pos = __shfl_sync(kFull, c1.pos, src);
+            best.slot = __shfl_sync(kFull, c1.slot, src);
             if (lane == 0) wl[w * kMaxQueue + rnd] = best;
-            if (best.slot >= 0 && ((best.slot - s0) & 31) == lane) {
+            if (lane == src) {
                 chosen[best.slot - s0] = 1;
-                mine = lane_min();
+                if (c2_valid) {
+                    c1 = c2;
+                    c2 = none;
+                    c2_valid = false;
+                } else {
+                    lane_scan();
+                    c2_valid = true;
+                }
             }
-            __syncwarp();
         }
         __syncthreads();
         if (tid == 0) {
