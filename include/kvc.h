@@ -88,9 +88,11 @@ typedef struct {
     int32_t L;               /* budget: slots kept per unit after a step     */
     int32_t rule;            /* KVC_RULE_*  (InertiaKV sec 3.1 eqs 2-4)      */
     float alpha;             /* EMA coefficient, 0 <= alpha < 1              */
-    int32_t refresh_period;  /* T >= 1, T <= L: utilities refresh on step
+    int32_t refresh_period;  /* 0 <= T <= L: utilities refresh on step
                                 t = 1 and whenever (t - 1) mod T == 0
-                                (InertiaKV-Lazy; T = 1 is full refresh)      */
+                                (InertiaKV-Lazy; T = 1 is full refresh);
+                                T = 0 refreshes on step 1 only (InertiaKV
+                                Score-Free: the step-1 ranking is frozen)    */
     int32_t correction;      /* KVC_CORR_* (MomentKV sec 4.2 eq 12; the zero-
                                 order variant of MomentKV Table 4)           */
 } kvc_params;
@@ -192,9 +194,9 @@ KVC_API kvc_status kvc_decode_attend(const kvc_params *p, int32_t t, int32_t new
  * while the cache exceeds the budget"; InertiaKV-Lazy periodic refresh;
  * MomentKV Algorithm 1 phase 1 (argmin loop).
  *
- * On a refresh step (t = 1 or (t - 1) mod T == 0) every live slot's utility
- * is updated from probs (required then): an unscored slot takes m = s, a
- * scored one the rule.  On other steps utilities are left as they are.
+ * On a refresh step (t = 1, or (t - 1) mod T == 0 when T >= 1) every live
+ * slot's utility is updated from probs (required then): an unscored slot
+ * takes m = s, a scored one the rule.  On other steps utilities are left as they are.
  * Then k = len[u] - L victims (0 if len <= L) are chosen among scored slots:
  * the k smallest (m, pos) pairs, utility ascending, ties to the smaller
  * token position.  evict_idx[u][0..k) receives their slot indices in

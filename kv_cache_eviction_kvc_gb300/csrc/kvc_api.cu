@@ -84,8 +84,9 @@ static kvc_status check_params(const kvc_params *p)
                   "rule = %d unknown", p->rule);
     KVC_CHECK_ARG(p->rule != KVC_RULE_EMA || (p->alpha >= 0.f && p->alpha < 1.f),
                   KVC_ERR_INVALID_ARG, "alpha = %g outside [0, 1)", (double)p->alpha);
-    KVC_CHECK_ARG(p->refresh_period >= 1 && p->refresh_period <= p->L, KVC_ERR_INVALID_ARG,
-                  "refresh period T = %d must satisfy 1 <= T <= L = %d", p->refresh_period, p->L);
+    KVC_CHECK_ARG(p->refresh_period >= 0 && p->refresh_period <= p->L, KVC_ERR_INVALID_ARG,
+                  "refresh period T = %d must satisfy 0 <= T <= L = %d (0 = Score-Free)",
+                  p->refresh_period, p->L);
     KVC_CHECK_ARG(p->correction >= KVC_CORR_OFF && p->correction <= KVC_CORR_FIRST_ORDER,
                   KVC_ERR_INVALID_ARG, "correction = %d unknown", p->correction);
     return KVC_OK;

@@ -131,10 +131,13 @@ __device__ __forceinline__ int block_exscan(int v, int *scratch, int *total)
     return ex;
 }
 
-// Is step t a utility-refresh step?  t = 1 and every T-th step after it.
+// Is step t a utility-refresh step?  t = 1 and every T-th step after it
+// (InertiaKV-Lazy); T = 0 is the Score-Free operating point: the utilities
+// are scored at the first decode step only and the ranking stays frozen.
 __host__ __device__ __forceinline__ bool is_refresh(int t, int T)
 {
-    return T <= 1 || ((t - 1) % T) == 0;
+    if (T == 0) return t == 1;
+    return T == 1 || ((t - 1) % T) == 0;
 }
 
 }  // namespace kvc

@@ -260,8 +260,11 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
     // ------------------------------------------------ victim (non-refresh)
     int victim = -1;
     if (!refresh) {
-        const int tr = a.t - ((a.t - 1) % a.T);      // last refresh step
-        const int idx = a.t - tr;                      // 1 .. T-1
+        // last refresh step (step 1 alone for a Score-Free run, T = 0) and
+        // this step's place in its queue; past the queue's end the victim is
+        // the argmin over the stale utilities
+        const int tr = a.T > 0 ? a.t - ((a.t - 1) % a.T) : 1;
+        const int idx = a.t - tr;
         const int32_t *pq = a.pend + (size_t)u * kPendStride;
         if (pq[0] == tr && pq[1] >= idx) {
             victim = pq[2 + idx - 1];
@@ -814,7 +817,10 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
         // low word, then position among equal keys), the winning lane
         // promotes its second entry and rescans only when it wins again.
         // Thread 0 then merges the sorted per-warp lists.
-        const int want = min(a.T, nloc);
+        // queue length: T (one victim per step until the next refresh); a
+        // Score-Free run (T = 0, no later refresh) queues as many as fit
+        const int Tq = a.T > 0 ? a.T : kMaxQueue;
+        const int want = min(Tq, nloc);
         Cand *wl = reinterpret_cast<Cand *>(chosen + align_up((size_t)(ch + 1)));   // [kWarps][kMaxQueue]
         const Cand none{~0ull, 0x7fffffff, -1};
         Cand c1 = none, c2 = none;         // this lane's two lowest not yet taken
@@ -890,8 +896,8 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
         // every CTA merges the candidate lists the same way: one parallel
         // gather over distributed shared memory, then a local merge
         Cand *gc = wl + kWarps * kMaxQueue;                  // [CS][kMaxQueue]
-        for (int e = tid; e < CS * a.T; e += blockDim.x) {
-            const int q = e / a.T, jj = e % a.T;
+        for (int e = tid; e < CS * Tq; e += blockDim.x) {
+            const int q = e / Tq, jj = e % Tq;
             FusedSmem<G> *R = cluster.map_shared_rank(&S, q);
             gc[q * kMaxQueue + jj] = jj < R->ncand ? R->cand[jj] : Cand{~0ull, 0x7fffffff, -1};
         }
@@ -901,11 +907,11 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             for (int q = 0; q < CS; q++) ptr[q] = 0;
             Cand sel[kMaxQueue];
             int nsel = 0;
-            while (nsel < a.T) {
+            while (nsel < Tq) {
                 int bq = -1;
                 Cand b{~0ull, 0x7fffffff, -1};
                 for (int q = 0; q < CS; q++) {
-                    if (ptr[q] >= a.T) continue;
+                    if (ptr[q] >= Tq) continue;
                     const Cand cq = gc[q * kMaxQueue + ptr[q]];
                     if (cq.slot >= 0 && cand_less(cq, b)) {
                         b = cq;

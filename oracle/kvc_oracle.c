@@ -373,6 +373,189 @@ int ocl_evict(void *h, const int32_t *victims, const int32_t *nvict, int kmax)
 }
 
 /*
+ * Nearest bf16 of a double, ties to the even pattern (one rounding step:
+ * the candidates around the float conversion are compared in double).
+ */
+static uint16_t dbf(double x)
+{
+    float f = (float)x;
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    uint16_t a = (uint16_t)(u >> 16);          /* bf16 of f truncated toward 0 */
+    uint16_t best = a;
+    double bd = fabs(bfd(a) - x);
+    for (int j = -1; j <= 1; j += 2) {
+        if (j < 0 && (a & 0x7FFF) == 0) continue;
+        uint16_t c = (uint16_t)(a + j);
+        double cd = fabs(bfd(c) - x);
+        if (cd < bd || (cd == bd && (c & 1) == 0)) { best = c; bd = cd; }
+    }
+    return best;
+}
+
+/*
+ * KeepKV ZIP-merging of one victim per unit into its most similar retained
+ * slot, instead of dropping it [KeepKV reading notes, "ZIP-Merging" eqs
+ * 7-12; candidate choice by the cosine similarity of keys, the most recent
+ * R tokens excluded ("why cosine similarity"); the epsilon guard of the
+ * "numerical stability" item 2].
+ *
+ * victim[u]: position of the unit's victim, or -1 (unit untouched).
+ * Candidates c: live slots other than the victim whose position is at most
+ * new_pos - R (the last R positions of the sequence are excluded).  The
+ * partner maximizes cos(k_e, k_c) = k_e . k_c / (|k_e| |k_c|) (0 when a norm
+ * is 0), ties to the smaller position; force[u] >= 0 (optional) names the
+ * partner's position instead (it must be a candidate).  No candidate: the
+ * unit is left untouched, partner[u] = -1.
+ *
+ * Scores (reading for a GQA group): ln s_j = xbar_j = (1/G) sum_h q_h . k_j
+ * / sqrt(d), the logit of the group's mean query, so that the page's
+ * single-head formula applies unchanged (G = 1 gives it exactly).  With
+ * weights w_j = p_j s_j (eq 8), lambda_j = w_j / (w_e + w_c):
+ *   v_r = lambda_e v_e + lambda_c v_c                            (eq 10)
+ *   xt  = lambda_e xbar_e + lambda_c xbar_c
+ *   ell = ln((w_e + w_c) / (p_e + p_c))
+ *   k_r = (lambda_e k_e + lambda_c k_c) ell / xt                 (eq 12,
+ *         numerator and denominator divided by w_e + w_c)
+ *   |xt| < eps: k_r = (k_e + k_c) / 2                            (guard)
+ *   p_r = p_e + p_c                                              (eq 7)
+ * Weights are formed after subtracting max(xbar_e, xbar_c).  The partner
+ * slot takes k_r, v_r rounded to bf16, the vote p_r and (reading) the sum
+ * of the two utilities, and keeps its position and scored flag; the
+ * victim's slot is removed.  Outputs per unit (any may be NULL): partner
+ * position, the largest candidate cosine and the partner's, the unrounded
+ * k_r and v_r [U][d], and the guard flag.  Returns 0, or -1 if a victim or
+ * a forced partner is not present / not a candidate.
+ */
+int ocl_zip_merge(void *h, const uint16_t *q, const int32_t *victim, int32_t new_pos,
+                  int R, double eps, const int32_t *force, int32_t *partner,
+                  double *cos_best, double *cos_used, double *kr, double *vr,
+                  int32_t *guard)
+{
+    ocl_session *s = (ocl_session *)h;
+    int G = s->G, d = s->d, rc = 0;
+    double rsd = 1.0 / sqrt((double)d);
+    double *kre = (double *)malloc((size_t)d * sizeof(double));
+    double *vre = (double *)malloc((size_t)d * sizeof(double));
+    for (int u = 0; u < s->U; u++) {
+        if (partner) partner[u] = -1;
+        if (guard) guard[u] = 0;
+        if (victim[u] < 0) continue;
+        size_t base = (size_t)u * s->cap;
+        int n = s->n[u], e = 0;
+        while (e < n && s->pos[base + e] != victim[u]) e++;
+        if (e == n) { rc = -1; continue; }
+        const uint16_t *ke = &s->k[(base + e) * d];
+        double nke = 0.0;
+        for (int a = 0; a < d; a++) nke += bfd(ke[a]) * bfd(ke[a]);
+        nke = sqrt(nke);
+        int c = -1, cf = -1;
+        double cb = -INFINITY, cu = 0.0;
+        for (int i = 0; i < n; i++) {
+            if (i == e || s->pos[base + i] > new_pos - R) continue;
+            const uint16_t *ki = &s->k[(base + i) * d];
+            double dot = 0.0, nki = 0.0;
+            for (int a = 0; a < d; a++) {
+                dot += bfd(ke[a]) * bfd(ki[a]);
+                nki += bfd(ki[a]) * bfd(ki[a]);
+            }
+            nki = sqrt(nki);
+            double cs = (nke > 0.0 && nki > 0.0) ? dot / (nke * nki) : 0.0;
+            /* slots are in position order: the first maximum is the oldest */
+            if (cs > cb) { cb = cs; c = i; }
+            if (force && force[u] >= 0 && s->pos[base + i] == force[u]) { cf = i; cu = cs; }
+        }
+        if (c < 0) continue;
+        if (force && force[u] >= 0) {
+            if (cf < 0) { rc = -1; continue; }
+            c = cf;
+        } else {
+            cu = cb;
+        }
+        if (cos_best) cos_best[u] = cb;
+        if (cos_used) cos_used[u] = cu;
+        const uint16_t *kc = &s->k[(base + c) * d];
+        const uint16_t *ve = &s->v[(base + e) * d], *vc = &s->v[(base + c) * d];
+        double xe = 0.0, xc = 0.0;
+        for (int hh = 0; hh < G; hh++) {
+            const uint16_t *qh = &q[((size_t)u * G + hh) * d];
+            for (int a = 0; a < d; a++) {
+                xe += bfd(qh[a]) * bfd(ke[a]);
+                xc += bfd(qh[a]) * bfd(kc[a]);
+            }
+        }
+        xe *= rsd / G;
+        xc *= rsd / G;
+        double pe = (double)s->vote[base + e], pc = (double)s->vote[base + c];
+        double m = xe > xc ? xe : xc;
+        double we = pe * exp(xe - m), wc = pc * exp(xc - m), W = we + wc;
+        double le = we / W, lc = wc / W;
+        double xt = le * xe + lc * xc;
+        double ell = m + log(W / (pe + pc));
+        int gd = fabs(xt) < eps;
+        for (int a = 0; a < d; a++) {
+            vre[a] = le * bfd(ve[a]) + lc * bfd(vc[a]);
+            kre[a] = gd ? 0.5 * (bfd(ke[a]) + bfd(kc[a]))
+                        : (le * bfd(ke[a]) + lc * bfd(kc[a])) * ell / xt;
+        }
+        if (kr) memcpy(&kr[(size_t)u * d], kre, d * sizeof(double));
+        if (vr) memcpy(&vr[(size_t)u * d], vre, d * sizeof(double));
+        if (guard) guard[u] = gd;
+        if (partner) partner[u] = s->pos[base + c];
+        uint16_t *kcw = &s->k[(base + c) * d], *vcw = &s->v[(base + c) * d];
+        for (int a = 0; a < d; a++) {
+            kcw[a] = dbf(kre[a]);
+            vcw[a] = dbf(vre[a]);
+        }
+        s->vote[base + c] = s->vote[base + e] + s->vote[base + c];
+        if (s->scored[base + c]) s->util[base + c] += s->util[base + e];
+        /* remove the victim, keeping position order */
+        for (int i = e; i + 1 < n; i++) {
+            s->pos[base + i] = s->pos[base + i + 1];
+            s->vote[base + i] = s->vote[base + i + 1];
+            s->util[base + i] = s->util[base + i + 1];
+            s->scored[base + i] = s->scored[base + i + 1];
+            memmove(&s->k[(base + i) * d], &s->k[(base + i + 1) * d], d * sizeof(uint16_t));
+            memmove(&s->v[(base + i) * d], &s->v[(base + i + 1) * d], d * sizeof(uint16_t));
+        }
+        s->n[u] = n - 1;
+    }
+    free(kre);
+    free(vre);
+    return rc;
+}
+
+/*
+ * Overwrite the key and value of the slot holding position p in unit u
+ * (test support: the parity driver lets the oracle adopt a row the GPU
+ * rounded differently within one bf16 unit).  Returns 0, or -1 if absent.
+ */
+int ocl_set_row(void *h, int u, int32_t p, const uint16_t *k, const uint16_t *v)
+{
+    ocl_session *s = (ocl_session *)h;
+    size_t base = (size_t)u * s->cap;
+    for (int i = 0; i < s->n[u]; i++)
+        if (s->pos[base + i] == p) {
+            memcpy(&s->k[(base + i) * s->d], k, s->d * sizeof(uint16_t));
+            memcpy(&s->v[(base + i) * s->d], v, s->d * sizeof(uint16_t));
+            return 0;
+        }
+    return -1;
+}
+
+/*
+ * Copy out the key and value rows of every live slot, in slot (position)
+ * order: k, v [U][cap][d] bf16 bits.
+ */
+void ocl_get_rows(void *h, uint16_t *k, uint16_t *v)
+{
+    ocl_session *s = (ocl_session *)h;
+    size_t rows = (size_t)s->U * s->cap * s->d;
+    memcpy(k, s->k, rows * sizeof(uint16_t));
+    memcpy(v, s->v, rows * sizeof(uint16_t));
+}
+
+/*
  * Moments in mean / covariance form, recovered from the raw sums
  * [MomentKV sec 4.1 and App. A.1: k_bar = s_k / n_e, v_bar = s_v / n_e,
  *  S_tilde = S - s_v s_k^T / n_e]; C = S_tilde / n_e (the population

@@ -70,6 +70,9 @@ def _load():
             "ocl_get_slots": (None, [P, P, P, P, P, P]),
             "ocl_select": (I, [P, I, I, P, P, P]),
             "ocl_evict": (I, [P, P, P, I]),
+            "ocl_zip_merge": (I, [P, P, P, ctypes.c_int32, I, D, P, P, P, P, P, P, P]),
+            "ocl_set_row": (I, [P, I, ctypes.c_int32, P, P]),
+            "ocl_get_rows": (None, [P, P, P]),
             "ocl_moments": (None, [P, P, P, P, P]),
             "ocl_output": (None, [P, P, I, P, P, P]),
             "ocl_prefill_gram": (None, [I, I, I, I, I, P, P]),
@@ -200,6 +203,38 @@ class DecodeSession:
         if self.lib.ocl_evict(self.h, _p(victims), _p(nvict), victims.shape[1]) != 0:
             raise ValueError("ocl_evict: position not present")
 
+    def zip_merge(self, q, victim, new_pos: int, R: int, eps: float = None, force=None):
+        """KeepKV ZIP-merging of victim[u] (a position, -1 = none) into its
+        most similar slot (see ocl_zip_merge).  Returns a dict of partner
+        positions [U] (-1 = none), cos_best, cos_used [U], the unrounded
+        k_r, v_r [U][d] and the guard flags [U]."""
+        qb = _bits(q)
+        eps = ZIP_EPS if eps is None else eps
+        victim = np.ascontiguousarray(victim, dtype=np.int32)
+        force = None if force is None else np.ascontiguousarray(force, dtype=np.int32)
+        out = dict(partner=np.full(self.U, -1, np.int32), cos_best=np.zeros(self.U),
+                   cos_used=np.zeros(self.U), kr=np.zeros((self.U, self.d)),
+                   vr=np.zeros((self.U, self.d)), guard=np.zeros(self.U, np.int32))
+        rc = self.lib.ocl_zip_merge(self.h, _p(qb), _p(victim), int(new_pos), int(R), float(eps),
+                                    _p(force), _p(out["partner"]), _p(out["cos_best"]),
+                                    _p(out["cos_used"]), _p(out["kr"]), _p(out["vr"]),
+                                    _p(out["guard"]))
+        if rc != 0:
+            raise ValueError("ocl_zip_merge: victim or forced partner not present")
+        return out
+
+    def set_row(self, u: int, pos: int, k, v):
+        kb, vb = _bits(k), _bits(v)
+        if self.lib.ocl_set_row(self.h, int(u), int(pos), _p(kb), _p(vb)) != 0:
+            raise ValueError("ocl_set_row: position not present")
+
+    def rows(self):
+        """Key and value rows [U][cap][d] as bf16 bit patterns (slot order)."""
+        k = np.zeros((self.U, self.cap, self.d), np.uint16)
+        v = np.zeros((self.U, self.cap, self.d), np.uint16)
+        self.lib.ocl_get_rows(self.h, _p(k), _p(v))
+        return k, v
+
     def moments(self):
         """Returns (n [U], mu_k [U][d], mu_v [U][d], C [U][d][d])."""
         n = np.zeros(self.U)
@@ -219,16 +254,25 @@ class DecodeSession:
         return o, fR, lz
 
 
+# Guard of the ZIP-merge key formula on the weighted mean logit (KeepKV
+# reading notes, "numerical stability" item 2; the pages give no value).
+ZIP_EPS = 1e-3
+
+
 def is_refresh(t: int, T: int) -> bool:
     """Refresh steps: t = 1 and every T-th step after it (t - 1 = 0 mod T)
     [InertiaKV abstract / sec 1, InertiaKV-Lazy periodic refresh; reading:
-    utilities are refreshed on those steps only and are stale in between]."""
-    return T <= 1 or (t - 1) % T == 0
+    utilities are refreshed on those steps only and are stale in between].
+    T = 0 is Score-Free (InertiaKV abstract and sec 1): scored at the first
+    decode step, then frozen."""
+    if T == 0:
+        return t == 1
+    return T == 1 or (t - 1) % T == 0
 
 
 def decode_step(sess: DecodeSession, t: int, new_pos: int, q, knew, vnew, *,
                 L: int, rule: int, alpha: float, T: int, correction: int,
-                choose=None):
+                choose=None, merge_recent: int | None = None, force_partner=None):
     """One decode step on every unit of ``sess``, in the order of MomentKV
     Algorithm 1 with the InertiaKV utility in place of its scoring:
 
@@ -242,6 +286,18 @@ def decode_step(sess: DecodeSession, t: int, new_pos: int, q, knew, vnew, *,
     ``choose(t, proposal)``, if given, receives the oracle's proposal dict and
     returns the victim positions to apply ([U][kmax], [U]); tests use it to
     validate a near-tie alternative before adopting it.
+
+    ``merge_recent = R`` (not None) selects KeepKV ZIP-merging: a unit that
+    removes exactly one slot this step merges its victim into the most
+    similar slot outside the last R positions instead of dropping it (no
+    moment fold), and its output is the one over the cache before the merge
+    (KeepKV Algorithm 1, decoding stage: attend, then compress; by KeepKV
+    Thm 3 the merged cache gives the same output for the group's mean
+    query).  Units that remove more than one slot, or find no partner, evict
+    as above.  ``force_partner`` [U] (positions, -1 = the oracle's own
+    choice) makes the oracle merge into a given slot; the result's
+    ``merge["cos_best"]`` and ``merge["cos_used"]`` let the caller check that
+    the forced choice is within a near-tie of the best.
     """
     sess.append(knew, vnew, new_pos)
     lse, f_all, probs = sess.attend(q)
@@ -255,15 +311,27 @@ def decode_step(sess: DecodeSession, t: int, new_pos: int, q, knew, vnew, *,
                     probs=probs if refresh else None, refresh=refresh)
     if choose is not None:
         vic, nv = choose(t, proposal)
+    merged = np.zeros(len(nv), bool)
+    if merge_recent is not None:
+        o0, fR0, lz0 = sess.output(q, correction)       # every slot, before the merge
+        victim = np.where(np.asarray(nv) == 1, np.asarray(vic)[:, 0], -1)
+        mres = sess.zip_merge(q, victim, new_pos, merge_recent, force=force_partner)
+        merged = mres["partner"] >= 0
+        proposal.update(merge=mres, merged=merged)
+        nv = np.where(merged, 0, nv).astype(np.int32)
     sess.evict(vic, nv)
     o, fR, lz = sess.output(q, correction)
-    proposal.update(o=o, f_R=fR, logZ_R=lz, applied_victims=vic, applied_nvict=nv)
+    if merge_recent is not None:
+        o[merged], fR[merged], lz[merged] = o0[merged], fR0[merged], lz0[merged]
+    proposal.update(o=o, f_R=fR, logZ_R=lz, applied_victims=vic, applied_nvict=nv,
+                    merged=merged)
     return proposal
 
 
 def decode_generation(k_pre, v_pre, q_steps, k_steps, v_steps, *, L: int,
                       rule: int, alpha: float, T: int, correction: int,
-                      votes_pre=None, G: int | None = None, cap: int | None = None):
+                      votes_pre=None, G: int | None = None, cap: int | None = None,
+                      merge_recent: int | None = None):
     """Run a whole generation on the oracle with its own decisions.
 
     k_pre, v_pre: [U][N][d]; q_steps: [S][U][G][d]; k_steps, v_steps: [S][U][d]
@@ -287,7 +355,7 @@ def decode_generation(k_pre, v_pre, q_steps, k_steps, v_steps, *, L: int,
             t = s + 1
             out.append(decode_step(sess, t, N + t - 1, qs[s], ks[s], vs[s], L=L,
                                    rule=rule, alpha=alpha, T=T,
-                                   correction=correction))
+                                   correction=correction, merge_recent=merge_recent))
             out[-1]["moments"] = sess.moments()
         return out
     finally:

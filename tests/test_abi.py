@@ -53,7 +53,7 @@ def _lib_call_attend(p, **kw):
 
 @pytest.mark.parametrize("field,value,code", [
     ("d", 64, 5), ("G", 3, 5), ("U", 0, 1), ("L", 0, 1), ("L", 100, 1),
-    ("refresh_period", 0, 1), ("refresh_period", 11, 1), ("rule", 7, 1),
+    ("refresh_period", -1, 1), ("refresh_period", 11, 1), ("rule", 7, 1),
     ("alpha", 1.0, 1), ("correction", 3, 1), ("cap", 0, 5)])
 def test_bad_params_rejected_on_host(field, value, code):
     p = K.make_params(U=2, G=4, cap=100, L=10)

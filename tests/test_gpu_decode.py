@@ -56,8 +56,10 @@ SMALL = W.C0.with_(name="small", N=700, L=50, steps=24)
     SMALL.with_(Hq=4, Hkv=2, N=129, L=128, steps=6),                 # k = 2 at step 1
     SMALL.with_(Hq=16, Hkv=2, B=2, N=513, L=17, votes_max=3),        # G = 8
     SMALL.with_(N=40, L=64, steps=30),                               # no eviction at first
+    SMALL.with_(T=0),                                                # Score-Free
+    SMALL.with_(N=100, L=100, T=0, steps=80),                        # queue of 70, then argmin
 ], ids=["ragged", "votes-cumulative", "single-lazy", "T=L-zero-order", "corr-off",
-        "G1", "k2", "G8-votes", "under-budget"])
+        "G1", "k2", "G8-votes", "under-budget", "score-free", "score-free-queue"])
 @pytest.mark.parametrize("fused", [True, False])
 def test_edge_cases(cfg, fused):
     check(run_decode_parity(cfg, fused=fused))

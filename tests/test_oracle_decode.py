@@ -454,3 +454,33 @@ def test_generation_invariants_and_lazy_refresh():
                 else:
                     assert pos[u, i] >= N + 1     # appended after the refresh
     sess.close()
+
+
+def test_score_free_evicts_in_step1_order():
+    """Score-Free (InertiaKV abstract, sec 1: score the full context once at
+    the first decode step, then keep that ranking): with T = 0 the victims
+    of the whole run are the step-1 head-mean softmax ranking, lowest first
+    (ties to the older token), N + 1 - L at step 1 and then one per step,
+    and no token appended after step 1 is ever evicted.  The ranking is
+    brute-forced here with numpy's softmax over the step-1 cache."""
+    rng = np.random.default_rng(15)
+    U, N, d, G, S, L = 2, 24, 8, 4, 9, 12
+    kp, vp = bf(rng.normal(size=(U, N, d))), bf(rng.normal(size=(U, N, d)))
+    qs = bf(rng.normal(size=(S, U, G, d)))
+    ks, vs = bf(rng.normal(size=(S, U, d))), bf(rng.normal(size=(S, U, d)))
+    res = O.decode_generation(kp, vp, qs, ks, vs, L=L, rule=O.RULE_EMA,
+                              alpha=0.9, T=0, correction=O.CORR_FIRST_ORDER)
+    assert [r["refresh"] for r in res] == [True] + [False] * (S - 1)
+    for u in range(U):
+        keys = np.concatenate([kp[u], ks[0, u][None]])          # positions 0..N
+        x = qs[0, u] @ keys.T / math.sqrt(d)                    # [G][N+1]
+        a = np.exp(x - x.max(axis=1, keepdims=True))
+        s1 = (a / a.sum(axis=1, keepdims=True)).mean(axis=0)
+        order = sorted(range(N + 1), key=lambda i: (s1[i], i))
+        got = []
+        for t, r in enumerate(res, start=1):
+            nv = int(r["applied_nvict"][u])
+            assert nv == (N + 1 - L if t == 1 else 1)
+            got.append(sorted(int(p) for p in r["applied_victims"][u, :nv]))
+        assert got[0] == sorted(order[:N + 1 - L])
+        assert [g[0] for g in got[1:]] == order[N + 1 - L:N + 1 - L + S - 1]
