@@ -95,7 +95,17 @@ typedef struct {
                                 Score-Free: the step-1 ranking is frozen)    */
     int32_t correction;      /* KVC_CORR_* (MomentKV sec 4.2 eq 12; the zero-
                                 order variant of MomentKV Table 4)           */
+    int32_t merge;           /* 0: victims are evicted; 1: a unit removing
+                                one slot ZIP-merges its victim instead
+                                (KeepKV; see kvc_zip_merge); needs votes     */
+    int32_t merge_recent;    /* R >= 0: merge partners exclude the last R
+                                token positions (KeepKV candidate choice)    */
 } kvc_params;
+
+/* Guard of the ZIP-merge key formula: below this |weighted mean logit| the
+ * merged key is the plain mean of the two keys (KeepKV reading notes,
+ * "numerical stability" item 2, which gives no value). */
+#define KVC_ZIP_EPS 1e-3
 
 /* The budgeted cache of every unit (device pointers, caller-owned). */
 typedef struct {
@@ -260,6 +270,44 @@ KVC_API kvc_status kvc_correct(const kvc_params *p, const uint16_t *q,
                        float *logZ_R, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * kvc_zip_merge -- merge each unit's single victim into its most similar
+ * slot instead of evicting it.
+ *
+ * Defined by: KeepKV reading notes, "ZIP-Merging" (eq 7 votes p_r = p_e +
+ * p_c, eq 8 score condition, eq 10 value, eq 12 key, Thm 3 single-step
+ * lossless), "why cosine similarity" (partner = most similar key, the most
+ * recent R tokens excluded) and "numerical stability" item 2 (guard).
+ *
+ * Call after kvc_aggregate_evict and before kvc_moment_update, with q and
+ * new_pos of the same step; needs cache->votes.  For each unit with
+ * n_evict[u] == 1 and victim slot e = evict_idx[u][0]:
+ *   candidates c: live slots other than e with pos <= new_pos - R
+ *     (R = p->merge_recent); partner = the largest cos(k_e, k_c) (0 when a
+ *     key is zero), ties to the smaller position.  No candidate: nothing
+ *     happens (the victim is evicted by the calls that follow).
+ *   xbar_j = (1/G) sum_h q_h . k_j / sqrt(d) (the group's mean query;
+ *     G = 1 is the page's single-head score), w_j = p_j exp(xbar_j),
+ *     lambda_j = w_j / (w_e + w_c), xt = lambda_e xbar_e + lambda_c xbar_c,
+ *     ell = ln((w_e + w_c) / (p_e + p_c));
+ *   v_c := lambda_e v_e + lambda_c v_c;
+ *   k_c := (lambda_e k_e + lambda_c k_c) ell / xt, or (k_e + k_c) / 2 when
+ *     |xt| < KVC_ZIP_EPS (both rounded to bf16, nearest even);
+ *   votes[c] := p_e + p_c; util[c] := util[c] + util[e]; pos[c] kept;
+ *   slot e is refilled from slot len - 1 (all fields), len[u] -= 1 and
+ *   n_evict[u] := 0, so the moment fold, the correction (which then returns
+ *   the output over every slot of the step, as KeepKV attends before it
+ *   compresses) and the compaction leave the unit alone.
+ * partner_pos [U] (optional) receives the partner's position or -1.
+ * Scores and weights are fp32; cosine near-ties (|difference| ~ 1e-6) may
+ * resolve either way.
+ */
+KVC_API kvc_status kvc_zip_merge(const kvc_params *p, int32_t new_pos, const uint16_t *q,
+                                 const kvc_cache *cache, int32_t kmax,
+                                 const int32_t *evict_idx, int32_t *n_evict,
+                                 int32_t *partner_pos, void *ws, size_t ws_bytes,
+                                 void *stream);
+
+/*
  * kvc_compact -- remove the evicted slots (MomentKV Algorithm 1, end of the
  * eviction phase).
  * Live slots keep their contents; the slot order is not significant (slots
@@ -276,7 +324,8 @@ KVC_API kvc_status kvc_compact(const kvc_params *p, const kvc_cache *cache,
  * kvc_decode_step -- the whole decode step, fused: the same results as
  * kvc_decode_attend, kvc_aggregate_evict, kvc_moment_update, kvc_correct and
  * kvc_compact called in that order (same sets; outputs within fp32
- * rounding).
+ * rounding); with p->merge = 1, kvc_zip_merge runs between
+ * kvc_aggregate_evict and kvc_moment_update (six calls, no fused kernel).
  *
  * In the steady state (max_len == L + 1: every unit enters with len = L and
  * evicts exactly one slot) one cluster kernel per step does everything: the

@@ -89,6 +89,10 @@ static kvc_status check_params(const kvc_params *p)
                   p->refresh_period, p->L);
     KVC_CHECK_ARG(p->correction >= KVC_CORR_OFF && p->correction <= KVC_CORR_FIRST_ORDER,
                   KVC_ERR_INVALID_ARG, "correction = %d unknown", p->correction);
+    KVC_CHECK_ARG(p->merge == 0 || p->merge == 1, KVC_ERR_INVALID_ARG,
+                  "merge = %d must be 0 or 1", p->merge);
+    KVC_CHECK_ARG(p->merge_recent >= 0, KVC_ERR_INVALID_ARG,
+                  "merge_recent = %d must be >= 0", p->merge_recent);
     return KVC_OK;
 }
 
@@ -272,6 +276,24 @@ kvc_status kvc_compact(const kvc_params *p, const kvc_cache *cache, int32_t kmax
                        "kvc_compact launch");
 }
 
+kvc_status kvc_zip_merge(const kvc_params *p, int32_t new_pos, const uint16_t *q,
+                         const kvc_cache *cache, int32_t kmax, const int32_t *evict_idx,
+                         int32_t *n_evict, int32_t *partner_pos, void *ws, size_t ws_bytes,
+                         void *stream)
+{
+    KVC_TRY(check_params(p));
+    KVC_TRY(check_cache(cache));
+    DecodeWs w;
+    KVC_TRY(check_ws(p, ws, ws_bytes, &w));
+    KVC_CHECK_ARG(cache->votes != nullptr, KVC_ERR_INVALID_ARG,
+                  "kvc_zip_merge needs cache votes (merged slots carry p_e + p_c)");
+    KVC_CHECK_ARG(q && evict_idx && n_evict && kmax >= 1, KVC_ERR_INVALID_ARG,
+                  "q, evict_idx, n_evict and kmax >= 1 required");
+    return cuda_status(launch_zip_merge(*p, new_pos, q, *cache, kmax, evict_idx, n_evict,
+                                        partner_pos, w, static_cast<cudaStream_t>(stream)),
+                       "kvc_zip_merge launch");
+}
+
 kvc_status kvc_decode_step(const kvc_params *p, int32_t t, int32_t new_pos, int32_t max_len,
                            const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
                            const kvc_cache *cache, const kvc_moments *mom, float *o,
@@ -292,11 +314,20 @@ kvc_status kvc_decode_step(const kvc_params *p, int32_t t, int32_t new_pos, int3
                   "q, k_new and v_new must be 16-byte aligned");
     KVC_CHECK_ARG(kmax >= 1 && kmax >= max_len - p->L, KVC_ERR_SHAPE,
                   "kmax = %d must be >= max(1, max_len - L = %d)", kmax, max_len - p->L);
+    KVC_CHECK_ARG(!p->merge || cache->votes != nullptr, KVC_ERR_INVALID_ARG,
+                  "merge mode needs cache votes (merged slots carry p_e + p_c)");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (max_len == p->L + 1) {
         cudaError_t e = launch_fused_step(*p, t, new_pos, q, k_new, v_new, *cache, *mom, o, probs,
                                           kmax, evict_idx, evict_pos, n_evict, w, st);
-        if (e != cudaErrorNotSupported) return cuda_status(e, "kvc_decode_step fused launch");
+        if (e != cudaErrorNotSupported) {
+            if (e != cudaSuccess || !p->merge) return cuda_status(e, "kvc_decode_step fused launch");
+            // merge mode: the fused kernel attended over every slot, appended
+            // the new token and published the victims; the merge follows
+            return cuda_status(launch_zip_merge(*p, new_pos, q, *cache, kmax, evict_idx, n_evict,
+                                                nullptr, w, st),
+                               "kvc_decode_step zip merge");
+        }
     }
     // general case: the five-call sequence with workspace scratch
     KVC_CHECK_ARG(evict_idx != nullptr, KVC_ERR_INVALID_ARG,
@@ -308,6 +339,11 @@ kvc_status kvc_decode_step(const kvc_params *p, int32_t t, int32_t new_pos, int3
                         "kvc_decode_step attend"));
     KVC_TRY(cuda_status(launch_aggregate(*p, t, pr, *cache, kmax, evict_idx, evict_pos, n_evict, w, st),
                         "kvc_decode_step aggregate"));
+    if (p->merge) {
+        KVC_TRY(cuda_status(launch_zip_merge(*p, new_pos, q, *cache, kmax, evict_idx, n_evict,
+                                             nullptr, w, st),
+                            "kvc_decode_step zip merge"));
+    }
     KVC_TRY(cuda_status(launch_moment(*p, *cache, kmax, evict_idx, n_evict, *mom, w, st),
                         "kvc_decode_step moments"));
     KVC_TRY(cuda_status(launch_correct(*p, q, *cache, kmax, evict_idx, n_evict, w.lse, w.fall, *mom,

@@ -66,6 +66,7 @@ struct FusedArgs {
     int32_t *pend, *status;
     int cap, L, T, rule, correction, t, new_pos, kmax, chunk;
     float alpha;
+    int merge;                  // KeepKV merge mode: attend over L + 1, append at L
 };
 
 struct Cand {
@@ -238,7 +239,9 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             for (int g = 0; g < pre; g++) mbar_wait(&S.full[g], 0);
         return;
     }
-    const bool has_new = refresh && (r == CS - 1);
+    // the new token is a separate (virtual) slot L on refresh steps, and on
+    // every step of merge mode, where the victim stays in place for the merge
+    const bool has_new = (refresh || a.merge) && (r == CS - 1);
     const int nloc = (s1 - s0) + (has_new ? 1 : 0);
     const float rs = rsqrtf((float)kD);
     const uint16_t *knew = a.k_new + (size_t)u * kD;
@@ -266,7 +269,7 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
         const int tr = a.T > 0 ? a.t - ((a.t - 1) % a.T) : 1;
         const int idx = a.t - tr;
         const int32_t *pq = a.pend + (size_t)u * kPendStride;
-        if (pq[0] == tr && pq[1] >= idx) {
+        if (!a.merge && pq[0] == tr && pq[1] >= idx) {
             victim = pq[2 + idx - 1];
             if (victim < 0 || victim >= L) victim = -1;
         }
@@ -346,7 +349,10 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             if (block_sync) __syncthreads();
             else __syncwarp();
         };
-        const float n0 = S.n0, pe = S.vp, n1 = n0 + pe, fw = pe / n1;
+        // merge mode folds nothing: the moments stay as they are and only
+        // C q and q . mu_k are formed for the correction
+        const bool upd = !a.merge;
+        const float n0 = S.n0, pe = S.vp, n1 = n0 + pe, fw = upd ? pe / n1 : 0.f;
         for (int e = p; e < kD; e += np) {
             const float mk = S.mk0[e], mv = S.mv0[e];
             S.muk[e] = mk + (S.vk[e] - mk) * fw;
@@ -355,7 +361,7 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             S.vv[e] -= mv;                  // delta v
         }
         psync();
-        const float sc_old = n0 / n1, sc_rank = pe * n0 / (n1 * n1);
+        const float sc_old = upd ? n0 / n1 : 1.f, sc_rank = upd ? pe * n0 / (n1 * n1) : 0.f;
         // participant -> (row, quarter of columns); the loop bound is uniform
         // so that every lane reaches the shuffles
         for (int rb = r0; rb < r1; rb += np >> 2) {
@@ -378,7 +384,7 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
                     cv[j].y = fmaf(cv[j].y, sc_old, dv * dk[1]);
                     cv[j].z = fmaf(cv[j].z, sc_old, dv * dk[2]);
                     cv[j].w = fmaf(cv[j].w, sc_old, dv * dk[3]);
-                    *reinterpret_cast<float4 *>(crow + 4 * j) = cv[j];
+                    if (upd) *reinterpret_cast<float4 *>(crow + 4 * j) = cv[j];
 #pragma unroll
                     for (int h = 0; h < G; h++) {
                         const float *qq = &S.qs[h][q4 * 32 + 4 * j];
@@ -417,7 +423,7 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
                 S.vv[e] = bf2f(vr[e]);
             }
             if (lane == 0) {
-                S.vp = a.votes ? (float)a.votes[ubase + victim] : 1.f;
+                S.vp = a.merge ? 0.f : (a.votes ? (float)a.votes[ubase + victim] : 1.f);
                 S.vpos = a.pos[ubase + victim];
             }
             __syncwarp();
@@ -470,8 +476,10 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
         float mx0 = -INFINITY, mx1 = -INFINITY;  // max logit of heads h0, h1 over this lane's slots
         // Rows of this warp that must not be used as loaded: slots past the
         // CTA's range (zeroed) and, on a lazy step, the victim's slot (the new
-        // token's row is written there).  Generic writes into the ring are
-        // fenced against the next TMA write of the stage.
+        // token's row is written there; in merge mode the victim stays).
+        // Generic writes into the ring are fenced against the next TMA write
+        // of the stage.
+        const int pvict = a.merge ? -1 : victim;
         auto patch = [&](uint32_t stage_off, int t, const uint16_t *newrow) -> bool {
             bool any = false;
             const int base_li = t * kTile + rb;
@@ -484,8 +492,8 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
                     }
                 }
             }
-            const int vr = victim - s0 - t * kTile - rb;
-            if (victim >= 0 && vr >= 0 && vr < 16) {
+            const int vr = pvict - s0 - t * kTile - rb;
+            if (pvict >= 0 && vr >= 0 && vr < 16) {
                 if (lane < 16)
                     *reinterpret_cast<uint4 *>(ring + stage_off + sw_off(rb + vr, lane)) =
                         *reinterpret_cast<const uint4 *>(newrow + 8 * lane);
@@ -520,7 +528,7 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
                 for (int hf = 0; hf < 2; hf++) {           // slot gq, then gq + 8
                     const int li = t * kTile + rb + gq + 8 * hf;
                     if (li < nrows) {
-                        const bool isnew = (s0 + li == victim);
+                        const bool isnew = (s0 + li == pvict);
                         const float lnp = (!isnew && a.votes) ? logf((float)a.votes[ubase + s0 + li]) : 0.f;
                         if (h0 < G) {
                             const float x = sacc[2 * hf] * rs + lnp;
@@ -819,7 +827,8 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
         // Thread 0 then merges the sorted per-warp lists.
         // queue length: T (one victim per step until the next refresh); a
         // Score-Free run (T = 0, no later refresh) queues as many as fit
-        const int Tq = a.T > 0 ? a.T : kMaxQueue;
+        // (merge mode keeps no queue: a merge changes the partner's utility)
+        const int Tq = a.merge ? 1 : (a.T > 0 ? a.T : kMaxQueue);
         const int want = min(Tq, nloc);
         Cand *wl = reinterpret_cast<Cand *>(chosen + align_up((size_t)(ch + 1)));   // [kWarps][kMaxQueue]
         const Cand none{~0ull, 0x7fffffff, -1};
@@ -925,7 +934,7 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             S.victim = sel[0].slot;
             if (r == 0) {
                 int32_t *pq = a.pend + (size_t)u * kPendStride;
-                pq[0] = a.t;
+                pq[0] = a.merge ? 0 : a.t;
                 pq[1] = nsel - 1;
                 for (int j = 1; j < nsel; j++)
                     pq[2 + j - 1] = sel[j].slot == L ? sel[0].slot : sel[j].slot;
@@ -946,7 +955,7 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             }
             if (tid < G) S.ae_pub[tid] = expf(XS(tid, li) - S.gM[tid]);
             if (tid == 0) {
-                S.pvp = (isv || !a.votes) ? 1.f : (float)a.votes[ubase + victim];
+                S.pvp = a.merge ? 0.f : ((isv || !a.votes) ? 1.f : (float)a.votes[ubase + victim]);
                 S.pvpos = isv ? a.new_pos : possm[li];
             }
         }
@@ -956,7 +965,7 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             const float ae = O->ae_pub[tid];
             S.ae[tid] = ae;
             S.mass[tid] = ae / S.gl[tid];
-            if (S.mass[tid] > 0.5f) atomicExch(&S.direct, 1);
+            if (!a.merge && S.mass[tid] > 0.5f) atomicExch(&S.direct, 1);
         }
         for (int e = tid; e < kD; e += blockDim.x) {
             S.vk[e] = O->pk[e];
@@ -964,7 +973,13 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
         }
         if (tid == 0) { S.vp = O->pvp; S.vpos = O->pvpos; }
         __syncthreads();
-        if (!S.direct) {
+        if (a.merge) {
+            // nothing leaves the attention set: the output is the one over
+            // every slot (the victim is merged after this kernel)
+            for (int e = tid; e < G * kD; e += blockDim.x) S.fR[e / kD][e % kD] /= S.gl[e / kD];
+            if (tid < G) S.lzR[tid] = S.gM[tid] + logf(S.gl[tid]);
+            __syncthreads();
+        } else if (!S.direct) {
             for (int e = tid; e < G * kD; e += blockDim.x) {
                 const int h = e / kD, dd = e % kD;
                 S.fR[h][dd] = (S.fR[h][dd] - S.ae[h] * S.vv[dd]) / (S.gl[h] - S.ae[h]);
@@ -1005,18 +1020,36 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
         }
         ou[(size_t)h * kD + dd] = val;
     }
-    for (int e = r0 + tid; e < r1; e += blockDim.x) a.mu_v[(size_t)u * kD + e] = S.muv[e];
+    if (!a.merge)
+        for (int e = r0 + tid; e < r1; e += blockDim.x) a.mu_v[(size_t)u * kD + e] = S.muv[e];
     if (r == 0) {
-        for (int e = tid; e < kD; e += blockDim.x) a.mu_k[(size_t)u * kD + e] = S.muk[e];
+        if (!a.merge)
+            for (int e = tid; e < kD; e += blockDim.x) a.mu_k[(size_t)u * kD + e] = S.muk[e];
         if (tid == 0) {
-            a.mn[u] = n1;
+            if (!a.merge) a.mn[u] = n1;
             a.n_evict[u] = 1;
             if (a.evict_idx) a.evict_idx[(size_t)u * a.kmax] = victim;
             if (a.evict_pos) a.evict_pos[(size_t)u * a.kmax] = S.vpos;
         }
     }
     // ------------------------------------------------ the new token's slot
-    if (victim != L && r == vic_owner) {
+    if (a.merge) {
+        // appended at slot L; the merge that follows refills the victim's
+        // slot from it and restores len = L
+        if (r == CS - 1) {
+            uint16_t *kd = a.K + (ubase + L) * kD;
+            uint16_t *vd = a.V + (ubase + L) * kD;
+            if (tid < 32) {
+                reinterpret_cast<uint2 *>(kd)[tid] = reinterpret_cast<const uint2 *>(knew)[tid];
+                reinterpret_cast<uint2 *>(vd)[tid] = reinterpret_cast<const uint2 *>(vnew)[tid];
+            } else if (tid == 32) {
+                if (a.votes) a.votes[ubase + L] = 1;
+                a.pos[ubase + L] = a.new_pos;
+                a.util[ubase + L] = refresh ? S.vm : __longlong_as_double(0x7ff0000000000000ll);
+                a.len[u] = L + 1;
+            }
+        }
+    } else if (victim != L && r == vic_owner) {
         uint16_t *kd = a.K + (ubase + victim) * kD;
         uint16_t *vd = a.V + (ubase + victim) * kD;
         if (tid < 32) {
@@ -1081,13 +1114,17 @@ cudaError_t launch_fused_step(const kvc_params &p, int t, int new_pos, const uin
                               const DecodeWs &ws, cudaStream_t st)
 {
     if (p.refresh_period > kMaxQueue) return cudaErrorNotSupported;
+    // merge mode: every unit must find a partner (positions are distinct, so
+    // at most R of the other L slots are recent: R < L guarantees one), and
+    // the victims must be published for the merge kernel
+    if (p.merge && (p.merge_recent >= p.L || !evict_idx)) return cudaErrorNotSupported;
     const int CS = fused_cluster_size(p.U, p.L);
     const int chunk = (p.L + CS - 1) / CS;
     if (chunk > kFusedMaxChunk || p.L + 1 > p.cap) return cudaErrorNotSupported;
     FusedArgs a{q, k_new, v_new, c.K, c.V, c.votes, c.pos, c.util, c.len,
                 m.n, m.mu_k, m.mu_v, m.C, o, probs, evict_idx, evict_pos, n_evict,
                 ws.pend, ws.status, p.cap, p.L, p.refresh_period, p.rule, p.correction,
-                t, new_pos, kmax, chunk, p.alpha};
+                t, new_pos, kmax, chunk, p.alpha, p.merge};
     switch (p.G) {
     case 1: return launch_fused_g<1>(a, p.U, CS, st);
     case 2: return launch_fused_g<2>(a, p.U, CS, st);

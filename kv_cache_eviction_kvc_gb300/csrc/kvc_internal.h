@@ -56,6 +56,10 @@ cudaError_t launch_correct(const kvc_params &p, const uint16_t *q,
                            const float *lse, const float *f_all,
                            const kvc_moments &m, float *o, float *f_R,
                            float *logZ_R, const DecodeWs &ws, cudaStream_t st);
+cudaError_t launch_zip_merge(const kvc_params &p, int new_pos, const uint16_t *q,
+                             const kvc_cache &c, int kmax, const int32_t *evict_idx,
+                             int32_t *n_evict, int32_t *partner_pos, const DecodeWs &ws,
+                             cudaStream_t st);
 cudaError_t launch_compact(const kvc_params &p, const kvc_cache &c, int kmax,
                            const int32_t *evict_idx, const int32_t *n_evict,
                            const DecodeWs &ws, cudaStream_t st);

@@ -27,7 +27,7 @@ EXPORTED = (
     "kvc_version", "kvc_last_error", "kvc_status_string",
     "kvc_decode_workspace_size", "kvc_decode_workspace_init", "kvc_get_device_status",
     "kvc_decode_attend", "kvc_aggregate_evict", "kvc_moment_update", "kvc_correct",
-    "kvc_compact", "kvc_decode_step", "kvc_decode_attend_noalloc", "kvc_prefill_prepare",
+    "kvc_compact", "kvc_zip_merge", "kvc_decode_step", "kvc_decode_attend_noalloc", "kvc_prefill_prepare",
     "kvc_prefill_workspace_size", "kvc_prefill_score",
 )
 
@@ -42,7 +42,8 @@ class kvc_params(ctypes.Structure):
     _fields_ = [("U", ctypes.c_int32), ("G", ctypes.c_int32), ("d", ctypes.c_int32),
                 ("cap", ctypes.c_int32), ("L", ctypes.c_int32), ("rule", ctypes.c_int32),
                 ("alpha", ctypes.c_float), ("refresh_period", ctypes.c_int32),
-                ("correction", ctypes.c_int32)]
+                ("correction", ctypes.c_int32), ("merge", ctypes.c_int32),
+                ("merge_recent", ctypes.c_int32)]
 
 
 class kvc_cache(ctypes.Structure):
@@ -87,6 +88,7 @@ def load(build: bool = True):
         "kvc_moment_update": (I32, [PP, PC, I32, P, P, PM, P, SZ, P]),
         "kvc_correct": (I32, [PP, P, PC, I32, P, P, P, P, PM, P, P, P, P, SZ, P]),
         "kvc_compact": (I32, [PP, PC, I32, P, P, P, SZ, P]),
+        "kvc_zip_merge": (I32, [PP, I32, P, PC, I32, P, P, P, P, SZ, P]),
         "kvc_decode_step": (I32, [PP, I32, I32, I32, P, P, P, PC, PM, P, P, I32, P, P, P, P, SZ, P]),
         "kvc_decode_attend_noalloc": (I32, [PP, I32, I32, I32, P, P, P, PC, P, P, P, P, P]),
         "kvc_prefill_prepare": (I32, [I32, I32, I32, I32, I32, P, P, P]),
@@ -130,8 +132,12 @@ def _stream(stream):
 
 
 def make_params(U, G, cap, L, rule=RULE_EMA, alpha=0.9, refresh_period=1,
-                correction=CORR_FIRST_ORDER, d=128) -> kvc_params:
-    return kvc_params(U, G, d, cap, L, rule, alpha, refresh_period, correction)
+                correction=CORR_FIRST_ORDER, d=128, merge_recent=None) -> kvc_params:
+    """merge_recent = R (not None) turns on KeepKV ZIP-merging with the last R
+    positions excluded from the partner search."""
+    merge = 0 if merge_recent is None else 1
+    return kvc_params(U, G, d, cap, L, rule, alpha, refresh_period, correction, merge,
+                      0 if merge_recent is None else int(merge_recent))
 
 
 def make_cache(K, V, votes, pos, util, length) -> kvc_cache:
@@ -226,6 +232,16 @@ def kvc_compact(p, cache: kvc_cache, kmax, evict_idx, n_evict, ws, stream=None):
         ctypes.byref(p), ctypes.byref(cache), int(kmax), _ptr(evict_idx, i32, "evict_idx"),
         _ptr(n_evict, i32, "n_evict"), _ptr(ws, torch.uint8, "ws"), ws.numel(),
         _stream(stream)))
+
+
+def kvc_zip_merge(p, new_pos, q, cache: kvc_cache, kmax, evict_idx, n_evict, partner_pos, ws,
+                  stream=None):
+    i32 = torch.int32
+    _check(load().kvc_zip_merge(
+        ctypes.byref(p), int(new_pos), _ptr(q, torch.bfloat16, "q"), ctypes.byref(cache),
+        int(kmax), _ptr(evict_idx, i32, "evict_idx"), _ptr(n_evict, i32, "n_evict"),
+        _ptr(partner_pos, i32, "partner_pos", optional=True), _ptr(ws, torch.uint8, "ws"),
+        ws.numel(), _stream(stream)))
 
 
 def kvc_decode_step(p, t, new_pos, max_len, q, k_new, v_new, cache: kvc_cache,

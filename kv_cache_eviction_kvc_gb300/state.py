@@ -14,10 +14,14 @@ class DecodeState:
     def __init__(self, U: int, G: int, cap: int, L: int, *, rule: int = K_.RULE_EMA,
                  alpha: float = 0.9, refresh_period: int = 1,
                  correction: int = K_.CORR_FIRST_ORDER, votes: bool = False,
-                 kmax: int = 1, device="cuda", d: int = 128):
+                 kmax: int = 1, device="cuda", d: int = 128, merge_recent: int | None = None):
         self.U, self.G, self.cap, self.L, self.d = U, G, cap, L, d
         self.device = torch.device(device)
-        self.params = K_.make_params(U, G, cap, L, rule, alpha, refresh_period, correction, d)
+        self.params = K_.make_params(U, G, cap, L, rule, alpha, refresh_period, correction, d,
+                                     merge_recent)
+        self.merge = merge_recent is not None
+        if self.merge and not votes:
+            raise ValueError("ZIP-merging needs per-slot votes (votes=True)")
         dev = self.device
         self.K = torch.zeros(U, cap, d, dtype=torch.bfloat16, device=dev)
         self.V = torch.zeros(U, cap, d, dtype=torch.bfloat16, device=dev)
@@ -41,6 +45,7 @@ class DecodeState:
         self.f_R = torch.zeros(U, G, d, dtype=torch.float32, device=dev)
         self.logZ_R = torch.zeros(U, G, dtype=torch.float32, device=dev)
         self.n_evict = torch.zeros(U, dtype=torch.int32, device=dev)
+        self.partner_pos = torch.full((U,), -1, dtype=torch.int32, device=dev)
         self.set_kmax(kmax)
 
     # --------------------------------------------------------------- helpers
@@ -90,13 +95,17 @@ class DecodeState:
 
     def step_calls(self, t: int, new_pos: int, q, k_new, v_new, max_len: int, stream=None):
         """The five entry points in order (attend, aggregate_evict,
-        moment_update, correct, compact)."""
+        moment_update, correct, compact), with zip_merge after aggregate_evict
+        in merge mode."""
         self.set_kmax(max_len - self.L)
         c = self.cache
         K_.kvc_decode_attend(self.params, t, new_pos, max_len, q, k_new, v_new, c, self.lse,
                              self.f_all, self.probs, self.ws, stream)
         K_.kvc_aggregate_evict(self.params, t, self.probs, c, self.kmax, self.evict_idx,
                                self.evict_pos, self.n_evict, self.ws, stream)
+        if self.merge:
+            K_.kvc_zip_merge(self.params, new_pos, q, c, self.kmax, self.evict_idx, self.n_evict,
+                             self.partner_pos, self.ws, stream)
         K_.kvc_moment_update(self.params, c, self.kmax, self.evict_idx, self.n_evict,
                              self.moments, self.ws, stream)
         K_.kvc_correct(self.params, q, c, self.kmax, self.evict_idx, self.n_evict, self.lse,

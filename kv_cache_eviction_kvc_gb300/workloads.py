@@ -66,6 +66,7 @@ class DecodeConfig:
     head_scale: tuple | None = None
     outliers: int = 0
     outlier_mult: float = 8.0
+    merge_recent: int | None = None   # KeepKV ZIP-merging, last R positions excluded
     description: str = ""
 
     @property

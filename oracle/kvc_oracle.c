@@ -424,13 +424,13 @@ static uint16_t dbf(double x)
  * of the two utilities, and keeps its position and scored flag; the
  * victim's slot is removed.  Outputs per unit (any may be NULL): partner
  * position, the largest candidate cosine and the partner's, the unrounded
- * k_r and v_r [U][d], and the guard flag.  Returns 0, or -1 if a victim or
+ * k_r and v_r [U][d], the guard flag and xt.  Returns 0, or -1 if a victim or
  * a forced partner is not present / not a candidate.
  */
 int ocl_zip_merge(void *h, const uint16_t *q, const int32_t *victim, int32_t new_pos,
                   int R, double eps, const int32_t *force, int32_t *partner,
                   double *cos_best, double *cos_used, double *kr, double *vr,
-                  int32_t *guard)
+                  int32_t *guard, double *xt_out)
 {
     ocl_session *s = (ocl_session *)h;
     int G = s->G, d = s->d, rc = 0;
@@ -501,6 +501,7 @@ int ocl_zip_merge(void *h, const uint16_t *q, const int32_t *victim, int32_t new
         if (kr) memcpy(&kr[(size_t)u * d], kre, d * sizeof(double));
         if (vr) memcpy(&vr[(size_t)u * d], vre, d * sizeof(double));
         if (guard) guard[u] = gd;
+        if (xt_out) xt_out[u] = xt;
         if (partner) partner[u] = s->pos[base + c];
         uint16_t *kcw = &s->k[(base + c) * d], *vcw = &s->v[(base + c) * d];
         for (int a = 0; a < d; a++) {

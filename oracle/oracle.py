@@ -70,7 +70,7 @@ def _load():
             "ocl_get_slots": (None, [P, P, P, P, P, P]),
             "ocl_select": (I, [P, I, I, P, P, P]),
             "ocl_evict": (I, [P, P, P, I]),
-            "ocl_zip_merge": (I, [P, P, P, ctypes.c_int32, I, D, P, P, P, P, P, P, P]),
+            "ocl_zip_merge": (I, [P, P, P, ctypes.c_int32, I, D, P, P, P, P, P, P, P, P]),
             "ocl_set_row": (I, [P, I, ctypes.c_int32, P, P]),
             "ocl_get_rows": (None, [P, P, P]),
             "ocl_moments": (None, [P, P, P, P, P]),
@@ -207,18 +207,20 @@ class DecodeSession:
         """KeepKV ZIP-merging of victim[u] (a position, -1 = none) into its
         most similar slot (see ocl_zip_merge).  Returns a dict of partner
         positions [U] (-1 = none), cos_best, cos_used [U], the unrounded
-        k_r, v_r [U][d] and the guard flags [U]."""
+        k_r, v_r [U][d], the guard flags [U] and the weighted mean logit xt
+        [U] the guard tests."""
         qb = _bits(q)
         eps = ZIP_EPS if eps is None else eps
         victim = np.ascontiguousarray(victim, dtype=np.int32)
         force = None if force is None else np.ascontiguousarray(force, dtype=np.int32)
         out = dict(partner=np.full(self.U, -1, np.int32), cos_best=np.zeros(self.U),
                    cos_used=np.zeros(self.U), kr=np.zeros((self.U, self.d)),
-                   vr=np.zeros((self.U, self.d)), guard=np.zeros(self.U, np.int32))
+                   vr=np.zeros((self.U, self.d)), guard=np.zeros(self.U, np.int32),
+                   xt=np.zeros(self.U))
         rc = self.lib.ocl_zip_merge(self.h, _p(qb), _p(victim), int(new_pos), int(R), float(eps),
                                     _p(force), _p(out["partner"]), _p(out["cos_best"]),
                                     _p(out["cos_used"]), _p(out["kr"]), _p(out["vr"]),
-                                    _p(out["guard"]))
+                                    _p(out["guard"]), _p(out["xt"]))
         if rc != 0:
             raise ValueError("ocl_zip_merge: victim or forced partner not present")
         return out

@@ -15,7 +15,14 @@ inputs step by step.  Each step compares:
 * the moments: ||d mu|| / ||mu|| and ||d C||_F / ||C||_F <= 1e-4 per unit
   (absolute 1e-6 when the norm is below 1e-3), n exact;
 * the head-mean probabilities on refresh steps (by position), and with the
-  five-call path lse and f_all.
+  five-call path lse and f_all;
+* in ZIP-merge mode (KeepKV), the partner of each merged victim: the oracle
+  merges into the GPU's partner when that partner's key cosine is within
+  1e-5 of the best one (counted as a near-tie when below it), otherwise the
+  step is a mismatch; the merged key and value rows must be within one bf16
+  unit of the oracle's unrounded k_r, v_r (either guard branch is accepted
+  when the weighted mean logit is within 0.1 % of the guard threshold), and
+  the oracle then adopts the GPU's rows.
 """
 from __future__ import annotations
 
@@ -32,6 +39,8 @@ TIE_REL = 1e-6
 O_TOL = 2e-3
 MOM_TOL = 1e-4
 PROB_TOL = 2e-3   # head-mean probabilities are attention outputs
+COS_BAND = 1e-5   # partner near-tie band (key cosines, fp32 on the GPU)
+ROW_REL = 2.0 ** -7   # one bf16 unit (8 significand bits)
 
 
 @dataclasses.dataclass
@@ -46,6 +55,8 @@ class ParityReport:
     max_lse_err: float = 0.0
     max_fall_err: float = 0.0
     n_err: int = 0
+    merges: int = 0
+    max_row_err: float = 0.0      # merged rows, in bf16 units of the reference
     first_mismatch: str = ""
 
     def ok(self):
@@ -64,6 +75,7 @@ def run_decode_parity(cfg: W.DecodeConfig, *, steps: int | None = None, units=No
                       fused: bool = True, seed: int = 0, device="cuda",
                       cap: int | None = None) -> ParityReport:
     S = cfg.steps if steps is None else steps
+    merge = cfg.merge_recent is not None
     U, G, d, N, L = cfg.U, cfg.G, cfg.d, cfg.N, cfg.L
     units = list(range(U)) if units is None else list(units)
     uidx = torch.tensor(units, device=device, dtype=torch.long)
@@ -71,8 +83,8 @@ def run_decode_parity(cfg: W.DecodeConfig, *, steps: int | None = None, units=No
     P = W.unit_params(cfg, device, seed)
     pre = W.gen_prefill(cfg, device, seed, cap=cap, P=P)
     st = DecodeState(U, G, cap, L, rule=cfg.rule, alpha=cfg.alpha, refresh_period=cfg.T,
-                     correction=cfg.correction, votes=bool(cfg.votes_max),
-                     kmax=max(1, N + 1 - L), device=device)
+                     correction=cfg.correction, votes=bool(cfg.votes_max) or merge,
+                     kmax=max(1, N + 1 - L), device=device, merge_recent=cfg.merge_recent)
     st.load_prefill(pre["K"], pre["V"], pre["votes"], pre["pos"], pre["len"])
     sess = O.DecodeSession(len(units), G, d, cap + 1)
     Kh = pre["K"][uidx, :N].cpu()
@@ -90,6 +102,7 @@ def run_decode_parity(cfg: W.DecodeConfig, *, steps: int | None = None, units=No
             max_len = n_len + 1
             refresh = O.is_refresh(t, cfg.T)
             pos_before = st.pos[uidx, :max_len].cpu().numpy().copy()
+            votes_before = st.votes[uidx, :max_len].cpu().numpy().copy() if merge else None
             len_before = st.len[uidx].cpu().numpy().copy()
             if fused:
                 st.step(t, new_pos, inp["q"], inp["k_new"], inp["v_new"], max_len)
@@ -99,6 +112,18 @@ def run_decode_parity(cfg: W.DecodeConfig, *, steps: int | None = None, units=No
             ds = st.device_status()
             assert ds == 0, f"device status {ds} at step {t}"
             nev = st.n_evict[uidx].cpu().numpy()
+            partner_g = None
+            if merge and not fused:
+                partner_g = st.partner_pos[uidx].cpu().numpy()
+            elif merge:
+                # kvc_decode_step reports no partner: it is the one slot whose
+                # vote grew (a merge adds the victim's vote to the partner's)
+                partner_g = _partners_from_votes(new_pos, len_before, pos_before, votes_before,
+                                                 st.len[uidx].cpu().numpy(),
+                                                 st.pos[uidx].cpu().numpy(),
+                                                 st.votes[uidx].cpu().numpy())
+            if merge:
+                nev = nev + (partner_g >= 0)          # a merged victim left n_evict at 0
             evp = st.evict_pos[uidx].cpu().numpy()
             o_gpu = st.o[uidx].cpu().numpy().astype(np.float64)
             probs_gpu = st.probs[uidx, :max_len].cpu().numpy() if refresh else None
@@ -135,9 +160,17 @@ def run_decode_parity(cfg: W.DecodeConfig, *, steps: int | None = None, units=No
                     out[j, : len(gl)] = gl
                 return out, nev.astype(np.int32)
 
-            prop = O.decode_step(sess, t, new_pos, qh, kh, vh2, L=L, rule=cfg.rule,
-                                 alpha=cfg.alpha, T=cfg.T, correction=cfg.correction,
-                                 choose=choose)
+            try:
+                prop = O.decode_step(sess, t, new_pos, qh, kh, vh2, L=L, rule=cfg.rule,
+                                     alpha=cfg.alpha, T=cfg.T, correction=cfg.correction,
+                                     choose=choose, merge_recent=cfg.merge_recent,
+                                     force_partner=partner_g)
+            except ValueError as ex:
+                rep.mismatches += 1
+                rep.first_mismatch = rep.first_mismatch or f"step {t}: oracle refused: {ex}"
+                break
+            if merge:
+                _check_merge(rep, t, units, st, uidx, sess, prop, partner_g)
             # output
             o_ref = prop["o"]
             num = np.abs(o_gpu - o_ref).max(axis=2)
@@ -173,6 +206,66 @@ def run_decode_parity(cfg: W.DecodeConfig, *, steps: int | None = None, units=No
     finally:
         sess.close()
     return rep
+
+
+def _partners_from_votes(new_pos, len0, pos0, votes0, len1, pos1, votes1):
+    out = np.full(len(len0), -1, np.int32)
+    for j in range(len(len0)):
+        before = dict(zip(pos0[j, : len0[j]].tolist(), votes0[j, : len0[j]].tolist()))
+        before[new_pos] = 1                   # the step's token (a partner when R = 0)
+        grew = [p for p, v in zip(pos1[j, : len1[j]].tolist(), votes1[j, : len1[j]].tolist())
+                if p in before and v > before[p]]
+        if len(grew) == 1:
+            out[j] = grew[0]
+        elif len(grew) > 1:
+            raise AssertionError(f"unit {j}: several votes grew {grew[:4]}")
+    return out
+
+
+def _check_merge(rep, t, units, st, uidx, sess, prop, partner_g):
+    """Partner choice and merged rows of one merge-mode step (see the module
+    docstring); the oracle adopts the GPU's merged rows."""
+    mres, merged = prop["merge"], prop["merged"]
+    pos_g = st.pos[uidx].cpu().numpy()
+    for j in range(len(units)):
+        g_m = partner_g[j] >= 0
+        if g_m != bool(merged[j]):
+            rep.mismatches += 1
+            rep.first_mismatch = rep.first_mismatch or (
+                f"step {t} unit {units[j]}: gpu merged {g_m} oracle merged {bool(merged[j])}")
+            continue
+        if not g_m:
+            continue
+        rep.merges += 1
+        gap = mres["cos_best"][j] - mres["cos_used"][j]
+        if gap > COS_BAND:
+            rep.mismatches += 1
+            rep.first_mismatch = rep.first_mismatch or (
+                f"step {t} unit {units[j]}: partner {partner_g[j]} cosine {gap!r} below the best")
+            continue
+        if gap > 0:
+            rep.band_hits += 1
+        slot = int(np.nonzero(pos_g[j] == partner_g[j])[0][0])
+        kb = st.K[units[j], slot].cpu().view(torch.int16).numpy().view(np.uint16)
+        vb = st.V[units[j], slot].cpu().view(torch.int16).numpy().view(np.uint16)
+        kg = (kb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        vg = (vb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        err = 0.0
+        for g_, r_ in ((kg, mres["kr"][j]), (vg, mres["vr"][j])):
+            e_ = np.abs(g_ - r_) / (ROW_REL * np.abs(r_) + 1e-6)
+            err = max(err, float(e_.max()))
+        if err > 1.0:
+            near = abs(abs(mres["xt"][j]) - O.ZIP_EPS) <= 1e-3 * O.ZIP_EPS
+            if near:
+                rep.band_hits += 1
+            else:
+                rep.mismatches += 1
+                rep.first_mismatch = rep.first_mismatch or (
+                    f"step {t} unit {units[j]}: merged row off by {err:.2f} bf16 units "
+                    f"(guard {mres['guard'][j]}, xt {mres['xt'][j]!r})")
+        else:
+            rep.max_row_err = max(rep.max_row_err, err)
+        sess.set_row(j, int(partner_g[j]), kb, vb)
 
 
 # ---------------------------------------------------------------------------

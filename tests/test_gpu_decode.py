@@ -76,3 +76,26 @@ def test_device_status_reports_overlong_unit():
     assert st.device_status() == 2          # KVC_ERR_SHAPE recorded, nothing done
     assert st.len.tolist() == [60, 60]
     assert st.device_status() == 0          # reading clears it
+
+
+@pytest.mark.parametrize("cfg", [
+    SMALL.with_(merge_recent=8),                                     # KeepKV ZIP-merging
+    SMALL.with_(Hq=2, Hkv=2, N=300, L=20, votes_max=4, merge_recent=0),   # G = 1, votes
+    SMALL.with_(Hq=16, Hkv=2, B=2, N=513, L=17, merge_recent=3, T=4),     # G = 8, lazy
+    SMALL.with_(N=40, L=32, steps=12, merge_recent=64),              # no candidate: evict
+], ids=["zip", "zip-G1-votes", "zip-G8-lazy", "zip-no-candidate"])
+@pytest.mark.parametrize("fused", [True, False])
+def test_zip_merge(cfg, fused):
+    rep = run_decode_parity(cfg, fused=fused)
+    check(rep)
+    if cfg.merge_recent < 64:
+        assert rep.merges > 0
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_zip_merge_c2_sampled_full_size(fused):
+    rep = run_decode_parity(W.C2.with_(merge_recent=32), units=sample_units(W.C2.U), steps=24,
+                            fused=fused)
+    check(rep)
+    assert rep.merges >= 64 * 22
+
