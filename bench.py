@@ -70,22 +70,37 @@ def step_bytes(cfg, refresh: bool, emit_probs: bool) -> int:
     the moment fold, the new token's row is written), q, k_new, v_new, o, the
     moments (C read + written, means, count), votes when present; on refresh
     steps the utilities (read + written, fp64), positions and the emitted
-    fp64 probabilities.
+    fp64 probabilities.  A lazy step without a victim queue (Score-Free, or
+    merge mode) reads the utilities and positions for its argmin.  Merge mode
+    (KeepKV ZIP-merging) reads the moments without writing them, appends the
+    new token, and its merge kernel reads every key row and position once
+    more, re-reads the victim and partner rows, writes the merged rows and
+    moves the appended slot into the victim's.
     """
     d, G, L = cfg.d, cfg.G, cfg.L
+    merge = cfg.merge_recent is not None
     b = 2 * L * d * 2                 # K, V rows read
     b += 2 * d * 2                    # k_new, v_new read
-    b += 2 * d * 2                    # new token written into the victim slot
+    b += 2 * d * 2                    # new token written (victim slot, or slot L)
     b += G * d * 2                    # q
     b += G * d * 4                    # o
-    b += 2 * (d * d * 4) + 4 * d * 4 + 8   # C r/w, mu_k / mu_v r/w, n
+    if merge:
+        b += d * d * 4 + 2 * d * 4 + 4    # C, mu_k, mu_v, n read
+    else:
+        b += 2 * (d * d * 4) + 4 * d * 4 + 8   # C r/w, mu_k / mu_v r/w, n
     b += 16                           # pos / votes / util of the new slot, counts
-    if cfg.votes_max:
+    if cfg.votes_max or merge:
         b += L * 4
     if refresh:
         b += (L + 1) * 8 * 2 + L * 4  # util r/w, positions
         if emit_probs:
             b += (L + 1) * 8
+    elif merge or cfg.T == 0:
+        b += L * (8 + 4)              # utilities and positions of the argmin
+    if merge:
+        b += (L + 1) * (d * 2 + 4)    # merge kernel: key rows and positions
+        b += 4 * d * 2 + 2 * d * 2    # victim / partner rows read, merged rows written
+        b += 2 * 2 * d * 2 + 32       # appended slot moved (read + write), votes, util
     return b * cfg.U
 
 
@@ -265,7 +280,8 @@ def oracle_sample(cfg, seconds: float, max_steps: int | None = None):
         inp = W.gen_step(small, "cpu", t, 0, P)
         t0 = time.perf_counter()
         O.decode_step(sess, t, cfg.L + t - 1, inp["q"], inp["k_new"], inp["v_new"], L=cfg.L,
-                      rule=cfg.rule, alpha=cfg.alpha, T=cfg.T, correction=cfg.correction)
+                      rule=cfg.rule, alpha=cfg.alpha, T=cfg.T, correction=cfg.correction,
+                      merge_recent=cfg.merge_recent)
         times.append(time.perf_counter() - t0)
         if max_steps is not None and t >= max_steps:
             break
@@ -292,9 +308,10 @@ def run_ours(args, cfg, rank, world):
     seed = rank
     U, G, N, L = cfg.U, cfg.G, cfg.N, cfg.L
     P = W.unit_params(cfg, dev, seed)
+    merge = cfg.merge_recent is not None
     st = DecodeState(U, G, N + 1, L, rule=cfg.rule, alpha=cfg.alpha, refresh_period=cfg.T,
-                     correction=cfg.correction, votes=bool(cfg.votes_max), kmax=N + 1 - L,
-                     device=dev)
+                     correction=cfg.correction, votes=bool(cfg.votes_max) or merge,
+                     kmax=N + 1 - L, device=dev, merge_recent=cfg.merge_recent)
     pre = W.gen_prefill(cfg, dev, seed, cap=N + 1, P=P)
     st.load_prefill(pre["K"], pre["V"], pre["votes"], pre["pos"], pre["len"])
     del pre
@@ -326,7 +343,7 @@ def run_ours(args, cfg, rank, world):
         st.step(t, N + t - 1, x["q"], x["k_new"], x["v_new"], max_len=L + 1)
         if events is not None:
             events[1].record(stream)
-        launches += 1
+        launches += 2 if merge else 1         # merge mode: fused step + merge kernel
 
     for i in range(args.warmup):
         do_step(i)
@@ -359,8 +376,8 @@ def run_ours(args, cfg, rank, world):
     assert st.device_status() == 0
 
     # algorithmic bytes of the timed launches (refresh pattern of steps 2 + i)
-    def is_refresh(t, T):      # utilities refresh on t = 1 and every T-th step after
-        return T <= 1 or (t - 1) % T == 0
+    def is_refresh(t, T):      # t = 1 and every T-th step after; T = 0: step 1 only
+        return t == 1 if T == 0 else (T == 1 or (t - 1) % T == 0)
     steps_t = [2 + args.warmup + k for k in range(args.steps)]
     bytes_list = [step_bytes(cfg, is_refresh(t, cfg.T), True) for t in steps_t]
     avg_bytes = sum(bytes_list) / len(bytes_list)
@@ -438,6 +455,7 @@ def run_ours(args, cfg, rank, world):
         "data": "synthetic (seeded K/V 64-centre mixtures; no model weights)",
         "config": {"workload": cfg.name, "description": cfg.description, "units": cfg.U,
                    "budget_L": L, "prefill_N": N, "refresh_period": cfg.T,
+                   "merge_recent": cfg.merge_recent,
                    "alpha": cfg.alpha, "parallelism": f"replicas x{world} (independent units)",
                    "l2": "inputs larger than L2: %.2f GB of HBM traffic per step" % (avg_bytes / 1e9)},
         "achieved_gbs": achieved,
@@ -450,7 +468,8 @@ def run_ours(args, cfg, rank, world):
                      "traffic_note": "ncu dram read+write per lazy-step launch, 864-unit capture "
                                      "scaled by units (profiles/fused_step_kernel_qwen3-4b.md)",
                      "peak_kind": peak_kind,
-                     "kernel": "fused_step_kernel (kvc_decode_step, steady state)",
+                     "kernel": ("fused_step_kernel + zip_merge_kernel (kvc_decode_step, merge mode)"
+                                if merge else "fused_step_kernel (kvc_decode_step, steady state)"),
                      "bytes_per_launch": avg_bytes, "avg_launch_ms": avg_launch_ms},
         "clocks": clocks,
         "gpu_launches": launches,

@@ -93,6 +93,7 @@ template <int G>
 struct FusedSmem {
     uint64_t full[kStages];     // ring: stage filled (producer -> consumers)
     uint64_t empty[kStages];    // ring: stage drained (consumers -> producer)
+    uint64_t vready;            // late victim: every CTA's candidate published
     float qs[G][kD];            // q / sqrt(d), fp32
     float red[kWarps][G];
     float pM[G], pl[G];         // this CTA's partial max / sum
@@ -216,6 +217,7 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             mbar_init(&S.full[j], 1);
             mbar_init(&S.empty[j], kNC);
         }
+        mbar_init(&S.vready, CS);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -239,9 +241,28 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             for (int g = 0; g < pre; g++) mbar_wait(&S.full[g], 0);
         return;
     }
-    // the new token is a separate (virtual) slot L on refresh steps, and on
-    // every step of merge mode, where the victim stays in place for the merge
-    const bool has_new = (refresh || a.merge) && (r == CS - 1);
+    // Lazy steps take the victim from the refresh step's queue when it has
+    // an entry for this step (never in merge mode: a merge raises the
+    // partner's utility).  Otherwise the victim is found "late": the fold
+    // warp takes the argmin over the stale utilities during pass 1, and pass
+    // 2 leaves the victim out (merge mode keeps it).
+    int victim = -1;
+    bool late = false;
+    if (!refresh) {
+        // last refresh step (step 1 alone for a Score-Free run, T = 0) and
+        // this step's place in its queue
+        const int tr = a.T > 0 ? a.t - ((a.t - 1) % a.T) : 1;
+        const int idx = a.t - tr;
+        const int32_t *pq = a.pend + (size_t)u * kPendStride;
+        if (!a.merge && pq[0] == tr && pq[1] >= idx) {
+            victim = pq[2 + idx - 1];
+            if (victim < 0 || victim >= L) victim = -1;
+        }
+        late = victim < 0;                  // uniform over the cluster
+    }
+    // the new token is a separate (virtual) slot L on refresh steps, on late
+    // lazy steps and in merge mode; otherwise it replaces the victim's row
+    const bool has_new = (refresh || a.merge || late) && (r == CS - 1);
     const int nloc = (s1 - s0) + (has_new ? 1 : 0);
     const float rs = rsqrtf((float)kD);
     const uint16_t *knew = a.k_new + (size_t)u * kD;
@@ -260,62 +281,23 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
     }
     __syncthreads();
 
-    // ------------------------------------------------ victim (non-refresh)
-    int victim = -1;
-    if (!refresh) {
-        // last refresh step (step 1 alone for a Score-Free run, T = 0) and
-        // this step's place in its queue; past the queue's end the victim is
-        // the argmin over the stale utilities
-        const int tr = a.T > 0 ? a.t - ((a.t - 1) % a.T) : 1;
-        const int idx = a.t - tr;
-        const int32_t *pq = a.pend + (size_t)u * kPendStride;
-        if (!a.merge && pq[0] == tr && pq[1] >= idx) {
-            victim = pq[2 + idx - 1];
-            if (victim < 0 || victim >= L) victim = -1;
-        }
-        if (victim < 0) {
-            // lowest scored (utility, position) over the unit: per-CTA argmin
-            Cand best{~0ull, 0x7fffffff, -1};
-            for (int i = s0 + tid; i < s1; i += blockDim.x) {
-                const double m = a.util[ubase + i];
-                if (isinf(m)) continue;
-                Cand cd{double_key(m), a.pos[ubase + i], i};
-                if (cand_less(cd, best)) best = cd;
-            }
-#pragma unroll
-            for (int m = 16; m > 0; m >>= 1) {
-                Cand o = shfl_cand(best, m);
-                if (cand_less(o, best)) best = o;
-            }
-            if (lane == 0) S.bc[w] = best;
-            __syncthreads();
-            if (tid == 0) {
-                Cand b = S.bc[0];
-                for (int j = 1; j < kWarps; j++)
-                    if (cand_less(S.bc[j], b)) b = S.bc[j];
-                S.cand[0] = b;
-                S.ncand = b.slot >= 0 ? 1 : 0;
-            }
-            cluster.sync();
-            Cand b{~0ull, 0x7fffffff, -1};
-            for (int q = 0; q < CS; q++) {
-                FusedSmem<G> *R = cluster.map_shared_rank(&S, q);
-                if (R->ncand > 0 && cand_less(R->cand[0], b)) b = R->cand[0];
-            }
-            victim = b.slot;
-            cluster.sync();
-            if (victim < 0) {                       // no scored slot: refuse
-                if (r == 0 && tid == 0) {
-                    record_status(a.status, KVC_ERR_INVALID_ARG);
-                    a.n_evict[u] = 0;
-                }
-                if (w == kNC && lane == 0)          // the copies land before the CTA leaves
-                    for (int g = 0; g < pre; g++) mbar_wait(&S.full[g], 0);
-                return;
-            }
-        }
-    }
+    // every CTA's vready barrier is initialized before any remote arrival
+    if (late) cluster.sync();
 
+    // the late victim: the lowest candidate over the cluster's CTAs (each CTA
+    // publishes its own before arriving on everyone's vready)
+    auto late_victim = [&]() -> int {
+        if (!mbar_wait_cluster(&S.vready, 0)) {
+            atomicExch(&S.bad, 1);
+            return -1;
+        }
+        Cand b{~0ull, 0x7fffffff, -1};
+        for (int q = 0; q < CS; q++) {
+            FusedSmem<G> *R = cluster.map_shared_rank(&S, q);
+            if (R->ncand > 0 && cand_less(R->cand[0], b)) b = R->cand[0];
+        }
+        return b.slot;
+    };
 
     // ------------------------------------------------ passes 1 and 2 over the ring
     // The producer warp streams the K rows of [s0, s1), then the V rows, in
@@ -414,8 +396,44 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
     };
 
     if (w == kNC + 1) {
-        // ---------------- moment fold (lazy steps), concurrent with the passes
-        if (!refresh) {
+        // ---------------- late victim and moment fold (lazy steps), concurrent
+        // with the passes
+        if (late) {
+            // eight slots per lane per round, every load issued before the
+            // comparisons, so that the scan ends well inside pass 1
+            constexpr int kScan = 8;
+            Cand best{~0ull, 0x7fffffff, -1};
+            for (int i0 = s0 + lane; i0 < s1; i0 += 32 * kScan) {
+                double m[kScan];
+                int32_t ps[kScan];
+#pragma unroll
+                for (int j = 0; j < kScan; j++) {
+                    const int i = i0 + 32 * j;
+                    m[j] = i < s1 ? a.util[ubase + i] : __longlong_as_double(0x7ff0000000000000ll);
+                    ps[j] = i < s1 ? a.pos[ubase + i] : 0;
+                }
+#pragma unroll
+                for (int j = 0; j < kScan; j++) {
+                    if (isinf(m[j])) continue;
+                    Cand cd{double_key(m[j]), ps[j], i0 + 32 * j};
+                    if (cand_less(cd, best)) best = cd;
+                }
+            }
+#pragma unroll
+            for (int m = 16; m > 0; m >>= 1) {
+                Cand o = shfl_cand(best, m);
+                if (cand_less(o, best)) best = o;
+            }
+            if (lane == 0) {
+                S.cand[0] = best;
+                S.ncand = best.slot >= 0 ? 1 : 0;
+                for (int q = 0; q < CS; q++) mbar_arrive_remote(&S.vready, (uint32_t)q);
+            }
+            __syncwarp();
+            victim = late_victim();
+            if (lane == 0) S.victim = victim;
+        }
+        if (!refresh && victim >= 0) {
             const uint16_t *kr = a.K + (ubase + victim) * kD;
             const uint16_t *vr = a.V + (ubase + victim) * kD;
             for (int e = lane; e < kD; e += 32) {
@@ -581,6 +599,12 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             S.pM[tid] = v;
         }
         consumer_sync();                          // S.red is reused below
+        // a late victim leaves pass 2 (evict mode)
+        int vmask = -1;
+        if (late) {
+            const int v = late_victim();
+            if (!a.merge && v >= s0 && v < s1) vmask = v - s0;
+        }
         // pass 2: O^T += V^T P^T
         for (int t = 0; t < ntile; t++, g++) {
             const int stage = g % kStages;
@@ -594,7 +618,7 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
 #pragma unroll
                 for (int e = 0; e < 4; e++) {
                     const int li = t * kTile + rb + sl[e];
-                    pv[e] = (gq < G && li < nrows) ? expf(XS(gq, li) - Mg) : 0.f;
+                    pv[e] = (gq < G && li < nrows && li != vmask) ? expf(XS(gq, li) - Mg) : 0.f;
                     lsq += pv[e];
                 }
                 uint16_t hi0, lo0, hi1, lo1, hi2, lo2, hi3, lo3;
@@ -760,6 +784,17 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
         __syncthreads();
     };
     merge();
+    if (late) {
+        victim = S.victim;
+        if (victim < 0) {                       // no scored slot (or a timeout): refuse
+            if (r == 0 && tid == 0) {
+                record_status(a.status, S.bad ? KVC_ERR_TIMEOUT : KVC_ERR_INVALID_ARG);
+                a.n_evict[u] = 0;
+            }
+            cluster.sync();                     // nobody reads this CTA's partials any more
+            return;
+        }
+    }
 
     int vic_owner;
     if (refresh) {

@@ -137,7 +137,17 @@ C3 = PrefillConfig(
     description="prefill scoring: 32 layers, 32 q / 8 KV heads, N=16384, "
                 "window 32, W_O 4096x4096 ~ N(0, 1/4096), global top-K 32768")
 
-DECODE_CONFIGS = {"C0": C0, "C1": C1, "C2": C2, "C4": C4}
+# variants of the Qwen3-4B decode workload for the aggregation and merging
+# rows: Score-Free (InertiaKV: scored at the first decode step only) and
+# KeepKV ZIP-merging (partners outside the last 32 positions)
+C2_SCORE_FREE = C2.with_(name="C2-qwen3-4b-score-free", T=0,
+                         description=C2.description.replace("lazy refresh every 8 steps",
+                                                            "Score-Free (no refresh after step 1)"))
+C2_ZIP = C2.with_(name="C2-qwen3-4b-zip", merge_recent=32,
+                  description=C2.description + ", KeepKV ZIP-merging (R = 32)")
+
+DECODE_CONFIGS = {"C0": C0, "C1": C1, "C2": C2, "C4": C4,
+                  "C2-score-free": C2_SCORE_FREE, "C2-zip": C2_ZIP}
 PREFILL_CONFIGS = {"C3": C3}
 
 
