@@ -800,25 +800,35 @@ static int skey_cmp(const void *a, const void *b)
 }
 
 /*
- * Indicator, per-layer normalization and one model-wide top-K
- * [LaProx key designs 1-3]:
+ * Indicator, per-layer normalization and top-K selection [LaProx key
+ * designs 1-3; the allocation ablation table of the experiments]:
  *   p_{l,g,i} = c_{l,g,i} * r_{l,g,i}
  *   s_{l,g,i} = p_{l,g,i} / sum_{g',i'} p_{l,g',i'}   (normalize != 0;
  *               the layer's heads and tokens flattened together)
- *   keep the B_total largest s over all (l, g, i); equal scores are kept in
- *   ascending flat index (l*Hkv + g)*N + i (a reading; the page does not
- *   order ties).
+ *   alloc 0 (LaProx: head- and layer-flatten): keep the B_total largest s
+ *           over all (l, g, i);
+ *   alloc 1 (head-flatten only): every layer keeps its B_total / NL largest
+ *           s over its heads and tokens;
+ *   alloc 2 (uniform per head): every (l, g) keeps its B_total / (NL Hkv)
+ *           largest s.
+ * Equal scores are kept in ascending flat index (l*Hkv + g)*N + i (a
+ * reading; the page does not order ties).  B_total must be a multiple of the
+ * number of segments (1, NL or NL*Hkv).
  * Outputs: s [NL][Hkv][N]; keep [NL][Hkv][N] (0/1); counts [NL][Hkv];
- * idx [B_total] kept flat indices in ascending order; thr = the B_total-th
- * largest score.  Returns 0, or -1 if B_total is out of range.
+ * idx [B_total] kept flat indices in ascending order; thr [segments] = the
+ * segment's smallest kept score.  Returns 0, or -1 if B_total or alloc is
+ * out of range.
  */
 int ocl_prefill_select(int NL, int Hkv, int N, const double *c,
-                       const double *r, int normalize, int64_t B_total,
+                       const double *r, int normalize, int alloc, int64_t B_total,
                        double *s, uint8_t *keep, int32_t *counts, int64_t *idx,
                        double *thr)
 {
     int64_t M = (int64_t)NL * Hkv * N;
-    if (B_total < 0 || B_total > M) return -1;
+    if (B_total < 0 || B_total > M || alloc < 0 || alloc > 2) return -1;
+    int64_t nseg = alloc == 0 ? 1 : alloc == 1 ? NL : (int64_t)NL * Hkv;
+    if (B_total % nseg != 0) return -1;
+    int64_t seg = M / nseg, kseg = B_total / nseg;
     for (int l = 0; l < NL; l++) {
         double sum = 0.0;
         size_t lo = (size_t)l * Hkv * N, hi = lo + (size_t)Hkv * N;
@@ -826,12 +836,17 @@ int ocl_prefill_select(int NL, int Hkv, int N, const double *c,
         for (size_t j = lo; j < hi; j++)
             s[j] = normalize ? (sum > 0.0 ? c[j] * r[j] / sum : 0.0) : c[j] * r[j];
     }
-    ocl_skey *keys = (ocl_skey *)malloc((size_t)M * sizeof(ocl_skey));
-    for (int64_t j = 0; j < M; j++) { keys[j].s = s[j]; keys[j].flat = j; }
-    qsort(keys, (size_t)M, sizeof(ocl_skey), skey_cmp);
     memset(keep, 0, (size_t)M);
-    for (int64_t j = 0; j < B_total; j++) keep[keys[j].flat] = 1;
-    if (thr) *thr = B_total > 0 ? keys[B_total - 1].s : 0.0;
+    ocl_skey *keys = (ocl_skey *)malloc((size_t)seg * sizeof(ocl_skey));
+    for (int64_t q = 0; q < nseg; q++) {
+        for (int64_t j = 0; j < seg; j++) {
+            keys[j].s = s[q * seg + j];
+            keys[j].flat = q * seg + j;
+        }
+        qsort(keys, (size_t)seg, sizeof(ocl_skey), skey_cmp);
+        for (int64_t j = 0; j < kseg; j++) keep[keys[j].flat] = 1;
+        if (thr) thr[q] = kseg > 0 ? keys[kseg - 1].s : 0.0;
+    }
     free(keys);
     int64_t w = 0;
     for (int l = 0; l < NL; l++)

@@ -79,7 +79,7 @@ def _load():
             "ocl_prefill_colnorm": (None, [I, I, I, I, I, I, P, P, P]),
             "ocl_prefill_rownorm": (None, [I, I, I, I, P, P, P]),
             "ocl_prefill_rownorm_direct": (None, [I, I, I, I, I, I, I, P, P, I, P, P]),
-            "ocl_prefill_select": (I, [I, I, I, P, P, I, I64, P, P, P, P, P]),
+            "ocl_prefill_select": (I, [I, I, I, P, P, I, I, I64, P, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -402,7 +402,14 @@ def prefill_rownorm_direct(V, W_O, Hq: int, Hkv: int, d: int, N: int, l: int,
     return out
 
 
-def prefill_select(c, r, B_total: int, normalize: bool = True):
+# budget allocations of the LaProx ablation: global (head- and layer-flatten),
+# per layer (head-flatten only), uniform per head
+ALLOC_GLOBAL, ALLOC_LAYER, ALLOC_HEAD = 0, 1, 2
+
+
+def prefill_select(c, r, B_total: int, normalize: bool = True, alloc: int = ALLOC_GLOBAL):
+    """Selection of the LaProx scorer; ``thr`` is a float for the global
+    allocation and an array (one threshold per segment) otherwise."""
     c = np.ascontiguousarray(c, dtype=np.float64)
     r = np.ascontiguousarray(r, dtype=np.float64)
     NL, Hkv, N = c.shape
@@ -410,21 +417,24 @@ def prefill_select(c, r, B_total: int, normalize: bool = True):
     keep = np.zeros(c.shape, np.uint8)
     counts = np.zeros((NL, Hkv), np.int32)
     idx = np.zeros(max(int(B_total), 1), np.int64)
-    thr = np.zeros(1)
-    rc = _load().ocl_prefill_select(NL, Hkv, N, _p(c), _p(r), int(bool(normalize)),
+    nseg = 1 if alloc == ALLOC_GLOBAL else NL if alloc == ALLOC_LAYER else NL * Hkv
+    thr = np.zeros(nseg)
+    rc = _load().ocl_prefill_select(NL, Hkv, N, _p(c), _p(r), int(bool(normalize)), int(alloc),
                                     int(B_total), _p(s), _p(keep), _p(counts),
                                     _p(idx), _p(thr))
     if rc != 0:
-        raise ValueError("B_total out of range")
-    return dict(s=s, keep=keep, counts=counts, idx=idx[:int(B_total)], thr=float(thr[0]))
+        raise ValueError("B_total out of range or not a multiple of the segments")
+    return dict(s=s, keep=keep, counts=counts, idx=idx[:int(B_total)],
+                thr=float(thr[0]) if alloc == ALLOC_GLOBAL else thr)
 
 
 def prefill_score(q_win, K, V, W_O, *, NL: int, Hq: int, Hkv: int, d: int,
-                  N: int, w: int, B_total: int, normalize: bool = True):
+                  N: int, w: int, B_total: int, normalize: bool = True,
+                  alloc: int = ALLOC_GLOBAL):
     """Whole LaProx prefill scorer on the oracle (Gram route for r)."""
     Gram = prefill_gram(W_O, NL, Hq, Hkv, d)
     c = prefill_colnorm(q_win, K, NL, Hq, Hkv, d, N, w)
     r = prefill_rownorm(V, Gram, NL, Hkv, d, N)
-    res = prefill_select(c, r, B_total, normalize)
+    res = prefill_select(c, r, B_total, normalize, alloc)
     res.update(c=c, r=r, Gram=Gram)
     return res

@@ -126,3 +126,64 @@ def test_global_topk_matches_brute_force(seed):
     assert res["keep"].ravel().nonzero()[0].tolist() == list(best[1])
     assert res["counts"].sum() == Kb
     np.testing.assert_array_equal(res["counts"], res["keep"].sum(axis=2))
+
+
+def _brute_segment_topk(s, lo, hi, k):
+    """The k-subset of [lo, hi) with the largest total score, ties towards
+    the lexicographically smallest indices (exact rationals)."""
+    best = None
+    for S in itertools.combinations(range(lo, hi), k):
+        key = (-sum(s[j] for j in S), list(S))
+        if best is None or key < best[0]:
+            best = (key, S)
+    return list(best[1])
+
+
+@pytest.mark.parametrize("alloc", [O.ALLOC_LAYER, O.ALLOC_HEAD])
+@pytest.mark.parametrize("seed", range(6))
+def test_segment_allocations_match_brute_force(alloc, seed):
+    """LaProx allocation ablation: head-flatten only (a B_total / NL budget
+    per layer over its heads and tokens) and uniform per head (B_total /
+    (NL Hkv) per KV head) against subset enumeration within each segment,
+    with exact rational scores and ties."""
+    from fractions import Fraction
+    rng = np.random.default_rng(80 + seed)
+    NL, Hkv, N = 2, 2, 3
+    M = NL * Hkv * N
+    nseg = NL if alloc == O.ALLOC_LAYER else NL * Hkv
+    kseg = int(rng.integers(1, M // nseg))
+    c = rng.integers(1, 4, size=(NL, Hkv, N)).astype(float)
+    r = np.ones((NL, Hkv, N))
+    res = O.prefill_select(c, r, kseg * nseg, normalize=True, alloc=alloc)
+    p = (c * r).astype(int)
+    s = [Fraction(int(p.ravel()[j]), int(p[j // (Hkv * N)].sum())) for j in range(M)]
+    seg = M // nseg
+    want = []
+    for q in range(nseg):
+        want += _brute_segment_topk(s, q * seg, (q + 1) * seg, kseg)
+    assert res["keep"].ravel().nonzero()[0].tolist() == want
+    assert res["idx"].tolist() == want
+    np.testing.assert_array_equal(res["counts"], res["keep"].sum(axis=2))
+    if alloc == O.ALLOC_HEAD:
+        assert (res["counts"] == kseg).all()
+    else:
+        assert (res["counts"].sum(axis=1) == kseg).all()
+
+
+def test_allocations_agree_on_one_segment():
+    """With one layer and one KV head every allocation is the same top-K;
+    with one layer the global and per-layer selections coincide."""
+    rng = np.random.default_rng(9)
+    c1, r1 = rng.random((1, 1, 40)), rng.random((1, 1, 40))
+    sets = [O.prefill_select(c1, r1, 11, alloc=a)["idx"].tolist()
+            for a in (O.ALLOC_GLOBAL, O.ALLOC_LAYER, O.ALLOC_HEAD)]
+    assert sets[0] == sets[1] == sets[2]
+    c2, r2 = rng.random((1, 4, 30)), rng.random((1, 4, 30))
+    assert (O.prefill_select(c2, r2, 20, alloc=O.ALLOC_GLOBAL)["idx"].tolist()
+            == O.prefill_select(c2, r2, 20, alloc=O.ALLOC_LAYER)["idx"].tolist())
+
+
+def test_segment_budget_must_divide():
+    c, r = np.ones((2, 2, 5)), np.ones((2, 2, 5))
+    with pytest.raises(ValueError):
+        O.prefill_select(c, r, 7, alloc=O.ALLOC_HEAD)
