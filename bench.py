@@ -146,21 +146,27 @@ def run_prefill(pc, dev, reps=5):
     counts = torch.empty(NL, Hkv, dtype=torch.int32, device=dev)
     idx = torch.empty(max(B, 1), dtype=torch.int64, device=dev)
 
-    def call():
+    def call(alloc):
         kvc.kvc_prefill_score(NL, Hq, Hkv, d, N, w, B, 1, inp["q_win"], inp["K"], inp["V"], R,
-                              scores, keep, counts, idx, ws)
-    for _ in range(2):
-        call()
-    torch.cuda.synchronize()
-    times = []
-    for _ in range(reps):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        call()
-        b.record(stream)
+                              scores, keep, counts, idx, ws, alloc=alloc)
+
+    def timed(alloc):
+        for _ in range(2):
+            call(alloc)
         torch.cuda.synchronize()
-        times.append(a.elapsed_time(b))
-    ms = sorted(times)[len(times) // 2]
+        times = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call(alloc)
+            b.record(stream)
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
+        return sorted(times)[len(times) // 2]
+    # the LaProx ablation's other budget allocations: per layer (head-flatten
+    # only) and uniform per KV head, same scorer, segmented selection
+    alloc_ms = {"head_flatten": timed(kvc.ALLOC_LAYER), "uniform": timed(kvc.ALLOC_HEAD)}
+    ms = timed(kvc.ALLOC_GLOBAL)
     peak, kind = peaks()
     by = prefill_bytes(pc)
     ach = by / (ms * 1e-3) / 1e9
@@ -171,7 +177,8 @@ def run_prefill(pc, dev, reps=5):
                          "frac": ach / peak, "peak_kind": kind, "bytes_per_call": by,
                          "algorithmic_tflops": fl / (ms * 1e-3) / 1e12,
                          "kernels": "pack + prefill_val + prefill_attn + radix select"},
-            "kept": int(counts.sum().item())}
+            "kept": int(counts.sum().item()),
+            "allocations_ms_per_call": alloc_ms}
 
 
 KERNEL_SOURCES = ["kv_cache_eviction_kvc_gb300/csrc/kvc_fused.cu",

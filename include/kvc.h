@@ -78,6 +78,7 @@ typedef enum {
 
 enum { KVC_RULE_SINGLE = 0, KVC_RULE_CUMULATIVE = 1, KVC_RULE_EMA = 2 };
 enum { KVC_CORR_OFF = 0, KVC_CORR_ZERO_ORDER = 1, KVC_CORR_FIRST_ORDER = 2 };
+enum { KVC_ALLOC_GLOBAL = 0, KVC_ALLOC_LAYER = 1, KVC_ALLOC_HEAD = 2 };
 
 /* Method parameters of a decode stream. */
 typedef struct {
@@ -417,6 +418,14 @@ KVC_API size_t kvc_prefill_workspace_size(int32_t NL, int32_t Hkv, int32_t N,
  *   p = c r; s = p / (sum of p over the layer's heads and tokens) when
  *   normalize != 0, else s = p; keep the B_total largest s over all
  *   (l, g, i), equal scores kept in ascending flat index (l*Hkv + g)*N + i.
+ * alloc selects the budget allocation of LaProx's ablation table:
+ *   KVC_ALLOC_GLOBAL  the above (head- and layer-flatten: LaProx itself);
+ *   KVC_ALLOC_LAYER   head-flatten only: each layer keeps its B_total / NL
+ *                     largest s over its heads and tokens (Hkv <= 64);
+ *   KVC_ALLOC_HEAD    uniform: each (layer, KV head) keeps its
+ *                     B_total / (NL Hkv) largest s;
+ *   B_total must be a multiple of the number of segments
+ *   (KVC_ERR_INVALID_ARG); ties as above; idx stays ascending.
  * q_win [NL][Hq][w][d] bf16 (4-byte aligned), K, V [NL][Hkv][N][d] bf16
  * (16-byte aligned); R from kvc_prefill_prepare.  Outputs: scores
  * [NL][Hkv][N] fp32, keep [NL][Hkv][N] uint8 (0/1), counts [NL][Hkv] int32,
@@ -428,7 +437,7 @@ KVC_API size_t kvc_prefill_workspace_size(int32_t NL, int32_t Hkv, int32_t N,
  */
 KVC_API kvc_status kvc_prefill_score(int32_t NL, int32_t Hq, int32_t Hkv, int32_t d,
                              int32_t N, int32_t w, int64_t B_total,
-                             int32_t normalize, const uint16_t *q_win,
+                             int32_t normalize, int32_t alloc, const uint16_t *q_win,
                              const uint16_t *K, const uint16_t *V,
                              const float *R, float *scores, uint8_t *keep,
                              int32_t *counts, int64_t *idx, void *ws,

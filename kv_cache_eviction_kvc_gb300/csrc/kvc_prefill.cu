@@ -892,9 +892,13 @@ __global__ void layer_inv_kernel(const double *layer_sum, float *inv, int NL)
 
 // Bin of a histogram (n bins, ascending order key) holding the element of
 // 0-based rank `rank`, and that element's rank inside the bin; whole block.
+// kGlobal: the histogram is in global memory (other blocks' atomics, read
+// through L2); otherwise in this block's shared memory.
+template <bool kGlobal = true>
 __device__ void block_pick(const unsigned *hist, int n, long long rank, int *scan, int *bin_out,
                            long long *rin_out)
 {
+    auto ld = [&](int b) -> unsigned { return kGlobal ? __ldcg(hist + b) : hist[b]; };
     __shared__ int sb;
     __shared__ long long sr;
     const int per = (n + blockDim.x - 1) / blockDim.x;
@@ -905,13 +909,13 @@ __device__ void block_pick(const unsigned *hist, int n, long long rank, int *sca
     }
     int loc = 0;
     for (int k = 0; k < per; k++)
-        if (b0 + k < n) loc += (int)__ldcg(hist + b0 + k);
+        if (b0 + k < n) loc += (int)ld(b0 + k);
     int total;
     const int ex = block_exscan(loc, scan, &total);
     if (ex <= rank && rank < (long long)ex + loc) {
         long long cum = ex;
         for (int k = 0; k < per; k++) {
-            const long long h = __ldcg(hist + b0 + k);
+            const long long h = ld(b0 + k);
             if (cum + h > rank) {
                 sb = b0 + k;
                 sr = rank - cum;
@@ -1100,6 +1104,123 @@ __global__ void __launch_bounds__(kTkBlock) topk_write_kernel(const float *s, in
     }
 }
 
+// Segmented selection for the LaProx allocation ablation: one block per
+// segment (a layer for head-flatten only, a (layer, KV head) for the uniform
+// allocation) keeps its kseg largest scores.  The same three radix passes
+// as the global select, on shared-memory histograms (pass 1 also
+// normalizes in place), then one ordered pass over the segment: equal keys
+// are kept in flat order (tie rank carried across chunks) and the kept flat
+// indices land in ascending order in idx[segment * kseg ...].
+constexpr int kSegMaxHeads = 64;          // KV heads a layer segment may span
+__global__ void __launch_bounds__(kTkBlock) seg_select_kernel(float *s, int N, int seg_len, int kseg,
+                                                               int per_layer, const float *inv,
+                                                               int normalize, uint8_t *keep,
+                                                               int *counts, int64_t *idx)
+{
+    __shared__ unsigned h[kH1];
+    __shared__ int scan[40];
+    __shared__ int cnt[kSegMaxHeads];
+    __shared__ long long carry[2];
+    const int q = blockIdx.x, tid = threadIdx.x;
+    const int64_t base = (int64_t)q * seg_len;
+    float *sg = s + base;
+    const float sc = normalize ? inv[(int)(base / per_layer)] : 1.f;
+    const int head0 = (int)(base / N), nheads = seg_len / N;
+    for (int i = tid; i < kSegMaxHeads; i += blockDim.x) cnt[i] = 0;
+    if (kseg == 0) {                         // nothing kept: scale and clear only
+        for (int i = tid; i < seg_len; i += blockDim.x) {
+            if (normalize) sg[i] *= sc;
+            keep[base + i] = 0;
+        }
+        __syncthreads();
+        if (counts)
+            for (int g = tid; g < nheads; g += blockDim.x) counts[head0 + g] = 0;
+        return;
+    }
+    uint32_t pre = 0;                        // digits picked so far
+    long long rank = kseg - 1;               // 0-based rank of the kseg-th largest
+    for (int pass = 1; pass <= 3; pass++) {
+        const int NB = pass == 3 ? kH3 : kH1;
+        for (int i = tid; i < NB; i += blockDim.x) h[i] = 0;
+        __syncthreads();
+        for (int i0 = 0; i0 < seg_len; i0 += 4 * kTkBlock) {
+            float v[4];
+#pragma unroll
+            for (int u = 0; u < 4; u++) {        // four loads in flight
+                const int i = i0 + u * kTkBlock + tid;
+                v[u] = i < seg_len ? sg[i] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const int i = i0 + u * kTkBlock + tid;
+                int bin = -1;
+                if (i < seg_len) {
+                    if (pass == 1 && normalize) {
+                        v[u] *= sc;
+                        sg[i] = v[u];
+                    }
+                    const uint32_t k = desc_key(v[u]);
+                    if (pass == 1) bin = (int)(k >> 20);
+                    else if (pass == 2) { if ((k >> 20) == pre) bin = (int)((k >> 8) & (kH2 - 1)); }
+                    else if ((k >> 8) == pre) bin = (int)(k & (kH3 - 1));
+                }
+                hist_add(h, bin);
+            }
+        }
+        __syncthreads();
+        int d;
+        long long r;
+        block_pick<false>(h, NB, rank, scan, &d, &r);
+        rank = r;
+        pre = pass == 3 ? ((pre << 8) | (uint32_t)d) : ((pre << 12) | (uint32_t)d);
+    }
+    const uint32_t thr = pre;                // order key of the kseg-th largest score
+    const long long need = rank + 1;         // keys equal to thr that are kept
+    if (tid == 0) carry[0] = carry[1] = 0;
+    __syncthreads();
+    for (int c0 = 0; c0 < seg_len; c0 += kTkSpan) {
+        const int i0 = c0 + kTkPer * tid;
+        uint32_t key[kTkPer];
+        int neq = 0;
+#pragma unroll
+        for (int u = 0; u < kTkPer; u++) {
+            key[u] = i0 + u < seg_len ? desc_key(sg[i0 + u]) : 0xffffffffu;
+            neq += i0 + u < seg_len && key[u] == thr;
+        }
+        int teq;
+        long long er = carry[0] + block_exscan(neq, scan, &teq);
+        bool kp[kTkPer];
+        int nk = 0;
+#pragma unroll
+        for (int u = 0; u < kTkPer; u++) {
+            const bool in = i0 + u < seg_len;
+            const bool iseq = in && key[u] == thr;
+            kp[u] = in && (key[u] < thr || (iseq && er < need));
+            er += iseq;
+            nk += kp[u];
+        }
+        int tk;
+        long long ko = carry[1] + block_exscan(nk, scan, &tk);
+#pragma unroll
+        for (int u = 0; u < kTkPer; u++) {
+            if (i0 + u < seg_len) keep[base + i0 + u] = (uint8_t)kp[u];
+            if (kp[u]) {
+                if (idx && ko < kseg) idx[(int64_t)q * kseg + ko] = base + i0 + u;
+                ko++;
+                atomicAdd(&cnt[(i0 + u) / N], 1);
+            }
+        }
+        __syncthreads();
+        if (tid == 0) {
+            carry[0] += teq;
+            carry[1] += tk;
+        }
+        __syncthreads();
+    }
+    if (counts)
+        for (int g = tid; g < nheads; g += blockDim.x) counts[head0 + g] = cnt[g];
+}
+
 struct PfWs {
     float *p;
     double *layer_sum;
@@ -1189,7 +1310,8 @@ size_t kvc_prefill_workspace_size(int32_t NL, int32_t Hkv, int32_t N, int64_t B_
 }
 
 kvc_status kvc_prefill_score(int32_t NL, int32_t Hq, int32_t Hkv, int32_t d, int32_t N,
-                             int32_t w, int64_t B_total, int32_t normalize, const uint16_t *q_win,
+                             int32_t w, int64_t B_total, int32_t normalize, int32_t alloc,
+                             const uint16_t *q_win,
                              const uint16_t *K, const uint16_t *V, const float *R,
                              float *scores, uint8_t *keep, int32_t *counts, int64_t *idx,
                              void *ws, size_t ws_bytes, void *stream)
@@ -1204,6 +1326,14 @@ kvc_status kvc_prefill_score(int32_t NL, int32_t Hq, int32_t Hkv, int32_t d, int
     const int64_t M = (int64_t)NL * Hkv * N;
     PF_CHECK(B_total >= 0 && B_total <= M, KVC_ERR_INVALID_ARG,
              "kvc_prefill_score: B_total = %lld outside [0, %lld]", (long long)B_total, (long long)M);
+    PF_CHECK(alloc >= KVC_ALLOC_GLOBAL && alloc <= KVC_ALLOC_HEAD, KVC_ERR_INVALID_ARG,
+             "kvc_prefill_score: alloc = %d unknown", alloc);
+    const int64_t nseg = alloc == KVC_ALLOC_GLOBAL ? 1 : alloc == KVC_ALLOC_LAYER ? NL : (int64_t)NL * Hkv;
+    PF_CHECK(B_total % nseg == 0, KVC_ERR_INVALID_ARG,
+             "kvc_prefill_score: B_total = %lld is not a multiple of the %lld segments",
+             (long long)B_total, (long long)nseg);
+    PF_CHECK(alloc != KVC_ALLOC_LAYER || Hkv <= kSegMaxHeads, KVC_ERR_UNSUPPORTED,
+             "kvc_prefill_score: per-layer allocation supports up to %d KV heads", kSegMaxHeads);
     const int per_cta = ((N + kCS - 1) / kCS + kTk - 1) / kTk * kTk;
     PF_CHECK(q_win && K && V && R && keep, KVC_ERR_INVALID_ARG,
              "kvc_prefill_score: q_win, K, V, R and keep are required");
@@ -1284,6 +1414,13 @@ kvc_status kvc_prefill_score(int32_t NL, int32_t Hq, int32_t Hkv, int32_t d, int
 
     // radix select of the B_total largest s (pass 1 also normalizes in place)
     if (normalize) layer_inv_kernel<<<1, 256, 0, st>>>(pw.layer_sum, pw.inv, NL);
+    if (alloc != KVC_ALLOC_GLOBAL) {
+        const int seg_len = (int)(M / nseg);
+        seg_select_kernel<<<(unsigned)nseg, kTkBlock, 0, st>>>(pbuf, N, seg_len, (int)(B_total / nseg),
+                                                              (int)per_layer, pw.inv, normalize, keep,
+                                                              counts, idx);
+        return pf_cuda(cudaGetLastError(), "kvc_prefill_score segmented select launch");
+    }
     const int sel_grid = (int)std::min<int64_t>((M + kTkBlock - 1) / kTkBlock, 2 * (int64_t)nsm);
     unsigned *h1 = pw.hist, *h2 = h1 + kH1, *h3 = h2 + kH2;
     const long long rank0 = B_total > 0 ? B_total - 1 : 0;

@@ -22,6 +22,7 @@ STATUS_NAMES = {0: "KVC_OK", 1: "KVC_ERR_INVALID_ARG", 2: "KVC_ERR_SHAPE",
                 6: "KVC_ERR_WORKSPACE"}
 RULE_SINGLE, RULE_CUMULATIVE, RULE_EMA = 0, 1, 2
 CORR_OFF, CORR_ZERO_ORDER, CORR_FIRST_ORDER = 0, 1, 2
+ALLOC_GLOBAL, ALLOC_LAYER, ALLOC_HEAD = 0, 1, 2
 
 EXPORTED = (
     "kvc_version", "kvc_last_error", "kvc_status_string",
@@ -93,8 +94,8 @@ def load(build: bool = True):
         "kvc_decode_attend_noalloc": (I32, [PP, I32, I32, I32, P, P, P, PC, P, P, P, P, P]),
         "kvc_prefill_prepare": (I32, [I32, I32, I32, I32, I32, P, P, P]),
         "kvc_prefill_workspace_size": (SZ, [I32, I32, I32, I64]),
-        "kvc_prefill_score": (I32, [I32, I32, I32, I32, I32, I32, I64, I32, P, P, P, P, P, P,
-                                    P, P, P, SZ, P]),
+        "kvc_prefill_score": (I32, [I32, I32, I32, I32, I32, I32, I64, I32, I32, P, P, P, P, P,
+                                    P, P, P, P, SZ, P]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -284,10 +285,11 @@ def kvc_prefill_workspace_size(NL, Hkv, N, B_total) -> int:
 
 
 def kvc_prefill_score(NL, Hq, Hkv, d, N, w, B_total, normalize, q_win, K, V, R, scores, keep,
-                      counts, idx, ws, stream=None):
+                      counts, idx, ws, stream=None, alloc=ALLOC_GLOBAL):
     bf = torch.bfloat16
     _check(load().kvc_prefill_score(
         int(NL), int(Hq), int(Hkv), int(d), int(N), int(w), int(B_total), int(normalize),
+        int(alloc),
         _ptr(q_win, bf, "q_win"), _ptr(K, bf, "K"), _ptr(V, bf, "V"),
         _ptr(R, torch.float32, "R"), _ptr(scores, torch.float32, "scores", optional=True),
         _ptr(keep, torch.uint8, "keep"), _ptr(counts, torch.int32, "counts", optional=True),

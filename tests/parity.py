@@ -289,7 +289,10 @@ class PrefillReport:
 
 
 def run_prefill_parity(cfg: W.PrefillConfig, *, seed: int = 0, device="cuda",
-                       normalize: bool = True) -> PrefillReport:
+                       normalize: bool = True, alloc: int = 0) -> PrefillReport:
+    """alloc: 0 global top-K (LaProx), 1 per layer (head-flatten only),
+    2 uniform per KV head; near-ties are judged against the threshold of
+    the element's own segment."""
     from kv_cache_eviction_kvc_gb300 import kvc as K
     NL, Hq, Hkv, d, N, w, B = cfg.NL, cfg.Hq, cfg.Hkv, cfg.d, cfg.N, cfg.w, cfg.B_total
     inp = W.gen_prefill_scorer(cfg, device, seed)
@@ -303,10 +306,10 @@ def run_prefill_parity(cfg: W.PrefillConfig, *, seed: int = 0, device="cuda",
     counts = torch.empty(NL, Hkv, dtype=torch.int32, device=device)
     idx = torch.empty(max(B, 1), dtype=torch.int64, device=device)
     K.kvc_prefill_score(NL, Hq, Hkv, d, N, w, B, int(normalize), inp["q_win"], inp["K"],
-                        inp["V"], R, scores, keep, counts, idx, ws)
+                        inp["V"], R, scores, keep, counts, idx, ws, alloc=alloc)
     torch.cuda.synchronize()
     ref = O.prefill_score(inp["q_win"], inp["K"], inp["V"], inp["W_O"], NL=NL, Hq=Hq, Hkv=Hkv,
-                          d=d, N=N, w=w, B_total=B, normalize=normalize)
+                          d=d, N=N, w=w, B_total=B, normalize=normalize, alloc=alloc)
     rep = PrefillReport()
     # the factor is not unique; R^T R is the Gram matrix
     Rn = R.cpu().numpy().astype(np.float64)
@@ -318,15 +321,17 @@ def run_prefill_parity(cfg: W.PrefillConfig, *, seed: int = 0, device="cuda",
     kg = keep.cpu().numpy().astype(bool).ravel()
     kr = ref["keep"].astype(bool).ravel()
     diff = np.nonzero(kg ^ kr)[0]
-    thr = ref["thr"]
+    thr = np.atleast_1d(ref["thr"])
+    seg = M // len(thr)
     flat_s = s_ref.ravel()
     for j in diff:
-        if abs(flat_s[j] - thr) <= TIE_REL * abs(thr):
+        t_ = thr[j // seg]
+        if abs(flat_s[j] - t_) <= TIE_REL * abs(t_):
             rep.band_hits += 1
         else:
             rep.mismatches += 1
             if not rep.first_mismatch:
-                rep.first_mismatch = f"flat {j}: s_ref {flat_s[j]!r} thr {thr!r} gpu keep {kg[j]}"
+                rep.first_mismatch = f"flat {j}: s_ref {flat_s[j]!r} thr {t_!r} gpu keep {kg[j]}"
     rep.kept = int(kg.sum())
     rep.counts_ok = bool(rep.kept == B and np.array_equal(
         counts.cpu().numpy(), kg.reshape(NL, Hkv, N).sum(axis=2)))

@@ -39,3 +39,20 @@ SMALL = W.C3.with_(NL=2, N=1024, B_total=512)
         "long", "rank-deficient"])
 def test_prefill_edge_cases(cfg, normalize):
     check(run_prefill_parity(cfg, normalize=normalize))
+
+
+@pytest.mark.parametrize("alloc", [1, 2], ids=["head-flatten", "uniform"])
+def test_c3_allocations(alloc):
+    check(run_prefill_parity(W.C3, alloc=alloc))
+
+
+@pytest.mark.parametrize("cfg,normalize,alloc", [
+    (SMALL, True, 1),
+    (SMALL, True, 2),
+    (SMALL.with_(N=1000, B_total=784), True, 2),          # ragged, 49 per head
+    (SMALL.with_(N=1000, B_total=786), False, 1),         # unnormalized, 393 per layer
+    (SMALL.with_(B_total=0), True, 2),                    # nothing kept
+    (SMALL.with_(NL=1, Hq=8, Hkv=2, N=513, B_total=1026), True, 2),   # keep everything
+], ids=["layer", "head", "head-ragged", "layer-unnormalized", "head-empty", "head-keep-all"])
+def test_prefill_allocation_edge_cases(cfg, normalize, alloc):
+    check(run_prefill_parity(cfg, normalize=normalize, alloc=alloc))
