@@ -376,10 +376,8 @@ def run_ours(args, cfg, rank, world):
     total_ms = t_start.elapsed_time(t_end)
     per_launch = [a.elapsed_time(b) for a, b in ev]
     if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+        from kv_cache_eviction_kvc_gb300.dist import max_over_ranks
+        total_ms = max_over_ranks(total_ms, dev)
     assert st.device_status() == 0
 
     # algorithmic bytes of the timed launches (refresh pattern of steps 2 + i)
