@@ -253,6 +253,50 @@ void ocl_update_util(void *h, const double *probs, int rule, double alpha)
     }
 }
 
+/*
+ * Moment-informed eviction scores [MomentKV sec 4.2, "moment residual" and
+ * "moment-aware eviction score"; Algorithm 1, phase 1]: for every live slot
+ *   r_i = v_i - v_bar - S_tilde (k_i - k_bar) / (n_e sqrt(d))
+ *   (v_bar = s_v / n_e, k_bar = s_k / n_e, S_tilde = S - s_v s_k^T / n_e;
+ *    r_i = v_i while n_e = 0, as the algorithm sets v_bar, S_tilde to 0)
+ *   score_i = alpha_i ||r_i||_2,
+ * alpha_i being the slot's attention weight, given in probs [U][cap] (the
+ * head-mean of the vote-weighted probabilities, as ocl_attend writes it).
+ * Output: out [U][cap] (entries past n[u] untouched).
+ */
+void ocl_mi_scores(void *h, const double *probs, double *out)
+{
+    ocl_session *s = (ocl_session *)h;
+    int d = s->d;
+    double rsd = 1.0 / sqrt((double)d);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int u = 0; u < s->U; u++) {
+        size_t base = (size_t)u * s->cap;
+        double ne = s->ne[u];
+        const double *sk = &s->sk[(size_t)u * d], *sv = &s->sv[(size_t)u * d];
+        const double *S = &s->S[(size_t)u * d * d];
+        double *dk = (double *)malloc((size_t)d * sizeof(double));
+        for (int i = 0; i < s->n[u]; i++) {
+            const uint16_t *ki = &s->k[(base + i) * d], *vi = &s->v[(base + i) * d];
+            double rr = 0.0;
+            if (ne > 0.0) {
+                for (int b = 0; b < d; b++) dk[b] = bfd(ki[b]) - sk[b] / ne;
+                for (int a = 0; a < d; a++) {
+                    double t = 0.0;
+                    for (int b = 0; b < d; b++)
+                        t += (S[(size_t)a * d + b] - sv[a] * sk[b] / ne) * dk[b];
+                    double r = bfd(vi[a]) - sv[a] / ne - t / ne * rsd;
+                    rr += r * r;
+                }
+            } else {
+                for (int a = 0; a < d; a++) rr += bfd(vi[a]) * bfd(vi[a]);
+            }
+            out[base + i] = probs[base + i] * sqrt(rr);
+        }
+        free(dk);
+    }
+}
+
 /* Export the slot table (positions, votes, utilities, scored flags). */
 void ocl_get_slots(void *h, int32_t *n, int32_t *pos, int32_t *vote,
                    double *util, uint8_t *scored)

@@ -33,6 +33,7 @@ _lock = threading.Lock()
 _lib = None
 
 RULE_SINGLE, RULE_CUMULATIVE, RULE_EMA = 0, 1, 2
+RULE_MI = 3   # MomentKV moment-informed score alpha_i ||r_i||, re-scored every step
 CORR_OFF, CORR_ZERO_ORDER, CORR_FIRST_ORDER = 0, 1, 2
 
 
@@ -74,6 +75,7 @@ def _load():
             "ocl_set_row": (I, [P, I, ctypes.c_int32, P, P]),
             "ocl_get_rows": (None, [P, P, P]),
             "ocl_moments": (None, [P, P, P, P, P]),
+            "ocl_mi_scores": (None, [P, P, P]),
             "ocl_output": (None, [P, P, I, P, P, P]),
             "ocl_prefill_gram": (None, [I, I, I, I, I, P, P]),
             "ocl_prefill_colnorm": (None, [I, I, I, I, I, I, P, P, P]),
@@ -237,6 +239,14 @@ class DecodeSession:
         self.lib.ocl_get_rows(self.h, _p(k), _p(v))
         return k, v
 
+    def mi_scores(self, probs):
+        """MomentKV moment-informed scores alpha_i ||r_i|| [U][cap] from the
+        attention weights probs [U][cap] and the session's moments."""
+        probs = np.ascontiguousarray(probs, dtype=np.float64)
+        out = np.zeros((self.U, self.cap))
+        self.lib.ocl_mi_scores(self.h, _p(probs), _p(out))
+        return out
+
     def moments(self):
         """Returns (n [U], mu_k [U][d], mu_v [U][d], C [U][d][d])."""
         n = np.zeros(self.U)
@@ -280,7 +290,10 @@ def decode_step(sess: DecodeSession, t: int, new_pos: int, q, knew, vnew, *,
 
     1. append (k_new, v_new) with vote 1
     2. vote-weighted attention over all slots -> lse, f_all, head-mean probs
-    3. refresh step: utility update                 (InertiaKV sec 3.1 eqs 2-4)
+    3. refresh step: utility update                 (InertiaKV sec 3.1 eqs 2-4);
+       rule RULE_MI: every step, utility = alpha ||r|| (MomentKV sec 4.2;
+       a step removing several slots takes the k lowest of these scores at
+       once, with the moments it entered with)
     4. victims: the k = n - L lowest (utility, position) scored slots
     5. fold victims into the moments and remove them  (eviction phase)
     6. retained attention + moment correction         (inference phase)
@@ -303,14 +316,22 @@ def decode_step(sess: DecodeSession, t: int, new_pos: int, q, knew, vnew, *,
     """
     sess.append(knew, vnew, new_pos)
     lse, f_all, probs = sess.attend(q)
-    refresh = is_refresh(t, T)
-    if refresh:
-        sess.update_util(probs, rule, alpha)
+    scores = None
+    if rule == RULE_MI:
+        # MomentKV Algorithm 1: every step scores every slot (the new one
+        # included) by alpha ||r|| with the moments as they enter the step
+        refresh = True
+        scores = sess.mi_scores(probs)
+        sess.update_util(scores, RULE_SINGLE, alpha)
+    else:
+        refresh = is_refresh(t, T)
+        if refresh:
+            sess.update_util(probs, rule, alpha)
     n = sess.slots()[0]
     kmax = int(max(1, (n - L).max()))
     vic, nv, thr = sess.select(L, kmax)
     proposal = dict(victims=vic, nvict=nv, thr=thr, lse=lse, f_all=f_all,
-                    probs=probs if refresh else None, refresh=refresh)
+                    probs=probs if refresh else None, refresh=refresh, mi_scores=scores)
     if choose is not None:
         vic, nv = choose(t, proposal)
     merged = np.zeros(len(nv), bool)

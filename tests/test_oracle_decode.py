@@ -484,3 +484,108 @@ def test_score_free_evicts_in_step1_order():
             got.append(sorted(int(p) for p in r["applied_victims"][u, :nv]))
         assert got[0] == sorted(order[:N + 1 - L])
         assert [g[0] for g in got[1:]] == order[N + 1 - L:N + 1 - L + S - 1]
+
+
+# ---------------------------------------------------------------- moment-informed eviction
+
+def _two_token_moments_session(G=1):
+    """One unit whose eviction set is {(k1, v1), (k2, v2)} (integer vectors),
+    so that k_bar = (k1 + k2)/2, dk = (k1 - k2)/2, C = dv dk^T (population
+    covariance of two points), plus retained slots appended afterwards."""
+    d = 16
+    k1 = np.zeros(d); k1[:4] = [3, 1, 1, 1]          # dk = (1,1,1,1,0..), |dk|^2 = 4 = sqrt(d)
+    k2 = np.zeros(d); k2[:4] = [1, -1, -1, -1]
+    v1 = np.zeros(d); v1[4:6] = [2, 0]
+    v2 = np.zeros(d); v2[4:6] = [0, 2]                # dv = (1, -1) in dims 4, 5
+    s = O.DecodeSession(1, G, d, 8)
+    s.load(0, np.stack([k1, k2]), np.stack([v1, v2]))
+    s.evict(np.array([[0, 1]], np.int32), np.array([2], np.int32))
+    return s, d, (k1 + k2) / 2, (k1 - k2) / 2, (v1 + v2) / 2, (v1 - v2) / 2
+
+
+def test_mi_residual_closed_form_and_exact_prediction():
+    """MomentKV moment residual r = v - v_bar - C (k - k_bar) / sqrt(d) with
+    the two-token eviction set: C (k - k_bar)/sqrt(d) = dv (dk . (k - k_bar))
+    / sqrt(d).  A token at k_bar + 2 dk with value v_bar + 2 dv is predicted
+    exactly (score 0); another one's residual norm is the closed form."""
+    s, d, kb, dk, vb, dv = _two_token_moments_session()
+    ka, va = kb + 2 * dk, vb + 2 * dv                 # on the affine model
+    kx, vx = kb + dk, vb + 3 * dv                     # off it by dv
+    ky = kb.copy(); ky[8] = 5.0
+    vy = vb.copy(); vy[9] = 2.0                       # dk . (ky - kb) = 0
+    for j, (kk, vv) in enumerate([(ka, va), (kx, vx), (ky, vy)]):
+        s.append(kk[None], vv[None], 10 + j)
+    probs = np.zeros((1, 8)); probs[0, :3] = [0.5, 0.25, 0.125]
+    sc = s.mi_scores(probs)[0, :3]
+    assert sc[0] == 0.0
+    assert sc[1] == pytest.approx(0.25 * 2.0 * np.linalg.norm(dv), rel=1e-14)
+    assert sc[2] == pytest.approx(0.125 * np.linalg.norm(vy - vb), rel=1e-14)
+    s.close()
+
+
+def test_mi_scores_without_moments_are_weight_times_value_norm():
+    """n_e = 0: v_bar and S_tilde are zero, r = v and the score is
+    alpha ||v|| (MomentKV Algorithm 1, phase 1)."""
+    rng = np.random.default_rng(21)
+    k, v = bf(rng.normal(size=(9, 8))), bf(rng.normal(size=(9, 8)))
+    s = make_session(k, v)
+    probs = np.zeros((1, s.cap)); probs[0, :9] = rng.random(9)
+    sc = s.mi_scores(probs)[0, :9]
+    np.testing.assert_allclose(sc, probs[0, :9] * np.linalg.norm(v, axis=1), rtol=1e-14)
+    s.close()
+
+
+def test_mi_residual_matches_numpy_covariance_and_is_shift_invariant():
+    """Residual norms against numpy's two-pass population covariance of the
+    evicted set (np.cov, bias=True), and invariant when every key, or every
+    value, is shifted by one common vector (the centring)."""
+    rng = np.random.default_rng(22)
+    d, nE, nR = 8, 6, 5
+    # quarter-integers: the shifted arrays stay exact in bf16
+    base_k = rng.integers(-8, 9, size=(nE + nR, d)) / 4.0
+    base_v = rng.integers(-8, 9, size=(nE + nR, d)) / 4.0
+    shift = rng.integers(-3, 4, size=d).astype(float)
+
+    def scores(k, v):
+        s = make_session(k, v, cap=nE + nR + 2)
+        s.evict(np.arange(nE, dtype=np.int32)[None], np.array([nE], np.int32))
+        probs = np.ones((1, s.cap))
+        out = s.mi_scores(probs)[0, :nR]
+        s.close()
+        return out
+    ref = scores(base_k, base_v)
+    KE, VE = base_k[:nE], base_v[:nE]
+    C = np.cov(np.hstack([VE, KE]).T, bias=True)[:d, d:]
+    R = base_v[nE:] - VE.mean(0) - (base_k[nE:] - KE.mean(0)) @ C.T / math.sqrt(d)
+    np.testing.assert_allclose(ref, np.linalg.norm(R, axis=1), rtol=1e-12)
+    np.testing.assert_allclose(scores(base_k + shift, base_v), ref, rtol=1e-12)
+    np.testing.assert_allclose(scores(base_k, base_v + shift), ref, rtol=1e-12)
+
+
+def test_mi_generation_evicts_the_lowest_score():
+    """Decode loop with the moment-informed rule: every step re-scores (the
+    new token included) and evicts the slot with the lowest alpha ||r||
+    (ties to the older position), checked by brute force on the step's
+    scores."""
+    rng = np.random.default_rng(23)
+    U, N, d, G, S, L = 2, 16, 8, 2, 6, 10
+    kp, vp = bf(rng.normal(size=(U, N, d))), bf(rng.normal(size=(U, N, d)))
+    qs = bf(rng.normal(size=(S, U, G, d)))
+    ks, vs = bf(rng.normal(size=(S, U, d))), bf(rng.normal(size=(S, U, d)))
+    sess = O.DecodeSession(U, G, d, N + S)
+    for u in range(U):
+        sess.load(u, kp[u], vp[u])
+    for s_ in range(S):
+        t = s_ + 1
+        n0, pos0, _, _, _ = sess.slots()
+        r = O.decode_step(sess, t, N + t - 1, qs[s_], ks[s_], vs[s_], L=L, rule=O.RULE_MI,
+                          alpha=0.9, T=1, correction=O.CORR_FIRST_ORDER)
+        assert r["refresh"]
+        for u in range(U):
+            n = int(n0[u]) + 1
+            pos = np.append(pos0[u, : n0[u]], N + t - 1)
+            sc = r["mi_scores"][u, :n]
+            k = n - L
+            want = sorted(pos[i] for i in sorted(range(n), key=lambda i: (sc[i], pos[i]))[:k])
+            assert sorted(r["applied_victims"][u, : r["applied_nvict"][u]].tolist()) == want
+    sess.close()
