@@ -104,6 +104,23 @@ def step_bytes(cfg, refresh: bool, emit_probs: bool) -> int:
     return b * cfg.U
 
 
+def fp32_peak_tflops() -> float:
+    """CUDA-core fp32 peak of the GPU from its unit counts and the measured
+    maximum SM clock: 152 SMs x 128 fp32 lanes x 2 FLOP (FMA) x clock."""
+    mhz = 2070.0
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            mhz = float(json.load(f).get("sm_max_mhz", mhz))
+    return 152 * 128 * 2 * mhz * 1e6 / 1e12
+
+
+def mi_flops(cfg) -> int:
+    """Algorithmic FLOPs of the moment-informed scores of one steady-state
+    step: C (k - mu_k) for every slot of every unit (L + 1 slots, d x d)."""
+    return 2 * (cfg.L + 1) * cfg.d * cfg.d * cfg.U
+
+
 def prefill_bytes(pc) -> int:
     """Algorithmic HBM bytes of one prefill scoring call: K and V once, the
     window queries, the value-norm factors, the indicator written, then read and
@@ -350,7 +367,10 @@ def run_ours(args, cfg, rank, world):
         st.step(t, N + t - 1, x["q"], x["k_new"], x["v_new"], max_len=L + 1)
         if events is not None:
             events[1].record(stream)
-        launches += 2 if merge else 1         # merge mode: fused step + merge kernel
+        # merge mode: fused step + merge kernel; the moment-informed rule runs
+        # the call sequence (attend split + final, scores, aggregate, fold,
+        # correction, compaction)
+        launches += 7 if cfg.rule == W.RULE_MI else (2 if merge else 1)
 
     for i in range(args.warmup):
         do_step(i)
@@ -451,6 +471,29 @@ def run_ours(args, cfg, rank, world):
 
     peak, peak_kind = peaks()
     ms_per_step = total_ms / args.steps
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak,
+                "traffic": (profiled_traffic() if (args.batch is None and args.prefill is None
+                                                   and args.config == "C2") else None),
+                "traffic_note": "ncu dram read+write per lazy-step launch, 864-unit capture "
+                                "scaled by units (profiles/fused_step_kernel_qwen3-4b.md)",
+                "peak_kind": peak_kind,
+                "kernel": ("fused_step_kernel + zip_merge_kernel (kvc_decode_step, merge mode)"
+                           if merge else "fused_step_kernel (kvc_decode_step, steady state)"),
+                "bytes_per_launch": avg_bytes, "avg_launch_ms": avg_launch_ms}
+    if cfg.rule == W.RULE_MI:
+        # the moment-informed scores are a CUDA-core fp32 contraction: the
+        # step is bounded by fp32 FMA throughput, not by HBM
+        tf = mi_flops(cfg) / (avg_launch_ms * 1e-3) / 1e12
+        pk = fp32_peak_tflops()
+        roofline = {"bound": "alu", "achieved": tf, "peak": pk, "unit": "TFLOP/s",
+                    "frac": tf / pk, "traffic": None,
+                    "peak_kind": "derived: 152 SMs x 128 fp32 lanes x 2 x max SM clock",
+                    "kernel": "mi_score_kernel inside the call sequence (kvc_decode_step, "
+                              "rule MI); the step time includes attend, aggregate, fold, "
+                              "correction and compaction",
+                    "flops_per_step": mi_flops(cfg), "avg_launch_ms": avg_launch_ms,
+                    "hbm_gbs_of_step": achieved}
     value = world * args.steps / (total_ms * 1e-3)
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -466,16 +509,7 @@ def run_ours(args, cfg, rank, world):
         "achieved_gbs": achieved,
         "hbm_frac": achieved / peak,
         "step1_ms": step1_ms,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak,
-                     "traffic": (profiled_traffic() if (args.batch is None and args.prefill is None
-                                                        and args.config == "C2") else None),
-                     "traffic_note": "ncu dram read+write per lazy-step launch, 864-unit capture "
-                                     "scaled by units (profiles/fused_step_kernel_qwen3-4b.md)",
-                     "peak_kind": peak_kind,
-                     "kernel": ("fused_step_kernel + zip_merge_kernel (kvc_decode_step, merge mode)"
-                                if merge else "fused_step_kernel (kvc_decode_step, steady state)"),
-                     "bytes_per_launch": avg_bytes, "avg_launch_ms": avg_launch_ms},
+        "roofline": roofline,
         "clocks": clocks,
         "gpu_launches": launches,
         "e2e": e2e,

@@ -76,7 +76,7 @@ typedef enum {
     KVC_ERR_WORKSPACE = 6     /* workspace missing, misaligned or too small  */
 } kvc_status;
 
-enum { KVC_RULE_SINGLE = 0, KVC_RULE_CUMULATIVE = 1, KVC_RULE_EMA = 2 };
+enum { KVC_RULE_SINGLE = 0, KVC_RULE_CUMULATIVE = 1, KVC_RULE_EMA = 2, KVC_RULE_MI = 3 };
 enum { KVC_CORR_OFF = 0, KVC_CORR_ZERO_ORDER = 1, KVC_CORR_FIRST_ORDER = 2 };
 enum { KVC_ALLOC_GLOBAL = 0, KVC_ALLOC_LAYER = 1, KVC_ALLOC_HEAD = 2 };
 
@@ -87,7 +87,10 @@ typedef struct {
     int32_t d;               /* head dimension (128)                         */
     int32_t cap;             /* slot capacity per unit (row stride of K, V)  */
     int32_t L;               /* budget: slots kept per unit after a step     */
-    int32_t rule;            /* KVC_RULE_*  (InertiaKV sec 3.1 eqs 2-4)      */
+    int32_t rule;            /* KVC_RULE_*  (InertiaKV sec 3.1 eqs 2-4;
+                                KVC_RULE_MI: MomentKV's moment-informed
+                                score, every step, needs T = 1; see
+                                kvc_mi_scores)                               */
     float alpha;             /* EMA coefficient, 0 <= alpha < 1              */
     int32_t refresh_period;  /* 0 <= T <= L: utilities refresh on step
                                 t = 1 and whenever (t - 1) mod T == 0
@@ -271,6 +274,24 @@ KVC_API kvc_status kvc_correct(const kvc_params *p, const uint16_t *q,
                        float *logZ_R, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * kvc_mi_scores -- MomentKV moment-informed eviction scores.
+ *
+ * Defined by: MomentKV sec 4.2 ("moment residual", "moment-aware eviction
+ * score") and Algorithm 1, phase 1.  For every live slot i < len[u]:
+ *   r_i = v_i - mu_v - C (k_i - mu_k) / sqrt(d)   (the moments as they are:
+ *         all zero before the first eviction, so r_i = v_i),
+ *   scores[u][i] = probs[u][i] * ||r_i||_2,
+ * probs being the head-mean probabilities kvc_decode_attend wrote for this
+ * step (the slot's attention weight).  scores may alias probs.  With rule
+ * KVC_RULE_MI, kvc_aggregate_evict takes these scores as the utilities of
+ * every slot (refreshed every step) and evicts the lowest.  fp32 residuals
+ * (CUDA cores), fp64 scores.  max_len bounds len[u] (<= cap).
+ */
+KVC_API kvc_status kvc_mi_scores(const kvc_params *p, const kvc_cache *cache,
+                                 const kvc_moments *mom, int32_t max_len,
+                                 const double *probs, double *scores, void *stream);
+
+/*
  * kvc_zip_merge -- merge each unit's single victim into its most similar
  * slot instead of evicting it.
  *
@@ -326,7 +347,9 @@ KVC_API kvc_status kvc_compact(const kvc_params *p, const kvc_cache *cache,
  * kvc_decode_attend, kvc_aggregate_evict, kvc_moment_update, kvc_correct and
  * kvc_compact called in that order (same sets; outputs within fp32
  * rounding); with p->merge = 1, kvc_zip_merge runs between
- * kvc_aggregate_evict and kvc_moment_update (six calls, no fused kernel).
+ * kvc_aggregate_evict and kvc_moment_update; with rule KVC_RULE_MI,
+ * kvc_mi_scores runs between kvc_decode_attend and kvc_aggregate_evict (the
+ * call sequence; no fused kernel).
  *
  * In the steady state (max_len == L + 1: every unit enters with len = L and
  * evicts exactly one slot) one cluster kernel per step does everything: the

@@ -8,6 +8,7 @@
 
 #include "kvc_common.cuh"
 #include "kvc_internal.h"
+#include "kvc_mi.h"
 
 namespace kvc {
 
@@ -80,8 +81,10 @@ static kvc_status check_params(const kvc_params *p)
                   "cap = %d outside [1, %d]", p->cap, kMaxCap);
     KVC_CHECK_ARG(p->L >= 1 && p->L < p->cap, KVC_ERR_INVALID_ARG,
                   "L = %d must satisfy 1 <= L < cap = %d", p->L, p->cap);
-    KVC_CHECK_ARG(p->rule >= KVC_RULE_SINGLE && p->rule <= KVC_RULE_EMA, KVC_ERR_INVALID_ARG,
+    KVC_CHECK_ARG(p->rule >= KVC_RULE_SINGLE && p->rule <= KVC_RULE_MI, KVC_ERR_INVALID_ARG,
                   "rule = %d unknown", p->rule);
+    KVC_CHECK_ARG(p->rule != KVC_RULE_MI || p->refresh_period == 1, KVC_ERR_INVALID_ARG,
+                  "the moment-informed rule scores every step: refresh period must be 1");
     KVC_CHECK_ARG(p->rule != KVC_RULE_EMA || (p->alpha >= 0.f && p->alpha < 1.f),
                   KVC_ERR_INVALID_ARG, "alpha = %g outside [0, 1)", (double)p->alpha);
     KVC_CHECK_ARG(p->refresh_period >= 0 && p->refresh_period <= p->L, KVC_ERR_INVALID_ARG,
@@ -276,6 +279,20 @@ kvc_status kvc_compact(const kvc_params *p, const kvc_cache *cache, int32_t kmax
                        "kvc_compact launch");
 }
 
+kvc_status kvc_mi_scores(const kvc_params *p, const kvc_cache *cache, const kvc_moments *mom,
+                         int32_t max_len, const double *probs, double *scores, void *stream)
+{
+    KVC_TRY(check_params(p));
+    KVC_TRY(check_cache(cache));
+    KVC_TRY(check_moments(mom));
+    KVC_CHECK_ARG(probs && scores, KVC_ERR_INVALID_ARG, "probs and scores are required");
+    KVC_CHECK_ARG(max_len >= 1 && max_len <= p->cap, KVC_ERR_SHAPE,
+                  "max_len = %d must satisfy 1 <= max_len <= cap = %d", max_len, p->cap);
+    return cuda_status(launch_mi_scores(*p, *cache, *mom, max_len, probs, scores,
+                                        static_cast<cudaStream_t>(stream)),
+                       "kvc_mi_scores launch");
+}
+
 kvc_status kvc_zip_merge(const kvc_params *p, int32_t new_pos, const uint16_t *q,
                          const kvc_cache *cache, int32_t kmax, const int32_t *evict_idx,
                          int32_t *n_evict, int32_t *partner_pos, void *ws, size_t ws_bytes,
@@ -317,7 +334,7 @@ kvc_status kvc_decode_step(const kvc_params *p, int32_t t, int32_t new_pos, int3
     KVC_CHECK_ARG(!p->merge || cache->votes != nullptr, KVC_ERR_INVALID_ARG,
                   "merge mode needs cache votes (merged slots carry p_e + p_c)");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (max_len == p->L + 1) {
+    if (max_len == p->L + 1 && p->rule != KVC_RULE_MI) {
         cudaError_t e = launch_fused_step(*p, t, new_pos, q, k_new, v_new, *cache, *mom, o, probs,
                                           kmax, evict_idx, evict_pos, n_evict, w, st);
         if (e != cudaErrorNotSupported) {
@@ -337,6 +354,13 @@ kvc_status kvc_decode_step(const kvc_params *p, int32_t t, int32_t new_pos, int3
     KVC_TRY(cuda_status(launch_attend(*p, t, new_pos, max_len, q, k_new, v_new, *cache, w.lse,
                                       w.fall, refresh ? pr : nullptr, w, st),
                         "kvc_decode_step attend"));
+    if (p->rule == KVC_RULE_MI) {
+        // the scores take the probabilities' place as the aggregate's input
+        // (in the workspace; the caller's probs keep the probabilities)
+        KVC_TRY(cuda_status(launch_mi_scores(*p, *cache, *mom, max_len, pr, w.probs, st),
+                            "kvc_decode_step moment-informed scores"));
+        pr = w.probs;
+    }
     KVC_TRY(cuda_status(launch_aggregate(*p, t, pr, *cache, kmax, evict_idx, evict_pos, n_evict, w, st),
                         "kvc_decode_step aggregate"));
     if (p->merge) {

@@ -405,7 +405,7 @@ __global__ void __launch_bounds__(512) aggregate_kernel(AggArgs a)
             const double s = pr[i], m = util[i];
             double r;
             if (isinf(m)) r = s;                           // first observation
-            else if (a.rule == KVC_RULE_SINGLE) r = s;
+            else if (a.rule == KVC_RULE_SINGLE || a.rule == KVC_RULE_MI) r = s;   // MI: s is the score
             else if (a.rule == KVC_RULE_CUMULATIVE) r = m + s;
             else r = al * m + (1.0 - al) * s;
             util[i] = r;
@@ -467,7 +467,8 @@ cudaError_t launch_aggregate(const kvc_params &p, int t, const double *probs,
                              const DecodeWs &ws, cudaStream_t st)
 {
     AggArgs a{probs, c.util, c.pos, c.len, evict_idx, evict_pos, n_evict,
-              ws.status, ws.pend, p.cap, p.L, p.rule, is_refresh(t, p.refresh_period),
+              ws.status, ws.pend, p.cap, p.L, p.rule,
+              p.rule == KVC_RULE_MI || is_refresh(t, p.refresh_period),
               kmax, p.alpha};
     aggregate_kernel<<<p.U, 512, 0, st>>>(a);
     return cudaGetLastError();

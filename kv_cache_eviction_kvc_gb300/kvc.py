@@ -20,7 +20,7 @@ KVC_OK = 0
 STATUS_NAMES = {0: "KVC_OK", 1: "KVC_ERR_INVALID_ARG", 2: "KVC_ERR_SHAPE",
                 3: "KVC_ERR_CUDA", 4: "KVC_ERR_TIMEOUT", 5: "KVC_ERR_UNSUPPORTED",
                 6: "KVC_ERR_WORKSPACE"}
-RULE_SINGLE, RULE_CUMULATIVE, RULE_EMA = 0, 1, 2
+RULE_SINGLE, RULE_CUMULATIVE, RULE_EMA, RULE_MI = 0, 1, 2, 3
 CORR_OFF, CORR_ZERO_ORDER, CORR_FIRST_ORDER = 0, 1, 2
 ALLOC_GLOBAL, ALLOC_LAYER, ALLOC_HEAD = 0, 1, 2
 
@@ -28,7 +28,7 @@ EXPORTED = (
     "kvc_version", "kvc_last_error", "kvc_status_string",
     "kvc_decode_workspace_size", "kvc_decode_workspace_init", "kvc_get_device_status",
     "kvc_decode_attend", "kvc_aggregate_evict", "kvc_moment_update", "kvc_correct",
-    "kvc_compact", "kvc_zip_merge", "kvc_decode_step", "kvc_decode_attend_noalloc", "kvc_prefill_prepare",
+    "kvc_compact", "kvc_zip_merge", "kvc_mi_scores", "kvc_decode_step", "kvc_decode_attend_noalloc", "kvc_prefill_prepare",
     "kvc_prefill_workspace_size", "kvc_prefill_score",
 )
 
@@ -90,6 +90,7 @@ def load(build: bool = True):
         "kvc_correct": (I32, [PP, P, PC, I32, P, P, P, P, PM, P, P, P, P, SZ, P]),
         "kvc_compact": (I32, [PP, PC, I32, P, P, P, SZ, P]),
         "kvc_zip_merge": (I32, [PP, I32, P, PC, I32, P, P, P, P, SZ, P]),
+        "kvc_mi_scores": (I32, [PP, PC, PM, I32, P, P, P]),
         "kvc_decode_step": (I32, [PP, I32, I32, I32, P, P, P, PC, PM, P, P, I32, P, P, P, P, SZ, P]),
         "kvc_decode_attend_noalloc": (I32, [PP, I32, I32, I32, P, P, P, PC, P, P, P, P, P]),
         "kvc_prefill_prepare": (I32, [I32, I32, I32, I32, I32, P, P, P]),
@@ -233,6 +234,13 @@ def kvc_compact(p, cache: kvc_cache, kmax, evict_idx, n_evict, ws, stream=None):
         ctypes.byref(p), ctypes.byref(cache), int(kmax), _ptr(evict_idx, i32, "evict_idx"),
         _ptr(n_evict, i32, "n_evict"), _ptr(ws, torch.uint8, "ws"), ws.numel(),
         _stream(stream)))
+
+
+def kvc_mi_scores(p, cache: kvc_cache, mom: kvc_moments, max_len, probs, scores, stream=None):
+    f64 = torch.float64
+    _check(load().kvc_mi_scores(
+        ctypes.byref(p), ctypes.byref(cache), ctypes.byref(mom), int(max_len),
+        _ptr(probs, f64, "probs"), _ptr(scores, f64, "scores"), _stream(stream)))
 
 
 def kvc_zip_merge(p, new_pos, q, cache: kvc_cache, kmax, evict_idx, n_evict, partner_pos, ws,

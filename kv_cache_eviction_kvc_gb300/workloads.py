@@ -31,7 +31,7 @@ from dataclasses import dataclass, field, replace
 
 import torch
 
-RULE_SINGLE, RULE_CUMULATIVE, RULE_EMA = 0, 1, 2
+RULE_SINGLE, RULE_CUMULATIVE, RULE_EMA, RULE_MI = 0, 1, 2, 3
 CORR_OFF, CORR_ZERO_ORDER, CORR_FIRST_ORDER = 0, 1, 2
 
 # fixed per-tensor seed offsets
@@ -146,8 +146,13 @@ C2_SCORE_FREE = C2.with_(name="C2-qwen3-4b-score-free", T=0,
 C2_ZIP = C2.with_(name="C2-qwen3-4b-zip", merge_recent=32,
                   description=C2.description + ", KeepKV ZIP-merging (R = 32)")
 
+# MomentKV's moment-informed eviction (alpha ||r|| every step) on the same shape
+C2_MI = C2.with_(name="C2-qwen3-4b-mi", rule=RULE_MI, T=1,
+                 description=C2.description.replace("lazy refresh every 8 steps",
+                                                    "MomentKV moment-informed eviction every step"))
+
 DECODE_CONFIGS = {"C0": C0, "C1": C1, "C2": C2, "C4": C4,
-                  "C2-score-free": C2_SCORE_FREE, "C2-zip": C2_ZIP}
+                  "C2-score-free": C2_SCORE_FREE, "C2-zip": C2_ZIP, "C2-mi": C2_MI}
 PREFILL_CONFIGS = {"C3": C3}
 
 

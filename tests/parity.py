@@ -22,7 +22,12 @@ inputs step by step.  Each step compares:
   step is a mismatch; the merged key and value rows must be within one bf16
   unit of the oracle's unrounded k_r, v_r (either guard branch is accepted
   when the weighted mean logit is within 0.1 % of the guard threshold), and
-  the oracle then adopts the GPU's rows.
+  the oracle then adopts the GPU's rows;
+* under MomentKV's moment-informed rule, the step's scores alpha ||r|| (the
+  utilities of the retained slots, by position) within 2e-3 relative (floor:
+  1e-4 of the unit's largest score), and eviction near-ties within 1e-4 of
+  the threshold score (the GPU forms the residuals with fp32 sums of 128
+  products).
 """
 from __future__ import annotations
 
@@ -40,6 +45,8 @@ O_TOL = 2e-3
 MOM_TOL = 1e-4
 PROB_TOL = 2e-3   # head-mean probabilities are attention outputs
 COS_BAND = 1e-5   # partner near-tie band (key cosines, fp32 on the GPU)
+MI_TIE_REL = 1e-4     # near-tie band of moment-informed scores
+MI_SCORE_TOL = 2e-3
 ROW_REL = 2.0 ** -7   # one bf16 unit (8 significand bits)
 
 
@@ -57,12 +64,14 @@ class ParityReport:
     n_err: int = 0
     merges: int = 0
     max_row_err: float = 0.0      # merged rows, in bf16 units of the reference
+    max_mi_err: float = 0.0       # moment-informed scores (retained slots)
     first_mismatch: str = ""
 
     def ok(self):
         return (self.mismatches == 0 and self.max_o_err <= O_TOL and self.max_mu_err <= MOM_TOL
                 and self.max_C_err <= MOM_TOL and self.max_prob_err <= PROB_TOL
-                and self.n_err == 0 and self.max_lse_err <= O_TOL and self.max_fall_err <= O_TOL)
+                and self.n_err == 0 and self.max_lse_err <= O_TOL and self.max_fall_err <= O_TOL
+                and self.max_mi_err <= MI_SCORE_TOL)
 
 
 def _rel(a, b, floor=1e-3, absfloor=1e-6):
@@ -76,6 +85,8 @@ def run_decode_parity(cfg: W.DecodeConfig, *, steps: int | None = None, units=No
                       cap: int | None = None) -> ParityReport:
     S = cfg.steps if steps is None else steps
     merge = cfg.merge_recent is not None
+    mi = cfg.rule == W.RULE_MI
+    tie_rel = MI_TIE_REL if mi else TIE_REL
     U, G, d, N, L = cfg.U, cfg.G, cfg.d, cfg.N, cfg.L
     units = list(range(U)) if units is None else list(units)
     uidx = torch.tensor(units, device=device, dtype=torch.long)
@@ -147,7 +158,7 @@ def run_decode_parity(cfg: W.DecodeConfig, *, steps: int | None = None, units=No
                     if g != o_set:
                         umap = dict(zip(pos_o[j, : n_o[j]].tolist(), util_o[j, : n_o[j]].tolist()))
                         bad = [p for p in g ^ o_set
-                               if p not in umap or abs(umap[p] - thr[j]) > TIE_REL * abs(thr[j])]
+                               if p not in umap or abs(umap[p] - thr[j]) > tie_rel * abs(thr[j])]
                         if bad or len(g) != len(o_set):
                             rep.mismatches += 1
                             if not rep.first_mismatch:
@@ -191,6 +202,17 @@ def run_decode_parity(cfg: W.DecodeConfig, *, steps: int | None = None, units=No
                     ref = pr[j, : nb + 1]          # oracle slots are in position order
                     err = np.abs(gp[order] - ref) / np.maximum(ref, 1e-300)
                     rep.max_prob_err = max(rep.max_prob_err, float(err.max()))
+            if mi:
+                # the step's scores are the utilities of every retained slot
+                ng_, pg_, ug_ = (st.len[uidx].cpu().numpy(), st.pos[uidx].cpu().numpy(),
+                                 st.util[uidx].cpu().numpy())
+                no_, po_, _, uo_, _ = sess.slots()
+                for j in range(len(units)):
+                    ref = dict(zip(po_[j, : no_[j]].tolist(), uo_[j, : no_[j]].tolist()))
+                    floor = 1e-4 * max(ref.values()) if ref else 0.0
+                    for p_, g_ in zip(pg_[j, : ng_[j]].tolist(), ug_[j, : ng_[j]].tolist()):
+                        r_ = ref[p_]
+                        rep.max_mi_err = max(rep.max_mi_err, abs(g_ - r_) / max(abs(r_), floor, 1e-300))
             # moments
             n_g = st.n[uidx].cpu().numpy()
             mk_g = st.mu_k[uidx].cpu().numpy()

@@ -99,3 +99,17 @@ def test_zip_merge_c2_sampled_full_size(fused):
     check(rep)
     assert rep.merges >= 64 * 22
 
+
+
+@pytest.mark.parametrize("cfg", [
+    SMALL.with_(rule=W.RULE_MI),                                     # MomentKV moment-informed
+    SMALL.with_(rule=W.RULE_MI, Hq=2, Hkv=2, N=300, L=20, votes_max=4),   # G = 1, votes
+    SMALL.with_(rule=W.RULE_MI, k_dist="mixture", centres=8, correction=W.CORR_ZERO_ORDER),
+], ids=["mi", "mi-G1-votes", "mi-mixture"])
+@pytest.mark.parametrize("fused", [True, False])
+def test_moment_informed(cfg, fused):
+    check(run_decode_parity(cfg, fused=fused))
+
+
+def test_moment_informed_c2_sampled_full_size():
+    check(run_decode_parity(W.C2_MI, units=sample_units(W.C2.U), steps=6))
