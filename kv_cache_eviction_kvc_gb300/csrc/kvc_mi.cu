@@ -6,15 +6,18 @@
 // attend pass wrote).  While nothing has been evicted the moments are zero
 // and r_i = v_i.
 //
-// One CTA per 64 slots of a unit (256 threads).  C is staged in shared memory
-// as fp32 with a padded row stride (129 floats: the 16 lanes of a half-warp
-// read 16 rows of one column from 16 banks); the chunk's keys are staged
-// centred on mu_k.  Thread (ty, tx) forms C (k_j - mu_k) for 4 slots and 8
-// output dimensions (tx + 16 i), so every shared-memory load feeds 2.7 FMAs;
-// the values then take the keys' place in shared memory, and the residual
-// norm is reduced over the 16 lanes of the slot's half-warp.  CUDA-core
-// fp32: this is a 128 x 128 x L contraction per unit against a matrix that
-// changes at every eviction.
+// One CTA per kMiChunks chunks of 64 slots of a unit (256 threads; C is
+// staged once for all of them).  C is staged transposed in
+// shared memory (CsT[b][a], fp32) and the chunk's keys transposed and
+// centred on mu_k (XsT[b][j]); thread (ty, tx) forms C (k_j - mu_k) for the
+// 4 slots 4 ty .. 4 ty + 3 and the 8 output dimensions 4 tx .. 4 tx + 3 and
+// 64 + 4 tx .. 64 + 4 tx + 3, so that one step of the contraction takes three
+// 16-byte shared-memory loads (conflict-free: a half-warp reads 256
+// contiguous bytes of a CsT row, the two halves of a warp two 16-byte pieces
+// of an XsT row) for 32 FMAs.  The values then take the keys' place (also
+// transposed), and the residual norm is reduced over the 16 lanes of the
+// slot's half-warp.  CUDA-core fp32: a 128 x 128 x L contraction per unit
+// against a matrix that changes at every eviction.
 #include <cuda_runtime.h>
 
 #include "kvc_common.cuh"
@@ -24,10 +27,10 @@ namespace kvc {
 
 namespace {
 
-constexpr int kMiSlots = 64;              // slots per CTA
+constexpr int kMiSlots = 64;              // slots per chunk
+constexpr int kMiChunks = 8;              // chunks per CTA (C staged once)
 constexpr int kMiThreads = 256;
-constexpr int kMiLd = kD + 1;             // padded row stride (floats)
-constexpr size_t kMiSmem = (size_t)(kD + kMiSlots) * kMiLd * sizeof(float) + 2 * kD * sizeof(float);
+constexpr size_t kMiSmem = ((size_t)kD * kD + (size_t)kD * kMiSlots + 2 * kD) * sizeof(float);
 
 struct MiArgs {
     const uint16_t *K, *V;    // [U][cap][d]
@@ -40,14 +43,14 @@ struct MiArgs {
 
 __global__ void __launch_bounds__(kMiThreads, 2) mi_score_kernel(MiArgs a)
 {
-    extern __shared__ float sm[];
-    float *Cs = sm;                               // [kD][kMiLd]
-    float *Xs = Cs + kD * kMiLd;                  // [kMiSlots][kMiLd]: k - mu_k, then v
-    float *mk = Xs + kMiSlots * kMiLd;            // [kD]
+    extern __shared__ __align__(16) float sm[];
+    float *CsT = sm;                              // [kD (b)][kD (a)]
+    float *XsT = CsT + kD * kD;                   // [kD][kMiSlots]: k - mu_k, then v
+    float *mk = XsT + kD * kMiSlots;              // [kD]
     float *mv = mk + kD;                          // [kD]
-    const int u = blockIdx.y, j0 = blockIdx.x * kMiSlots;
+    const int u = blockIdx.y, jc0 = blockIdx.x * kMiSlots * kMiChunks;
     const int n = min(a.len[u], a.cap);
-    if (j0 >= n) return;
+    if (jc0 >= n) return;
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
     const size_t ubase = (size_t)u * a.cap;
     const float *Cu = a.C + (size_t)u * kD * kD;
@@ -55,21 +58,26 @@ __global__ void __launch_bounds__(kMiThreads, 2) mi_score_kernel(MiArgs a)
         mk[e] = a.mu_k[(size_t)u * kD + e];
         mv[e] = a.mu_v[(size_t)u * kD + e];
     }
+    // C transposed: lanes run along the row index a, so the stores into
+    // CsT[b][a] hit consecutive banks
     for (int e = tid; e < kD * kD / 4; e += kMiThreads) {
-        const float4 c4 = reinterpret_cast<const float4 *>(Cu)[e];
-        const int r = (4 * e) / kD, col = (4 * e) % kD;
-        float *dst = Cs + r * kMiLd + col;
-        dst[0] = c4.x; dst[1] = c4.y; dst[2] = c4.z; dst[3] = c4.w;
+        const int row = e % kD, b4 = (e / kD) * 4;
+        const float4 c4 = *reinterpret_cast<const float4 *>(Cu + (size_t)row * kD + b4);
+        CsT[(b4 + 0) * kD + row] = c4.x;
+        CsT[(b4 + 1) * kD + row] = c4.y;
+        CsT[(b4 + 2) * kD + row] = c4.z;
+        CsT[(b4 + 3) * kD + row] = c4.w;
     }
-    __syncthreads();
+    for (int j0 = jc0; j0 < min(n, jc0 + kMiSlots * kMiChunks); j0 += kMiSlots) {
+    __syncthreads();                              // C staged / the last chunk's values consumed
     const int nj = min(kMiSlots, n - j0);
-    // keys of the chunk, centred (8 bf16 per 16-byte load)
+    // keys of the chunk, centred and transposed (lanes run along the slot)
     for (int e = tid; e < kMiSlots * (kD / 8); e += kMiThreads) {
-        const int j = e / (kD / 8), c8 = (e % (kD / 8)) * 8;
+        const int j = e % kMiSlots, c8 = (e / kMiSlots) * 8;
         float f[8];
         if (j < nj) unpack8(ldg_nc_v4(a.K + (ubase + j0 + j) * kD + c8), f);
         else for (int t = 0; t < 8; t++) f[t] = mk[c8 + t];
-        for (int t = 0; t < 8; t++) Xs[j * kMiLd + c8 + t] = f[t] - mk[c8 + t];
+        for (int t = 0; t < 8; t++) XsT[(c8 + t) * kMiSlots + j] = f[t] - mk[c8 + t];
     }
     __syncthreads();
     float acc[4][8];
@@ -79,43 +87,50 @@ __global__ void __launch_bounds__(kMiThreads, 2) mi_score_kernel(MiArgs a)
         for (int i = 0; i < 8; i++) acc[jj][i] = 0.f;
 #pragma unroll 4
     for (int b = 0; b < kD; b++) {
-        float x[4], c[8];
-#pragma unroll
-        for (int jj = 0; jj < 4; jj++) x[jj] = Xs[(4 * ty + jj) * kMiLd + b];
-#pragma unroll
-        for (int i = 0; i < 8; i++) c[i] = Cs[(tx + 16 * i) * kMiLd + b];
+        const float4 x = *reinterpret_cast<const float4 *>(XsT + b * kMiSlots + 4 * ty);
+        const float4 c0 = *reinterpret_cast<const float4 *>(CsT + b * kD + 4 * tx);
+        const float4 c1 = *reinterpret_cast<const float4 *>(CsT + b * kD + 64 + 4 * tx);
+        const float xv[4] = {x.x, x.y, x.z, x.w};
+        const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
         for (int jj = 0; jj < 4; jj++)
 #pragma unroll
-            for (int i = 0; i < 8; i++) acc[jj][i] = fmaf(c[i], x[jj], acc[jj][i]);
+            for (int i = 0; i < 8; i++) acc[jj][i] = fmaf(cv[i], xv[jj], acc[jj][i]);
     }
     __syncthreads();                              // the keys are consumed
     for (int e = tid; e < kMiSlots * (kD / 8); e += kMiThreads) {
-        const int j = e / (kD / 8), c8 = (e % (kD / 8)) * 8;
+        const int j = e % kMiSlots, c8 = (e / kMiSlots) * 8;
         float f[8];
         if (j < nj) unpack8(ldg_nc_v4(a.V + (ubase + j0 + j) * kD + c8), f);
         else for (int t = 0; t < 8; t++) f[t] = 0.f;
-        for (int t = 0; t < 8; t++) Xs[j * kMiLd + c8 + t] = f[t];
+        for (int t = 0; t < 8; t++) XsT[(c8 + t) * kMiSlots + j] = f[t];
     }
     __syncthreads();
     const float rs = rsqrtf((float)kD);
+    float rr[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int jj = 0; jj < 4; jj++) {
-        const int j = 4 * ty + jj;
-        float rr = 0.f;
+    for (int i = 0; i < 8; i++) {
+        const int aa = (i < 4 ? 0 : 64) + 4 * tx + (i & 3);
+        const float4 v4 = *reinterpret_cast<const float4 *>(XsT + aa * kMiSlots + 4 * ty);
+        const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
-        for (int i = 0; i < 8; i++) {
-            const int aa = tx + 16 * i;
-            const float r = Xs[j * kMiLd + aa] - mv[aa] - acc[jj][i] * rs;
-            rr = fmaf(r, r, rr);
-        }
-#pragma unroll
-        for (int m = 8; m > 0; m >>= 1) rr += __shfl_xor_sync(kFull, rr, m);
-        if (tx == 0 && j < nj) {
-            const size_t i = ubase + j0 + j;
-            a.scores[i] = a.probs[i] * sqrt((double)rr);
+        for (int jj = 0; jj < 4; jj++) {
+            const float r = vv[jj] - mv[aa] - acc[jj][i] * rs;
+            rr[jj] = fmaf(r, r, rr[jj]);
         }
     }
+#pragma unroll
+    for (int jj = 0; jj < 4; jj++) {
+        float q = rr[jj];
+#pragma unroll
+        for (int m = 8; m > 0; m >>= 1) q += __shfl_xor_sync(kFull, q, m);
+        const int j = 4 * ty + jj;
+        if (tx == 0 && j < nj) {
+            const size_t i = ubase + j0 + j;
+            a.scores[i] = a.probs[i] * sqrt((double)q);
+        }
+    }
+    }                                             // chunks
 }
 
 }  // namespace
@@ -127,7 +142,8 @@ cudaError_t launch_mi_scores(const kvc_params &p, const kvc_cache &c, const kvc_
                                          (int)kMiSmem);
     if (e != cudaSuccess) return e;
     MiArgs a{c.K, c.V, c.len, m.mu_k, m.mu_v, m.C, probs, scores, p.cap};
-    const dim3 grid((unsigned)((max_len + kMiSlots - 1) / kMiSlots), (unsigned)p.U);
+    const int span = kMiSlots * kMiChunks;
+    const dim3 grid((unsigned)((max_len + span - 1) / span), (unsigned)p.U);
     mi_score_kernel<<<grid, kMiThreads, kMiSmem, st>>>(a);
     return cudaGetLastError();
 }
