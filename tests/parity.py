@@ -313,7 +313,7 @@ class PrefillReport:
 def run_prefill_parity(cfg: W.PrefillConfig, *, seed: int = 0, device="cuda",
                        normalize: bool = True, alloc: int = 0) -> PrefillReport:
     """alloc: 0 global top-K (LaProx), 1 per layer (head-flatten only),
-    2 uniform per KV head; near-ties are judged against the threshold of
+    2 uniform per KV head; near-ties are measured against the threshold of
     the element's own segment."""
     from kv_cache_eviction_kvc_gb300 import kvc as K
     NL, Hq, Hkv, d, N, w, B = cfg.NL, cfg.Hq, cfg.Hkv, cfg.d, cfg.N, cfg.w, cfg.B_total
