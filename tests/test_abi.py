@@ -79,3 +79,43 @@ def test_binding_refuses_host_tensors():
     p = K.make_params(U=1, G=4, cap=8, L=4)
     with pytest.raises(ValueError):
         K.kvc_decode_workspace_init(p, torch.zeros(16, dtype=torch.uint8))
+
+
+@pytest.mark.parametrize("field,value", [
+    ("merge", 2), ("merge_recent", -1), ("rule", 4)])
+def test_bad_extension_params_rejected_on_host(field, value):
+    """ZIP-merging and moment-informed parameters are validated before any
+    launch."""
+    p = K.make_params(U=2, G=4, cap=100, L=10)
+    setattr(p, field, value)
+    assert _lib_call_attend(p) == 1
+    assert K.kvc_last_error() != ""
+
+
+def test_moment_informed_rule_needs_refresh_every_step():
+    # (every call in this file is refused before a launch: the pointers are fake)
+    p = K.make_params(U=2, G=4, cap=100, L=10, rule=K.RULE_MI, refresh_period=4)
+    assert _lib_call_attend(p) == 1
+    assert "refresh period" in K.kvc_last_error()
+
+
+def test_zip_merge_needs_votes():
+    """Merged slots carry p_e + p_c: kvc_zip_merge refuses a cache without
+    votes (host check, no launch)."""
+    lib = K.load()
+    p = K.make_params(U=2, G=4, cap=100, L=10, merge_recent=4)
+    cache = K.kvc_cache(16, 32, None, 64, 128, 256)
+    rc = lib.kvc_zip_merge(ctypes.byref(p), 5, 16, ctypes.byref(cache), 1, 16, 16, None,
+                           256, 1 << 40, None)
+    assert rc == 1 and "votes" in K.kvc_last_error()
+
+
+def test_prefill_allocation_arguments_checked_on_host():
+    """An unknown allocation, or a budget that does not divide into the
+    allocation's segments, is refused before any pointer is touched."""
+    lib = K.load()
+    args = [None] * 10
+    rc = lib.kvc_prefill_score(2, 8, 2, 128, 64, 8, 12, 1, 5, *args[:8], None, 0, None)
+    assert rc == 1 and "alloc" in K.kvc_last_error()
+    rc = lib.kvc_prefill_score(2, 8, 2, 128, 64, 8, 6, 1, K.ALLOC_HEAD, *args[:8], None, 0, None)
+    assert rc == 1 and "multiple" in K.kvc_last_error()
