@@ -297,6 +297,23 @@ void ocl_mi_scores(void *h, const double *probs, double *out)
     }
 }
 
+/*
+ * Set the utilities of unit u's first n slots and mark them scored (a
+ * utility carried over from the prefill, e.g. KeepKV's windowed EMA
+ * initialization).  Returns 0, or -1 if n exceeds the slots present.
+ */
+int ocl_set_util(void *h, int u, int n, const double *util)
+{
+    ocl_session *s = (ocl_session *)h;
+    if (u < 0 || u >= s->U || n < 0 || n > s->n[u]) return -1;
+    size_t base = (size_t)u * s->cap;
+    for (int i = 0; i < n; i++) {
+        s->util[base + i] = util[i];
+        s->scored[base + i] = 1;
+    }
+    return 0;
+}
+
 /* Export the slot table (positions, votes, utilities, scored flags). */
 void ocl_get_slots(void *h, int32_t *n, int32_t *pos, int32_t *vote,
                    double *util, uint8_t *scored)
@@ -776,6 +793,51 @@ void ocl_prefill_colnorm(int NL, int Hq, int Hkv, int d, int N, int w,
                 cg[i] = sqrt(ss);
             }
             free(Abar);
+            free(x);
+        }
+}
+
+/*
+ * KeepKV's windowed EMA initialization of the utilities [KeepKV reading
+ * notes, eq 15 at the end of the prefill: S = sum over the last window of
+ * queries of (1 - alpha) alpha^(age) s^k]: with the same causal window
+ * attention as above (query j of w at position N - w + j, A_bar the group
+ * mean of the head probabilities),
+ *   S_i = sum_{j=0}^{w-1} (1 - alpha) alpha^(w-1-j) A_bar[j, i],
+ * the last window query weighing (1 - alpha).  q_win: [NL][Hq][w][d];
+ * K: [NL][Hkv][N][d]; S: [NL][Hkv][N].
+ */
+void ocl_prefill_ema_init(int NL, int Hq, int Hkv, int d, int N, int w, double alpha,
+                          const uint16_t *q_win, const uint16_t *K, double *S)
+{
+    int G = Hq / Hkv;
+    double rsd = 1.0 / sqrt((double)d);
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int l = 0; l < NL; l++)
+        for (int g = 0; g < Hkv; g++) {
+            const uint16_t *Kg = &K[((size_t)l * Hkv + g) * N * d];
+            double *Sg = &S[((size_t)l * Hkv + g) * N];
+            double *x = (double *)malloc((size_t)N * sizeof(double));
+            for (int i = 0; i < N; i++) Sg[i] = 0.0;
+            for (int j = 0; j < w; j++) {
+                double wj = (1.0 - alpha) * pow(alpha, (double)(w - 1 - j));
+                int last = N - w + j;
+                for (int hh = g * G; hh < (g + 1) * G; hh++) {
+                    const uint16_t *qj = &q_win[(((size_t)l * Hq + hh) * w + j) * d];
+                    double mx = -INFINITY;
+                    for (int i = 0; i <= last; i++) {
+                        double dot = 0.0;
+                        for (int a = 0; a < d; a++)
+                            dot += bfd(qj[a]) * bfd(Kg[(size_t)i * d + a]);
+                        x[i] = dot * rsd;
+                        if (x[i] > mx) mx = x[i];
+                    }
+                    double z = 0.0;
+                    for (int i = 0; i <= last; i++) z += exp(x[i] - mx);
+                    for (int i = 0; i <= last; i++)
+                        Sg[i] += wj * exp(x[i] - mx) / z / (double)G;
+                }
+            }
             free(x);
         }
 }

@@ -76,6 +76,8 @@ def _load():
             "ocl_get_rows": (None, [P, P, P]),
             "ocl_moments": (None, [P, P, P, P, P]),
             "ocl_mi_scores": (None, [P, P, P]),
+            "ocl_set_util": (I, [P, I, I, P]),
+            "ocl_prefill_ema_init": (None, [I, I, I, I, I, I, D, P, P, P]),
             "ocl_output": (None, [P, P, I, P, P, P]),
             "ocl_prefill_gram": (None, [I, I, I, I, I, P, P]),
             "ocl_prefill_colnorm": (None, [I, I, I, I, I, I, P, P, P]),
@@ -238,6 +240,12 @@ class DecodeSession:
         v = np.zeros((self.U, self.cap, self.d), np.uint16)
         self.lib.ocl_get_rows(self.h, _p(k), _p(v))
         return k, v
+
+    def set_util(self, u: int, util):
+        """Utilities of unit u's first len(util) slots (marked scored)."""
+        util = np.ascontiguousarray(util, dtype=np.float64)
+        if self.lib.ocl_set_util(self.h, int(u), int(util.shape[0]), _p(util)) != 0:
+            raise ValueError("ocl_set_util: more utilities than slots")
 
     def mi_scores(self, probs):
         """MomentKV moment-informed scores alpha_i ||r_i|| [U][cap] from the
@@ -447,6 +455,16 @@ def prefill_select(c, r, B_total: int, normalize: bool = True, alloc: int = ALLO
         raise ValueError("B_total out of range or not a multiple of the segments")
     return dict(s=s, keep=keep, counts=counts, idx=idx[:int(B_total)],
                 thr=float(thr[0]) if alloc == ALLOC_GLOBAL else thr)
+
+
+def prefill_ema_init(q_win, K, NL: int, Hq: int, Hkv: int, d: int, N: int, w: int,
+                     alpha: float) -> np.ndarray:
+    """KeepKV windowed EMA initialization of the utilities, S [NL][Hkv][N]
+    (see ocl_prefill_ema_init)."""
+    qb, kb = _bits(q_win), _bits(K)
+    S = np.zeros((NL, Hkv, N))
+    _load().ocl_prefill_ema_init(NL, Hq, Hkv, d, N, w, float(alpha), _p(qb), _p(kb), _p(S))
+    return S
 
 
 def prefill_score(q_win, K, V, W_O, *, NL: int, Hq: int, Hkv: int, d: int,

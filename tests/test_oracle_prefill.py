@@ -187,3 +187,63 @@ def test_segment_budget_must_divide():
     c, r = np.ones((2, 2, 5)), np.ones((2, 2, 5))
     with pytest.raises(ValueError):
         O.prefill_select(c, r, 7, alloc=O.ALLOC_HEAD)
+
+
+# ---------------------------------------------------------------- KeepKV windowed EMA init
+
+def _window_case(seed, NL=1, Hq=4, Hkv=2, N=20, w=5, d=8, zero_q=False):
+    rng = np.random.default_rng(seed)
+    q = np.zeros((NL, Hq, w, d)) if zero_q else O.bf16_round(rng.normal(size=(NL, Hq, w, d)))
+    K = O.bf16_round(rng.normal(size=(NL, Hkv, N, d)))
+    return q, K
+
+
+@pytest.mark.parametrize("alpha", [0.0, 0.5, 0.9])
+def test_ema_init_mass_is_one_minus_alpha_to_the_w(alpha):
+    """Every window row is a probability distribution, so the initialized
+    utilities of a (layer, KV head) sum to sum_j (1 - a) a^(w-1-j) =
+    1 - a^w (the bias KeepKV's eq 14 corrects)."""
+    q, K = _window_case(31)
+    S = O.prefill_ema_init(q, K, 1, 4, 2, 8, 20, 5, alpha)
+    np.testing.assert_allclose(S.sum(axis=2), 1.0 - alpha ** 5, rtol=1e-13)
+
+
+def test_ema_init_alpha_zero_is_the_last_query():
+    """alpha = 0 keeps only the last window query's group-mean attention
+    (scipy softmax, causal: it sees every key)."""
+    from scipy.special import softmax
+    q, K = _window_case(32)
+    S = O.prefill_ema_init(q, K, 1, 4, 2, 8, 20, 5, 0.0)
+    for g in range(2):
+        x = np.stack([K[0, g] @ q[0, h, -1] / math.sqrt(8) for h in (2 * g, 2 * g + 1)])
+        np.testing.assert_allclose(S[0, g], softmax(x, axis=1).mean(axis=0), rtol=1e-12)
+
+
+def test_ema_init_zero_query_closed_form():
+    """q = 0: window query j attends uniformly to its N - w + j + 1 visible
+    keys, so S_i = sum over the queries that see i of (1 - a) a^(w-1-j) /
+    (N - w + j + 1)."""
+    N, w, a = 20, 5, 0.7
+    q, K = _window_case(33, zero_q=True)
+    S = O.prefill_ema_init(q, K, 1, 4, 2, 8, N, w, a)
+    want = np.array([sum((1 - a) * a ** (w - 1 - j) / (N - w + j + 1)
+                         for j in range(w) if i <= N - w + j) for i in range(N)])
+    np.testing.assert_allclose(S[0, 0], want, rtol=1e-13)
+    np.testing.assert_allclose(S[0, 1], want, rtol=1e-13)
+
+
+def test_initialized_utilities_continue_the_ema_at_step_one():
+    """A slot carrying an initialized utility is scored: the first decode
+    step applies m = a m0 + (1 - a) s instead of m = s."""
+    rng = np.random.default_rng(34)
+    k, v = O.bf16_round(rng.normal(size=(6, 8))), O.bf16_round(rng.normal(size=(6, 8)))
+    s = O.DecodeSession(1, 1, 8, 8)
+    s.load(0, k, v)
+    m0 = rng.random(6)
+    s.set_util(0, m0)
+    probs = np.zeros((1, 8)); probs[0, :6] = rng.random(6)
+    s.update_util(probs, O.RULE_EMA, 0.9)
+    _, _, _, util, scored = s.slots()
+    np.testing.assert_allclose(util[0, :6], 0.9 * m0 + 0.1 * probs[0, :6], rtol=1e-15)
+    assert scored[0, :6].all()
+    s.close()
