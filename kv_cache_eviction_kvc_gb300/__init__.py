@@ -2,6 +2,7 @@
 
 The compute lives in libkvc (``csrc/``, C ABI in ``include/kvc.h``); ``kvc``
 is its thin ctypes binding, ``state`` allocates device memory for a decode
-stream and ``workloads`` draws the seeded synthetic inputs.
+stream, ``workloads`` draws the seeded synthetic inputs and ``dist`` holds
+the multi-process plumbing (the layer-sharded prefill exchange).
 """
-__all__ = ["kvc", "state", "workloads"]
+__all__ = ["kvc", "state", "workloads", "dist"]
