@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--prefill-layers", type=int, default=None,
                     help="override the layer count of the prefill-scoring workload")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the secondary decode workloads (long context, Llama-3.1-8B, tiny)")
     return ap.parse_args()
 
 
@@ -198,32 +200,27 @@ def run_prefill(pc, dev, reps=5):
             "allocations_ms_per_call": alloc_ms}
 
 
-KERNEL_SOURCES = ["kv_cache_eviction_kvc_gb300/csrc/kvc_fused.cu",
-                  "kv_cache_eviction_kvc_gb300/csrc/kvc_tma.cuh",
-                  "kv_cache_eviction_kvc_gb300/csrc/kvc_common.cuh",
-                  "kv_cache_eviction_kvc_gb300/csrc/kvc_internal.h"]
-
-
-def profiled_traffic():
-    """DRAM bytes per lazy-step launch of the fused kernel on this workload
-    from the committed ncu summary, or None when the kernel sources changed
-    since the counters were taken."""
+def profiled_traffic(kernel: str):
+    """DRAM bytes (read + write) per launch of ``kernel`` on the full workload,
+    from the ncu capture recorded in profiles/traffic.json, or None when the
+    kernel's sources changed since the counters were taken (the record holds
+    a hash of those sources)."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "fused_step_kernel_qwen3-4b.md")
+    path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
-    h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
-    want, traffic = None, None
     with open(path) as fh:
-        for line in fh:
-            if line.startswith("source_sha256_16:"):
-                want = line.split(":", 1)[1].strip()
-            elif line.startswith("traffic_bytes_per_launch_full:"):
-                traffic = int(line.split(":", 1)[1].strip())
-    return traffic if want == h.hexdigest()[:16] else None
+        rec = json.load(fh).get(kernel)
+    if not rec:
+        return None
+    h = hashlib.sha256()
+    for f in rec["sources"]:
+        fp = os.path.join(ROOT, f)
+        if not os.path.exists(fp):
+            return None
+        with open(fp, "rb") as fh:
+            h.update(fh.read())
+    return int(rec["traffic_bytes_per_launch"]) if h.hexdigest()[:16] == rec["sha256_16"] else None
 
 
 # ------------------------------------------------------------ clocks
@@ -321,11 +318,20 @@ def oracle_sample(cfg, seconds: float, max_steps: int | None = None):
 
 
 # ------------------------------------------------------------ GPU arm
-def run_ours(args, cfg, rank, world):
+def is_refresh(t, T):
+    """Refresh steps: t = 1 and every T-th step after it; T = 0: step 1 only."""
+    return t == 1 if T == 0 else (T == 1 or (t - 1) % T == 0)
+
+
+def run_ours(args, cfg, rank, world, steps=None, warmup=None, e2e=True, sample_clocks=True):
+    """Step 1, then W warm-up and K timed steady-state steps of kvc_decode_step
+    over every unit of ``cfg``; returns the JSON record."""
     import torch
     from kv_cache_eviction_kvc_gb300 import kvc, workloads as W
     from kv_cache_eviction_kvc_gb300.state import DecodeState
 
+    steps = args.steps if steps is None else steps
+    warmup = args.warmup if warmup is None else warmup
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     kvc.load()
@@ -333,66 +339,75 @@ def run_ours(args, cfg, rank, world):
     U, G, N, L = cfg.U, cfg.G, cfg.N, cfg.L
     P = W.unit_params(cfg, dev, seed)
     merge = cfg.merge_recent is not None
+    mi = cfg.rule == W.RULE_MI
     st = DecodeState(U, G, N + 1, L, rule=cfg.rule, alpha=cfg.alpha, refresh_period=cfg.T,
                      correction=cfg.correction, votes=bool(cfg.votes_max) or merge,
                      kmax=N + 1 - L, device=dev, merge_recent=cfg.merge_recent)
-    pre = W.gen_prefill(cfg, dev, seed, cap=N + 1, P=P)
+    # the prefill is drawn straight into the state's K / V (no second copy)
+    pre = W.gen_prefill(cfg, dev, seed, cap=N + 1, P=P, out_K=st.K, out_V=st.V)
     st.load_prefill(pre["K"], pre["V"], pre["votes"], pre["pos"], pre["len"])
     del pre
     torch.cuda.empty_cache()
     stream = torch.cuda.current_stream(dev)
 
-    # step 1: the one-off pass over N + 1 slots (general five-kernel path)
+    # step 1: the one-off pass over N + 1 slots (general path).  Under the
+    # moment-informed rule the prompt is first compressed by the attention
+    # rule, as MomentKV's setup compresses it with the SnapKV protocol before
+    # decoding; every token this removes is folded into the moments.
     inp = W.gen_step(cfg, dev, 1, seed, P)
+    if mi:
+        st.params.rule = W.RULE_EMA
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     st.step(1, N, inp["q"], inp["k_new"], inp["v_new"], max_len=N + 1)
     e1.record(stream)
     torch.cuda.synchronize()
     step1_ms = e0.elapsed_time(e1)
+    st.params.rule = cfg.rule
     assert st.device_status() == 0
     st.set_kmax(1)
 
-    total = args.warmup + args.steps
+    total = warmup + steps
     inputs = [W.gen_step(cfg, dev, 2 + i, seed, P) for i in range(total)]
     torch.cuda.synchronize()
     launches = 0
+    per_step_launches = 7 if mi else (2 if merge else 1)
 
-    def do_step(i, events=None):
+    def do_step(t, x, events=None, o=None):
         nonlocal launches
-        t = 2 + i
-        x = inputs[i]
         if events is not None:
             events[0].record(stream)
-        st.step(t, N + t - 1, x["q"], x["k_new"], x["v_new"], max_len=L + 1)
+        st.step(t, N + t - 1, x["q"], x["k_new"], x["v_new"], max_len=L + 1, o=o)
         if events is not None:
             events[1].record(stream)
         # merge mode: fused step + merge kernel; the moment-informed rule runs
         # the call sequence (attend split + final, scores, aggregate, fold,
         # correction, compaction)
-        launches += 7 if cfg.rule == W.RULE_MI else (2 if merge else 1)
+        launches += per_step_launches
 
-    for i in range(args.warmup):
-        do_step(i)
+    for i in range(warmup):
+        do_step(2 + i, inputs[i])
     torch.cuda.synchronize()
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
-    sampler = ClockSampler(dev.index if dev.index is not None else 0)
-    sampler.start()
-    time.sleep(0.3)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0) if sample_clocks else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+          for _ in range(steps)]
     launches = 0
     torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
-    for k in range(args.steps):
-        do_step(args.warmup + k, ev[k])
+    for k in range(steps):
+        do_step(2 + warmup + k, inputs[warmup + k], ev[k])
     t_end.record(stream)
     torch.cuda.synchronize()
-    clocks = sampler.stop()
+    clocks = sampler.stop() if sampler else None
+    timed_launches = launches
     total_ms = t_start.elapsed_time(t_end)
     per_launch = [a.elapsed_time(b) for a, b in ev]
     if world > 1:
@@ -401,24 +416,48 @@ def run_ours(args, cfg, rank, world):
     assert st.device_status() == 0
 
     # algorithmic bytes of the timed launches (refresh pattern of steps 2 + i)
-    def is_refresh(t, T):      # t = 1 and every T-th step after; T = 0: step 1 only
-        return t == 1 if T == 0 else (T == 1 or (t - 1) % T == 0)
-    steps_t = [2 + args.warmup + k for k in range(args.steps)]
-    bytes_list = [step_bytes(cfg, is_refresh(t, cfg.T), True) for t in steps_t]
+    steps_t = [2 + warmup + k for k in range(steps)]
+    ref_flags = [is_refresh(t, cfg.T) for t in steps_t]
+    bytes_list = [step_bytes(cfg, r, True) for r in ref_flags]
     avg_bytes = sum(bytes_list) / len(bytes_list)
     avg_launch_ms = sum(per_launch) / len(per_launch)
     achieved = avg_bytes / (avg_launch_ms * 1e-3) / 1e9
+    lazy = [ms for ms, r in zip(per_launch, ref_flags) if not r]
+    refr = [ms for ms, r in zip(per_launch, ref_flags) if r]
+    lazy_ms = statistics.median(lazy) if lazy else None
+    refresh_ms = statistics.median(refr) if refr else None
+    # steady state weighted by the refresh period: one refresh step in T
+    if cfg.T >= 2 and lazy_ms is not None and refresh_ms is not None:
+        steady_ms = (refresh_ms + (cfg.T - 1) * lazy_ms) / cfg.T
+        steady_bytes = (step_bytes(cfg, True, True) + (cfg.T - 1) * step_bytes(cfg, False, True)) / cfg.T
+    else:
+        steady_ms = lazy_ms if (cfg.T == 0 and lazy_ms is not None) else statistics.median(per_launch)
+        steady_bytes = step_bytes(cfg, cfg.T == 1, True)
 
     # end to end through host buffers: every step copies its inputs from
     # pinned host memory and its output o back.  Two copy streams (one per
     # direction) and double-buffered device inputs / outputs let the copies of
     # step k + 1 / k - 1 overlap the compute of step k, as a serving loop would.
-    e2e = None
-    if not args.no_e2e:
-        nE = min(args.steps, 100)
+    # The window has as many steps as the timed one and starts at the same
+    # step index modulo T, so both hold the same mix of refresh and lazy steps.
+    e2e_rec = None
+    if e2e:
+        nE = steps
+        t_next = 2 + total
+        t0 = 2 + warmup
+        if cfg.T >= 2:
+            pad = (t0 - t_next) % cfg.T
+        else:
+            pad = 0
+        extra = [W.gen_step(cfg, dev, t_next + i, seed, P) for i in range(pad)]
+        for i in range(pad):                       # untimed: align the refresh phase
+            do_step(t_next + i, extra[i])
+        base_t = t_next + pad
         names = ("q", "k_new", "v_new")
-        host_in = [{k: inputs[args.warmup + j][k].cpu().pin_memory() for k in names}
-                   for j in range(nE)]
+        host_in = []
+        for j in range(nE):
+            x = W.gen_step(cfg, dev, base_t + j, seed, P)
+            host_in.append({k: x[k].cpu().pin_memory() for k in names})
         din = [{k: torch.empty_like(inputs[0][k]) for k in names} for _ in range(2)]
         dout = [torch.empty_like(st.o) for _ in range(2)]
         o_host = [torch.empty(st.o.shape, dtype=st.o.dtype).pin_memory() for _ in range(2)]
@@ -426,7 +465,6 @@ def run_ours(args, cfg, rank, world):
         ev_in = [torch.cuda.Event() for _ in range(nE)]
         ev_done = [torch.cuda.Event() for _ in range(nE)]
         ev_out = [torch.cuda.Event() for _ in range(nE)]
-        base_t = 2 + total
         torch.cuda.synchronize()
 
         def h2d(j):
@@ -448,9 +486,7 @@ def run_ours(args, cfg, rank, world):
             stream.wait_event(ev_in[j])
             if j >= 2:
                 stream.wait_event(ev_out[j - 2])           # o buffer read back
-            t = base_t + j
-            x = din[j % 2]
-            st.step(t, N + t - 1, x["q"], x["k_new"], x["v_new"], max_len=L + 1, o=dout[j % 2])
+            do_step(base_t + j, din[j % 2], o=dout[j % 2])
             ev_done[j].record(stream)
             with torch.cuda.stream(ds):
                 ds.wait_event(ev_done[j])
@@ -461,27 +497,39 @@ def run_ours(args, cfg, rank, world):
         b.record(stream)
         torch.cuda.synchronize()
         e2e_ms = a.elapsed_time(b) / nE
+        if world > 1:
+            from kv_cache_eviction_kvc_gb300.dist import max_over_ranks
+            e2e_ms = max_over_ranks(e2e_ms, dev)
         bi = sum(v.numel() * v.element_size() for v in host_in[0].values())
         bo = o_host[0].numel() * o_host[0].element_size()
-        e2e = {"value": world * 1000.0 / e2e_ms, "unit": UNIT, "h2d_bytes_per_step": bi,
-               "d2h_bytes_per_step": bo, "steps": nE,
-               "note": "inputs H2D from pinned memory and o D2H every step, on two copy "
-                       "streams overlapping the compute stream"}
+        e2e_rec = {"value": world * 1000.0 / e2e_ms, "unit": UNIT, "h2d_bytes_per_step": bi,
+                   "d2h_bytes_per_step": bo, "steps": nE,
+                   "first_step": base_t,
+                   "note": "inputs H2D from pinned memory and o D2H every step, on two copy "
+                           "streams overlapping the compute stream; same step count and "
+                           "refresh phase as the timed window"}
         assert st.device_status() == 0
 
     peak, peak_kind = peaks()
-    ms_per_step = total_ms / args.steps
+    ms_per_step = total_ms / steps
+    kname = ("fused_step_kernel + zip_merge_kernel (kvc_decode_step, merge mode)"
+             if merge else "fused_step_kernel (kvc_decode_step, steady state)")
+    traffic = None
+    if (not merge and not mi and args.batch is None and args.prefill is None
+            and cfg.T >= 1 and args.config == "C2" and cfg.name == W.C2.name):
+        tr_lazy = profiled_traffic("fused_step_kernel_qwen3-4b_lazy")
+        tr_ref = profiled_traffic("fused_step_kernel_qwen3-4b_refresh")
+        if tr_lazy is not None and tr_ref is not None:
+            nr = sum(ref_flags)
+            traffic = (nr * tr_ref + (steps - nr) * tr_lazy) / steps
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak,
-                "traffic": (profiled_traffic() if (args.batch is None and args.prefill is None
-                                                   and args.config == "C2") else None),
-                "traffic_note": "ncu dram read+write per lazy-step launch, 864-unit capture "
-                                "scaled by units (profiles/fused_step_kernel_qwen3-4b.md)",
-                "peak_kind": peak_kind,
-                "kernel": ("fused_step_kernel + zip_merge_kernel (kvc_decode_step, merge mode)"
-                           if merge else "fused_step_kernel (kvc_decode_step, steady state)"),
+                "frac": achieved / peak, "traffic": traffic,
+                "traffic_note": "ncu dram read+write per launch (profiles/traffic.json), "
+                                "averaged over the window's refresh / lazy mix; null when "
+                                "the kernel changed since the capture",
+                "peak_kind": peak_kind, "kernel": kname,
                 "bytes_per_launch": avg_bytes, "avg_launch_ms": avg_launch_ms}
-    if cfg.rule == W.RULE_MI:
+    if mi:
         # the moment-informed scores are a CUDA-core fp32 contraction: the
         # step is bounded by fp32 FMA throughput, not by HBM
         tf = mi_flops(cfg) / (avg_launch_ms * 1e-3) / 1e12
@@ -494,10 +542,10 @@ def run_ours(args, cfg, rank, world):
                               "correction and compaction",
                     "flops_per_step": mi_flops(cfg), "avg_launch_ms": avg_launch_ms,
                     "hbm_gbs_of_step": achieved}
-    value = world * args.steps / (total_ms * 1e-3)
+    value = world * steps / (total_ms * 1e-3)
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "steps": steps, "warmup": warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16 K/V/q, fp32 accumulate and moments, fp64 utilities",
         "data": "synthetic (seeded K/V 64-centre mixtures; no model weights)",
@@ -505,16 +553,37 @@ def run_ours(args, cfg, rank, world):
                    "budget_L": L, "prefill_N": N, "refresh_period": cfg.T,
                    "merge_recent": cfg.merge_recent,
                    "alpha": cfg.alpha, "parallelism": f"replicas x{world} (independent units)",
-                   "l2": "inputs larger than L2: %.2f GB of HBM traffic per step" % (avg_bytes / 1e9)},
+                   "l2": "inputs larger than L2: %.2f GB of HBM traffic per step" % (avg_bytes / 1e9)
+                         if avg_bytes > 129e6 else
+                         "working set %.1f MB fits L2: launch-bound, no flush" % (avg_bytes / 1e6)},
         "achieved_gbs": achieved,
         "hbm_frac": achieved / peak,
         "step1_ms": step1_ms,
+        "lazy_ms": lazy_ms,
+        "refresh_ms": refresh_ms,
+        "refresh_steps_in_window": sum(ref_flags),
+        "steady_state": {"ms_per_step": steady_ms, "steps_per_s": world * 1000.0 / steady_ms,
+                         "hbm_frac": steady_bytes / (steady_ms * 1e-3) / 1e9 / peak,
+                         "note": "one refresh step in T (median refresh and lazy launch times)"},
         "roofline": roofline,
         "clocks": clocks,
-        "gpu_launches": launches,
-        "e2e": e2e,
+        "gpu_launches": timed_launches,
+        "e2e": e2e_rec,
     }
+    del st, inputs
+    torch.cuda.empty_cache()
     return res
+
+
+def summary(rec):
+    """The figures of a secondary workload's line."""
+    keys = ("value", "unit", "ms_per_step", "step1_ms", "lazy_ms", "refresh_ms",
+            "achieved_gbs", "hbm_frac", "steady_state", "gpu_launches")
+    out = {k: rec[k] for k in keys if k in rec}
+    out["config"] = rec["config"]
+    out["roofline_frac"] = rec["roofline"]["frac"]
+    out["clocks"] = rec["clocks"]
+    return out
 
 
 def main():
@@ -565,6 +634,17 @@ def main():
         import torch
         torch.cuda.empty_cache()
         res["prefill"] = run_prefill(W.C3, torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0))))
+    if not args.no_extra and args.batch is None and args.prefill is None and args.config == "C2":
+        # the other decode workloads at 1 GPU (every rank runs its replica)
+        res["other_workloads"] = {}
+        for name in ("C4", "C1", "C0"):
+            try:
+                rec = run_ours(args, W.DECODE_CONFIGS[name], rank, world,
+                               steps=max(args.steps, 20), warmup=max(args.warmup, 3),
+                               e2e=False, sample_clocks=(name == "C4"))
+                res["other_workloads"][name] = summary(rec)
+            except Exception as exc:      # a secondary line never sinks the main one
+                res["other_workloads"][name] = {"error": f"{type(exc).__name__}: {exc}"}
     if rank == 0:
         if not args.no_cpu_baseline:
             rate, cores, sample, _ = oracle_sample(cfg, args.cpu_seconds)

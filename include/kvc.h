@@ -377,21 +377,29 @@ KVC_API kvc_status kvc_decode_step(const kvc_params *p, int32_t t, int32_t new_p
  * runtime that reserves its memory pool at start-up and allows no cudaMalloc
  * afterwards, a plugin interface that passes tensors but no workspace).
  *
- * Same arguments, arithmetic and outputs as kvc_decode_attend, without the
- * workspace: the scratch (status word, logits, split partials, lengths) lives
- * in a static device array of 32 MiB inside the library, which every GPU that
- * loads the library holds until the process exits.  The call allocates
- * nothing (no cudaMalloc, cudaFree or allocating library routine).
- * - Sizes whose scratch exceeds 32 MiB (about U*G*cap*4 + U*ceil(cap/512)*
- *   G*520 bytes) are rejected with KVC_ERR_WORKSPACE and a message.
- * - The first call on a device resolves the array's device address
- *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.
+ * Same arguments, arithmetic, outputs and argument checks (with the same
+ * status codes) as kvc_decode_attend, without the workspace: the scratch
+ * (status word, logits, split partials, lengths) lives in a static device
+ * array of 32 MiB inside the library, which every GPU that loads the library
+ * holds until the process exits.  The call allocates nothing (no cudaMalloc,
+ * cudaFree or allocating library routine).
+ * - Sizes whose scratch exceeds 32 MiB are rejected with KVC_ERR_WORKSPACE
+ *   and a message.  The scratch is about U*ceil(cap/512)*G*520 bytes, plus
+ *   U*G*cap*4 bytes of logits when probs != NULL (the logits are only kept
+ *   to form the probabilities).
+ * - Each call looks up the array's device address in the calling thread's
+ *   current device context (cudaGetSymbolAddress), so a device reset or a
+ *   change of context needs nothing from the caller.  The first call on a
+ *   device also loads the library's device code there: make that first
+ *   call before any stream capture.
  * - Every call on a device shares the one array and it keeps the previous
  *   call's contents: calls whose kernels overlap on the GPU race and must be
- *   ordered by the caller.
+ *   ordered by the caller (one stream, or events).
  * - device_status (optional device pointer to one int32) receives the device
- *   status of this call (KVC_OK or the KVC_ERR_* a kernel recorded).
+ *   status of this call (KVC_OK or the KVC_ERR_* a kernel recorded, e.g.
+ *   KVC_ERR_SHAPE for a unit with len + 1 > max_len, which is left
+ *   untouched).  With device_status = NULL such device-side errors are
+ *   discarded: there is no workspace to read them from later.
  */
 KVC_API kvc_status kvc_decode_attend_noalloc(const kvc_params *p, int32_t t,
                                              int32_t new_pos, int32_t max_len,

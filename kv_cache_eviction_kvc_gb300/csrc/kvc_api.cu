@@ -51,8 +51,6 @@ DecodeWs decode_ws_layout(const kvc_params &p, void *base)
 
 }  // namespace kvc
 
-using namespace kvc;
-
 #define KVC_CHECK_ARG(cond, code, ...)       \
     do {                                     \
         if (!(cond)) {                       \
@@ -60,6 +58,8 @@ using namespace kvc;
             return (code);                   \
         }                                    \
     } while (0)
+
+namespace kvc {
 
 static kvc_status cuda_status(cudaError_t e, const char *what)
 {
@@ -70,7 +70,7 @@ static kvc_status cuda_status(cudaError_t e, const char *what)
 
 static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
-static kvc_status check_params(const kvc_params *p)
+kvc_status check_params(const kvc_params *p)
 {
     KVC_CHECK_ARG(p != nullptr, KVC_ERR_INVALID_ARG, "params is NULL");
     KVC_CHECK_ARG(p->d == kD, KVC_ERR_UNSUPPORTED, "d = %d unsupported (only 128)", p->d);
@@ -99,7 +99,7 @@ static kvc_status check_params(const kvc_params *p)
     return KVC_OK;
 }
 
-static kvc_status check_cache(const kvc_cache *c)
+kvc_status check_cache(const kvc_cache *c)
 {
     KVC_CHECK_ARG(c != nullptr, KVC_ERR_INVALID_ARG, "cache is NULL");
     KVC_CHECK_ARG(c->K && c->V && c->pos && c->util && c->len, KVC_ERR_INVALID_ARG,
@@ -136,6 +136,24 @@ static kvc_status check_moments(const kvc_moments *m)
         kvc_status _s = (expr);           \
         if (_s != KVC_OK) return _s;      \
     } while (0)
+
+kvc_status check_attend_args(const kvc_params *p, int32_t t, int32_t max_len, const uint16_t *q,
+                             const uint16_t *k_new, const uint16_t *v_new, const float *lse,
+                             const float *f_all)
+{
+    KVC_CHECK_ARG(t >= 1, KVC_ERR_INVALID_ARG, "step t = %d must be >= 1", t);
+    KVC_CHECK_ARG(max_len >= 1 && max_len <= p->cap, KVC_ERR_SHAPE,
+                  "max_len = %d must satisfy 1 <= max_len <= cap = %d", max_len, p->cap);
+    KVC_CHECK_ARG(q && k_new && v_new && lse && f_all, KVC_ERR_INVALID_ARG,
+                  "q, k_new, v_new, lse and f_all must be non-NULL");
+    KVC_CHECK_ARG(aligned16(q) && aligned16(k_new) && aligned16(v_new), KVC_ERR_INVALID_ARG,
+                  "q, k_new and v_new must be 16-byte aligned");
+    return KVC_OK;
+}
+
+}  // namespace kvc
+
+using namespace kvc;
 
 extern "C" {
 
@@ -199,13 +217,7 @@ kvc_status kvc_decode_attend(const kvc_params *p, int32_t t, int32_t new_pos, in
     KVC_TRY(check_cache(cache));
     DecodeWs w;
     KVC_TRY(check_ws(p, ws, ws_bytes, &w));
-    KVC_CHECK_ARG(t >= 1, KVC_ERR_INVALID_ARG, "step t = %d must be >= 1", t);
-    KVC_CHECK_ARG(max_len >= 1 && max_len <= p->cap, KVC_ERR_SHAPE,
-                  "max_len = %d must satisfy 1 <= max_len <= cap = %d", max_len, p->cap);
-    KVC_CHECK_ARG(q && k_new && v_new && lse && f_all, KVC_ERR_INVALID_ARG,
-                  "q, k_new, v_new, lse and f_all must be non-NULL");
-    KVC_CHECK_ARG(aligned16(q) && aligned16(k_new) && aligned16(v_new), KVC_ERR_INVALID_ARG,
-                  "q, k_new and v_new must be 16-byte aligned");
+    KVC_TRY(check_attend_args(p, t, max_len, q, k_new, v_new, lse, f_all));
     return cuda_status(launch_attend(*p, t, new_pos, max_len, q, k_new, v_new, *cache, lse, f_all,
                                      probs, w, static_cast<cudaStream_t>(stream)),
                        "kvc_decode_attend launch");

@@ -36,6 +36,14 @@ DecodeWs decode_ws_layout(const kvc_params &p, void *base);
 // thread-local error message
 void set_error(const char *fmt, ...);
 
+// host-side argument checks shared by the entry points (each sets the error
+// message and returns the status the entry point returns)
+kvc_status check_params(const kvc_params *p);
+kvc_status check_cache(const kvc_cache *c);
+kvc_status check_attend_args(const kvc_params *p, int32_t t, int32_t max_len, const uint16_t *q,
+                             const uint16_t *k_new, const uint16_t *v_new, const float *lse,
+                             const float *f_all);
+
 // launchers (return cudaError_t of the launch)
 cudaError_t launch_attend(const kvc_params &p, int t, int new_pos, int max_len,
                           const uint16_t *q, const uint16_t *k_new,

@@ -13,8 +13,6 @@
 // The caller still passes every input and output.  All calls share the one
 // array (per device): two calls whose kernels overlap on the GPU race on it
 // and must be ordered by the caller (one stream, or events).
-#include <mutex>
-
 #include <cuda_runtime.h>
 
 #include "kvc_common.cuh"
@@ -23,48 +21,55 @@
 namespace kvc {
 namespace {
 
-// Scratch for the split-K partials, per-unit lengths, logits and the status
-// word of one attention call.
+// Scratch for the status word, logits, split-K partials and per-unit lengths
+// of one attention call.
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;   // 32 MiB
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void *g_addr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device.  In host code
-// the array's name is only a host-side stand-in; the address a kernel may use
-// comes from cudaGetSymbolAddress, resolved once per device with that device
-// current (the first call on a device does this set-up).
+// Device address of the scratch array in the calling thread's current
+// device context.  In host code the array's name is only a host-side
+// stand-in; the address a kernel may use comes from cudaGetSymbolAddress.
+// It is looked up on every call (a cheap host-side lookup once the library's
+// device code is loaded), so it stays right after a device reset or when
+// another context is made current; the first call on a device also loads
+// the device code there.
 kvc_status scratch_address(void **out)
 {
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) {
-        set_error("kvc_decode_attend_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+        set_error("kvc_decode_attend_noalloc: cudaGetSymbolAddress: %s",
+                  cudaGetErrorString(e));
         return KVC_ERR_CUDA;
     }
-    if (dev < 0 || dev >= kMaxDevices) {
-        set_error("kvc_decode_attend_noalloc: device %d out of range", dev);
-        return KVC_ERR_UNSUPPORTED;
-    }
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (g_addr[dev] == nullptr) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || p == nullptr) {
-            set_error("kvc_decode_attend_noalloc: cudaGetSymbolAddress: %s",
-                      cudaGetErrorString(e));
-            return KVC_ERR_CUDA;
-        }
-        g_addr[dev] = p;
-    }
-    *out = g_addr[dev];
+    *out = p;
     return KVC_OK;
 }
 
-bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+// The regions of the decode workspace that the attention pass uses, packed
+// into the static array: the status word, the logits (only written when
+// probabilities are wanted), the split partials and the per-unit lengths.
+DecodeWs noalloc_layout(const kvc_params &p, char *base, bool want_logits)
+{
+    const size_t U = (size_t)p.U, G = (size_t)p.G, cap = (size_t)p.cap;
+    const size_t S = (cap + kAttendChunk - 1) / kAttendChunk;
+    DecodeWs w{};
+    size_t off = 0;
+    auto at = [&](size_t o) { return base ? base + o : nullptr; };   // sizes only: no base
+    w.status = reinterpret_cast<int32_t *>(at(off));
+    off += align_up(sizeof(WsHeader));
+    if (want_logits) {
+        w.xbuf = reinterpret_cast<float *>(at(off));
+        off += align_up(U * G * cap * sizeof(float));
+    }
+    w.part = reinterpret_cast<float *>(at(off));
+    off += align_up(U * S * G * (kD + 2) * sizeof(float));
+    w.nlen = reinterpret_cast<int32_t *>(at(off));
+    off += align_up(U * sizeof(int32_t));
+    w.bytes = off;
+    return w;
+}
 
 }  // namespace
 }  // namespace kvc
@@ -76,52 +81,23 @@ extern "C" KVC_API kvc_status kvc_decode_attend_noalloc(
     const uint16_t *k_new, const uint16_t *v_new, const kvc_cache *cache, float *lse,
     float *f_all, double *probs, int32_t *device_status, void *stream)
 {
-    if (p == nullptr || cache == nullptr) {
-        set_error("kvc_decode_attend_noalloc: params and cache are required");
-        return KVC_ERR_INVALID_ARG;
-    }
-    // argument checks of kvc_decode_attend, without a workspace
-    if (p->d != kD || !(p->G == 1 || p->G == 2 || p->G == 4 || p->G == 8)) {
-        set_error("kvc_decode_attend_noalloc: d = %d, G = %d unsupported", p->d, p->G);
-        return KVC_ERR_UNSUPPORTED;
-    }
-    if (p->U < 1 || p->cap < 1 || p->cap > kMaxCap) {
-        set_error("kvc_decode_attend_noalloc: U = %d or cap = %d out of range", p->U, p->cap);
-        return KVC_ERR_INVALID_ARG;
-    }
-    if (t < 1 || max_len < 1 || max_len > p->cap) {
-        set_error("kvc_decode_attend_noalloc: t = %d or max_len = %d out of range", t, max_len);
-        return t < 1 ? KVC_ERR_INVALID_ARG : KVC_ERR_SHAPE;
-    }
-    if (!cache->K || !cache->V || !cache->pos || !cache->util || !cache->len || !q || !k_new ||
-        !v_new || !lse || !f_all) {
-        set_error("kvc_decode_attend_noalloc: a required pointer is NULL");
-        return KVC_ERR_INVALID_ARG;
-    }
-    if (!aligned16(cache->K) || !aligned16(cache->V) || !aligned16(q) || !aligned16(k_new) ||
-        !aligned16(v_new) || ((uintptr_t)cache->util & 7u)) {
-        set_error("kvc_decode_attend_noalloc: K, V, q, k_new, v_new must be 16-byte aligned, "
-                  "util 8-byte aligned");
-        return KVC_ERR_INVALID_ARG;
-    }
-    // the attention pass uses the first regions of the decode workspace
-    // layout: status word, logits, split partials and per-unit lengths
-    void *base = nullptr;
-    kvc_status s = scratch_address(&base);
+    // the same checks, in the same order and with the same status codes, as
+    // kvc_decode_attend (the workspace checks excepted)
+    kvc_status s = check_params(p);
+    if (s == KVC_OK) s = check_cache(cache);
+    if (s == KVC_OK) s = check_attend_args(p, t, max_len, q, k_new, v_new, lse, f_all);
     if (s != KVC_OK) return s;
-    DecodeWs w = decode_ws_layout(*p, base);
-    const size_t bytes = (size_t)(reinterpret_cast<char *>(w.pend) - static_cast<char *>(base));
+    const size_t bytes = noalloc_layout(*p, nullptr, probs != nullptr).bytes;
     if (bytes > kNoAllocScratchBytes) {
         set_error("kvc_decode_attend_noalloc: U = %d, G = %d, cap = %d need %zu bytes of "
                   "scratch; the static scratch holds %zu bytes (use kvc_decode_attend with a "
                   "workspace)", p->U, p->G, p->cap, bytes, kNoAllocScratchBytes);
         return KVC_ERR_WORKSPACE;
     }
-    w.pend = nullptr;        // regions past the attention scratch are not used
-    w.lse = nullptr;
-    w.fall = nullptr;
-    w.probs = nullptr;
-    w.bytes = bytes;
+    void *base = nullptr;
+    s = scratch_address(&base);
+    if (s != KVC_OK) return s;
+    const DecodeWs w = noalloc_layout(*p, static_cast<char *>(base), probs != nullptr);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // the array keeps the previous call's contents: the status word must
     // start at zero; every other region is written before it is read

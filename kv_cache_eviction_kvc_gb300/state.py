@@ -69,8 +69,10 @@ class DecodeState:
     def load_prefill(self, K, V, votes, pos, length):
         """Copy a prefill cache laid out [U][>=N][d] into the state."""
         n = K.shape[1]
-        self.K[:, :n].copy_(K)
-        self.V[:, :n].copy_(V)
+        if K.data_ptr() != self.K.data_ptr():      # drawn in place: nothing to copy
+            self.K[:, :n].copy_(K)
+        if V.data_ptr() != self.V.data_ptr():
+            self.V[:, :n].copy_(V)
         if self.votes is not None and votes is not None:
             self.votes[:, :n].copy_(votes[:, :n])
         self.pos[:, :n].copy_(pos[:, :n])

@@ -224,20 +224,26 @@ def _draw_kv(cfg: DecodeConfig, P: UnitParams, u0: int, u1: int, n: int,
 
 
 def gen_prefill(cfg: DecodeConfig, device, seed: int = 0, cap: int | None = None,
-                P: UnitParams | None = None):
+                P: UnitParams | None = None, out_K=None, out_V=None):
     """Prefill cache of every unit.
 
     Returns dict with K, V [U][cap][d] bf16 (slots [0, N) filled, the rest
     zero), votes [U][cap] int32 or None (prefill slots U{1..votes_max}, the rest
     1), pos [U][cap] int32 (prefill slot i holds position i, the rest -1),
-    len [U] int32 = N.
+    len [U] int32 = N.  ``out_K`` / ``out_V`` (bf16 [U][cap][d]) receive the
+    draw in place of new tensors (slots past N untouched), so a large cache is
+    drawn straight into its final buffers; the numbers do not change.
     """
     cap = cfg.N + 1 if cap is None else cap
     assert cap >= cfg.N
     P = unit_params(cfg, device, seed) if P is None else P
     U, N, d = cfg.U, cfg.N, cfg.d
-    K = torch.zeros(U, cap, d, dtype=torch.bfloat16, device=device)
-    V = torch.zeros(U, cap, d, dtype=torch.bfloat16, device=device)
+    if out_K is not None:
+        assert out_K.shape == (U, cap, d) and out_V is not None and out_V.shape == out_K.shape
+        K, V = out_K, out_V
+    else:
+        K = torch.zeros(U, cap, d, dtype=torch.bfloat16, device=device)
+        V = torch.zeros(U, cap, d, dtype=torch.bfloat16, device=device)
     g = _gen(device, seed * 7919 + _OFF_PREFILL)
     cu = _chunk_units(cfg)
     for u0 in range(0, U, cu):

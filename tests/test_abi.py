@@ -119,3 +119,32 @@ def test_prefill_allocation_arguments_checked_on_host():
     assert rc == 1 and "alloc" in K.kvc_last_error()
     rc = lib.kvc_prefill_score(2, 8, 2, 128, 64, 8, 6, 1, K.ALLOC_HEAD, *args[:8], None, 0, None)
     assert rc == 1 and "multiple" in K.kvc_last_error()
+
+
+def _lib_call_attend_noalloc(p, **kw):
+    lib = K.load()
+    cache = K.kvc_cache(*(kw.get(k, 16 * (i + 1)) for i, k in enumerate(["K", "V", "votes", "pos", "util", "len"])))
+    return lib.kvc_decode_attend_noalloc(ctypes.byref(p), kw.get("t", 1), 0, kw.get("max_len", 5),
+                                         16, 16, 16, ctypes.byref(cache), 16, 16, None, None, None)
+
+
+@pytest.mark.parametrize("field,value", [
+    ("d", 64), ("G", 3), ("U", 0), ("L", 0), ("L", 100), ("refresh_period", 11),
+    ("rule", 7), ("alpha", 1.0), ("correction", 3), ("cap", 0), ("cap", 1 << 20),
+    ("merge", 2), ("merge_recent", -1)])
+def test_noalloc_rejects_what_attend_rejects(field, value):
+    """The entry point without a workspace validates its parameters exactly as
+    kvc_decode_attend does: the same status code for every rejected field
+    (host checks only; the pointers are fake and nothing launches)."""
+    p = K.make_params(U=2, G=4, cap=100, L=10)
+    setattr(p, field, value)
+    code = _lib_call_attend(p)
+    assert code != 0
+    assert _lib_call_attend_noalloc(p) == code
+    assert K.kvc_last_error() != ""
+
+
+def test_noalloc_rejects_bad_buffers_like_attend():
+    p = K.make_params(U=2, G=4, cap=100, L=10)
+    for kw in ({"K": None}, {"K": 18}, {"max_len": 101}, {"t": 0}):
+        assert _lib_call_attend_noalloc(p, **kw) == _lib_call_attend(p, **kw) != 0

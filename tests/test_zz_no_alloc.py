@@ -80,6 +80,35 @@ def test_noalloc_attend_matches_workspace_attend():
         assert torch.equal(nal["pos"], ref["pos"])
 
 
+def test_noalloc_reports_device_side_shape_errors():
+    """A unit whose appended length exceeds max_len is left untouched and the
+    device status of the call says KVC_ERR_SHAPE (the status word lives in
+    the static scratch, so it is only visible through device_status)."""
+    dev = torch.device("cuda", 0)
+    cfg = W.C0
+    cap = cfg.N + 2
+    pre = W.gen_prefill(cfg, dev, 0, cap=cfg.N + 1)
+    st = _state(cfg, pre, cap, dev)
+    U, G = cfg.U, cfg.G
+    p = K.make_params(U, G, cap, cfg.L, cfg.rule, cfg.alpha, cfg.T, cfg.correction)
+    lse = torch.zeros(U, G, device=dev)
+    f_all = torch.zeros(U, G, 128, device=dev)
+    status = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    inp = W.gen_step(cfg, dev, 1, 0)
+    len0 = st["len"].clone()
+    K.kvc_decode_attend_noalloc(p, 1, cfg.N, cfg.N, inp["q"], inp["k_new"], inp["v_new"],
+                                st["cache"], lse, f_all, None, status)     # max_len = len
+    torch.cuda.synchronize()
+    assert status.item() == 2                      # KVC_ERR_SHAPE
+    assert torch.equal(st["len"], len0)
+    # the next call starts from a clear status word
+    K.kvc_decode_attend_noalloc(p, 1, cfg.N, cfg.N + 1, inp["q"], inp["k_new"], inp["v_new"],
+                                st["cache"], lse, f_all, None, status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    assert torch.equal(st["len"], len0 + 1)
+
+
 def test_noalloc_rejects_sizes_beyond_its_scratch():
     dev = torch.device("cuda", 0)
     p = K.make_params(4608, 4, 32769, 3277)          # ~2.5 GB of scratch
