@@ -177,14 +177,14 @@ int ocl_append(void *h, const uint16_t *knew, const uint16_t *vnew,
  * Outputs: lse [U][G], f [U][G][d], probs [U][cap] (slot order; entries past
  * n[u] untouched).  Any output pointer may be NULL.
  */
-void ocl_attend(void *h, const uint16_t *q, double *lse, double *f,
-                double *probs)
+/* One unit of ocl_attend; lse [G], f [G][d] and probs [n] are the unit's
+ * own rows (any may be NULL). */
+static void attend_unit(ocl_session *s, int u, const uint16_t *q, double *lse, double *f,
+                        double *probs)
 {
-    ocl_session *s = (ocl_session *)h;
     int G = s->G, d = s->d, cap = s->cap;
     double rsd = 1.0 / sqrt((double)d);
-#pragma omp parallel for schedule(dynamic, 1)
-    for (int u = 0; u < s->U; u++) {
+    {
         int n = s->n[u];
         size_t base = (size_t)u * cap;
         double *x = (double *)malloc((size_t)(n > 0 ? n : 1) * sizeof(double));
@@ -202,9 +202,9 @@ void ocl_attend(void *h, const uint16_t *q, double *lse, double *f,
             double z = 0.0;
             for (int i = 0; i < n; i++) z += exp(x[i] - mx);
             double l = mx + log(z);
-            if (lse) lse[(size_t)u * G + hh] = l;
+            if (lse) lse[hh] = l;
             if (f) {
-                double *fh = &f[((size_t)u * G + hh) * d];
+                double *fh = &f[(size_t)hh * d];
                 for (int a = 0; a < d; a++) fh[a] = 0.0;
                 for (int i = 0; i < n; i++) {
                     double ai = exp(x[i] - l);
@@ -215,10 +215,21 @@ void ocl_attend(void *h, const uint16_t *q, double *lse, double *f,
             for (int i = 0; i < n; i++) ps[i] += exp(x[i] - l);
         }
         if (probs)
-            for (int i = 0; i < n; i++) probs[base + i] = ps[i] / (double)G;
+            for (int i = 0; i < n; i++) probs[i] = ps[i] / (double)G;
         free(x);
         free(ps);
     }
+}
+
+void ocl_attend(void *h, const uint16_t *q, double *lse, double *f,
+                double *probs)
+{
+    ocl_session *s = (ocl_session *)h;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int u = 0; u < s->U; u++)
+        attend_unit(s, u, q, lse ? &lse[(size_t)u * s->G] : NULL,
+                    f ? &f[(size_t)u * s->G * s->d] : NULL,
+                    probs ? &probs[(size_t)u * s->cap] : NULL);
 }
 
 /*
@@ -264,13 +275,12 @@ void ocl_update_util(void *h, const double *probs, int rule, double alpha)
  * head-mean of the vote-weighted probabilities, as ocl_attend writes it).
  * Output: out [U][cap] (entries past n[u] untouched).
  */
-void ocl_mi_scores(void *h, const double *probs, double *out)
+/* One unit of ocl_mi_scores; probs and out are the unit's rows [n]. */
+static void mi_unit(ocl_session *s, int u, const double *probs, double *out)
 {
-    ocl_session *s = (ocl_session *)h;
     int d = s->d;
     double rsd = 1.0 / sqrt((double)d);
-#pragma omp parallel for schedule(dynamic, 1)
-    for (int u = 0; u < s->U; u++) {
+    {
         size_t base = (size_t)u * s->cap;
         double ne = s->ne[u];
         const double *sk = &s->sk[(size_t)u * d], *sv = &s->sv[(size_t)u * d];
@@ -291,10 +301,18 @@ void ocl_mi_scores(void *h, const double *probs, double *out)
             } else {
                 for (int a = 0; a < d; a++) rr += bfd(vi[a]) * bfd(vi[a]);
             }
-            out[base + i] = probs[base + i] * sqrt(rr);
+            out[i] = probs[i] * sqrt(rr);
         }
         free(dk);
     }
+}
+
+void ocl_mi_scores(void *h, const double *probs, double *out)
+{
+    ocl_session *s = (ocl_session *)h;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int u = 0; u < s->U; u++)
+        mi_unit(s, u, &probs[(size_t)u * s->cap], &out[(size_t)u * s->cap]);
 }
 
 /*
@@ -386,16 +404,15 @@ int ocl_select(void *h, int L, int kmax, int32_t *victims, int32_t *nvict,
  * addition], then the slot is removed, keeping the rest in position order.
  * Returns 0, or -1 if a position is not present.
  */
-int ocl_evict(void *h, const int32_t *victims, const int32_t *nvict, int kmax)
+static int evict_unit(ocl_session *s, int u, const int32_t *victims, int nv)
 {
-    ocl_session *s = (ocl_session *)h;
     int d = s->d, rc = 0;
-    for (int u = 0; u < s->U; u++) {
+    {
         size_t base = (size_t)u * s->cap;
         int n = s->n[u];
         uint8_t *gone = (uint8_t *)calloc((size_t)(n > 0 ? n : 1), 1);
-        for (int j = 0; j < nvict[u]; j++) {
-            int32_t p = victims[(size_t)u * kmax + j];
+        for (int j = 0; j < nv; j++) {
+            int32_t p = victims[j];
             int i = 0;
             while (i < n && (s->pos[base + i] != p || gone[i])) i++;
             if (i == n) { rc = -1; continue; }
@@ -429,6 +446,87 @@ int ocl_evict(void *h, const int32_t *victims, const int32_t *nvict, int kmax)
         }
         s->n[u] = w;
         free(gone);
+    }
+    return rc;
+}
+
+int ocl_evict(void *h, const int32_t *victims, const int32_t *nvict, int kmax)
+{
+    ocl_session *s = (ocl_session *)h;
+    int rc = 0;
+    for (int u = 0; u < s->U; u++)
+        if (evict_unit(s, u, &victims[(size_t)u * kmax], nvict[u]) != 0) rc = -1;
+    return rc;
+}
+
+/*
+ * Moment-aware eviction phase of one decode step [MomentKV Algorithm 1,
+ * phase 1; sec 4.2 "moment residual" and "moment-aware eviction score"]:
+ * while a unit holds more than L slots,
+ *   - alpha = softmax over the slots still present (re-formed every round,
+ *     so it renormalizes over R; for a GQA group the head mean of the G
+ *     query heads' vote-weighted probabilities, as ocl_attend forms it),
+ *   - k_bar, v_bar, S_tilde from the running sums as they stand (zero
+ *     residual model while n_e = 0),
+ *   - score(j) = alpha_j ||v_j - v_bar - S_tilde (k_j - k_bar)/(n_e sqrt d)||,
+ *   - the slot with the lowest score goes (ties to the smaller position),
+ *     folded into the sums with its vote as weight and removed,
+ * so every round sees the moments and the softmax left by the previous one.
+ * With one victim this is one scoring pass and one argmin.
+ * forced [U][kmax] (positions, or NULL): when given, round r of unit u
+ * removes forced[u][r] instead of its own argmin (the caller replays another
+ * implementation's choices and checks each against best / used).
+ * Outputs: victims [U][kmax] positions in eviction order, nvict [U],
+ * best [U][kmax] the lowest score of each round, used [U][kmax] the score of
+ * the slot removed in that round (NULL allowed), scores0 [U][cap] the scores
+ * of the first round (slot order before the step's removals; NULL allowed).
+ * Returns 0, or -1 if k > kmax or a forced position is not present.
+ */
+int ocl_mi_greedy(void *h, const uint16_t *q, int L, int kmax, const int32_t *forced,
+                  int32_t *victims, int32_t *nvict, double *best, double *used,
+                  double *scores0)
+{
+    ocl_session *s = (ocl_session *)h;
+    int rc = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(min : rc)
+    for (int u = 0; u < s->U; u++) {
+        size_t base = (size_t)u * s->cap;
+        int k = s->n[u] > L ? s->n[u] - L : 0;
+        nvict[u] = 0;
+        if (k > kmax) { rc = -1; continue; }
+        double *pr = (double *)malloc((size_t)s->cap * sizeof(double));
+        double *sc = (double *)malloc((size_t)s->cap * sizeof(double));
+        for (int r = 0; r < k; r++) {
+            attend_unit(s, u, q, NULL, NULL, pr);
+            mi_unit(s, u, pr, sc);
+            int n = s->n[u], jb = 0;
+            for (int i = 1; i < n; i++) {
+                double a = sc[i], b = sc[jb];
+                if (a < b || (a == b && s->pos[base + i] < s->pos[base + jb])) jb = i;
+            }
+            if (r == 0 && scores0)
+                for (int i = 0; i < n; i++) scores0[base + i] = sc[i];
+            int32_t vp = s->pos[base + jb];
+            double vs = sc[jb];
+            if (best) best[(size_t)u * kmax + r] = sc[jb];
+            if (forced) {
+                vp = forced[(size_t)u * kmax + r];
+                int i = 0;
+                while (i < n && s->pos[base + i] != vp) i++;
+                if (i == n) { rc = -1; break; }
+                vs = sc[i];
+            }
+            if (used) used[(size_t)u * kmax + r] = vs;
+            for (int i = 0; i < n; i++) {          /* the slot's score as its utility */
+                s->util[base + i] = sc[i];
+                s->scored[base + i] = 1;
+            }
+            victims[(size_t)u * kmax + r] = vp;
+            nvict[u] = r + 1;
+            if (evict_unit(s, u, &vp, 1) != 0) { rc = -1; break; }
+        }
+        free(pr);
+        free(sc);
     }
     return rc;
 }

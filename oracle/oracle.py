@@ -76,6 +76,7 @@ def _load():
             "ocl_get_rows": (None, [P, P, P]),
             "ocl_moments": (None, [P, P, P, P, P]),
             "ocl_mi_scores": (None, [P, P, P]),
+            "ocl_mi_greedy": (I, [P, P, I, I, P, P, P, P, P, P]),
             "ocl_set_util": (I, [P, I, I, P]),
             "ocl_prefill_ema_init": (None, [I, I, I, I, I, I, D, P, P, P]),
             "ocl_output": (None, [P, P, I, P, P, P]),
@@ -255,6 +256,30 @@ class DecodeSession:
         self.lib.ocl_mi_scores(self.h, _p(probs), _p(out))
         return out
 
+    def mi_greedy(self, q, L: int, kmax: int, forced=None):
+        """MomentKV Algorithm 1 phase 1 on every unit: while a unit holds more
+        than L slots, score every slot (alpha ||r|| with alpha re-formed over
+        the slots present and the moments as they stand), evict the lowest
+        and fold it (see ocl_mi_greedy).  ``forced`` [U][kmax] (positions in
+        eviction order) replays another implementation's choices.  Returns a
+        dict: victims [U][kmax] (eviction order), nvict [U], best / used
+        [U][kmax] (each round's lowest score and the removed slot's score),
+        scores0 [U][cap] (first-round scores, slot order before the step)."""
+        qb = _bits(q)
+        kmax = max(1, int(kmax))
+        forced = None if forced is None else np.ascontiguousarray(forced, dtype=np.int32)
+        if forced is not None and forced.shape != (self.U, kmax):
+            raise ValueError("forced must be [U][kmax]")
+        out = dict(victims=np.full((self.U, kmax), -1, np.int32),
+                   nvict=np.zeros(self.U, np.int32), best=np.zeros((self.U, kmax)),
+                   used=np.zeros((self.U, kmax)), scores0=np.zeros((self.U, self.cap)))
+        rc = self.lib.ocl_mi_greedy(self.h, _p(qb), int(L), kmax, _p(forced),
+                                    _p(out["victims"]), _p(out["nvict"]), _p(out["best"]),
+                                    _p(out["used"]), _p(out["scores0"]))
+        if rc != 0:
+            raise ValueError("ocl_mi_greedy: kmax too small or a forced position is not present")
+        return out
+
     def moments(self):
         """Returns (n [U], mu_k [U][d], mu_v [U][d], C [U][d][d])."""
         n = np.zeros(self.U)
@@ -292,23 +317,29 @@ def is_refresh(t: int, T: int) -> bool:
 
 def decode_step(sess: DecodeSession, t: int, new_pos: int, q, knew, vnew, *,
                 L: int, rule: int, alpha: float, T: int, correction: int,
-                choose=None, merge_recent: int | None = None, force_partner=None):
+                choose=None, merge_recent: int | None = None, force_partner=None,
+                mi_forced=None):
     """One decode step on every unit of ``sess``, in the order of MomentKV
     Algorithm 1 with the InertiaKV utility in place of its scoring:
 
     1. append (k_new, v_new) with vote 1
     2. vote-weighted attention over all slots -> lse, f_all, head-mean probs
-    3. refresh step: utility update                 (InertiaKV sec 3.1 eqs 2-4);
-       rule RULE_MI: every step, utility = alpha ||r|| (MomentKV sec 4.2;
-       a step removing several slots takes the k lowest of these scores at
-       once, with the moments it entered with)
+    3. refresh step: utility update                 (InertiaKV sec 3.1 eqs 2-4)
     4. victims: the k = n - L lowest (utility, position) scored slots
     5. fold victims into the moments and remove them  (eviction phase)
     6. retained attention + moment correction         (inference phase)
 
+    Under rule RULE_MI steps 3-5 are MomentKV's moment-aware eviction phase
+    itself (Algorithm 1 phase 1, :meth:`DecodeSession.mi_greedy`): every
+    step, while a unit holds more than L slots, score alpha ||r|| over the
+    slots present, evict the lowest, fold it, and score again.
+    ``mi_forced`` [U][kmax] (positions in eviction order) replays another
+    implementation's choices; the result's ``mi_best`` / ``mi_used`` give
+    each round's lowest score and the score of the slot removed.
+
     ``choose(t, proposal)``, if given, receives the oracle's proposal dict and
     returns the victim positions to apply ([U][kmax], [U]); tests use it to
-    validate a near-tie alternative before adopting it.
+    validate a near-tie alternative before adopting it (not under RULE_MI).
 
     ``merge_recent = R`` (not None) selects KeepKV ZIP-merging: a unit that
     removes exactly one slot this step merges its victim into the most
@@ -324,24 +355,35 @@ def decode_step(sess: DecodeSession, t: int, new_pos: int, q, knew, vnew, *,
     """
     sess.append(knew, vnew, new_pos)
     lse, f_all, probs = sess.attend(q)
-    scores = None
     if rule == RULE_MI:
-        # MomentKV Algorithm 1: every step scores every slot (the new one
-        # included) by alpha ||r|| with the moments as they enter the step
-        refresh = True
-        scores = sess.mi_scores(probs)
-        sess.update_util(scores, RULE_SINGLE, alpha)
+        if merge_recent is not None:
+            raise ValueError("the moment-informed rule evicts; it is not combined with merging")
+        n = sess.slots()[0]
+        kmax = int(max(1, (n - L).max()))
+        if mi_forced is not None:
+            mi_forced = np.asarray(mi_forced)
+            kmax = max(kmax, mi_forced.shape[1])
+            f = np.full((sess.U, kmax), -1, np.int32)
+            f[:, : mi_forced.shape[1]] = mi_forced
+            mi_forced = f
+        g = sess.mi_greedy(q, L, kmax, forced=mi_forced)
+        vic, nv = g["victims"], g["nvict"]
+        last = np.maximum(nv - 1, 0)
+        thr = np.where(nv > 0, g["best"][np.arange(sess.U), last], 0.0)
+        proposal = dict(victims=vic, nvict=nv, thr=thr, lse=lse, f_all=f_all, probs=probs,
+                        refresh=True, mi_scores=g["scores0"], mi_best=g["best"],
+                        mi_used=g["used"])
     else:
         refresh = is_refresh(t, T)
         if refresh:
             sess.update_util(probs, rule, alpha)
-    n = sess.slots()[0]
-    kmax = int(max(1, (n - L).max()))
-    vic, nv, thr = sess.select(L, kmax)
-    proposal = dict(victims=vic, nvict=nv, thr=thr, lse=lse, f_all=f_all,
-                    probs=probs if refresh else None, refresh=refresh, mi_scores=scores)
-    if choose is not None:
-        vic, nv = choose(t, proposal)
+        n = sess.slots()[0]
+        kmax = int(max(1, (n - L).max()))
+        vic, nv, thr = sess.select(L, kmax)
+        proposal = dict(victims=vic, nvict=nv, thr=thr, lse=lse, f_all=f_all,
+                        probs=probs if refresh else None, refresh=refresh, mi_scores=None)
+        if choose is not None:
+            vic, nv = choose(t, proposal)
     merged = np.zeros(len(nv), bool)
     if merge_recent is not None:
         o0, fR0, lz0 = sess.output(q, correction)       # every slot, before the merge
@@ -350,7 +392,8 @@ def decode_step(sess: DecodeSession, t: int, new_pos: int, q, knew, vnew, *,
         merged = mres["partner"] >= 0
         proposal.update(merge=mres, merged=merged)
         nv = np.where(merged, 0, nv).astype(np.int32)
-    sess.evict(vic, nv)
+    if rule != RULE_MI:                 # the moment-aware phase already evicted
+        sess.evict(vic, nv)
     o, fR, lz = sess.output(q, correction)
     if merge_recent is not None:
         o[merged], fR[merged], lz[merged] = o0[merged], fR0[merged], lz0[merged]

@@ -562,11 +562,102 @@ def test_mi_residual_matches_numpy_covariance_and_is_shift_invariant():
     np.testing.assert_allclose(scores(base_k, base_v + shift), ref, rtol=1e-12)
 
 
+def _numpy_mi_round(k, v, p, q, evk, evv, evp):
+    """Scores of one round of MomentKV Algorithm 1 phase 1, restated with
+    numpy / scipy: alpha = head mean of the vote-weighted softmax over the
+    slots present, moments of the evicted tokens by numpy's weighted
+    two-pass covariance (fweights = votes), residual and score."""
+    from scipy.special import softmax
+    d = k.shape[1]
+    x = q @ k.T / math.sqrt(d) + np.log(p)[None, :]          # [G][n]
+    alpha = softmax(x, axis=1).mean(axis=0)
+    if len(evp) == 0:
+        r = v
+    else:
+        w = np.asarray(evp)
+        mk = np.average(evk, axis=0, weights=w)
+        mv = np.average(evv, axis=0, weights=w)
+        C = np.cov(np.hstack([evv, evk]).T, fweights=w, bias=True)[:d, d:]
+        r = v - mv - (k - mk) @ C.T / math.sqrt(d)
+    return alpha * np.linalg.norm(r, axis=1)
+
+
+def test_mi_greedy_rounds_are_the_argmin_of_independent_scores():
+    """MomentKV Algorithm 1 phase 1 with k > 1: every round removes the
+    slot whose score, recomputed from scratch (numpy: softmax over the
+    slots still present, weighted covariance of every token evicted so far)
+    is lowest among all slots present, by brute force over the candidates,
+    ties to the smaller position; votes weight the fold (KeepKV eq 6)."""
+    rng = np.random.default_rng(31)
+    for trial in range(12):
+        d, G = 8, 2
+        n = int(rng.integers(6, 13))
+        k_ = int(rng.integers(2, 5))
+        L = n - k_
+        kk = bf(rng.normal(size=(n, d)))
+        vv = bf(rng.normal(size=(n, d)))
+        p = rng.integers(1, 4, size=n).astype(np.int32)
+        q = bf(rng.normal(size=(1, G, d)))
+        s = O.DecodeSession(1, G, d, n + 2)
+        s.load(0, kk, vv, p)
+        g = s.mi_greedy(q, L, k_)
+        assert g["nvict"][0] == k_
+        present = list(range(n))
+        evk, evv, evp = [], [], []
+        for r in range(k_):
+            sc = _numpy_mi_round(kk[present], vv[present], p[present].astype(float), q[0],
+                                 np.array(evk).reshape(-1, d), np.array(evv).reshape(-1, d), evp)
+            j = min(range(len(present)), key=lambda i: (sc[i], present[i]))
+            assert g["victims"][0, r] == present[j], (trial, r)
+            assert g["best"][0, r] == pytest.approx(sc[j], rel=1e-9, abs=1e-300)
+            evk.append(kk[present[j]]); evv.append(vv[present[j]]); evp.append(float(p[present[j]]))
+            del present[j]
+        s.close()
+
+
+def test_mi_greedy_refolds_between_rounds():
+    """A case where scoring once and taking the two lowest differs from the
+    page's loop.  Logits 0, 1, 1/2, 2, 2 (q = 2 e_0, d = 4) and unit values
+    v_A = v_B = e_0, v_C = e_1, v_D = e_2, v_E = e_3, nothing evicted yet:
+    the first scores are alpha ||v|| with the order A < C < B < D = E.
+    Round 1 evicts A; folding it makes (v_bar, S_tilde) = (e_0, 0), so B's
+    residual is exactly 0 and round 2 evicts B, not C."""
+    d = 4
+    q = np.zeros((1, 1, d)); q[0, 0, 0] = 2.0
+    k = np.zeros((5, d)); k[:, 0] = [0.0, 1.0, 0.5, 2.0, 2.0]
+    v = np.zeros((5, d)); v[0, 0] = v[1, 0] = 1.0; v[2, 1] = 1.0; v[3, 2] = 1.0; v[4, 3] = 1.0
+    s = make_session(k, v)
+    g = s.mi_greedy(q, 3, 2)
+    assert g["victims"][0, :2].tolist() == [0, 1]
+    assert g["best"][0, 1] == 0.0
+    e = np.exp([0.0, 1.0, 0.5, 2.0, 2.0])
+    np.testing.assert_allclose(g["scores0"][0, :5], e / e.sum(), rtol=1e-14)
+    s.close()
+
+
+def test_mi_greedy_equals_one_round_at_a_time():
+    """k rounds in one call are k calls of one round each with the budget
+    lowered by one (the same query, no token appended in between)."""
+    rng = np.random.default_rng(33)
+    d, G, n, k_ = 8, 4, 11, 4
+    kk, vv = bf(rng.normal(size=(n, d))), bf(rng.normal(size=(n, d)))
+    q = bf(rng.normal(size=(1, G, d)))
+    a = make_session(kk, vv, G=G)
+    b = make_session(kk, vv, G=G)
+    ga = a.mi_greedy(q, n - k_, k_)
+    order = [int(b.mi_greedy(q, n - 1 - r, 1)["victims"][0, 0]) for r in range(k_)]
+    assert ga["victims"][0, :k_].tolist() == order
+    for x, y in zip(a.moments(), b.moments()):
+        np.testing.assert_array_equal(x, y)
+    a.close(); b.close()
+
+
 def test_mi_generation_evicts_the_lowest_score():
     """Decode loop with the moment-informed rule: every step re-scores (the
     new token included) and evicts the slot with the lowest alpha ||r||
     (ties to the older position), checked by brute force on the step's
-    scores."""
+    scores; the first step removes several slots, one argmin and one fold
+    at a time (MomentKV Algorithm 1 phase 1)."""
     rng = np.random.default_rng(23)
     U, N, d, G, S, L = 2, 16, 8, 2, 6, 10
     kp, vp = bf(rng.normal(size=(U, N, d))), bf(rng.normal(size=(U, N, d)))
@@ -583,9 +674,12 @@ def test_mi_generation_evicts_the_lowest_score():
         assert r["refresh"]
         for u in range(U):
             n = int(n0[u]) + 1
-            pos = np.append(pos0[u, : n0[u]], N + t - 1)
-            sc = r["mi_scores"][u, :n]
             k = n - L
-            want = sorted(pos[i] for i in sorted(range(n), key=lambda i: (sc[i], pos[i]))[:k])
-            assert sorted(r["applied_victims"][u, : r["applied_nvict"][u]].tolist()) == want
+            assert r["applied_nvict"][u] == k
+            if k == 1:
+                pos = np.append(pos0[u, : n0[u]], N + t - 1)
+                sc = r["mi_scores"][u, :n]
+                want = min(range(n), key=lambda i: (sc[i], pos[i]))
+                assert r["applied_victims"][u, 0] == pos[want]
+            assert r["mi_used"][u, :k].tolist() == r["mi_best"][u, :k].tolist()
     sess.close()
