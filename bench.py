@@ -350,13 +350,13 @@ def run_ours(args, cfg, rank, world, steps=None, warmup=None, e2e=True, sample_c
     torch.cuda.empty_cache()
     stream = torch.cuda.current_stream(dev)
 
-    # step 1: the one-off pass over N + 1 slots (general path).  Under the
-    # moment-informed rule the prompt is first compressed by the attention
-    # rule, as MomentKV's setup compresses it with the SnapKV protocol before
-    # decoding; every token this removes is folded into the moments.
+    # step 1: the one-off pass over N + 1 slots (general path), under the
+    # workload's first-step rule where it has one (the moment-informed
+    # workload compresses the prompt by attention first; every token this
+    # removes is folded into the moments)
     inp = W.gen_step(cfg, dev, 1, seed, P)
-    if mi:
-        st.params.rule = W.RULE_EMA
+    if cfg.first_rule is not None:
+        st.params.rule = cfg.first_rule
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     st.step(1, N, inp["q"], inp["k_new"], inp["v_new"], max_len=N + 1)

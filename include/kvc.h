@@ -89,8 +89,9 @@ typedef struct {
     int32_t L;               /* budget: slots kept per unit after a step     */
     int32_t rule;            /* KVC_RULE_*  (InertiaKV sec 3.1 eqs 2-4;
                                 KVC_RULE_MI: MomentKV's moment-informed
-                                score, every step, needs T = 1; see
-                                kvc_mi_scores)                               */
+                                score, every step, needs T = 1 and
+                                merge = 0; see kvc_mi_scores and
+                                kvc_mi_evict)                                */
     float alpha;             /* EMA coefficient, 0 <= alpha < 1              */
     int32_t refresh_period;  /* 0 <= T <= L: utilities refresh on step
                                 t = 1 and whenever (t - 1) mod T == 0
@@ -284,12 +285,46 @@ KVC_API kvc_status kvc_correct(const kvc_params *p, const uint16_t *q,
  * probs being the head-mean probabilities kvc_decode_attend wrote for this
  * step (the slot's attention weight).  scores may alias probs.  With rule
  * KVC_RULE_MI, kvc_aggregate_evict takes these scores as the utilities of
- * every slot (refreshed every step) and evicts the lowest.  fp32 residuals
- * (CUDA cores), fp64 scores.  max_len bounds len[u] (<= cap).
+ * every slot (refreshed every step) and evicts the lowest, for steps that
+ * remove one slot; a unit removing more (which MomentKV Algorithm 1 does
+ * one fold at a time, re-scoring in between) is refused there with device
+ * status KVC_ERR_UNSUPPORTED: use kvc_mi_evict.  fp32 residuals (CUDA
+ * cores), fp64 scores.  max_len bounds len[u] (<= cap).
  */
 KVC_API kvc_status kvc_mi_scores(const kvc_params *p, const kvc_cache *cache,
                                  const kvc_moments *mom, int32_t max_len,
                                  const double *probs, double *scores, void *stream);
+
+/*
+ * kvc_mi_evict -- MomentKV's moment-aware eviction phase for a step that
+ * removes several slots.
+ *
+ * Defined by: MomentKV Algorithm 1, phase 1 (while |R| > L: re-form the
+ * means and S_tilde from the running statistics, alpha = softmax over R,
+ * score(j) = alpha_j ||r_j||, evict the argmin, fold it, remove it), sec 4.2
+ * ("moment residual", "moment-aware eviction score"), sec 4.1 "efficient
+ * statistics update".
+ *
+ * Call right after kvc_decode_attend of the same step, with probs requested
+ * there: it reads the logits that call left in the workspace, and lse is
+ * that call's output.  For each unit with k = len[u] - L > 0, k rounds:
+ * alpha_i = (1/G) sum_h exp(x_hi - lse_h) / Z_h with Z_h summed over the
+ * slots still present (fp64), r_i = v_i - mu_v - C (k_i - mu_k) / sqrt(d)
+ * with the moments as they stand, the lowest alpha_i ||r_i|| goes (ties to
+ * the smaller position) and is folded into the moments (weighted by its
+ * vote, KeepKV eq 6).  evict_idx / evict_pos (optional) [U][kmax] receive
+ * the victims in eviction order, n_evict[u] = k, util[i] the last score of
+ * each slot still present.  Nothing is compacted: kvc_correct (whose
+ * moments are then already folded: do not call kvc_moment_update) and
+ * kvc_compact follow.  Each round re-scores the whole unit (O(len d^2)):
+ * max_len <= 8192 and (max_len - L) * max_len <= 2^22, else
+ * KVC_ERR_UNSUPPORTED (compress a long prompt first).  kmax >=
+ * max_len - L.  fp32 residuals, fp64 weights and scores.
+ */
+KVC_API kvc_status kvc_mi_evict(const kvc_params *p, int32_t max_len, const kvc_cache *cache,
+                                const kvc_moments *mom, const float *lse, int32_t kmax,
+                                int32_t *evict_idx, int32_t *evict_pos, int32_t *n_evict,
+                                void *ws, size_t ws_bytes, void *stream);
 
 /*
  * kvc_zip_merge -- merge each unit's single victim into its most similar
@@ -348,8 +383,11 @@ KVC_API kvc_status kvc_compact(const kvc_params *p, const kvc_cache *cache,
  * kvc_compact called in that order (same sets; outputs within fp32
  * rounding); with p->merge = 1, kvc_zip_merge runs between
  * kvc_aggregate_evict and kvc_moment_update; with rule KVC_RULE_MI,
- * kvc_mi_scores runs between kvc_decode_attend and kvc_aggregate_evict (the
- * call sequence; no fused kernel).
+ * kvc_mi_scores runs between kvc_decode_attend and kvc_aggregate_evict when
+ * one slot goes, and kvc_mi_evict replaces kvc_mi_scores,
+ * kvc_aggregate_evict and kvc_moment_update when several go (the call
+ * sequence; no fused kernel; evict_idx / evict_pos then in eviction order,
+ * and the bounds of kvc_mi_evict apply).
  *
  * In the steady state (max_len == L + 1: every unit enters with len = L and
  * evicts exactly one slot) one cluster kernel per step does everything: the

@@ -96,6 +96,8 @@ kvc_status check_params(const kvc_params *p)
                   "merge = %d must be 0 or 1", p->merge);
     KVC_CHECK_ARG(p->merge_recent >= 0, KVC_ERR_INVALID_ARG,
                   "merge_recent = %d must be >= 0", p->merge_recent);
+    KVC_CHECK_ARG(!(p->merge && p->rule == KVC_RULE_MI), KVC_ERR_INVALID_ARG,
+                  "the moment-informed rule evicts (and folds); it is not combined with merging");
     return KVC_OK;
 }
 
@@ -136,6 +138,20 @@ static kvc_status check_moments(const kvc_moments *m)
         kvc_status _s = (expr);           \
         if (_s != KVC_OK) return _s;      \
     } while (0)
+
+// The greedy moment-aware phase costs O(rounds x slots x d^2): bound it.
+static kvc_status check_mi_greedy(const kvc_params *p, int32_t max_len)
+{
+    const long long rounds = (long long)max_len - p->L;
+    KVC_CHECK_ARG(max_len <= kMiGreedyMaxSlots && rounds * max_len <= kMiGreedyMaxWork,
+                  KVC_ERR_UNSUPPORTED,
+                  "a moment-informed step removing %lld slots from %d takes %lld rounds of "
+                  "scoring over the whole cache (MomentKV Algorithm 1); supported up to %d slots "
+                  "and %lld rounds x slots: compress the prompt first (e.g. the prefill scorer "
+                  "and kvc_prefill_handoff) or take the first step with an attention rule",
+                  rounds, max_len, rounds, kMiGreedyMaxSlots, kMiGreedyMaxWork);
+    return KVC_OK;
+}
 
 kvc_status check_attend_args(const kvc_params *p, int32_t t, int32_t max_len, const uint16_t *q,
                              const uint16_t *k_new, const uint16_t *v_new, const float *lse,
@@ -305,6 +321,28 @@ kvc_status kvc_mi_scores(const kvc_params *p, const kvc_cache *cache, const kvc_
                        "kvc_mi_scores launch");
 }
 
+kvc_status kvc_mi_evict(const kvc_params *p, int32_t max_len, const kvc_cache *cache,
+                        const kvc_moments *mom, const float *lse, int32_t kmax,
+                        int32_t *evict_idx, int32_t *evict_pos, int32_t *n_evict, void *ws,
+                        size_t ws_bytes, void *stream)
+{
+    KVC_TRY(check_params(p));
+    KVC_TRY(check_cache(cache));
+    KVC_TRY(check_moments(mom));
+    DecodeWs w;
+    KVC_TRY(check_ws(p, ws, ws_bytes, &w));
+    KVC_CHECK_ARG(lse && evict_idx && n_evict, KVC_ERR_INVALID_ARG,
+                  "lse, evict_idx and n_evict are required");
+    KVC_CHECK_ARG(max_len >= 1 && max_len <= p->cap, KVC_ERR_SHAPE,
+                  "max_len = %d must satisfy 1 <= max_len <= cap = %d", max_len, p->cap);
+    KVC_CHECK_ARG(kmax >= 1 && kmax >= max_len - p->L, KVC_ERR_SHAPE,
+                  "kmax = %d must be >= max(1, max_len - L = %d)", kmax, max_len - p->L);
+    KVC_TRY(check_mi_greedy(p, max_len));
+    return cuda_status(launch_mi_greedy(*p, *cache, *mom, w.xbuf, lse, kmax, evict_idx, evict_pos,
+                                        n_evict, w.status, static_cast<cudaStream_t>(stream)),
+                       "kvc_mi_evict launch");
+}
+
 kvc_status kvc_zip_merge(const kvc_params *p, int32_t new_pos, const uint16_t *q,
                          const kvc_cache *cache, int32_t kmax, const int32_t *evict_idx,
                          int32_t *n_evict, int32_t *partner_pos, void *ws, size_t ws_bytes,
@@ -361,12 +399,26 @@ kvc_status kvc_decode_step(const kvc_params *p, int32_t t, int32_t new_pos, int3
     // general case: the five-call sequence with workspace scratch
     KVC_CHECK_ARG(evict_idx != nullptr, KVC_ERR_INVALID_ARG,
                   "evict_idx is required when the step is not in the steady state");
+    if (p->rule == KVC_RULE_MI && max_len - p->L > 1) KVC_TRY(check_mi_greedy(p, max_len));
     const bool refresh = is_refresh(t, p->refresh_period);
     double *pr = probs ? probs : w.probs;
     KVC_TRY(cuda_status(launch_attend(*p, t, new_pos, max_len, q, k_new, v_new, *cache, w.lse,
                                       w.fall, refresh ? pr : nullptr, w, st),
                         "kvc_decode_step attend"));
+    if (p->rule == KVC_RULE_MI && max_len - p->L > 1) {
+        // several slots go: MomentKV Algorithm 1's loop (score, evict the
+        // lowest, fold, score again) in one kernel, then the inference phase
+        KVC_TRY(cuda_status(launch_mi_greedy(*p, *cache, *mom, w.xbuf, w.lse, kmax, evict_idx,
+                                             evict_pos, n_evict, w.status, st),
+                            "kvc_decode_step moment-aware eviction"));
+        KVC_TRY(cuda_status(launch_correct(*p, q, *cache, kmax, evict_idx, n_evict, w.lse, w.fall,
+                                           *mom, o, nullptr, nullptr, w, st),
+                            "kvc_decode_step correct"));
+        return cuda_status(launch_compact(*p, *cache, kmax, evict_idx, n_evict, w, st),
+                           "kvc_decode_step compact");
+    }
     if (p->rule == KVC_RULE_MI) {
+        // one slot goes: one scoring pass and the argmin, as separate kernels;
         // the scores take the probabilities' place as the aggregate's input
         // (in the workspace; the caller's probs keep the probabilities)
         KVC_TRY(cuda_status(launch_mi_scores(*p, *cache, *mom, max_len, pr, w.probs, st),

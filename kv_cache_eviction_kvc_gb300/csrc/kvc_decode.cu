@@ -417,6 +417,12 @@ __global__ void __launch_bounds__(512) aggregate_kernel(AggArgs a)
         if (tid == 0) a.n_evict[u] = 0;
         return;
     }
+    if (a.rule == KVC_RULE_MI && k > 1) {
+        // MomentKV's loop re-scores after every fold: taking the k lowest
+        // scores of one pass is not the method (kvc_mi_evict runs the loop)
+        if (tid == 0) { a.n_evict[u] = 0; record_status(a.status, KVC_ERR_UNSUPPORTED); }
+        return;
+    }
     if (k > a.kmax) {
         if (tid == 0) { a.n_evict[u] = 0; record_status(a.status, KVC_ERR_SHAPE); }
         return;

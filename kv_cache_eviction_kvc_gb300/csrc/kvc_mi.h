@@ -12,4 +12,18 @@ namespace kvc {
 cudaError_t launch_mi_scores(const kvc_params &p, const kvc_cache &c, const kvc_moments &m,
                              int max_len, const double *probs, double *scores, cudaStream_t st);
 
+// MomentKV Algorithm 1 phase 1 for steps removing k = len - L > 0 slots:
+// k rounds of (scores over the slots present, argmin, fold); xbuf / lse are
+// the logits and log-partition functions of this step's attend pass.
+// evict_idx / evict_pos receive the victims in eviction order, n_evict = k;
+// the moments and the utilities (each slot's last score) are updated.
+// Units with len > kMiGreedyMaxSlots or k > kmax record KVC_ERR_SHAPE.
+constexpr int kMiGreedyMaxSlots = 8192;
+// rounds x slots a greedy call may take (host bound: O(rounds n d^2) work)
+constexpr long long kMiGreedyMaxWork = 1ll << 22;
+cudaError_t launch_mi_greedy(const kvc_params &p, const kvc_cache &c, const kvc_moments &m,
+                             const float *xbuf, const float *lse, int kmax, int32_t *evict_idx,
+                             int32_t *evict_pos, int32_t *n_evict, int32_t *status,
+                             cudaStream_t st);
+
 }  // namespace kvc

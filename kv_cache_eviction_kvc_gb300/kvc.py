@@ -28,7 +28,7 @@ EXPORTED = (
     "kvc_version", "kvc_last_error", "kvc_status_string",
     "kvc_decode_workspace_size", "kvc_decode_workspace_init", "kvc_get_device_status",
     "kvc_decode_attend", "kvc_aggregate_evict", "kvc_moment_update", "kvc_correct",
-    "kvc_compact", "kvc_zip_merge", "kvc_mi_scores", "kvc_decode_step", "kvc_decode_attend_noalloc", "kvc_prefill_prepare",
+    "kvc_compact", "kvc_zip_merge", "kvc_mi_scores", "kvc_mi_evict", "kvc_decode_step", "kvc_decode_attend_noalloc", "kvc_prefill_prepare",
     "kvc_prefill_workspace_size", "kvc_prefill_score",
 )
 
@@ -91,6 +91,7 @@ def load(build: bool = True):
         "kvc_compact": (I32, [PP, PC, I32, P, P, P, SZ, P]),
         "kvc_zip_merge": (I32, [PP, I32, P, PC, I32, P, P, P, P, SZ, P]),
         "kvc_mi_scores": (I32, [PP, PC, PM, I32, P, P, P]),
+        "kvc_mi_evict": (I32, [PP, I32, PC, PM, P, I32, P, P, P, P, SZ, P]),
         "kvc_decode_step": (I32, [PP, I32, I32, I32, P, P, P, PC, PM, P, P, I32, P, P, P, P, SZ, P]),
         "kvc_decode_attend_noalloc": (I32, [PP, I32, I32, I32, P, P, P, PC, P, P, P, P, P]),
         "kvc_prefill_prepare": (I32, [I32, I32, I32, I32, I32, P, P, P]),
@@ -241,6 +242,16 @@ def kvc_mi_scores(p, cache: kvc_cache, mom: kvc_moments, max_len, probs, scores,
     _check(load().kvc_mi_scores(
         ctypes.byref(p), ctypes.byref(cache), ctypes.byref(mom), int(max_len),
         _ptr(probs, f64, "probs"), _ptr(scores, f64, "scores"), _stream(stream)))
+
+
+def kvc_mi_evict(p, max_len, cache: kvc_cache, mom: kvc_moments, lse, kmax, evict_idx, evict_pos,
+                 n_evict, ws, stream=None):
+    i32 = torch.int32
+    _check(load().kvc_mi_evict(
+        ctypes.byref(p), int(max_len), ctypes.byref(cache), ctypes.byref(mom),
+        _ptr(lse, torch.float32, "lse"), int(kmax), _ptr(evict_idx, i32, "evict_idx"),
+        _ptr(evict_pos, i32, "evict_pos", optional=True), _ptr(n_evict, i32, "n_evict"),
+        _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
 
 
 def kvc_zip_merge(p, new_pos, q, cache: kvc_cache, kmax, evict_idx, n_evict, partner_pos, ws,

@@ -46,8 +46,8 @@ class DecodeState:
         self.logZ_R = torch.zeros(U, G, dtype=torch.float32, device=dev)
         self.n_evict = torch.zeros(U, dtype=torch.int32, device=dev)
         self.partner_pos = torch.full((U,), -1, dtype=torch.int32, device=dev)
-        self.mi = rule == K_.RULE_MI
-        self.scores = torch.zeros(U, cap, dtype=torch.float64, device=dev) if self.mi else None
+        self.scores = (torch.zeros(U, cap, dtype=torch.float64, device=dev)
+                       if rule == K_.RULE_MI else None)
         self.set_kmax(kmax)
 
     # --------------------------------------------------------------- helpers
@@ -100,13 +100,26 @@ class DecodeState:
     def step_calls(self, t: int, new_pos: int, q, k_new, v_new, max_len: int, stream=None):
         """The five entry points in order (attend, aggregate_evict,
         moment_update, correct, compact), with zip_merge after aggregate_evict
-        in merge mode and mi_scores before it under the moment-informed rule."""
+        in merge mode and mi_scores before it under the moment-informed rule
+        (mi_evict in place of scores, aggregate and fold when that rule
+        removes several slots)."""
         self.set_kmax(max_len - self.L)
         c = self.cache
         K_.kvc_decode_attend(self.params, t, new_pos, max_len, q, k_new, v_new, c, self.lse,
                              self.f_all, self.probs, self.ws, stream)
+        mi = self.params.rule == K_.RULE_MI          # the rule of this step
+        if mi and max_len - self.L > 1:
+            # MomentKV Algorithm 1's loop: score, evict the lowest, fold, again
+            K_.kvc_mi_evict(self.params, max_len, c, self.moments, self.lse, self.kmax,
+                            self.evict_idx, self.evict_pos, self.n_evict, self.ws, stream)
+            K_.kvc_correct(self.params, q, c, self.kmax, self.evict_idx, self.n_evict, self.lse,
+                           self.f_all, self.moments, self.o, self.f_R, self.logZ_R, self.ws,
+                           stream)
+            K_.kvc_compact(self.params, c, self.kmax, self.evict_idx, self.n_evict, self.ws,
+                           stream)
+            return
         agg_in = self.probs
-        if self.mi:
+        if mi:
             K_.kvc_mi_scores(self.params, c, self.moments, max_len, self.probs, self.scores, stream)
             agg_in = self.scores
         K_.kvc_aggregate_evict(self.params, t, agg_in, c, self.kmax, self.evict_idx,

@@ -67,6 +67,7 @@ class DecodeConfig:
     outliers: int = 0
     outlier_mult: float = 8.0
     merge_recent: int | None = None   # KeepKV ZIP-merging, last R positions excluded
+    first_rule: int | None = None     # rule of the first decode step (None: ``rule``)
     description: str = ""
 
     @property
@@ -146,10 +147,16 @@ C2_SCORE_FREE = C2.with_(name="C2-qwen3-4b-score-free", T=0,
 C2_ZIP = C2.with_(name="C2-qwen3-4b-zip", merge_recent=32,
                   description=C2.description + ", KeepKV ZIP-merging (R = 32)")
 
-# MomentKV's moment-informed eviction (alpha ||r|| every step) on the same shape
-C2_MI = C2.with_(name="C2-qwen3-4b-mi", rule=RULE_MI, T=1,
-                 description=C2.description.replace("lazy refresh every 8 steps",
-                                                    "MomentKV moment-informed eviction every step"))
+# MomentKV's moment-informed eviction (alpha ||r|| every step) on the same
+# shape.  The 32768-token prompt is first brought to the budget by one
+# attention-scored eviction at the first decode step (MomentKV's own setup
+# compresses the prompt before decoding, with the SnapKV protocol); the
+# moment-aware loop then removes one slot per step.
+C2_MI = C2.with_(name="C2-qwen3-4b-mi", rule=RULE_MI, T=1, first_rule=RULE_EMA,
+                 description=C2.description.replace(
+                     "lazy refresh every 8 steps",
+                     "prompt compressed by attention at step 1, then MomentKV "
+                     "moment-informed eviction every step"))
 
 DECODE_CONFIGS = {"C0": C0, "C1": C1, "C2": C2, "C4": C4,
                   "C2-score-free": C2_SCORE_FREE, "C2-zip": C2_ZIP, "C2-mi": C2_MI}

@@ -25,9 +25,10 @@ inputs step by step.  Each step compares:
   the oracle then adopts the GPU's rows;
 * under MomentKV's moment-informed rule, the step's scores alpha ||r|| (the
   utilities of the retained slots, by position) within 2e-3 relative (floor:
-  1e-4 of the unit's largest score), and eviction near-ties within 1e-4 of
-  the threshold score (the GPU forms the residuals with fp32 sums of 128
-  products).
+  1e-4 of the unit's largest score); the oracle replays the GPU's victims
+  round by round (MomentKV Algorithm 1 removes one slot per round and
+  re-scores), and each must score within 1e-4 of that round's lowest score
+  (the scores are functions of the moments, whose tolerance is 1e-4).
 """
 from __future__ import annotations
 
@@ -65,6 +66,8 @@ class ParityReport:
     merges: int = 0
     max_row_err: float = 0.0      # merged rows, in bf16 units of the reference
     max_mi_err: float = 0.0       # moment-informed scores (retained slots)
+    mi_rounds: int = 0            # moment-aware eviction rounds compared
+    max_mi_gap: float = 0.0       # largest accepted relative score gap of a round
     first_mismatch: str = ""
 
     def ok(self):
@@ -85,8 +88,6 @@ def run_decode_parity(cfg: W.DecodeConfig, *, steps: int | None = None, units=No
                       cap: int | None = None) -> ParityReport:
     S = cfg.steps if steps is None else steps
     merge = cfg.merge_recent is not None
-    mi = cfg.rule == W.RULE_MI
-    tie_rel = MI_TIE_REL if mi else TIE_REL
     U, G, d, N, L = cfg.U, cfg.G, cfg.d, cfg.N, cfg.L
     units = list(range(U)) if units is None else list(units)
     uidx = torch.tensor(units, device=device, dtype=torch.long)
@@ -111,7 +112,11 @@ def run_decode_parity(cfg: W.DecodeConfig, *, steps: int | None = None, units=No
             inp = W.gen_step(cfg, device, t, seed, P)
             new_pos = N + t - 1
             max_len = n_len + 1
-            refresh = O.is_refresh(t, cfg.T)
+            rule = cfg.first_rule if (t == 1 and cfg.first_rule is not None) else cfg.rule
+            mi = rule == W.RULE_MI
+            tie_rel = MI_TIE_REL if mi else TIE_REL
+            st.params.rule = rule
+            refresh = True if mi else O.is_refresh(t, cfg.T)
             pos_before = st.pos[uidx, :max_len].cpu().numpy().copy()
             votes_before = st.votes[uidx, :max_len].cpu().numpy().copy() if merge else None
             len_before = st.len[uidx].cpu().numpy().copy()
@@ -171,15 +176,43 @@ def run_decode_parity(cfg: W.DecodeConfig, *, steps: int | None = None, units=No
                     out[j, : len(gl)] = gl
                 return out, nev.astype(np.int32)
 
+            mi_forced = None
+            if mi:
+                # the GPU's victims in eviction order, replayed round by round
+                kf = max(1, int(nev.max()))
+                mi_forced = np.full((len(units), kf), -1, np.int32)
+                for j in range(len(units)):
+                    mi_forced[j, : nev[j]] = evp[j, : nev[j]]
             try:
-                prop = O.decode_step(sess, t, new_pos, qh, kh, vh2, L=L, rule=cfg.rule,
+                prop = O.decode_step(sess, t, new_pos, qh, kh, vh2, L=L, rule=rule,
                                      alpha=cfg.alpha, T=cfg.T, correction=cfg.correction,
-                                     choose=choose, merge_recent=cfg.merge_recent,
-                                     force_partner=partner_g)
+                                     choose=None if mi else choose,
+                                     merge_recent=cfg.merge_recent,
+                                     force_partner=partner_g, mi_forced=mi_forced)
             except ValueError as ex:
                 rep.mismatches += 1
                 rep.first_mismatch = rep.first_mismatch or f"step {t}: oracle refused: {ex}"
                 break
+            if mi:
+                for j in range(len(units)):
+                    if prop["nvict"][j] != nev[j]:
+                        rep.mismatches += 1
+                        rep.first_mismatch = rep.first_mismatch or (
+                            f"step {t} unit {units[j]}: gpu removed {nev[j]}, "
+                            f"oracle {prop['nvict'][j]}")
+                        continue
+                    for r in range(int(nev[j])):
+                        b_, u_ = prop["mi_best"][j, r], prop["mi_used"][j, r]
+                        rep.mi_rounds += 1
+                        gap = (u_ - b_) / max(abs(b_), 1e-300)
+                        if gap > MI_TIE_REL:
+                            rep.mismatches += 1
+                            rep.first_mismatch = rep.first_mismatch or (
+                                f"step {t} unit {units[j]} round {r}: gpu victim "
+                                f"{mi_forced[j, r]} scores {u_!r}, the lowest is {b_!r}")
+                        elif gap > 0:
+                            rep.band_hits += 1
+                            rep.max_mi_gap = max(rep.max_mi_gap, float(gap))
             if merge:
                 _check_merge(rep, t, units, st, uidx, sess, prop, partner_g)
             # output
@@ -224,6 +257,7 @@ def run_decode_parity(cfg: W.DecodeConfig, *, steps: int | None = None, units=No
                 rep.max_mu_err = max(rep.max_mu_err, _rel(mk_g[j], mk_r[j]), _rel(mv_g[j], mv_r[j]))
                 rep.max_C_err = max(rep.max_C_err, _rel(C_g[j], C_r[j]))
             n_len = int(st.len.max().item())
+            st.params.rule = cfg.rule
             rep.steps += 1
     finally:
         sess.close()

@@ -148,3 +148,22 @@ def test_noalloc_rejects_bad_buffers_like_attend():
     p = K.make_params(U=2, G=4, cap=100, L=10)
     for kw in ({"K": None}, {"K": 18}, {"max_len": 101}, {"t": 0}):
         assert _lib_call_attend_noalloc(p, **kw) == _lib_call_attend(p, **kw) != 0
+
+
+def test_long_moment_informed_first_step_refused_on_host():
+    """MomentKV's loop re-scores the whole cache after every fold: a step
+    that would remove thousands of slots from a long prompt is refused
+    before any launch (KVC_ERR_UNSUPPORTED), by kvc_decode_step and by
+    kvc_mi_evict alike; a combination of the rule with merging is invalid."""
+    lib = K.load()
+    p = K.make_params(U=2, G=4, cap=40000, L=100, rule=K.RULE_MI, refresh_period=1)
+    cache = K.kvc_cache(16, 32, None, 64, 128, 256)
+    mom = K.kvc_moments(16, 32, 64, 128)
+    rc = lib.kvc_decode_step(ctypes.byref(p), 1, 0, 32769, 16, 16, 16, ctypes.byref(cache),
+                             ctypes.byref(mom), 16, None, 40000, 16, None, 16, 256, 1 << 40, None)
+    assert rc == 5 and "rounds" in K.kvc_last_error()
+    rc = lib.kvc_mi_evict(ctypes.byref(p), 32769, ctypes.byref(cache), ctypes.byref(mom), 16,
+                          40000, 16, None, 16, 256, 1 << 40, None)
+    assert rc == 5
+    p2 = K.make_params(U=2, G=4, cap=100, L=10, rule=K.RULE_MI, refresh_period=1, merge_recent=4)
+    assert _lib_call_attend(p2) == 1 and "merging" in K.kvc_last_error()

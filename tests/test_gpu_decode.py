@@ -102,14 +102,43 @@ def test_zip_merge_c2_sampled_full_size(fused):
 
 
 @pytest.mark.parametrize("cfg", [
-    SMALL.with_(rule=W.RULE_MI),                                     # MomentKV moment-informed
+    SMALL.with_(rule=W.RULE_MI),                                     # 651 rounds at step 1
     SMALL.with_(rule=W.RULE_MI, Hq=2, Hkv=2, N=300, L=20, votes_max=4),   # G = 1, votes
     SMALL.with_(rule=W.RULE_MI, k_dist="mixture", centres=8, correction=W.CORR_ZERO_ORDER),
-], ids=["mi", "mi-G1-votes", "mi-mixture"])
+    SMALL.with_(rule=W.RULE_MI, Hq=16, Hkv=2, N=129, L=126, steps=8, votes_max=3),  # k = 4, G = 8
+    W.C0.with_(rule=W.RULE_MI, steps=12),                            # the tiny workload, 449 rounds
+], ids=["mi", "mi-G1-votes", "mi-mixture", "mi-k4-G8-votes", "mi-c0"])
 @pytest.mark.parametrize("fused", [True, False])
 def test_moment_informed(cfg, fused):
-    check(run_decode_parity(cfg, fused=fused))
+    """MomentKV's moment-aware phase: a first step removing several slots
+    runs the loop of Algorithm 1 (kvc_mi_evict), later steps one round; the
+    oracle replays the GPU's victims round by round."""
+    rep = run_decode_parity(cfg, fused=fused)
+    check(rep)
+    assert rep.mi_rounds >= (cfg.N + 1 - cfg.L) * cfg.U
 
 
 def test_moment_informed_c2_sampled_full_size():
-    check(run_decode_parity(W.C2_MI, units=sample_units(W.C2.U), steps=6))
+    rep = run_decode_parity(W.C2_MI, units=sample_units(W.C2.U), steps=6)
+    check(rep)
+    assert rep.mi_rounds == 64 * 5
+
+
+def test_aggregate_refuses_one_shot_moment_informed_eviction():
+    """kvc_aggregate_evict under the moment-informed rule evicts one slot per
+    unit; a unit that would lose several is refused on the device
+    (KVC_ERR_UNSUPPORTED) and loses nothing: the loop is kvc_mi_evict's."""
+    from kv_cache_eviction_kvc_gb300 import kvc as K
+    from kv_cache_eviction_kvc_gb300.state import DecodeState
+    cfg = SMALL.with_(N=60, L=50)
+    st = DecodeState(2, 4, 80, 50, rule=W.RULE_MI, kmax=16)
+    pre = W.gen_prefill(cfg.with_(B=1, NL=1, Hkv=2, Hq=8), "cuda", 0, cap=80)
+    st.load_prefill(pre["K"], pre["V"], None, pre["pos"], pre["len"])
+    inp = W.gen_step(cfg.with_(B=1, NL=1, Hkv=2, Hq=8), "cuda", 1)
+    K.kvc_decode_attend(st.params, 1, 60, 61, inp["q"], inp["k_new"], inp["v_new"], st.cache,
+                        st.lse, st.f_all, st.probs, st.ws)
+    K.kvc_aggregate_evict(st.params, 1, st.probs, st.cache, st.kmax, st.evict_idx, st.evict_pos,
+                          st.n_evict, st.ws)
+    torch.cuda.synchronize()
+    assert st.device_status() == 5
+    assert st.n_evict.tolist() == [0, 0]
