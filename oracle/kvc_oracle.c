@@ -363,17 +363,18 @@ static int key_cmp(const void *a, const void *b)
  * ascending) order; unscored slots are never candidates.  Writes victim
  * positions in that order to victims [U][kmax], their count to nvict [U],
  * and the k-th (largest evicted) utility to thr [U] (0 when k = 0).
+ * Lu [U] (or NULL): a budget per unit in place of L.
  * Returns 0, or -1 if some unit has fewer than k scored slots or k > kmax.
  */
 int ocl_select(void *h, int L, int kmax, int32_t *victims, int32_t *nvict,
-               double *thr)
+               double *thr, const int32_t *Lu)
 {
     ocl_session *s = (ocl_session *)h;
     int rc = 0;
     for (int u = 0; u < s->U; u++) {
         size_t base = (size_t)u * s->cap;
-        int n = s->n[u];
-        int k = n > L ? n - L : 0;
+        int n = s->n[u], Lb = Lu ? Lu[u] : L;
+        int k = n > Lb ? n - Lb : 0;
         nvict[u] = 0;
         if (thr) thr[u] = 0.0;
         if (k == 0) continue;
@@ -484,14 +485,15 @@ int ocl_evict(void *h, const int32_t *victims, const int32_t *nvict, int kmax)
  */
 int ocl_mi_greedy(void *h, const uint16_t *q, int L, int kmax, const int32_t *forced,
                   int32_t *victims, int32_t *nvict, double *best, double *used,
-                  double *scores0)
+                  double *scores0, const int32_t *Lu)
 {
     ocl_session *s = (ocl_session *)h;
     int rc = 0;
 #pragma omp parallel for schedule(dynamic, 1) reduction(min : rc)
     for (int u = 0; u < s->U; u++) {
         size_t base = (size_t)u * s->cap;
-        int k = s->n[u] > L ? s->n[u] - L : 0;
+        int Lb = Lu ? Lu[u] : L;
+        int k = s->n[u] > Lb ? s->n[u] - Lb : 0;
         nvict[u] = 0;
         if (k > kmax) { rc = -1; continue; }
         double *pr = (double *)malloc((size_t)s->cap * sizeof(double));
@@ -896,17 +898,19 @@ void ocl_prefill_colnorm(int NL, int Hq, int Hkv, int d, int N, int w,
 }
 
 /*
- * KeepKV's windowed EMA initialization of the utilities [KeepKV reading
- * notes, eq 15 at the end of the prefill: S = sum over the last window of
- * queries of (1 - alpha) alpha^(age) s^k]: with the same causal window
- * attention as above (query j of w at position N - w + j, A_bar the group
- * mean of the head probabilities),
- *   S_i = sum_{j=0}^{w-1} (1 - alpha) alpha^(w-1-j) A_bar[j, i],
- * the last window query weighing (1 - alpha).  q_win: [NL][Hq][w][d];
- * K: [NL][Hkv][N][d]; S: [NL][Hkv][N].
+ * Weighted column sum of the group-mean window attention: with the causal
+ * window attention of the LaProx column norm (query j of w at position
+ * N - w + j sees keys 0..N-w+j; A^h the row softmax of q K^T / sqrt(d);
+ * A_bar the mean over the group's G query heads),
+ *   S_i = sum_{j=0}^{w-1} roww[j] A_bar[j, i].
+ * With roww = 1 this is SnapKV's attention accumulated over the observation
+ * window [MomentKV sec A4 setup, "SnapKV prefill protocol"]; with the
+ * weights below it is KeepKV's windowed EMA initialization.
+ * q_win: [NL][Hq][w][d]; K: [NL][Hkv][N][d]; roww: [w]; S: [NL][Hkv][N].
  */
-void ocl_prefill_ema_init(int NL, int Hq, int Hkv, int d, int N, int w, double alpha,
-                          const uint16_t *q_win, const uint16_t *K, double *S)
+void ocl_prefill_window_colsum(int NL, int Hq, int Hkv, int d, int N, int w,
+                               const double *roww, const uint16_t *q_win,
+                               const uint16_t *K, double *S)
 {
     int G = Hq / Hkv;
     double rsd = 1.0 / sqrt((double)d);
@@ -918,7 +922,7 @@ void ocl_prefill_ema_init(int NL, int Hq, int Hkv, int d, int N, int w, double a
             double *x = (double *)malloc((size_t)N * sizeof(double));
             for (int i = 0; i < N; i++) Sg[i] = 0.0;
             for (int j = 0; j < w; j++) {
-                double wj = (1.0 - alpha) * pow(alpha, (double)(w - 1 - j));
+                double wj = roww[j];
                 int last = N - w + j;
                 for (int hh = g * G; hh < (g + 1) * G; hh++) {
                     const uint16_t *qj = &q_win[(((size_t)l * Hq + hh) * w + j) * d];
@@ -938,6 +942,48 @@ void ocl_prefill_ema_init(int NL, int Hq, int Hkv, int d, int N, int w, double a
             }
             free(x);
         }
+}
+
+/*
+ * KeepKV's windowed EMA initialization of the utilities [KeepKV reading
+ * notes, eq 15 at the end of the prefill: S = sum over the last window of
+ * queries of (1 - alpha) alpha^(age) s^k]: the weighted column sum above
+ * with roww[j] = (1 - alpha) alpha^(w-1-j), the last window query weighing
+ * (1 - alpha).
+ */
+void ocl_prefill_ema_init(int NL, int Hq, int Hkv, int d, int N, int w, double alpha,
+                          const uint16_t *q_win, const uint16_t *K, double *S)
+{
+    double *roww = (double *)malloc((size_t)(w > 0 ? w : 1) * sizeof(double));
+    for (int j = 0; j < w; j++) roww[j] = (1.0 - alpha) * pow(alpha, (double)(w - 1 - j));
+    ocl_prefill_window_colsum(NL, Hq, Hkv, d, N, w, roww, q_win, K, S);
+    free(roww);
+}
+
+/*
+ * SnapKV's scores under MomentKV's prefill protocol [MomentKV sec A4
+ * setup: attention accumulated over the observation window, the first
+ * token kept as the attention sink, adjacent tokens merged into blocks of
+ * 4 before scoring]: acc is the accumulated window attention [NL][Hkv][N];
+ * each block of `pool` consecutive positions [b pool, (b + 1) pool) takes
+ * the mean of its tokens' acc and every token of the block that score; with
+ * sink != 0 position 0 scores +infinity (always kept).  s: [NL][Hkv][N].
+ */
+void ocl_snapkv_scores(int NL, int Hkv, int N, int pool, int sink, const double *acc,
+                       double *s)
+{
+    for (size_t u = 0; u < (size_t)NL * Hkv; u++) {
+        const double *a = &acc[u * N];
+        double *o = &s[u * N];
+        for (int b0 = 0; b0 < N; b0 += pool) {
+            int b1 = b0 + pool < N ? b0 + pool : N;
+            double m = 0.0;
+            for (int i = b0; i < b1; i++) m += a[i];
+            m /= (double)(b1 - b0);
+            for (int i = b0; i < b1; i++) o[i] = m;
+        }
+        if (sink && N > 0) o[0] = INFINITY;
+    }
 }
 
 /*

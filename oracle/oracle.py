@@ -69,16 +69,18 @@ def _load():
             "ocl_attend": (None, [P, P, P, P, P]),
             "ocl_update_util": (None, [P, P, I, D]),
             "ocl_get_slots": (None, [P, P, P, P, P, P]),
-            "ocl_select": (I, [P, I, I, P, P, P]),
+            "ocl_select": (I, [P, I, I, P, P, P, P]),
             "ocl_evict": (I, [P, P, P, I]),
             "ocl_zip_merge": (I, [P, P, P, ctypes.c_int32, I, D, P, P, P, P, P, P, P, P]),
             "ocl_set_row": (I, [P, I, ctypes.c_int32, P, P]),
             "ocl_get_rows": (None, [P, P, P]),
             "ocl_moments": (None, [P, P, P, P, P]),
             "ocl_mi_scores": (None, [P, P, P]),
-            "ocl_mi_greedy": (I, [P, P, I, I, P, P, P, P, P, P]),
+            "ocl_mi_greedy": (I, [P, P, I, I, P, P, P, P, P, P, P]),
             "ocl_set_util": (I, [P, I, I, P]),
             "ocl_prefill_ema_init": (None, [I, I, I, I, I, I, D, P, P, P]),
+            "ocl_prefill_window_colsum": (None, [I, I, I, I, I, I, P, P, P, P]),
+            "ocl_snapkv_scores": (None, [I, I, I, I, I, P, P]),
             "ocl_output": (None, [P, P, I, P, P, P]),
             "ocl_prefill_gram": (None, [I, I, I, I, I, P, P]),
             "ocl_prefill_colnorm": (None, [I, I, I, I, I, I, P, P, P]),
@@ -192,12 +194,15 @@ class DecodeSession:
         self.lib.ocl_get_slots(self.h, _p(n), _p(pos), _p(vote), _p(util), _p(scored))
         return n, pos, vote, util, scored
 
-    def select(self, L: int, kmax: int):
-        """Oracle's victims: (positions [U][kmax], count [U], threshold [U])."""
+    def select(self, L, kmax: int):
+        """Oracle's victims: (positions [U][kmax], count [U], threshold [U]).
+        L: one budget, or one per unit ([U])."""
         vic = np.full((self.U, max(kmax, 1)), -1, np.int32)
         nv = np.zeros(self.U, np.int32)
         thr = np.zeros(self.U)
-        rc = self.lib.ocl_select(self.h, int(L), max(kmax, 1), _p(vic), _p(nv), _p(thr))
+        Lu = None if np.isscalar(L) else np.ascontiguousarray(L, dtype=np.int32)
+        rc = self.lib.ocl_select(self.h, int(L) if Lu is None else 0, max(kmax, 1), _p(vic),
+                                 _p(nv), _p(thr), _p(Lu))
         if rc != 0:
             raise ValueError("ocl_select: not enough scored slots or kmax too small")
         return vic, nv, thr
@@ -256,7 +261,7 @@ class DecodeSession:
         self.lib.ocl_mi_scores(self.h, _p(probs), _p(out))
         return out
 
-    def mi_greedy(self, q, L: int, kmax: int, forced=None):
+    def mi_greedy(self, q, L, kmax: int, forced=None):
         """MomentKV Algorithm 1 phase 1 on every unit: while a unit holds more
         than L slots, score every slot (alpha ||r|| with alpha re-formed over
         the slots present and the moments as they stand), evict the lowest
@@ -273,9 +278,11 @@ class DecodeSession:
         out = dict(victims=np.full((self.U, kmax), -1, np.int32),
                    nvict=np.zeros(self.U, np.int32), best=np.zeros((self.U, kmax)),
                    used=np.zeros((self.U, kmax)), scores0=np.zeros((self.U, self.cap)))
-        rc = self.lib.ocl_mi_greedy(self.h, _p(qb), int(L), kmax, _p(forced),
-                                    _p(out["victims"]), _p(out["nvict"]), _p(out["best"]),
-                                    _p(out["used"]), _p(out["scores0"]))
+        Lu = None if np.isscalar(L) else np.ascontiguousarray(L, dtype=np.int32)
+        rc = self.lib.ocl_mi_greedy(self.h, _p(qb), int(L) if Lu is None else 0, kmax,
+                                    _p(forced), _p(out["victims"]), _p(out["nvict"]),
+                                    _p(out["best"]), _p(out["used"]), _p(out["scores0"]),
+                                    _p(Lu))
         if rc != 0:
             raise ValueError("ocl_mi_greedy: kmax too small or a forced position is not present")
         return out
@@ -316,7 +323,7 @@ def is_refresh(t: int, T: int) -> bool:
 
 
 def decode_step(sess: DecodeSession, t: int, new_pos: int, q, knew, vnew, *,
-                L: int, rule: int, alpha: float, T: int, correction: int,
+                L, rule: int, alpha: float, T: int, correction: int,
                 choose=None, merge_recent: int | None = None, force_partner=None,
                 mi_forced=None):
     """One decode step on every unit of ``sess``, in the order of MomentKV
@@ -336,6 +343,9 @@ def decode_step(sess: DecodeSession, t: int, new_pos: int, q, knew, vnew, *,
     ``mi_forced`` [U][kmax] (positions in eviction order) replays another
     implementation's choices; the result's ``mi_best`` / ``mi_used`` give
     each round's lowest score and the score of the slot removed.
+
+    ``L`` is one budget or one per unit ([U]; a cache handed over from a
+    prefill scorer keeps each unit at its own length).
 
     ``choose(t, proposal)``, if given, receives the oracle's proposal dict and
     returns the victim positions to apply ([U][kmax], [U]); tests use it to
@@ -359,7 +369,7 @@ def decode_step(sess: DecodeSession, t: int, new_pos: int, q, knew, vnew, *,
         if merge_recent is not None:
             raise ValueError("the moment-informed rule evicts; it is not combined with merging")
         n = sess.slots()[0]
-        kmax = int(max(1, (n - L).max()))
+        kmax = int(max(1, (n - np.asarray(L)).max()))
         if mi_forced is not None:
             mi_forced = np.asarray(mi_forced)
             kmax = max(kmax, mi_forced.shape[1])
@@ -378,7 +388,7 @@ def decode_step(sess: DecodeSession, t: int, new_pos: int, q, knew, vnew, *,
         if refresh:
             sess.update_util(probs, rule, alpha)
         n = sess.slots()[0]
-        kmax = int(max(1, (n - L).max()))
+        kmax = int(max(1, (n - np.asarray(L)).max()))
         vic, nv, thr = sess.select(L, kmax)
         proposal = dict(victims=vic, nvict=nv, thr=thr, lse=lse, f_all=f_all,
                         probs=probs if refresh else None, refresh=refresh, mi_scores=None)
@@ -508,6 +518,41 @@ def prefill_ema_init(q_win, K, NL: int, Hq: int, Hkv: int, d: int, N: int, w: in
     S = np.zeros((NL, Hkv, N))
     _load().ocl_prefill_ema_init(NL, Hq, Hkv, d, N, w, float(alpha), _p(qb), _p(kb), _p(S))
     return S
+
+
+def prefill_window_colsum(q_win, K, NL: int, Hq: int, Hkv: int, d: int, N: int, w: int,
+                          roww) -> np.ndarray:
+    """Weighted column sum of the group-mean window attention,
+    S [NL][Hkv][N] (see ocl_prefill_window_colsum)."""
+    qb, kb = _bits(q_win), _bits(K)
+    roww = np.ascontiguousarray(roww, dtype=np.float64)
+    assert roww.shape == (w,)
+    S = np.zeros((NL, Hkv, N))
+    _load().ocl_prefill_window_colsum(NL, Hq, Hkv, d, N, w, _p(roww), _p(qb), _p(kb), _p(S))
+    return S
+
+
+def snapkv_scores(acc, pool: int = 4, sink: bool = True) -> np.ndarray:
+    """SnapKV scores under MomentKV's prefill protocol: block means of the
+    accumulated window attention, sink at position 0 (see ocl_snapkv_scores)."""
+    acc = np.ascontiguousarray(acc, dtype=np.float64)
+    NL, Hkv, N = acc.shape
+    s = np.zeros_like(acc)
+    _load().ocl_snapkv_scores(NL, Hkv, N, int(pool), int(bool(sink)), _p(acc), _p(s))
+    return s
+
+
+def prefill_snapkv(q_win, K, *, NL: int, Hq: int, Hkv: int, d: int, N: int, w: int,
+                   B_total: int, pool: int = 4, sink: bool = True):
+    """MomentKV's SnapKV prefill protocol: attention accumulated over the
+    observation window, block pooling, the sink kept, and each layer's
+    budget B_total / NL shared by its heads (adaptive per-head allocation
+    within the layer)."""
+    acc = prefill_window_colsum(q_win, K, NL, Hq, Hkv, d, N, w, np.ones(w))
+    sc = snapkv_scores(acc, pool, sink)
+    res = prefill_select(sc, np.ones_like(sc), B_total, normalize=False, alloc=ALLOC_LAYER)
+    res.update(acc=acc, scores=sc)
+    return res
 
 
 def prefill_score(q_win, K, V, W_O, *, NL: int, Hq: int, Hkv: int, d: int,

@@ -683,3 +683,27 @@ def test_mi_generation_evicts_the_lowest_score():
                 assert r["applied_victims"][u, 0] == pos[want]
             assert r["mi_used"][u, :k].tolist() == r["mi_best"][u, :k].tolist()
     sess.close()
+
+
+def test_per_unit_budgets_select_like_single_units():
+    """Budgets per unit (a cache handed over from a prefill scorer keeps each
+    unit at its own length) select, per unit, what a one-unit session with
+    that budget selects."""
+    rng = np.random.default_rng(51)
+    U, n, d = 3, 12, 4
+    Lu = np.array([9, 11, 5], np.int32)
+    k, v = bf(rng.normal(size=(U, n, d))), bf(rng.normal(size=(U, n, d)))
+    util = rng.random((U, n))
+    s = O.DecodeSession(U, 1, d, n + 2)
+    for u in range(U):
+        s.load(u, k[u], v[u])
+        s.set_util(u, util[u])
+    vic, nv, _ = s.select(Lu, 8)
+    for u in range(U):
+        one = make_session(k[u], v[u])
+        one.set_util(0, util[u])
+        v1, n1, _ = one.select(int(Lu[u]), 8)
+        assert nv[u] == n1[0] == n - Lu[u]
+        assert vic[u, : nv[u]].tolist() == v1[0, : n1[0]].tolist()
+        one.close()
+    s.close()

@@ -247,3 +247,89 @@ def test_initialized_utilities_continue_the_ema_at_step_one():
     np.testing.assert_allclose(util[0, :6], 0.9 * m0 + 0.1 * probs[0, :6], rtol=1e-15)
     assert scored[0, :6].all()
     s.close()
+
+
+# ------------------------------------------------------- SnapKV protocol
+
+def test_window_colsum_unit_weights_sum_to_the_window():
+    """With every row weight 1 (SnapKV's accumulated window attention) each
+    window row's group-mean softmax sums to 1 over the keys it sees, so the
+    accumulated scores of a (layer, KV head) sum to w."""
+    rng = np.random.default_rng(41)
+    NL, Hq, Hkv, d, N, w = 2, 8, 2, 16, 40, 6
+    q = bf(rng.normal(size=(NL, Hq, w, d)))
+    K = bf(rng.normal(size=(NL, Hkv, N, d)))
+    S = O.prefill_window_colsum(q, K, NL, Hq, Hkv, d, N, w, np.ones(w))
+    np.testing.assert_allclose(S.sum(axis=2), w, rtol=1e-13)
+
+
+def test_window_colsum_single_row_is_scipy_group_softmax():
+    """A weight vector selecting window row j alone gives the group mean of
+    the G heads' causal softmax of that row (scipy), keys past its position
+    zero; a weighted sum is linear in the weights."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(42)
+    NL, Hq, Hkv, d, N, w = 1, 4, 1, 8, 24, 5
+    q = bf(rng.normal(size=(NL, Hq, w, d)))
+    K = bf(rng.normal(size=(NL, Hkv, N, d)))
+    j = 2
+    e = np.zeros(w); e[j] = 1.0
+    S = O.prefill_window_colsum(q, K, NL, Hq, Hkv, d, N, w, e)
+    last = N - w + j
+    ref = np.mean([softmax(q[0, h, j] @ K[0, 0, : last + 1].T / math.sqrt(d)) for h in range(Hq)],
+                  axis=0)
+    np.testing.assert_allclose(S[0, 0, : last + 1], ref, rtol=1e-12)
+    assert not S[0, 0, last + 1:].any()
+    wts = rng.random(w)
+    Sw = O.prefill_window_colsum(q, K, NL, Hq, Hkv, d, N, w, wts)
+    parts = sum(wts[jj] * O.prefill_window_colsum(q, K, NL, Hq, Hkv, d, N, w, np.eye(w)[jj])
+                for jj in range(w))
+    np.testing.assert_allclose(Sw, parts, rtol=1e-12)
+
+
+def test_ema_init_is_the_colsum_with_ema_weights():
+    rng = np.random.default_rng(43)
+    NL, Hq, Hkv, d, N, w, al = 1, 8, 2, 8, 30, 7, 0.8
+    q = bf(rng.normal(size=(NL, Hq, w, d)))
+    K = bf(rng.normal(size=(NL, Hkv, N, d)))
+    wts = (1 - al) * al ** (w - 1 - np.arange(w))
+    np.testing.assert_allclose(O.prefill_ema_init(q, K, NL, Hq, Hkv, d, N, w, al),
+                               O.prefill_window_colsum(q, K, NL, Hq, Hkv, d, N, w, wts),
+                               rtol=1e-14)
+
+
+@pytest.mark.parametrize("N,pool", [(17, 4), (16, 4), (9, 1), (5, 8)])
+def test_snapkv_block_means_and_sink(N, pool):
+    """Blocks of `pool` consecutive positions take the mean of their tokens'
+    accumulated attention (a ragged last block its own mean); the sink at
+    position 0 scores +infinity; no sink leaves block 0 its mean."""
+    rng = np.random.default_rng(44 + N)
+    acc = rng.random((2, 3, N))
+    s = O.snapkv_scores(acc, pool, sink=True)
+    s0 = O.snapkv_scores(acc, pool, sink=False)
+    for l, g in itertools.product(range(2), range(3)):
+        for i in range(N):
+            b = i // pool
+            blk = acc[l, g, b * pool: min(N, (b + 1) * pool)]
+            assert s0[l, g, i] == pytest.approx(blk.sum() / len(blk), rel=1e-15)
+            if i > 0:
+                assert s[l, g, i] == s0[l, g, i]
+        assert s[l, g, 0] == math.inf
+
+
+def test_snapkv_selection_keeps_sinks_and_splits_budgets_by_layer():
+    """The protocol's selection: every layer keeps B_total / NL tokens over
+    its KV heads (adaptive per-head budgets within the layer), the sink of
+    every head first, then the highest pooled scores (brute-force sort)."""
+    rng = np.random.default_rng(45)
+    NL, Hq, Hkv, d, N, w, B = 2, 8, 2, 8, 40, 8, 24
+    q = bf(rng.normal(size=(NL, Hq, w, d)))
+    K = bf(rng.normal(size=(NL, Hkv, N, d)))
+    res = O.prefill_snapkv(q, K, NL=NL, Hq=Hq, Hkv=Hkv, d=d, N=N, w=w, B_total=B)
+    keep = res["keep"].astype(bool)
+    assert keep.reshape(NL, -1).sum(axis=1).tolist() == [B // NL] * NL
+    assert keep[:, :, 0].all()
+    for l in range(NL):
+        sc = res["scores"][l].ravel()
+        order = sorted(range(sc.size), key=lambda j: (-sc[j], j))[: B // NL]
+        assert sorted(order) == np.nonzero(keep[l].ravel())[0].tolist()
