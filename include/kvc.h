@@ -57,7 +57,7 @@
 extern "C" {
 #endif
 
-#define KVC_VERSION 10000  /* major*10000 + minor*100 + patch */
+#define KVC_VERSION 10100  /* major*10000 + minor*100 + patch */
 
 /* Exported symbols (the library is built with hidden default visibility). */
 #if defined(__GNUC__)
@@ -105,6 +105,18 @@ typedef struct {
                                 (KeepKV; see kvc_zip_merge); needs votes     */
     int32_t merge_recent;    /* R >= 0: merge partners exclude the last R
                                 token positions (KeepKV candidate choice)    */
+    const int32_t *budget;   /* NULL, or a DEVICE array [U]: the budget of
+                                each unit (1 <= budget[u] <= L; L is then
+                                the largest), e.g. the variable per-head
+                                budgets a prefill selection hands over
+                                (LaProx key design 3, MomentKV's adaptive
+                                per-head allocation; kvc_prefill_handoff).
+                                A unit outside [1, L] records KVC_ERR_SHAPE
+                                and is left untouched.  Wherever the other
+                                entry points say L of a unit, they mean
+                                budget[u].  The fused steady state runs when
+                                max_len == L + 1 and every unit enters at
+                                its own budget.                              */
 } kvc_params;
 
 /* Guard of the ZIP-merge key formula: below this |weighted mean logit| the
@@ -448,6 +460,56 @@ KVC_API kvc_status kvc_decode_attend_noalloc(const kvc_params *p, int32_t t,
                                              int32_t *device_status, void *stream);
 
 /* ------------------------------------------------------------------ */
+/* prefill -> decode hand-off                                           */
+/* ------------------------------------------------------------------ */
+
+/* Bytes of workspace kvc_prefill_handoff needs for U units of N prompt
+ * tokens. */
+KVC_API size_t kvc_prefill_handoff_workspace_size(int32_t U, int32_t N);
+
+/*
+ * kvc_prefill_handoff -- start a decode stream from a prefill selection.
+ *
+ * Defined by: LaProx key design 3 (the kept set of a global or per-layer
+ * selection gives every (layer, KV head) its own budget) and MomentKV's
+ * setup (the prompt is compressed before decoding, sec A4; the moment
+ * statistics start at zero at the start of each generation and every
+ * evicted token is folded, Algorithm 1 / sec 4.1 "efficient statistics
+ * update"); KeepKV eq 15 for the optional initial utilities.
+ *
+ * keep [U][N] uint8 is the kept mask of a prefill selection (the
+ * [NL][Hkv][N] output of kvc_prefill_score / kvc_prefill_snapkv of one
+ * sequence is [U][N] with U = NL * Hkv; B sequences stack their masks);
+ * K_src, V_src [U][N][d] bf16 are the prompt's keys and values in the same
+ * order; votes_src [U][N] int32 or NULL (all 1); util_init [U][N] fp64 or
+ * NULL.  For every unit u, with c = the number of kept tokens:
+ *   slots [0, c) of cache receive the kept tokens in ascending position
+ *     (K, V rows; pos = the token's index i in the prompt; votes (when the
+ *     cache has votes) = votes_src or 1; util = util_init[u][i], i.e.
+ *     scored, or +inf (unscored) when util_init is NULL); len[u] = c;
+ *   the moments are reset and every token not kept is folded into them,
+ *     weighted by its vote (the vote-weighted mean / covariance of the
+ *     prompt's evicted set);
+ *   budget[u] (optional DEVICE output [U]) = max(c, 1): the budget to
+ *     decode with (pass it as kvc_params.budget, with L >= every budget).
+ *     A unit that kept nothing decodes with budget 1 (every decode step
+ *     appends before it evicts); its first step leaves it at length 1, so
+ *     that step must not take the fused steady-state path (pass max_len !=
+ *     L + 1, e.g. L + 2 when cap allows).
+ * p: the decode stream's parameters (U, G, d, cap; budget is not read
+ * here).  A unit whose c exceeds cap - 1 records KVC_ERR_SHAPE and gets
+ * len 0.  Device memory ws of kvc_prefill_handoff_workspace_size(U, N)
+ * bytes (256-byte aligned) carries the evicted lists and a status word
+ * (KVC_ERR_* of the call; read it with kvc_get_device_status(ws, ...)).
+ */
+KVC_API kvc_status kvc_prefill_handoff(const kvc_params *p, int32_t N, const uint8_t *keep,
+                                       const uint16_t *K_src, const uint16_t *V_src,
+                                       const int32_t *votes_src, const double *util_init,
+                                       const kvc_cache *cache, const kvc_moments *mom,
+                                       int32_t *budget, void *ws, size_t ws_bytes,
+                                       void *stream);
+
+/* ------------------------------------------------------------------ */
 /* prefill scorer                                                       */
 /* ------------------------------------------------------------------ */
 
@@ -511,6 +573,58 @@ KVC_API kvc_status kvc_prefill_score(int32_t NL, int32_t Hq, int32_t Hkv, int32_
                              const float *R, float *scores, uint8_t *keep,
                              int32_t *counts, int64_t *idx, void *ws,
                              size_t ws_bytes, void *stream);
+
+/*
+ * kvc_prefill_window_attention -- weighted column sums of the group-mean
+ * window attention.
+ *
+ * Defined by: KeepKV reading notes eq 15 at the end of the prefill
+ * (S = sum over the last w queries of (1 - alpha) alpha^(age) s^k, the
+ * windowed EMA initialization of the utilities: row_weight[j] =
+ * (1 - alpha) alpha^(w-1-j)); MomentKV sec A4 setup, SnapKV's prefill
+ * protocol (attention accumulated over the observation window:
+ * row_weight[j] = 1).  With the window and the causal mask of
+ * kvc_prefill_score (query j of w at position N - w + j sees keys
+ * 0..N-w+j; A_bar the mean over the group's query heads of the row
+ * softmax of q K^T / sqrt(d)):
+ *   S[l][g][i] = sum_{j<w} row_weight[j] A_bar[j, i].
+ * row_weight: HOST array of w floats.  q_win [NL][Hq][w][d], K
+ * [NL][Hkv][N][d] bf16 as in kvc_prefill_score; S [NL][Hkv][N] fp32.
+ * Supported: d = 128, Hq = 4 Hkv, 1 <= w <= min(32, N).  ws: device memory
+ * of kvc_prefill_workspace_size(NL, Hkv, N, 0) bytes, 256-byte aligned.
+ * Tensor cores (tcgen05) for the logits, fp32 probabilities.
+ */
+KVC_API kvc_status kvc_prefill_window_attention(int32_t NL, int32_t Hq, int32_t Hkv, int32_t d,
+                                                int32_t N, int32_t w, const float *row_weight,
+                                                const uint16_t *q_win, const uint16_t *K,
+                                                float *S, void *ws, size_t ws_bytes,
+                                                void *stream);
+
+/*
+ * kvc_prefill_snapkv -- the prompt selection of MomentKV's prefill protocol.
+ *
+ * Defined by: MomentKV sec A4 setup ("SnapKV's prefill protocol": attention
+ * scores accumulated over a 32-token observation window at the end of the
+ * prompt; the first token kept as the attention sink; adjacent tokens
+ * merged into blocks of 4 before scoring; the cache budget allocated
+ * adaptively over the heads of a layer from their attention).
+ *   acc = kvc_prefill_window_attention with every row weight 1;
+ *   scores[l][g][i] = mean of acc over the block of `pool` consecutive
+ *     positions holding i ([b pool, (b + 1) pool), the last block ragged);
+ *     with sink != 0, scores[l][g][0] = +infinity;
+ *   each layer keeps its B_total / NL largest scores over all its KV heads
+ *     and tokens (equal scores in ascending flat index).
+ * Outputs as kvc_prefill_score (scores [NL][Hkv][N] fp32 optional, keep
+ * [NL][Hkv][N] uint8 required, counts [NL][Hkv] and idx [B_total] optional,
+ * idx ascending within each layer's slice [l B_total/NL, (l+1) B_total/NL)).
+ * B_total must be a multiple of NL (KVC_ERR_INVALID_ARG); 1 <= pool <= 64;
+ * Hkv <= 64; other limits and the workspace as kvc_prefill_window_attention.
+ */
+KVC_API kvc_status kvc_prefill_snapkv(int32_t NL, int32_t Hq, int32_t Hkv, int32_t d, int32_t N,
+                                      int32_t w, int64_t B_total, int32_t pool, int32_t sink,
+                                      const uint16_t *q_win, const uint16_t *K, float *scores,
+                                      uint8_t *keep, int32_t *counts, int64_t *idx, void *ws,
+                                      size_t ws_bytes, void *stream);
 
 #ifdef __cplusplus
 }

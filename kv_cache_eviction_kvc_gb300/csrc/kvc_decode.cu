@@ -342,7 +342,7 @@ cudaError_t launch_attend(const kvc_params &p, int t, int new_pos, int max_len,
 struct AggArgs {
     const double *probs;
     double *util;
-    const int32_t *pos, *len;
+    const int32_t *pos, *len, *budget;
     int32_t *evict_idx, *evict_pos, *n_evict, *status, *pend;
     int cap, L, rule, refresh, kmax;
     float alpha;
@@ -412,7 +412,12 @@ __global__ void __launch_bounds__(512) aggregate_kernel(AggArgs a)
         }
         __syncthreads();
     }
-    const int k = n - a.L;
+    const int Lb = a.budget ? a.budget[u] : a.L;      // this unit's budget
+    if (Lb < 1 || Lb > a.L) {
+        if (tid == 0) { a.n_evict[u] = 0; record_status(a.status, KVC_ERR_SHAPE); }
+        return;
+    }
+    const int k = n - Lb;
     if (k <= 0) {
         if (tid == 0) a.n_evict[u] = 0;
         return;
@@ -472,7 +477,7 @@ cudaError_t launch_aggregate(const kvc_params &p, int t, const double *probs,
                              int32_t *evict_pos, int32_t *n_evict,
                              const DecodeWs &ws, cudaStream_t st)
 {
-    AggArgs a{probs, c.util, c.pos, c.len, evict_idx, evict_pos, n_evict,
+    AggArgs a{probs, c.util, c.pos, c.len, p.budget, evict_idx, evict_pos, n_evict,
               ws.status, ws.pend, p.cap, p.L, p.rule,
               p.rule == KVC_RULE_MI || is_refresh(t, p.refresh_period),
               kmax, p.alpha};

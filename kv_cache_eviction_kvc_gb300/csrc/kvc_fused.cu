@@ -71,6 +71,7 @@ struct FusedArgs {
     double *probs;
     int32_t *evict_idx, *evict_pos, *n_evict;
     int32_t *pend, *status;
+    const int32_t *budget;      // per-unit budgets (NULL: L for every unit)
     int cap, L, T, rule, correction, t, new_pos, kmax, chunk;
     float alpha;
     int merge;                  // KeepKV merge mode: attend over L + 1, append at L
@@ -215,7 +216,14 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
     unsigned char *chosen = ring + align_up((size_t)(ch + 1) * 8) + align_up((size_t)(ch + 1) * 4);
     auto XS = [&](int h, int li) -> float & { return xsb[h * (ch + 1) + li]; };
 
-    const int L = a.L;
+    // this unit's budget (the grid is laid out for the largest, a.L)
+    int L = a.L;
+    bool bad_budget = false;
+    if (a.budget) {
+        const int b = a.budget[u];
+        if (b >= 1 && b <= a.L) L = b;
+        else bad_budget = true;
+    }
     const bool refresh = is_refresh(a.t, a.T);
     const size_t ubase = (size_t)u * a.cap;
     const int s0 = min(L, r * ch), s1 = min(L, s0 + ch);
@@ -247,7 +255,7 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
         }
     }
     const int n_old = a.len[u];
-    if (n_old != L) {                      // uniform over the cluster
+    if (n_old != L || bad_budget) {        // uniform over the cluster
         if (r == 0 && tid == 0) {
             record_status(a.status, KVC_ERR_SHAPE);
             a.n_evict[u] = 0;
@@ -1395,8 +1403,8 @@ cudaError_t launch_fused_step(const kvc_params &p, int t, int new_pos, const uin
     if (chunk > kFusedMaxChunk || p.L + 1 > p.cap) return cudaErrorNotSupported;
     FusedArgs a{q, k_new, v_new, c.K, c.V, c.votes, c.pos, c.util, c.len,
                 m.n, m.mu_k, m.mu_v, m.C, o, probs, evict_idx, evict_pos, n_evict,
-                ws.pend, ws.status, p.cap, p.L, p.refresh_period, p.rule, p.correction,
-                t, new_pos, kmax, chunk, p.alpha, p.merge};
+                ws.pend, ws.status, p.budget, p.cap, p.L, p.refresh_period, p.rule,
+                p.correction, t, new_pos, kmax, chunk, p.alpha, p.merge};
     switch (p.G) {
     case 1: return launch_fused_g<1>(a, p.U, CS, st);
     case 2: return launch_fused_g<2>(a, p.U, CS, st);

@@ -162,7 +162,7 @@ constexpr int kGrMaxSlots = 8192;           // slots per unit (alive bitmap)
 
 struct GreedyArgs {
     const uint16_t *K, *V;
-    const int32_t *votes, *pos, *len;
+    const int32_t *votes, *pos, *len, *budget;
     double *util;
     float *n, *mu_k, *mu_v, *C;
     const float *xbuf;        // [U][G][cap] logits of the attend pass
@@ -191,7 +191,12 @@ __global__ void __launch_bounds__(kGrThreads, 1) mi_greedy_kernel(GreedyArgs a)
 
     const int u = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int n = a.len[u];
-    const int k = n - a.L;
+    const int Lb = a.budget ? a.budget[u] : a.L;      // this unit's budget
+    const int k = n - Lb;
+    if (Lb < 1 || Lb > a.L) {
+        if (tid == 0) { a.n_evict[u] = 0; record_status(a.status, KVC_ERR_SHAPE); }
+        return;
+    }
     if (k <= 0) {
         if (tid == 0) a.n_evict[u] = 0;
         return;
@@ -358,7 +363,7 @@ cudaError_t launch_mi_greedy(const kvc_params &p, const kvc_cache &c, const kvc_
                              int32_t *evict_pos, int32_t *n_evict, int32_t *status,
                              cudaStream_t st)
 {
-    GreedyArgs a{c.K, c.V, c.votes, c.pos, c.len, c.util, m.n, m.mu_k, m.mu_v, m.C, xbuf, lse,
+    GreedyArgs a{c.K, c.V, c.votes, c.pos, c.len, p.budget, c.util, m.n, m.mu_k, m.mu_v, m.C, xbuf, lse,
                  evict_idx, evict_pos, n_evict, status, p.cap, p.L, kmax};
     switch (p.G) {
     case 1: return launch_greedy_g<1>(a, p.U, st);

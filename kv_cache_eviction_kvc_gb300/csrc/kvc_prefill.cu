@@ -15,7 +15,10 @@
 //                               window logits, merged over the cluster
 //                        norm   S^T = K Q^T (keys x rows): group-mean
 //                               attention column norms c_i = ||A_bar[:, i]||_2
-//                      p_i = c_i r_i and the per-layer sums of p (fp64)
+//                      p_i = c_i r_i and the per-layer sums of p (fp64);
+//                      optionally the weighted column sum
+//                      S_i = sum_j roww_j A_bar[j, i] (SnapKV's accumulated
+//                      window attention, KeepKV's windowed EMA init)
 //                      Both kernels: every contraction on tcgen05 (128 x 128
 //                      x 128 bf16, fp32 accumulators in tensor memory), a TMA
 //                      producer warp, one MMA-issuing thread, epilogue warps
@@ -96,11 +99,14 @@ struct Ring {
 struct AttnArgs {
     const unsigned char *pack;   // [NL][Hkv][kPackBytes] from pack_kernel
     const float *r2;             // [NL][Hkv][N]: squared value norms (value-norm kernel)
-    float *p;                    // [NL][Hkv][N]: p = c r
+    float *p;                    // [NL][Hkv][N]: p = c r (want_p)
     float2 *stats;               // [NL][Hkv][kCS][kASets][kRows] partial (max, sum) per row
     double *layer_sum;           // [NL]: per-layer sums of p; NaN on a timed-out wait
+    float *colsum;               // [NL][Hkv][N]: sum_j roww_j A_bar[j, i], or NULL
     int Hkv, N, w, per_cta, nitem;
+    int want_p;                  // LaProx's p = c r and its layer sums
     float cs;                    // log2(e) / sqrt(d): logits in base-2 units
+    float roww[32];              // window row weights of colsum
 };
 
 struct AttnSmem {
@@ -113,6 +119,7 @@ struct AttnSmem {
     uint64_t ready[2];           // the cluster's partial statistics of an item are published
     uint64_t fin;                // every MMA of the CTA completed
     __align__(16) float2 rs[kRows];   // per row: cluster max (base 2) and 1 / sum; read as float4
+    float roww[32];              // colsum weights per window row
     uint32_t tmem;
     int bad;
 };
@@ -155,6 +162,7 @@ prefill_attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap tmK)
     };
     auto none = [] {};
 
+    if (tid < 32) S.roww[tid] = a.roww[tid];
     if (tid == 0) {
         S.bad = 0;
         for (int j = 0; j < kAStages; j++) {
@@ -364,11 +372,12 @@ prefill_attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap tmK)
                 const int kl = t * kTk + ln;
                 const size_t o = (size_t)lgn * N + k0 + kl;
                 // r^2 of the key (from the value-norm kernel), in flight during the wait
-                const float r2 = k0 + kl < k1 ? a.r2[o] : 0.f;
+                const float r2 = (a.want_p && k0 + kl < k1) ? a.r2[o] : 0.f;
                 if (acquire(gi)) {
                     const uint32_t tb = lane_base + (uint32_t)((gi % kAcc) * 128);
                     const int jmin = k0 + kl - (N - W);     // window rows j < jmin do not see the key
                     float c2[4] = {0.f, 0.f, 0.f, 0.f};
+                    float cw[4] = {0.f, 0.f, 0.f, 0.f};    // weighted column sum (times G)
 #pragma unroll 1
                     for (int hh = 0; hh < 2; hh++) {      // window rows 64 hh .. 64 hh + 63
                         float x[64];
@@ -383,13 +392,17 @@ prefill_attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap tmK)
                             sh = fmaf(ex2_approx(fmaf(x[4 * jj + 3], cs, -B.z)), B.w, sh);
                             sh = (j >= jmin) ? sh : 0.f;
                             c2[jj & 3] = fmaf(sh, sh, c2[jj & 3]);
+                            cw[jj & 3] = fmaf(S.roww[j], sh, cw[jj & 3]);
                         }
                     }
                     if (k0 + kl < k1) {
-                        const float pv = sqrtf(((c2[0] + c2[1]) + (c2[2] + c2[3])) *
-                                               (1.f / (kPG * kPG))) * sqrtf(r2);
-                        a.p[o] = pv;
-                        lsum += (double)pv;
+                        if (a.want_p) {
+                            const float pv = sqrtf(((c2[0] + c2[1]) + (c2[2] + c2[3])) *
+                                                   (1.f / (kPG * kPG))) * sqrtf(r2);
+                            a.p[o] = pv;
+                            lsum += (double)pv;
+                        }
+                        if (a.colsum) a.colsum[o] = ((cw[0] + cw[1]) + (cw[2] + cw[3])) * (1.f / kPG);
                     }
                 }
                 release(gi);
@@ -729,6 +742,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint16_t *q, const floa
         }
         *reinterpret_cast<uint4 *>(dst + opnd_off(r, c)) = v;
     }
+    if (R == nullptr) return;                // window attention only: no value-norm factor
     const float *G0 = R + (size_t)lg * kD * kD;
     for (int e = threadIdx.x; e < kD * 16; e += blockDim.x) {
         const int b = e >> 4, c = e & 15;
@@ -1221,6 +1235,24 @@ __global__ void __launch_bounds__(kTkBlock) seg_select_kernel(float *s, int N, i
         for (int g = tid; g < nheads; g += blockDim.x) counts[head0 + g] = cnt[g];
 }
 
+// SnapKV's scores under MomentKV's prefill protocol: each block of `pool`
+// consecutive positions of a (layer, KV head) takes the mean of its tokens'
+// accumulated window attention, and position 0 (the attention sink) scores
+// +infinity when sink != 0.  One thread per token.
+__global__ void snapkv_pool_kernel(const float *acc, float *s, int N, int pool, int sink,
+                                   int64_t M)
+{
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= M) return;
+    const int i = (int)(e % N);
+    const int64_t row = e - i;
+    const int b0 = i - i % pool, b1 = min(N, b0 + pool);
+    float m = 0.f;
+    for (int j = b0; j < b1; j++) m += acc[row + j];
+    m /= (float)(b1 - b0);
+    s[e] = (sink && i == 0) ? __int_as_float(0x7f800000) : m;
+}
+
 struct PfWs {
     float *p;
     double *layer_sum;
@@ -1283,6 +1315,77 @@ static kvc_status pf_cuda(cudaError_t e, const char *what)
     if (e == cudaSuccess) return KVC_OK;
     set_error("%s: %s", what, cudaGetErrorString(e));
     return KVC_ERR_CUDA;
+}
+
+// The persistent attention kernel: as many 8-CTA clusters as the GPU holds
+// at once, each looping over (layer, KV head) items.
+static cudaError_t launch_attn(const AttnArgs &aa, const CUtensorMap &tmK, int nitem, int nsm,
+                               cudaStream_t st)
+{
+    cudaError_t e = cudaFuncSetAttribute(prefill_attn_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kADyn);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kAThreads);
+    cfg.dynamicSmemBytes = kADyn;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(kCS * std::min(nitem, std::max(1, nsm / kCS)));
+    int nclu = 0;
+    if (cudaOccupancyMaxActiveClusters(&nclu, prefill_attn_kernel, &cfg) != cudaSuccess || nclu < 1)
+        nclu = std::max(1, nsm / (2 * kCS));
+    (void)cudaGetLastError();
+    cfg.gridDim = dim3(kCS * std::min(nitem, nclu));
+    return cudaLaunchKernelEx(&cfg, prefill_attn_kernel, aa, tmK);
+}
+
+// Window attention shared by kvc_prefill_window_attention and
+// kvc_prefill_snapkv: checks, pack (window queries only) and the attention
+// kernel writing the weighted column sums into S.
+static kvc_status window_colsum(const char *who, int32_t NL, int32_t Hq, int32_t Hkv, int32_t d,
+                                int32_t N, int32_t w, const float *row_weight,
+                                const uint16_t *q_win, const uint16_t *K, float *S, void *ws,
+                                size_t ws_bytes, cudaStream_t st)
+{
+    PF_CHECK(NL >= 1 && Hkv >= 1 && N >= 1 && w >= 1, KVC_ERR_INVALID_ARG,
+             "%s: NL, Hkv, N, w must be >= 1", who);
+    PF_CHECK(d == kD, KVC_ERR_UNSUPPORTED, "%s: d = %d unsupported", who, d);
+    PF_CHECK(Hq == kPG * Hkv, KVC_ERR_UNSUPPORTED,
+             "%s: only 4 query heads per KV head are supported (Hq = %d, Hkv = %d)", who, Hq, Hkv);
+    PF_CHECK(w <= 32 && w <= N, KVC_ERR_UNSUPPORTED, "%s: window w = %d must be <= 32 and <= N",
+             who, w);
+    PF_CHECK(q_win && K && S && row_weight, KVC_ERR_INVALID_ARG,
+             "%s: q_win, K, the row weights and the output are required", who);
+    PF_CHECK(((uintptr_t)K & 15u) == 0 && ((uintptr_t)q_win & 3u) == 0, KVC_ERR_INVALID_ARG,
+             "%s: K must be 16-byte aligned, q_win 4-byte", who);
+    PfWs pw = pf_layout(NL, Hkv, N, nullptr);
+    PF_CHECK(ws != nullptr && ws_bytes >= pw.bytes && ((uintptr_t)ws & 255u) == 0, KVC_ERR_WORKSPACE,
+             "%s: workspace of %zu bytes (256-byte aligned) required", who, pw.bytes);
+    pw = pf_layout(NL, Hkv, N, ws);
+    const uint64_t rows = (uint64_t)NL * Hkv * N;
+    PF_CHECK(rows + kTk < (1ull << 31), KVC_ERR_UNSUPPORTED, "%s: too many rows", who);
+    CUtensorMap tmK;
+    PF_CHECK(make_row_map(&tmK, K, rows, kTk), KVC_ERR_CUDA, "%s: tensor map encoding failed", who);
+    int dev = 0, nsm = 0;
+    cudaError_t e;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return pf_cuda(e, who);
+    kvc_status s = pf_cuda(cudaMemsetAsync(pw.layer_sum, 0, (size_t)NL * 8, st), "memset");
+    if (s != KVC_OK) return s;
+    pack_kernel<<<NL * Hkv, 256, 0, st>>>(q_win, nullptr, pw.pack, Hq, Hkv, w);
+    if ((e = cudaGetLastError()) != cudaSuccess) return pf_cuda(e, who);
+    const int per_cta = ((N + kCS - 1) / kCS + kTk - 1) / kTk * kTk;
+    AttnArgs aa{pw.pack, nullptr, nullptr, pw.stats, pw.layer_sum, S, Hkv, N, w, per_cta, NL * Hkv,
+                0, (float)(1.4426950408889634 / sqrt((double)kD)), {}};
+    for (int j = 0; j < 32; j++) aa.roww[j] = j < w ? row_weight[j] : 0.f;
+    return pf_cuda(launch_attn(aa, tmK, NL * Hkv, nsm, st), who);
 }
 
 extern "C" {
@@ -1385,30 +1488,9 @@ kvc_status kvc_prefill_score(int32_t NL, int32_t Hq, int32_t Hkv, int32_t d, int
                          kVDyn, st>>>(va, tmV);
     if ((e = cudaGetLastError()) != cudaSuccess) return pf_cuda(e, "kvc_prefill_score value launch");
 
-    AttnArgs aa{pw.pack, pw.r2, pbuf, pw.stats, pw.layer_sum, Hkv, N, w, per_cta, nitem,
-                (float)(1.4426950408889634 / sqrt((double)kD))};
-    e = cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kADyn);
-    if (e != cudaSuccess) return pf_cuda(e, "kvc_prefill_score attribute");
-    cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(kAThreads);
-    cfg.dynamicSmemBytes = kADyn;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCS;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    // persistent: as many clusters as the GPU holds at once (each loops over items)
-    cfg.gridDim = dim3(kCS * std::min(nitem, std::max(1, nsm / kCS)));
-    int nclu = 0;
-    if (cudaOccupancyMaxActiveClusters(&nclu, prefill_attn_kernel, &cfg) != cudaSuccess || nclu < 1)
-        nclu = std::max(1, nsm / (2 * kCS));
-    (void)cudaGetLastError();
-    cfg.gridDim = dim3(kCS * std::min(nitem, nclu));
-    e = cudaLaunchKernelEx(&cfg, prefill_attn_kernel, aa, tmK);
+    AttnArgs aa{pw.pack, pw.r2, pbuf, pw.stats, pw.layer_sum, nullptr, Hkv, N, w, per_cta, nitem,
+                1, (float)(1.4426950408889634 / sqrt((double)kD)), {}};
+    e = launch_attn(aa, tmK, nitem, nsm, st);
     if (e != cudaSuccess) return pf_cuda(e, "kvc_prefill_score attention launch");
     const int64_t per_layer = (int64_t)Hkv * N;
 
@@ -1441,6 +1523,48 @@ kvc_status kvc_prefill_score(int32_t NL, int32_t Hq, int32_t Hkv, int32_t d, int
     topk_write_kernel<<<nblk, kTkBlock, 0, st>>>(pbuf, (int)M, N, pw.st, pw.eq_off, pw.keep_off, keep,
                                                  counts, idx);
     return pf_cuda(cudaGetLastError(), "kvc_prefill_score top-K launch");
+}
+
+kvc_status kvc_prefill_window_attention(int32_t NL, int32_t Hq, int32_t Hkv, int32_t d, int32_t N,
+                                        int32_t w, const float *row_weight, const uint16_t *q_win,
+                                        const uint16_t *K, float *S, void *ws, size_t ws_bytes,
+                                        void *stream)
+{
+    return window_colsum("kvc_prefill_window_attention", NL, Hq, Hkv, d, N, w, row_weight, q_win,
+                         K, S, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+kvc_status kvc_prefill_snapkv(int32_t NL, int32_t Hq, int32_t Hkv, int32_t d, int32_t N, int32_t w,
+                              int64_t B_total, int32_t pool, int32_t sink, const uint16_t *q_win,
+                              const uint16_t *K, float *scores, uint8_t *keep, int32_t *counts,
+                              int64_t *idx, void *ws, size_t ws_bytes, void *stream)
+{
+    const char *who = "kvc_prefill_snapkv";
+    PF_CHECK(NL >= 1 && Hkv >= 1 && N >= 1, KVC_ERR_INVALID_ARG, "%s: NL, Hkv, N must be >= 1", who);
+    const int64_t M = (int64_t)NL * Hkv * N;
+    PF_CHECK(B_total >= 0 && B_total <= M && B_total % NL == 0, KVC_ERR_INVALID_ARG,
+             "%s: B_total = %lld must be a multiple of NL = %d in [0, %lld]", who,
+             (long long)B_total, NL, (long long)M);
+    PF_CHECK(pool >= 1 && pool <= 64, KVC_ERR_INVALID_ARG, "%s: pool = %d outside [1, 64]", who, pool);
+    PF_CHECK(Hkv <= kSegMaxHeads, KVC_ERR_UNSUPPORTED,
+             "%s: per-layer allocation supports up to %d KV heads", who, kSegMaxHeads);
+    PF_CHECK(keep != nullptr, KVC_ERR_INVALID_ARG, "%s: keep is required", who);
+    PF_CHECK(M < (1ll << 31), KVC_ERR_UNSUPPORTED, "%s: too many tokens", who);
+    float ones[32];
+    for (int j = 0; j < 32; j++) ones[j] = 1.f;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // accumulated window attention into the workspace's score buffer
+    PfWs pw = pf_layout(NL, Hkv, N, ws);
+    kvc_status s = window_colsum(who, NL, Hq, Hkv, d, N, w, ones, q_win, K, pw.p, ws, ws_bytes, st);
+    if (s != KVC_OK) return s;
+    float *sc = scores ? scores : pw.r2;
+    snapkv_pool_kernel<<<(unsigned)((M + 255) / 256), 256, 0, st>>>(pw.p, sc, N, pool, sink, M);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return pf_cuda(e, who);
+    // each layer keeps B_total / NL over its heads and tokens
+    seg_select_kernel<<<(unsigned)NL, kTkBlock, 0, st>>>(sc, N, (int)(M / NL), (int)(B_total / NL),
+                                                          (int)(M / NL), pw.inv, 0, keep, counts, idx);
+    return pf_cuda(cudaGetLastError(), "kvc_prefill_snapkv select launch");
 }
 
 }  // extern "C"

@@ -29,7 +29,8 @@ EXPORTED = (
     "kvc_decode_workspace_size", "kvc_decode_workspace_init", "kvc_get_device_status",
     "kvc_decode_attend", "kvc_aggregate_evict", "kvc_moment_update", "kvc_correct",
     "kvc_compact", "kvc_zip_merge", "kvc_mi_scores", "kvc_mi_evict", "kvc_decode_step", "kvc_decode_attend_noalloc", "kvc_prefill_prepare",
-    "kvc_prefill_workspace_size", "kvc_prefill_score",
+    "kvc_prefill_workspace_size", "kvc_prefill_score", "kvc_prefill_window_attention",
+    "kvc_prefill_snapkv", "kvc_prefill_handoff_workspace_size", "kvc_prefill_handoff",
 )
 
 
@@ -44,7 +45,7 @@ class kvc_params(ctypes.Structure):
                 ("cap", ctypes.c_int32), ("L", ctypes.c_int32), ("rule", ctypes.c_int32),
                 ("alpha", ctypes.c_float), ("refresh_period", ctypes.c_int32),
                 ("correction", ctypes.c_int32), ("merge", ctypes.c_int32),
-                ("merge_recent", ctypes.c_int32)]
+                ("merge_recent", ctypes.c_int32), ("budget", ctypes.c_void_p)]
 
 
 class kvc_cache(ctypes.Structure):
@@ -98,6 +99,12 @@ def load(build: bool = True):
         "kvc_prefill_workspace_size": (SZ, [I32, I32, I32, I64]),
         "kvc_prefill_score": (I32, [I32, I32, I32, I32, I32, I32, I64, I32, I32, P, P, P, P, P,
                                     P, P, P, P, SZ, P]),
+        "kvc_prefill_window_attention": (I32, [I32, I32, I32, I32, I32, I32, P, P, P, P, P, SZ,
+                                               P]),
+        "kvc_prefill_handoff_workspace_size": (SZ, [I32, I32]),
+        "kvc_prefill_handoff": (I32, [PP, I32, P, P, P, P, P, PC, PM, P, P, SZ, P]),
+        "kvc_prefill_snapkv": (I32, [I32, I32, I32, I32, I32, I32, I64, I32, I32, P, P, P, P, P,
+                                     P, P, SZ, P]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -135,12 +142,14 @@ def _stream(stream):
 
 
 def make_params(U, G, cap, L, rule=RULE_EMA, alpha=0.9, refresh_period=1,
-                correction=CORR_FIRST_ORDER, d=128, merge_recent=None) -> kvc_params:
+                correction=CORR_FIRST_ORDER, d=128, merge_recent=None, budget=None) -> kvc_params:
     """merge_recent = R (not None) turns on KeepKV ZIP-merging with the last R
-    positions excluded from the partner search."""
+    positions excluded from the partner search; budget (a device int32 [U]
+    tensor, kept alive by the caller) gives every unit its own budget."""
     merge = 0 if merge_recent is None else 1
     return kvc_params(U, G, d, cap, L, rule, alpha, refresh_period, correction, merge,
-                      0 if merge_recent is None else int(merge_recent))
+                      0 if merge_recent is None else int(merge_recent),
+                      _ptr(budget, torch.int32, "budget", optional=True))
 
 
 def make_cache(K, V, votes, pos, util, length) -> kvc_cache:
@@ -314,3 +323,40 @@ def kvc_prefill_score(NL, Hq, Hkv, d, N, w, B_total, normalize, q_win, K, V, R, 
         _ptr(keep, torch.uint8, "keep"), _ptr(counts, torch.int32, "counts", optional=True),
         _ptr(idx, torch.int64, "idx", optional=True), _ptr(ws, torch.uint8, "ws", optional=True),
         0 if ws is None else ws.numel(), _stream(stream)))
+
+
+def kvc_prefill_window_attention(NL, Hq, Hkv, d, N, w, row_weight, q_win, K, S, ws, stream=None):
+    """row_weight: w host floats (a sequence); S: [NL][Hkv][N] fp32 output."""
+    rw = (ctypes.c_float * max(1, len(row_weight)))(*[float(x) for x in row_weight])
+    bf = torch.bfloat16
+    _check(load().kvc_prefill_window_attention(
+        int(NL), int(Hq), int(Hkv), int(d), int(N), int(w), ctypes.cast(rw, ctypes.c_void_p),
+        _ptr(q_win, bf, "q_win"), _ptr(K, bf, "K"), _ptr(S, torch.float32, "S"),
+        _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
+
+
+def kvc_prefill_snapkv(NL, Hq, Hkv, d, N, w, B_total, pool, sink, q_win, K, scores, keep, counts,
+                       idx, ws, stream=None):
+    bf = torch.bfloat16
+    _check(load().kvc_prefill_snapkv(
+        int(NL), int(Hq), int(Hkv), int(d), int(N), int(w), int(B_total), int(pool), int(sink),
+        _ptr(q_win, bf, "q_win"), _ptr(K, bf, "K"),
+        _ptr(scores, torch.float32, "scores", optional=True), _ptr(keep, torch.uint8, "keep"),
+        _ptr(counts, torch.int32, "counts", optional=True),
+        _ptr(idx, torch.int64, "idx", optional=True), _ptr(ws, torch.uint8, "ws"), ws.numel(),
+        _stream(stream)))
+
+
+def kvc_prefill_handoff_workspace_size(U, N) -> int:
+    return int(load().kvc_prefill_handoff_workspace_size(int(U), int(N)))
+
+
+def kvc_prefill_handoff(p, N, keep, K_src, V_src, votes_src, util_init, cache: kvc_cache,
+                        mom: kvc_moments, budget, ws, stream=None):
+    bf = torch.bfloat16
+    _check(load().kvc_prefill_handoff(
+        ctypes.byref(p), int(N), _ptr(keep, torch.uint8, "keep"), _ptr(K_src, bf, "K_src"),
+        _ptr(V_src, bf, "V_src"), _ptr(votes_src, torch.int32, "votes_src", optional=True),
+        _ptr(util_init, torch.float64, "util_init", optional=True), ctypes.byref(cache),
+        ctypes.byref(mom), _ptr(budget, torch.int32, "budget", optional=True),
+        _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))

@@ -14,11 +14,16 @@ class DecodeState:
     def __init__(self, U: int, G: int, cap: int, L: int, *, rule: int = K_.RULE_EMA,
                  alpha: float = 0.9, refresh_period: int = 1,
                  correction: int = K_.CORR_FIRST_ORDER, votes: bool = False,
-                 kmax: int = 1, device="cuda", d: int = 128, merge_recent: int | None = None):
+                 kmax: int = 1, device="cuda", d: int = 128, merge_recent: int | None = None,
+                 budgets: bool = False):
         self.U, self.G, self.cap, self.L, self.d = U, G, cap, L, d
         self.device = torch.device(device)
+        # per-unit budgets (a cache handed over from a prefill selection);
+        # the tensor lives as long as the parameters that point at it
+        self.budget = (torch.full((U,), L, dtype=torch.int32, device=self.device)
+                       if budgets else None)
         self.params = K_.make_params(U, G, cap, L, rule, alpha, refresh_period, correction, d,
-                                     merge_recent)
+                                     merge_recent, self.budget)
         self.merge = merge_recent is not None
         if self.merge and not votes:
             raise ValueError("ZIP-merging needs per-slot votes (votes=True)")
@@ -80,6 +85,16 @@ class DecodeState:
         self.len.copy_(length)
         for t in (self.n, self.mu_k, self.mu_v, self.C):
             t.zero_()
+
+    def load_handoff(self, N, keep, K_src, V_src, votes_src=None, util_init=None):
+        """Start the stream from a prefill selection (kvc_prefill_handoff):
+        keep [U][N] uint8, K_src / V_src [U][N][d]; the per-unit budgets land
+        in self.budget.  Returns the device status of the call."""
+        ws = torch.empty(K_.kvc_prefill_handoff_workspace_size(self.U, N), dtype=torch.uint8,
+                         device=self.device)
+        K_.kvc_prefill_handoff(self.params, N, keep, K_src, V_src, votes_src, util_init,
+                               self.cache, self.moments, self.budget, ws)
+        return K_.kvc_get_device_status(ws)
 
     def device_status(self) -> int:
         return K_.kvc_get_device_status(self.ws)

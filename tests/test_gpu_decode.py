@@ -142,3 +142,29 @@ def test_aggregate_refuses_one_shot_moment_informed_eviction():
     torch.cuda.synchronize()
     assert st.device_status() == 5
     assert st.n_evict.tolist() == [0, 0]
+
+
+# ------------------------------------------- prefill selection -> hand-off -> decode
+
+PIPE = W.C3.with_(name="pipe", NL=2, B_total=2 * 8 * 128)       # full prompt length, 2 layers
+
+
+@pytest.mark.parametrize("scorer,rule,T,pc", [
+    ("snapkv", W.RULE_EMA, 1, PIPE),                  # SnapKV protocol, EMA decode
+    ("snapkv", W.RULE_MI, 1, PIPE),                   # MomentKV's pipeline: SnapKV then MI decode
+    ("laprox", W.RULE_EMA, 4, PIPE),                  # LaProx global top-K, variable budgets, lazy
+    ("laprox", W.RULE_EMA, 1, PIPE.with_(N=2000, B_total=40)),   # heads left empty: budget 1
+], ids=["snapkv-ema", "snapkv-mi", "laprox-lazy", "laprox-empty-heads"])
+def test_prefill_handoff_then_decode(scorer, rule, T, pc):
+    """The prefill selection's kept set handed over to decoding: every unit
+    keeps its own budget (LaProx key design 3; MomentKV's adaptive per-head
+    allocation), the prompt's dropped tokens are the first eviction set of
+    the moments (MomentKV Algorithm 1), and decode steps evict each unit
+    down to its own budget."""
+    from parity import run_pipeline_parity
+    rep = run_pipeline_parity(pc, scorer=scorer, rule=rule, T=T, steps=10)
+    print(rep)
+    assert rep.ok(), rep
+    assert rep.decode.steps == 10
+    if scorer == "laprox":
+        assert rep.min_kept != rep.max_kept            # budgets really vary

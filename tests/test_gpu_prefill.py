@@ -56,3 +56,31 @@ def test_c3_allocations(alloc):
 ], ids=["layer", "head", "head-ragged", "layer-unnormalized", "head-empty", "head-keep-all"])
 def test_prefill_allocation_edge_cases(cfg, normalize, alloc):
     check(run_prefill_parity(cfg, normalize=normalize, alloc=alloc))
+
+
+# ------------------------------------------------ window attention, SnapKV
+
+@pytest.mark.parametrize("cfg,alpha", [
+    (W.C3.with_(NL=2), 0.9),                              # full key length, KeepKV eq 15 weights
+    (SMALL.with_(N=1000, w=8), 0.5),                      # ragged tiles, short window
+    (SMALL.with_(N=32), 0.0),                             # every key in the window; the last query alone
+], ids=["ema-c3-2layers", "ema-ragged-w8", "ema-all-window"])
+def test_window_attention_ema_init(cfg, alpha):
+    """KeepKV's windowed EMA initialization of the utilities on the GPU
+    (weights (1 - alpha) alpha^(w-1-j) over the window rows)."""
+    from parity import run_window_parity
+    wts = [(1 - alpha) * alpha ** (cfg.w - 1 - j) for j in range(cfg.w)]
+    err = run_window_parity(cfg, wts)
+    print("max rel err", err)
+    assert err <= 2e-3
+
+
+@pytest.mark.parametrize("cfg,pool,sink", [
+    (W.C3.with_(NL=2, B_total=2 * 8 * 128), 4, True),     # the protocol at full key length
+    (SMALL.with_(N=1000, B_total=2 * 700), 4, True),      # ragged last block
+    (SMALL.with_(N=200, w=8, B_total=2 * 40), 1, False),  # no pooling, no sink
+    (SMALL.with_(N=513, B_total=2 * 16), 8, True),        # budget below the sinks' blocks
+], ids=["snapkv-c3-2layers", "snapkv-ragged", "snapkv-plain", "snapkv-tight"])
+def test_snapkv_protocol(cfg, pool, sink):
+    from parity import run_snapkv_parity
+    check(run_snapkv_parity(cfg, pool=pool, sink=sink))
