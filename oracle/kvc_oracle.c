@@ -265,6 +265,55 @@ void ocl_update_util(void *h, const double *probs, int rule, double alpha)
 }
 
 /*
+ * The layer-chained EMA of InertiaKV's evaluated implementation [InertiaKV
+ * sec 1 and sec 3.1, last paragraph: compression runs at several layers and
+ * one running EMA state is updated after each of them, so that alpha weighs
+ * both the persistence across decode steps and the influence of consecutive
+ * layers; sec 3.1 eq 1: s_t(i) is the mean over all H query heads].  Units
+ * are grouped by sequence: unit u = (b NL + l) Hkv + g, and every unit of a
+ * sequence holds the same positions in the same slot order (one retained set
+ * per sequence).  On a refresh step, for every slot i of sequence b, for
+ * l = 0 .. NL - 1 in order:
+ *   s_l(i) = (1/Hkv) sum_g probs[(b NL + l) Hkv + g][i]   (the layer's mean
+ *            over its H = Hkv G query heads: probs are group means already)
+ *   m(i)   = s_l(i) at the first observation, else alpha m(i) + (1-alpha) s_l(i).
+ * The result is stored as the utility of slot i in every unit of the
+ * sequence (so a per-unit selection picks the same slots everywhere).
+ * Returns 0, or -1 if U is not a multiple of NL Hkv or the sequence's units
+ * differ in length.
+ */
+int ocl_update_util_chained(void *h, const double *probs, int NL, int Hkv, double alpha)
+{
+    ocl_session *s = (ocl_session *)h;
+    int per = NL * Hkv;
+    if (NL < 1 || Hkv < 1 || s->U % per != 0) return -1;
+    for (int b = 0; b < s->U / per; b++) {
+        int u0 = b * per, n = s->n[u0];
+        for (int q = 1; q < per; q++)
+            if (s->n[u0 + q] != n) return -1;
+        for (int i = 0; i < n; i++) {
+            size_t i0 = (size_t)u0 * s->cap + i;
+            double m = s->util[i0];
+            int seen = s->scored[i0];
+            for (int l = 0; l < NL; l++) {
+                double sl = 0.0;
+                for (int g = 0; g < Hkv; g++)
+                    sl += probs[(size_t)(u0 + l * Hkv + g) * s->cap + i];
+                sl /= (double)Hkv;
+                if (!seen) { m = sl; seen = 1; }
+                else m = alpha * m + (1.0 - alpha) * sl;
+            }
+            for (int q = 0; q < per; q++) {
+                size_t iq = (size_t)(u0 + q) * s->cap + i;
+                s->util[iq] = m;
+                s->scored[iq] = 1;
+            }
+        }
+    }
+    return 0;
+}
+
+/*
  * Moment-informed eviction scores [MomentKV sec 4.2, "moment residual" and
  * "moment-aware eviction score"; Algorithm 1, phase 1]: for every live slot
  *   r_i = v_i - v_bar - S_tilde (k_i - k_bar) / (n_e sqrt(d))

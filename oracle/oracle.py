@@ -34,6 +34,7 @@ _lib = None
 
 RULE_SINGLE, RULE_CUMULATIVE, RULE_EMA = 0, 1, 2
 RULE_MI = 3   # MomentKV moment-informed score alpha_i ||r_i||, re-scored every step
+RULE_CHAINED = 4   # InertiaKV's layer-chained EMA (one state per sequence, updated per layer)
 CORR_OFF, CORR_ZERO_ORDER, CORR_FIRST_ORDER = 0, 1, 2
 
 
@@ -68,6 +69,7 @@ def _load():
             "ocl_append": (I, [P, P, P, ctypes.c_int32]),
             "ocl_attend": (None, [P, P, P, P, P]),
             "ocl_update_util": (None, [P, P, I, D]),
+            "ocl_update_util_chained": (I, [P, P, I, I, D]),
             "ocl_get_slots": (None, [P, P, P, P, P, P]),
             "ocl_select": (I, [P, I, I, P, P, P, P]),
             "ocl_evict": (I, [P, P, P, I]),
@@ -183,6 +185,13 @@ class DecodeSession:
     def update_util(self, probs, rule: int, alpha: float):
         probs = np.ascontiguousarray(probs, dtype=np.float64)
         self.lib.ocl_update_util(self.h, _p(probs), int(rule), float(alpha))
+
+    def update_util_chained(self, probs, NL: int, Hkv: int, alpha: float):
+        """InertiaKV's layer-chained EMA over each sequence's NL x Hkv units
+        (see ocl_update_util_chained)."""
+        probs = np.ascontiguousarray(probs, dtype=np.float64)
+        if self.lib.ocl_update_util_chained(self.h, _p(probs), int(NL), int(Hkv), float(alpha)) != 0:
+            raise ValueError("chained EMA: units not grouped by sequence or lengths differ")
 
     def slots(self):
         """Returns (n [U], pos, vote, util, scored), each [U][cap]."""
@@ -325,7 +334,7 @@ def is_refresh(t: int, T: int) -> bool:
 def decode_step(sess: DecodeSession, t: int, new_pos: int, q, knew, vnew, *,
                 L, rule: int, alpha: float, T: int, correction: int,
                 choose=None, merge_recent: int | None = None, force_partner=None,
-                mi_forced=None):
+                mi_forced=None, chain=None):
     """One decode step on every unit of ``sess``, in the order of MomentKV
     Algorithm 1 with the InertiaKV utility in place of its scoring:
 
@@ -346,6 +355,10 @@ def decode_step(sess: DecodeSession, t: int, new_pos: int, q, knew, vnew, *,
 
     ``L`` is one budget or one per unit ([U]; a cache handed over from a
     prefill scorer keeps each unit at its own length).
+
+    Under rule RULE_CHAINED (InertiaKV's layer-chained EMA) ``chain`` =
+    (NL, Hkv) groups the units by sequence; one utility per slot of a
+    sequence, so every unit of it evicts the same slots.
 
     ``choose(t, proposal)``, if given, receives the oracle's proposal dict and
     returns the victim positions to apply ([U][kmax], [U]); tests use it to
@@ -385,7 +398,9 @@ def decode_step(sess: DecodeSession, t: int, new_pos: int, q, knew, vnew, *,
                         mi_used=g["used"])
     else:
         refresh = is_refresh(t, T)
-        if refresh:
+        if refresh and rule == RULE_CHAINED:
+            sess.update_util_chained(probs, chain[0], chain[1], alpha)
+        elif refresh:
             sess.update_util(probs, rule, alpha)
         n = sess.slots()[0]
         kmax = int(max(1, (n - np.asarray(L)).max()))

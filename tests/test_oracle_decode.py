@@ -707,3 +707,88 @@ def test_per_unit_budgets_select_like_single_units():
         assert vic[u, : nv[u]].tolist() == v1[0, : n1[0]].tolist()
         one.close()
     s.close()
+
+
+# ------------------------------------------------------ layer-chained EMA
+
+def _chained_session(rng, B, NL, Hkv, n, d=4):
+    U = B * NL * Hkv
+    k = bf(rng.normal(size=(B, n, d)))
+    s = O.DecodeSession(U, 1, d, n + 2)
+    for u in range(U):
+        b = u // (NL * Hkv)
+        s.load(u, k[b], k[b])            # every unit of a sequence: the same positions
+    return s, U
+
+
+def test_chained_ema_closed_form_over_layers():
+    """One refresh from utilities m0 with layer means s_l: the state passes
+    the layers in order, m = alpha^NL m0 + sum_l (1 - alpha) alpha^(NL-1-l) s_l,
+    s_l the mean over the layer's KV units of their head-mean probabilities
+    (InertiaKV sec 3.1: all H heads of the layer); every unit of the
+    sequence gets the same utility."""
+    rng = np.random.default_rng(61)
+    B, NL, Hkv, n, al = 2, 3, 2, 5, 0.7
+    s, U = _chained_session(rng, B, NL, Hkv, n)
+    m0 = rng.random((B, n))
+    for u in range(U):
+        s.set_util(u, m0[u // (NL * Hkv)])
+    probs = np.zeros((U, s.cap))
+    probs[:, :n] = rng.random((U, n))
+    s.update_util_chained(probs, NL, Hkv, al)
+    util = s.slots()[3]
+    for b in range(B):
+        sl = [probs[b * NL * Hkv + l * Hkv: b * NL * Hkv + (l + 1) * Hkv, :n].mean(axis=0)
+              for l in range(NL)]
+        want = al ** NL * m0[b] + sum((1 - al) * al ** (NL - 1 - l) * sl[l] for l in range(NL))
+        for q in range(NL * Hkv):
+            np.testing.assert_allclose(util[b * NL * Hkv + q, :n], want, rtol=1e-14)
+    s.close()
+
+
+def test_chained_ema_first_observation_and_one_layer():
+    """An unscored slot starts from the first layer's mean (the plain EMA's
+    first observation), then chains; with one layer and one KV head the
+    chained rule is the per-unit EMA."""
+    rng = np.random.default_rng(62)
+    NL, Hkv, n, al = 4, 1, 6, 0.9
+    s, U = _chained_session(rng, 1, NL, Hkv, n)
+    probs = np.zeros((U, s.cap)); probs[:, :n] = rng.random((U, n))
+    s.update_util_chained(probs, NL, Hkv, al)
+    m = probs[0, :n].copy()
+    for l in range(1, NL):
+        m = al * m + (1 - al) * probs[l, :n]
+    np.testing.assert_allclose(s.slots()[3][0, :n], m, rtol=1e-14)
+    s.close()
+    a, U = _chained_session(rng, 1, 1, 1, n)
+    b, _ = _chained_session(rng, 1, 1, 1, n)
+    for t in range(3):
+        p = np.zeros((1, a.cap)); p[0, :n] = rng.random(n)
+        a.update_util_chained(p, 1, 1, al)
+        b.update_util(p, O.RULE_EMA, al)
+    np.testing.assert_array_equal(a.slots()[3], b.slots()[3])
+    a.close(); b.close()
+
+
+def test_chained_generation_evicts_the_same_positions_everywhere():
+    """A whole decode run under the chained rule: every unit of a sequence
+    evicts the same positions each step, the lowest chained utility (brute
+    force over the sequence's slots)."""
+    rng = np.random.default_rng(63)
+    B, NL, Hkv, G, N, d, S, L = 2, 3, 2, 2, 12, 8, 6, 8
+    U = B * NL * Hkv
+    kp, vp = bf(rng.normal(size=(U, N, d))), bf(rng.normal(size=(U, N, d)))
+    qs = bf(rng.normal(size=(S, U, G, d)))
+    ks, vs = bf(rng.normal(size=(S, U, d))), bf(rng.normal(size=(S, U, d)))
+    sess = O.DecodeSession(U, G, d, N + S)
+    for u in range(U):
+        sess.load(u, kp[u], vp[u])
+    for s_ in range(S):
+        t = s_ + 1
+        r = O.decode_step(sess, t, N + t - 1, qs[s_], ks[s_], vs[s_], L=L, rule=O.RULE_CHAINED,
+                          alpha=0.8, T=1, correction=O.CORR_FIRST_ORDER, chain=(NL, Hkv))
+        for b in range(B):
+            sets = {tuple(sorted(r["applied_victims"][u, : r["applied_nvict"][u]].tolist()))
+                    for u in range(b * NL * Hkv, (b + 1) * NL * Hkv)}
+            assert len(sets) == 1
+    sess.close()
