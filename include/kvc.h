@@ -76,7 +76,14 @@ typedef enum {
     KVC_ERR_WORKSPACE = 6     /* workspace missing, misaligned or too small  */
 } kvc_status;
 
-enum { KVC_RULE_SINGLE = 0, KVC_RULE_CUMULATIVE = 1, KVC_RULE_EMA = 2, KVC_RULE_MI = 3 };
+enum {
+    KVC_RULE_SINGLE = 0,
+    KVC_RULE_CUMULATIVE = 1,
+    KVC_RULE_EMA = 2,
+    KVC_RULE_MI = 3,
+    KVC_RULE_EMA_CHAINED = 4   /* InertiaKV's layer-chained EMA: see
+                                  kvc_params.chain_layers */
+};
 enum { KVC_CORR_OFF = 0, KVC_CORR_ZERO_ORDER = 1, KVC_CORR_FIRST_ORDER = 2 };
 enum { KVC_ALLOC_GLOBAL = 0, KVC_ALLOC_LAYER = 1, KVC_ALLOC_HEAD = 2 };
 
@@ -88,6 +95,7 @@ typedef struct {
     int32_t cap;             /* slot capacity per unit (row stride of K, V)  */
     int32_t L;               /* budget: slots kept per unit after a step     */
     int32_t rule;            /* KVC_RULE_*  (InertiaKV sec 3.1 eqs 2-4;
+                                KVC_RULE_EMA_CHAINED: see chain_layers;
                                 KVC_RULE_MI: MomentKV's moment-informed
                                 score, every step, needs T = 1 and
                                 merge = 0; see kvc_mi_scores and
@@ -117,6 +125,24 @@ typedef struct {
                                 budget[u].  The fused steady state runs when
                                 max_len == L + 1 and every unit enters at
                                 its own budget.                              */
+    int32_t chain_layers;    /* KVC_RULE_EMA_CHAINED (InertiaKV sec 1 and sec
+                                3.1, the evaluated implementation: one EMA
+                                state updated after each layer): units are
+                                grouped by sequence, NL = chain_layers layers
+                                of Hkv = chain_heads KV heads (u = (b NL + l)
+                                Hkv + g; U a multiple of NL Hkv), every unit
+                                of a sequence holding the same positions in
+                                the same slots.  On a refresh step each
+                                slot's utility passes the layers in order,
+                                m = alpha m + (1 - alpha) s_l (m = s_l at the
+                                first observation), s_l the layer's mean
+                                over its Hkv units' probabilities (all H
+                                heads), and is stored in every unit; every
+                                unit of the sequence evicts the same slots
+                                (budget: the sequence's first unit's).  The
+                                call sequence runs (no fused kernel).  Other
+                                rules ignore both fields.                    */
+    int32_t chain_heads;
 } kvc_params;
 
 /* Guard of the ZIP-merge key formula: below this |weighted mean logit| the

@@ -81,11 +81,20 @@ kvc_status check_params(const kvc_params *p)
                   "cap = %d outside [1, %d]", p->cap, kMaxCap);
     KVC_CHECK_ARG(p->L >= 1 && p->L < p->cap, KVC_ERR_INVALID_ARG,
                   "L = %d must satisfy 1 <= L < cap = %d", p->L, p->cap);
-    KVC_CHECK_ARG(p->rule >= KVC_RULE_SINGLE && p->rule <= KVC_RULE_MI, KVC_ERR_INVALID_ARG,
-                  "rule = %d unknown", p->rule);
+    KVC_CHECK_ARG(p->rule >= KVC_RULE_SINGLE && p->rule <= KVC_RULE_EMA_CHAINED,
+                  KVC_ERR_INVALID_ARG, "rule = %d unknown", p->rule);
+    KVC_CHECK_ARG(p->rule != KVC_RULE_EMA_CHAINED ||
+                      (p->chain_layers >= 1 && p->chain_heads >= 1 &&
+                       p->U % (p->chain_layers * p->chain_heads) == 0),
+                  KVC_ERR_INVALID_ARG,
+                  "the layer-chained EMA needs chain_layers, chain_heads >= 1 dividing U = %d "
+                  "(got %d x %d)", p->U, p->chain_layers, p->chain_heads);
+    KVC_CHECK_ARG(p->rule != KVC_RULE_EMA_CHAINED || !p->merge, KVC_ERR_INVALID_ARG,
+                  "the layer-chained EMA is not combined with merging");
     KVC_CHECK_ARG(p->rule != KVC_RULE_MI || p->refresh_period == 1, KVC_ERR_INVALID_ARG,
                   "the moment-informed rule scores every step: refresh period must be 1");
-    KVC_CHECK_ARG(p->rule != KVC_RULE_EMA || (p->alpha >= 0.f && p->alpha < 1.f),
+    KVC_CHECK_ARG((p->rule != KVC_RULE_EMA && p->rule != KVC_RULE_EMA_CHAINED) ||
+                      (p->alpha >= 0.f && p->alpha < 1.f),
                   KVC_ERR_INVALID_ARG, "alpha = %g outside [0, 1)", (double)p->alpha);
     KVC_CHECK_ARG(p->refresh_period >= 0 && p->refresh_period <= p->L, KVC_ERR_INVALID_ARG,
                   "refresh period T = %d must satisfy 0 <= T <= L = %d (0 = Score-Free)",
@@ -384,7 +393,7 @@ kvc_status kvc_decode_step(const kvc_params *p, int32_t t, int32_t new_pos, int3
     KVC_CHECK_ARG(!p->merge || cache->votes != nullptr, KVC_ERR_INVALID_ARG,
                   "merge mode needs cache votes (merged slots carry p_e + p_c)");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (max_len == p->L + 1 && p->rule != KVC_RULE_MI) {
+    if (max_len == p->L + 1 && p->rule != KVC_RULE_MI && p->rule != KVC_RULE_EMA_CHAINED) {
         cudaError_t e = launch_fused_step(*p, t, new_pos, q, k_new, v_new, *cache, *mom, o, probs,
                                           kmax, evict_idx, evict_pos, n_evict, w, st);
         if (e != cudaErrorNotSupported) {

@@ -384,34 +384,14 @@ __device__ Key block_select(int n, int rank, KeyF key, ValidF valid,
     return prefix;
 }
 
-__global__ void __launch_bounds__(512) aggregate_kernel(AggArgs a)
+// Victim selection of unit u (len n): the k = n - budget smallest (utility,
+// position) pairs among its scored slots, in ascending slot order.  The
+// whole block calls it.
+__device__ void aggregate_select(const AggArgs &a, int u, int n, int *hist, int *bcast, int *scan)
 {
-    __shared__ int hist[256];
-    __shared__ int bcast[4];
-    __shared__ int scan[40];
-    const int u = blockIdx.x, tid = threadIdx.x;
-    const int n = a.len[u];
+    const int tid = threadIdx.x;
     double *util = a.util + (size_t)u * a.cap;
     const int32_t *pos = a.pos + (size_t)u * a.cap;
-    if (n < 0 || n > a.cap) {
-        if (tid == 0) { a.n_evict[u] = 0; record_status(a.status, KVC_ERR_SHAPE); }
-        return;
-    }
-    if (a.refresh) {
-        if (tid == 0) a.pend[(size_t)u * kPendStride] = 0;   // fused-step queue now stale
-        const double *pr = a.probs + (size_t)u * a.cap;
-        const double al = (double)a.alpha;
-        for (int i = tid; i < n; i += blockDim.x) {
-            const double s = pr[i], m = util[i];
-            double r;
-            if (isinf(m)) r = s;                           // first observation
-            else if (a.rule == KVC_RULE_SINGLE || a.rule == KVC_RULE_MI) r = s;   // MI: s is the score
-            else if (a.rule == KVC_RULE_CUMULATIVE) r = m + s;
-            else r = al * m + (1.0 - al) * s;
-            util[i] = r;
-        }
-        __syncthreads();
-    }
     const int Lb = a.budget ? a.budget[u] : a.L;      // this unit's budget
     if (Lb < 1 || Lb > a.L) {
         if (tid == 0) { a.n_evict[u] = 0; record_status(a.status, KVC_ERR_SHAPE); }
@@ -472,6 +452,95 @@ __global__ void __launch_bounds__(512) aggregate_kernel(AggArgs a)
     }
 }
 
+
+__global__ void __launch_bounds__(512) aggregate_kernel(AggArgs a)
+{
+    __shared__ int hist[256];
+    __shared__ int bcast[4];
+    __shared__ int scan[40];
+    const int u = blockIdx.x, tid = threadIdx.x;
+    const int n = a.len[u];
+    double *util = a.util + (size_t)u * a.cap;
+    const int32_t *pos = a.pos + (size_t)u * a.cap;
+    if (n < 0 || n > a.cap) {
+        if (tid == 0) { a.n_evict[u] = 0; record_status(a.status, KVC_ERR_SHAPE); }
+        return;
+    }
+    if (a.refresh) {
+        if (tid == 0) a.pend[(size_t)u * kPendStride] = 0;   // fused-step queue now stale
+        const double *pr = a.probs + (size_t)u * a.cap;
+        const double al = (double)a.alpha;
+        for (int i = tid; i < n; i += blockDim.x) {
+            const double s = pr[i], m = util[i];
+            double r;
+            if (isinf(m)) r = s;                           // first observation
+            else if (a.rule == KVC_RULE_SINGLE || a.rule == KVC_RULE_MI) r = s;   // MI: s is the score
+            else if (a.rule == KVC_RULE_CUMULATIVE) r = m + s;
+            else r = al * m + (1.0 - al) * s;
+            util[i] = r;
+        }
+        __syncthreads();
+    }
+    aggregate_select(a, u, n, hist, bcast, scan);
+}
+
+// InertiaKV's layer-chained EMA (rule KVC_RULE_EMA_CHAINED): one CTA per
+// sequence (its NL x Hkv units hold the same positions in the same slots).
+// On a refresh step every slot's utility passes the layers in order,
+// m = s_l at the first observation, else alpha m + (1 - alpha) s_l, with s_l
+// the layer's mean over its KV units' head-mean probabilities (all H heads),
+// and is stored in every unit of the sequence; the victims are selected once
+// (on the sequence's first unit) and written to every unit.
+__global__ void __launch_bounds__(512) aggregate_chained_kernel(AggArgs a, int NL, int Hkv)
+{
+    __shared__ int hist[256];
+    __shared__ int bcast[4];
+    __shared__ int scan[40];
+    __shared__ int okf;
+    const int per = NL * Hkv, u0 = blockIdx.x * per, tid = threadIdx.x;
+    const int n = a.len[u0];
+    if (tid == 0) okf = 1;
+    __syncthreads();
+    for (int q = tid; q < per; q += blockDim.x)
+        if (a.len[u0 + q] != n) okf = 0;
+    __syncthreads();
+    if (!okf || n < 0 || n > a.cap) {
+        for (int q = tid; q < per; q += blockDim.x) a.n_evict[u0 + q] = 0;
+        if (tid == 0) record_status(a.status, okf ? KVC_ERR_SHAPE : KVC_ERR_INVALID_ARG);
+        return;
+    }
+    if (a.refresh) {
+        for (int q = tid; q < per; q += blockDim.x) a.pend[(size_t)(u0 + q) * kPendStride] = 0;
+        const double al = (double)a.alpha, rh = 1.0 / Hkv;
+        for (int i = tid; i < n; i += blockDim.x) {
+            double m = a.util[(size_t)u0 * a.cap + i];
+            bool seen = !isinf(m);
+            for (int l = 0; l < NL; l++) {
+                double sl = 0.0;
+                for (int g = 0; g < Hkv; g++) sl += a.probs[(size_t)(u0 + l * Hkv + g) * a.cap + i];
+                sl *= rh;
+                m = seen ? al * m + (1.0 - al) * sl : sl;
+                seen = true;
+            }
+            for (int q = 0; q < per; q++) a.util[(size_t)(u0 + q) * a.cap + i] = m;
+        }
+        __syncthreads();
+    }
+    aggregate_select(a, u0, n, hist, bcast, scan);
+    __syncthreads();
+    // the sequence's other units take the same victims (global writes of this
+    // block are visible to it after the barrier)
+    const int k = a.n_evict[u0];
+    for (int q = 1; q < per; q++) {
+        if (tid == 0) a.n_evict[u0 + q] = k;
+        for (int e = tid; e < k; e += blockDim.x) {
+            a.evict_idx[(size_t)(u0 + q) * a.kmax + e] = a.evict_idx[(size_t)u0 * a.kmax + e];
+            if (a.evict_pos)
+                a.evict_pos[(size_t)(u0 + q) * a.kmax + e] = a.evict_pos[(size_t)u0 * a.kmax + e];
+        }
+    }
+}
+
 cudaError_t launch_aggregate(const kvc_params &p, int t, const double *probs,
                              const kvc_cache &c, int kmax, int32_t *evict_idx,
                              int32_t *evict_pos, int32_t *n_evict,
@@ -481,7 +550,12 @@ cudaError_t launch_aggregate(const kvc_params &p, int t, const double *probs,
               ws.status, ws.pend, p.cap, p.L, p.rule,
               p.rule == KVC_RULE_MI || is_refresh(t, p.refresh_period),
               kmax, p.alpha};
-    aggregate_kernel<<<p.U, 512, 0, st>>>(a);
+    if (p.rule == KVC_RULE_EMA_CHAINED) {
+        const int per = p.chain_layers * p.chain_heads;
+        aggregate_chained_kernel<<<p.U / per, 512, 0, st>>>(a, p.chain_layers, p.chain_heads);
+    } else {
+        aggregate_kernel<<<p.U, 512, 0, st>>>(a);
+    }
     return cudaGetLastError();
 }
 

@@ -20,7 +20,7 @@ KVC_OK = 0
 STATUS_NAMES = {0: "KVC_OK", 1: "KVC_ERR_INVALID_ARG", 2: "KVC_ERR_SHAPE",
                 3: "KVC_ERR_CUDA", 4: "KVC_ERR_TIMEOUT", 5: "KVC_ERR_UNSUPPORTED",
                 6: "KVC_ERR_WORKSPACE"}
-RULE_SINGLE, RULE_CUMULATIVE, RULE_EMA, RULE_MI = 0, 1, 2, 3
+RULE_SINGLE, RULE_CUMULATIVE, RULE_EMA, RULE_MI, RULE_EMA_CHAINED = 0, 1, 2, 3, 4
 CORR_OFF, CORR_ZERO_ORDER, CORR_FIRST_ORDER = 0, 1, 2
 ALLOC_GLOBAL, ALLOC_LAYER, ALLOC_HEAD = 0, 1, 2
 
@@ -45,7 +45,8 @@ class kvc_params(ctypes.Structure):
                 ("cap", ctypes.c_int32), ("L", ctypes.c_int32), ("rule", ctypes.c_int32),
                 ("alpha", ctypes.c_float), ("refresh_period", ctypes.c_int32),
                 ("correction", ctypes.c_int32), ("merge", ctypes.c_int32),
-                ("merge_recent", ctypes.c_int32), ("budget", ctypes.c_void_p)]
+                ("merge_recent", ctypes.c_int32), ("budget", ctypes.c_void_p),
+                ("chain_layers", ctypes.c_int32), ("chain_heads", ctypes.c_int32)]
 
 
 class kvc_cache(ctypes.Structure):
@@ -142,14 +143,17 @@ def _stream(stream):
 
 
 def make_params(U, G, cap, L, rule=RULE_EMA, alpha=0.9, refresh_period=1,
-                correction=CORR_FIRST_ORDER, d=128, merge_recent=None, budget=None) -> kvc_params:
+                correction=CORR_FIRST_ORDER, d=128, merge_recent=None, budget=None,
+                chain=None) -> kvc_params:
     """merge_recent = R (not None) turns on KeepKV ZIP-merging with the last R
     positions excluded from the partner search; budget (a device int32 [U]
-    tensor, kept alive by the caller) gives every unit its own budget."""
+    tensor, kept alive by the caller) gives every unit its own budget;
+    chain = (NL, Hkv) groups the units by sequence for the layer-chained EMA."""
     merge = 0 if merge_recent is None else 1
+    NL, Hkv = (0, 0) if chain is None else (int(chain[0]), int(chain[1]))
     return kvc_params(U, G, d, cap, L, rule, alpha, refresh_period, correction, merge,
                       0 if merge_recent is None else int(merge_recent),
-                      _ptr(budget, torch.int32, "budget", optional=True))
+                      _ptr(budget, torch.int32, "budget", optional=True), NL, Hkv)
 
 
 def make_cache(K, V, votes, pos, util, length) -> kvc_cache:

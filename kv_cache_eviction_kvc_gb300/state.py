@@ -15,7 +15,7 @@ class DecodeState:
                  alpha: float = 0.9, refresh_period: int = 1,
                  correction: int = K_.CORR_FIRST_ORDER, votes: bool = False,
                  kmax: int = 1, device="cuda", d: int = 128, merge_recent: int | None = None,
-                 budgets: bool = False):
+                 budgets: bool = False, chain=None):
         self.U, self.G, self.cap, self.L, self.d = U, G, cap, L, d
         self.device = torch.device(device)
         # per-unit budgets (a cache handed over from a prefill selection);
@@ -23,7 +23,7 @@ class DecodeState:
         self.budget = (torch.full((U,), L, dtype=torch.int32, device=self.device)
                        if budgets else None)
         self.params = K_.make_params(U, G, cap, L, rule, alpha, refresh_period, correction, d,
-                                     merge_recent, self.budget)
+                                     merge_recent, self.budget, chain)
         self.merge = merge_recent is not None
         if self.merge and not votes:
             raise ValueError("ZIP-merging needs per-slot votes (votes=True)")

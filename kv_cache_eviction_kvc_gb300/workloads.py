@@ -31,7 +31,7 @@ from dataclasses import dataclass, field, replace
 
 import torch
 
-RULE_SINGLE, RULE_CUMULATIVE, RULE_EMA, RULE_MI = 0, 1, 2, 3
+RULE_SINGLE, RULE_CUMULATIVE, RULE_EMA, RULE_MI, RULE_EMA_CHAINED = 0, 1, 2, 3, 4
 CORR_OFF, CORR_ZERO_ORDER, CORR_FIRST_ORDER = 0, 1, 2
 
 # fixed per-tensor seed offsets

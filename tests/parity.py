@@ -94,9 +94,13 @@ def run_decode_parity(cfg: W.DecodeConfig, *, steps: int | None = None, units=No
     cap = max(N + 1, L + 1) if cap is None else cap
     P = W.unit_params(cfg, device, seed)
     pre = W.gen_prefill(cfg, device, seed, cap=cap, P=P)
+    chained = cfg.rule == W.RULE_EMA_CHAINED
+    if chained:
+        assert len(units) == U, "the layer-chained EMA compares whole sequences"
     st = DecodeState(U, G, cap, L, rule=cfg.rule, alpha=cfg.alpha, refresh_period=cfg.T,
                      correction=cfg.correction, votes=bool(cfg.votes_max) or merge,
-                     kmax=max(1, N + 1 - L), device=device, merge_recent=cfg.merge_recent)
+                     kmax=max(1, N + 1 - L), device=device, merge_recent=cfg.merge_recent,
+                     chain=(cfg.NL, cfg.Hkv) if chained else None)
     st.load_prefill(pre["K"], pre["V"], pre["votes"], pre["pos"], pre["len"])
     sess = O.DecodeSession(len(units), G, d, cap + 1)
     Kh = pre["K"][uidx, :N].cpu()
@@ -199,7 +203,8 @@ def _step_loop(cfg, st, sess, units, uidx, P, seed, device, fused, S, n_len, L, 
                                  alpha=cfg.alpha, T=cfg.T, correction=cfg.correction,
                                  choose=None if mi else choose,
                                  merge_recent=cfg.merge_recent,
-                                 force_partner=partner_g, mi_forced=mi_forced)
+                                 force_partner=partner_g, mi_forced=mi_forced,
+                                 chain=(cfg.NL, cfg.Hkv))
         except ValueError as ex:
             rep.mismatches += 1
             rep.first_mismatch = rep.first_mismatch or f"step {t}: oracle refused: {ex}"

@@ -21,7 +21,7 @@ int main(void)
     kvc_params p;
     p.U = 2; p.G = 4; p.d = 128; p.cap = 100; p.L = 10; p.rule = KVC_RULE_EMA;
     p.alpha = 0.9f; p.refresh_period = 1; p.correction = KVC_CORR_FIRST_ORDER;
-    p.merge = 0; p.merge_recent = 0; p.budget = NULL;
+    p.merge = 0; p.merge_recent = 0; p.budget = NULL; p.chain_layers = 0; p.chain_heads = 0;
     printf("%zu %zu %zu %zu %zu %zu %d %zu\n", sizeof(kvc_params), sizeof(kvc_cache),
            sizeof(kvc_moments), offsetof(kvc_params, alpha), offsetof(kvc_params, merge_recent),
            kvc_decode_workspace_size(&p), kvc_version(), offsetof(kvc_params, budget));

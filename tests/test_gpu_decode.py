@@ -168,3 +168,18 @@ def test_prefill_handoff_then_decode(scorer, rule, T, pc):
     assert rep.decode.steps == 10
     if scorer == "laprox":
         assert rep.min_kept != rep.max_kept            # budgets really vary
+
+
+# ------------------------------------------------------ layer-chained EMA
+
+@pytest.mark.parametrize("cfg", [
+    W.C1.with_(rule=W.RULE_EMA_CHAINED, steps=24),                       # Llama-3.1-8B shape
+    SMALL.with_(rule=W.RULE_EMA_CHAINED, B=2, NL=3, Hq=8, Hkv=2, N=300, L=40, T=4,
+                votes_max=3),                                           # lazy, votes, 2 sequences
+], ids=["chained-c1", "chained-lazy-votes"])
+@pytest.mark.parametrize("fused", [True, False])
+def test_layer_chained_ema(cfg, fused):
+    """InertiaKV's evaluated aggregation: one EMA state per sequence passed
+    through the layers in order; every unit of a sequence evicts the same
+    positions (compared unit by unit against the oracle)."""
+    check(run_decode_parity(cfg, fused=fused))
