@@ -17,15 +17,9 @@
 // Refresh step: the pass covers the L slots plus the new token (a virtual
 // slot L).  Head-mean probabilities (InertiaKV sec 3.1 eq 1) update the
 // utilities (eqs 2-4); the T lowest pairs are selected; the first is the
-// victim and the rest form the queue.  With T <= kSel this happens between
-// the two passes: after pass 1 every CTA has its logits, the CTAs exchange
-// their softmax statistics (max, sum per head) through distributed shared
-// memory, score and select their own slots, exchange candidates, and pass 2
-// leaves the victim out, so the retained output comes out directly while
-// the fold warp folds the victim (the producer keeps streaming V meanwhile).
-// Longer queues select after both passes: the victim's share is removed from
-// the merged output by the eviction-error identity (KeepKV eq 3), or the
-// retained output is recomputed when its mass exceeds 1/2 in some head.
+// victim and the rest form the queue.  The victim's share is removed from the
+// merged output by the eviction-error identity (KeepKV eq 3); when its mass
+// exceeds 1/2 in some head the retained output is recomputed instead.
 //
 // Both: the victim is folded into the moments (West's weighted incremental
 // update of the mean / covariance form), and the normalization correction of
@@ -55,7 +49,6 @@ constexpr int kTile = 64;              // slots per ring stage: 16 per consumer 
 constexpr int kBoxBytes = kTile * 128; // one box: 64 rows x 64 bf16, 128B-swizzled
 constexpr int kTileBytes = 2 * kBoxBytes;
 constexpr int kStages = 4;
-constexpr int kSel = 8;                // longest queue selected between the passes
 
 __device__ __forceinline__ uint32_t sw_off(int r, int j) { return sw_off_t<kTile>(r, j); }
 __device__ __forceinline__ void consumer_sync() { named_sync<kNC * 32>(); }
@@ -102,11 +95,6 @@ struct FusedSmem {
     uint64_t full[kStages];     // ring: stage filled (producer -> consumers)
     uint64_t empty[kStages];    // ring: stage drained (consumers -> producer)
     uint64_t vready;            // late victim: every CTA's candidate published
-    uint64_t lready;            // refresh: every CTA's pass-1 max / sum published
-    uint64_t cready;            // refresh: every CTA's candidates published
-    uint64_t vknown;            // refresh: the victim is known (consumers -> fold warp)
-    float pubM[G], pubL[G];     // this CTA's pass-1 max and sum per head (published)
-    Cand wsel[kNC][kSel];       // per consumer warp: its lowest candidates
     float qs[G][kD];            // q / sqrt(d), fp32
     float red[kWarps][G];
     float pM[G], pl[G];         // this CTA's partial max / sum
@@ -238,9 +226,6 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             mbar_init(&S.empty[j], kNC);
         }
         mbar_init(&S.vready, CS);
-        mbar_init(&S.lready, CS);
-        mbar_init(&S.cready, CS);
-        mbar_init(&S.vknown, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -283,11 +268,6 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
         }
         late = victim < 0;                  // uniform over the cluster
     }
-    // queue length of a refresh step: T (one victim per step until the next
-    // refresh); a Score-Free run (T = 0, no later refresh) queues as many as
-    // fit (merge mode keeps no queue: a merge changes the partner's utility)
-    const int Tq = a.merge ? 1 : (a.T > 0 ? a.T : kMaxQueue);
-    const bool early = refresh && Tq <= kSel;     // select between the passes
     // the new token is a separate (virtual) slot L on refresh steps, on late
     // lazy steps and in merge mode; otherwise it replaces the victim's row
     const bool has_new = (refresh || a.merge || late) && (r == CS - 1);
@@ -309,8 +289,8 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
     }
     __syncthreads();
 
-    // every CTA's barriers are initialized before any remote arrival
-    if (late || early) cluster.sync();
+    // every CTA's vready barrier is initialized before any remote arrival
+    if (late) cluster.sync();
 
     // the late victim: the lowest candidate over the cluster's CTAs (each CTA
     // publishes its own before arriving on everyone's vready)
@@ -325,184 +305,6 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             if (R->ncand > 0 && cand_less(R->cand[0], b)) b = R->cand[0];
         }
         return b.slot;
-    };
-
-    // Refresh-step selection between the passes (consumer warps; S.pM holds
-    // this CTA's pass-1 max per head, XS its logits, the virtual slot L
-    // included).  Returns the victim's slot (L = the new token), or -1 when a
-    // cluster wait ran out.
-    auto refresh_select = [&]() -> int {
-        // this CTA's pass-1 sum per head, relative to its max
-        float lp[G];
-#pragma unroll
-        for (int h = 0; h < G; h++) lp[h] = 0.f;
-        for (int li = tid; li < nloc; li += kNC * 32)
-#pragma unroll
-            for (int h = 0; h < G; h++) lp[h] += expf(XS(h, li) - S.pM[h]);
-#pragma unroll
-        for (int h = 0; h < G; h++) {
-            const float v = warp_sum(lp[h]);
-            if (lane == 0) S.red[w][h] = v;
-        }
-        consumer_sync();
-        if (tid == 0) {
-            for (int h = 0; h < G; h++) {
-                float l = 0.f;
-                for (int j = 0; j < kNC; j++) l += S.red[j][h];
-                S.pubL[h] = l;
-                S.pubM[h] = S.pM[h];
-            }
-            for (int q = 0; q < CS; q++) mbar_arrive_remote(&S.lready, (uint32_t)q);
-        }
-        bool ok = mbar_wait_cluster(&S.lready, 0);
-        if (tid < G) {
-            // merged max and sum of the step's softmax (every slot and the
-            // new token), (1/G) / sum in fp64 (G is a power of two)
-            const int h = tid;
-            float M = -INFINITY;
-            for (int q = 0; q < CS; q++) M = fmaxf(M, cluster.map_shared_rank(&S, q)->pubM[h]);
-            float l = 0.f;
-            for (int q = 0; q < CS; q++) {
-                FusedSmem<G> *R = cluster.map_shared_rank(&S, q);
-                if (R->pubM[h] != -INFINITY) l += R->pubL[h] * expf(R->pubM[h] - M);
-            }
-            S.gM[h] = M;
-            S.igl[h] = (1.0 / G) / (double)l;
-            S.igl32[h] = (float)S.igl[h];
-        }
-        consumer_sync();
-        // head-mean probabilities, utilities, and this thread's lowest
-        // (utility, position) pairs, ascending, in registers
-        const double al = (double)a.alpha;
-        const Cand none{~0ull, 0x7fffffff, -1};
-        Cand lst[kSel];
-#pragma unroll
-        for (int j = 0; j < kSel; j++) lst[j] = none;
-        for (int li0 = tid; li0 < nloc; li0 += 4 * kNC * 32) {
-            double mo[4];
-            int32_t po[4];
-#pragma unroll
-            for (int b = 0; b < 4; b++) {       // independent loads first
-                const int li = li0 + b * kNC * 32, i = s0 + li;
-                const bool in = li < nloc, isv = in && i == L;
-                mo[b] = (in && !isv) ? a.util[ubase + i] : __longlong_as_double(0x7ff0000000000000ll);
-                po[b] = (in && !isv) ? a.pos[ubase + i] : a.new_pos;
-            }
-#pragma unroll
-            for (int b = 0; b < 4; b++) {
-                const int li = li0 + b * kNC * 32, i = s0 + li;
-                if (li >= nloc) break;
-                // head-mean probability: fp32 while the largest head term is
-                // above e^-60 (the sum then lies far inside fp32's range),
-                // the fp64 form below that
-                float y[G], ymax = -INFINITY;
-#pragma unroll
-                for (int h = 0; h < G; h++) {
-                    y[h] = XS(h, li) - S.gM[h];
-                    ymax = fmaxf(ymax, y[h]);
-                }
-                double sp;
-                if (ymax > -60.f) {
-                    float s32 = 0.f;
-#pragma unroll
-                    for (int h = 0; h < G; h++) s32 = fmaf(expf(y[h]), S.igl32[h], s32);
-                    sp = (double)s32;
-                } else {
-                    sp = 0.0;
-#pragma unroll
-                    for (int h = 0; h < G; h++) sp = fma(exp_wide(y[h]), S.igl[h], sp);
-                }
-                const double m = mo[b];
-                double mn;
-                if (isinf(m)) mn = sp;
-                else if (a.rule == KVC_RULE_SINGLE) mn = sp;
-                else if (a.rule == KVC_RULE_CUMULATIVE) mn = m + sp;
-                else mn = al * m + (1.0 - al) * sp;
-                if (i != L) a.util[ubase + i] = mn;
-                else S.vm = mn;
-                if (a.probs) a.probs[ubase + i] = sp;
-                Cand x{double_key(mn), po[b], i};
-#pragma unroll
-                for (int j = 0; j < kSel; j++)
-                    if (cand_less(x, lst[j])) { const Cand t_ = lst[j]; lst[j] = x; x = t_; }
-            }
-        }
-        // warp: the Tq lowest by repeated minima over the list heads
-        for (int rnd = 0; rnd < Tq; rnd++) {
-            const Cand c1 = lst[0];
-            const uint32_t hi = (uint32_t)(c1.key >> 32), lo = (uint32_t)c1.key;
-            const uint32_t mhi = __reduce_min_sync(kFull, hi);
-            const uint32_t mlo = __reduce_min_sync(kFull, hi == mhi ? lo : 0xffffffffu);
-            const bool tie = hi == mhi && lo == mlo;
-            const uint32_t mpos = __reduce_min_sync(kFull, tie ? (uint32_t)c1.pos ^ 0x80000000u : 0xffffffffu);
-            const bool win = tie && ((uint32_t)c1.pos ^ 0x80000000u) == mpos && c1.slot >= 0;
-            const uint32_t wm = __ballot_sync(kFull, win);
-            if (wm == 0u) {
-                if (lane == 0) S.wsel[w][rnd] = none;
-                continue;
-            }
-            const int src = __ffs(wm) - 1;
-            if (lane == src) {
-                S.wsel[w][rnd] = c1;
-#pragma unroll
-                for (int j = 0; j < kSel - 1; j++) lst[j] = lst[j + 1];
-                lst[kSel - 1] = none;
-            }
-        }
-        consumer_sync();
-        if (tid == 0) {
-            int ptr[kNC];
-            for (int q = 0; q < kNC; q++) ptr[q] = 0;
-            int nc = 0;
-            for (; nc < Tq; nc++) {
-                int bq = -1;
-                Cand b = none;
-                for (int q = 0; q < kNC; q++) {
-                    if (ptr[q] >= Tq) continue;
-                    const Cand cq = S.wsel[q][ptr[q]];
-                    if (cq.slot >= 0 && cand_less(cq, b)) { b = cq; bq = q; }
-                }
-                if (bq < 0) break;
-                ptr[bq]++;
-                S.cand[nc] = b;
-            }
-            S.ncand = nc;
-            for (int q = 0; q < CS; q++) mbar_arrive_remote(&S.cready, (uint32_t)q);
-        }
-        ok = mbar_wait_cluster(&S.cready, 0) && ok;
-        if (tid == 0) {
-            // every CTA merges the candidate lists the same way
-            int ptr[kFusedMaxCS];
-            for (int q = 0; q < CS; q++) ptr[q] = 0;
-            Cand sel[kSel];
-            int nsel = 0;
-            while (ok && nsel < Tq) {
-                int bq = -1;
-                Cand b = none;
-                for (int q = 0; q < CS; q++) {
-                    FusedSmem<G> *R = cluster.map_shared_rank(&S, q);
-                    if (ptr[q] >= min(Tq, R->ncand)) continue;
-                    const Cand cq = R->cand[ptr[q]];
-                    if (cq.slot >= 0 && cand_less(cq, b)) { b = cq; bq = q; }
-                }
-                if (bq < 0) break;
-                ptr[bq]++;
-                sel[nsel++] = b;
-            }
-            const int v = nsel > 0 && sel[0].slot >= 0 && sel[0].slot <= L ? sel[0].slot : -1;
-            S.victim = v;
-            if (!ok) atomicExch(&S.bad, 1);
-            if (r == 0 && v >= 0) {
-                int32_t *pq = a.pend + (size_t)u * kPendStride;
-                pq[0] = a.merge ? 0 : a.t;
-                pq[1] = nsel - 1;
-                for (int j = 1; j < nsel; j++)
-                    pq[2 + j - 1] = sel[j].slot == L ? sel[0].slot : sel[j].slot;
-            }
-            mbar_arrive(&S.vknown);               // the fold warp may fold now
-        }
-        consumer_sync();
-        return S.victim;
     };
 
     // ------------------------------------------------ passes 1 and 2 over the ring
@@ -652,25 +454,6 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             }
             __syncwarp();
             fold(lane, 32, false);
-        } else if (early) {
-            // the consumers select the victim between the passes; fold it
-            // while they run pass 2
-            const int v = mbar_wait(&S.vknown, 0) ? *(volatile int *)&S.victim : -1;
-            if (v >= 0) {
-                const bool isv = (v == L);
-                const uint16_t *kr = isv ? knew : a.K + (ubase + v) * kD;
-                const uint16_t *vr = isv ? vnew : a.V + (ubase + v) * kD;
-                for (int e = lane; e < kD; e += 32) {
-                    S.vk[e] = bf2f(kr[e]);
-                    S.vv[e] = bf2f(vr[e]);
-                }
-                if (lane == 0) {
-                    S.vp = a.merge ? 0.f : ((isv || !a.votes) ? 1.f : (float)a.votes[ubase + v]);
-                    S.vpos = isv ? a.new_pos : a.pos[ubase + v];
-                }
-                __syncwarp();
-                fold(lane, 32, false);
-            }
         }
     } else if (w == kNC) {
         // ---------------- producer
@@ -826,14 +609,9 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
         consumer_sync();                          // S.red is reused below
         // a late victim leaves pass 2 (evict mode)
         int vmask = -1;
-        bool drop_new = false;                    // the victim is the new token
         if (late) {
             const int v = late_victim();
             if (!a.merge && v >= s0 && v < s1) vmask = v - s0;
-        } else if (early) {
-            const int v = refresh_select();
-            if (!a.merge && v >= s0 && v < s1) vmask = v - s0;
-            drop_new = !a.merge && v == L;
         }
         // pass 2: O^T += V^T P^T
         for (int t = 0; t < ntile; t++, g++) {
@@ -871,7 +649,7 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             __syncwarp();
             if (lane == 0 && good) mbar_arrive(&S.empty[stage]);
         }
-        if (has_new && w == 0 && !drop_new) {
+        if (has_new && w == 0) {
             float pn0 = 0.f, pn1 = 0.f, pnq = 0.f;
             const float M0 = h0 < G ? S.pM[h0] : 0.f, M1 = h1 < G ? S.pM[h1] : 0.f;
 #pragma unroll
@@ -1026,27 +804,8 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
         }
     }
 
-    if (early) {
-        victim = S.victim;
-        if (victim < 0) {                       // a cluster wait ran out: refuse
-            if (r == 0 && tid == 0) {
-                record_status(a.status, KVC_ERR_TIMEOUT);
-                a.n_evict[u] = 0;
-            }
-            cluster.sync();                     // nobody reads this CTA's partials any more
-            return;
-        }
-    }
-
     int vic_owner;
-    if (early) {
-        // pass 2 left the victim out (merge mode kept it): the merged
-        // partials are the retained output
-        vic_owner = (victim == L) ? CS - 1 : victim / ch;
-        for (int e = tid; e < G * kD; e += blockDim.x) S.fR[e / kD][e % kD] /= S.gl[e / kD];
-        if (tid < G) S.lzR[tid] = S.gM[tid] + logf(S.gl[tid]);
-        __syncthreads();
-    } else if (refresh) {
+    if (refresh) {
         // -------------------------------------------- probabilities + utilities
         const double al = (double)a.alpha;
         if (tid < G) {
@@ -1109,6 +868,10 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
         // low word, then position among equal keys), the winning lane
         // promotes its second entry and rescans only when it wins again.
         // Thread 0 then merges the sorted per-warp lists.
+        // queue length: T (one victim per step until the next refresh); a
+        // Score-Free run (T = 0, no later refresh) queues as many as fit
+        // (merge mode keeps no queue: a merge changes the partner's utility)
+        const int Tq = a.merge ? 1 : (a.T > 0 ? a.T : kMaxQueue);
         const int want = min(Tq, nloc);
         Cand *wl = reinterpret_cast<Cand *>(chosen + align_up((size_t)(ch + 1)));   // [kWarps][kMaxQueue]
         const Cand none{~0ull, 0x7fffffff, -1};
@@ -1283,7 +1046,7 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
         __syncthreads();
     }
 
-    if (refresh && !early) fold(tid, blockDim.x, true);   // otherwise folded during the passes
+    if (refresh) fold(tid, blockDim.x, true);         // lazy steps folded during the passes
     const float n1 = S.n0 + S.vp;
     for (int h = tid; h < G; h += blockDim.x) {
         const float logZE = logf(n1) + S.zq[h];
