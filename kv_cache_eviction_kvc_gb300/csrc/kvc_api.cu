@@ -393,9 +393,19 @@ kvc_status kvc_decode_step(const kvc_params *p, int32_t t, int32_t new_pos, int3
     KVC_CHECK_ARG(!p->merge || cache->votes != nullptr, KVC_ERR_INVALID_ARG,
                   "merge mode needs cache votes (merged slots carry p_e + p_c)");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (max_len == p->L + 1 && p->rule != KVC_RULE_MI && p->rule != KVC_RULE_EMA_CHAINED) {
-        cudaError_t e = launch_fused_step(*p, t, new_pos, q, k_new, v_new, *cache, *mom, o, probs,
-                                          kmax, evict_idx, evict_pos, n_evict, w, st);
+    if (max_len == p->L + 1 && p->rule != KVC_RULE_EMA_CHAINED) {
+        // the moment-informed rule: the residual norms of every slot and the
+        // new token first (tensor cores), then the fused step scores
+        // alpha ||r|| in its refresh epilogue
+        float *rr = nullptr;
+        cudaError_t e = cudaSuccess;
+        if (p->rule == KVC_RULE_MI) {
+            rr = w.xbuf;
+            e = launch_mi_norms(*p, *cache, *mom, k_new, v_new, rr, w.status, st);
+        }
+        if (e == cudaSuccess)
+            e = launch_fused_step(*p, t, new_pos, q, k_new, v_new, *cache, *mom, o, probs, kmax,
+                                  evict_idx, evict_pos, n_evict, w, st, rr);
         if (e != cudaErrorNotSupported) {
             if (e != cudaSuccess || !p->merge) return cuda_status(e, "kvc_decode_step fused launch");
             // merge mode: the fused kernel attended over every slot, appended

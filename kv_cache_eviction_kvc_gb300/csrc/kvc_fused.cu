@@ -65,6 +65,7 @@ struct FusedArgs {
     int32_t *evict_idx, *evict_pos, *n_evict;
     int32_t *pend, *status;
     const int32_t *budget;      // per-unit budgets (NULL: L for every unit)
+    const float *rr;            // moment-informed rule: ||r|| per slot ([U][cap], the new token at L)
     int cap, L, T, rule, correction, t, new_pos, kmax, chunk;
     float alpha;
     int merge;                  // KeepKV merge mode: attend over L + 1, append at L
@@ -533,10 +534,21 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             return any;
         };
         int g = 0;
+        // votes of this lane's two slots of a tile (gq, gq + 8), loaded one
+        // tile ahead so that the loads are in flight during the previous tile
+        auto load_votes = [&](int t, int &v0, int &v1) {
+            const int li = t * kTile + rb + gq;
+            v0 = li < nrows ? a.votes[ubase + s0 + li] : 1;
+            v1 = li + 8 < nrows ? a.votes[ubase + s0 + li + 8] : 1;
+        };
+        int vn0 = 1, vn1 = 1;
+        if (a.votes && ntile > 0) load_votes(0, vn0, vn1);
         // pass 1: logits
         for (int t = 0; t < ntile; t++, g++) {
             const int stage = g % kStages;
             const uint32_t ph = (uint32_t)(g / kStages) & 1u;
+            const int vc[2] = {vn0, vn1};
+            if (a.votes && t + 1 < ntile) load_votes(t + 1, vn0, vn1);
             if (good && !mbar_wait(&S.full[stage], ph)) good = false;
             if (good) {
                 const uint32_t so = (uint32_t)stage * kTileBytes;
@@ -555,7 +567,7 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
                     const int li = t * kTile + rb + gq + 8 * hf;
                     if (li < nrows) {
                         const bool isnew = (s0 + li == pvict);
-                        const float lnp = (!isnew && a.votes) ? logf((float)a.votes[ubase + s0 + li]) : 0.f;
+                        const float lnp = (!isnew && a.votes) ? logf((float)vc[hf]) : 0.f;
                         if (h0 < G) {
                             const float x = sacc[2 * hf] * rs + lnp;
                             XS(h0, li) = x;
@@ -849,7 +861,8 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             const bool isv = (i == L);
             const double m = msm[li];
             double mn;
-            if (isinf(m)) mn = s;
+            if (a.rule == KVC_RULE_MI) mn = s * (double)a.rr[ubase + i];   // MomentKV alpha ||r||
+            else if (isinf(m)) mn = s;
             else if (a.rule == KVC_RULE_SINGLE) mn = s;
             else if (a.rule == KVC_RULE_CUMULATIVE) mn = m + s;
             else mn = al * m + (1.0 - al) * s;
@@ -1154,8 +1167,9 @@ cudaError_t launch_fused_step(const kvc_params &p, int t, int new_pos, const uin
                               const uint16_t *k_new, const uint16_t *v_new, const kvc_cache &c,
                               const kvc_moments &m, float *o, double *probs, int kmax,
                               int32_t *evict_idx, int32_t *evict_pos, int32_t *n_evict,
-                              const DecodeWs &ws, cudaStream_t st)
+                              const DecodeWs &ws, cudaStream_t st, const float *rr)
 {
+    if (p.rule == KVC_RULE_MI && (rr == nullptr || p.refresh_period != 1)) return cudaErrorNotSupported;
     if (p.refresh_period > kMaxQueue) return cudaErrorNotSupported;
     // merge mode: every unit must find a partner (positions are distinct, so
     // at most R of the other L slots are recent: R < L guarantees one), and
@@ -1166,7 +1180,7 @@ cudaError_t launch_fused_step(const kvc_params &p, int t, int new_pos, const uin
     if (chunk > kFusedMaxChunk || p.L + 1 > p.cap) return cudaErrorNotSupported;
     FusedArgs a{q, k_new, v_new, c.K, c.V, c.votes, c.pos, c.util, c.len,
                 m.n, m.mu_k, m.mu_v, m.C, o, probs, evict_idx, evict_pos, n_evict,
-                ws.pend, ws.status, p.budget, p.cap, p.L, p.refresh_period, p.rule,
+                ws.pend, ws.status, p.budget, rr, p.cap, p.L, p.refresh_period, p.rule,
                 p.correction, t, new_pos, kmax, chunk, p.alpha, p.merge};
     switch (p.G) {
     case 1: return launch_fused_g<1>(a, p.U, CS, st);

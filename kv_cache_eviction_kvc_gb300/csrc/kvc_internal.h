@@ -77,6 +77,7 @@ cudaError_t launch_fused_step(const kvc_params &p, int t, int new_pos,
                               const kvc_moments &m, float *o, double *probs,
                               int kmax, int32_t *evict_idx,
                               int32_t *evict_pos, int32_t *n_evict,
-                              const DecodeWs &ws, cudaStream_t st);
+                              const DecodeWs &ws, cudaStream_t st,
+                              const float *rr = nullptr);
 
 }  // namespace kvc

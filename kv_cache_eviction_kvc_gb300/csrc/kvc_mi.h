@@ -26,4 +26,13 @@ cudaError_t launch_mi_greedy(const kvc_params &p, const kvc_cache &c, const kvc_
                              int32_t *evict_pos, int32_t *n_evict, int32_t *status,
                              cudaStream_t st);
 
+// ||r_i|| of every live slot i < len[u] of every unit into rr[u][i], and of
+// the step's new token (k_new, v_new) into rr[u][len[u]] (fp32): the
+// contraction on tensor cores (tcgen05, C as three bf16 terms), the moments
+// as they are.  Returns cudaErrorNotSupported when the key tensor map cannot
+// be encoded (more than 2^31 rows).
+cudaError_t launch_mi_norms(const kvc_params &p, const kvc_cache &c, const kvc_moments &m,
+                            const uint16_t *k_new, const uint16_t *v_new, float *rr,
+                            int32_t *status, cudaStream_t st);
+
 }  // namespace kvc
