@@ -46,3 +46,11 @@ def test_moment_informed_flops_and_fp32_peak():
     if os.path.exists(path):
         mhz = float(json.load(open(path)).get("sm_max_mhz", mhz))
     assert bench.fp32_peak_tflops() == pytest.approx(152 * 128 * 2 * mhz * 1e6 / 1e12)
+
+
+def test_moment_informed_norm_bytes():
+    """Keys and values of L slots, C, the two means, the new token, the norms
+    written then read by the fused step, per unit."""
+    d, L, U = 128, 3277, 4608
+    per = 2 * L * d * 2 + d * d * 4 + 2 * d * 4 + 2 * d * 2 + (L + 1) * 8
+    assert bench.mi_norm_bytes(W.C2_MI) == per * U
