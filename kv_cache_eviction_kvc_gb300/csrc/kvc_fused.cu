@@ -19,14 +19,7 @@
 // utilities (eqs 2-4); the T lowest pairs are selected; the first is the
 // victim and the rest form the queue.  The victim's share is removed from the
 // merged output by the eviction-error identity (KeepKV eq 3); when its mass
-// exceeds 1/2 in some head the retained output is recomputed instead.  With
-// queues up to kSel the fold warp does the refresh work while the consumers
-// run pass 2: during pass 1 it forms C q for the CTA's rows of C; once pass 1
-// has fixed the logits, the CTAs exchange their softmax statistics through
-// distributed shared memory, the fold warp scores and selects the CTA's
-// slots, the CTAs exchange candidates and the victim, and the victim's fold
-// enters C q as a rank-one term; the epilogue is left with the merge, the
-// identity and the write-back of C.
+// exceeds 1/2 in some head the retained output is recomputed instead.
 //
 // Both: the victim is folded into the moments (West's weighted incremental
 // update of the mean / covariance form), and the normalization correction of
@@ -56,7 +49,6 @@ constexpr int kTile = 64;              // slots per ring stage: 16 per consumer 
 constexpr int kBoxBytes = kTile * 128; // one box: 64 rows x 64 bf16, 128B-swizzled
 constexpr int kTileBytes = 2 * kBoxBytes;
 constexpr int kStages = 4;
-constexpr int kSel = 8;                // longest queue the fold warp selects during pass 2
 
 __device__ __forceinline__ uint32_t sw_off(int r, int j) { return sw_off_t<kTile>(r, j); }
 __device__ __forceinline__ void consumer_sync() { named_sync<kNC * 32>(); }
@@ -103,15 +95,7 @@ template <int G>
 struct FusedSmem {
     uint64_t full[kStages];     // ring: stage filled (producer -> consumers)
     uint64_t empty[kStages];    // ring: stage drained (consumers -> producer)
-    uint64_t vready;            // late victim: every CTA's candidate published;
-                                // refresh (fold warp): every CTA's victim data published
-    uint64_t p1done;            // refresh: pass 1 done, logits and CTA max in place
-    uint64_t lready;            // refresh: every CTA's pass-1 max / sum published
-    uint64_t cready;            // refresh: every CTA's candidates published
-    uint64_t vpub;              // refresh: every CTA's fold warp passed the victim
-                                // publication (32 lanes of each CTA arrive)
-    float pubM[G], pubL[G];     // this CTA's pass-1 max and sum per head (published)
-    float ve[kD];               // the victim's value row (kept for the identity)
+    uint64_t vready;            // late victim: every CTA's candidate published
     float qs[G][kD];            // q / sqrt(d), fp32
     float red[kWarps][G];
     float pM[G], pl[G];         // this CTA's partial max / sum
@@ -243,10 +227,6 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             mbar_init(&S.empty[j], kNC);
         }
         mbar_init(&S.vready, CS);
-        mbar_init(&S.p1done, 1);
-        mbar_init(&S.lready, CS);
-        mbar_init(&S.cready, CS);
-        mbar_init(&S.vpub, 32 * CS);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -289,11 +269,6 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
         }
         late = victim < 0;                  // uniform over the cluster
     }
-    // queue length of a refresh step: T (one victim per step until the next
-    // refresh); a Score-Free run (T = 0, no later refresh) queues as many as
-    // fit (merge mode keeps no queue: a merge changes the partner's utility)
-    const int Tq = a.merge ? 1 : (a.T > 0 ? a.T : kMaxQueue);
-    const bool fw = refresh && Tq <= kSel;      // the fold warp does the refresh work
     // the new token is a separate (virtual) slot L on refresh steps, on late
     // lazy steps and in merge mode; otherwise it replaces the victim's row
     const bool has_new = (refresh || a.merge || late) && (r == CS - 1);
@@ -315,8 +290,8 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
     }
     __syncthreads();
 
-    // every CTA's barriers are initialized before any remote arrival
-    if (late || fw) cluster.sync();
+    // every CTA's vready barrier is initialized before any remote arrival
+    if (late) cluster.sync();
 
     // the late victim: the lowest candidate over the cluster's CTAs (each CTA
     // publishes its own before arriving on everyone's vready)
@@ -429,23 +404,22 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
         psync();
     };
 
-    // ---------------- the refresh work of the fold warp (fw steps)
-    auto refresh_worker = [&]() {
-        const Cand none{~0ull, 0x7fffffff, -1};
-        bool ok = true;
-        // (1) this CTA's utilities and positions into L2 for the selection
-        {
-            const char *ub = reinterpret_cast<const char *>(a.util + ubase + s0);
-            const char *pb = reinterpret_cast<const char *>(a.pos + ubase + s0);
-            for (int o = lane * 128; o < (s1 - s0) * 8; o += 32 * 128)
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(ub + o));
-            for (int o = lane * 128; o < (s1 - s0) * 4; o += 32 * 128)
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(pb + o));
-        }
-        // (2) C q / sqrt(d) for this CTA's rows of C (q already carries
-        // 1/sqrt(d)); two rows per lane per round (lane -> row quarter)
+    // Refresh steps: the victim is only known after both passes, but the
+    // costly part of its fold does not depend on it.  The fold warp, idle
+    // during the passes, forms C q / sqrt(d) for the CTA's rows of C (two
+    // rows per lane per round; q already carries 1/sqrt(d)), which brings
+    // those rows into L2 for the write-back, and prefetches the utilities
+    // and positions the epilogue reads.  The fold then enters C q as a
+    // rank-one term (fold_cq below).
+    auto refresh_prep = [&]() {
+        const char *ub = reinterpret_cast<const char *>(a.util + ubase + s0);
+        const char *pb = reinterpret_cast<const char *>(a.pos + ubase + s0);
+        for (int o = lane * 128; o < (s1 - s0) * 8; o += 32 * 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(ub + o));
+        for (int o = lane * 128; o < (s1 - s0) * 4; o += 32 * 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(pb + o));
+        const int q4 = lane & 3;
         for (int rb = r0; rb < r1; rb += 16) {
-            const int q4 = lane & 3;
             float4 cv[2][8];
             bool vr_[2];
 #pragma unroll
@@ -482,231 +456,60 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
                 }
             }
         }
-        // (3) pass 1 done: the logits of every slot and the CTA max
-        ok = mbar_wait(&S.p1done, 0);
-        // (4) this CTA's sums relative to its max; publish; merge over the cluster
-        float lp[G];
-#pragma unroll
-        for (int h = 0; h < G; h++) lp[h] = 0.f;
-        if (ok)
-            for (int li = lane; li < nloc; li += 32)
-#pragma unroll
-                for (int h = 0; h < G; h++) lp[h] += expf(XS(h, li) - S.pM[h]);
-#pragma unroll
-        for (int h = 0; h < G; h++) lp[h] = warp_sum(lp[h]);
-        if (lane == 0) {
-#pragma unroll
-            for (int h = 0; h < G; h++) {
-                S.pubM[h] = S.pM[h];
-                S.pubL[h] = lp[h];
-            }
-            for (int qc = 0; qc < CS; qc++) mbar_arrive_remote(&S.lready, (uint32_t)qc);
-        }
-        __syncwarp();
-        ok = mbar_wait_cluster(&S.lready, 0) && ok;
-        float gm[G];
-        double ig[G];
-        float ig32[G];
-#pragma unroll
-        for (int h = 0; h < G; h++) {
-            float M = -INFINITY;
-            for (int qc = 0; qc < CS; qc++) M = fmaxf(M, cluster.map_shared_rank(&S, qc)->pubM[h]);
-            float l = 0.f;
-            for (int qc = 0; qc < CS; qc++) {
-                FusedSmem<G> *R = cluster.map_shared_rank(&S, qc);
-                if (R->pubM[h] != -INFINITY) l += R->pubL[h] * expf(R->pubM[h] - M);
-            }
-            gm[h] = M;
-            ig[h] = (1.0 / G) / (double)l;     // G is a power of two: the 1/G factor is exact
-            ig32[h] = (float)ig[h];
-        }
-        // (5) probabilities, utilities and this lane's lowest (utility,
-        // position) pairs, ascending, in registers
-        const double al = (double)a.alpha;
-        Cand lst[kSel];
-#pragma unroll
-        for (int j = 0; j < kSel; j++) lst[j] = none;
-        for (int li0 = lane; li0 < nloc && ok; li0 += 4 * 32) {
-            double mo[4];
-            int32_t po[4];
-#pragma unroll
-            for (int b = 0; b < 4; b++) {       // independent loads first
-                const int li = li0 + 32 * b, i = s0 + li;
-                const bool in = li < nloc, isv = in && i == L;
-                mo[b] = (in && !isv) ? a.util[ubase + i] : __longlong_as_double(0x7ff0000000000000ll);
-                po[b] = (in && !isv) ? a.pos[ubase + i] : a.new_pos;
-            }
-#pragma unroll
-            for (int b = 0; b < 4; b++) {
-                const int li = li0 + 32 * b, i = s0 + li;
-                if (li >= nloc) break;
-                // head-mean probability: fp32 while the largest head term is
-                // above e^-60 (the sum lies far inside fp32's range), else fp64
-                float y[G], ymax = -INFINITY;
-#pragma unroll
-                for (int h = 0; h < G; h++) {
-                    y[h] = XS(h, li) - gm[h];
-                    ymax = fmaxf(ymax, y[h]);
-                }
-                double sp;
-                if (ymax > -60.f) {
-                    float s32 = 0.f;
-#pragma unroll
-                    for (int h = 0; h < G; h++) s32 = fmaf(expf(y[h]), ig32[h], s32);
-                    sp = (double)s32;
-                } else {
-                    sp = 0.0;
-#pragma unroll
-                    for (int h = 0; h < G; h++) sp = fma(exp_wide(y[h]), ig[h], sp);
-                }
-                const double m = mo[b];
-                double mn;
-                if (a.rule == KVC_RULE_MI) mn = sp * (double)a.rr[ubase + i];   // MomentKV alpha ||r||
-                else if (isinf(m)) mn = sp;
-                else if (a.rule == KVC_RULE_SINGLE) mn = sp;
-                else if (a.rule == KVC_RULE_CUMULATIVE) mn = m + sp;
-                else mn = al * m + (1.0 - al) * sp;
-                if (i != L) a.util[ubase + i] = mn;
-                else S.vm = mn;
-                if (a.probs) a.probs[ubase + i] = sp;
-                Cand x{double_key(mn), po[b], i};
-#pragma unroll
-                for (int j = 0; j < kSel; j++)
-                    if (cand_less(x, lst[j])) { const Cand t_ = lst[j]; lst[j] = x; x = t_; }
-            }
-        }
-        // (6) the CTA's Tq lowest by repeated minima over the lane heads
-        int nc = 0;
-        for (int rnd = 0; rnd < Tq; rnd++) {
-            const Cand c1 = lst[0];
-            const uint32_t hi = (uint32_t)(c1.key >> 32), lo = (uint32_t)c1.key;
-            const uint32_t mhi = __reduce_min_sync(kFull, hi);
-            const uint32_t mlo = __reduce_min_sync(kFull, hi == mhi ? lo : 0xffffffffu);
-            const bool tie = hi == mhi && lo == mlo;
-            const uint32_t mpos = __reduce_min_sync(kFull, tie ? (uint32_t)c1.pos ^ 0x80000000u : 0xffffffffu);
-            const bool win = tie && ((uint32_t)c1.pos ^ 0x80000000u) == mpos && c1.slot >= 0;
-            const uint32_t wm = __ballot_sync(kFull, win);
-            if (wm == 0u) break;
-            const int src = __ffs(wm) - 1;
-            Cand best;
-            best.key = __shfl_sync(kFull, (unsigned long long)c1.key, src);
-            best.pos = __shfl_sync(kFull, c1.pos, src);
-            best.slot = __shfl_sync(kFull, c1.slot, src);
-            if (lane == 0) S.cand[rnd] = best;   // the lane that publishes writes
-            if (lane == src) {
-#pragma unroll
-                for (int j = 0; j < kSel - 1; j++) lst[j] = lst[j + 1];
-                lst[kSel - 1] = none;
-            }
-            nc++;
-        }
-        __syncwarp();
-        if (lane == 0) {
-            S.ncand = nc;
-            for (int qc = 0; qc < CS; qc++) mbar_arrive_remote(&S.cready, (uint32_t)qc);
-        }
-        __syncwarp();
-        ok = mbar_wait_cluster(&S.cready, 0) && ok;
-        // (7) every CTA merges the candidate lists the same way
-        int vic = -1;
-        if (lane == 0) {
-            int ptr[kFusedMaxCS];
-            for (int qc = 0; qc < CS; qc++) ptr[qc] = 0;
-            Cand sel[kSel];
-            int nsel = 0;
-            while (ok && nsel < Tq) {
-                int bq = -1;
-                Cand b = none;
-                for (int qc = 0; qc < CS; qc++) {
-                    FusedSmem<G> *R = cluster.map_shared_rank(&S, qc);
-                    if (ptr[qc] >= min(Tq, R->ncand)) continue;
-                    const Cand cq = R->cand[ptr[qc]];
-                    if (cq.slot >= 0 && cand_less(cq, b)) { b = cq; bq = qc; }
-                }
-                if (bq < 0) break;
-                ptr[bq]++;
-                sel[nsel++] = b;
-            }
-            vic = (nsel > 0 && sel[0].slot >= 0 && sel[0].slot <= L) ? sel[0].slot : -1;
-            if (r == 0 && vic >= 0) {
-                int32_t *pq = a.pend + (size_t)u * kPendStride;
-                pq[0] = a.merge ? 0 : a.t;
-                pq[1] = nsel - 1;
-                for (int j = 1; j < nsel; j++)
-                    pq[2 + j - 1] = sel[j].slot == L ? sel[0].slot : sel[j].slot;
-            }
-        }
-        vic = __shfl_sync(kFull, vic, 0);
-        // (8) the victim's owner publishes its row, vote, position and share
-        const int owner = vic < 0 ? -1 : (vic == L ? CS - 1 : vic / ch);
-        if (r == owner) {
-            const bool isv = (vic == L);
-            const int li = vic - s0;
-            const uint16_t *kr = isv ? knew : a.K + (ubase + vic) * kD;
-            const uint16_t *vr = isv ? vnew : a.V + (ubase + vic) * kD;
-            for (int e = lane; e < kD; e += 32) {
-                S.pk[e] = bf2f(kr[e]);
-                S.pv[e] = bf2f(vr[e]);
-            }
-            if (lane < G) S.ae_pub[lane] = expf(XS(lane, li) - gm[lane]);
-            if (lane == 0) {
-                S.pvp = a.merge ? 0.f : ((isv || !a.votes) ? 1.f : (float)a.votes[ubase + vic]);
-                S.pvpos = isv ? a.new_pos : a.pos[ubase + vic];
-            }
-        }
-        // every lane releases its own part of the publication
-        for (int qc = 0; qc < CS; qc++) mbar_arrive_remote(&S.vpub, (uint32_t)qc);
-        ok = mbar_wait_cluster(&S.vpub, 0) && ok;
-        if (!ok || vic < 0) {
-            if (lane == 0) {
-                atomicExch(&S.bad, 1);
-                S.victim = -1;
-            }
-            return;
-        }
-        FusedSmem<G> *O = cluster.map_shared_rank(&S, owner);
-        for (int e = lane; e < kD; e += 32) {
-            const float vk = O->pk[e], vv = O->pv[e];
-            S.vk[e] = vk;
-            S.vv[e] = vv;
-            S.ve[e] = vv;
-        }
-        if (lane < G) S.ae[lane] = O->ae_pub[lane];
-        if (lane == 0) {
-            S.vp = O->pvp;
-            S.vpos = O->pvpos;
-            S.victim = vic;
-        }
-        __syncwarp();
-        // (9) the fold: means, deltas, and C' q = (n/n') C q + (p n/n'^2) dv (dk . q)
+    };
+    // The fold of a refresh step given C q (from refresh_prep): the means,
+    // the deltas dk, dv against the old means, and C' q = (n/n') C q +
+    // (p n/n'^2) dv (dk . q); C itself is written back by write_back_C.
+    auto fold_cq = [&](int p, int np) {
         const bool upd = !a.merge;
         const float n0 = S.n0, pe = S.vp, n1 = n0 + pe, fwt = upd ? pe / n1 : 0.f;
-        for (int e = lane; e < kD; e += 32) {
+        for (int e = p; e < kD; e += np) {
             const float mk = S.mk0[e], mv = S.mv0[e];
             S.muk[e] = mk + (S.vk[e] - mk) * fwt;
             S.muv[e] = mv + (S.vv[e] - mv) * fwt;
             S.vk[e] -= mk;
             S.vv[e] -= mv;
         }
-        __syncwarp();
-        const float sc_old = upd ? n0 / n1 : 1.f, sc_rank = upd ? pe * n0 / (n1 * n1) : 0.f;
-        float dq[G], zq_[G];
-#pragma unroll
-        for (int h = 0; h < G; h++) {
-            float s1_ = 0.f, s2_ = 0.f;
-            for (int e = lane; e < kD; e += 32) {
-                s1_ = fmaf(S.vk[e], S.qs[h][e], s1_);
-                s2_ = fmaf(S.muk[e], S.qs[h][e], s2_);
+        __syncthreads();
+        // dk . q and q . mu_k' per head: one warp per (head, quantity)
+        const int pw = p >> 5, npw = np >> 5, pl = p & 31;
+        for (int job = pw; job < 2 * G; job += npw) {
+            const int h = job >> 1;
+            const float *x = (job & 1) ? S.muk : S.vk;
+            float acc = 0.f;
+            for (int j = pl; j < kD; j += 32) acc = fmaf(S.qs[h][j], x[j], acc);
+            acc = warp_sum(acc);
+            if (pl == 0) {
+                if (job & 1) S.zq[h] = acc;
+                else S.mass[h] = acc;           // dk . q / sqrt(d) (mass is free by now)
             }
-            dq[h] = warp_sum(s1_);
-            zq_[h] = warp_sum(s2_);
         }
-        for (int rr = r0 + lane; rr < r1; rr += 32)
-#pragma unroll
-            for (int h = 0; h < G; h++)
-                S.cq[h][rr] = fmaf(sc_rank * S.vv[rr], dq[h], sc_old * S.cq[h][rr]);
-        if (lane < G) S.zq[lane] = zq_[lane];
-        __syncwarp();
+        __syncthreads();
+        if (upd) {
+            const float sc_old = n0 / n1, sc_rank = pe * n0 / (n1 * n1);
+            for (int e = p; e < G * (r1 - r0); e += np) {
+                const int h = e / (r1 - r0), rr = r0 + e % (r1 - r0);
+                S.cq[h][rr] = fmaf(sc_rank * S.vv[rr], S.mass[h], sc_old * S.cq[h][rr]);
+            }
+        }
+        __syncthreads();
+    };
+    // C' = (n/n') C + (p n/n'^2) dv dk^T for the CTA's rows (L2-hot since
+    // refresh_prep read them)
+    auto write_back_C = [&]() {
+        const float n0 = S.n0, pe = S.vp, n1 = n0 + pe;
+        const float sc_old = n0 / n1, sc_rank = pe * n0 / (n1 * n1);
+        for (int e = tid; e < (r1 - r0) * (kD / 4); e += blockDim.x) {
+            const int rr = r0 + e / (kD / 4), c4 = (e % (kD / 4)) * 4;
+            float4 *cp = reinterpret_cast<float4 *>(Cu + (size_t)rr * kD + c4);
+            float4 cv = *cp;
+            const float dv = S.vv[rr] * sc_rank;
+            cv.x = fmaf(cv.x, sc_old, dv * S.vk[c4]);
+            cv.y = fmaf(cv.y, sc_old, dv * S.vk[c4 + 1]);
+            cv.z = fmaf(cv.z, sc_old, dv * S.vk[c4 + 2]);
+            cv.w = fmaf(cv.w, sc_old, dv * S.vk[c4 + 3]);
+            *cp = cv;
+        }
     };
 
     if (w == kNC + 1) {
@@ -760,8 +563,8 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             }
             __syncwarp();
             fold(lane, 32, false);
-        } else if (fw) {
-            refresh_worker();
+        } else if (refresh) {
+            refresh_prep();
         }
     } else if (w == kNC) {
         // ---------------- producer
@@ -926,7 +729,6 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             S.pM[tid] = v;
         }
         consumer_sync();                          // S.red is reused below
-        if (fw && tid == 0) mbar_arrive(&S.p1done);   // logits and CTA max in place
         // a late victim leaves pass 2 (evict mode)
         int vmask = -1;
         if (late) {
@@ -1124,49 +926,8 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
         }
     }
 
-    if (fw) {
-        victim = S.victim;
-        if (victim < 0) {                       // a cluster wait ran out: refuse
-            if (r == 0 && tid == 0) {
-                record_status(a.status, KVC_ERR_TIMEOUT);
-                a.n_evict[u] = 0;
-            }
-            cluster.sync();                     // nobody reads this CTA's partials any more
-            return;
-        }
-    }
-
     int vic_owner;
-    if (fw) {
-        // -------------------------------------------- identity (the fold warp
-        // selected and folded the victim during pass 2)
-        vic_owner = (victim == L) ? CS - 1 : victim / ch;
-        if (tid < G) {
-            S.mass[tid] = S.ae[tid] / S.gl[tid];
-            if (!a.merge && S.mass[tid] > 0.5f) atomicExch(&S.direct, 1);
-        }
-        __syncthreads();
-        if (a.merge) {
-            for (int e = tid; e < G * kD; e += blockDim.x) S.fR[e / kD][e % kD] /= S.gl[e / kD];
-            if (tid < G) S.lzR[tid] = S.gM[tid] + logf(S.gl[tid]);
-            __syncthreads();
-        } else if (!S.direct) {
-            for (int e = tid; e < G * kD; e += blockDim.x) {
-                const int h = e / kD, dd = e % kD;
-                S.fR[h][dd] = (S.fR[h][dd] - S.ae[h] * S.ve[dd]) / (S.gl[h] - S.ae[h]);
-            }
-            if (tid < G) S.lzR[tid] = S.gM[tid] + logf(S.gl[tid] - S.ae[tid]);
-            __syncthreads();
-        } else {
-            cluster.sync();                         // everyone is done reading partials
-            pv_pass(victim, S.pM);
-            cluster.sync();
-            merge();
-            for (int e = tid; e < G * kD; e += blockDim.x) S.fR[e / kD][e % kD] /= S.gl[e / kD];
-            if (tid < G) S.lzR[tid] = S.gM[tid] + logf(S.gl[tid]);
-            __syncthreads();
-        }
-    } else if (refresh) {
+    if (refresh) {
         // -------------------------------------------- probabilities + utilities
         const double al = (double)a.alpha;
         if (tid < G) {
@@ -1230,6 +991,10 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
         // low word, then position among equal keys), the winning lane
         // promotes its second entry and rescans only when it wins again.
         // Thread 0 then merges the sorted per-warp lists.
+        // queue length: T (one victim per step until the next refresh); a
+        // Score-Free run (T = 0, no later refresh) queues as many as fit
+        // (merge mode keeps no queue: a merge changes the partner's utility)
+        const int Tq = a.merge ? 1 : (a.T > 0 ? a.T : kMaxQueue);
         const int want = min(Tq, nloc);
         Cand *wl = reinterpret_cast<Cand *>(chosen + align_up((size_t)(ch + 1)));   // [kWarps][kMaxQueue]
         const Cand none{~0ull, 0x7fffffff, -1};
@@ -1281,26 +1046,25 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             }
         }
         __syncthreads();
-        if (tid == 0) {
-            int ptr[kWarps];
-            for (int q = 0; q < kWarps; q++) ptr[q] = 0;
-            int nc = 0;
-            for (; nc < want; nc++) {
-                int bq = -1;
-                Cand b{~0ull, 0x7fffffff, -1};
-                for (int q = 0; q < kWarps; q++) {
-                    if (ptr[q] >= want) continue;
-                    const Cand cq = wl[q * kMaxQueue + ptr[q]];
-                    if (cq.slot >= 0 && cand_less(cq, b)) {
-                        b = cq;
-                        bq = q;
-                    }
+        // the CTA's want lowest of the warps' lists: warp 0 ranks every entry
+        // against all the others (pairs (key, position) are distinct) and
+        // scatters the ranks below want in order
+        if (w == 0) {
+            const int n_all = kWarps * want;
+            int nvalid = 0;
+            for (int i = lane; i < n_all; i += 32) {
+                const Cand ci = wl[(i / want) * kMaxQueue + i % want];
+                if (ci.slot < 0) continue;
+                nvalid++;
+                int rk = 0;
+                for (int j2 = 0; j2 < n_all; j2++) {
+                    const Cand cj = wl[(j2 / want) * kMaxQueue + j2 % want];
+                    rk += cj.slot >= 0 && cand_less(cj, ci);
                 }
-                if (bq < 0) break;
-                ptr[bq]++;
-                S.cand[nc] = b;
+                if (rk < want) S.cand[rk] = ci;
             }
-            S.ncand = nc;
+            nvalid = warp_isum(nvalid);
+            if (lane == 0) S.ncand = min(want, nvalid);
         }
         cluster.sync();                                                // candidates visible
         // every CTA merges the candidate lists the same way: one parallel
@@ -1312,32 +1076,34 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             gc[q * kMaxQueue + jj] = jj < R->ncand ? R->cand[jj] : Cand{~0ull, 0x7fffffff, -1};
         }
         __syncthreads();
-        if (tid == 0) {
-            int ptr[kFusedMaxCS];
-            for (int q = 0; q < CS; q++) ptr[q] = 0;
-            Cand sel[kMaxQueue];
-            int nsel = 0;
-            while (nsel < Tq) {
-                int bq = -1;
-                Cand b{~0ull, 0x7fffffff, -1};
-                for (int q = 0; q < CS; q++) {
-                    if (ptr[q] >= Tq) continue;
-                    const Cand cq = gc[q * kMaxQueue + ptr[q]];
-                    if (cq.slot >= 0 && cand_less(cq, b)) {
-                        b = cq;
-                        bq = q;
-                    }
+        // the cluster's Tq lowest, ranked the same way on every CTA; the
+        // lowest is the victim, the rest the queue of the next lazy steps
+        Cand *sel = gc + kFusedMaxCS * kMaxQueue;            // [kMaxQueue]
+        if (w == 0) {
+            const int n_all = CS * Tq;
+            int nvalid = 0;
+            for (int i = lane; i < n_all; i += 32) {
+                const Cand ci = gc[(i / Tq) * kMaxQueue + i % Tq];
+                if (ci.slot < 0) continue;
+                nvalid++;
+                int rk = 0;
+                for (int j2 = 0; j2 < n_all; j2++) {
+                    const Cand cj = gc[(j2 / Tq) * kMaxQueue + j2 % Tq];
+                    rk += cj.slot >= 0 && cand_less(cj, ci);
                 }
-                if (bq < 0) break;
-                ptr[bq]++;
-                sel[nsel++] = b;
+                if (rk < Tq) sel[rk] = ci;
             }
-            S.victim = sel[0].slot;
-            if (r == 0) {
+            nvalid = warp_isum(nvalid);
+            const int nsel = min(Tq, nvalid);
+            __syncwarp();
+            if (lane == 0) S.victim = nsel > 0 ? sel[0].slot : -1;
+            if (r == 0 && nsel > 0) {
                 int32_t *pq = a.pend + (size_t)u * kPendStride;
-                pq[0] = a.merge ? 0 : a.t;
-                pq[1] = nsel - 1;
-                for (int j = 1; j < nsel; j++)
+                if (lane == 0) {
+                    pq[0] = a.merge ? 0 : a.t;
+                    pq[1] = nsel - 1;
+                }
+                for (int j = 1 + lane; j < nsel; j += 32)
                     pq[2 + j - 1] = sel[j].slot == L ? sel[0].slot : sel[j].slot;
             }
         }
@@ -1404,7 +1170,7 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
         __syncthreads();
     }
 
-    if (refresh && !fw) fold(tid, blockDim.x, true);   // otherwise folded during the passes
+    if (refresh) fold_cq(tid, blockDim.x);            // lazy steps folded during the passes
     const float n1 = S.n0 + S.vp;
     for (int h = tid; h < G; h += blockDim.x) {
         const float logZE = logf(n1) + S.zq[h];
@@ -1433,23 +1199,7 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             if (a.evict_pos) a.evict_pos[(size_t)u * a.kmax] = S.vpos;
         }
     }
-    // the write-back of this CTA's rows of C for a fold made by the fold warp
-    // (it formed C' q from C q): C' = (n/n') C + (p n/n'^2) dv dk^T
-    if (fw && !a.merge) {
-        const float n0 = S.n0, pe = S.vp, n1 = n0 + pe;
-        const float sc_old = n0 / n1, sc_rank = pe * n0 / (n1 * n1);
-        for (int e = tid; e < (r1 - r0) * (kD / 4); e += blockDim.x) {
-            const int rr = r0 + e / (kD / 4), c4 = (e % (kD / 4)) * 4;
-            float4 *cp = reinterpret_cast<float4 *>(Cu + (size_t)rr * kD + c4);
-            float4 cv = *cp;
-            const float dv = S.vv[rr] * sc_rank;
-            cv.x = fmaf(cv.x, sc_old, dv * S.vk[c4]);
-            cv.y = fmaf(cv.y, sc_old, dv * S.vk[c4 + 1]);
-            cv.z = fmaf(cv.z, sc_old, dv * S.vk[c4 + 2]);
-            cv.w = fmaf(cv.w, sc_old, dv * S.vk[c4 + 3]);
-            *cp = cv;
-        }
-    }
+    if (refresh && !a.merge) write_back_C();
     // ------------------------------------------------ the new token's slot
     if (a.merge) {
         // appended at slot L; the merge that follows refills the victim's
@@ -1489,7 +1239,8 @@ static cudaError_t launch_fused_g(const FusedArgs &a0, int U, int CS, cudaStream
 {
     FusedArgs a = a0;
     const size_t sel = align_up((size_t)(a.chunk + 1) * 8) + align_up((size_t)(a.chunk + 1) * 4) +
-                       align_up((size_t)(a.chunk + 1)) + (size_t)(kWarps + kFusedMaxCS) * kMaxQueue * sizeof(Cand);
+                       align_up((size_t)(a.chunk + 1)) +
+                       (size_t)(kWarps + kFusedMaxCS + 1) * kMaxQueue * sizeof(Cand);
     if (sel > (size_t)kStages * kTileBytes) return cudaErrorNotSupported;
     CUtensorMap tmK, tmV;
     const uint64_t rows = (uint64_t)U * (uint64_t)a.cap;
