@@ -499,16 +499,30 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
     auto write_back_C = [&]() {
         const float n0 = S.n0, pe = S.vp, n1 = n0 + pe;
         const float sc_old = n0 / n1, sc_rank = pe * n0 / (n1 * n1);
-        for (int e = tid; e < (r1 - r0) * (kD / 4); e += blockDim.x) {
-            const int rr = r0 + e / (kD / 4), c4 = (e % (kD / 4)) * 4;
-            float4 *cp = reinterpret_cast<float4 *>(Cu + (size_t)rr * kD + c4);
-            float4 cv = *cp;
-            const float dv = S.vv[rr] * sc_rank;
-            cv.x = fmaf(cv.x, sc_old, dv * S.vk[c4]);
-            cv.y = fmaf(cv.y, sc_old, dv * S.vk[c4 + 1]);
-            cv.z = fmaf(cv.z, sc_old, dv * S.vk[c4 + 2]);
-            cv.w = fmaf(cv.w, sc_old, dv * S.vk[c4 + 3]);
-            *cp = cv;
+        // eight float4 per thread in flight before any is written back
+        const int total = (r1 - r0) * (kD / 4);
+        for (int e0 = tid; e0 < total; e0 += 8 * (int)blockDim.x) {
+            float4 cv[8];
+#pragma unroll
+            for (int k = 0; k < 8; k++) {
+                const int e = e0 + k * (int)blockDim.x;
+                cv[k] = e < total ? *reinterpret_cast<const float4 *>(Cu + (size_t)(r0 + e / (kD / 4)) * kD +
+                                                                      (e % (kD / 4)) * 4)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int k = 0; k < 8; k++) {
+                const int e = e0 + k * (int)blockDim.x;
+                if (e >= total) break;
+                const int rr = r0 + e / (kD / 4), c4 = (e % (kD / 4)) * 4;
+                const float dv = S.vv[rr] * sc_rank;
+                float4 c = cv[k];
+                c.x = fmaf(c.x, sc_old, dv * S.vk[c4]);
+                c.y = fmaf(c.y, sc_old, dv * S.vk[c4 + 1]);
+                c.z = fmaf(c.z, sc_old, dv * S.vk[c4 + 2]);
+                c.w = fmaf(c.w, sc_old, dv * S.vk[c4 + 3]);
+                *reinterpret_cast<float4 *>(Cu + (size_t)rr * kD + c4) = c;
+            }
         }
     };
 
@@ -1046,25 +1060,26 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             }
         }
         __syncthreads();
-        // the CTA's want lowest of the warps' lists: warp 0 ranks every entry
-        // against all the others (pairs (key, position) are distinct) and
-        // scatters the ranks below want in order
-        if (w == 0) {
-            const int n_all = kWarps * want;
-            int nvalid = 0;
-            for (int i = lane; i < n_all; i += 32) {
-                const Cand ci = wl[(i / want) * kMaxQueue + i % want];
-                if (ci.slot < 0) continue;
-                nvalid++;
-                int rk = 0;
-                for (int j2 = 0; j2 < n_all; j2++) {
-                    const Cand cj = wl[(j2 / want) * kMaxQueue + j2 % want];
-                    rk += cj.slot >= 0 && cand_less(cj, ci);
+        if (tid == 0) {
+            int ptr[kWarps];
+            for (int q = 0; q < kWarps; q++) ptr[q] = 0;
+            int nc = 0;
+            for (; nc < want; nc++) {
+                int bq = -1;
+                Cand b{~0ull, 0x7fffffff, -1};
+                for (int q = 0; q < kWarps; q++) {
+                    if (ptr[q] >= want) continue;
+                    const Cand cq = wl[q * kMaxQueue + ptr[q]];
+                    if (cq.slot >= 0 && cand_less(cq, b)) {
+                        b = cq;
+                        bq = q;
+                    }
                 }
-                if (rk < want) S.cand[rk] = ci;
+                if (bq < 0) break;
+                ptr[bq]++;
+                S.cand[nc] = b;
             }
-            nvalid = warp_isum(nvalid);
-            if (lane == 0) S.ncand = min(want, nvalid);
+            S.ncand = nc;
         }
         cluster.sync();                                                // candidates visible
         // every CTA merges the candidate lists the same way: one parallel
@@ -1076,34 +1091,32 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             gc[q * kMaxQueue + jj] = jj < R->ncand ? R->cand[jj] : Cand{~0ull, 0x7fffffff, -1};
         }
         __syncthreads();
-        // the cluster's Tq lowest, ranked the same way on every CTA; the
-        // lowest is the victim, the rest the queue of the next lazy steps
-        Cand *sel = gc + kFusedMaxCS * kMaxQueue;            // [kMaxQueue]
-        if (w == 0) {
-            const int n_all = CS * Tq;
-            int nvalid = 0;
-            for (int i = lane; i < n_all; i += 32) {
-                const Cand ci = gc[(i / Tq) * kMaxQueue + i % Tq];
-                if (ci.slot < 0) continue;
-                nvalid++;
-                int rk = 0;
-                for (int j2 = 0; j2 < n_all; j2++) {
-                    const Cand cj = gc[(j2 / Tq) * kMaxQueue + j2 % Tq];
-                    rk += cj.slot >= 0 && cand_less(cj, ci);
+        if (tid == 0) {
+            int ptr[kFusedMaxCS];
+            for (int q = 0; q < CS; q++) ptr[q] = 0;
+            Cand *sel = gc + kFusedMaxCS * kMaxQueue;       // [kMaxQueue]
+            int nsel = 0;
+            while (nsel < Tq) {
+                int bq = -1;
+                Cand b{~0ull, 0x7fffffff, -1};
+                for (int q = 0; q < CS; q++) {
+                    if (ptr[q] >= Tq) continue;
+                    const Cand cq = gc[q * kMaxQueue + ptr[q]];
+                    if (cq.slot >= 0 && cand_less(cq, b)) {
+                        b = cq;
+                        bq = q;
+                    }
                 }
-                if (rk < Tq) sel[rk] = ci;
+                if (bq < 0) break;
+                ptr[bq]++;
+                sel[nsel++] = b;
             }
-            nvalid = warp_isum(nvalid);
-            const int nsel = min(Tq, nvalid);
-            __syncwarp();
-            if (lane == 0) S.victim = nsel > 0 ? sel[0].slot : -1;
+            S.victim = nsel > 0 ? sel[0].slot : -1;
             if (r == 0 && nsel > 0) {
                 int32_t *pq = a.pend + (size_t)u * kPendStride;
-                if (lane == 0) {
-                    pq[0] = a.merge ? 0 : a.t;
-                    pq[1] = nsel - 1;
-                }
-                for (int j = 1 + lane; j < nsel; j += 32)
+                pq[0] = a.merge ? 0 : a.t;
+                pq[1] = nsel - 1;
+                for (int j = 1; j < nsel; j++)
                     pq[2 + j - 1] = sel[j].slot == L ? sel[0].slot : sel[j].slot;
             }
         }

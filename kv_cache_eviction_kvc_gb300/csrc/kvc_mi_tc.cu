@@ -134,6 +134,19 @@ mi_norm_kernel(NormArgs a, const __grid_constant__ CUtensorMap tmK)
                     const int row = (int)((size_t)u * a.cap + (size_t)t * kTs);
                     tma_2d_hint(dst, &tmK, 0, row, &S.full[s], once);
                     tma_2d_hint(dst + kUmmaBox, &tmK, 64, row, &S.full[s], once);
+                    // the tile's value rows (contiguous) into L2 for the epilogue
+                    const size_t rows_left = (size_t)a.U * a.cap - (size_t)row;
+                    const uint32_t vbytes = (uint32_t)(min((size_t)kTs, rows_left) * kD * 2);
+                    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.V + (size_t)row * kD),
+                                 "r"(vbytes)
+                                 : "memory");
+                    if (t == 0 && j + 1 < nmine) {
+                        // the next unit's C for the converter
+                        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                                         a.C + (size_t)unit_of(j + 1) * kD * kD),
+                                     "r"((uint32_t)(kD * kD * 4))
+                                     : "memory");
+                    }
                     issued = jt + 1;
                 }
             }
@@ -196,7 +209,7 @@ mi_norm_kernel(NormArgs a, const __grid_constant__ CUtensorMap tmK)
             const bool valid = slot < n;
             const uint4 *vp = reinterpret_cast<const uint4 *>(a.V + ((size_t)u * a.cap + slot) * kD);
 #pragma unroll
-            for (int c = 0; c < 16; c++) vr[c] = valid ? ldg_nc_v4(vp + c) : make_uint4(0, 0, 0, 0);
+            for (int c = 0; c < 16; c++) vr[c] = valid ? __ldg(vp + c) : make_uint4(0, 0, 0, 0);
         };
         auto tile = [&](int u, int n, int t, const uint4 (&vr)[16], const float *cmu, const float *mv) {
             const int b = jt % kNacc;
