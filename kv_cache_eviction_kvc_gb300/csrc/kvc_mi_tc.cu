@@ -13,10 +13,11 @@
 //               boxes) into a ring
 //   warp 1      tensor-memory owner and MMA issuer (one thread): 3 x 8 MMAs
 //               of 128 x 128 x 16 per tile into one of four accumulators
-//   warps 2-5   epilogue, one slot per thread (the warp's tensor-memory lane
-//               quarter): D row from tensor memory, the value row from global
-//               memory, ||r||
-//   warps 6-9   converter: per unit C (fp32) -> three bf16 operand tiles in
+//   warps 2-9   epilogue, two sets of four warps taking alternate tiles; one
+//               slot per thread (the warp's tensor-memory lane quarter): D
+//               row from tensor memory, the value row from L2 (the producer
+//               bulk-prefetches each tile's value rows), ||r||
+//   warps 10-13 converter: per unit C (fp32) -> three bf16 operand tiles in
 //               shared memory, C mu_k, and the new token's ||r|| on CUDA cores
 // Every wait is bounded (~2 s); a wait that ran out records KVC_ERR_TIMEOUT.
 #include <cuda_runtime.h>
@@ -36,7 +37,9 @@ constexpr int kTs = 128;                 // slots per tile
 constexpr int kOpB = 2 * kUmmaBox;       // one 128 x 128 bf16 operand: 32 KB
 constexpr int kNs = 3;                   // ring stages
 constexpr int kNacc = 4;                 // tensor-memory accumulators (128 columns each)
-constexpr int kNThreads = 10 * 32;
+constexpr int kNEpi = 8;                 // epilogue warps: two sets of four
+constexpr int kNConv0 = 2 + kNEpi;       // first converter warp
+constexpr int kNThreads = (kNConv0 + 4) * 32;
 constexpr size_t kNDyn = 1024 + (size_t)3 * kOpB + (size_t)kNs * kOpB;
 constexpr uint32_t kNIdesc = umma_idesc_bf16(128, 128);
 
@@ -105,7 +108,7 @@ mi_norm_kernel(NormArgs a, const __grid_constant__ CUtensorMap tmK)
         }
         for (int j = 0; j < 2; j++) {
             mbar_init(&S.cfull[j], 1);
-            mbar_init(&S.cdone[j], 4);
+            mbar_init(&S.cdone[j], kNEpi);
         }
         mbar_init(&S.cfree, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -195,112 +198,101 @@ mi_norm_kernel(NormArgs a, const __grid_constant__ CUtensorMap tmK)
             if (!ok) atomicExch(&S.bad, 1);
         }
         __syncwarp();
-    } else if (w < 6) {
-        // ------------------------------------------------ epilogue (warps 2-5)
-        // The value rows of the next tile are loaded while this tile is
-        // computed (two register buffers), so that their latency is hidden.
-        const int qd = w & 3;
+    } else if (w < kNConv0) {
+        // ------------------------------------------------ epilogue (warps 2-9)
+        // Set `set` takes the tiles jt with jt % 2 == set; a set's four warps
+        // cover the four tensor-memory lane quarters (warp w reaches lanes
+        // 32 (w % 4) ..).  A tile's value rows are loaded before its
+        // accumulator is awaited.
+        const int set = (w - 2) >> 2, qd = w & 3;
         const uint32_t lane_base = tmem + ((uint32_t)(32 * qd) << 16);
         bool good = true;
         int jt = 0;
-        uint4 va[16], vb[16];
-        auto load_v = [&](int u, int n, int t, uint4 (&vr)[16]) {
-            const int slot = t * kTs + 32 * qd + lane;
-            const bool valid = slot < n;
-            const uint4 *vp = reinterpret_cast<const uint4 *>(a.V + ((size_t)u * a.cap + slot) * kD);
-#pragma unroll
-            for (int c = 0; c < 16; c++) vr[c] = valid ? __ldg(vp + c) : make_uint4(0, 0, 0, 0);
-        };
-        auto tile = [&](int u, int n, int t, const uint4 (&vr)[16], const float *cmu, const float *mv) {
-            const int b = jt % kNacc;
-            const int slot = t * kTs + 32 * qd + lane;
-            const bool ok = good && mbar_wait(&S.accf[b], (uint32_t)(jt / kNacc) & 1u);
-            good = __all_sync(kFull, ok);
-            if (good) {
-                tc_fence_after();
-                float acc = 0.f;
-#pragma unroll
-                for (int h = 0; h < 4; h++) {            // 32 dims at a time
-                    float x[32];
-                    tmem_ld32(lane_base + (uint32_t)(b * 128 + 32 * h), x);
-#pragma unroll
-                    for (int c = 0; c < 4; c++) {
-                        float v8[8];
-                        unpack8(vr[4 * h + c], v8);
-#pragma unroll
-                        for (int e = 0; e < 8; e++) {
-                            const int dd = 32 * h + 8 * c + e;
-                            const float r = v8[e] - mv[dd] - (x[8 * c + e] - cmu[dd]) * a.rs;
-                            acc = fmaf(r, r, acc);
-                        }
-                    }
-                }
-                if (slot < n) a.rr[(size_t)u * a.cap + slot] = sqrtf(acc);
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0 && good) mbar_arrive(&S.acce[b]);
-            jt++;
-        };
         for (int j = 0; j < nmine && good; j++) {
             const int u = unit_of(j), nt = tiles_of(u), n = min(max(a.len[u], 0), a.cap);
-            if (nt > 0) load_v(u, n, 0, va);
             bool ok = mbar_wait(&S.cfull[j & 1], (uint32_t)(j >> 1) & 1u);
             good = __all_sync(kFull, ok);
             if (!good) break;
             const float *cmu = S.cmu[j & 1], *mv = S.mv[j & 1];
-            for (int t = 0; t < nt; t += 2) {
-                if (t + 1 < nt) load_v(u, n, t + 1, vb);
-                tile(u, n, t, va, cmu, mv);
-                if (t + 1 < nt) {
-                    if (t + 2 < nt) load_v(u, n, t + 2, va);
-                    tile(u, n, t + 1, vb, cmu, mv);
+            for (int t = 0; t < nt; t++, jt++) {
+                if ((jt & 1) != set) continue;
+                const int b = jt % kNacc;
+                const int slot = t * kTs + 32 * qd + lane;
+                const bool valid = slot < n;
+                uint4 vr[16];
+                const uint4 *vp = reinterpret_cast<const uint4 *>(a.V + ((size_t)u * a.cap + slot) * kD);
+#pragma unroll
+                for (int c = 0; c < 16; c++) vr[c] = valid ? __ldg(vp + c) : make_uint4(0, 0, 0, 0);
+                ok = good && mbar_wait(&S.accf[b], (uint32_t)(jt / kNacc) & 1u);
+                good = __all_sync(kFull, ok);
+                if (good) {
+                    tc_fence_after();
+                    float acc = 0.f;
+#pragma unroll
+                    for (int h = 0; h < 4; h++) {            // 32 dims at a time
+                        float x[32];
+                        tmem_ld32(lane_base + (uint32_t)(b * 128 + 32 * h), x);
+#pragma unroll
+                        for (int c = 0; c < 4; c++) {
+                            float v8[8];
+                            unpack8(vr[4 * h + c], v8);
+#pragma unroll
+                            for (int e = 0; e < 8; e++) {
+                                const int dd = 32 * h + 8 * c + e;
+                                const float r = v8[e] - mv[dd] - (x[8 * c + e] - cmu[dd]) * a.rs;
+                                acc = fmaf(r, r, acc);
+                            }
+                        }
+                    }
+                    if (valid) a.rr[(size_t)u * a.cap + slot] = sqrtf(acc);
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0 && good) mbar_arrive(&S.acce[b]);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.cdone[j & 1]);    // this unit's vectors are no longer read
         }
         if (!good) atomicExch(&S.bad, 1);
     } else {
-        // ------------------------------------------------ converter (warps 6-9)
-        // Thread ct owns row ct of C.  The unit's row is loaded into registers
-        // while the previous unit's MMAs still read the terms; the split and
-        // the shared-memory writes wait for them.
-        const int ct = tid - 6 * 32;                 // 0..127: row a of C
+        // ------------------------------------------------ converter (warps 10-13)
+        // Thread ct owns row ct of C.  Once the previous unit's MMAs are done
+        // with the terms, the row (in L2: the producer prefetched it) is
+        // split in two halves of 64 columns.
+        const int ct = tid - kNConv0 * 32;           // 0..127: row a of C
         bool good = true;
         for (int j = 0; j < nmine && good; j++) {
             const int u = unit_of(j), n = min(max(a.len[u], 0), a.cap);
             const float *Cr = a.C + (size_t)u * kD * kD + (size_t)ct * kD;
-            float4 cr[32];
-#pragma unroll
-            for (int c = 0; c < 32; c++) cr[c] = *reinterpret_cast<const float4 *>(Cr + 4 * c);
             const float *mk = a.mu_k + (size_t)u * kD;
             const uint16_t *kn = a.k_new + (size_t)u * kD;
-            float dot_mu = 0.f, dot_new = 0.f;
-#pragma unroll
-            for (int c = 0; c < 32; c++) {
-                const float4 mk4 = *reinterpret_cast<const float4 *>(mk + 4 * c);
-                const uint2 kn4 = *reinterpret_cast<const uint2 *>(kn + 4 * c);
-                dot_mu = fmaf(cr[c].x, mk4.x, dot_mu);
-                dot_mu = fmaf(cr[c].y, mk4.y, dot_mu);
-                dot_mu = fmaf(cr[c].z, mk4.z, dot_mu);
-                dot_mu = fmaf(cr[c].w, mk4.w, dot_mu);
-                dot_new = fmaf(cr[c].x, bf_lo(kn4.x), dot_new);
-                dot_new = fmaf(cr[c].y, bf_hi(kn4.x), dot_new);
-                dot_new = fmaf(cr[c].z, bf_lo(kn4.y), dot_new);
-                dot_new = fmaf(cr[c].w, bf_hi(kn4.y), dot_new);
-            }
             const float muv = a.mu_v[(size_t)u * kD + ct];
-            // the new token: r = v_new - mu_v - (C k_new - C mu_k) / sqrt(d)
-            const float rn = bf2f(a.v_new[(size_t)u * kD + ct]) - muv - (dot_new - dot_mu) * a.rs;
             // the previous unit's MMAs read the terms; the epilogue of unit
             // j - 2 read this parity's vectors
             bool ok = j < 1 || mbar_wait(&S.cfree, (uint32_t)(j - 1) & 1u);
             ok = ok && (j < 2 || mbar_wait(&S.cdone[j & 1], (uint32_t)((j - 2) >> 1) & 1u));
             if (!ok) good = false;
-            if (good) {
+            float dot_mu = 0.f, dot_new = 0.f;
+#pragma unroll 1
+            for (int half = 0; half < 2 && good; half++) {
+                float4 cr[16];
 #pragma unroll
-                for (int c = 0; c < 16; c++) {       // chunk c: columns 8c .. 8c + 7
+                for (int c = 0; c < 16; c++) cr[c] = *reinterpret_cast<const float4 *>(Cr + 64 * half + 4 * c);
+#pragma unroll
+                for (int c = 0; c < 16; c++) {
+                    const float4 mk4 = *reinterpret_cast<const float4 *>(mk + 64 * half + 4 * c);
+                    const uint2 kn4 = *reinterpret_cast<const uint2 *>(kn + 64 * half + 4 * c);
+                    dot_mu = fmaf(cr[c].x, mk4.x, dot_mu);
+                    dot_mu = fmaf(cr[c].y, mk4.y, dot_mu);
+                    dot_mu = fmaf(cr[c].z, mk4.z, dot_mu);
+                    dot_mu = fmaf(cr[c].w, mk4.w, dot_mu);
+                    dot_new = fmaf(cr[c].x, bf_lo(kn4.x), dot_new);
+                    dot_new = fmaf(cr[c].y, bf_hi(kn4.x), dot_new);
+                    dot_new = fmaf(cr[c].z, bf_lo(kn4.y), dot_new);
+                    dot_new = fmaf(cr[c].w, bf_hi(kn4.y), dot_new);
+                }
+#pragma unroll
+                for (int c = 0; c < 8; c++) {        // chunk 8 half + c: columns 8 (8 half + c) ..
                     const float x[8] = {cr[2 * c].x, cr[2 * c].y, cr[2 * c].z, cr[2 * c].w,
                                         cr[2 * c + 1].x, cr[2 * c + 1].y, cr[2 * c + 1].z,
                                         cr[2 * c + 1].w};
@@ -319,15 +311,19 @@ mi_norm_kernel(NormArgs a, const __grid_constant__ CUtensorMap tmK)
                     }
 #pragma unroll
                     for (int sp = 0; sp < 3; sp++)
-                        *reinterpret_cast<uint4 *>(sm + (size_t)sp * kOpB + op_off(ct, c)) =
+                        *reinterpret_cast<uint4 *>(sm + (size_t)sp * kOpB + op_off(ct, 8 * half + c)) =
                             make_uint4(tw[sp][0], tw[sp][1], tw[sp][2], tw[sp][3]);
                 }
+            }
+            if (good) {
                 S.cmu[j & 1][ct] = dot_mu;
                 S.mv[j & 1][ct] = muv;
             }
             proxy_fence_smem();                      // the terms reach the tensor cores' view
+            // the new token: r = v_new - mu_v - (C k_new - C mu_k) / sqrt(d)
+            const float rn = bf2f(a.v_new[(size_t)u * kD + ct]) - muv - (dot_new - dot_mu) * a.rs;
             const float q = warp_sum(rn * rn);
-            if (lane == 0) S.red[w - 6] = q;
+            if (lane == 0) S.red[w - kNConv0] = q;
             asm volatile("bar.sync 2, 128;" ::: "memory");
             if (ct == 0) {
                 if (good && n < a.cap)
