@@ -950,13 +950,28 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             S.igl[tid] = (1.0 / G) / (double)S.gl[tid];
             S.igl32[tid] = (float)S.igl[tid];
         }
-        // the old utilities and the positions first: independent loads, all
-        // in flight at once, staged in shared memory
-        for (int li = tid; li < nloc; li += blockDim.x) {
-            const int i = s0 + li;
-            const bool isv = (i == L);
-            msm[li] = isv ? __longlong_as_double(0x7ff0000000000000ll) : a.util[ubase + i];
-            possm[li] = isv ? a.new_pos : a.pos[ubase + i];
+        // the old utilities and the positions first, staged in shared
+        // memory: eight slots per thread loaded into registers before any is
+        // stored (the stores could alias the loads for all the compiler
+        // knows, which would serialize them)
+        for (int li0 = tid; li0 < nloc; li0 += 8 * (int)blockDim.x) {
+            double mv8[8];
+            int32_t pv8[8];
+#pragma unroll
+            for (int k = 0; k < 8; k++) {
+                const int li = li0 + k * (int)blockDim.x, i = s0 + li;
+                const bool in = li < nloc, isv = in && i == L;
+                mv8[k] = (in && !isv) ? a.util[ubase + i] : __longlong_as_double(0x7ff0000000000000ll);
+                pv8[k] = (in && !isv) ? a.pos[ubase + i] : a.new_pos;
+            }
+#pragma unroll
+            for (int k = 0; k < 8; k++) {
+                const int li = li0 + k * (int)blockDim.x;
+                if (li < nloc) {
+                    msm[li] = mv8[k];
+                    possm[li] = pv8[k];
+                }
+            }
         }
         __syncthreads();
         for (int li = tid; li < nloc; li += blockDim.x) {

@@ -247,3 +247,34 @@ def test_generation_conserves_votes_and_matches_full_attention():
         prev_ne = ne
     assert n_merged >= S - 3
     sess.close()
+
+
+def test_figure3_worked_votes():
+    """The worked merge of the KeepKV notes' Figure 3 (tests/golden): votes
+    1 and 2 merge into one entry of vote 3 with weights 1 s_e and 2 s_c, and
+    the output over the merged cache equals the output before (Thm 3)."""
+    import json
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "keepkv_fig3_merge.json")))
+    rng = np.random.default_rng(77)
+    d = 16
+    k = bf(rng.normal(size=(4, d)))
+    v = bf(rng.normal(size=(4, d)))
+    k[1] = bf(k[0] + 0.05 * rng.normal(size=d))      # slot 1: the victim's most similar key
+    p = np.array([g["p_e"], g["p_c"], 1, 1], np.int32)
+    q = bf(rng.normal(size=(1, 1, d)))
+    s = session(k, v, p)
+    r = s.zip_merge(q, [0], new_pos=4, R=0)
+    assert int(r["partner"][0]) == 1
+    _, _, vote, _, _ = s.slots()
+    assert sorted(vote[0, :3].tolist()) == sorted([g["p_r"], 1, 1])
+    # v_r = (w_e v_e + w_c v_c) / (w_e + w_c) with w = (vote) * s and s = exp(q k / sqrt(d))
+    se = math.exp(float(k[0] @ q[0, 0]) / math.sqrt(d))
+    sc = math.exp(float(k[1] @ q[0, 0]) / math.sqrt(d))
+    we, wc = g["w_e_over_s_e"] * se, g["w_c_over_s_c"] * sc
+    np.testing.assert_allclose(r["vr"][0], (we * v[0] + wc * v[1]) / (we + wc), rtol=1e-12)
+    f_full, _ = attention(q[0, 0], k, v, p.astype(float))
+    k2, v2, p2 = merged_cache(k, v, p, 0, 1, r["kr"][0], r["vr"][0])
+    f_m, _ = attention(q[0, 0], k2, v2, p2)
+    np.testing.assert_allclose(f_m, f_full, rtol=1e-11, atol=1e-12)
+    s.close()
