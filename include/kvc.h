@@ -466,8 +466,12 @@ KVC_API kvc_status kvc_decode_step(const kvc_params *p, int32_t t, int32_t new_p
  * - Each call looks up the array's device address in the calling thread's
  *   current device context (cudaGetSymbolAddress), so a device reset or a
  *   change of context needs nothing from the caller.  The first call on a
- *   device also loads the library's device code there: make that first
- *   call before any stream capture.
+ *   device also loads the library's device code there, the 32 MiB array
+ *   with it: make that first call before any stream capture, and while
+ *   32 MiB of device memory are free (a host that reserves the whole device
+ *   for its pool calls once before reserving it, or loads modules eagerly,
+ *   CUDA_MODULE_LOADING=EAGER); a load that finds no room returns
+ *   KVC_ERR_CUDA.
  * - Every call on a device shares the one array and it keeps the previous
  *   call's contents: calls whose kernels overlap on the GPU race and must be
  *   ordered by the caller (one stream, or events).

@@ -20,6 +20,16 @@ if not torch.cuda.is_available():  # pragma: no cover
 TOL = 2e-3
 
 
+@pytest.fixture(autouse=True)
+def _free_cached_device_memory():
+    """The first call on a device loads the library's device code, the
+    32 MiB scratch array with it: that needs free device memory, which the
+    tensors cached by earlier tests of this process may hold."""
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    yield
+
+
 def _state(cfg, pre, cap, dev):
     U = cfg.U
     st = {
