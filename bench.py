@@ -194,7 +194,16 @@ def run_prefill(pc, dev, reps=5):
     # the LaProx ablation's other budget allocations: per layer (head-flatten
     # only) and uniform per KV head, same scorer, segmented selection
     alloc_ms = {"head_flatten": timed(kvc.ALLOC_LAYER), "uniform": timed(kvc.ALLOC_HEAD)}
+    # MomentKV's SnapKV protocol on the same prompt and budget: accumulated
+    # window attention, first-token sink, blocks of 4, per-layer budgets
+    snap_keep = torch.empty_like(keep)
+
+    def snap():
+        kvc.kvc_prefill_snapkv(NL, Hq, Hkv, d, N, w, B, 4, 1, inp["q_win"], inp["K"], None,
+                               snap_keep, None, None, ws)
+    snap_ms = median_ms(snap, stream, reps)
     ms = timed(kvc.ALLOC_GLOBAL)
+    handoff = run_handoff(pc, inp, keep, dev, stream, reps)
     peak, kind = peaks()
     by = prefill_bytes(pc)
     ach = by / (ms * 1e-3) / 1e9
@@ -206,7 +215,50 @@ def run_prefill(pc, dev, reps=5):
                          "algorithmic_tflops": fl / (ms * 1e-3) / 1e12,
                          "kernels": "pack + prefill_val + prefill_attn + radix select"},
             "kept": int(counts.sum().item()),
-            "allocations_ms_per_call": alloc_ms}
+            "allocations_ms_per_call": alloc_ms,
+            "snapkv_ms_per_call": snap_ms,
+            "handoff": handoff}
+
+
+def median_ms(fn, stream, reps):
+    import torch
+    for _ in range(2):
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    return sorted(times)[len(times) // 2]
+
+
+def run_handoff(pc, inp, keep, dev, stream, reps):
+    """The LaProx global selection turned into a decode cache (kept rows
+    gathered, a budget per (layer, KV head), the dropped tokens folded into
+    the eviction-set moments), timed alone."""
+    import torch
+    from kv_cache_eviction_kvc_gb300 import kvc
+    U, N, d, G = pc.NL * pc.Hkv, pc.N, pc.d, pc.G
+    counts = keep.view(U, N).sum(dim=1)
+    cap = int(counts.max().item()) + 2
+    cap = (cap + 7) // 8 * 8
+    from kv_cache_eviction_kvc_gb300.state import DecodeState
+    st = DecodeState(U, G, cap, cap - 1, d=d, rule=kvc.RULE_MI, budgets=True, device=dev)
+    ws = torch.empty(kvc.kvc_prefill_handoff_workspace_size(U, N), dtype=torch.uint8, device=dev)
+
+    def call():
+        kvc.kvc_prefill_handoff(st.params, N, keep, inp["K"], inp["V"], None, None, st.cache,
+                                st.moments, st.budget, ws)
+    ms = median_ms(call, stream, reps)
+    kept = int(counts.sum().item())
+    # every prompt row read once (K and V, bf16), the kept rows written once
+    by = 2 * U * N * d * 2 + 2 * kept * d * 2
+    return {"ms_per_call": ms, "units": U, "cap": cap, "kept": kept,
+            "algorithmic_gbs": by / (ms * 1e-3) / 1e9}
 
 
 def profiled_traffic(kernel: str):
@@ -349,9 +401,11 @@ def run_ours(args, cfg, rank, world, steps=None, warmup=None, e2e=True, sample_c
     P = W.unit_params(cfg, dev, seed)
     merge = cfg.merge_recent is not None
     mi = cfg.rule == W.RULE_MI
+    chained = cfg.rule == W.RULE_EMA_CHAINED
     st = DecodeState(U, G, N + 1, L, rule=cfg.rule, alpha=cfg.alpha, refresh_period=cfg.T,
                      correction=cfg.correction, votes=bool(cfg.votes_max) or merge,
-                     kmax=N + 1 - L, device=dev, merge_recent=cfg.merge_recent)
+                     kmax=N + 1 - L, device=dev, merge_recent=cfg.merge_recent,
+                     chain=(cfg.NL, cfg.Hkv) if chained else None)
     # the prefill is drawn straight into the state's K / V (no second copy)
     pre = W.gen_prefill(cfg, dev, seed, cap=N + 1, P=P, out_K=st.K, out_V=st.V)
     st.load_prefill(pre["K"], pre["V"], pre["votes"], pre["pos"], pre["len"])
@@ -381,8 +435,10 @@ def run_ours(args, cfg, rank, world, steps=None, warmup=None, e2e=True, sample_c
     torch.cuda.synchronize()
     launches = 0
     # moment-informed rule: the residual-norm kernel, then the fused step;
-    # merge mode: the fused step, then the merge kernel
-    per_step_launches = 2 if (mi or merge) else 1
+    # merge mode: the fused step, then the merge kernel; the layer-chained EMA
+    # takes the five-call sequence (attend in two kernels, the per-sequence
+    # aggregation, fold, correction, compaction)
+    per_step_launches = 6 if chained else (2 if (mi or merge) else 1)
 
     def do_step(t, x, events=None, o=None):
         nonlocal launches
@@ -521,7 +577,10 @@ def run_ours(args, cfg, rank, world, steps=None, warmup=None, e2e=True, sample_c
     peak, peak_kind = peaks()
     ms_per_step = total_ms / steps
     kname = ("fused_step_kernel + zip_merge_kernel (kvc_decode_step, merge mode)"
-             if merge else "fused_step_kernel (kvc_decode_step, steady state)")
+             if merge else
+             "attend_chunk + attend_final + aggregate_chained + moment_fold + correct + "
+             "compact (kvc_decode_step, layer-chained EMA)" if chained else
+             "fused_step_kernel (kvc_decode_step, steady state)")
     traffic = None
     if (not merge and not mi and args.batch is None and args.prefill is None
             and cfg.T >= 1 and args.config == "C2" and cfg.name == W.C2.name):

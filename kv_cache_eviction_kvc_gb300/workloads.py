@@ -158,8 +158,15 @@ C2_MI = C2.with_(name="C2-qwen3-4b-mi", rule=RULE_MI, T=1, first_rule=RULE_EMA,
                      "prompt compressed by attention at step 1, then MomentKV "
                      "moment-informed eviction every step"))
 
+# InertiaKV's layer-chained EMA on the Llama-3.1-8B shape: one utility state
+# per sequence, carried from layer to layer of each step
+C1_CHAINED = C1.with_(name="C1-llama8b-chained", rule=RULE_EMA_CHAINED,
+                      description=C1.description.replace("EMA 0.9",
+                                                         "layer-chained EMA 0.9"))
+
 DECODE_CONFIGS = {"C0": C0, "C1": C1, "C2": C2, "C4": C4,
-                  "C2-score-free": C2_SCORE_FREE, "C2-zip": C2_ZIP, "C2-mi": C2_MI}
+                  "C2-score-free": C2_SCORE_FREE, "C2-zip": C2_ZIP, "C2-mi": C2_MI,
+                  "C1-chained": C1_CHAINED}
 PREFILL_CONFIGS = {"C3": C3}
 
 
