@@ -13,6 +13,7 @@
 #include <math.h>
 
 #include "kvc_common.cuh"
+#include "kvc_fold.h"
 #include "kvc_internal.h"
 
 namespace kvc {
@@ -98,48 +99,56 @@ __global__ void __launch_bounds__(256) attend_chunk_kernel(AttendArgs a)
         for (int j = 0; j < 16; j++) qf[h][j] *= rs;
     }
 
-    // ---- pass 1: logits
+    // ---- pass 1: logits (two groups of 4 slots per warp and iteration:
+    // both groups' rows are requested before either is used)
     float mx[G];
 #pragma unroll
     for (int h = 0; h < G; h++) mx[h] = -INFINITY;
-    for (int base = s0 + w * 4; base < s1; base += 32) {
-        const int i = base + grp;
-        const bool ok = i < s1;
-        float kf[16];
-        if (ok) {
-            const uint16_t *kr = (i == n_old) ? knew : a.K + (ubase + i) * kD;
-            uint4 r0 = (i == n_old) ? *reinterpret_cast<const uint4 *>(kr + 8 * c)
-                                    : ldg_nc_v4(kr + 8 * c);
-            uint4 r1 = (i == n_old) ? *reinterpret_cast<const uint4 *>(kr + 64 + 8 * c)
-                                    : ldg_nc_v4(kr + 64 + 8 * c);
-            unpack8(r0, kf);
-            unpack8(r1, kf + 8);
-        } else {
+    for (int base = s0 + w * 8; base < s1; base += 64) {
+        uint4 kr[2][2];
 #pragma unroll
-            for (int j = 0; j < 16; j++) kf[j] = 0.f;
-        }
-        float part[G];
-#pragma unroll
-        for (int h = 0; h < G; h++) {
-            float acc = 0.f;
-#pragma unroll
-            for (int j = 0; j < 16; j++) acc = fmaf(qf[h][j], kf[j], acc);
-            part[h] = acc;
+        for (int q2 = 0; q2 < 2; q2++) {
+            const int i = base + 4 * q2 + grp;
+            if (i < s1) {
+                const uint16_t *kp = (i == n_old) ? knew : a.K + (ubase + i) * kD;
+                kr[q2][0] = (i == n_old) ? *reinterpret_cast<const uint4 *>(kp + 8 * c)
+                                         : ldg_nc_v4(kp + 8 * c);
+                kr[q2][1] = (i == n_old) ? *reinterpret_cast<const uint4 *>(kp + 64 + 8 * c)
+                                         : ldg_nc_v4(kp + 64 + 8 * c);
+            } else {
+                kr[q2][0] = kr[q2][1] = make_uint4(0, 0, 0, 0);
+            }
         }
 #pragma unroll
-        for (int m = 1; m < 8; m <<= 1)
-#pragma unroll
-            for (int h = 0; h < G; h++) part[h] += __shfl_xor_sync(kFull, part[h], m);
-        if (ok) {
-            float lnp = 0.f;
-            if (a.votes && i != n_old) lnp = logf((float)a.votes[ubase + i]);
+        for (int q2 = 0; q2 < 2; q2++) {
+            const int i = base + 4 * q2 + grp;
+            const bool ok = i < s1;
+            float kf[16];
+            unpack8(kr[q2][0], kf);
+            unpack8(kr[q2][1], kf + 8);
+            float part[G];
 #pragma unroll
             for (int h = 0; h < G; h++) {
-                const float x = part[h] + lnp;
-                mx[h] = fmaxf(mx[h], x);
-                if (c == h) {
-                    xs[h][i - s0] = x;
-                    if (a.want_x) a.xbuf[((size_t)u * G + h) * a.cap + i] = x;
+                float acc = 0.f;
+#pragma unroll
+                for (int j = 0; j < 16; j++) acc = fmaf(qf[h][j], kf[j], acc);
+                part[h] = acc;
+            }
+#pragma unroll
+            for (int m = 1; m < 8; m <<= 1)
+#pragma unroll
+                for (int h = 0; h < G; h++) part[h] += __shfl_xor_sync(kFull, part[h], m);
+            if (ok) {
+                float lnp = 0.f;
+                if (a.votes && i != n_old) lnp = logf((float)a.votes[ubase + i]);
+#pragma unroll
+                for (int h = 0; h < G; h++) {
+                    const float x = part[h] + lnp;
+                    mx[h] = fmaxf(mx[h], x);
+                    if (c == h) {
+                        xs[h][i - s0] = x;
+                        if (a.want_x) a.xbuf[((size_t)u * G + h) * a.cap + i] = x;
+                    }
                 }
             }
         }
@@ -169,23 +178,33 @@ __global__ void __launch_bounds__(256) attend_chunk_kernel(AttendArgs a)
 #pragma unroll
         for (int j = 0; j < 16; j++) acc[h][j] = 0.f;
     }
-    for (int base = s0 + w * 4; base < s1; base += 32) {
-        const int i = base + grp;
-        if (i < s1) {
-            const uint16_t *vr = (i == n_old) ? vnew : a.V + (ubase + i) * kD;
-            uint4 r0 = (i == n_old) ? *reinterpret_cast<const uint4 *>(vr + 8 * c)
-                                    : ldg_nc_v4(vr + 8 * c);
-            uint4 r1 = (i == n_old) ? *reinterpret_cast<const uint4 *>(vr + 64 + 8 * c)
-                                    : ldg_nc_v4(vr + 64 + 8 * c);
-            float vf[16];
-            unpack8(r0, vf);
-            unpack8(r1, vf + 8);
+    for (int base = s0 + w * 8; base < s1; base += 64) {
+        uint4 vr[2][2];
 #pragma unroll
-            for (int h = 0; h < G; h++) {
-                const float p = expf(xs[h][i - s0] - M[h]);
-                if (c == 0) lsum[h] += p;
+        for (int q2 = 0; q2 < 2; q2++) {
+            const int i = base + 4 * q2 + grp;
+            if (i < s1) {
+                const uint16_t *vp = (i == n_old) ? vnew : a.V + (ubase + i) * kD;
+                vr[q2][0] = (i == n_old) ? *reinterpret_cast<const uint4 *>(vp + 8 * c)
+                                         : ldg_nc_v4(vp + 8 * c);
+                vr[q2][1] = (i == n_old) ? *reinterpret_cast<const uint4 *>(vp + 64 + 8 * c)
+                                         : ldg_nc_v4(vp + 64 + 8 * c);
+            }
+        }
 #pragma unroll
-                for (int j = 0; j < 16; j++) acc[h][j] = fmaf(p, vf[j], acc[h][j]);
+        for (int q2 = 0; q2 < 2; q2++) {
+            const int i = base + 4 * q2 + grp;
+            if (i < s1) {
+                float vf[16];
+                unpack8(vr[q2][0], vf);
+                unpack8(vr[q2][1], vf + 8);
+#pragma unroll
+                for (int h = 0; h < G; h++) {
+                    const float p = expf(xs[h][i - s0] - M[h]);
+                    if (c == 0) lsum[h] += p;
+#pragma unroll
+                    for (int j = 0; j < 16; j++) acc[h][j] = fmaf(p, vf[j], acc[h][j]);
+                }
             }
         }
     }
@@ -350,29 +369,57 @@ struct AggArgs {
 
 // k-th smallest (0-based rank) key among the slots where valid(i); returns
 // the key and, through *below, how many valid keys are strictly smaller.
+// blockDim.x is a multiple of 32 and at least 64.  Histogram updates are
+// aggregated per warp over the lanes with the same digit (the digits of a
+// pass are often concentrated in a few bins); warp 0 scans the 256 bins.
 template <typename Key, typename KeyF, typename ValidF>
 __device__ Key block_select(int n, int rank, KeyF key, ValidF valid,
                             int *hist, int *bcast, int *below)
 {
     Key prefix = 0, mask = 0;
     const int rank0 = rank;
+    const int lane = threadIdx.x & 31;
     for (int shift = (int)sizeof(Key) * 8 - 8; shift >= 0; shift -= 8) {
         for (int b = threadIdx.x; b < 256; b += blockDim.x) hist[b] = 0;
         __syncthreads();
-        for (int i = threadIdx.x; i < n; i += blockDim.x) {
-            if (!valid(i)) continue;
-            const Key k = key(i);
-            if ((k & mask) == prefix) atomicAdd(&hist[(int)((k >> shift) & 255)], 1);
+        for (int b0 = 0; b0 < n; b0 += blockDim.x) {
+            const int i = b0 + (int)threadIdx.x;
+            int bin = -1;
+            if (i < n && valid(i)) {
+                const Key k = key(i);
+                if ((k & mask) == prefix) bin = (int)((k >> shift) & 255);
+            }
+            const unsigned peers = __match_any_sync(kFull, bin);
+            if (bin >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
         }
         __syncthreads();
-        if (threadIdx.x == 0) {
-            int cum = 0, b = 0;
-            for (; b < 255; b++) {
-                if (cum + hist[b] > rank) break;
-                cum += hist[b];
+        if (threadIdx.x < 32) {
+            // lane l holds bins 8l .. 8l + 7
+            int h[8], loc = 0;
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                h[j] = hist[8 * lane + j];
+                loc += h[j];
             }
-            bcast[0] = b;
-            bcast[1] = rank - cum;
+            int incl = loc;
+#pragma unroll
+            for (int m = 1; m < 32; m <<= 1) {
+                const int t = __shfl_up_sync(kFull, incl, m);
+                if (lane >= m) incl += t;
+            }
+            const int excl = incl - loc;
+            // the first lane whose bins take the cumulative count past rank
+            const unsigned over = __ballot_sync(kFull, incl > rank);
+            const int src = over ? __ffs(over) - 1 : 31;
+            if (lane == src) {
+                int cum = excl, b = 0;
+                for (; b < 7; b++) {
+                    if (cum + h[b] > rank) break;
+                    cum += h[b];
+                }
+                bcast[0] = 8 * lane + b;
+                bcast[1] = rank - cum;
+            }
         }
         __syncthreads();
         prefix |= ((Key)bcast[0]) << shift;
@@ -727,6 +774,10 @@ cudaError_t launch_moment(const kvc_params &p, const kvc_cache &c, int kmax,
                           const kvc_moments &m, const DecodeWs &ws,
                           cudaStream_t st)
 {
+    // many victims per unit (the first step over the prompt, a hand-off):
+    // the tensor-core fold, one 128-victim tile at a time
+    if (kmax >= kFoldTcMin)
+        return launch_fold_tc(c, p.cap, p.U, kmax, evict_idx, n_evict, m, ws.status, st);
     MomArgs a{c.K, c.V, c.votes, c.len, evict_idx, n_evict, m.n, m.mu_k, m.mu_v, m.C,
               ws.status, p.cap, kmax};
     moment_fold_kernel<<<p.U, 256, 0, st>>>(a);
@@ -850,9 +901,34 @@ __global__ void __launch_bounds__(256) correct_kernel(CorrArgs a)
 #pragma unroll
             for (int j = 0; j < 16; j++) acc[h][j] = 0.f;
         }
-        for (int base = w * 4; base < n; base += 32) {
-            const int i = base + grp;
-            const bool live = i < n && !((evbits[i >> 5] >> (i & 31)) & 1u);
+        // warp w walks the bitmap words w, w + 8, ...; the slots of a word
+        // that were not evicted go four at a time (slot group grp takes the
+        // grp-th lowest of the next four), so evicted slots cost nothing
+        const int nwords = (n + 31) >> 5;
+        int wi = w;
+        uint32_t pend = 0;
+        if (wi < nwords) {
+            pend = ~evbits[wi];
+            if (wi == nwords - 1 && (n & 31)) pend &= (1u << (n & 31)) - 1u;
+        }
+        for (;;) {
+            while (pend == 0 && wi < nwords) {
+                wi += 8;
+                if (wi < nwords) {
+                    pend = ~evbits[wi];
+                    if (wi == nwords - 1 && (n & 31)) pend &= (1u << (n & 31)) - 1u;
+                }
+            }
+            if (wi >= nwords) break;
+            int i = -1;
+#pragma unroll
+            for (int g = 0; g < 4; g++) {
+                if (pend) {
+                    if (g == grp) i = 32 * wi + __ffs(pend) - 1;
+                    pend &= pend - 1u;
+                }
+            }
+            const bool live = i >= 0;
             float kf[16], vf[16];
             if (live) {
                 const uint16_t *kr = a.K + (ubase + i) * kD;
