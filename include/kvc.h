@@ -460,7 +460,7 @@ KVC_API kvc_status kvc_decode_step(const kvc_params *p, int32_t t, int32_t new_p
  * holds until the process exits.  The call allocates nothing (no cudaMalloc,
  * cudaFree or allocating library routine).
  * - Sizes whose scratch exceeds 32 MiB are rejected with KVC_ERR_WORKSPACE
- *   and a message.  The scratch is about U*ceil(cap/512)*G*520 bytes, plus
+ *   and a message.  The scratch is about U*ceil(cap/1024)*G*520 bytes, plus
  *   U*G*cap*4 bytes of logits when probs != NULL (the logits are only kept
  *   to form the probabilities).
  * - Each call looks up the array's device address in the calling thread's

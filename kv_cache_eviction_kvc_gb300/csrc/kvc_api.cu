@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include "kvc_common.cuh"
+#include "kvc_general.h"
 #include "kvc_internal.h"
 #include "kvc_mi.h"
 
@@ -45,6 +46,8 @@ DecodeWs decode_ws_layout(const kvc_params &p, void *base)
     off += align_up(U * G * kD * sizeof(float));
     w.probs = reinterpret_cast<double *>(b ? b + off : nullptr);
     off += align_up(U * cap * sizeof(double));
+    w.pmom = reinterpret_cast<float *>(b ? b + off : nullptr);
+    off += align_up(U * (size_t)kPMomStride * sizeof(float));
     w.bytes = off;
     return w;
 }
@@ -421,6 +424,36 @@ kvc_status kvc_decode_step(const kvc_params *p, int32_t t, int32_t new_pos, int3
     if (p->rule == KVC_RULE_MI && max_len - p->L > 1) KVC_TRY(check_mi_greedy(p, max_len));
     const bool refresh = is_refresh(t, p->refresh_period);
     double *pr = probs ? probs : w.probs;
+    // most of every unit goes (the first step over the prompt): one pass
+    // gives the attention and the moments of all slots; after compaction a
+    // second pass over the retained slots gives f_R, log Z_R and, by the
+    // reverse of Chan's update, the evicted set's moments
+    if (!p->merge && p->rule != KVC_RULE_MI && max_len - p->L >= kFoldTcMin &&
+        2 * (max_len - p->L) > max_len) {
+        cudaError_t e = launch_prompt_pass(*p, new_pos, max_len, q, k_new, v_new, *cache, true,
+                                           refresh, nullptr, *mom, w, st);
+        if (e != cudaErrorNotSupported) {
+            KVC_TRY(cuda_status(e, "kvc_decode_step prompt pass"));
+            KVC_TRY(cuda_status(launch_attend_final(*p, max_len, *cache, w.lse, w.fall,
+                                                    refresh ? pr : nullptr, w, st),
+                                "kvc_decode_step attend merge"));
+            KVC_TRY(cuda_status(launch_aggregate(*p, t, pr, *cache, kmax, evict_idx, evict_pos,
+                                                 n_evict, w, st),
+                                "kvc_decode_step aggregate"));
+            KVC_TRY(cuda_status(launch_fold_tc(*cache, p->cap, p->U, kmax, evict_idx, n_evict, *mom,
+                                               w.status, st, true),
+                                "kvc_decode_step moments"));
+            KVC_TRY(cuda_status(launch_compact(*p, *cache, kmax, evict_idx, n_evict, w, st),
+                                "kvc_decode_step compact"));
+            KVC_TRY(cuda_status(launch_prompt_pass(*p, new_pos, p->L, q, nullptr, nullptr, *cache,
+                                                   false, false, n_evict, *mom, w, st),
+                                "kvc_decode_step retained pass"));
+            KVC_TRY(cuda_status(launch_attend_final(*p, p->L, *cache, w.lse, w.fall, nullptr, w, st),
+                                "kvc_decode_step retained merge"));
+            return cuda_status(launch_correct_retained(*p, q, *cache, w.lse, w.fall, *mom, o, w, st),
+                               "kvc_decode_step correct");
+        }
+    }
     KVC_TRY(cuda_status(launch_attend(*p, t, new_pos, max_len, q, k_new, v_new, *cache, w.lse,
                                       w.fall, refresh ? pr : nullptr, w, st),
                         "kvc_decode_step attend"));
@@ -446,6 +479,18 @@ kvc_status kvc_decode_step(const kvc_params *p, int32_t t, int32_t new_pos, int3
     }
     KVC_TRY(cuda_status(launch_aggregate(*p, t, pr, *cache, kmax, evict_idx, evict_pos, n_evict, w, st),
                         "kvc_decode_step aggregate"));
+    if (!p->merge && max_len - p->L > kRetainedMin) {
+        // many slots go: fold them, compact, then attend over the slots that
+        // stay (contiguous now) for f_R and log Z_R, and correct
+        KVC_TRY(cuda_status(launch_moment(*p, *cache, kmax, evict_idx, n_evict, *mom, w, st),
+                            "kvc_decode_step moments"));
+        KVC_TRY(cuda_status(launch_compact(*p, *cache, kmax, evict_idx, n_evict, w, st),
+                            "kvc_decode_step compact"));
+        KVC_TRY(cuda_status(launch_attend_retained(*p, p->L, q, *cache, w.lse, w.fall, w, st),
+                            "kvc_decode_step retained attention"));
+        return cuda_status(launch_correct_retained(*p, q, *cache, w.lse, w.fall, *mom, o, w, st),
+                           "kvc_decode_step correct");
+    }
     if (p->merge) {
         KVC_TRY(cuda_status(launch_zip_merge(*p, new_pos, q, *cache, kmax, evict_idx, n_evict,
                                              nullptr, w, st),

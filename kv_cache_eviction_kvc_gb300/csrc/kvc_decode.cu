@@ -13,7 +13,7 @@
 #include <math.h>
 
 #include "kvc_common.cuh"
-#include "kvc_fold.h"
+#include "kvc_general.h"
 #include "kvc_internal.h"
 
 namespace kvc {
@@ -37,6 +37,7 @@ struct AttendArgs {
     int32_t *nlen, *status;
     int U, cap, max_len, new_pos, S;
     int want_x;
+    int append;        // 0: attend over the live slots as they are (no new token)
 };
 
 template <int G>
@@ -54,7 +55,7 @@ __global__ void __launch_bounds__(256) attend_chunk_kernel(AttendArgs a)
     const int grp = lane >> 3, c = lane & 7;
 
     const int n_old = a.len[u];
-    const int n = n_old + 1;
+    const int n = a.append ? n_old + 1 : n_old;
     if (n_old < 0 || n > a.max_len || n > a.cap) {
         if (s == 0 && tid == 0) {
             record_status(a.status, KVC_ERR_SHAPE);
@@ -68,11 +69,11 @@ __global__ void __launch_bounds__(256) attend_chunk_kernel(AttendArgs a)
     if (s == 0 && tid == 0) a.nlen[u] = n;
 
     const size_t ubase = (size_t)u * a.cap;
-    const uint16_t *knew = a.k_new + (size_t)u * kD;
-    const uint16_t *vnew = a.v_new + (size_t)u * kD;
+    const uint16_t *knew = a.append ? a.k_new + (size_t)u * kD : nullptr;
+    const uint16_t *vnew = a.append ? a.v_new + (size_t)u * kD : nullptr;
 
     // the chunk holding the new slot appends it
-    if (n_old >= s0 && n_old < s1) {
+    if (a.append && n_old >= s0 && n_old < s1) {
         if (tid < 32) {
             uint16_t *kd = a.K + (ubase + n_old) * kD;
             uint16_t *vd = a.V + (ubase + n_old) * kD;
@@ -300,14 +301,35 @@ __global__ void __launch_bounds__(256) attend_final_kernel(FinalArgs a)
         }
     }
     if (a.probs) {
-        // s_i = (1/G) sum_h exp(x_hi - M_h) / l_h, formed in fp64
+        // s_i = (1/G) sum_h exp(x_hi - M_h) / l_h.  While the largest head
+        // term is above e^-60 the sum is far inside fp32's range and fp32
+        // carries it to a few units in the last place (the fused step forms
+        // it the same way); below that the fp64 form keeps the range.  G is a
+        // power of two, so the 1/G factor is exact.
         const int i0 = s2 * kProbsChunk, i1 = min(n, i0 + kProbsChunk);
-        for (int i = i0 + tid; i < i1; i += blockDim.x) {
-            double sacc = 0.0;
+        float rl32[G];
 #pragma unroll
-            for (int h = 0; h < G; h++)
-                sacc += exp_wide(a.xbuf[((size_t)u * G + h) * a.cap + i] - Ms[h]) * Rl[h];
-            a.probs[(size_t)u * a.cap + i] = sacc / G;
+        for (int h = 0; h < G; h++) rl32[h] = (float)(Rl[h] * (1.0 / G));
+        for (int i = i0 + tid; i < i1; i += blockDim.x) {
+            float y[G], ymax = -INFINITY;
+#pragma unroll
+            for (int h = 0; h < G; h++) {
+                y[h] = a.xbuf[((size_t)u * G + h) * a.cap + i] - Ms[h];
+                ymax = fmaxf(ymax, y[h]);
+            }
+            double sv;
+            if (ymax > -60.f) {
+                float s32 = 0.f;
+#pragma unroll
+                for (int h = 0; h < G; h++) s32 = fmaf(expf(y[h]), rl32[h], s32);
+                sv = (double)s32;
+            } else {
+                double sacc = 0.0;
+#pragma unroll
+                for (int h = 0; h < G; h++) sacc = fma(exp_wide(y[h]), Rl[h], sacc);
+                sv = sacc * (1.0 / G);
+            }
+            a.probs[(size_t)u * a.cap + i] = sv;
         }
     }
 }
@@ -317,13 +339,13 @@ static cudaError_t launch_attend_g(const kvc_params &p, int new_pos, int max_len
                                    const uint16_t *q, const uint16_t *k_new,
                                    const uint16_t *v_new, const kvc_cache &c,
                                    float *lse, float *f_all, double *probs,
-                                   const DecodeWs &ws, cudaStream_t st)
+                                   const DecodeWs &ws, cudaStream_t st, bool append = true)
 {
     const int S = (p.cap + kAttendChunk - 1) / kAttendChunk;
     const int Sl = (max_len + kAttendChunk - 1) / kAttendChunk;
     AttendArgs a{q, k_new, v_new, c.K, c.V, c.votes, c.pos, c.util, c.len,
                  ws.xbuf, ws.part, ws.nlen, ws.status, p.U, p.cap, max_len,
-                 new_pos, S, probs != nullptr};
+                 new_pos, S, probs != nullptr, append ? 1 : 0};
     dim3 g1(p.U, Sl);
     attend_chunk_kernel<G><<<g1, 256, 0, st>>>(a);
     cudaError_t e = cudaGetLastError();
@@ -350,6 +372,42 @@ cudaError_t launch_attend(const kvc_params &p, int t, int new_pos, int max_len,
     }
 }
 
+template <int G>
+static cudaError_t launch_final_g(const kvc_params &p, int max_len, const kvc_cache &c, float *lse,
+                                  float *f, double *probs, const DecodeWs &ws, cudaStream_t st)
+{
+    const int S = (p.cap + kAttendChunk - 1) / kAttendChunk;
+    FinalArgs fa{ws.part, ws.xbuf, ws.nlen, c.len, lse, f, probs, p.U, p.cap, S};
+    const int S2 = probs ? (max_len + kProbsChunk - 1) / kProbsChunk : 1;
+    attend_final_kernel<G><<<dim3(p.U, S2), 256, 0, st>>>(fa);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attend_final(const kvc_params &p, int max_len, const kvc_cache &c, float *lse,
+                                float *f, double *probs, const DecodeWs &ws, cudaStream_t st)
+{
+    switch (p.G) {
+    case 1: return launch_final_g<1>(p, max_len, c, lse, f, probs, ws, st);
+    case 2: return launch_final_g<2>(p, max_len, c, lse, f, probs, ws, st);
+    case 4: return launch_final_g<4>(p, max_len, c, lse, f, probs, ws, st);
+    case 8: return launch_final_g<8>(p, max_len, c, lse, f, probs, ws, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_attend_retained(const kvc_params &p, int max_len, const uint16_t *q,
+                                   const kvc_cache &c, float *lse, float *f, const DecodeWs &ws,
+                                   cudaStream_t st)
+{
+    switch (p.G) {
+    case 1: return launch_attend_g<1>(p, 0, max_len, q, nullptr, nullptr, c, lse, f, nullptr, ws, st, false);
+    case 2: return launch_attend_g<2>(p, 0, max_len, q, nullptr, nullptr, c, lse, f, nullptr, ws, st, false);
+    case 4: return launch_attend_g<4>(p, 0, max_len, q, nullptr, nullptr, c, lse, f, nullptr, ws, st, false);
+    case 8: return launch_attend_g<8>(p, 0, max_len, q, nullptr, nullptr, c, lse, f, nullptr, ws, st, false);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
 // ================================================================== aggregate
 //
 // One CTA per unit.  Refresh steps update the utilities in place; then the
@@ -367,6 +425,19 @@ struct AggArgs {
     float alpha;
 };
 
+// Utilities of slots not yet scored are +inf.  The tests below look at the
+// bit pattern (integer operations): fp64 compares run on the fp64 pipe, which
+// is narrow on this part, and these loops touch every slot several times.
+__device__ __forceinline__ bool unscored_bits(uint64_t b)
+{
+    return (b & 0x7fffffffffffffffull) == 0x7ff0000000000000ull;
+}
+
+__device__ __forceinline__ uint64_t util_bits(const double *util, int i)
+{
+    return (uint64_t)__double_as_longlong(util[i]);
+}
+
 // k-th smallest (0-based rank) key among the slots where valid(i); returns
 // the key and, through *below, how many valid keys are strictly smaller.
 // blockDim.x is a multiple of 32 and at least 64.  Histogram updates are
@@ -374,7 +445,7 @@ struct AggArgs {
 // pass are often concentrated in a few bins); warp 0 scans the 256 bins.
 template <typename Key, typename KeyF, typename ValidF>
 __device__ Key block_select(int n, int rank, KeyF key, ValidF valid,
-                            int *hist, int *bcast, int *below)
+                            int *hist, int *bcast, int *below, int *equal = nullptr)
 {
     Key prefix = 0, mask = 0;
     const int rank0 = rank;
@@ -382,15 +453,24 @@ __device__ Key block_select(int n, int rank, KeyF key, ValidF valid,
     for (int shift = (int)sizeof(Key) * 8 - 8; shift >= 0; shift -= 8) {
         for (int b = threadIdx.x; b < 256; b += blockDim.x) hist[b] = 0;
         __syncthreads();
-        for (int b0 = 0; b0 < n; b0 += blockDim.x) {
-            const int i = b0 + (int)threadIdx.x;
-            int bin = -1;
-            if (i < n && valid(i)) {
-                const Key k = key(i);
-                if ((k & mask) == prefix) bin = (int)((k >> shift) & 255);
+        // four slots per thread per iteration: every key is read before any
+        // is binned (the reads overlap)
+        for (int b0 = 0; b0 < n; b0 += 4 * (int)blockDim.x) {
+            int bin[4];
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const int i = b0 + j * (int)blockDim.x + (int)threadIdx.x;
+                bin[j] = -1;
+                if (i < n && valid(i)) {
+                    const Key k = key(i);
+                    if ((k & mask) == prefix) bin[j] = (int)((k >> shift) & 255);
+                }
             }
-            const unsigned peers = __match_any_sync(kFull, bin);
-            if (bin >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const unsigned peers = __match_any_sync(kFull, bin[j]);
+                if (bin[j] >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[bin[j]], __popc(peers));
+            }
         }
         __syncthreads();
         if (threadIdx.x < 32) {
@@ -419,12 +499,14 @@ __device__ Key block_select(int n, int rank, KeyF key, ValidF valid,
                 }
                 bcast[0] = 8 * lane + b;
                 bcast[1] = rank - cum;
+                bcast[2] = h[b];                  // keys in the chosen bin
             }
         }
         __syncthreads();
         prefix |= ((Key)bcast[0]) << shift;
         mask |= ((Key)255) << shift;
         rank = bcast[1];
+        if (shift == 0 && equal) *equal = bcast[2];   // keys equal to the result
         __syncthreads();
     }
     *below = rank0 - rank;
@@ -460,38 +542,74 @@ __device__ void aggregate_select(const AggArgs &a, int u, int n, int *hist, int 
         return;
     }
     int cnt = 0;
-    for (int i = tid; i < n; i += blockDim.x) cnt += !isinf(util[i]);
+    for (int i0 = tid; i0 < n; i0 += 4 * blockDim.x) {
+        bool sc[4];
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const int i = i0 + j * blockDim.x;
+            sc[j] = i < n && !unscored_bits(util_bits(util, i));
+        }
+#pragma unroll
+        for (int j = 0; j < 4; j++) cnt += sc[j];
+    }
     int total;
     block_exscan(cnt, scan, &total);
     if (total < k) {
         if (tid == 0) { a.n_evict[u] = 0; record_status(a.status, KVC_ERR_INVALID_ARG); }
         return;
     }
-    auto scored = [&](int i) { return !isinf(util[i]); };
+    auto scored = [&](int i) { return !unscored_bits(util_bits(util, i)); };
     auto ukey = [&](int i) { return double_key(util[i]); };
-    int below;
-    const uint64_t kth = block_select<uint64_t>(n, k - 1, ukey, scored, hist, bcast, &below);
+    int below, equal;
+    const uint64_t kth = block_select<uint64_t>(n, k - 1, ukey, scored, hist, bcast, &below, &equal);
     const int need = k - below;       // slots to take from the tie group
-    auto tie = [&](int i) { return !isinf(util[i]) && double_key(util[i]) == kth; };
+    auto tie = [&](int i) {
+        const uint64_t b = util_bits(util, i);
+        return !unscored_bits(b) && double_key(__longlong_as_double((long long)b)) == kth;
+    };
     auto pkey = [&](int i) { return (uint32_t)pos[i] ^ 0x80000000u; };
+    // the positions settle the tie group only when part of it goes (with
+    // distinct utilities the group is the one slot at the threshold)
     int below2;
-    const uint32_t pth = block_select<uint32_t>(n, need - 1, pkey, tie, hist, bcast, &below2);
-    // write the victims in ascending slot order
-    int written = 0;
-    for (int b0 = 0; b0 < n; b0 += blockDim.x) {
-        const int i = b0 + tid;
-        int sel = 0;
-        if (i < n && !isinf(util[i])) {
-            const uint64_t kk = double_key(util[i]);
-            sel = kk < kth || (kk == kth && pkey(i) <= pth);
+    const uint32_t pth = equal == need
+                             ? 0xffffffffu
+                             : block_select<uint32_t>(n, need - 1, pkey, tie, hist, bcast, &below2);
+    // write the victims in ascending slot order: warp w takes a contiguous
+    // segment of the slots, counts its victims (one block scan of the
+    // counts), then writes them from its offset
+    auto selected = [&](int i) {
+        const uint64_t b = util_bits(util, i);
+        if (unscored_bits(b)) return false;
+        const uint64_t kk = double_key(__longlong_as_double((long long)b));
+        return kk < kth || (kk == kth && pkey(i) <= pth);
+    };
+    const int lane = tid & 31, nwarps = blockDim.x >> 5;
+    const int seg = (((n + nwarps - 1) / nwarps) + 31) & ~31;
+    const int sb = (tid >> 5) * seg, se = min(n, sb + seg);
+    int wc = 0;
+    for (int i0 = sb; i0 < se; i0 += 128) {
+        bool sl[4];
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const int i = i0 + 32 * j + lane;
+            sl[j] = i < se && selected(i);
         }
-        int tot;
-        const int ex = block_exscan(sel, scan, &tot);
-        if (sel && written + ex < a.kmax) {
-            a.evict_idx[(size_t)u * a.kmax + written + ex] = i;
-            if (a.evict_pos) a.evict_pos[(size_t)u * a.kmax + written + ex] = pos[i];
+#pragma unroll
+        for (int j = 0; j < 4; j++) wc += __popc(__ballot_sync(kFull, sl[j]));
+    }
+    int written;
+    int off = block_exscan(lane == 0 ? wc : 0, scan, &written);
+    off = __shfl_sync(kFull, off, 0);
+    for (int i0 = sb; i0 < se; i0 += 32) {
+        const int i = i0 + lane;
+        const bool sl = i < se && selected(i);
+        const unsigned b = __ballot_sync(kFull, sl);
+        const int r = off + __popc(b & ((1u << lane) - 1u));
+        if (sl && r < a.kmax) {
+            a.evict_idx[(size_t)u * a.kmax + r] = i;
+            if (a.evict_pos) a.evict_pos[(size_t)u * a.kmax + r] = pos[i];
         }
-        written += tot;
+        off += __popc(b);
     }
     if (tid == 0) {
         a.n_evict[u] = written == k ? k : 0;     // duplicate positions: refuse
@@ -508,7 +626,6 @@ __global__ void __launch_bounds__(512) aggregate_kernel(AggArgs a)
     const int u = blockIdx.x, tid = threadIdx.x;
     const int n = a.len[u];
     double *util = a.util + (size_t)u * a.cap;
-    const int32_t *pos = a.pos + (size_t)u * a.cap;
     if (n < 0 || n > a.cap) {
         if (tid == 0) { a.n_evict[u] = 0; record_status(a.status, KVC_ERR_SHAPE); }
         return;
@@ -517,14 +634,25 @@ __global__ void __launch_bounds__(512) aggregate_kernel(AggArgs a)
         if (tid == 0) a.pend[(size_t)u * kPendStride] = 0;   // fused-step queue now stale
         const double *pr = a.probs + (size_t)u * a.cap;
         const double al = (double)a.alpha;
-        for (int i = tid; i < n; i += blockDim.x) {
-            const double s = pr[i], m = util[i];
-            double r;
-            if (isinf(m)) r = s;                           // first observation
-            else if (a.rule == KVC_RULE_SINGLE || a.rule == KVC_RULE_MI) r = s;   // MI: s is the score
-            else if (a.rule == KVC_RULE_CUMULATIVE) r = m + s;
-            else r = al * m + (1.0 - al) * s;
-            util[i] = r;
+        for (int i0 = tid; i0 < n; i0 += 4 * blockDim.x) {
+            double sv[4], mv[4];
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const int i = i0 + j * blockDim.x;
+                sv[j] = i < n ? pr[i] : 0.0;
+                mv[j] = i < n ? util[i] : 0.0;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const int i = i0 + j * blockDim.x;
+                const double s = sv[j], m = mv[j];
+                double r;
+                if (unscored_bits((uint64_t)__double_as_longlong(m))) r = s;   // first observation
+                else if (a.rule == KVC_RULE_SINGLE || a.rule == KVC_RULE_MI) r = s;   // MI: s is the score
+                else if (a.rule == KVC_RULE_CUMULATIVE) r = m + s;
+                else r = al * m + (1.0 - al) * s;
+                if (i < n) util[i] = r;
+            }
         }
         __syncthreads();
     }
@@ -588,6 +716,163 @@ __global__ void __launch_bounds__(512) aggregate_chained_kernel(AggArgs a, int N
     }
 }
 
+// Steps with many victims per unit: the same selection with the keys in
+// shared memory.  One pass updates the utilities (refresh steps) and keeps
+// the top 32 bits of every order key; the radix passes run on those; the
+// group of slots whose top bits equal the threshold's is settled by the
+// full key and the position.  One CTA of 1024 threads per unit, the keys
+// of up to kAggKeysMax slots.
+constexpr int kAggKeysMax = 49152;
+constexpr int kAggGroupMax = 1024;
+constexpr uint32_t kUnscored32 = 0xFFF00000u;     // top bits of +inf's order key
+
+__global__ void __launch_bounds__(1024, 1) aggregate_keys_kernel(AggArgs a)
+{
+    extern __shared__ uint32_t k32[];              // [len]
+    __shared__ int hist[256];
+    __shared__ int bcast[4];
+    __shared__ int scan[40];
+    __shared__ int gidx[kAggGroupMax];
+    __shared__ unsigned long long gkey[kAggGroupMax];
+    __shared__ int gcount;
+    __shared__ unsigned long long th_key;
+    __shared__ int th_pos;
+    const int u = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+    const int n = a.len[u];
+    double *util = a.util + (size_t)u * a.cap;
+    const int32_t *pos = a.pos + (size_t)u * a.cap;
+    if (n < 0 || n > a.cap || n > kAggKeysMax) {
+        if (tid == 0) { a.n_evict[u] = 0; record_status(a.status, KVC_ERR_SHAPE); }
+        return;
+    }
+    const double al = (double)a.alpha;
+    const double *pr = a.probs + (size_t)u * a.cap;
+    if (a.refresh && tid == 0) a.pend[(size_t)u * kPendStride] = 0;   // fused-step queue now stale
+    for (int i0 = tid; i0 < n; i0 += 4 * blockDim.x) {
+        double sv[4], mv[4];
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const int i = i0 + j * blockDim.x;
+            sv[j] = (a.refresh && i < n) ? pr[i] : 0.0;
+            mv[j] = i < n ? util[i] : 0.0;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const int i = i0 + j * blockDim.x;
+            if (i >= n) continue;
+            double r = mv[j];
+            if (a.refresh) {
+                const double s = sv[j], m = mv[j];
+                if (unscored_bits((uint64_t)__double_as_longlong(m))) r = s;   // first observation
+                else if (a.rule == KVC_RULE_SINGLE || a.rule == KVC_RULE_MI) r = s;
+                else if (a.rule == KVC_RULE_CUMULATIVE) r = m + s;
+                else r = al * m + (1.0 - al) * s;
+                util[i] = r;
+            }
+            k32[i] = (uint32_t)(double_key(r) >> 32);
+        }
+    }
+    __syncthreads();
+    const int Lb = a.budget ? a.budget[u] : a.L;
+    if (Lb < 1 || Lb > a.L) {
+        if (tid == 0) { a.n_evict[u] = 0; record_status(a.status, KVC_ERR_SHAPE); }
+        return;
+    }
+    const int k = n - Lb;
+    if (k <= 0) {
+        if (tid == 0) a.n_evict[u] = 0;
+        return;
+    }
+    if ((a.rule == KVC_RULE_MI && k > 1) || k > a.kmax) {
+        if (tid == 0) {
+            a.n_evict[u] = 0;
+            record_status(a.status, a.rule == KVC_RULE_MI && k > 1 ? KVC_ERR_UNSUPPORTED : KVC_ERR_SHAPE);
+        }
+        return;
+    }
+    int cnt = 0;
+    for (int i = tid; i < n; i += blockDim.x) cnt += k32[i] < kUnscored32;
+    int total;
+    block_exscan(cnt, scan, &total);
+    if (total < k) {
+        if (tid == 0) { a.n_evict[u] = 0; record_status(a.status, KVC_ERR_INVALID_ARG); }
+        return;
+    }
+    auto valid = [&](int i) { return k32[i] < kUnscored32; };
+    auto key = [&](int i) { return k32[i]; };
+    int below, equal;
+    const uint32_t T32 = block_select<uint32_t>(n, k - 1, key, valid, hist, bcast, &below, &equal);
+    const int need = k - below;            // from the group whose top bits equal T32
+    const bool whole = need == equal;
+    if (!whole) {
+        if (equal > kAggGroupMax) {        // a large tie group: the selection on the full keys
+            aggregate_select(a, u, n, hist, bcast, scan);
+            return;
+        }
+        if (tid == 0) gcount = 0;
+        __syncthreads();
+        for (int i = tid; i < n; i += blockDim.x)
+            if (k32[i] == T32) {
+                const int j = atomicAdd(&gcount, 1);
+                gidx[j] = i;
+                gkey[j] = double_key(util[i]);
+            }
+        __syncthreads();
+        const int m = gcount;
+        for (int j = tid; j < m; j += blockDim.x) {
+            const unsigned long long kj = gkey[j];
+            const int pj = pos[gidx[j]];
+            int rank = 0;
+            for (int l = 0; l < m; l++) {
+                const unsigned long long kl = gkey[l];
+                rank += kl < kj || (kl == kj && pos[gidx[l]] < pj);
+            }
+            if (rank == need - 1) {
+                th_key = kj;
+                th_pos = pj;
+            }
+        }
+        __syncthreads();
+    }
+    const unsigned long long tk = whole ? 0ull : th_key;
+    const int tp = whole ? 0 : th_pos;
+    auto selected = [&](int i) {
+        const uint32_t k_ = k32[i];
+        if (k_ < T32) return true;
+        if (k_ != T32) return false;
+        if (whole) return true;
+        const unsigned long long kk = double_key(util[i]);
+        return kk < tk || (kk == tk && pos[i] <= tp);
+    };
+    // victims in ascending slot order: contiguous warp segments, one scan
+    const int nwarps = blockDim.x >> 5;
+    const int seg = (((n + nwarps - 1) / nwarps) + 31) & ~31;
+    const int sb = (tid >> 5) * seg, se = min(n, sb + seg);
+    int wc = 0;
+    for (int i0 = sb; i0 < se; i0 += 32) {
+        const int i = i0 + lane;
+        wc += __popc(__ballot_sync(kFull, i < se && selected(i)));
+    }
+    int written;
+    int off = block_exscan(lane == 0 ? wc : 0, scan, &written);
+    off = __shfl_sync(kFull, off, 0);
+    for (int i0 = sb; i0 < se; i0 += 32) {
+        const int i = i0 + lane;
+        const bool sl = i < se && selected(i);
+        const unsigned b = __ballot_sync(kFull, sl);
+        const int r = off + __popc(b & ((1u << lane) - 1u));
+        if (sl && r < a.kmax) {
+            a.evict_idx[(size_t)u * a.kmax + r] = i;
+            if (a.evict_pos) a.evict_pos[(size_t)u * a.kmax + r] = pos[i];
+        }
+        off += __popc(b);
+    }
+    if (tid == 0) {
+        a.n_evict[u] = written == k ? k : 0;     // duplicate positions: refuse
+        if (written != k) record_status(a.status, KVC_ERR_INVALID_ARG);
+    }
+}
+
 cudaError_t launch_aggregate(const kvc_params &p, int t, const double *probs,
                              const kvc_cache &c, int kmax, int32_t *evict_idx,
                              int32_t *evict_pos, int32_t *n_evict,
@@ -600,6 +885,12 @@ cudaError_t launch_aggregate(const kvc_params &p, int t, const double *probs,
     if (p.rule == KVC_RULE_EMA_CHAINED) {
         const int per = p.chain_layers * p.chain_heads;
         aggregate_chained_kernel<<<p.U / per, 512, 0, st>>>(a, p.chain_layers, p.chain_heads);
+    } else if (kmax > 16 && p.cap <= kAggKeysMax) {
+        const size_t smem = (size_t)p.cap * 4;
+        cudaError_t e = cudaFuncSetAttribute(aggregate_keys_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        aggregate_keys_kernel<<<p.U, 1024, smem, st>>>(a);
     } else {
         aggregate_kernel<<<p.U, 512, 0, st>>>(a);
     }
@@ -800,6 +1091,7 @@ struct CorrArgs {
     float *o, *f_R, *logZ_R;
     int32_t *status;
     int cap, kmax, correction;
+    int retained;      // lse / f_all are already log Z_R / f_R (no victims to remove)
 };
 
 constexpr int kIdentityMax = 16;
@@ -818,7 +1110,7 @@ __global__ void __launch_bounds__(256) correct_kernel(CorrArgs a)
     __shared__ float wst[8][4][G][2];      // per warp/group (m, l)
 
     const int u = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    const int k = max(0, a.n_evict[u]);
+    const int k = a.retained ? 0 : max(0, a.n_evict[u]);
     const int n = a.len[u];
     if (k > a.kmax || !victims_ok(a.evict_idx + (size_t)u * a.kmax, k, n, a.cap, &okf)) {
         if (tid == 0) record_status(a.status, KVC_ERR_INVALID_ARG);
@@ -1093,7 +1385,22 @@ cudaError_t launch_correct(const kvc_params &p, const uint16_t *q,
                            float *logZ_R, const DecodeWs &ws, cudaStream_t st)
 {
     CorrArgs a{q, c.K, c.V, c.votes, c.len, evict_idx, n_evict, lse, f_all,
-               m.n, m.mu_k, m.mu_v, m.C, o, f_R, logZ_R, ws.status, p.cap, kmax, p.correction};
+               m.n, m.mu_k, m.mu_v, m.C, o, f_R, logZ_R, ws.status, p.cap, kmax, p.correction, 0};
+    switch (p.G) {
+    case 1: return launch_correct_g<1>(a, p.U, p.cap, st);
+    case 2: return launch_correct_g<2>(a, p.U, p.cap, st);
+    case 4: return launch_correct_g<4>(a, p.U, p.cap, st);
+    case 8: return launch_correct_g<8>(a, p.U, p.cap, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_correct_retained(const kvc_params &p, const uint16_t *q, const kvc_cache &c,
+                                    const float *lse_R, const float *f_R, const kvc_moments &m,
+                                    float *o, const DecodeWs &ws, cudaStream_t st)
+{
+    CorrArgs a{q, c.K, c.V, c.votes, c.len, nullptr, nullptr, lse_R, f_R,
+               m.n, m.mu_k, m.mu_v, m.C, o, nullptr, nullptr, ws.status, p.cap, 1, p.correction, 1};
     switch (p.G) {
     case 1: return launch_correct_g<1>(a, p.U, p.cap, st);
     case 2: return launch_correct_g<2>(a, p.U, p.cap, st);
@@ -1181,19 +1488,38 @@ __global__ void __launch_bounds__(512) compact_kernel(CompactArgs a)
         }
         __syncthreads();
         const int np = r1 - r0;
-        for (int e = tid; e < np * 32; e += blockDim.x) {
-            const int pr = e >> 5, ch = e & 31;
-            const size_t from = ubase + src[pr], to = ubase + dst[pr];
-            if (ch < 16)
-                reinterpret_cast<uint4 *>(a.K + to * kD)[ch] =
-                    reinterpret_cast<const uint4 *>(a.K + from * kD)[ch];
-            else
-                reinterpret_cast<uint4 *>(a.V + to * kD)[ch - 16] =
-                    reinterpret_cast<const uint4 *>(a.V + from * kD)[ch - 16];
-            if (ch == 0) {
-                a.pos[to] = a.pos[from];
-                a.util[to] = a.util[from];
-                if (a.votes) a.votes[to] = a.votes[from];
+        // four 16-byte chunks per thread in flight (the source rows are at
+        // or above n2, the destinations below: no chunk is both read and
+        // written)
+        constexpr int kU = 4;
+        for (int e0 = tid; e0 < np * 32; e0 += kU * blockDim.x) {
+            uint4 x[kU];
+#pragma unroll
+            for (int j = 0; j < kU; j++) {
+                const int e = e0 + j * blockDim.x;
+                if (e < np * 32) {
+                    const int pr = e >> 5, ch = e & 31;
+                    const size_t from = ubase + src[pr];
+                    x[j] = ch < 16 ? reinterpret_cast<const uint4 *>(a.K + from * kD)[ch]
+                                   : reinterpret_cast<const uint4 *>(a.V + from * kD)[ch - 16];
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kU; j++) {
+                const int e = e0 + j * blockDim.x;
+                if (e < np * 32) {
+                    const int pr = e >> 5, ch = e & 31;
+                    const size_t from = ubase + src[pr], to = ubase + dst[pr];
+                    if (ch < 16)
+                        reinterpret_cast<uint4 *>(a.K + to * kD)[ch] = x[j];
+                    else
+                        reinterpret_cast<uint4 *>(a.V + to * kD)[ch - 16] = x[j];
+                    if (ch == 0) {
+                        a.pos[to] = a.pos[from];
+                        a.util[to] = a.util[from];
+                        if (a.votes) a.votes[to] = a.votes[from];
+                    }
+                }
             }
         }
         __syncthreads();

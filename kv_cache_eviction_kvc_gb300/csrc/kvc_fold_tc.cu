@@ -20,13 +20,14 @@
 //               with votes) MMAs of 128 x 128 x 16 per tile, both operands
 //               MN-major, into one of two accumulators
 //   warps 5-12  gather: the tile's victim rows from global memory into the
-//               ring (128-byte swizzle), w v split, per-warp tile sums
+//               ring (cp.async, 128-byte swizzle, two tiles in flight per
+//               thread), w v split, per-warp tile sums
 // Every wait is bounded (~2 s); a wait that ran out records KVC_ERR_TIMEOUT.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "kvc_common.cuh"
-#include "kvc_fold.h"
+#include "kvc_general.h"
 #include "kvc_tma.cuh"
 #include "kvc_umma.cuh"
 
@@ -102,6 +103,7 @@ struct FoldArgs {
     float *n, *mu_k, *mu_v, *C;
     int32_t *status;
     int cap, kmax;
+    int minor_only;
 };
 
 struct FoldSmem {
@@ -125,6 +127,7 @@ __global__ void __launch_bounds__(kFThreads, 1) fold_tc_kernel(FoldArgs a)
     const int k = a.n_evict[u];
     if (k <= 0) return;
     const int n_len = a.len[u];
+    if (a.minor_only && 2 * k > n_len) return;       // left for the complement
     const int32_t *ev = a.evict_idx + (size_t)u * a.kmax;
     // the victim list: k <= kmax, every slot below the unit's length
     if (tid == 0) S.okv = (k <= a.kmax && n_len >= 0 && n_len <= a.cap) ? 1 : 0;
@@ -166,66 +169,88 @@ __global__ void __launch_bounds__(kFThreads, 1) fold_tc_kernel(FoldArgs a)
 
     if (w >= kFLoad0) {
         // ------------------------------------------------ gather
-        // Thread lt: 16-byte chunk c of the rows rg, rg + 16, ..., rg + 112.
+        // Thread lt: 16-byte chunk c of the rows rg, rg + 16, ..., rg + 112,
+        // copied straight into the operand tiles (cp.async, 16 bytes each;
+        // rows past k are zero-filled).  Two tiles are in flight per thread:
+        // tile t + 1 is requested before tile t is finished (its sums read
+        // back from shared memory, with votes w v split into hi and lo).
         const int lt = tid - kFLoad0 * 32, c = lt & 15, rg = lt >> 4, wl = w - kFLoad0;
         bool good = true;
-        int slot[8];
+        float wnext[8], wcur[8];
+        // victim slots of the tile to issue next (loaded one tile ahead, so
+        // the copies do not wait on the index loads)
+        int slot_n[8];
+        auto load_slots = [&](int t) {
 #pragma unroll
-        for (int jj = 0; jj < 8; jj++) {
-            const int e = rg + 16 * jj;
-            slot[jj] = e < k ? __ldg(ev + e) : -1;
-        }
-        for (int t = 0; t < nt; t++) {
+            for (int jj = 0; jj < 8; jj++) {
+                const int e = t * kFt + rg + 16 * jj;
+                slot_n[jj] = e < k ? __ldg(ev + e) : -1;
+            }
+        };
+        load_slots(0);
+        auto issue = [&](int t, float (&wt)[8]) {
             const int s = t % NS;
-            const bool ok = mbar_wait(&S.empty[s], ((uint32_t)(t / NS) & 1u) ^ 1u);
-            if (!__all_sync(kFull, ok)) {
-                good = false;
-                break;
+            unsigned char *A = ring + (size_t)s * stage_bytes;
+            unsigned char *B = A + kFOp;
+            int slot_i[8];
+#pragma unroll
+            for (int jj = 0; jj < 8; jj++) slot_i[jj] = slot_n[jj];
+            load_slots(t + 1);
+#pragma unroll
+            for (int jj = 0; jj < 8; jj++) {
+                const int r = rg + 16 * jj, e = t * kFt + r;
+                const int sl = slot_i[jj] >= 0 ? slot_i[jj] : 0;
+                const size_t row = (ubase + (size_t)sl) * kD + 8 * c;
+                const uint32_t bytes = e < k ? 16u : 0u;
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(B + fop_off(r, c))),
+                             "l"(a.K + row), "r"(bytes)
+                             : "memory");
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(A + fop_off(r, c))),
+                             "l"(a.V + row), "r"(bytes)
+                             : "memory");
+                wt[jj] = e < k ? (wv ? (float)__ldg(a.votes + ubase + sl) : 1.f) : 0.f;
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+        if (mbar_wait(&S.empty[0], 1u)) issue(0, wnext);
+        else good = false;
+        if (!__all_sync(kFull, good)) good = false;
+        for (int t = 0; t < nt && good; t++) {
+            const int s = t % NS;
+#pragma unroll
+            for (int jj = 0; jj < 8; jj++) wcur[jj] = wnext[jj];
+            if (t + 1 < nt) {
+                const bool ok = mbar_wait(&S.empty[(t + 1) % NS], ((uint32_t)((t + 1) / NS) & 1u) ^ 1u);
+                if (!__all_sync(kFull, ok)) {
+                    good = false;
+                    asm volatile("cp.async.wait_group 0;" ::: "memory");
+                    break;
+                }
+                issue(t + 1, wnext);
+                asm volatile("cp.async.wait_group 1;" ::: "memory");   // tile t landed
+            } else {
+                asm volatile("cp.async.wait_group 0;" ::: "memory");
             }
             unsigned char *A = ring + (size_t)s * stage_bytes;
             unsigned char *B = A + kFOp;
             unsigned char *Al = B + kFOp;
-            uint4 kr[8], vr[8];
-            float wr[8];
-#pragma unroll
-            for (int jj = 0; jj < 8; jj++) {
-                if (slot[jj] >= 0) {
-                    const size_t row = (ubase + (size_t)slot[jj]) * kD + 8 * c;
-                    kr[jj] = ldg_nc_v4(a.K + row);
-                    vr[jj] = ldg_nc_v4(a.V + row);
-                    wr[jj] = wv ? (float)__ldg(a.votes + ubase + slot[jj]) : 1.f;
-                } else {
-                    kr[jj] = make_uint4(0, 0, 0, 0);
-                    vr[jj] = make_uint4(0, 0, 0, 0);
-                    wr[jj] = 0.f;
-                }
-            }
-            // the next tile's victim slots
-#pragma unroll
-            for (int jj = 0; jj < 8; jj++) {
-                const int e = (t + 1) * kFt + rg + 16 * jj;
-                slot[jj] = e < k ? __ldg(ev + e) : -1;
-            }
             float sk[8], sv[8], sw = 0.f;
 #pragma unroll
             for (int q = 0; q < 8; q++) sk[q] = sv[q] = 0.f;
 #pragma unroll
             for (int jj = 0; jj < 8; jj++) {
                 const int r = rg + 16 * jj;
+                const float wt = wcur[jj];
                 float kf[8], vf[8];
-                unpack8(kr[jj], kf);
-                unpack8(vr[jj], vf);
-                const float wt = wr[jj];
+                unpack8(*reinterpret_cast<const uint4 *>(B + fop_off(r, c)), kf);
+                unpack8(*reinterpret_cast<const uint4 *>(A + fop_off(r, c)), vf);
                 sw += wt;
 #pragma unroll
                 for (int q = 0; q < 8; q++) {
                     sk[q] = fmaf(wt, kf[q], sk[q]);
                     sv[q] = fmaf(wt, vf[q], sv[q]);
                 }
-                *reinterpret_cast<uint4 *>(B + fop_off(r, c)) = kr[jj];
-                if (!wv) {
-                    *reinterpret_cast<uint4 *>(A + fop_off(r, c)) = vr[jj];
-                } else {
+                if (wv) {
                     float hi[8], lo[8];
 #pragma unroll
                     for (int q = 0; q < 8; q++) {
@@ -403,13 +428,13 @@ __global__ void __launch_bounds__(kFThreads, 1) fold_tc_kernel(FoldArgs a)
 
 cudaError_t launch_fold_tc(const kvc_cache &c, int cap, int U, int kmax, const int32_t *evict_idx,
                            const int32_t *n_evict, const kvc_moments &m, int32_t *status,
-                           cudaStream_t st)
+                           cudaStream_t st, bool minor_only)
 {
     cudaError_t e = cudaFuncSetAttribute(fold_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kFDyn);
     if (e != cudaSuccess) return e;
     FoldArgs a{c.K, c.V, c.votes, c.len, evict_idx, n_evict, m.n, m.mu_k, m.mu_v, m.C,
-               status, cap, kmax};
+               status, cap, kmax, minor_only ? 1 : 0};
     fold_tc_kernel<<<U, kFThreads, kFDyn, st>>>(a);
     return cudaGetLastError();
 }

@@ -69,6 +69,7 @@ struct FusedArgs {
     int cap, L, T, rule, correction, t, new_pos, kmax, chunk;
     float alpha;
     int merge;                  // KeepKV merge mode: attend over L + 1, append at L
+    int R;                      // merge mode: the last R positions are never partners
 };
 
 struct Cand {
@@ -124,6 +125,10 @@ struct FusedSmem {
     Cand cand[kMaxQueue];
     int ncand;
     Cand bc[kWarps];
+    Cand zc[kNC];               // merge mode, lazy: each consumer warp's best partner
+    Cand zbest;                 // this CTA's best partner (key: cosine, then older position)
+    float zred[kWarps][2];
+    float zcoef[4];
     int victim;                 // slot index of the victim (L = the new token)
     int qvalid;
     int direct;
@@ -180,7 +185,9 @@ __device__ __forceinline__ void stream_rows(const uint16_t *rows, const uint16_t
     }
 }
 
-template <int G>
+// ZS: merge mode with the partner search in pass 1 (G = 2 or 4); the
+// other instances carry none of its code.
+template <int G, bool ZS>
 __global__ void __launch_bounds__(kThreads, 2)
 fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV)
@@ -257,6 +264,9 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
     // 2 leaves the victim out (merge mode keeps it).
     int victim = -1;
     bool late = false;
+    // merge mode, lazy step, victim known up front: the partner search runs
+    // in pass 1 and the merge in the epilogue (no separate merge pass)
+    bool zl = false;
     if (!refresh) {
         // last refresh step (step 1 alone for a Score-Free run, T = 0) and
         // this step's place in its queue
@@ -266,6 +276,36 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
         if (!a.merge && pq[0] == tr && pq[1] >= idx) {
             victim = pq[2 + idx - 1];
             if (victim < 0 || victim >= L) victim = -1;
+        } else if (ZS && pq[0] == tr) {
+            // merge mode: a merge only raises the partner's utility, so the
+            // lowest (utility, position) pair among the queued slots is the
+            // unit's lowest while it is not above the queue's threshold (the
+            // last pair queued at the refresh step: every slot left out was
+            // above it then and can only have risen; slots refilled by a new
+            // token since are unscored).  Every CTA reads the same entries.
+            // lane j of every warp takes entry j (the loads of all entries
+            // are in flight together), then a warp minimum
+            const int cnt = min(pq[1], kMaxQueue - 3);
+            Cand b{~0ull, 0x7fffffff, -1};
+            for (int j = lane; j < cnt; j += 32) {
+                const int sl = pq[2 + j];
+                if (sl < 0 || sl >= L) continue;
+                const uint64_t ub = (uint64_t)__double_as_longlong(a.util[ubase + sl]);
+                if ((ub & 0x7fffffffffffffffull) == 0x7ff0000000000000ull) continue;
+                const Cand cd{double_key(__longlong_as_double((long long)ub)), a.pos[ubase + sl], sl};
+                if (cand_less(cd, b)) b = cd;
+            }
+#pragma unroll
+            for (int m = 16; m > 0; m >>= 1) {
+                const Cand o = shfl_cand(b, m);
+                if (cand_less(o, b)) b = o;
+            }
+            const Cand th{((uint64_t)(uint32_t)pq[kPendStride - 3] << 32) | (uint32_t)pq[kPendStride - 2],
+                          pq[kPendStride - 1], 0};
+            if (b.slot >= 0 && !cand_less(th, b)) {
+                victim = b.slot;
+                zl = true;
+            }
         }
         late = victim < 0;                  // uniform over the cluster
     }
@@ -614,13 +654,32 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
         // slots gq, gq + 8 for heads 2 tq, 2 tq + 1, and p of head gq.
         uint32_t qb[8][2];
         {
+            // merge mode, lazy: column G carries the victim's key, so that
+            // the same MMAs give k_e . k_j for the partner search
             const uint32_t *q32 = reinterpret_cast<const uint32_t *>(a.q + (size_t)u * G * kD);
+            const uint32_t *ke32 = reinterpret_cast<const uint32_t *>(a.K + (ubase + (zl ? victim : 0)) * kD);
+            const bool kecol = ZS && zl && gq == G;
 #pragma unroll
             for (int ks = 0; ks < 8; ks++) {
-                qb[ks][0] = gq < G ? q32[(gq * kD + 16 * ks + 2 * tq) >> 1] : 0u;
-                qb[ks][1] = gq < G ? q32[(gq * kD + 16 * ks + 8 + 2 * tq) >> 1] : 0u;
+                qb[ks][0] = gq < G ? q32[(gq * kD + 16 * ks + 2 * tq) >> 1]
+                                   : (kecol ? ke32[(16 * ks + 2 * tq) >> 1] : 0u);
+                qb[ks][1] = gq < G ? q32[(gq * kD + 16 * ks + 8 + 2 * tq) >> 1]
+                                   : (kecol ? ke32[(16 * ks + 8 + 2 * tq) >> 1] : 0u);
             }
         }
+        // partner search (merge mode, lazy): cosine of k_e with every slot
+        // outside the last R positions, k_e . k_j / |k_j| (|k_e| > 0 is a
+        // common factor); lanes tq = G / 2 hold column G
+        const long long zlim = (long long)a.new_pos - a.R;
+        unsigned long long zkey = 0ull;
+        int zslot = -1;
+        auto load_pos = [&](int t, int &p0, int &p1) {
+            const int li = t * kTile + w * 16 + gq;
+            p0 = li < nrows ? a.pos[ubase + s0 + li] : 0x7fffffff;
+            p1 = li + 8 < nrows ? a.pos[ubase + s0 + li + 8] : 0x7fffffff;
+        };
+        int pn0 = 0x7fffffff, pn1 = 0x7fffffff;
+        if (ZS && zl && ntile > 0) load_pos(0, pn0, pn1);
         const int rb = w * 16;                   // this warp's rows in a tile
         const int h0 = 2 * tq, h1 = 2 * tq + 1;  // heads of this lane's logits
         bool good = true;
@@ -673,11 +732,17 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             const uint32_t ph = (uint32_t)(g / kStages) & 1u;
             const int vc[2] = {vn0, vn1};
             if (a.votes && t + 1 < ntile) load_votes(t + 1, vn0, vn1);
+            const int pc[2] = {pn0, pn1};
+            if (ZS && zl && t + 1 < ntile) load_pos(t + 1, pn0, pn1);
             if (good && !mbar_wait(&S.full[stage], ph)) good = false;
             if (good) {
                 const uint32_t so = (uint32_t)stage * kTileBytes;
                 patch(so, t, knew);
                 float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+                // merge mode, lazy: the Gram blocks of the warp's 16 rows with
+                // rows 0-7 and 8-15 (the A fragments are also the B fragments
+                // of those rows), whose diagonals are |k_j|^2
+                float g0[4] = {0.f, 0.f, 0.f, 0.f}, g1[4] = {0.f, 0.f, 0.f, 0.f};
                 const int mi = lane >> 3;
                 const int lrow = rb + ((mi & 1) << 3) + (lane & 7);
 #pragma unroll
@@ -685,6 +750,36 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
                     uint32_t a0, a1, a2, a3;
                     ldsm_x4(ring_s + so + sw_off(lrow, 2 * ks + (mi >> 1)), a0, a1, a2, a3);
                     mma16816(sacc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+                    if (ZS && zl) {
+                        mma16816(g0, a0, a1, a2, a3, a0, a2);
+                        mma16816(g1, a0, a1, a2, a3, a1, a3);
+                    }
+                }
+                if (ZS && zl) {
+                    // |k|^2 of row gq sits in lane (gq, gq / 2) of g0, of row
+                    // gq + 8 in the same lane of g1; bring both to this lane
+                    const int src = 4 * gq + (gq >> 1);
+                    const float d0 = (gq & 1) ? g0[1] : g0[0];
+                    const float d1 = (gq & 1) ? g1[3] : g1[2];
+                    const float sq0 = __shfl_sync(kFull, d0, src);
+                    const float sq1 = __shfl_sync(kFull, d1, src);
+                    if (2 * tq == G) {
+#pragma unroll
+                        for (int hf = 0; hf < 2; hf++) {
+                            const int li = t * kTile + rb + gq + 8 * hf;
+                            const int i = s0 + li;
+                            const float ss = hf ? sq1 : sq0;
+                            if (li < nrows && i != victim && (long long)pc[hf] <= zlim) {
+                                const float sc = ss > 0.f ? sacc[2 * hf] * rsqrtf(ss) : 0.f;
+                                const unsigned long long key =
+                                    ((unsigned long long)float_key(sc) << 32) | (uint32_t)(0x7fffffff - pc[hf]);
+                                if (key > zkey) {
+                                    zkey = key;
+                                    zslot = i;
+                                }
+                            }
+                        }
+                    }
                 }
 #pragma unroll
                 for (int hf = 0; hf < 2; hf++) {           // slot gq, then gq + 8
@@ -707,6 +802,18 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             }
             __syncwarp();
             if (lane == 0 && good) mbar_arrive(&S.empty[stage]);
+        }
+        if (ZS && zl) {
+#pragma unroll
+            for (int m = 16; m > 0; m >>= 1) {
+                const unsigned long long ok = __shfl_xor_sync(kFull, zkey, m);
+                const int os = __shfl_xor_sync(kFull, zslot, m);
+                if (ok > zkey) {
+                    zkey = ok;
+                    zslot = os;
+                }
+            }
+            if (lane == 0) S.zc[w] = Cand{zkey, 0, zslot};
         }
         // the virtual slot L (refresh steps): scalar dot products on warp 0
         float xv_new[G];
@@ -900,6 +1007,12 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
         __syncthreads();
     };
 
+    if (ZS && zl && tid == 0) {
+        Cand b{0ull, 0, -1};
+        for (int j = 0; j < kNC; j++)
+            if (S.zc[j].slot >= 0 && S.zc[j].key > b.key) b = S.zc[j];
+        S.zbest = b;
+    }
     // ------------------------------------------------ cluster merge
     cluster.sync();                                                    // partials visible
     auto merge = [&]() {
@@ -1021,9 +1134,13 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
         // promotes its second entry and rescans only when it wins again.
         // Thread 0 then merges the sorted per-warp lists.
         // queue length: T (one victim per step until the next refresh); a
-        // Score-Free run (T = 0, no later refresh) queues as many as fit
-        // (merge mode keeps no queue: a merge changes the partner's utility)
-        const int Tq = a.merge ? 1 : (a.T > 0 ? a.T : kMaxQueue);
+        // Score-Free run (T = 0, no later refresh) queues as many as fit.
+        // Merge mode queues 2 T (a merge can lift a queued partner out of
+        // the lowest) with the last pair as the queue's threshold; it is
+        // used where the partner search can run in pass 1 (G = 2 or 4).
+        const bool mq = ZS;
+        const int Tq = a.merge ? (mq ? min(a.T > 0 ? 2 * a.T : kMaxQueue, kMaxQueue - 3) : 1)
+                               : (a.T > 0 ? a.T : kMaxQueue);
         const int want = min(Tq, nloc);
         Cand *wl = reinterpret_cast<Cand *>(chosen + align_up((size_t)(ch + 1)));   // [kWarps][kMaxQueue]
         const Cand none{~0ull, 0x7fffffff, -1};
@@ -1129,10 +1246,18 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             S.victim = nsel > 0 ? sel[0].slot : -1;
             if (r == 0 && nsel > 0) {
                 int32_t *pq = a.pend + (size_t)u * kPendStride;
-                pq[0] = a.merge ? 0 : a.t;
+                pq[0] = (a.merge && !mq) ? 0 : a.t;
                 pq[1] = nsel - 1;
                 for (int j = 1; j < nsel; j++)
                     pq[2 + j - 1] = sel[j].slot == L ? sel[0].slot : sel[j].slot;
+                if (mq) {
+                    // threshold: the last pair queued, or above everything
+                    // when every scored slot is in the queue
+                    const Cand th = nsel == Tq ? sel[nsel - 1] : Cand{~0ull, 0x7fffffff, -1};
+                    pq[kPendStride - 3] = (int32_t)(uint32_t)(th.key >> 32);
+                    pq[kPendStride - 2] = (int32_t)(uint32_t)th.key;
+                    pq[kPendStride - 1] = th.pos;
+                }
             }
         }
         __syncthreads();
@@ -1215,6 +1340,79 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
         }
         ou[(size_t)h * kD + dd] = val;
     }
+    // merge mode, lazy step with the partner found in pass 1: KeepKV's
+    // ZIP-merge (the weights w = p exp(x) of the group's mean logit, eqs
+    // 10 and 12, the epsilon guard) of the victim into it on CTA 0, then the
+    // new token takes the victim's slot: the unit keeps L slots and nothing
+    // is left for the merge kernel (n_evict = 0).
+    bool zdone = false;
+    if (ZS && zl) {
+        Cand b{0ull, 0, -1};
+        for (int q = 0; q < CS; q++) {
+            const Cand cq = cluster.map_shared_rank(&S, q)->zbest;
+            if (cq.slot >= 0 && cq.key > b.key) b = cq;
+        }
+        const int cp = b.slot;
+        zdone = cp >= 0;
+        if (zdone && r == 0) {
+            const int e = victim;
+            float kef = 0.f, kcf = 0.f, vef = 0.f, vcf = 0.f;
+            if (tid < kD) {
+                kef = bf2f(a.K[(ubase + e) * kD + tid]);
+                kcf = bf2f(a.K[(ubase + cp) * kD + tid]);
+                vef = bf2f(a.V[(ubase + e) * kD + tid]);
+                vcf = bf2f(a.V[(ubase + cp) * kD + tid]);
+                float qbs = 0.f;                      // sum of the group's queries
+                for (int h = 0; h < G; h++) qbs += bf2f(a.q[((size_t)u * G + h) * kD + tid]);
+                const float se = warp_sum(qbs * kef), sc = warp_sum(qbs * kcf);
+                if (lane == 0) {
+                    S.zred[w][0] = se;
+                    S.zred[w][1] = sc;
+                }
+            }
+            __syncthreads();
+            if (tid == 0) {
+                const float scale = rsqrtf((float)kD) / (float)G;
+                const float xe = (S.zred[0][0] + S.zred[1][0] + S.zred[2][0] + S.zred[3][0]) * scale;
+                const float xc = (S.zred[0][1] + S.zred[1][1] + S.zred[2][1] + S.zred[3][1]) * scale;
+                const float pe = a.votes ? (float)a.votes[ubase + e] : 1.f;
+                const float pc = a.votes ? (float)a.votes[ubase + cp] : 1.f;
+                const float m = fmaxf(xe, xc);
+                const float we = pe * expf(xe - m), wc = pc * expf(xc - m), W = we + wc;
+                const float le = we / W, lc = wc / W;
+                const float xt = le * xe + lc * xc;
+                const float ell = m + logf(W / (pe + pc));
+                const bool guard = fabsf(xt) < (float)KVC_ZIP_EPS;
+                S.zcoef[0] = le;
+                S.zcoef[1] = lc;
+                S.zcoef[2] = guard ? 0.f : ell / xt;
+                S.zcoef[3] = guard ? 1.f : 0.f;
+            }
+            __syncthreads();
+            if (tid < kD) {
+                const float le = S.zcoef[0], lc = S.zcoef[1];
+                const float kr = S.zcoef[3] != 0.f ? 0.5f * (kef + kcf) : (le * kef + lc * kcf) * S.zcoef[2];
+                const float vr = le * vef + lc * vcf;
+                a.K[(ubase + cp) * kD + tid] = __bfloat16_as_ushort(__float2bfloat16_rn(kr));
+                a.V[(ubase + cp) * kD + tid] = __bfloat16_as_ushort(__float2bfloat16_rn(vr));
+            }
+            if (tid == kD) {
+                if (a.votes) a.votes[ubase + cp] += a.votes[ubase + e];
+                a.util[ubase + cp] += a.util[ubase + e];
+            }
+            __syncthreads();                          // the victim's rows were read
+            uint16_t *kd = a.K + (ubase + e) * kD;
+            uint16_t *vd = a.V + (ubase + e) * kD;
+            if (tid < 32) {
+                reinterpret_cast<uint2 *>(kd)[tid] = reinterpret_cast<const uint2 *>(knew)[tid];
+                reinterpret_cast<uint2 *>(vd)[tid] = reinterpret_cast<const uint2 *>(vnew)[tid];
+            } else if (tid == 32) {
+                if (a.votes) a.votes[ubase + e] = 1;
+                a.pos[ubase + e] = a.new_pos;
+                a.util[ubase + e] = __longlong_as_double(0x7ff0000000000000ll);
+            }
+        }
+    }
     if (!a.merge)
         for (int e = r0 + tid; e < r1; e += blockDim.x) a.mu_v[(size_t)u * kD + e] = S.muv[e];
     if (r == 0) {
@@ -1222,14 +1420,14 @@ fused_step_kernel(FusedArgs a, const __grid_constant__ CUtensorMap tmK,
             for (int e = tid; e < kD; e += blockDim.x) a.mu_k[(size_t)u * kD + e] = S.muk[e];
         if (tid == 0) {
             if (!a.merge) a.mn[u] = n1;
-            a.n_evict[u] = 1;
+            a.n_evict[u] = zdone ? 0 : 1;
             if (a.evict_idx) a.evict_idx[(size_t)u * a.kmax] = victim;
             if (a.evict_pos) a.evict_pos[(size_t)u * a.kmax] = S.vpos;
         }
     }
     if (refresh && !a.merge) write_back_C();
     // ------------------------------------------------ the new token's slot
-    if (a.merge) {
+    if (a.merge && !zdone) {
         // appended at slot L; the merge that follows refills the victim's
         // slot from it and restores len = L
         if (r == CS - 1) {
@@ -1275,10 +1473,13 @@ static cudaError_t launch_fused_g(const FusedArgs &a0, int U, int CS, cudaStream
     if (rows >= (1ull << 31) || !make_row_map(&tmK, a.K, rows, kTile) || !make_row_map(&tmV, a.V, rows, kTile))
         return cudaErrorNotSupported;
     const size_t dyn = 1024 + (size_t)kStages * kTileBytes + align_up((size_t)G * (a.chunk + 1) * 4);
-    cudaError_t e = cudaFuncSetAttribute(fused_step_kernel<G>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+    // merge mode with G = 2 or 4 and R >= 1 searches the partner in pass 1
+    auto kern = fused_step_kernel<G, false>;
+    if constexpr (G == 2 || G == 4)
+        if (a.merge && a.R >= 1) kern = fused_step_kernel<G, true>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(fused_step_kernel<G>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     (void)e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(U * CS);
@@ -1292,7 +1493,7 @@ static cudaError_t launch_fused_g(const FusedArgs &a0, int U, int CS, cudaStream
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fused_step_kernel<G>, a, tmK, tmV);
+    return cudaLaunchKernelEx(&cfg, kern, a, tmK, tmV);
 }
 
 int fused_cluster_size(int U, int L)
@@ -1322,7 +1523,7 @@ cudaError_t launch_fused_step(const kvc_params &p, int t, int new_pos, const uin
     FusedArgs a{q, k_new, v_new, c.K, c.V, c.votes, c.pos, c.util, c.len,
                 m.n, m.mu_k, m.mu_v, m.C, o, probs, evict_idx, evict_pos, n_evict,
                 ws.pend, ws.status, p.budget, rr, p.cap, p.L, p.refresh_period, p.rule,
-                p.correction, t, new_pos, kmax, chunk, p.alpha, p.merge};
+                p.correction, t, new_pos, kmax, chunk, p.alpha, p.merge, p.merge_recent};
     switch (p.G) {
     case 1: return launch_fused_g<1>(a, p.U, CS, st);
     case 2: return launch_fused_g<2>(a, p.U, CS, st);

@@ -9,7 +9,7 @@
 
 namespace kvc {
 
-constexpr int kAttendChunk = 512;     // slots per CTA of the split attention
+constexpr int kAttendChunk = 1024;    // slots per CTA of the split attention
 constexpr int kProbsChunk = 4096;     // slots per CTA of the probability pass
 constexpr int kMaxCap = 1 << 19;      // largest supported slot capacity
 constexpr size_t kAlign = 256;
@@ -26,8 +26,12 @@ struct DecodeWs {
     float *lse;        // [U][G]              general-step scratch
     float *fall;       // [U][G][d]           general-step scratch
     double *probs;     // [U][cap]            general-step scratch
+    float *pmom;       // [U][kPMomStride]    general-step moments of all slots
     size_t bytes;
 };
+
+// one unit's moments in the workspace: M [d][d], mu_k [d], mu_v [d], n
+constexpr int kPMomStride = 16768;
 
 constexpr int kPendStride = 72;  // [0] refresh step, [1] count, [2..] slots
 
