@@ -22,7 +22,7 @@
 //               1024-slot chunk; logits for the probabilities
 //   warp 4      producer (TMA)
 //   warp 5      tensor-memory owner and MMA issuer: P = sum w v k^T of each
-//               256-slot group (tcgen05, both operands MN-major) into one of
+//               512-slot group (tcgen05, both operands MN-major) into one of
 //               two accumulators
 //   warps 6-9   moments: the group's sums from the tiles (a thread takes a
 //               16-byte chunk of 8 rows per tile), then thread i (tensor-
@@ -45,10 +45,10 @@ namespace {
 constexpr int kPT = 64;                        // slots per tile
 constexpr int kPBox = kPT * 128;               // 8 KB: 64 rows x 64 dimensions
 constexpr int kPTile = 2 * kPBox;              // 16 KB: a tile of keys or values
-constexpr int kPGroup = 4;                     // tiles per co-moment group
-constexpr int kPNC = 4;                        // consumer warps
-constexpr int kPProd = 4, kPMma = 5, kPEpi0 = 6;
-constexpr int kPThreads = 10 * 32;
+constexpr int kPGroup = 8;                     // tiles per co-moment group (512 slots)
+constexpr int kPNC = 8;                        // consumer warps: two sets of four
+constexpr int kPProd = 8, kPMma = 9, kPEpi0 = 10;
+constexpr int kPThreads = 14 * 32;
 constexpr int kPChunkTiles = kAttendChunk / kPT;
 constexpr int kPRing = 12 * kPTile;            // 6 stages of (K, V) or 3 of (K, V, hi, lo)
 constexpr size_t kPDyn = 1024 + (size_t)kPRing;
@@ -114,13 +114,15 @@ struct PromptArgs {
 
 template <int G>
 struct PromptSmem {
+    // read as float4: 16-byte aligned, first
+    alignas(16) float vsk[2][kD];
+    alignas(16) float vdk[2][kD];
     uint64_t full[kPMaxStages], ready[kPMaxStages], empty[kPMaxStages];
     uint64_t accf[2], acce[2], done;
     float xs[kPNC][G][16];       // a consumer warp's logits of the current tile
     float wm[kPNC][G], wl[kPNC][G];
     float po[G][kD];
     float gm[G];
-    float vsk[2][kD], vdk[2][kD];
     float gk[8][kD], gv[8][kD];  // a group's sums per row group (moments warps)
     float gw[8];
     uint32_t tmem;
@@ -160,10 +162,14 @@ prompt_pass_kernel(PromptArgs a, const __grid_constant__ CUtensorMap tmK,
     if (tid == 0) {
         S.bad = 0;
         S.epibad = 0;
+        // ready: the consumers patched the stage (and, with votes, the
+        // moments warps wrote w v); empty: the consumers and the MMAs are
+        // done with it (and, without votes, the moments warps read it, so
+        // that they never hold back the MMAs)
         for (int j = 0; j < kPMaxStages; j++) {
             mbar_init(&S.full[j], 1);
-            mbar_init(&S.ready[j], kPNC + 4);              // consumers patched, moments warps read
-            mbar_init(&S.empty[j], kPNC + 1);              // consumers done, MMAs done
+            mbar_init(&S.ready[j], 4 + (wv ? 4 : 0));
+            mbar_init(&S.empty[j], 4 + 1 + (wv ? 0 : 4));
         }
         for (int j = 0; j < 2; j++) {
             mbar_init(&S.accf[j], 1);
@@ -322,7 +328,7 @@ prompt_pass_kernel(PromptArgs a, const __grid_constant__ CUtensorMap tmK,
                 }
                 if (wv) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&S.ready[s]);
+                if (lane == 0) mbar_arrive(wv ? &S.ready[s] : &S.empty[s]);
             }
 #pragma unroll
             for (int e = 0; e < 8; e++) {
@@ -371,10 +377,15 @@ prompt_pass_kernel(PromptArgs a, const __grid_constant__ CUtensorMap tmK,
                 tmem_bind(mr);
                 float m[32];
 #pragma unroll
-                for (int e = 0; e < 32; e++) {
-                    const int j = 32 * h + e;
-                    const float ct = fmaf(bcoef, S.vdk[b][j], fmaf(-acoef, S.vsk[b][j], __uint_as_float(xr[e])));
-                    m[e] = __uint_as_float(mr[e]) + ct;
+                for (int e = 0; e < 32; e += 4) {
+                    const float4 dk4 = *reinterpret_cast<const float4 *>(&S.vdk[b][32 * h + e]);
+                    const float4 sk4 = *reinterpret_cast<const float4 *>(&S.vsk[b][32 * h + e]);
+                    const float dkv[4] = {dk4.x, dk4.y, dk4.z, dk4.w}, skv[4] = {sk4.x, sk4.y, sk4.z, sk4.w};
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        const float ct = fmaf(bcoef, dkv[q], fmaf(-acoef, skv[q], __uint_as_float(xr[e + q])));
+                        m[e + q] = __uint_as_float(mr[e + q]) + ct;
+                    }
                 }
                 p_tmem_st32(lane_base + kPColM + (uint32_t)(32 * h), m);
             }
@@ -458,7 +469,8 @@ prompt_pass_kernel(PromptArgs a, const __grid_constant__ CUtensorMap tmK,
         // (gq, tq) holds logits of slots gq, gq + 8 for heads 2 tq, 2 tq + 1
         // and p of head gq.
         const int gq = lane >> 2, tq = lane & 3;
-        const int rb = w * 16;
+        const int cset = w >> 2;                     // set 0 takes the even tiles, set 1 the odd
+        const int rb = (w & 3) * 16;
         const int h0 = 2 * tq, h1 = 2 * tq + 1;
         const float rs = rsqrtf((float)kD);
         uint32_t qb[8][2];
@@ -479,7 +491,10 @@ prompt_pass_kernel(PromptArgs a, const __grid_constant__ CUtensorMap tmK,
 #pragma unroll
         for (int m = 0; m < 8; m++) O[m][0] = O[m][1] = O[m][2] = O[m][3] = 0.f;
         bool good = true;
-        for (int t = 0; t < nt; t++) {
+        const int nch = (nt + kPChunkTiles - 1) / kPChunkTiles;
+        for (int cidx = 0; cidx < nch; cidx++) {
+          const int tc1 = min(nt, (cidx + 1) * kPChunkTiles);
+          for (int t = cidx * kPChunkTiles + cset; t < tc1; t += 2) {
             const int s = t % NS;
             const uint32_t so = (uint32_t)(s * stage_bytes);
             const bool ok = good && mbar_wait(&S.full[s], (uint32_t)(t / NS) & 1u);
@@ -512,16 +527,21 @@ prompt_pass_kernel(PromptArgs a, const __grid_constant__ CUtensorMap tmK,
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&S.ready[s]);
                 // logits
-                float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+                float sacc[4] = {0.f, 0.f, 0.f, 0.f}, sacc2[4] = {0.f, 0.f, 0.f, 0.f};
                 {
+                    // two accumulator chains (k-steps 0-3, 4-7)
                     const int mi = lane >> 3;
                     const int lrow = rb + ((mi & 1) << 3) + (lane & 7);
 #pragma unroll
-                    for (int ks = 0; ks < 8; ks++) {
-                        uint32_t a0, a1, a2, a3;
+                    for (int ks = 0; ks < 4; ks++) {
+                        uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
                         ldsm_x4(ring_s + so + p_off(lrow, 2 * ks + (mi >> 1)), a0, a1, a2, a3);
+                        ldsm_x4(ring_s + so + p_off(lrow, 2 * (ks + 4) + (mi >> 1)), c0, c1, c2, c3);
                         mma16816(sacc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+                        mma16816(sacc2, c0, c1, c2, c3, qb[ks + 4][0], qb[ks + 4][1]);
                     }
+#pragma unroll
+                    for (int e = 0; e < 4; e++) sacc[e] += sacc2[e];
                 }
                 float tm0 = -INFINITY, tm1 = -INFINITY;
 #pragma unroll
@@ -562,14 +582,16 @@ prompt_pass_kernel(PromptArgs a, const __grid_constant__ CUtensorMap tmK,
                     mrun[h] = mn_;
                 }
                 __syncwarp();
-                // rescale the running output and sum
+                // rescale the running output and sum (only when a max rose)
                 const float s0 = h0 < G ? scl[h0] : 1.f, s1 = h1 < G ? scl[h1] : 1.f;
+                if (__any_sync(kFull, s0 != 1.f || s1 != 1.f)) {
 #pragma unroll
-                for (int m = 0; m < 8; m++) {
-                    O[m][0] *= s0;
-                    O[m][2] *= s0;
-                    O[m][1] *= s1;
-                    O[m][3] *= s1;
+                    for (int m = 0; m < 8; m++) {
+                        O[m][0] *= s0;
+                        O[m][2] *= s0;
+                        O[m][1] *= s1;
+                        O[m][3] *= s1;
+                    }
                 }
                 float mg = -INFINITY;
 #pragma unroll
@@ -608,9 +630,9 @@ prompt_pass_kernel(PromptArgs a, const __grid_constant__ CUtensorMap tmK,
             }
             __syncwarp();
             if (lane == 0 && good) mbar_arrive(&S.empty[s]);
-            // a 1024-slot chunk ends: merge the four warps into its partial
-            const bool chunk_end = ((t + 1) % kPChunkTiles == 0) || (t + 1 == nt);
-            if (chunk_end) {
+          }
+            // a 1024-slot chunk ends: merge the eight warps into its partial
+            {
                 float l = lsq;
                 l += __shfl_xor_sync(kFull, l, 1);
                 l += __shfl_xor_sync(kFull, l, 2);
@@ -619,13 +641,13 @@ prompt_pass_kernel(PromptArgs a, const __grid_constant__ CUtensorMap tmK,
                     for (int h = 0; h < G; h++) S.wm[w][h] = mrun[h];
                 if (tq == 0 && gq < G) S.wl[w][gq] = l;
                 for (int e = tid; e < G * kD; e += kPNC * 32) S.po[e / kD][e % kD] = 0.f;
-                asm volatile("bar.sync 1, 128;" ::: "memory");
+                asm volatile("bar.sync 1, 256;" ::: "memory");
                 if (tid < G) {
                     float M = -INFINITY;
                     for (int q = 0; q < kPNC; q++) M = fmaxf(M, S.wm[q][tid]);
                     S.gm[tid] = M;
                 }
-                asm volatile("bar.sync 1, 128;" ::: "memory");
+                asm volatile("bar.sync 1, 256;" ::: "memory");
                 const float f0 = (h0 < G && mrun[h0] != -INFINITY) ? expf(mrun[h0] - S.gm[h0]) : 0.f;
                 const float f1 = (h1 < G && mrun[h1] != -INFINITY) ? expf(mrun[h1] - S.gm[h1]) : 0.f;
 #pragma unroll
@@ -639,8 +661,8 @@ prompt_pass_kernel(PromptArgs a, const __grid_constant__ CUtensorMap tmK,
                         atomicAdd(&S.po[h1][16 * m + gq + 8], O[m][3] * f1);
                     }
                 }
-                asm volatile("bar.sync 1, 128;" ::: "memory");
-                const int sc = t / kPChunkTiles;
+                asm volatile("bar.sync 1, 256;" ::: "memory");
+                const int sc = cidx;
                 float *pp = a.part + ((size_t)u * a.S + sc) * G * (kD + 2);
                 for (int e = tid; e < G * kD; e += kPNC * 32) {
                     const int h = e / kD, dd = e % kD;
@@ -653,7 +675,7 @@ prompt_pass_kernel(PromptArgs a, const __grid_constant__ CUtensorMap tmK,
                     pp[tid * (kD + 2) + 0] = S.gm[tid];
                     pp[tid * (kD + 2) + 1] = ll;
                 }
-                asm volatile("bar.sync 1, 128;" ::: "memory");
+                asm volatile("bar.sync 1, 256;" ::: "memory");
 #pragma unroll
                 for (int h = 0; h < G; h++) mrun[h] = -INFINITY;
                 lsq = 0.f;
