@@ -1490,7 +1490,7 @@ __global__ void __launch_bounds__(512) compact_kernel(CompactArgs a)
         const int np = r1 - r0;
         // four 16-byte chunks per thread in flight (the source rows are at
         // or above n2, the destinations below: no chunk is both read and
-        // written)
+        // written; eight cost a resident CTA per SM and were slower)
         constexpr int kU = 4;
         for (int e0 = tid; e0 < np * 32; e0 += kU * blockDim.x) {
             uint4 x[kU];

@@ -51,12 +51,14 @@ constexpr int kPProd = 8, kPMma = 9, kPEpi0 = 10;
 constexpr int kPThreads = 14 * 32;
 constexpr int kPChunkTiles = kAttendChunk / kPT;
 constexpr int kPRing = 12 * kPTile;            // 6 stages of (K, V) or 3 of (K, V, hi, lo)
-constexpr size_t kPDyn = 1024 + (size_t)kPRing;
+constexpr size_t kPDyn = 1024 + (size_t)kPRing + kPBox;   // + the all-ones operand
 constexpr int kPMaxStages = 6;
 constexpr uint32_t kPColM = 256;
+constexpr uint32_t kPColS = 384;               // sums: [b] at 384 + 32 b (k at +0, v at +16)
 static_assert(kAttendChunk % kPT == 0, "attention chunks hold whole tiles");
 
 constexpr uint32_t kPIdesc = umma_idesc_bf16(128, 128) | (1u << 15) | (1u << 16);
+constexpr uint32_t kPIdesc16 = umma_idesc_bf16(128, 16) | (1u << 15) | (1u << 16);
 
 __device__ __forceinline__ uint32_t p_off(int r, int c)
 {
@@ -159,17 +161,25 @@ prompt_pass_kernel(PromptArgs a, const __grid_constant__ CUtensorMap tmK,
     const uint16_t *knew = a.append ? a.k_new + (size_t)u * kD : nullptr;
     const uint16_t *vnew = a.append ? a.v_new + (size_t)u * kD : nullptr;
 
+    // the all-ones operand (column 0 of a 64-row box = 1, the rest 0):
+    // without votes, sum_r v_r and sum_r k_r come from MMAs against it
+    unsigned char *ones = ring + kPRing;
+    for (int e = tid; e < kPBox / 16; e += blockDim.x) {
+        const int r = e >> 3, c = e & 7;
+        const uint32_t lo = (c == ((0 ^ (r & 7)))) ? 0x3F80u : 0u;   // bf16 1.0 in element 0 of chunk 0
+        *reinterpret_cast<uint4 *>(ones + (r << 7) + (c << 4)) = make_uint4(lo, 0u, 0u, 0u);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (tid == 0) {
         S.bad = 0;
         S.epibad = 0;
         // ready: the consumers patched the stage (and, with votes, the
-        // moments warps wrote w v); empty: the consumers and the MMAs are
-        // done with it (and, without votes, the moments warps read it, so
-        // that they never hold back the MMAs)
+        // moments warps wrote w v and took the sums); empty: the consumers
+        // and the MMAs are done with it
         for (int j = 0; j < kPMaxStages; j++) {
             mbar_init(&S.full[j], 1);
             mbar_init(&S.ready[j], 4 + (wv ? 4 : 0));
-            mbar_init(&S.empty[j], 4 + 1 + (wv ? 0 : 4));
+            mbar_init(&S.empty[j], 4 + 1);
         }
         for (int j = 0; j < 2; j++) {
             mbar_init(&S.accf[j], 1);
@@ -222,6 +232,8 @@ prompt_pass_kernel(PromptArgs a, const __grid_constant__ CUtensorMap tmK,
                     break;
                 }
                 const uint32_t d = tmem + (uint32_t)(b * 128);
+                const uint32_t ds = tmem + kPColS + (uint32_t)(32 * b);
+                const uint32_t aO = ring_s + (uint32_t)kPRing;
                 const int t0 = g * kPGroup, t1 = min(nt, t0 + kPGroup);
                 for (int t = t0; t < t1 && ok; t++) {
                     const int s = t % NS;
@@ -241,6 +253,9 @@ prompt_pass_kernel(PromptArgs a, const __grid_constant__ CUtensorMap tmK,
                             umma_bf16(d, p_desc(aL + off), p_desc(aK + off), kPIdesc, true);
                         } else {
                             umma_bf16(d, p_desc(aV + off), p_desc(aK + off), kPIdesc, acc);
+                            // sum_r k_r and sum_r v_r (column 0 of each 16-column block)
+                            umma_bf16(ds, p_desc(aK + off), p_desc(aO + off), kPIdesc16, acc);
+                            umma_bf16(ds + 16, p_desc(aV + off), p_desc(aO + off), kPIdesc16, acc);
                         }
                     }
                     umma_commit(&S.empty[s]);
@@ -276,7 +291,7 @@ prompt_pass_kernel(PromptArgs a, const __grid_constant__ CUtensorMap tmK,
             float sk8[8], sv8[8], swp = 0.f;
 #pragma unroll
             for (int e = 0; e < 8; e++) sk8[e] = sv8[e] = 0.f;
-            for (int t = t0; t < t1; t++) {
+            for (int t = t0; t < t1 && wv; t++) {
                 const int s = t % NS;
                 const bool ok = mbar_wait(&S.full[s], (uint32_t)(t / NS) & 1u);
                 if (!__all_sync(kFull, ok)) {
@@ -326,16 +341,18 @@ prompt_pass_kernel(PromptArgs a, const __grid_constant__ CUtensorMap tmK,
                                        pk_bf2(lo[6], lo[7]));
                     }
                 }
-                if (wv) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
-                if (lane == 0) mbar_arrive(wv ? &S.ready[s] : &S.empty[s]);
+                if (lane == 0) mbar_arrive(&S.ready[s]);
             }
+            if (wv) {
 #pragma unroll
-            for (int e = 0; e < 8; e++) {
-                S.gk[rg][8 * c16 + e] = sk8[e];
-                S.gv[rg][8 * c16 + e] = sv8[e];
+                for (int e = 0; e < 8; e++) {
+                    S.gk[rg][8 * c16 + e] = sk8[e];
+                    S.gv[rg][8 * c16 + e] = sv8[e];
+                }
+                if (c16 == 0) S.gw[rg] = swp;
             }
-            if (c16 == 0) S.gw[rg] = swp;
             // the group's centred co-moment into M (Chan)
             const bool okg = good && mbar_wait(&S.accf[b], (uint32_t)(g >> 1) & 1u);
             if (!__all_sync(kFull, okg) && lane == 0) S.epibad = 1;
@@ -346,11 +363,21 @@ prompt_pass_kernel(PromptArgs a, const __grid_constant__ CUtensorMap tmK,
             }
             tc_fence_after();
             float sk = 0.f, sv = 0.f, sw = 0.f;
+            if (wv) {
 #pragma unroll
-            for (int q = 0; q < 8; q++) {
-                sk += S.gk[q][i];
-                sv += S.gv[q][i];
-                sw += S.gw[q];
+                for (int q = 0; q < 8; q++) {
+                    sk += S.gk[q][i];
+                    sv += S.gv[q][i];
+                    sw += S.gw[q];
+                }
+            } else {
+                // the sums from the MMAs against the all-ones operand; every
+                // valid slot weighs 1
+                float sr[32];
+                tmem_ld32(lane_base + kPColS + (uint32_t)(32 * b), sr);
+                sk = sr[0];
+                sv = sr[16];
+                sw = (float)(min(n, t1 * kPT) - t0 * kPT);
             }
             const float nn = n_run + sw;
             float acoef = 0.f, bcoef = 0.f, dk = 0.f;
