@@ -428,8 +428,7 @@ kvc_status kvc_decode_step(const kvc_params *p, int32_t t, int32_t new_pos, int3
     // gives the attention and the moments of all slots; after compaction a
     // second pass over the retained slots gives f_R, log Z_R and, by the
     // reverse of Chan's update, the evicted set's moments
-    if (!p->merge && p->rule != KVC_RULE_MI && max_len - p->L >= kFoldTcMin &&
-        2 * (max_len - p->L) > max_len) {
+    if (p->rule != KVC_RULE_MI && max_len - p->L >= kFoldTcMin && 2 * (max_len - p->L) > max_len) {
         cudaError_t e = launch_prompt_pass(*p, new_pos, max_len, q, k_new, v_new, *cache, true,
                                            refresh, nullptr, *mom, w, st);
         if (e != cudaErrorNotSupported) {
@@ -440,6 +439,13 @@ kvc_status kvc_decode_step(const kvc_params *p, int32_t t, int32_t new_pos, int3
             KVC_TRY(cuda_status(launch_aggregate(*p, t, pr, *cache, kmax, evict_idx, evict_pos,
                                                  n_evict, w, st),
                                 "kvc_decode_step aggregate"));
+            if (p->merge) {
+                // a unit with a single victim merges it (and then keeps the
+                // output over every slot); the others evict
+                KVC_TRY(cuda_status(launch_zip_merge(*p, new_pos, q, *cache, kmax, evict_idx, n_evict,
+                                                     nullptr, w, st),
+                                    "kvc_decode_step zip merge"));
+            }
             KVC_TRY(cuda_status(launch_fold_tc(*cache, p->cap, p->U, kmax, evict_idx, n_evict, *mom,
                                                w.status, st, true),
                                 "kvc_decode_step moments"));
@@ -448,9 +454,14 @@ kvc_status kvc_decode_step(const kvc_params *p, int32_t t, int32_t new_pos, int3
             KVC_TRY(cuda_status(launch_prompt_pass(*p, new_pos, p->L, q, nullptr, nullptr, *cache,
                                                    false, false, n_evict, *mom, w, st),
                                 "kvc_decode_step retained pass"));
-            KVC_TRY(cuda_status(launch_attend_final(*p, p->L, *cache, w.lse, w.fall, nullptr, w, st),
+            // the retained pass's lse and output go where the logits were
+            // (the probabilities are formed by now; this pass keeps none)
+            float *lse_r = w.xbuf;
+            float *f_r = w.xbuf + align_up((size_t)p->U * p->G * sizeof(float)) / sizeof(float);
+            KVC_TRY(cuda_status(launch_attend_final(*p, p->L, *cache, lse_r, f_r, nullptr, w, st),
                                 "kvc_decode_step retained merge"));
-            return cuda_status(launch_correct_retained(*p, q, *cache, w.lse, w.fall, *mom, o, w, st),
+            return cuda_status(launch_correct_retained(*p, q, *cache, lse_r, f_r, *mom, o, w, st,
+                                                       w.lse, w.fall, n_evict),
                                "kvc_decode_step correct");
         }
     }

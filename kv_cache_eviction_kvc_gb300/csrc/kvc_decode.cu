@@ -1092,6 +1092,10 @@ struct CorrArgs {
     int32_t *status;
     int cap, kmax, correction;
     int retained;      // lse / f_all are already log Z_R / f_R (no victims to remove)
+    // retained form: units left with n_evict = 0 (nothing went, or a merge
+    // that keeps the full-cache output) take these (the pass over all slots)
+    const float *lse_all, *f_all_all;
+    const int32_t *n_evict_sel;
 };
 
 constexpr int kIdentityMax = 16;
@@ -1125,9 +1129,12 @@ __global__ void __launch_bounds__(256) correct_kernel(CorrArgs a)
 
     const int32_t *ev = a.evict_idx + (size_t)u * a.kmax;
     if (k <= 0) {
+        const bool whole = a.retained && a.n_evict_sel && a.n_evict_sel[u] == 0;
+        const float *fa = whole ? a.f_all_all : a.f_all;
+        const float *la = whole ? a.lse_all : a.lse;
         for (int e = tid; e < G * kD; e += blockDim.x)
-            fR[e / kD][e % kD] = a.f_all[(size_t)u * G * kD + e];
-        if (tid < G) lz[tid] = a.lse[(size_t)u * G + tid];
+            fR[e / kD][e % kD] = fa[(size_t)u * G * kD + e];
+        if (tid < G) lz[tid] = la[(size_t)u * G + tid];
     } else if (k <= kIdentityMax) {
         // A_e^h = exp(q_h . k_e / sqrt(d) + ln p_e - lse_h)
         for (int e = w; e < k; e += 8) {
@@ -1385,7 +1392,8 @@ cudaError_t launch_correct(const kvc_params &p, const uint16_t *q,
                            float *logZ_R, const DecodeWs &ws, cudaStream_t st)
 {
     CorrArgs a{q, c.K, c.V, c.votes, c.len, evict_idx, n_evict, lse, f_all,
-               m.n, m.mu_k, m.mu_v, m.C, o, f_R, logZ_R, ws.status, p.cap, kmax, p.correction, 0};
+               m.n, m.mu_k, m.mu_v, m.C, o, f_R, logZ_R, ws.status, p.cap, kmax, p.correction, 0,
+               nullptr, nullptr, nullptr};
     switch (p.G) {
     case 1: return launch_correct_g<1>(a, p.U, p.cap, st);
     case 2: return launch_correct_g<2>(a, p.U, p.cap, st);
@@ -1397,10 +1405,12 @@ cudaError_t launch_correct(const kvc_params &p, const uint16_t *q,
 
 cudaError_t launch_correct_retained(const kvc_params &p, const uint16_t *q, const kvc_cache &c,
                                     const float *lse_R, const float *f_R, const kvc_moments &m,
-                                    float *o, const DecodeWs &ws, cudaStream_t st)
+                                    float *o, const DecodeWs &ws, cudaStream_t st,
+                                    const float *lse_all, const float *f_all, const int32_t *n_evict)
 {
     CorrArgs a{q, c.K, c.V, c.votes, c.len, nullptr, nullptr, lse_R, f_R,
-               m.n, m.mu_k, m.mu_v, m.C, o, nullptr, nullptr, ws.status, p.cap, 1, p.correction, 1};
+               m.n, m.mu_k, m.mu_v, m.C, o, nullptr, nullptr, ws.status, p.cap, 1, p.correction, 1,
+               lse_all, f_all, n_evict};
     switch (p.G) {
     case 1: return launch_correct_g<1>(a, p.U, p.cap, st);
     case 2: return launch_correct_g<2>(a, p.U, p.cap, st);

@@ -41,9 +41,13 @@ cudaError_t launch_attend_retained(const kvc_params &p, int max_len, const uint1
 
 // MomentKV's normalization-corrected output from f_R, log Z_R (as given) and
 // the moments: o = w_R f_R + (1 - w_R) (mu_v + C q / sqrt(d)) per head.
+// With lse_all, f_all and n_evict given, units with n_evict = 0 take those
+// instead (the output over every slot: nothing went, or merge mode merged).
 cudaError_t launch_correct_retained(const kvc_params &p, const uint16_t *q, const kvc_cache &c,
                                     const float *lse_R, const float *f_R, const kvc_moments &m,
-                                    float *o, const DecodeWs &ws, cudaStream_t st);
+                                    float *o, const DecodeWs &ws, cudaStream_t st,
+                                    const float *lse_all = nullptr, const float *f_all = nullptr,
+                                    const int32_t *n_evict = nullptr);
 
 // The split-attention merge alone (lse, f and, with probs, the head-mean
 // probabilities from the kept logits) over the partials in the workspace.

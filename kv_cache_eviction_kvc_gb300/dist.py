@@ -75,3 +75,33 @@ def gather_topk(scores: torch.Tensor, flat: torch.Tensor, B_total: int, group=No
     dist.all_gather(ss, s, group=group)
     dist.all_gather(fs, f, group=group)
     return merge_topk(torch.cat(ss), torch.cat(fs), B_total)
+
+
+def prefill_score_sharded(NL_local: int, Hq: int, Hkv: int, d: int, N: int, w: int, B_total: int,
+                          q_win, K, V, R, l0: int, normalize: int = 1, group=None, stream=None):
+    """The layer-sharded LaProx scorer: this rank's layers [l0, l0 + NL_local)
+    (q_win [NL_local][Hq][w][d], K, V [NL_local][Hkv][N][d], R [NL_local]
+    [Hkv][d][d], on this rank's GPU) are scored by kvc_prefill_score with the
+    rank's own per-layer normalization and its local top-min(B_total, shard)
+    selection; one exchange (gather_topk: on the device over NCCL, through the
+    host over gloo) gives the global top-B_total.  Returns (keep
+    [NL_local][Hkv][N] uint8 under the global selection, the global flat
+    indices ascending, their scores)."""
+    from . import kvc as K_
+    dev = K.device
+    n_local = NL_local * Hkv * N
+    b_local = min(int(B_total), n_local)
+    scores = torch.empty(NL_local, Hkv, N, dtype=torch.float32, device=dev)
+    keep = torch.empty(NL_local, Hkv, N, dtype=torch.uint8, device=dev)
+    idx = torch.empty(b_local, dtype=torch.int64, device=dev)
+    ws = torch.empty(K_.kvc_prefill_workspace_size(NL_local, Hkv, N, b_local), dtype=torch.uint8,
+                     device=dev)
+    K_.kvc_prefill_score(NL_local, Hq, Hkv, d, N, w, b_local, normalize, q_win, K, V, R, scores,
+                         keep, None, idx, ws, stream)
+    off = l0 * Hkv * N
+    xdev = dev if dist.get_backend(group) == "nccl" else torch.device("cpu")
+    gflat, gs = gather_topk(scores.view(-1)[idx].to(xdev), (idx + off).to(xdev), int(B_total), group)
+    mine = gflat[(gflat >= off) & (gflat < off + n_local)] - off
+    keep_g = torch.zeros(n_local, dtype=torch.uint8, device=dev)
+    keep_g[mine.to(dev)] = 1
+    return keep_g.view(NL_local, Hkv, N), gflat, gs

@@ -84,3 +84,50 @@ def test_window_attention_ema_init(cfg, alpha):
 def test_snapkv_protocol(cfg, pool, sink):
     from parity import run_snapkv_parity
     check(run_snapkv_parity(cfg, pool=pool, sink=sink))
+
+
+def _sharded_worker(rank, world, port, NL, N, B):
+    import os
+    import torch.distributed as dist
+    from kv_cache_eviction_kvc_gb300 import dist as D
+    from kv_cache_eviction_kvc_gb300 import kvc as K
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        pc = W.C3.with_(NL=NL, N=N, B_total=B)
+        inp = W.gen_prefill_scorer(pc, dev, 3)
+        R = torch.empty(NL, pc.Hkv, pc.d, pc.d, dtype=torch.float32, device=dev)
+        K.kvc_prefill_prepare(NL, pc.Hq, pc.Hkv, pc.d, pc.D, inp["W_O"], R)
+        l0, l1 = D.layer_shard(NL, world, rank)
+        keep_g, gflat, gs = D.prefill_score_sharded(
+            l1 - l0, pc.Hq, pc.Hkv, pc.d, N, pc.w, B, inp["q_win"][l0:l1], inp["K"][l0:l1],
+            inp["V"][l0:l1], R[l0:l1], l0)
+        # the single-process selection over every layer
+        scores = torch.empty(NL, pc.Hkv, N, dtype=torch.float32, device=dev)
+        keep = torch.empty(NL, pc.Hkv, N, dtype=torch.uint8, device=dev)
+        idx = torch.empty(B, dtype=torch.int64, device=dev)
+        ws = torch.empty(K.kvc_prefill_workspace_size(NL, pc.Hkv, N, B), dtype=torch.uint8, device=dev)
+        K.kvc_prefill_score(NL, pc.Hq, pc.Hkv, pc.d, N, pc.w, B, 1, inp["q_win"], inp["K"], inp["V"], R,
+                            scores, keep, None, idx, ws)
+        torch.cuda.synchronize()
+        assert gflat.tolist() == idx.cpu().tolist()
+        assert torch.equal(keep_g.cpu(), keep[l0:l1].cpu())
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("NL,N,B", [(4, 1024, 512), (3, 640, 900)])
+def test_layer_sharded_prefill_matches_single_process(NL, N, B):
+    """Two ranks score a layer shard each on the GPU (the exchange over gloo;
+    the ranks' kernels never wait on one another): the global selection and
+    each rank's kept tokens equal the single-process kvc_prefill_score."""
+    import socket
+    import torch.multiprocessing as mp
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    mp.spawn(_sharded_worker, args=(2, port, NL, N, B), nprocs=2, join=True)
