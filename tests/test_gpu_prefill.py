@@ -127,6 +127,10 @@ def test_layer_sharded_prefill_matches_single_process(NL, N, B):
     each rank's kept tokens equal the single-process kvc_prefill_score."""
     import socket
     import torch.multiprocessing as mp
+    # the ranks are processes of their own on this GPU: release the memory
+    # this process's allocator still caches from earlier tests
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
     with socket.socket() as s:
         s.bind(("127.0.0.1", 0))
         port = s.getsockname()[1]
