@@ -293,13 +293,20 @@ prompt_pass_kernel(PromptArgs a, const __grid_constant__ CUtensorMap tmK,
             for (int e = 0; e < 8; e++) sk8[e] = sv8[e] = 0.f;
             for (int t = t0; t < t1 && wv; t++) {
                 const int s = t % NS;
+                // this thread's eight rows' votes, requested before the wait
+                int vv[kPT / 8];
+#pragma unroll
+                for (int j = 0; j < kPT / 8; j++) {
+                    const int slot = t * kPT + rg + 8 * j;
+                    vv[j] = (slot < n && !(a.append && slot == n_old)) ? __ldg(a.votes + ubase + slot) : 1;
+                }
                 const bool ok = mbar_wait(&S.full[s], (uint32_t)(t / NS) & 1u);
                 if (!__all_sync(kFull, ok)) {
                     good = false;
                     break;
                 }
                 unsigned char *st = ring + (size_t)s * stage_bytes;
-#pragma unroll 2
+#pragma unroll
                 for (int j = 0; j < kPT / 8; j++) {
                     const int r = rg + 8 * j, slot = t * kPT + r;
                     const uint32_t o = p_off(r, c16);
@@ -313,7 +320,7 @@ prompt_pass_kernel(PromptArgs a, const __grid_constant__ CUtensorMap tmK,
                         } else {
                             kc = *reinterpret_cast<const uint4 *>(st + o);
                             vc = *reinterpret_cast<const uint4 *>(st + kPTile + o);
-                            wt = wv ? (float)__ldg(a.votes + ubase + slot) : 1.f;
+                            wt = (float)vv[j];
                         }
                     }
                     float kf[8], vf[8];
@@ -518,11 +525,22 @@ prompt_pass_kernel(PromptArgs a, const __grid_constant__ CUtensorMap tmK,
 #pragma unroll
         for (int m = 0; m < 8; m++) O[m][0] = O[m][1] = O[m][2] = O[m][3] = 0.f;
         bool good = true;
+        // votes of this lane's two slots (gq, gq + 8) of the set's next tile,
+        // loaded one tile ahead so that the loads are in flight meanwhile
+        auto load_votes = [&](int t, int &v0, int &v1) {
+            const int i = t * kPT + rb + gq;
+            v0 = (a.votes && i < n) ? a.votes[ubase + i] : 1;
+            v1 = (a.votes && i + 8 < n) ? a.votes[ubase + i + 8] : 1;
+        };
+        int vn0 = 1, vn1 = 1;
+        if (a.votes && cset < nt) load_votes(cset, vn0, vn1);
         const int nch = (nt + kPChunkTiles - 1) / kPChunkTiles;
         for (int cidx = 0; cidx < nch; cidx++) {
           const int tc1 = min(nt, (cidx + 1) * kPChunkTiles);
           for (int t = cidx * kPChunkTiles + cset; t < tc1; t += 2) {
             const int s = t % NS;
+            const int vc[2] = {vn0, vn1};
+            if (a.votes && t + 2 < nt) load_votes(t + 2, vn0, vn1);
             const uint32_t so = (uint32_t)(s * stage_bytes);
             const bool ok = good && mbar_wait(&S.full[s], (uint32_t)(t / NS) & 1u);
             good = __all_sync(kFull, ok);
@@ -578,7 +596,7 @@ prompt_pass_kernel(PromptArgs a, const __grid_constant__ CUtensorMap tmK,
                     float x0 = -INFINITY, x1 = -INFINITY;
                     if (i < n) {
                         const bool isnew = a.append && i == n_old;
-                        const float lnp = (!isnew && a.votes) ? logf((float)a.votes[ubase + i]) : 0.f;
+                        const float lnp = (!isnew && a.votes) ? logf((float)vc[hf]) : 0.f;
                         x0 = sacc[2 * hf] * rs + lnp;
                         x1 = sacc[2 * hf + 1] * rs + lnp;
                     }
