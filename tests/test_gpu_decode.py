@@ -58,8 +58,9 @@ SMALL = W.C0.with_(name="small", N=700, L=50, steps=24)
     SMALL.with_(N=40, L=64, steps=30),                               # no eviction at first
     SMALL.with_(T=0),                                                # Score-Free
     SMALL.with_(N=100, L=100, T=0, steps=80),                        # queue of 70, then argmin
+    SMALL.with_(Hq=8, Hkv=4, N=400, L=30),                           # G = 2 (first-step pass)
 ], ids=["ragged", "votes-cumulative", "single-lazy", "T=L-zero-order", "corr-off",
-        "G1", "k2", "G8-votes", "under-budget", "score-free", "score-free-queue"])
+        "G1", "k2", "G8-votes", "under-budget", "score-free", "score-free-queue", "G2"])
 @pytest.mark.parametrize("fused", [True, False])
 def test_edge_cases(cfg, fused):
     check(run_decode_parity(cfg, fused=fused))
@@ -83,7 +84,9 @@ def test_device_status_reports_overlong_unit():
     SMALL.with_(Hq=2, Hkv=2, N=300, L=20, votes_max=4, merge_recent=0),   # G = 1, votes
     SMALL.with_(Hq=16, Hkv=2, B=2, N=513, L=17, merge_recent=3, T=4),     # G = 8, lazy
     SMALL.with_(N=40, L=32, steps=12, merge_recent=64),              # no candidate: evict
-], ids=["zip", "zip-G1-votes", "zip-G8-lazy", "zip-no-candidate"])
+    SMALL.with_(merge_recent=8, T=4),                                # lazy: queue, search in pass 1
+    SMALL.with_(Hq=4, Hkv=2, N=400, L=40, merge_recent=8, T=4),      # the same with G = 2
+], ids=["zip", "zip-G1-votes", "zip-G8-lazy", "zip-no-candidate", "zip-G4-lazy", "zip-G2-lazy"])
 @pytest.mark.parametrize("fused", [True, False])
 def test_zip_merge(cfg, fused):
     rep = run_decode_parity(cfg, fused=fused)
