@@ -118,12 +118,112 @@ struct AttnSmem {
     uint64_t qfree[kAQ];         // every MMA reading the Q buffer completed
     uint64_t ready[2];           // the cluster's partial statistics of an item are published
     uint64_t fin;                // every MMA of the CTA completed
-    __align__(16) float2 rs[kRows];   // per row: cluster max (base 2) and 1 / sum; read as float4
+    __align__(16) float rm[kRows];    // per row: minus the cluster max (base 2); read as float4
+    __align__(16) float rz[kRows];    // per row: 1 / cluster sum; read as float4
     float roww[32];              // colsum weights per window row
     uint32_t tmem;
     int bad;
 };
-static_assert(offsetof(AttnSmem, rs) % 16 == 0, "rs is read as float4");
+static_assert(offsetof(AttnSmem, rm) % 16 == 0 && offsetof(AttnSmem, rz) % 16 == 0,
+              "rm and rz are read as float4");
+
+// Two fp32 lanes per instruction (Blackwell's packed f32x2 arithmetic): each
+// lane is rounded exactly as the scalar fma / mul / add would round it.
+__device__ __forceinline__ uint64_t f2pk(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 f2up(uint64_t v)
+{
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// max of three (one instruction on sm_100 and later)
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t ex2_2(uint64_t t)
+{
+    const float2 v = f2up(t);
+    return f2pk(ex2_approx(v.x), ex2_approx(v.y));
+}
+
+// Statistics of one window row over a 128-key tile (x: logits, masked keys
+// at -inf): the running base-2 max m and sum of 2^(x cs - m).
+__device__ __forceinline__ void row_stats(const float (&x)[128], float cs, float &m, float &sum)
+{
+    float mx[4];
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+        float a = fmax3(x[32 * k], x[32 * k + 1], x[32 * k + 2]);
+#pragma unroll
+        for (int i = 3; i < 31; i += 2) a = fmax3(a, x[32 * k + i], x[32 * k + i + 1]);
+        mx[k] = fmaxf(a, x[32 * k + 31]);
+    }
+    const float tm = fmax3(fmax3(mx[0], mx[1], mx[2]), mx[3], mx[3]);
+    if (tm == -INFINITY) return;
+    const float mn = fmaxf(m, tm * cs);
+    const uint64_t cs2 = f2pk(cs, cs), nm2 = f2pk(-mn, -mn);
+    uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+    for (int i = 0; i < 64; i++)
+        acc[i & 3] = add2(acc[i & 3], ex2_2(fma2(f2pk(x[2 * i], x[2 * i + 1]), cs2, nm2)));
+    const float2 a = f2up(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])));
+    sum = sum * ex2_approx(m - mn) + (a.x + a.y);
+    m = mn;
+}
+
+// Column sums of one key over the 128 window rows (x[4 j + h]: window query
+// j, head h): sum_j sh_j^2 and sum_j roww_j sh_j with sh_j the group sum of
+// the probabilities 2^(x cs - M) / Z.  MASK: rows j < jmin do not see the key.
+template <bool MASK, bool COLSUM>
+__device__ __forceinline__ void key_norms(const float (&x)[128], float cs, const float *rm,
+                                          const float *rz, const float *roww, int jmin,
+                                          float &c2s, float &cws)
+{
+    const float4 *rm4 = reinterpret_cast<const float4 *>(rm);
+    const float4 *rz4 = reinterpret_cast<const float4 *>(rz);
+    const uint64_t cs2 = f2pk(cs, cs);
+    float c2[4] = {0.f, 0.f, 0.f, 0.f};
+    float cw[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 32; j++) {
+        const float4 A = rm4[j], Z = rz4[j];
+        const uint64_t e01 = ex2_2(fma2(f2pk(x[4 * j], x[4 * j + 1]), cs2, f2pk(A.x, A.y)));
+        const uint64_t e23 = ex2_2(fma2(f2pk(x[4 * j + 2], x[4 * j + 3]), cs2, f2pk(A.z, A.w)));
+        const float2 pr = f2up(fma2(e23, f2pk(Z.z, Z.w), mul2(e01, f2pk(Z.x, Z.y))));
+        float sh = pr.x + pr.y;
+        if (MASK) sh = (j >= jmin) ? sh : 0.f;
+        c2[j & 3] = fmaf(sh, sh, c2[j & 3]);
+        if (COLSUM) cw[j & 3] = fmaf(roww[j], sh, cw[j & 3]);
+    }
+    c2s = (c2[0] + c2[1]) + (c2[2] + c2[3]);
+    cws = (cw[0] + cw[1]) + (cw[2] + cw[3]);
+}
 
 __global__ void __launch_bounds__(kAThreads, 1)
 prefill_attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap tmK)
@@ -282,7 +382,6 @@ prefill_attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap tmK)
         const int ln = 32 * qd + lane;             // row (stat) or tile key (norm)
         const uint32_t lane_base = tmem + ((uint32_t)(32 * qd) << 16);
         const float cs = a.cs;
-        const float4 *rs4 = reinterpret_cast<const float4 *>(S.rs);
         const int jr = ln >> 2;
         const int lim = N - W + jr;                // last key window row jr sees
         bool good = true;
@@ -310,38 +409,20 @@ prefill_attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap tmK)
                     const uint32_t tb = lane_base + (uint32_t)((gi % kAcc) * 128);
                     const int kbase = k0 + t * kTk;
                     const bool interior = kbase + kTk <= k1 && kbase + kTk - 1 <= N - W;
-#pragma unroll 1
-                    for (int hh = 0; hh < 2; hh++) {      // 64 keys at a time
-                        float x[64];
-                        tmem_ld64(tb + 64 * hh, x);
-                        if (!interior) {
+                    float x[128];
+                    tmem_ld128(tb, x);
+                    release(gi);                  // the accumulator is drained into registers
+                    if (!interior) {
 #pragma unroll
-                            for (int i = 0; i < 64; i++) {
-                                const int key = kbase + 64 * hh + i;
-                                if (key >= k1 || key > lim) x[i] = -INFINITY;
-                            }
-                        }
-                        float mx[8];
-#pragma unroll
-                        for (int k = 0; k < 8; k++) mx[k] = x[k];
-#pragma unroll
-                        for (int i = 8; i < 64; i++) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
-                        const float tm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-                        if (tm != -INFINITY) {
-                            const float mn = fmaxf(m, tm * cs);
-                            float e[8];
-#pragma unroll
-                            for (int k = 0; k < 8; k++) e[k] = 0.f;
-#pragma unroll
-                            for (int i = 0; i < 64; i++) e[i & 7] += ex2_approx(fmaf(x[i], cs, -mn));
-                            sum = sum * ex2_approx(m - mn) +
-                                  (((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7])));
-                            m = mn;
+                        for (int i = 0; i < 128; i++) {
+                            const int key = kbase + i;
+                            if (key >= k1 || key > lim) x[i] = -INFINITY;
                         }
                     }
+                    row_stats(x, cs, m, sum);
+                } else {
+                    release(gi);
                 }
-                release(gi);
             };
             // ---------------- merged statistics of item p - 1 (needed by its norm jobs)
             auto mid = [&] {
@@ -361,7 +442,8 @@ prefill_attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap tmK)
                         if (v[c].x != -INFINITY) Z += v[c].y * ex2_approx(v[c].x - M);
                     // rows past the window (zero queries) and empty rows contribute 0
                     const bool live = jr < W && M != -INFINITY && Z > 0.f;
-                    S.rs[ln] = live ? make_float2(M, 1.f / Z) : make_float2(0.f, 0.f);
+                    S.rm[ln] = live ? -M : 0.f;
+                    S.rz[ln] = live ? 1.f / Z : 0.f;
                 }
                 asm volatile("bar.sync 1, %0;" ::"n"(kAEpiWarps * 32) : "memory");
             };
@@ -376,36 +458,29 @@ prefill_attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap tmK)
                 if (acquire(gi)) {
                     const uint32_t tb = lane_base + (uint32_t)((gi % kAcc) * 128);
                     const int jmin = k0 + kl - (N - W);     // window rows j < jmin do not see the key
-                    float c2[4] = {0.f, 0.f, 0.f, 0.f};
-                    float cw[4] = {0.f, 0.f, 0.f, 0.f};    // weighted column sum (times G)
-#pragma unroll 1
-                    for (int hh = 0; hh < 2; hh++) {      // window rows 64 hh .. 64 hh + 63
-                        float x[64];
-                        tmem_ld64(tb + 64 * hh, x);
-#pragma unroll
-                        for (int jj = 0; jj < 16; jj++) {
-                            const int j = 16 * hh + jj;
-                            const float4 A = rs4[2 * j], B = rs4[2 * j + 1];
-                            float sh = ex2_approx(fmaf(x[4 * jj], cs, -A.x)) * A.y;
-                            sh = fmaf(ex2_approx(fmaf(x[4 * jj + 1], cs, -A.z)), A.w, sh);
-                            sh = fmaf(ex2_approx(fmaf(x[4 * jj + 2], cs, -B.x)), B.y, sh);
-                            sh = fmaf(ex2_approx(fmaf(x[4 * jj + 3], cs, -B.z)), B.w, sh);
-                            sh = (j >= jmin) ? sh : 0.f;
-                            c2[jj & 3] = fmaf(sh, sh, c2[jj & 3]);
-                            cw[jj & 3] = fmaf(S.roww[j], sh, cw[jj & 3]);
-                        }
+                    float x[128];
+                    tmem_ld128(tb, x);
+                    release(gi);                  // the accumulator is drained into registers
+                    float c2 = 0.f, cw = 0.f;     // cw: weighted column sum (times G)
+                    const bool mask = __any_sync(kFull, jmin > 0);
+                    if (a.colsum) {
+                        if (mask) key_norms<true, true>(x, cs, S.rm, S.rz, S.roww, jmin, c2, cw);
+                        else key_norms<false, true>(x, cs, S.rm, S.rz, S.roww, jmin, c2, cw);
+                    } else {
+                        if (mask) key_norms<true, false>(x, cs, S.rm, S.rz, S.roww, jmin, c2, cw);
+                        else key_norms<false, false>(x, cs, S.rm, S.rz, S.roww, jmin, c2, cw);
                     }
                     if (k0 + kl < k1) {
                         if (a.want_p) {
-                            const float pv = sqrtf(((c2[0] + c2[1]) + (c2[2] + c2[3])) *
-                                                   (1.f / (kPG * kPG))) * sqrtf(r2);
+                            const float pv = sqrtf(c2 * (1.f / (kPG * kPG))) * sqrtf(r2);
                             a.p[o] = pv;
                             lsum += (double)pv;
                         }
-                        if (a.colsum) a.colsum[o] = ((cw[0] + cw[1]) + (cw[2] + cw[3])) * (1.f / kPG);
+                        if (a.colsum) a.colsum[o] = cw * (1.f / kPG);
                     }
+                } else {
+                    release(gi);
                 }
-                release(gi);
             };
             for_block(p, stat, norm, mid);
             if (p >= 1) {
