@@ -213,7 +213,7 @@ def run_prefill(pc, dev, reps=5):
             "roofline": {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
                          "frac": ach / peak, "peak_kind": kind, "bytes_per_call": by,
                          "algorithmic_tflops": fl / (ms * 1e-3) / 1e12,
-                         "kernels": "pack + prefill_val + prefill_attn + radix select"},
+                         "kernels": "pack + prefill_attn beside prefill_val + combine + radix select"},
             "kept": int(counts.sum().item()),
             "allocations_ms_per_call": alloc_ms,
             "snapkv_ms_per_call": snap_ms,

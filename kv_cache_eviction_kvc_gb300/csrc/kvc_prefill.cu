@@ -36,6 +36,7 @@
 
 #include <algorithm>
 #include <cstddef>
+#include <mutex>
 
 #include "kvc_common.cuh"
 #include "kvc_internal.h"
@@ -94,17 +95,17 @@ struct Ring {
 // software-pipelined: block p runs stat(p) and then norm(p - 1), so the
 // cluster-wide merge of item p - 1's statistics is hidden behind a whole
 // statistics pass.  Q of item p lives in buffer p % 3.
-// Output: p_i = c_i r_i with c_i = ||A_bar[:, i]||_2 and r_i^2 from the
-// value-norm kernel, and the per-layer sums of p.
+// Output: the column norms c_i = ||A_bar[:, i]||_2 (combine_kernel then
+// forms p_i = c_i r_i with r_i from the value-norm kernel, which runs beside
+// this one), and/or the weighted column sums.
 struct AttnArgs {
     const unsigned char *pack;   // [NL][Hkv][kPackBytes] from pack_kernel
-    const float *r2;             // [NL][Hkv][N]: squared value norms (value-norm kernel)
-    float *p;                    // [NL][Hkv][N]: p = c r (want_p)
+    float *c;                    // [NL][Hkv][N]: column norms c (want_c)
     float2 *stats;               // [NL][Hkv][kCS][kASets][kRows] partial (max, sum) per row
-    double *layer_sum;           // [NL]: per-layer sums of p; NaN on a timed-out wait
+    double *layer_sum;           // [NL]: NaN on a timed-out wait
     float *colsum;               // [NL][Hkv][N]: sum_j roww_j A_bar[j, i], or NULL
     int Hkv, N, w, per_cta, nitem;
-    int want_p;                  // LaProx's p = c r and its layer sums
+    int want_c;                  // LaProx's attention column norms
     float cs;                    // log2(e) / sqrt(d): logits in base-2 units
     float roww[32];              // window row weights of colsum
 };
@@ -447,14 +448,11 @@ prefill_attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap tmK)
                 }
                 asm volatile("bar.sync 1, %0;" ::"n"(kAEpiWarps * 32) : "memory");
             };
-            // ---------------- column-norm job: tile t of item p - 1, p = c r out
-            double lsum = 0.0;
+            // ---------------- column-norm job: tile t of item p - 1
             auto norm = [&](int gi, int t) {
                 if (t % kASets != set) return;
                 const int kl = t * kTk + ln;
                 const size_t o = (size_t)lgn * N + k0 + kl;
-                // r^2 of the key (from the value-norm kernel), in flight during the wait
-                const float r2 = (a.want_p && k0 + kl < k1) ? a.r2[o] : 0.f;
                 if (acquire(gi)) {
                     const uint32_t tb = lane_base + (uint32_t)((gi % kAcc) * 128);
                     const int jmin = k0 + kl - (N - W);     // window rows j < jmin do not see the key
@@ -471,11 +469,7 @@ prefill_attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap tmK)
                         else key_norms<false, false>(x, cs, S.rm, S.rz, S.roww, jmin, c2, cw);
                     }
                     if (k0 + kl < k1) {
-                        if (a.want_p) {
-                            const float pv = sqrtf(c2 * (1.f / (kPG * kPG))) * sqrtf(r2);
-                            a.p[o] = pv;
-                            lsum += (double)pv;
-                        }
+                        if (a.want_c) a.c[o] = sqrtf(c2 * (1.f / (kPG * kPG)));
                         if (a.colsum) a.colsum[o] = cw * (1.f / kPG);
                     }
                 } else {
@@ -483,12 +477,6 @@ prefill_attn_kernel(AttnArgs a, const __grid_constant__ CUtensorMap tmK)
                 }
             };
             for_block(p, stat, norm, mid);
-            if (p >= 1) {
-                // the layer's partial sum of p
-#pragma unroll
-                for (int msk = 16; msk > 0; msk >>= 1) lsum += __shfl_xor_sync(kFull, lsum, msk);
-                if (lane == 0 && lsum != 0.0) atomicAdd(&a.layer_sum[lgn / a.Hkv], lsum);
-            }
             if (p < nmine) {
                 // publish this set's partial statistics of row ln; one thread
                 // then tells every CTA of the cluster (release at cluster scope)
@@ -970,6 +958,54 @@ constexpr int kH1 = 4096, kH2 = 4096, kH3 = 256;
 // order key: ascending key = descending score
 __device__ __forceinline__ uint32_t desc_key(float s) { return ~float_key(s); }
 
+// LaProx's indicator p_i = c_i r_i, written over the column norms c, and the
+// per-layer sums of p (fp32 within a thread, fp64 across threads).  Grid
+// (blocks per layer, NL); block b of layer l strides over the layer's Hkv N
+// scores.
+constexpr int kCbBlock = 256;
+constexpr unsigned kPauseNs = 10000;   // head start of the attention kernel over the value norms
+__global__ void __launch_bounds__(kCbBlock) combine_kernel(float *p, const float *r2,
+                                                           double *layer_sum, int per_layer)
+{
+    const int l = blockIdx.y, lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
+    float *pl = p + (size_t)l * per_layer;
+    const float *rl = r2 + (size_t)l * per_layer;
+    float part = 0.f;
+#pragma unroll 4
+    for (int i = blockIdx.x * kCbBlock + threadIdx.x; i < per_layer; i += gridDim.x * kCbBlock) {
+        const float v = pl[i] * sqrtf(rl[i]);
+        pl[i] = v;
+        part += v;
+    }
+    double d = (double)part;
+#pragma unroll
+    for (int msk = 16; msk > 0; msk >>= 1) d += __shfl_xor_sync(kFull, d, msk);
+    __shared__ double wsum[kCbBlock / 32];
+    if (lane == 0) wsum[wp] = d;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double t = 0.0;
+        for (int k = 0; k < kCbBlock / 32; k++) t += wsum[k];
+        if (t != 0.0) atomicAdd(&layer_sum[l], t);
+    }
+}
+
+// A pause of about ns nanoseconds (one warp, no shared memory, at most ~1 ms
+// whatever the clock does), queued ahead of the value-norm launch so that the
+// attention kernel's clusters, made eligible at the same moment, are placed
+// first; the value-norm CTAs then start on the SMs the clusters leave free.
+__global__ void pause_kernel(unsigned ns)
+{
+    uint64_t t0;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    for (int i = 0; i < 4096; i++) {
+        uint64_t t;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        if (t - t0 >= ns) break;
+        __nanosleep(256);
+    }
+}
+
 // inv[l] = 1 / (sum of p over layer l), 0 for an all-zero layer
 __global__ void layer_inv_kernel(const double *layer_sum, float *inv, int NL)
 {
@@ -1392,10 +1428,51 @@ static kvc_status pf_cuda(cudaError_t e, const char *what)
     return KVC_ERR_CUDA;
 }
 
+// One library-owned stream per device (created on first use, lowest
+// priority, non-blocking) for work that runs beside the caller's stream; it
+// joins the caller's stream through events, so a stream capture follows it.
+static cudaError_t side_stream(int dev, cudaStream_t *out)
+{
+    constexpr int kMaxDev = 64;
+    static cudaStream_t streams[kMaxDev] = {};
+    static std::mutex mu;
+    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (streams[dev] == nullptr) {
+        int lo = 0, hi = 0;
+        cudaError_t e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
+        if (e != cudaSuccess) return e;
+        e = cudaStreamCreateWithPriority(&streams[dev], cudaStreamNonBlocking, lo);
+        if (e != cudaSuccess) {
+            streams[dev] = nullptr;
+            return e;
+        }
+    }
+    *out = streams[dev];
+    return cudaSuccess;
+}
+
+// Two events for a fork and a join, destroyed with the call (a recorded
+// event's resources are released once it completes).
+struct EventPair {
+    cudaEvent_t a = nullptr, b = nullptr;
+    cudaError_t create()
+    {
+        cudaError_t e = cudaEventCreateWithFlags(&a, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&b, cudaEventDisableTiming);
+        return e;
+    }
+    ~EventPair()
+    {
+        if (a) cudaEventDestroy(a);
+        if (b) cudaEventDestroy(b);
+    }
+};
+
 // The persistent attention kernel: as many 8-CTA clusters as the GPU holds
 // at once, each looping over (layer, KV head) items.
 static cudaError_t launch_attn(const AttnArgs &aa, const CUtensorMap &tmK, int nitem, int nsm,
-                               cudaStream_t st)
+                               cudaStream_t st, int priority = 0)
 {
     cudaError_t e = cudaFuncSetAttribute(prefill_attn_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kADyn);
@@ -1404,18 +1481,21 @@ static cudaError_t launch_attn(const AttnArgs &aa, const CUtensorMap &tmK, int n
     cfg.blockDim = dim3(kAThreads);
     cfg.dynamicSmemBytes = kADyn;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = kCS;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributePriority;
+    attr[1].val.priority = priority;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 1;            // the occupancy query sees the cluster shape only
     cfg.gridDim = dim3(kCS * std::min(nitem, std::max(1, nsm / kCS)));
     int nclu = 0;
     if (cudaOccupancyMaxActiveClusters(&nclu, prefill_attn_kernel, &cfg) != cudaSuccess || nclu < 1)
         nclu = std::max(1, nsm / (2 * kCS));
     (void)cudaGetLastError();
+    cfg.numAttrs = 2;
     cfg.gridDim = dim3(kCS * std::min(nitem, nclu));
     return cudaLaunchKernelEx(&cfg, prefill_attn_kernel, aa, tmK);
 }
@@ -1457,8 +1537,8 @@ static kvc_status window_colsum(const char *who, int32_t NL, int32_t Hq, int32_t
     pack_kernel<<<NL * Hkv, 256, 0, st>>>(q_win, nullptr, pw.pack, Hq, Hkv, w);
     if ((e = cudaGetLastError()) != cudaSuccess) return pf_cuda(e, who);
     const int per_cta = ((N + kCS - 1) / kCS + kTk - 1) / kTk * kTk;
-    AttnArgs aa{pw.pack, nullptr, nullptr, pw.stats, pw.layer_sum, S, Hkv, N, w, per_cta, NL * Hkv,
-                0, (float)(1.4426950408889634 / sqrt((double)kD)), {}};
+    AttnArgs aa{pw.pack, nullptr, pw.stats, pw.layer_sum, S, Hkv, N, w, per_cta, NL * Hkv, 0,
+                (float)(1.4426950408889634 / sqrt((double)kD)), {}};
     for (int j = 0; j < 32; j++) aa.roww[j] = j < w ? row_weight[j] : 0.f;
     return pf_cuda(launch_attn(aa, tmK, NL * Hkv, nsm, st), who);
 }
@@ -1546,27 +1626,48 @@ kvc_status kvc_prefill_score(int32_t NL, int32_t Hq, int32_t Hkv, int32_t d, int
     pack_kernel<<<NL * Hkv, 256, 0, st>>>(q_win, R, pw.pack, Hq, Hkv, w);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return pf_cuda(e, "kvc_prefill_score pack launch");
-    // value norms r^2, then the attention kernel's column norms c^2 into the
-    // score buffer, then p = c r with the per-layer sums
+    // The value norms r^2 (a library stream) and the attention column norms c
+    // (the caller's stream) run side by side: the attention kernel's
+    // clusters cannot fill every SM, and the value-norm CTAs take the SMs
+    // left over, then the rest once the clusters finish.  Then p = c r with
+    // the per-layer sums.
     const int ntl = (N + kTk - 1) / kTk;
     const long long total = (long long)NL * Hkv * ntl;
-    int dev = 0, nsm = 0;
+    int dev = 0, nsm = 0, prio_lo = 0, prio_hi = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
-        (e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        (e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetStreamPriorityRange(&prio_lo, &prio_hi)) != cudaSuccess)
         return pf_cuda(e, "kvc_prefill_score device query");
     e = cudaFuncSetAttribute(prefill_val_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kVDyn);
     if (e != cudaSuccess) return pf_cuda(e, "kvc_prefill_score attribute");
+    cudaStream_t aux = nullptr;
+    if ((e = side_stream(dev, &aux)) != cudaSuccess) return pf_cuda(e, "kvc_prefill_score stream");
+    EventPair ev;
+    if ((e = ev.create()) != cudaSuccess) return pf_cuda(e, "kvc_prefill_score event");
     const int nitem = NL * Hkv;
+    // the attention kernel is enqueued first and at the higher priority, so
+    // its clusters are placed before the value-norm CTAs take SMs
+    if ((e = cudaEventRecord(ev.a, st)) != cudaSuccess) return pf_cuda(e, "kvc_prefill_score record");
+    AttnArgs aa{pw.pack, pbuf, pw.stats, pw.layer_sum, nullptr, Hkv, N, w, per_cta, nitem, 1,
+                (float)(1.4426950408889634 / sqrt((double)kD)), {}};
+    e = launch_attn(aa, tmK, nitem, nsm, st, prio_hi);
+    if (e != cudaSuccess) return pf_cuda(e, "kvc_prefill_score attention launch");
+    if ((e = cudaStreamWaitEvent(aux, ev.a, 0)) != cudaSuccess)
+        return pf_cuda(e, "kvc_prefill_score stream wait");
+    pause_kernel<<<1, 32, 0, aux>>>(kPauseNs);
     ValArgs va{pw.pack, pw.r2, pw.layer_sum, pw.counter, pw.counter + 1, NL, N, ntl, nitem};
     prefill_val_kernel<<<(unsigned)std::min<long long>((total + kVChunk - 1) / kVChunk, nsm), kVThreads,
-                         kVDyn, st>>>(va, tmV);
+                         kVDyn, aux>>>(va, tmV);
     if ((e = cudaGetLastError()) != cudaSuccess) return pf_cuda(e, "kvc_prefill_score value launch");
-
-    AttnArgs aa{pw.pack, pw.r2, pbuf, pw.stats, pw.layer_sum, nullptr, Hkv, N, w, per_cta, nitem,
-                1, (float)(1.4426950408889634 / sqrt((double)kD)), {}};
-    e = launch_attn(aa, tmK, nitem, nsm, st);
-    if (e != cudaSuccess) return pf_cuda(e, "kvc_prefill_score attention launch");
+    if ((e = cudaEventRecord(ev.b, aux)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(st, ev.b, 0)) != cudaSuccess)
+        return pf_cuda(e, "kvc_prefill_score stream join");
+    const int per_layer_i = Hkv * N;
+    combine_kernel<<<dim3((unsigned)std::min(64, (per_layer_i + kCbBlock * 32 - 1) / (kCbBlock * 32)),
+                          (unsigned)NL),
+                     kCbBlock, 0, st>>>(pbuf, pw.r2, pw.layer_sum, per_layer_i);
+    if ((e = cudaGetLastError()) != cudaSuccess) return pf_cuda(e, "kvc_prefill_score combine launch");
     const int64_t per_layer = (int64_t)Hkv * N;
 
     // radix select of the B_total largest s (pass 1 also normalizes in place)
