@@ -135,3 +135,63 @@ def test_layer_sharded_prefill_matches_single_process(NL, N, B):
         s.bind(("127.0.0.1", 0))
         port = s.getsockname()[1]
     mp.spawn(_sharded_worker, args=(2, port, NL, N, B), nprocs=2, join=True)
+
+
+def _prefill_buffers(cfg, dev):
+    from kv_cache_eviction_kvc_gb300 import kvc as K
+    NL, Hq, Hkv, d, N, w, B = cfg.NL, cfg.Hq, cfg.Hkv, cfg.d, cfg.N, cfg.w, cfg.B_total
+    inp = W.gen_prefill_scorer(cfg, dev, 3)
+    R = torch.empty(NL, Hkv, d, d, dtype=torch.float32, device=dev)
+    K.kvc_prefill_prepare(NL, Hq, Hkv, d, cfg.D, inp["W_O"], R)
+    ws = torch.empty(K.kvc_prefill_workspace_size(NL, Hkv, N, B), dtype=torch.uint8, device=dev)
+
+    def outputs():
+        return (torch.full((NL, Hkv, N), -1.0, dtype=torch.float32, device=dev),
+                torch.full((NL, Hkv, N), 7, dtype=torch.uint8, device=dev),
+                torch.full((NL, Hkv), -1, dtype=torch.int32, device=dev),
+                torch.full((B,), -1, dtype=torch.int64, device=dev))
+
+    def call(out, stream=None):
+        K.kvc_prefill_score(NL, Hq, Hkv, d, N, w, B, 1, inp["q_win"], inp["K"], inp["V"], R,
+                            *out, ws, stream=stream)
+    return outputs, call
+
+
+def _same(a, b):
+    sa, ka, ca, ia = a
+    sb, kb, cb, ib = b
+    assert torch.equal(ka, kb) and torch.equal(ca, cb) and torch.equal(ia, ib)
+    # the per-layer sums are fp64 atomics: the normalization may differ in the
+    # last bit between runs
+    torch.testing.assert_close(sa, sb, rtol=1e-6, atol=0.0)
+
+
+def test_prefill_score_stream_order_and_graph_capture():
+    """The value norms run on a library stream forked from and joined back
+    into the caller's stream: results read after synchronizing only the
+    caller's (non-default) stream are complete, and a CUDA graph captured
+    from that stream replays the same selection."""
+    dev = torch.device("cuda", 0)
+    cfg = W.C3.with_(NL=4, N=4096, B_total=2048)
+    outputs, call = _prefill_buffers(cfg, dev)
+    ref = outputs()
+    call(ref)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    for _ in range(3):
+        out = outputs()
+        torch.cuda.current_stream().wait_stream(s)
+        s.wait_stream(torch.cuda.current_stream())
+        call(out, stream=s)
+        s.synchronize()
+        _same(ref, out)
+    got = outputs()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call(got, stream=torch.cuda.current_stream())
+    for _ in range(2):
+        for t in got:
+            t.fill_(0)
+        g.replay()
+        torch.cuda.synchronize()
+        _same(ref, got)
