@@ -15,14 +15,19 @@
 //                               window logits, merged over the cluster
 //                        norm   S^T = K Q^T (keys x rows): group-mean
 //                               attention column norms c_i = ||A_bar[:, i]||_2
-//                      p_i = c_i r_i and the per-layer sums of p (fp64);
+//                      the column norms c_i (combine_kernel then writes
+//                      p_i = c_i r_i and the per-layer sums of p, fp64);
 //                      optionally the weighted column sum
 //                      S_i = sum_j roww_j A_bar[j, i] (SnapKV's accumulated
 //                      window attention, KeepKV's windowed EMA init)
 //                      Both kernels: every contraction on tcgen05 (128 x 128
 //                      x 128 bf16, fp32 accumulators in tensor memory), a TMA
 //                      producer warp, one MMA-issuing thread, epilogue warps
-//                      reading the accumulators by lane quarter.
+//                      reading the accumulators by lane quarter.  They run
+//                      side by side: the attention clusters on the caller's
+//                      stream, the value norms on a library stream (behind a
+//                      short pause_kernel, so that the clusters are placed
+//                      first) taking the SMs the clusters leave free.
 //   select             s = p / layer sum; three-pass radix select of the
 //                      B_total largest (ties to the smaller flat index); keep
 //                      mask, per-(layer, KV head) counts, ascending kept
