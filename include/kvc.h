@@ -596,10 +596,11 @@ KVC_API size_t kvc_prefill_workspace_size(int32_t NL, int32_t Hkv, int32_t N,
  * kvc_prefill_workspace_size bytes, 256-byte aligned (KVC_ERR_WORKSPACE).
  * A kernel wait that ran out (a fault) leaves NaN scores.
  * Streams: the value norms run on a stream the library owns (one per
- * device, created on the first call, never destroyed), forked from and
- * joined back into `stream` through events, so every output is ordered on
- * `stream` as usual and a stream capture of `stream` takes both branches.
- * Calls on different caller streams share that stream and queue there.
+ * context and device, created on the first call in that context, never
+ * destroyed), forked from and joined back into `stream` through events, so
+ * every output is ordered on `stream` as usual and a stream capture of
+ * `stream` takes both branches.  Calls on different caller streams share
+ * that stream and queue there.
  */
 KVC_API kvc_status kvc_prefill_score(int32_t NL, int32_t Hq, int32_t Hkv, int32_t d,
                              int32_t N, int32_t w, int64_t B_total,

@@ -1433,27 +1433,69 @@ static kvc_status pf_cuda(cudaError_t e, const char *what)
     return KVC_ERR_CUDA;
 }
 
-// One library-owned stream per device (created on first use, lowest
-// priority, non-blocking) for work that runs beside the caller's stream; it
-// joins the caller's stream through events, so a stream capture follows it.
+// Identity of the calling thread's current context (cuCtxGetId, through the
+// runtime's driver entry points): unique for the process's lifetime, so a
+// context made after a device reset, or another context made current, gets
+// an id of its own.  0 when the entry points are unavailable.
+static unsigned long long current_context_id()
+{
+    static std::once_flag once;
+    static PFN_cuCtxGetCurrent_v4000 get_cur = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_cur = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_cur && get_id && get_cur(&ctx) == CUDA_SUCCESS && ctx != nullptr &&
+        get_id(ctx, &id) == CUDA_SUCCESS)
+        return id;
+    return 0;
+}
+
+// One library-owned stream per (context, device), created on first use at
+// the lowest priority, non-blocking and never destroyed, for work that runs
+// beside the caller's stream; it joins the caller's stream through events,
+// so a stream capture follows it.  Keyed on the context id, a stream made in
+// a context that has since been destroyed is never handed out again.
 static cudaError_t side_stream(int dev, cudaStream_t *out)
 {
-    constexpr int kMaxDev = 64;
-    static cudaStream_t streams[kMaxDev] = {};
+    struct Entry {
+        unsigned long long ctx;
+        int dev;
+        cudaStream_t s;
+    };
+    constexpr int kMax = 64;
+    static Entry tab[kMax] = {};
+    static int used = 0, next = 0;
     static std::mutex mu;
-    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lock(mu);
-    if (streams[dev] == nullptr) {
-        int lo = 0, hi = 0;
-        cudaError_t e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
-        if (e != cudaSuccess) return e;
-        e = cudaStreamCreateWithPriority(&streams[dev], cudaStreamNonBlocking, lo);
-        if (e != cudaSuccess) {
-            streams[dev] = nullptr;
-            return e;
+    for (int i = 0; i < used; i++)
+        if (tab[i].ctx == ctx && tab[i].dev == dev) {
+            *out = tab[i].s;
+            return cudaSuccess;
         }
-    }
-    *out = streams[dev];
+    int lo = 0, hi = 0;
+    cudaError_t e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
+    if (e != cudaSuccess) return e;
+    cudaStream_t s = nullptr;
+    e = cudaStreamCreateWithPriority(&s, cudaStreamNonBlocking, lo);
+    if (e != cudaSuccess) return e;
+    // a full table forgets its oldest entry (the stream stays valid)
+    const int slot = used < kMax ? used++ : (next++ % kMax);
+    tab[slot] = Entry{ctx, dev, s};
+    *out = s;
     return cudaSuccess;
 }
 
